@@ -1,0 +1,299 @@
+"""Seeded synthetic workloads for paged attention.
+
+This module only draws inputs: queries, K/V page pools, block tables, sequence
+lengths and query offsets.  It holds none of the attention arithmetic, so both
+the CUDA path and the CPU oracle can consume exactly the same bytes.
+
+Input structure follows the pages' workloads:
+
+* K/V live in a pool of fixed-size pages ``[num_pages, page_size, Hkv, D]``
+  whose physical order is a seeded random permutation ("shuffled page
+  ordering", rocMLIR PR #2222, Key Changes 2; rocm-libraries PR #14349,
+  Performance: "contiguous and random" page tables).
+* A per-sequence block table ``int32 [B, W]`` maps logical page ``j // ps`` of
+  sequence ``b`` to a physical page; slots past ``ceil(L_b / ps)`` hold a
+  sentinel that must never be read (-1, or 0x7FFFFFFF as in PR #14349,
+  Coverage: "the table's tail holds an unmapped page id").
+* Values are N(0, 1) draws rounded to bf16/f16 with round-to-nearest-even.
+
+Two generators are used for the page pools.  Small pools are drawn on the host
+with ``numpy.random.default_rng``.  The two 2-GiB pools (Llama-3-8B decode and
+the over-2^31 decode) are drawn on the device by ``torch.randn`` with a seeded
+``torch.Generator`` and cast to bf16 by torch (round-to-nearest-even); tests
+that check them copy the device bytes back to the host for the oracle.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+SENTINEL_MAX = 0x7FFFFFFF  # unmapped page id used for table tails
+SENTINEL_NEG = -1
+
+DTYPES = ("f32", "f16", "bf16")
+ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
+
+
+def bf16_bits_rne(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest, ties to even); return the uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = (u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def f16_bits_rne(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to IEEE binary16 (numpy's cast is round-to-nearest-even)."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def _normal_elems(rng: np.random.Generator, n: int, dtype: str) -> np.ndarray:
+    x = rng.standard_normal(n, dtype=np.float32)
+    if dtype == "f32":
+        return x
+    if dtype == "bf16":
+        return bf16_bits_rne(x)
+    return f16_bits_rne(x)
+
+
+@dataclasses.dataclass
+class Workload:
+    """One paged-attention problem instance (host arrays; K/V may live on the device)."""
+
+    name: str
+    dtype: str
+    B: int
+    Sq: int
+    Hq: int
+    Hkv: int
+    D: int
+    page_size: int
+    num_pages: int
+    causal: bool
+    scale: float
+    split_kv: tuple
+    seq_lens: np.ndarray            # int32 [B]
+    block_table: np.ndarray         # int32 [B, W]
+    q: np.ndarray                   # [B, Sq, Hq, D]; float32 for f32, uint16 bits otherwise
+    q_offset: Optional[np.ndarray] = None   # int32 [B] or None
+    k_cache: Optional[np.ndarray] = None    # [P, ps, Hkv, D] (host) or None if device-drawn
+    v_cache: Optional[np.ndarray] = None
+    device_cache_seed: Optional[int] = None  # set when the pools are drawn on the device
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def W(self) -> int:
+        return int(self.block_table.shape[1])
+
+    @property
+    def esize(self) -> int:
+        return ESIZE[self.dtype]
+
+    @property
+    def cache_shape(self):
+        return (self.num_pages, self.page_size, self.Hkv, self.D)
+
+    def nblk(self) -> np.ndarray:
+        """Pages each sequence occupies (ceil(L_b / page_size))."""
+        ps = self.page_size
+        return (self.seq_lens.astype(np.int64) + ps - 1) // ps
+
+    def host_cache_available(self) -> bool:
+        return self.k_cache is not None
+
+
+def _pack_tables(B: int, W: int, nblk: Sequence[int], pages: np.ndarray, tail: int) -> np.ndarray:
+    bt = np.full((B, W), tail, dtype=np.int64)
+    pos = 0
+    for b in range(B):
+        n = int(nblk[b])
+        bt[b, :n] = pages[pos:pos + n]
+        pos += n
+    return bt.astype(np.int32)
+
+
+def make_custom(*, name: str = "custom", dtype: str = "bf16", B: int, Sq: int, Hq: int, Hkv: int,
+                D: int, page_size: int, seq_lens: Sequence[int], num_pages: Optional[int] = None,
+                W: Optional[int] = None, causal: bool = False, q_offset: Optional[Sequence[int]] = None,
+                split_kv: Sequence[int] = (1,), seed: int = 0, shuffle: bool = True,
+                tail: int = SENTINEL_MAX, scale: Optional[float] = None,
+                zero_q: bool = False) -> Workload:
+    """Draw a small host-resident workload with the given shape.
+
+    Pages are assigned to sequences in order from a seeded permutation of the
+    pool (or in identity order when ``shuffle`` is False).
+    """
+    assert dtype in DTYPES
+    rng = np.random.default_rng(seed)
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    assert seq_lens.shape == (B,)
+    nblk = (seq_lens.astype(np.int64) + page_size - 1) // page_size
+    need = int(nblk.sum())
+    if num_pages is None:
+        num_pages = max(need, 1)
+    assert num_pages >= need, "page pool smaller than the sequences need"
+    if W is None:
+        W = max(int(nblk.max()) if B else 1, 1)
+    assert W >= (int(nblk.max()) if B else 0)
+    q = _normal_elems(rng, B * Sq * Hq * D, dtype).reshape(B, Sq, Hq, D)
+    if zero_q:
+        q = np.zeros_like(q)
+    n_cache = num_pages * page_size * Hkv * D
+    k = _normal_elems(rng, n_cache, dtype).reshape(num_pages, page_size, Hkv, D)
+    v = _normal_elems(rng, n_cache, dtype).reshape(num_pages, page_size, Hkv, D)
+    perm = rng.permutation(num_pages) if shuffle else np.arange(num_pages)
+    bt = _pack_tables(B, W, nblk, perm, tail)
+    qo = None if q_offset is None else np.asarray(q_offset, dtype=np.int32)
+    return Workload(name=name, dtype=dtype, B=B, Sq=Sq, Hq=Hq, Hkv=Hkv, D=D, page_size=page_size,
+                    num_pages=num_pages, causal=causal,
+                    scale=(1.0 / math.sqrt(D)) if scale is None else float(scale),
+                    split_kv=tuple(split_kv), seq_lens=seq_lens, block_table=bt, q=q, q_offset=qo,
+                    k_cache=k, v_cache=v)
+
+
+def tiny_decode_f32(seed: int = 1001) -> Workload:
+    """Tiny f32 decode: B=2, L={37,50}, Hq=4, Hkv=2, D=64, 16 shuffled pages, table 4 wide, tail -1."""
+    return make_custom(name="tiny_decode_f32", dtype="f32", B=2, Sq=1, Hq=4, Hkv=2, D=64,
+                       page_size=16, seq_lens=[37, 50], num_pages=16, W=4, split_kv=(1, 2),
+                       seed=seed, tail=SENTINEL_NEG)
+
+
+def ragged_decode(seed: int = 1003) -> Workload:
+    """Ragged bf16 decode: B=32, Hq=64, Hkv=4, D=128, L~U[17,1000], table 63 wide, 2048 pages."""
+    rng = np.random.default_rng(seed)
+    B, Hq, Hkv, D, ps, P, W = 32, 64, 4, 128, 16, 2048, 63
+    seq_lens = rng.integers(17, 1001, size=B).astype(np.int32)
+    q = _normal_elems(rng, B * Hq * D, "bf16").reshape(B, 1, Hq, D)
+    n_cache = P * ps * Hkv * D
+    k = _normal_elems(rng, n_cache, "bf16").reshape(P, ps, Hkv, D)
+    v = _normal_elems(rng, n_cache, "bf16").reshape(P, ps, Hkv, D)
+    nblk = (seq_lens.astype(np.int64) + ps - 1) // ps
+    perm = rng.permutation(P)
+    bt = _pack_tables(B, W, nblk, perm, SENTINEL_MAX)
+    return Workload(name="ragged_decode", dtype="bf16", B=B, Sq=1, Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
+                    num_pages=P, causal=False, scale=1.0 / math.sqrt(D), split_kv=(8,),
+                    seq_lens=seq_lens, block_table=bt, q=q, k_cache=k, v_cache=v)
+
+
+def causal_prefill(seed: int = 1005, B: int = 4, Sq: int = 1024, max_q_offset: int = 3072,
+                   num_pages: int = 1024, W: int = 256) -> Workload:
+    """Causal bf16 prefill: B=4, Sq=1024, Hq=32, Hkv=8, D=128, q_offset~U[0,3072], L=q_offset+Sq."""
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D, ps = 32, 8, 128, 16
+    q_offset = rng.integers(0, max_q_offset + 1, size=B).astype(np.int32)
+    seq_lens = (q_offset + Sq).astype(np.int32)
+    q = _normal_elems(rng, B * Sq * Hq * D, "bf16").reshape(B, Sq, Hq, D)
+    n_cache = num_pages * ps * Hkv * D
+    k = _normal_elems(rng, n_cache, "bf16").reshape(num_pages, ps, Hkv, D)
+    v = _normal_elems(rng, n_cache, "bf16").reshape(num_pages, ps, Hkv, D)
+    nblk = (seq_lens.astype(np.int64) + ps - 1) // ps
+    assert int(nblk.sum()) <= num_pages and int(nblk.max()) <= W
+    perm = rng.permutation(num_pages)
+    bt = _pack_tables(B, W, nblk, perm, SENTINEL_MAX)
+    return Workload(name="causal_prefill", dtype="bf16", B=B, Sq=Sq, Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
+                    num_pages=num_pages, causal=True, scale=1.0 / math.sqrt(D), split_kv=(8,),
+                    seq_lens=seq_lens, block_table=bt, q=q, q_offset=q_offset, k_cache=k, v_cache=v)
+
+
+def llama8b_decode(seed: int = 1002, B: int = 256) -> Workload:
+    """Llama-3-8B-shaped bf16 decode: Hq=32, Hkv=8, D=128, L=4096, 65536 pages (2 GiB per pool).
+
+    The page pools are drawn on the device (see ``fill_device_cache``).
+    """
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D, ps, L = 32, 8, 128, 16, 4096
+    per_seq = L // ps
+    P = 65536 if B == 256 else B * per_seq
+    q = _normal_elems(rng, B * Hq * D, "bf16").reshape(B, 1, Hq, D)
+    perm = rng.permutation(P).astype(np.int64)
+    bt = perm[:B * per_seq].reshape(B, per_seq).astype(np.int32)
+    seq_lens = np.full(B, L, dtype=np.int32)
+    return Workload(name="llama8b_decode", dtype="bf16", B=B, Sq=1, Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
+                    num_pages=P, causal=False, scale=1.0 / math.sqrt(D), split_kv=(1, 4),
+                    seq_lens=seq_lens, block_table=bt, q=q, device_cache_seed=seed)
+
+
+OVER2G_PAGES = 135168          # 2 GiB + 64 MiB per pool at 16 KiB pages
+OVER2G_FIRST_HIGH = 131072     # page whose first byte sits at byte 2^31
+
+
+def over2gib_decode(seed: int = 1004, B: int = 256) -> Workload:
+    """bf16 decode past 2^31 bytes: Hq=64, Hkv=4, D=128, L=8192, 135168 pages per pool.
+
+    Every sequence gets 16 pages from the top 4096 (which start at or past byte
+    2^31 of the pool) and 496 from below, shuffled within its table row.
+    """
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D, ps, L = 64, 4, 128, 16, 8192
+    per_seq = L // ps                     # 512
+    n_high = 16
+    n_low = per_seq - n_high
+    assert B * n_high <= OVER2G_PAGES - OVER2G_FIRST_HIGH
+    q = _normal_elems(rng, B * Hq * D, "bf16").reshape(B, 1, Hq, D)
+    high = OVER2G_FIRST_HIGH + rng.permutation(OVER2G_PAGES - OVER2G_FIRST_HIGH).astype(np.int64)
+    low = rng.permutation(OVER2G_FIRST_HIGH).astype(np.int64)
+    rows = np.concatenate([high[:B * n_high].reshape(B, n_high),
+                           low[:B * n_low].reshape(B, n_low)], axis=1)
+    rows = rng.permuted(rows, axis=1)
+    bt = rows.astype(np.int32)
+    seq_lens = np.full(B, L, dtype=np.int32)
+    return Workload(name="over2gib_decode", dtype="bf16", B=B, Sq=1, Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
+                    num_pages=OVER2G_PAGES, causal=False, scale=1.0 / math.sqrt(D), split_kv=(4,),
+                    seq_lens=seq_lens, block_table=bt, q=q, device_cache_seed=seed)
+
+
+CONFIGS = {
+    "tiny_decode_f32": tiny_decode_f32,
+    "llama8b_decode": llama8b_decode,
+    "ragged_decode": ragged_decode,
+    "over2gib_decode": over2gib_decode,
+    "causal_prefill": causal_prefill,
+}
+
+
+def make(name: str, **kw) -> Workload:
+    return CONFIGS[name](**kw)
+
+
+# ----------------------------------------------------------------------------- device helpers
+def torch_dtype(dtype: str):
+    import torch
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+
+
+def host_to_torch(arr: np.ndarray, dtype: str):
+    """Wrap host element bits as a CPU torch tensor of the workload dtype (no copy of values)."""
+    import torch
+    if dtype == "f32":
+        return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32))
+    t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16))
+    return t.view(torch_dtype(dtype))
+
+
+def fill_device_cache(wl: Workload, device="cuda", chunk: int = 1 << 27):
+    """Draw the K and V pools on the device from the workload's seed.
+
+    ``torch.randn`` (float32, seeded ``torch.Generator`` on the device) rounded to
+    the workload dtype by torch's cast (round-to-nearest-even).
+    """
+    import torch
+    assert wl.device_cache_seed is not None
+    tdt = torch_dtype(wl.dtype)
+    out = []
+    for which in (0, 1):
+        g = torch.Generator(device=device)
+        g.manual_seed(int(wl.device_cache_seed) * 2 + which)
+        t = torch.empty(wl.cache_shape, dtype=tdt, device=device)
+        flat = t.view(-1)
+        n = flat.numel()
+        for s in range(0, n, chunk):
+            e = min(n, s + chunk)
+            flat[s:e].copy_(torch.randn(e - s, generator=g, device=device, dtype=torch.float32))
+        out.append(t)
+    return out[0], out[1]
