@@ -1,0 +1,429 @@
+"""Benchmark: paged decode over a 2-GiB-per-pool paged K/V cache on GB300.
+
+Default workload: Llama-3-8B-shaped bf16 decode (B=256, one query token,
+Hq=32, Hkv=8, D=128, 4096 keys per sequence, page_size 16, 65536 shuffled pages
+per pool = 2 GiB each).  A step is one pass of the whole hot path over the
+batch: the paged forward (block-table gather, staging, QK, mask, online
+softmax, PV, per-split finalise) and, when split_kv > 1, the combine.
+
+Prints one JSON line.  ``value`` is algorithmic bytes per step / step time
+(GB/s), where algorithmic bytes = the K and V bytes of every valid token + q +
+out + the block-table ids read; inputs (2 x 2 GiB) exceed L2, so no flush is
+needed between steps.  ``--impl reference`` times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "paged decode KV-read HBM GB/s and % of GB300 peak; µs per decode step"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b_decode",
+                    choices=["llama8b_decode", "over2gib_decode", "ragged_decode", "causal_prefill"])
+    ap.add_argument("--split-kv", type=int, default=None)
+    ap.add_argument("--variant", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("PA_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, max clock, throttle reasons)."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, enabled=True):
+        self.index, self.enabled, self.lines, self.proc = index, enabled, [], None
+
+    def __enter__(self):
+        if self.enabled:
+            try:
+                self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                              "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                             stderr=subprocess.DEVNULL, text=True)
+                self.thread = threading.Thread(target=self._read, daemon=True)
+                self.thread.start()
+                time.sleep(0.3)
+            except OSError:
+                self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                return json.load(f)
+        except (OSError, ValueError):
+            return None
+    return None
+
+
+def algorithmic_bytes(wl, split_kv: int) -> dict:
+    """Bytes a decode step must move: valid K and V tokens, q, out, block-table ids, seq_lens."""
+    L = wl.seq_lens.astype(np.int64)
+    kv = int(L.sum()) * wl.Hkv * wl.D * wl.esize * 2
+    q = wl.B * wl.Sq * wl.Hq * wl.D * wl.esize
+    out = q
+    ids = int(wl.nblk().sum()) * 4 + wl.B * 4
+    return {"kv": kv, "q": q, "out": out, "ids": ids, "total": kv + q + out + ids}
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_201_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(f"{kernel}/{workload}")
+    if not ent or ent.get("source_digest") != kernel_source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def build_workload(name):
+    from paged_kv_cache_201_gb300 import workloads as W
+    return W.make(name)
+
+
+def cpu_sample_rows(wl, n_seq: int):
+    """Rows (b, i, h) of the first n_seq sequences, every query token and head."""
+    import oracle
+    rows = oracle.all_rows(n_seq, wl.Sq, wl.Hq)
+    return rows
+
+
+def time_oracle(wl, k_host, v_host, split_kv: int, n_seq: int):
+    """Run the oracle on the first n_seq sequences; return (seconds, kv_bytes_processed, threads)."""
+    import oracle
+    rows = cpu_sample_rows(wl, n_seq)
+    t0 = time.perf_counter()
+    oracle.workload_rows(wl, split_kv=split_kv, row_bih=rows, k_cache=k_host, v_cache=v_host,
+                         want_split=split_kv > 1)
+    dt = time.perf_counter() - t0
+    kv = int(wl.seq_lens[:n_seq].astype(np.int64).sum()) * wl.Hkv * wl.D * wl.esize * 2
+    return dt, kv, oracle.num_threads()
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, ws, rank, local):
+    import torch
+    import paged_kv_cache_201_gb300 as pa
+    from paged_kv_cache_201_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa.load_library()
+    wl = build_workload(args.workload)
+    S = args.split_kv or wl.split_kv[0]
+    q = W.host_to_torch(wl.q, wl.dtype).to(dev)
+    if wl.k_cache is not None:
+        k = W.host_to_torch(wl.k_cache, wl.dtype).to(dev)
+        v = W.host_to_torch(wl.v_cache, wl.dtype).to(dev)
+    else:
+        k, v = W.fill_device_cache(wl, dev)
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    sl = torch.from_numpy(wl.seq_lens).to(dev)
+    qo = None if wl.q_offset is None else torch.from_numpy(wl.q_offset).to(dev)
+    B, Sq, Hq, D = wl.B, wl.Sq, wl.Hq, wl.D
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=dev)
+    po = torch.empty((S, B, Sq, Hq, D), dtype=torch.float32, device=dev) if S > 1 else None
+    pl = torch.empty((S, B, Sq, Hq), dtype=torch.float32, device=dev) if S > 1 else None
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        if S == 1:
+            pa.paged_attn_fwd_variant(q, k, v, bt, sl, wl.causal, qo, 1, wl.scale, out, lse, args.variant, stream)
+        else:
+            pa.paged_attn_fwd_variant(q, k, v, bt, sl, wl.causal, qo, S, wl.scale, po, pl, args.variant, stream)
+
+    def step():
+        fwd()
+        if S > 1:
+            pa.paged_attn_combine(po, pl, out, lse, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev_f0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_f1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local, enabled=not args.no_clocks) as clk:
+        t_start.record(stream)
+        for i in range(K):
+            ev_f0[i].record(stream)
+            fwd()
+            ev_f1[i].record(stream)
+            if S > 1:
+                pa.paged_attn_combine(po, pl, out, lse, stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    ms_total = t_start.elapsed_time(t_end)
+    fwd_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)]))
+    ms_step = max_over_ranks(ms_total / K, ws, dev)
+    flags = pa.paged_attn_last_error_word()
+    if flags:
+        raise RuntimeError(f"device error word {flags:#x} during the bench")
+
+    ab = algorithmic_bytes(wl, S)
+    value = ab["total"] * ws / (ms_step * 1e-3) / 1e9
+    peaks = measured_peaks()
+    if peaks and peaks.get("hbm_gbs"):
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    else:
+        peak, peak_src = FALLBACK_HBM_GBS, "fallback"
+    kname = "paged_attn_mma_kernel" if args.variant != 1 else "paged_attn_simt_kernel"
+    fwd_bytes = ab["total"]
+    achieved = fwd_bytes / (fwd_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API: host inputs in, host result out, every step
+    e2e = None
+    if not args.no_e2e:
+        q_h = q.cpu().pin_memory()
+        bt_h = bt.cpu().pin_memory()
+        sl_h = sl.cpu().pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+        def e2e_step():
+            q.copy_(q_h, non_blocking=True)
+            bt.copy_(bt_h, non_blocking=True)
+            sl.copy_(sl_h, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        Ke = max(10, K // 4)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b_) / Ke, ws, dev)
+        hb = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
+        db = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+        e2e = {"value": round(ab["total"] * ws / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(hb), "d2h_bytes_per_step": int(db)}
+
+    # ---- CPU baseline: the oracle on a bounded sample of the same workload (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        k_h = k.view(torch.int16).cpu().numpy().view(np.uint16) if wl.dtype != "f32" else k.cpu().numpy()
+        v_h = v.view(torch.int16).cpu().numpy().view(np.uint16) if wl.dtype != "f32" else v.cpu().numpy()
+        n_seq = min(wl.B, 16)
+        dt, kvb, thr = time_oracle(wl, k_h, v_h, S, n_seq)
+        cpu = {"value": round(kvb / dt / 1e9, 3), "unit": "GB/s", "cores": thr, "kind": "oracle",
+               "sample": f"first {n_seq} of {wl.B} sequences, every head, split_kv={S}; {dt:.2f} s fp64",
+               "seconds": round(dt, 3)}
+
+    clocks = clk.summary() if not args.no_clocks else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(ms_step * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic (seeded N(0,1) rounded to bf16; shuffled pages)",
+        "config": {"workload": args.workload, "B": wl.B, "Sq": wl.Sq, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+                   "page_size": wl.page_size, "num_pages": wl.num_pages, "seq_len": int(wl.seq_lens.max()),
+                   "split_kv": S, "variant": args.variant, "l2": "inputs (2 x 2 GiB pools) larger than L2",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "pct_of_peak": round(100.0 * value / ws / peak, 2),
+        "bytes_per_step": ab,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "kernel_ms": round(fwd_ms, 5), "traffic": recorded_traffic(kname, args.workload)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * (2 if S > 1 else 1),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args, ws, rank, local):
+    if rank != 0:
+        return
+    import torch
+    from paged_kv_cache_201_gb300 import workloads as W
+    import oracle
+
+    wl = build_workload(args.workload)
+    S = args.split_kv or wl.split_kv[0]
+    if wl.k_cache is not None:
+        k_h, v_h = wl.k_cache, wl.v_cache
+    else:
+        dev = torch.device("cuda", local) if torch.cuda.is_available() else None
+        if dev is None:
+            print(json.dumps({"impl": "reference", "unavailable": "the 2-GiB pools are drawn on a CUDA device"}))
+            return
+        k, v = W.fill_device_cache(wl, dev)
+        k_h = k.view(torch.int16).cpu().numpy().view(np.uint16)
+        v_h = v.view(torch.int16).cpu().numpy().view(np.uint16)
+        del k, v
+    n_seq = min(wl.B, 4)
+    for _ in range(max(args.warmup, 3) if args.warmup < 3 else 1):
+        time_oracle(wl, k_h, v_h, S, 1)
+    times, kv = [], 0
+    for _ in range(args.steps if args.steps <= 20 else 20):
+        dt, kv, thr = time_oracle(wl, k_h, v_h, S, n_seq)
+        times.append(dt)
+    ms = float(np.mean(times)) * 1e3
+    value = kv / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": len(times),
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) rounded to bf16; shuffled pages)",
+        "config": {"workload": args.workload, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+                   "page_size": wl.page_size, "split_kv": S, "sample_sequences": n_seq},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"first {n_seq} of {wl.B} sequences per step, every head"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, ws, rank, local)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

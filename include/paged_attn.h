@@ -1,0 +1,172 @@
+/*
+ * paged_attn.h — C ABI of the GB300 (sm_103a) paged-attention library.
+ *
+ * The operation: for every query token i of sequence b and every query head h,
+ * attend over that sequence's keys, which live in a pool of fixed-size pages
+ * reached through a per-sequence block table.  Scores are scale * q.k; key j is
+ * valid iff j < seq_lens[b] and, when causal, j <= q_offset[b] + i; the softmax
+ * of the valid scores weights the V rows.  The keys may be split into split_kv
+ * partitions, each giving a normalised partial output plus its log-sum-exp,
+ * which paged_attn_combine merges.
+ *
+ * Sources (page titles and sections):
+ *   rocm-libraries PR #14349 (gfx942 tiled-2D attention), Motivation and
+ *     Technical Details: paged K/V through a block table; pages of page_size
+ *     tokens holding every kv head; 64-bit page bases for pools past 2^31
+ *     bytes; page ids loaded once per tile; GQA head groups.
+ *   rocMLIR PR #2220 "Paged Attention: migraphx & highlevel pipeline changes":
+ *     attention whose K/V arrive through an address view of paged storage.
+ *   rocMLIR PR #2371 "Fix split-kv attention masking...", Technical Details:
+ *     ceil-divided split partition with clamped (empty) trailing splits; the
+ *     -inf - (-inf) guard; the 0/0 guard; per-row causal reach with the prefix
+ *     offset; an f32 combine for narrow float types.
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers, dense and row-major, 16-byte
+ *     aligned.  The caller owns every buffer; the library allocates nothing.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  The returned status reports argument validation and launch
+ *     errors only; faults inside a kernel surface on the stream as CUDA errors.
+ *   - Block-table slots at or past ceil(seq_lens[b] / page_size) are never
+ *     read, so they may hold anything (-1, 0x7FFFFFFF, garbage).
+ *   - A page id that is read and lies outside [0, num_pages) is not
+ *     dereferenced: its tokens read as zero and bit PA_ERRBIT_PAGE_RANGE is set
+ *     in the device error word (see paged_attn_last_error_word).
+ */
+#ifndef PAGED_ATTN_H
+#define PAGED_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types */
+enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 };
+
+/* status codes */
+enum {
+    PA_OK = 0,
+    PA_EINVAL = -1,        /* inconsistent or out-of-range argument */
+    PA_EDTYPE = -2,        /* unsupported element type */
+    PA_EUNSUPPORTED = -3,  /* shape outside the supported envelope (or forced variant cannot run it) */
+    PA_ECUDA = -4,         /* a CUDA runtime/driver call failed */
+    PA_EBOUNDS = -5        /* device error word reported an out-of-range page id */
+};
+
+/* bits of the device error word */
+enum {
+    PA_ERRBIT_PAGE_RANGE = 1u,   /* a block-table page id used by a sequence was outside [0, num_pages) */
+    PA_ERRBIT_TIMEOUT = 2u,      /* a pipeline wait gave up after its time limit (results invalid) */
+    PA_ERRBIT_SEQ_CLIPPED = 4u   /* seq_lens[b] needed more pages than bt_stride holds; clipped to bt_stride pages */
+};
+
+/* kernel variants (paged_attn_fwd_variant) */
+enum {
+    PA_VARIANT_AUTO = 0,         /* planner's choice */
+    PA_VARIANT_SIMT = 1,         /* CUDA-core kernel: any dtype, any head grouping */
+    PA_VARIANT_MMA_DECODE = 2,   /* tensor-core decode: Sq * (Hq/Hkv) <= 16 rows, keys split across warps */
+    PA_VARIANT_MMA_PREFILL = 3   /* tensor-core 64-row query tiles (prefill / long query runs) */
+};
+
+/*
+ * Problem shape.
+ *   q            [batch, q_len, num_q_heads, head_dim]               (dtype)
+ *   k/v pools    [num_pages, page_size, num_kv_heads, head_dim]      (dtype)
+ *   block_table  [batch, bt_stride] int32; row b lists the physical pages of
+ *                sequence b in logical order
+ *   seq_lens     [batch] int32: valid K/V tokens of sequence b, including its
+ *                q_len newest tokens
+ *   q_offset     [batch] int32 or NULL: position of query row 0 of sequence b
+ *                inside its K/V sequence (NULL means seq_lens[b] - q_len)
+ * Supported: dtype in {PA_F32, PA_F16, PA_BF16}; head_dim in {64, 128};
+ * page_size in {16, 32, 64}; num_q_heads a multiple of num_kv_heads;
+ * num_pages * page_size < 2^31 tokens (each pool may exceed 2^31 bytes).
+ */
+typedef struct pa_dims {
+    int32_t batch;         /* B */
+    int32_t q_len;         /* Sq */
+    int32_t num_q_heads;   /* Hq */
+    int32_t num_kv_heads;  /* Hkv */
+    int32_t head_dim;      /* D */
+    int32_t page_size;     /* tokens per page */
+    int64_t num_pages;     /* pages in each of the K and V pools */
+    int32_t bt_stride;     /* elements between consecutive block-table rows */
+    int32_t dtype;         /* PA_F32 / PA_F16 / PA_BF16 */
+} pa_dims;
+
+/*
+ * paged_attn_fwd — attention over the paged K/V cache, per split partition.
+ *
+ * split_kv = S >= 1.  Sequence b's nblk = ceil(seq_lens[b] / page_size) pages
+ * are cut into S runs of per = ceil(nblk / S) pages; run s covers pages
+ * [min(s*per, nblk), min((s+1)*per, nblk)), so trailing runs may be empty
+ * (rocMLIR PR #2371, split-KV iteration math).
+ *
+ * scale multiplies q.k.  Outputs:
+ *   S == 1: out [B, Sq, Hq, D] in dtype (round to nearest even);
+ *           lse [B, Sq, Hq] float32 natural-log sum-exp, or NULL.
+ *   S >  1: out [S, B, Sq, Hq, D] float32 per-split outputs, each normalised by
+ *           its own softmax sum; lse [S, B, Sq, Hq] float32 (required).
+ * A row with no valid key in a partition gets output 0 and lse -inf, never
+ * NaN (rocMLIR PR #2371, the -inf - (-inf) and 0/0 guards).
+ * Returns PA_OK or a negative status; nothing is launched on error.
+ */
+int paged_attn_fwd(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                   const int32_t *seq_lens, int causal, const int32_t *q_offset, int split_kv, float scale,
+                   void *out, float *lse, const pa_dims *dims, void *stream);
+
+/* paged_attn_fwd with a forced kernel variant (PA_VARIANT_*); PA_EUNSUPPORTED
+ * if that variant cannot run the shape or dtype.  Same arguments otherwise. */
+int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                           const int32_t *seq_lens, int causal, const int32_t *q_offset, int split_kv,
+                           float scale, void *out, float *lse, const pa_dims *dims, int variant, void *stream);
+
+/*
+ * paged_attn_combine — merge split partials (rocMLIR PR #2371, f32 combine).
+ *   part_out [S, rows, head_dim] float32, part_lse [S, rows] float32, where
+ *   rows = B * Sq * Hq.  For each row: M = max_s lse_s; w_s = exp(lse_s - M);
+ *   out = sum_s w_s O_s / sum_s w_s in float32, stored in out_dtype (round to
+ *   nearest even); lse = M + log(sum_s w_s).  M = -inf gives out 0, lse -inf.
+ *   out [rows, head_dim] (out_dtype); lse [rows] float32 or NULL.
+ */
+int paged_attn_combine(const float *part_out, const float *part_lse, int split_kv, int64_t rows, int head_dim,
+                       int out_dtype, void *out, float *lse, void *stream);
+
+/*
+ * paged_attn_plan — the split plan as data: plan [batch, split_kv, 2] int32 =
+ * {first page, one past the last page} of each run (see paged_attn_fwd).
+ * seq_lens is a device pointer [batch]; negative lengths count as 0.
+ */
+int paged_attn_plan(const int32_t *seq_lens, int batch, int page_size, int split_kv, int32_t *plan,
+                    void *stream);
+
+/*
+ * paged_attn_debug_gather — logically ordered copy of one pool:
+ * out [batch, out_tokens, num_kv_heads, head_dim] (dtype); token j of sequence
+ * b is copied bit for bit from its page for j < min(seq_lens[b], out_tokens)
+ * and written as zero bits beyond seq_lens[b] (rocMLIR PR #2222, Key Changes
+ * 1: the [numPages, pageSize] -> [seqK] view).
+ */
+int paged_attn_debug_gather(const void *cache, const int32_t *block_table, const int32_t *seq_lens,
+                            const pa_dims *dims, int out_tokens, void *out, void *stream);
+
+/*
+ * paged_attn_last_error_word — synchronise the current device, then read and
+ * clear its error word (PA_ERRBIT_* bits accumulated by every call since the
+ * last read).  Returns PA_OK, or PA_ECUDA if the read failed.
+ */
+int paged_attn_last_error_word(uint32_t *flags);
+
+/* Human-readable text for a status code (static storage). */
+const char *paged_attn_strerror(int code);
+
+/* Library version as an integer, major * 10000 + minor * 100 + patch. */
+int paged_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTN_H */

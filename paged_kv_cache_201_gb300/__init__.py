@@ -1,0 +1,247 @@
+"""Paged attention over a paged K/V cache on GB300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/paged_attn.h``: it checks that the
+tensors are CUDA, dense and of the right type, marshals their pointers and the
+current stream, and calls the library.  Every step of the computation runs in
+the library's CUDA kernels; there is no CPU or PyTorch fallback, and a missing
+library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import build as _build
+
+__all__ = [
+    "PagedAttnError", "load_library", "library_path", "paged_attn_fwd", "paged_attn_fwd_variant",
+    "paged_attn_combine", "paged_attn_plan", "paged_attn_debug_gather", "paged_attn_last_error_word",
+    "paged_attn_strerror", "paged_attn_version", "attention", "PA_F32", "PA_F16", "PA_BF16",
+    "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL",
+]
+
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA_DECODE, VARIANT_MMA_PREFILL = 0, 1, 2, 3
+ERRBIT_PAGE_RANGE, ERRBIT_TIMEOUT, ERRBIT_SEQ_CLIPPED = 1, 2, 4
+
+
+class PaDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("q_len", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64), ("bt_stride", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: status {code} ({paged_attn_strerror(code)})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = False):
+    """Load the CUDA library (``_build/libpaged_attn_gb300.so``); raise if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"paged-attention CUDA library not built ({path}); run "
+                               "paged_kv_cache_201_gb300.build.build()")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    P, I32, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    D = ctypes.POINTER(PaDims)
+    lib.paged_attn_fwd.argtypes = [P, P, P, P, P, I32, P, I32, F, P, P, D, P]
+    lib.paged_attn_fwd_variant.argtypes = [P, P, P, P, P, I32, P, I32, F, P, P, D, I32, P]
+    lib.paged_attn_combine.argtypes = [P, P, I32, I64, I32, I32, P, P, P]
+    lib.paged_attn_plan.argtypes = [P, I32, I32, I32, P, P]
+    lib.paged_attn_debug_gather.argtypes = [P, P, P, D, I32, P, P]
+    lib.paged_attn_last_error_word.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.paged_attn_strerror.argtypes = [I32]
+    lib.paged_attn_strerror.restype = ctypes.c_char_p
+    lib.paged_attn_version.argtypes = []
+    for name in ("paged_attn_fwd", "paged_attn_fwd_variant", "paged_attn_combine", "paged_attn_plan",
+                 "paged_attn_debug_gather", "paged_attn_last_error_word", "paged_attn_version"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+# ----------------------------------------------------------------------------- marshalling helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    m = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, dtype=None, ndim=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def dims_of(q, k_cache, block_table) -> PaDims:
+    B, Sq, Hq, D = q.shape
+    P, ps, Hkv, D2 = k_cache.shape
+    if D2 != D:
+        raise ValueError("q and k_cache head dims differ")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, W]")
+    return PaDims(B, Sq, Hq, Hkv, D, ps, P, block_table.shape[1], _dtype_code(q))
+
+
+def _raise(rc: int, where: str):
+    if rc != 0:
+        raise PagedAttnError(rc, where)
+
+
+# ----------------------------------------------------------------------------- C ABI wrappers
+def paged_attn_fwd_variant(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale, out,
+                           lse, variant: int = VARIANT_AUTO, stream=None) -> None:
+    """Forward over the paged cache; see ``paged_attn_fwd`` in include/paged_attn.h."""
+    torch = _torch()
+    _check(q, "q", ndim=4)
+    _check(k_cache, "k_cache", q.dtype, 4)
+    _check(v_cache, "v_cache", q.dtype, 4)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    _check(q_offset, "q_offset", torch.int32, 1)
+    _check(out, "out")
+    _check(lse, "lse", torch.float32)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    dims = dims_of(q, k_cache, block_table)
+    rc = load_library().paged_attn_fwd_variant(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), int(bool(causal)),
+        _ptr(q_offset), int(split_kv), float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), int(variant),
+        _stream(stream))
+    _raise(rc, "paged_attn_fwd")
+
+
+def paged_attn_fwd(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale, out, lse,
+                   stream=None) -> None:
+    paged_attn_fwd_variant(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale, out, lse,
+                           VARIANT_AUTO, stream)
+
+
+def paged_attn_combine(part_out, part_lse, out, lse=None, stream=None) -> None:
+    """Merge split partials: part_out [S, ..., D] f32, part_lse [S, ...] f32 -> out [..., D], lse [...]."""
+    torch = _torch()
+    _check(part_out, "part_out", torch.float32)
+    _check(part_lse, "part_lse", torch.float32)
+    _check(out, "out")
+    _check(lse, "lse", torch.float32)
+    S = part_out.shape[0]
+    D = part_out.shape[-1]
+    rows = part_out.numel() // (S * D) if S * D else 0
+    if part_lse.numel() != S * rows or out.numel() != rows * D:
+        raise ValueError("combine shapes disagree")
+    rc = load_library().paged_attn_combine(_ptr(part_out), _ptr(part_lse), int(S), int(rows), int(D),
+                                           _dtype_code(out), _ptr(out), _ptr(lse), _stream(stream))
+    _raise(rc, "paged_attn_combine")
+
+
+def paged_attn_plan(seq_lens, page_size: int, split_kv: int, plan=None, stream=None):
+    torch = _torch()
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    B = seq_lens.shape[0]
+    if plan is None:
+        plan = torch.empty((B, split_kv, 2), dtype=torch.int32, device=seq_lens.device)
+    _check(plan, "plan", torch.int32)
+    rc = load_library().paged_attn_plan(_ptr(seq_lens), B, int(page_size), int(split_kv), _ptr(plan),
+                                        _stream(stream))
+    _raise(rc, "paged_attn_plan")
+    return plan
+
+
+def paged_attn_debug_gather(cache, block_table, seq_lens, out_tokens: int, out=None, stream=None):
+    torch = _torch()
+    _check(cache, "cache", ndim=4)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    P, ps, Hkv, D = cache.shape
+    B = block_table.shape[0]
+    if out is None:
+        out = torch.empty((B, out_tokens, Hkv, D), dtype=cache.dtype, device=cache.device)
+    _check(out, "out", cache.dtype)
+    dims = PaDims(B, 1, Hkv, Hkv, D, ps, P, block_table.shape[1], _dtype_code(cache))
+    rc = load_library().paged_attn_debug_gather(_ptr(cache), _ptr(block_table), _ptr(seq_lens), ctypes.byref(dims),
+                                                int(out_tokens), _ptr(out), _stream(stream))
+    _raise(rc, "paged_attn_debug_gather")
+    return out
+
+
+def paged_attn_last_error_word() -> int:
+    v = ctypes.c_uint32(0)
+    _raise(load_library().paged_attn_last_error_word(ctypes.byref(v)), "paged_attn_last_error_word")
+    return int(v.value)
+
+
+def paged_attn_strerror(code: int) -> str:
+    return load_library().paged_attn_strerror(int(code)).decode()
+
+
+def paged_attn_version() -> int:
+    return int(load_library().paged_attn_version())
+
+
+# ----------------------------------------------------------------------------- convenience
+def attention(q, k_cache, v_cache, block_table, seq_lens, *, causal: bool = False, q_offset=None,
+              split_kv: int = 1, scale: Optional[float] = None, want_lse: bool = False,
+              variant: int = VARIANT_AUTO, partials=None, stream=None):
+    """Full forward: allocate outputs, run the split forward and, when split_kv > 1, the combine.
+
+    Returns ``out`` ([B, Sq, Hq, D], q's dtype) or ``(out, lse)`` with ``want_lse``.
+    ``partials`` may pass preallocated (part_out [S,B,Sq,Hq,D] f32, part_lse [S,B,Sq,Hq] f32).
+    """
+    torch = _torch()
+    B, Sq, Hq, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device) if (want_lse or split_kv > 1) else None
+    if split_kv == 1:
+        paged_attn_fwd_variant(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, 1, scale, out, lse,
+                               variant, stream)
+    else:
+        if partials is None:
+            po = torch.empty((split_kv, B, Sq, Hq, D), dtype=torch.float32, device=q.device)
+            pl = torch.empty((split_kv, B, Sq, Hq), dtype=torch.float32, device=q.device)
+        else:
+            po, pl = partials
+        paged_attn_fwd_variant(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale, po,
+                               pl, variant, stream)
+        paged_attn_combine(po, pl, out, lse, stream)
+    return (out, lse) if want_lse else out

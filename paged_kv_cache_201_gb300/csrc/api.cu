@@ -1,0 +1,248 @@
+// C ABI of the paged-attention library: argument validation, kernel choice,
+// TMA descriptor set-up and launches.  Everything here runs on the host; the
+// arithmetic of the operation lives in the kernels.
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kernels.h"
+
+namespace {
+
+// Device error word: kernels OR PA_ERRBIT_* bits into it; paged_attn_last_error_word reads and clears it.
+__device__ unsigned int g_pa_error_word;
+
+constexpr int kMaxDevices = 128;
+unsigned int *g_err_ptr[kMaxDevices];
+std::mutex g_err_mu;
+
+int error_word_ptr(unsigned int **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ECUDA;
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_err_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_pa_error_word) != cudaSuccess) return PA_ECUDA;
+        g_err_ptr[dev] = static_cast<unsigned int *>(ptr);
+    }
+    *out = g_err_ptr[dev];
+    return PA_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int esize_of(int dtype) { return dtype == PA_F32 ? 4 : 2; }
+
+// Shape checks shared by the forward and gather entry points.
+int check_dims(const pa_dims *d) {
+    if (!d) return PA_EINVAL;
+    if (d->dtype != PA_F32 && d->dtype != PA_F16 && d->dtype != PA_BF16) return PA_EDTYPE;
+    if (d->batch < 0 || d->q_len < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->bt_stride < 0)
+        return PA_EINVAL;
+    if (d->num_q_heads % d->num_kv_heads != 0) return PA_EINVAL;
+    if (d->head_dim != 64 && d->head_dim != 128) return PA_EUNSUPPORTED;
+    if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64) return PA_EUNSUPPORTED;
+    if (d->num_pages < 1) return PA_EINVAL;
+    if (d->num_pages * (int64_t)d->page_size >= (int64_t)1 << 31) return PA_EUNSUPPORTED;
+    if ((int64_t)d->bt_stride * d->page_size >= (int64_t)1 << 31) return PA_EUNSUPPORTED;
+    if ((int64_t)d->q_len * (d->num_q_heads / d->num_kv_heads) >= (int64_t)1 << 31) return PA_EUNSUPPORTED;
+    return PA_OK;
+}
+
+// 4-D view of one pool for TMA: (d within a 64-element half, token, half, kv head),
+// box = (64, page_size, D/64, 1): one page of one kv head per copy.
+int make_pool_map(CUtensorMap *m, const void *base, const pa_dims *d) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PA_ECUDA;
+    const cuuint64_t esz = 2;
+    const cuuint64_t D = (cuuint64_t)d->head_dim, Hkv = (cuuint64_t)d->num_kv_heads;
+    const cuuint64_t dims[4] = {64, (cuuint64_t)d->num_pages * (cuuint64_t)d->page_size, D / 64, Hkv};
+    const cuuint64_t strides[3] = {Hkv * D * esz, 64 * esz, D * esz};
+    const cuuint32_t box[4] = {64, (cuuint32_t)d->page_size, (cuuint32_t)(D / 64), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt =
+        d->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
+}
+
+int choose_variant(const pa_dims *d) {
+    if (d->dtype == PA_F32) return PA_VARIANT_SIMT;
+    const int64_t rows = (int64_t)d->q_len * (d->num_q_heads / d->num_kv_heads);
+    if (rows <= 1) return PA_VARIANT_SIMT;  // single-head decode: a 16-row tile would be 1/16 used
+    if (rows <= pa::kDecodeRows) return PA_VARIANT_MMA_DECODE;
+    return PA_VARIANT_MMA_PREFILL;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                           const int32_t *seq_lens, int causal, const int32_t *q_offset, int split_kv,
+                           float scale, void *out, float *lse, const pa_dims *dims, int variant, void *stream) {
+    int rc = check_dims(dims);
+    if (rc != PA_OK) return rc;
+    if (split_kv < 1 || split_kv > 65535) return PA_EINVAL;
+    if (!isfinite(scale)) return PA_EINVAL;
+    const int64_t nrows = (int64_t)dims->batch * dims->q_len * dims->num_q_heads;
+    if (nrows == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PA_EINVAL;
+    if (split_kv > 1 && !lse) return PA_EINVAL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(q_offset) & 3u))
+        return PA_EINVAL;
+    if (variant == PA_VARIANT_AUTO) variant = choose_variant(dims);
+    const int G = dims->num_q_heads / dims->num_kv_heads;
+    const int rows = dims->q_len * G;
+    switch (variant) {
+        case PA_VARIANT_SIMT:
+            break;
+        case PA_VARIANT_MMA_DECODE:
+            if (dims->dtype == PA_F32 || rows > pa::kDecodeRows) return PA_EUNSUPPORTED;
+            break;
+        case PA_VARIANT_MMA_PREFILL:
+            if (dims->dtype == PA_F32) return PA_EUNSUPPORTED;
+            break;
+        default:
+            return PA_EINVAL;
+    }
+    if (dims->batch == 0 || dims->q_len == 0) return PA_OK;
+
+    unsigned int *err = nullptr;
+    rc = error_word_ptr(&err);
+    if (rc != PA_OK) return rc;
+
+    pa::FwdParams p{};
+    p.q = q;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.q_offset = q_offset;
+    p.out = out;
+    p.lse = lse;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.err = err;
+    p.num_pages = dims->num_pages;
+    p.B = dims->batch;
+    p.Sq = dims->q_len;
+    p.Hq = dims->num_q_heads;
+    p.Hkv = dims->num_kv_heads;
+    p.D = dims->head_dim;
+    p.ps = dims->page_size;
+    p.W = dims->bt_stride;
+    p.G = G;
+    p.rows = rows;
+    p.causal = causal ? 1 : 0;
+    p.split_kv = split_kv;
+    p.scale_log2 = scale * pa::kLog2e;
+    p.row_tiles = 1;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (variant == PA_VARIANT_SIMT) {
+        e = pa::launch_simt(p, dims->dtype, st);
+    } else {
+        CUtensorMap tmk, tmv;
+        if ((rc = make_pool_map(&tmk, k_cache, dims)) != PA_OK) return rc;
+        if ((rc = make_pool_map(&tmv, v_cache, dims)) != PA_OK) return rc;
+        const int mode = variant == PA_VARIANT_MMA_DECODE ? pa::MODE_DECODE : pa::MODE_PREFILL;
+        if (mode == pa::MODE_PREFILL) p.row_tiles = (rows + pa::kPrefillRows - 1) / pa::kPrefillRows;
+        e = pa::launch_mma(p, mode, dims->dtype, tmk, tmv, st);
+    }
+    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+int paged_attn_fwd(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                   const int32_t *seq_lens, int causal, const int32_t *q_offset, int split_kv, float scale,
+                   void *out, float *lse, const pa_dims *dims, void *stream) {
+    return paged_attn_fwd_variant(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale, out,
+                                  lse, dims, PA_VARIANT_AUTO, stream);
+}
+
+int paged_attn_combine(const float *part_out, const float *part_lse, int split_kv, int64_t rows, int head_dim,
+                       int out_dtype, void *out, float *lse, void *stream) {
+    if (out_dtype != PA_F32 && out_dtype != PA_F16 && out_dtype != PA_BF16) return PA_EDTYPE;
+    if (split_kv < 1 || split_kv > 65535 || rows < 0) return PA_EINVAL;
+    if (head_dim != 64 && head_dim != 128) return PA_EUNSUPPORTED;
+    if (rows == 0) return PA_OK;
+    if (!part_out || !part_lse || !out) return PA_EINVAL;
+    if (!aligned16(part_out) || !aligned16(out) || (reinterpret_cast<uintptr_t>(part_lse) & 3u) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return PA_EINVAL;
+    cudaError_t e = pa::launch_combine(part_out, part_lse, split_kv, (long long)rows, head_dim, out_dtype, out, lse,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+int paged_attn_plan(const int32_t *seq_lens, int batch, int page_size, int split_kv, int32_t *plan, void *stream) {
+    if (batch < 0 || page_size <= 0 || split_kv < 1 || split_kv > 65535) return PA_EINVAL;
+    if (batch == 0) return PA_OK;
+    if (!seq_lens || !plan) return PA_EINVAL;
+    cudaError_t e = pa::launch_plan(seq_lens, batch, page_size, split_kv, plan, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+int paged_attn_debug_gather(const void *cache, const int32_t *block_table, const int32_t *seq_lens,
+                            const pa_dims *dims, int out_tokens, void *out, void *stream) {
+    int rc = check_dims(dims);
+    if (rc != PA_OK) return rc;
+    if (out_tokens < 0) return PA_EINVAL;
+    if (dims->batch == 0 || out_tokens == 0) return PA_OK;
+    if (!cache || !block_table || !seq_lens || !out) return PA_EINVAL;
+    if (!aligned16(cache) || !aligned16(out)) return PA_EINVAL;
+    unsigned int *err = nullptr;
+    if ((rc = error_word_ptr(&err)) != PA_OK) return rc;
+    cudaError_t e = pa::launch_gather(cache, block_table, seq_lens, dims->batch, dims->bt_stride, dims->page_size,
+                                      dims->num_kv_heads, dims->head_dim, esize_of(dims->dtype), dims->num_pages,
+                                      out_tokens, out, err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+}
+
+int paged_attn_last_error_word(uint32_t *flags) {
+    if (!flags) return PA_EINVAL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return PA_ECUDA;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_pa_error_word, sizeof v) != cudaSuccess) return PA_ECUDA;
+    if (cudaMemcpyToSymbol(g_pa_error_word, &zero, sizeof zero) != cudaSuccess) return PA_ECUDA;
+    *flags = v;
+    return PA_OK;
+}
+
+const char *paged_attn_strerror(int code) {
+    switch (code) {
+        case PA_OK: return "ok";
+        case PA_EINVAL: return "invalid argument";
+        case PA_EDTYPE: return "unsupported element type";
+        case PA_EUNSUPPORTED: return "unsupported shape or variant";
+        case PA_ECUDA: return "CUDA call failed";
+        case PA_EBOUNDS: return "out-of-range page id";
+        default: return "unknown status";
+    }
+}
+
+int paged_attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,495 @@
+// Tensor-core paged attention for sm_103a (bf16 / f16, head_dim 64 or 128).
+//
+// One CTA = one (sequence b, kv head, split s[, query-row tile]) unit:
+//   * warp 4 (producer) walks the unit's pages.  It loads the block-table ids
+//     of 32 pages at a time (one id per lane, guarded by the sequence's page
+//     count, never past it) and turns each id into a TMA coordinate; the TMA
+//     unit forms the 64-bit address, so pools past 2^31 bytes need no special
+//     path.  Each page of each pool is one 4-D TMA box (page_size tokens x one
+//     kv head x head_dim) landing 128-byte-swizzled in a NSTAGE-deep ring of
+//     64-key stages (rocm-libraries PR #14349, Technical Details: page ids
+//     loaded once per tile, no per-copy reload).
+//   * warps 0-3 (consumers) compute S = Q K^T and O += P V with
+//     mma.m16n8k16 (fp32 accumulate).  Decode mode: the 16 rows are the GQA
+//     group (x query tokens) and the 4 warps split each stage's 64 keys, then
+//     merge their softmax states once at the end.  Prefill mode: each warp owns
+//     16 query rows and reads all 64 keys of the stage.
+//   * online softmax in the log2 domain with the rocMLIR PR #2371 guards: a
+//     running max of -inf is replaced by 0 before exp2 (so -inf - (-inf)
+//     never appears), and a row whose sum is 0 stores 0 / lse -inf.
+#include "kernels.h"
+
+namespace pa {
+
+namespace {
+
+
+
+template <int D>
+struct Geo {
+    static constexpr int NH = D / 64;                              // 128-byte halves of a row
+    static constexpr int kStageBytes = kMmaTileKeys * D * 2;       // K (or V) bytes of one stage
+    static constexpr int kChunks = D / 8;                          // 16-byte chunks per row
+};
+
+// Shared address of 16-byte chunk c of key row k (0..63) of a stage buffer.
+// A stage holds 64 / page_size page boxes; a box is [NH halves][page_size][64]
+// with the TMA 128-byte swizzle (chunk index XOR row % 8, row % 8 == k % 8).
+template <int D>
+__device__ __forceinline__ uint32_t kv_chunk_addr(uint32_t base, int k, int c, int ps_shift) {
+    const int page = k >> ps_shift;
+    const int t = k & ((1 << ps_shift) - 1);
+    const int row = ((page * Geo<D>::NH + (c >> 3)) << ps_shift) + t;
+    return base + (uint32_t)(row << 7) + (uint32_t)((((c & 7) ^ (k & 7))) << 4);
+}
+
+__device__ __forceinline__ long long out_row_index(const FwdParams &p, int b, int kvh, int r) {
+    const int i = r / p.G;
+    const int h = kvh * p.G + (r - i * p.G);
+    return ((long long)b * p.Sq + i) * p.Hq + h;
+}
+
+// Write two adjacent output columns of one row.
+template <typename T>
+__device__ __forceinline__ void store_pair(const FwdParams &p, int s, long long ridx, int col, float v0, float v1) {
+    if (p.split_kv == 1) {
+        T *o = reinterpret_cast<T *>(p.out) + ridx * p.D + col;
+        o[0] = from_float<T>(v0);
+        o[1] = from_float<T>(v1);
+    } else {
+        const long long rows_total = (long long)p.B * p.Sq * p.Hq;
+        float2 *o = reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.out) +
+                                               ((long long)s * rows_total + ridx) * p.D + col);
+        *o = make_float2(v0, v1);
+    }
+}
+
+__device__ __forceinline__ void store_lse(const FwdParams &p, int s, long long ridx, float v) {
+    if (p.split_kv == 1) {
+        if (p.lse) p.lse[ridx] = v;
+    } else {
+        const long long rows_total = (long long)p.B * p.Sq * p.Hq;
+        p.lse[(long long)s * rows_total + ridx] = v;
+    }
+}
+
+}  // namespace
+
+template <typename T, int D, int MODE, int NSTAGE>
+__global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
+    paged_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const FwdParams p, int ps_shift) {
+    using Op = MmaOp<T>;
+    constexpr int kStage = Geo<D>::kStageBytes;
+    constexpr int kChunks = Geo<D>::kChunks;
+    constexpr int NKW = (MODE == MODE_DECODE) ? 16 : 64;  // keys a warp handles per stage
+    constexpr int NT = NKW / 8;                           // score n-tiles per warp per stage
+    constexpr int CTA_ROWS = (MODE == MODE_DECODE) ? kDecodeRows : kPrefillRows;
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[3 * NSTAGE];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int ps = 1 << ps_shift;
+
+    // ---- unit coordinates
+    int unit = blockIdx.x;
+    int rt = 0;
+    if (MODE == MODE_PREFILL) {
+        rt = unit % p.row_tiles;
+        unit /= p.row_tiles;
+    }
+    const int kvh = unit % p.Hkv;
+    unit /= p.Hkv;
+    const int s = unit % p.split_kv;
+    const int b = unit / p.split_kv;
+
+    int L = max(p.seq_lens[b], 0);
+    if (L > p.W * ps) {  // never read past the sequence's block-table row
+        if (threadIdx.x == 0) atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
+        L = p.W * ps;
+    }
+    int pg0, pg1;
+    split_pages(L, ps, p.split_kv, s, pg0, pg1);
+    const int k_lo = pg0 * ps;
+    const int k_hi_split = min(pg1 * ps, L);
+    const int row0 = rt * CTA_ROWS;
+    const int row_end = min(row0 + CTA_ROWS, p.rows);
+    // causal reach grows with the query index, so the CTA's last row reaches furthest
+    const int k_hi = min(k_hi_split, row_key_limit(p, b, L, (row_end - 1) / p.G));
+    const int n_tiles = k_hi > k_lo ? (k_hi - k_lo + kMmaTileKeys - 1) / kMmaTileKeys : 0;
+
+    if (n_tiles == 0) {
+        // no valid key for any row of this unit: output 0, lse -inf
+        if (warp < kMmaConsumerWarps) {
+            const int nrows = row_end - row0;
+            for (int idx = threadIdx.x; idx < nrows * (D / 2); idx += kMmaConsumerWarps * 32) {
+                const int r = row0 + idx / (D / 2);
+                const int col = (idx % (D / 2)) * 2;
+                const long long ridx = out_row_index(p, b, kvh, r);
+                store_pair<T>(p, s, ridx, col, 0.f, 0.f);
+                if (col == 0) store_lse(p, s, ridx, kNegInf);
+            }
+        }
+        return;
+    }
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    const uint32_t bar_fk = smem_u32(&bars[0]);
+    const uint32_t bar_fv = smem_u32(&bars[NSTAGE]);
+    const uint32_t bar_em = smem_u32(&bars[2 * NSTAGE]);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < NSTAGE; ++st) {
+            mbar_init(bar_fk + 8 * st, 1);
+            mbar_init(bar_fv + 8 * st, 1);
+            mbar_init(bar_em + 8 * st, kMmaConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kMmaConsumerWarps) {
+        // ================================================================ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+        }
+        const int pps = kMmaTileKeys >> ps_shift;                 // pages per stage (divides 32)
+        const uint32_t box_bytes = (uint32_t)(Geo<D>::NH * ps * 128);
+        const int pg_end = (k_hi + ps - 1) >> ps_shift;          // pages this unit reads
+        const int32_t *bt_row = p.block_table + (long long)b * p.W;
+        int batch = pg0;                                           // page held by lane 0 of id_cur
+        int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
+        int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
+        bool bad = false;
+        int issued = 0;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t % NSTAGE;
+            if (t >= NSTAGE && !bad) {
+                const bool ok = mbar_wait(bar_em + 8 * st, ((t / NSTAGE) - 1) & 1, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+            }
+            const int pg_first = pg0 + t * pps;
+            if (pg_first >= batch + 32) {
+                batch += 32;
+                id_cur = id_next;
+                const int nx = batch + 32 + lane;
+                id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
+            }
+            const int my_pg = pg_first + lane;
+            const int id = __shfl_sync(0xffffffffu, id_cur, (my_pg - batch) & 31);
+            if (bad) break;
+            const int nvalid = min(pps, pg_end - pg_first);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar_fk + 8 * st, (uint32_t)nvalid * box_bytes);
+                mbar_arrive_expect_tx(bar_fv + 8 * st, (uint32_t)nvalid * box_bytes);
+            }
+            __syncwarp();
+            if (lane < nvalid) {
+                int tok;
+                if (id < 0 || (long long)id >= p.num_pages) {
+                    atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
+                    tok = -ps;  // wholly out of the tensor: the box reads as zeros
+                } else {
+                    tok = id << ps_shift;
+                }
+                const uint32_t off = (uint32_t)lane * box_bytes;
+                const uint32_t kdst = sbase + (uint32_t)(st * 2 * kStage) + off;
+                tma_load_4d(kdst, &tmK, bar_fk + 8 * st, 0, tok, 0, kvh);
+                tma_load_4d(kdst + kStage, &tmV, bar_fv + 8 * st, 0, tok, 0, kvh);
+            }
+            issued = t + 1;
+        }
+        // Every copy must have landed before the CTA may exit: wait (bounded) for the
+        // last phase of each stage that was armed.
+        for (int t = max(0, issued - NSTAGE); t < issued; ++t) {
+            const int st = t % NSTAGE;
+            const uint32_t par = (t / NSTAGE) & 1;
+            mbar_wait(bar_fk + 8 * st, par, p.err);
+            mbar_wait(bar_fv + 8 * st, par, p.err);
+        }
+        return;
+    }
+
+    // ==================================================================== consumers
+    const int g = lane >> 2;
+    const int tq = lane & 3;
+    const int rbase = (MODE == MODE_DECODE) ? 0 : row0 + warp * 16;
+    const int ra = rbase + g, rb = rbase + g + 8;
+    const int kw0 = (MODE == MODE_DECODE) ? warp * 16 : 0;  // first key (in the stage) of this warp
+
+    // Q fragments (A operand, row-major 16 x D): rows ra / rb, zero beyond the unit's rows
+    uint32_t qf[D / 16][4];
+    {
+        const T *q = reinterpret_cast<const T *>(p.q);
+        const bool va = ra < p.rows, vb = rb < p.rows;
+        const T *qa = q + (va ? out_row_index(p, b, kvh, ra) * D : 0);
+        const T *qb = q + (vb ? out_row_index(p, b, kvh, rb) * D : 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int c0 = kk * 16 + 2 * tq;
+            qf[kk][0] = va ? __ldg(reinterpret_cast<const uint32_t *>(qa + c0)) : 0u;
+            qf[kk][1] = vb ? __ldg(reinterpret_cast<const uint32_t *>(qb + c0)) : 0u;
+            qf[kk][2] = va ? __ldg(reinterpret_cast<const uint32_t *>(qa + c0 + 8)) : 0u;
+            qf[kk][3] = vb ? __ldg(reinterpret_cast<const uint32_t *>(qb + c0 + 8)) : 0u;
+        }
+    }
+    // exclusive key bounds of the two rows (pad rows see nothing)
+    const int lim_a = ra < p.rows ? min(k_hi_split, row_key_limit(p, b, L, ra / p.G)) : k_lo;
+    const int lim_b = rb < p.rows ? min(k_hi_split, row_key_limit(p, b, L, rb / p.G)) : k_lo;
+
+    float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;
+    float acc[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+    bool bad = false;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % NSTAGE;
+        const uint32_t par = (t / NSTAGE) & 1;
+        const uint32_t kbuf = sbase + (uint32_t)(st * 2 * kStage);
+        const uint32_t vbuf = kbuf + kStage;
+        const int tile_k0 = k_lo + t * kMmaTileKeys;
+        const bool active = tile_k0 + kw0 < k_hi;  // warp-uniform
+
+        if (!bad) {
+            const bool ok = mbar_wait(bar_fk + 8 * st, par, p.err);
+            bad = __any_sync(0xffffffffu, !ok);
+        }
+        uint32_t pp[NT][2];
+        if (!bad && active) {
+            float sc[NT][4];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+            // ---- S = Q K^T over this warp's NKW keys
+            const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                const int key = kw0 + np * 16 + rr + ((mi >> 1) << 3);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(kv_chunk_addr<D>(kbuf, key, 2 * kk + (mi & 1), ps_shift), b0, b1, b2, b3);
+                    Op::run(sc[2 * np], qf[kk], b0, b1);
+                    Op::run(sc[2 * np + 1], qf[kk], b2, b3);
+                }
+            }
+            // ---- mask + scale (log2 domain)
+            float mx_a = kNegInf, mx_b = kNegInf;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int j = tile_k0 + kw0 + n * 8 + 2 * tq;
+                sc[n][0] = (j < lim_a) ? sc[n][0] * p.scale_log2 : kNegInf;
+                sc[n][1] = (j + 1 < lim_a) ? sc[n][1] * p.scale_log2 : kNegInf;
+                sc[n][2] = (j < lim_b) ? sc[n][2] * p.scale_log2 : kNegInf;
+                sc[n][3] = (j + 1 < lim_b) ? sc[n][3] * p.scale_log2 : kNegInf;
+                mx_a = fmaxf(mx_a, fmaxf(sc[n][0], sc[n][1]));
+                mx_b = fmaxf(mx_b, fmaxf(sc[n][2], sc[n][3]));
+            }
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+            const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+            // -inf - (-inf) guard: an all-masked row keeps max -inf and uses 0 as its offset
+            const float mu_a = (mn_a == kNegInf) ? 0.f : mn_a;
+            const float mu_b = (mn_b == kNegInf) ? 0.f : mn_b;
+            const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
+            m_a = mn_a;
+            m_b = mn_b;
+            float rs_a = 0.f, rs_b = 0.f;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                pp[n][0] = Op::pack(exp2f(sc[n][0] - mu_a), exp2f(sc[n][1] - mu_a));
+                pp[n][1] = Op::pack(exp2f(sc[n][2] - mu_b), exp2f(sc[n][3] - mu_b));
+                // the row sum uses the rounded weights that enter P V
+                const float2 fa = Op::unpack(pp[n][0]), fb = Op::unpack(pp[n][1]);
+                rs_a += fa.x + fa.y;
+                rs_b += fb.x + fb.y;
+            }
+            l_a = l_a * al_a + rs_a;
+            l_b = l_b * al_b + rs_b;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                acc[n][0] *= al_a;
+                acc[n][1] *= al_a;
+                acc[n][2] *= al_b;
+                acc[n][3] *= al_b;
+            }
+        }
+
+        if (!bad) {
+            const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
+            bad = __any_sync(0xffffffffu, !ok);
+        }
+        if (tile_k0 + kMmaTileKeys > k_hi) {
+            // Last stage: keys at or past k_hi (past the sequence, or pages never loaded) may
+            // hold any bits.  Their weight is 0, but 0 * NaN is NaN, so zero those V rows.
+            const int kz0 = (MODE == MODE_DECODE) ? kw0 : warp * 16;
+            for (int idx = lane; idx < 16 * kChunks; idx += 32) {
+                const int key = kz0 + idx / kChunks;
+                if (tile_k0 + key >= k_hi) {
+                    const uint32_t a = kv_chunk_addr<D>(vbuf, key, idx % kChunks, ps_shift);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                }
+            }
+            fence_proxy_async_smem();
+            if (MODE == MODE_DECODE)
+                __syncwarp();
+            else
+                named_bar_sync(1, kMmaConsumerWarps * 32);
+        }
+        if (!bad && active) {
+            // ---- O += P V (P from the score fragments, V via transposed ldmatrix)
+            const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+            for (int ks = 0; ks < NKW / 16; ++ks) {
+                const uint32_t a[4] = {pp[2 * ks][0], pp[2 * ks][1], pp[2 * ks + 1][0], pp[2 * ks + 1][1]};
+                const int key = kw0 + ks * 16 + rr + ((mi & 1) << 3);
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) {
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(kv_chunk_addr<D>(vbuf, key, 2 * j + (mi >> 1), ps_shift), b0, b1, b2, b3);
+                    Op::run(acc[2 * j], a, b0, b1);
+                    Op::run(acc[2 * j + 1], a, b2, b3);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_em + 8 * st);
+    }
+
+    // quad sums of the row sums (alpha is uniform across a quad)
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+
+    if (MODE == MODE_PREFILL) {
+        // each warp owns its rows: finalise (0/0 guard) and store
+        const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f;
+        const float inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
+        const bool va = ra < row_end, vb = rb < row_end;
+        const long long ia = va ? out_row_index(p, b, kvh, ra) : 0;
+        const long long ib = vb ? out_row_index(p, b, kvh, rb) : 0;
+        if (!bad) {
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                const int col = n * 8 + 2 * tq;
+                if (va) store_pair<T>(p, s, ia, col, acc[n][0] * inv_a, acc[n][1] * inv_a);
+                if (vb) store_pair<T>(p, s, ib, col, acc[n][2] * inv_b, acc[n][3] * inv_b);
+            }
+            if (tq == 0) {
+                if (va) store_lse(p, s, ia, l_a > 0.f ? m_a * kLn2 + logf(l_a) : kNegInf);
+                if (vb) store_lse(p, s, ib, l_b > 0.f ? m_b * kLn2 + logf(l_b) : kNegInf);
+            }
+        }
+        return;
+    }
+
+    // ---- decode: merge the four warps' (m, l, acc) through shared memory (reuses the ring)
+    constexpr int ACC_STRIDE = D + 4;
+    float *sm = reinterpret_cast<float *>(smem_raw + (sbase - raw));
+    float *s_acc = sm;                                            // [4][16][ACC_STRIDE]
+    float *s_m = sm + kMmaConsumerWarps * 16 * ACC_STRIDE;        // [4][16]
+    float *s_l = s_m + kMmaConsumerWarps * 16;                    // [4][16]
+    named_bar_sync(1, kMmaConsumerWarps * 32);  // every warp is done reading the ring
+    {
+        float *wa = s_acc + (warp * 16) * ACC_STRIDE;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+            const int col = n * 8 + 2 * tq;
+            *reinterpret_cast<float2 *>(wa + g * ACC_STRIDE + col) = make_float2(acc[n][0], acc[n][1]);
+            *reinterpret_cast<float2 *>(wa + (g + 8) * ACC_STRIDE + col) = make_float2(acc[n][2], acc[n][3]);
+        }
+        if (tq == 0) {
+            s_m[warp * 16 + g] = m_a;
+            s_m[warp * 16 + g + 8] = m_b;
+            s_l[warp * 16 + g] = l_a;
+            s_l[warp * 16 + g + 8] = l_b;
+        }
+    }
+    named_bar_sync(1, kMmaConsumerWarps * 32);
+    if (bad) return;
+    {
+        const int tid = threadIdx.x;  // 0..127
+        const int r = tid >> 3;       // 16 rows x 8 column groups
+        const int cg = tid & 7;
+        constexpr int COLS = D / 8;
+        if (r < row_end) {
+            float M = kNegInf;
+#pragma unroll
+            for (int w = 0; w < kMmaConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + r]);
+            float wsc[kMmaConsumerWarps];
+            float Lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kMmaConsumerWarps; ++w) {
+                wsc[w] = (M == kNegInf) ? 0.f : exp2f(s_m[w * 16 + r] - M);
+                Lsum += wsc[w] * s_l[w * 16 + r];
+            }
+            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+            const long long ridx = out_row_index(p, b, kvh, r);
+#pragma unroll
+            for (int c = 0; c < COLS; c += 2) {
+                const int col = cg * COLS + c;
+                float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+                for (int w = 0; w < kMmaConsumerWarps; ++w) {
+                    const float2 v = *reinterpret_cast<const float2 *>(s_acc + (w * 16 + r) * ACC_STRIDE + col);
+                    o0 += wsc[w] * v.x;
+                    o1 += wsc[w] * v.y;
+                }
+                store_pair<T>(p, s, ridx, col, o0 * inv, o1 * inv);
+            }
+            if (cg == 0) store_lse(p, s, ridx, Lsum > 0.f ? M * kLn2 + logf(Lsum) : kNegInf);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------ host side
+int mma_stages(int head_dim) { return head_dim == 128 ? 3 : 4; }
+
+size_t mma_smem_bytes(int head_dim, int stages) {
+    return (size_t)stages * 2 * kMmaTileKeys * head_dim * 2 + 1024;
+}
+
+template <typename T, int D, int MODE, int NSTAGE>
+static cudaError_t launch_mma_t(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                cudaStream_t stream) {
+    auto kern = paged_attn_mma_kernel<T, D, MODE, NSTAGE>;
+    const size_t smem = mma_smem_bytes(D, NSTAGE);
+    static_assert((size_t)kMmaConsumerWarps * 16 * (D + 4) * 4 + 2 * kMmaConsumerWarps * 16 * 4 <=
+                      (size_t)NSTAGE * 2 * kMmaTileKeys * D * 2,
+                  "decode merge scratch must fit in the ring");
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int ps_shift = 0;
+    while ((1 << ps_shift) < p.ps) ++ps_shift;
+    const long long units = (long long)p.B * p.split_kv * p.Hkv * (MODE == MODE_PREFILL ? p.row_tiles : 1);
+    if (units <= 0) return cudaSuccess;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)units, kMmaThreads, smem, stream>>>(tmk, tmv, p, ps_shift);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_mma_dt(const FwdParams &p, int mode, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                 cudaStream_t stream) {
+    if (p.D == 128) {
+        return mode == MODE_DECODE ? launch_mma_t<T, 128, MODE_DECODE, 3>(p, tmk, tmv, stream)
+                                   : launch_mma_t<T, 128, MODE_PREFILL, 3>(p, tmk, tmv, stream);
+    }
+    return mode == MODE_DECODE ? launch_mma_t<T, 64, MODE_DECODE, 4>(p, tmk, tmv, stream)
+                               : launch_mma_t<T, 64, MODE_PREFILL, 4>(p, tmk, tmv, stream);
+}
+
+cudaError_t launch_mma(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                       cudaStream_t stream) {
+    if (dtype == PA_BF16) return launch_mma_dt<__nv_bfloat16>(p, mode, tmk, tmv, stream);
+    return launch_mma_dt<__half>(p, mode, tmk, tmv, stream);
+}
+
+}  // namespace pa

@@ -1,0 +1,34 @@
+// Host-side launchers of the paged-attention kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace pa {
+
+// Tensor-core kernel modes.
+enum { MODE_DECODE = 0, MODE_PREFILL = 1 };
+
+constexpr int kMmaTileKeys = 64;      // keys per pipeline stage
+constexpr int kMmaConsumerWarps = 4;  // warps doing QK / softmax / PV
+constexpr int kMmaThreads = (kMmaConsumerWarps + 1) * 32;
+constexpr int kDecodeRows = 16;       // query rows of one decode CTA (one m16 tile)
+constexpr int kPrefillRows = 64;      // query rows of one prefill CTA (4 warps x 16)
+
+// Pipeline depth and the matching dynamic shared-memory size.
+int mma_stages(int head_dim);
+size_t mma_smem_bytes(int head_dim, int stages);
+
+cudaError_t launch_mma(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                       cudaStream_t stream);
+cudaError_t launch_simt(const FwdParams &p, int dtype, cudaStream_t stream);
+cudaError_t launch_combine(const float *part_out, const float *part_lse, int S, long long rows, int D,
+                           int out_dtype, void *out, float *lse, cudaStream_t stream);
+cudaError_t launch_plan(const int32_t *seq_lens, int B, int ps, int S, int32_t *plan, cudaStream_t stream);
+cudaError_t launch_gather(const void *cache, const int32_t *block_table, const int32_t *seq_lens, int B, int W,
+                          int ps, int Hkv, int D, int esize, long long num_pages, int out_tokens, void *out,
+                          unsigned int *err, cudaStream_t stream);
+
+}  // namespace pa

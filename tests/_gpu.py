@@ -1,0 +1,110 @@
+"""Helpers for the GPU tests: place a workload on the device, run the library, compare with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+from paged_kv_cache_201_gb300 import workloads as W
+
+# Tolerances: bf16/f16 atol=2e-3, rtol=2^-8 (rocm-libraries PR #14349 numeric tests); f32 1e-5.
+TOL = {"bf16": (2e-3, 2.0 ** -8), "f16": (2e-3, 2.0 ** -8), "f32": (1e-5, 1e-5)}
+
+
+class DeviceWorkload:
+    """Device tensors of a workload (K/V drawn on the device when the workload says so)."""
+
+    def __init__(self, wl: W.Workload, device="cuda"):
+        import torch
+        self.wl = wl
+        self.q = W.host_to_torch(wl.q, wl.dtype).to(device)
+        if wl.k_cache is not None:
+            self.k = W.host_to_torch(wl.k_cache, wl.dtype).to(device)
+            self.v = W.host_to_torch(wl.v_cache, wl.dtype).to(device)
+        else:
+            self.k, self.v = W.fill_device_cache(wl, device)
+        self.bt = torch.from_numpy(np.ascontiguousarray(wl.block_table)).to(device)
+        self.sl = torch.from_numpy(np.ascontiguousarray(wl.seq_lens)).to(device)
+        self.qo = None if wl.q_offset is None else torch.from_numpy(np.ascontiguousarray(wl.q_offset)).to(device)
+
+    def host_pools(self):
+        """The device pools as host element arrays (uint16 bits or float32), for the oracle."""
+        return to_host_elems(self.k, self.wl.dtype), to_host_elems(self.v, self.wl.dtype)
+
+
+def to_host_elems(t, dtype):
+    import torch
+    if dtype == "f32":
+        return t.detach().cpu().numpy()
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def to_f64(t, dtype):
+    """Device tensor of the workload dtype (or float32) -> float64 numpy."""
+    import torch
+    if t.dtype == torch.float32:
+        return t.detach().cpu().numpy().astype(np.float64)
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def run(dw: DeviceWorkload, split_kv: int, variant: int = 0):
+    """Forward (+ combine for split_kv > 1).  Returns dict of float64 numpy arrays:
+    out [B,Sq,Hq,D], lse [B,Sq,Hq] and, for split_kv > 1, part_out [S,B,Sq,Hq,D], part_lse [S,B,Sq,Hq]."""
+    import torch
+    import paged_kv_cache_201_gb300 as pa
+    wl = dw.wl
+    B, Sq, Hq, D = wl.B, wl.Sq, wl.Hq, wl.D
+    res = {}
+    if split_kv == 1:
+        out = torch.empty_like(dw.q)
+        lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=dw.q.device)
+        pa.paged_attn_fwd_variant(dw.q, dw.k, dw.v, dw.bt, dw.sl, wl.causal, dw.qo, 1, wl.scale, out, lse, variant)
+    else:
+        po = torch.empty((split_kv, B, Sq, Hq, D), dtype=torch.float32, device=dw.q.device)
+        pl = torch.empty((split_kv, B, Sq, Hq), dtype=torch.float32, device=dw.q.device)
+        pa.paged_attn_fwd_variant(dw.q, dw.k, dw.v, dw.bt, dw.sl, wl.causal, dw.qo, split_kv, wl.scale, po, pl,
+                                  variant)
+        out = torch.empty_like(dw.q)
+        lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=dw.q.device)
+        pa.paged_attn_combine(po, pl, out, lse)
+        res["part_out"] = to_f64(po, "f32")
+        res["part_lse"] = to_f64(pl, "f32")
+    torch.cuda.synchronize()
+    res["out"] = to_f64(out, wl.dtype)
+    res["lse"] = to_f64(lse, "f32")
+    return res
+
+
+def assert_close(got, want, dtype, what):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    assert not np.isnan(got).any(), f"{what}: NaN in GPU result"
+    ninf_w, ninf_g = np.isneginf(want), np.isneginf(got)
+    assert np.array_equal(ninf_w, ninf_g), f"{what}: -inf pattern differs ({ninf_w.sum()} vs {ninf_g.sum()})"
+    fin = ~ninf_w
+    assert np.isfinite(got[fin]).all(), f"{what}: non-finite GPU values"
+    atol, rtol = TOL[dtype]
+    err = np.abs(got[fin] - want[fin])
+    bound = atol + rtol * np.abs(want[fin])
+    bad = err > bound
+    if bad.any():
+        k = int(np.argmax(err - bound))
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements beyond atol={atol} rtol={rtol}; "
+                             f"worst |d|={err[k]:.3g} at want={want[fin][k]:.6g} got={got[fin][k]:.6g}")
+    return float(err.max()) if err.size else 0.0
+
+
+def compare_rows(res, ref, rows_bih, wl, split_kv, what):
+    """Compare GPU results at the sampled rows with oracle row results."""
+    b, i, h = rows_bih[:, 0], rows_bih[:, 1], rows_bih[:, 2]
+    dt = wl.dtype
+    if split_kv == 1:
+        e = assert_close(res["out"][b, i, h], ref["out"], dt, f"{what} out")
+        assert_close(res["lse"][b, i, h], ref["lse"], dt, f"{what} lse")
+    else:
+        e = assert_close(res["out"][b, i, h], ref["comb_out"], dt, f"{what} combined out")
+        assert_close(res["lse"][b, i, h], ref["comb_lse"], dt, f"{what} combined lse")
+        po = np.moveaxis(res["part_out"][:, b, i, h], 0, 1)  # [n, S, D]
+        pl = np.moveaxis(res["part_lse"][:, b, i, h], 0, 1)  # [n, S]
+        assert_close(po, ref["part_out"], dt, f"{what} partial out")
+        assert_close(pl, ref["part_lse"], dt, f"{what} partial lse")
+    return e

@@ -1,0 +1,112 @@
+"""The C-ABI library loads, exports every symbol the header declares, and its host-side
+argument validation returns the documented status codes (CPU only; no kernel is launched)."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+import paged_kv_cache_201_gb300 as pa
+from paged_kv_cache_201_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "paged_attn.h")
+OK, EINVAL, EDTYPE, EUNSUP = 0, -1, -2, -3
+FAKE = 0x10000  # never dereferenced: every call below fails validation (or has no work) first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return pa.load_library()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(paged_attn_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"paged_attn_fwd", "paged_attn_combine", "paged_attn_plan", "paged_attn_debug_gather",
+            "paged_attn_last_error_word", "paged_attn_strerror"} <= set(names)
+    nm = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH], capture_output=True, text=True,
+                        check=True).stdout
+    exported = {line.split()[-1] for line in nm.splitlines() if line.strip()}
+    missing = [n for n in names if n not in exported]
+    assert not missing, f"declared but not exported (C linkage): {missing}"
+    for n in names:
+        assert hasattr(lib, n)
+
+
+def test_strerror_and_version(lib):
+    assert pa.paged_attn_strerror(0) == "ok"
+    assert pa.paged_attn_strerror(-3).startswith("unsupported")
+    assert pa.paged_attn_strerror(12345) == "unknown status"
+    assert pa.paged_attn_version() >= 100
+
+
+def _dims(**kw):
+    base = dict(batch=2, q_len=1, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16, num_pages=64,
+                bt_stride=8, dtype=pa.PA_BF16)
+    base.update(kw)
+    return pa.PaDims(**base)
+
+
+def _fwd(lib, dims, split=1, scale=0.1, lse=FAKE, q=FAKE, out=FAKE, variant=0):
+    return lib.paged_attn_fwd_variant(q, FAKE, FAKE, FAKE, FAKE, 0, None, split, scale, out, lse,
+                                      None if dims is None else ctypes.byref(dims), variant, None)
+
+
+@pytest.mark.parametrize("kw,split,scale,extra,code", [
+    (None, 1, 0.1, {}, EINVAL),
+    (dict(dtype=7), 1, 0.1, {}, EDTYPE),
+    (dict(head_dim=96), 1, 0.1, {}, EUNSUP),
+    (dict(page_size=8), 1, 0.1, {}, EUNSUP),
+    (dict(num_q_heads=6, num_kv_heads=4), 1, 0.1, {}, EINVAL),
+    (dict(num_pages=0), 1, 0.1, {}, EINVAL),
+    (dict(num_pages=1 << 27), 1, 0.1, {}, EUNSUP),
+    ({}, 0, 0.1, {}, EINVAL),
+    ({}, 1, math.nan, {}, EINVAL),
+    ({}, 2, 0.1, dict(lse=None), EINVAL),
+    ({}, 1, 0.1, dict(q=FAKE + 2), EINVAL),
+    ({}, 1, 0.1, dict(q=None), EINVAL),
+    (dict(dtype=pa.PA_F32), 1, 0.1, dict(variant=2), EUNSUP),
+    (dict(q_len=2, num_q_heads=32), 1, 0.1, dict(variant=2), EUNSUP),
+    ({}, 1, 0.1, dict(variant=9), EINVAL),
+    (dict(batch=0), 1, 0.1, {}, OK),
+    (dict(q_len=0), 4, 0.1, dict(lse=None), OK),
+    (dict(q_len=0), 4, 0.1, {}, OK),
+])
+def test_fwd_validation(lib, kw, split, scale, extra, code):
+    dims = None if kw is None else _dims(**kw)
+    assert _fwd(lib, dims, split, scale, **extra) == code
+
+
+def test_combine_plan_gather_validation(lib):
+    f = lib.paged_attn_combine
+    assert f(FAKE, FAKE, 2, 10, 128, 9, FAKE, None, None) == EDTYPE
+    assert f(FAKE, FAKE, 2, 10, 96, 0, FAKE, None, None) == EUNSUP
+    assert f(FAKE, FAKE, 0, 10, 128, 0, FAKE, None, None) == EINVAL
+    assert f(FAKE, FAKE, 2, 0, 128, 0, FAKE, None, None) == OK
+    assert f(FAKE + 4, FAKE, 2, 10, 128, 0, FAKE, None, None) == EINVAL
+    assert f(None, FAKE, 2, 10, 128, 0, FAKE, None, None) == EINVAL
+    p = lib.paged_attn_plan
+    assert p(FAKE, -1, 16, 2, FAKE, None) == EINVAL
+    assert p(FAKE, 4, 0, 2, FAKE, None) == EINVAL
+    assert p(FAKE, 0, 16, 2, FAKE, None) == OK
+    g = lib.paged_attn_debug_gather
+    d = _dims()
+    assert g(FAKE, FAKE, FAKE, ctypes.byref(d), -1, FAKE, None) == EINVAL
+    assert g(FAKE, FAKE, FAKE, ctypes.byref(d), 0, FAKE, None) == OK
+    assert g(FAKE, FAKE, FAKE, ctypes.byref(_dims(head_dim=32)), 4, FAKE, None) == EUNSUP
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """The binding never falls back: without the built library every call raises."""
+    monkeypatch.setattr(pa, "_lib", None)
+    monkeypatch.setattr(pa, "library_path", lambda: str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        pa.load_library()
