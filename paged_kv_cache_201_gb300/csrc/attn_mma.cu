@@ -82,8 +82,9 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
     using Op = MmaOp<T>;
     constexpr int kStage = Geo<D>::kStageBytes;
     constexpr int kChunks = Geo<D>::kChunks;
-    constexpr int NKW = (MODE == MODE_DECODE) ? 16 : 64;  // keys a warp handles per stage
-    constexpr int NT = NKW / 8;                           // score n-tiles per warp per stage
+    constexpr int KB = (MODE == MODE_DECODE) ? 16 : 32;   // keys per softmax block
+    constexpr int SUBS = (MODE == MODE_DECODE) ? 1 : 2;   // blocks a warp handles per stage
+    constexpr int NTB = KB / 8;                           // score n-tiles per block
     constexpr int CTA_ROWS = (MODE == MODE_DECODE) ? kDecodeRows : kPrefillRows;
 
     extern __shared__ uint8_t smem_raw[];
@@ -246,6 +247,9 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
+    // Keys at or past the furthest limit of this warp's rows are masked for all of them.
+    const int warp_lim = __reduce_max_sync(0xffffffffu, (unsigned)max(lim_a, lim_b));
+
     bool bad = false;
     for (int t = 0; t < n_tiles; ++t) {
         const int st = t % NSTAGE;
@@ -253,108 +257,123 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
         const uint32_t kbuf = sbase + (uint32_t)(st * 2 * kStage);
         const uint32_t vbuf = kbuf + kStage;
         const int tile_k0 = k_lo + t * kMmaTileKeys;
-        const bool active = tile_k0 + kw0 < k_hi;  // warp-uniform
 
         if (!bad) {
             const bool ok = mbar_wait(bar_fk + 8 * st, par, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
-        uint32_t pp[NT][2];
-        if (!bad && active) {
-            float sc[NT][4];
 #pragma unroll
-            for (int n = 0; n < NT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-            // ---- S = Q K^T over this warp's NKW keys
-            const int mi = lane >> 3, rr = lane & 7;
+        for (int sb = 0; sb < SUBS; ++sb) {
+            const int kb0 = kw0 + sb * KB;                              // first key (in the stage) of the block
+            const bool active = tile_k0 + kb0 < min(k_hi, warp_lim);    // warp-uniform
+            // P split into a bf16/f16 high part and the rounding remainder: P V = Ph V + Pl V keeps
+            // the weights to ~2^-17 relative instead of the 2^-9 of a single 16-bit P.
+            uint32_t ph[NTB][2], pl[NTB][2];
+            if (!bad && active) {
+                float sc[NTB][4];
 #pragma unroll
-            for (int np = 0; np < NT / 2; ++np) {
-                const int key = kw0 + np * 16 + rr + ((mi >> 1) << 3);
+                for (int n = 0; n < NTB; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+                // ---- S = Q K^T over the block's KB keys
+                const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(kv_chunk_addr<D>(kbuf, key, 2 * kk + (mi & 1), ps_shift), b0, b1, b2, b3);
-                    Op::run(sc[2 * np], qf[kk], b0, b1);
-                    Op::run(sc[2 * np + 1], qf[kk], b2, b3);
+                for (int np = 0; np < NTB / 2; ++np) {
+                    const int key = kb0 + np * 16 + rr + ((mi >> 1) << 3);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4(kv_chunk_addr<D>(kbuf, key, 2 * kk + (mi & 1), ps_shift), b0, b1, b2, b3);
+                        Op::run(sc[2 * np], qf[kk], b0, b1);
+                        Op::run(sc[2 * np + 1], qf[kk], b2, b3);
+                    }
+                }
+                // ---- mask + scale (log2 domain)
+                float mx_a = kNegInf, mx_b = kNegInf;
+#pragma unroll
+                for (int n = 0; n < NTB; ++n) {
+                    const int j = tile_k0 + kb0 + n * 8 + 2 * tq;
+                    sc[n][0] = (j < lim_a) ? sc[n][0] * p.scale_log2 : kNegInf;
+                    sc[n][1] = (j + 1 < lim_a) ? sc[n][1] * p.scale_log2 : kNegInf;
+                    sc[n][2] = (j < lim_b) ? sc[n][2] * p.scale_log2 : kNegInf;
+                    sc[n][3] = (j + 1 < lim_b) ? sc[n][3] * p.scale_log2 : kNegInf;
+                    mx_a = fmaxf(mx_a, fmaxf(sc[n][0], sc[n][1]));
+                    mx_b = fmaxf(mx_b, fmaxf(sc[n][2], sc[n][3]));
+                }
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+                const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+                // -inf - (-inf) guard: an all-masked row keeps max -inf and uses 0 as its offset
+                const float mu_a = (mn_a == kNegInf) ? 0.f : mn_a;
+                const float mu_b = (mn_b == kNegInf) ? 0.f : mn_b;
+                const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
+                m_a = mn_a;
+                m_b = mn_b;
+                float rs_a = 0.f, rs_b = 0.f;
+#pragma unroll
+                for (int n = 0; n < NTB; ++n) {
+                    const float p0 = exp2f(sc[n][0] - mu_a), p1 = exp2f(sc[n][1] - mu_a);
+                    const float p2 = exp2f(sc[n][2] - mu_b), p3 = exp2f(sc[n][3] - mu_b);
+                    ph[n][0] = Op::pack(p0, p1);
+                    ph[n][1] = Op::pack(p2, p3);
+                    const float2 ha = Op::unpack(ph[n][0]), hb = Op::unpack(ph[n][1]);
+                    pl[n][0] = Op::pack(p0 - ha.x, p1 - ha.y);
+                    pl[n][1] = Op::pack(p2 - hb.x, p3 - hb.y);
+                    rs_a += p0 + p1;
+                    rs_b += p2 + p3;
+                }
+                l_a = l_a * al_a + rs_a;
+                l_b = l_b * al_b + rs_b;
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    acc[n][0] *= al_a;
+                    acc[n][1] *= al_a;
+                    acc[n][2] *= al_b;
+                    acc[n][3] *= al_b;
                 }
             }
-            // ---- mask + scale (log2 domain)
-            float mx_a = kNegInf, mx_b = kNegInf;
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const int j = tile_k0 + kw0 + n * 8 + 2 * tq;
-                sc[n][0] = (j < lim_a) ? sc[n][0] * p.scale_log2 : kNegInf;
-                sc[n][1] = (j + 1 < lim_a) ? sc[n][1] * p.scale_log2 : kNegInf;
-                sc[n][2] = (j < lim_b) ? sc[n][2] * p.scale_log2 : kNegInf;
-                sc[n][3] = (j + 1 < lim_b) ? sc[n][3] * p.scale_log2 : kNegInf;
-                mx_a = fmaxf(mx_a, fmaxf(sc[n][0], sc[n][1]));
-                mx_b = fmaxf(mx_b, fmaxf(sc[n][2], sc[n][3]));
-            }
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-            const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-            // -inf - (-inf) guard: an all-masked row keeps max -inf and uses 0 as its offset
-            const float mu_a = (mn_a == kNegInf) ? 0.f : mn_a;
-            const float mu_b = (mn_b == kNegInf) ? 0.f : mn_b;
-            const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
-            m_a = mn_a;
-            m_b = mn_b;
-            float rs_a = 0.f, rs_b = 0.f;
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                pp[n][0] = Op::pack(exp2f(sc[n][0] - mu_a), exp2f(sc[n][1] - mu_a));
-                pp[n][1] = Op::pack(exp2f(sc[n][2] - mu_b), exp2f(sc[n][3] - mu_b));
-                // the row sum uses the rounded weights that enter P V
-                const float2 fa = Op::unpack(pp[n][0]), fb = Op::unpack(pp[n][1]);
-                rs_a += fa.x + fa.y;
-                rs_b += fb.x + fb.y;
-            }
-            l_a = l_a * al_a + rs_a;
-            l_b = l_b * al_b + rs_b;
-#pragma unroll
-            for (int n = 0; n < D / 8; ++n) {
-                acc[n][0] *= al_a;
-                acc[n][1] *= al_a;
-                acc[n][2] *= al_b;
-                acc[n][3] *= al_b;
-            }
-        }
 
-        if (!bad) {
-            const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
-            bad = __any_sync(0xffffffffu, !ok);
-        }
-        if (tile_k0 + kMmaTileKeys > k_hi) {
-            // Last stage: keys at or past k_hi (past the sequence, or pages never loaded) may
-            // hold any bits.  Their weight is 0, but 0 * NaN is NaN, so zero those V rows.
-            const int kz0 = (MODE == MODE_DECODE) ? kw0 : warp * 16;
-            for (int idx = lane; idx < 16 * kChunks; idx += 32) {
-                const int key = kz0 + idx / kChunks;
-                if (tile_k0 + key >= k_hi) {
-                    const uint32_t a = kv_chunk_addr<D>(vbuf, key, idx % kChunks, ps_shift);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+            if (sb == 0) {
+                if (!bad) {
+                    const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
+                    bad = __any_sync(0xffffffffu, !ok);
+                }
+                if (tile_k0 + kMmaTileKeys > k_hi) {
+                    // Last stage: keys at or past k_hi (past the sequence, or pages never loaded)
+                    // may hold any bits.  Their weight is 0, but 0 * NaN is NaN, so zero those V rows.
+                    const int kz0 = (MODE == MODE_DECODE) ? kw0 : warp * 16;
+                    for (int idx = lane; idx < 16 * kChunks; idx += 32) {
+                        const int key = kz0 + idx / kChunks;
+                        if (tile_k0 + key >= k_hi) {
+                            const uint32_t a = kv_chunk_addr<D>(vbuf, key, idx % kChunks, ps_shift);
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    if (MODE == MODE_DECODE)
+                        __syncwarp();
+                    else
+                        named_bar_sync(1, kMmaConsumerWarps * 32);
                 }
             }
-            fence_proxy_async_smem();
-            if (MODE == MODE_DECODE)
-                __syncwarp();
-            else
-                named_bar_sync(1, kMmaConsumerWarps * 32);
-        }
-        if (!bad && active) {
-            // ---- O += P V (P from the score fragments, V via transposed ldmatrix)
-            const int mi = lane >> 3, rr = lane & 7;
+            if (!bad && active) {
+                // ---- O += (Ph + Pl) V  (P from the score fragments, V via transposed ldmatrix)
+                const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
-            for (int ks = 0; ks < NKW / 16; ++ks) {
-                const uint32_t a[4] = {pp[2 * ks][0], pp[2 * ks][1], pp[2 * ks + 1][0], pp[2 * ks + 1][1]};
-                const int key = kw0 + ks * 16 + rr + ((mi & 1) << 3);
+                for (int ks = 0; ks < KB / 16; ++ks) {
+                    const uint32_t ah[4] = {ph[2 * ks][0], ph[2 * ks][1], ph[2 * ks + 1][0], ph[2 * ks + 1][1]};
+                    const uint32_t al[4] = {pl[2 * ks][0], pl[2 * ks][1], pl[2 * ks + 1][0], pl[2 * ks + 1][1]};
+                    const int key = kb0 + ks * 16 + rr + ((mi & 1) << 3);
 #pragma unroll
-                for (int j = 0; j < D / 16; ++j) {
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4_trans(kv_chunk_addr<D>(vbuf, key, 2 * j + (mi >> 1), ps_shift), b0, b1, b2, b3);
-                    Op::run(acc[2 * j], a, b0, b1);
-                    Op::run(acc[2 * j + 1], a, b2, b3);
+                    for (int j = 0; j < D / 16; ++j) {
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4_trans(kv_chunk_addr<D>(vbuf, key, 2 * j + (mi >> 1), ps_shift), b0, b1, b2,
+                                          b3);
+                        Op::run(acc[2 * j], ah, b0, b1);
+                        Op::run(acc[2 * j + 1], ah, b2, b3);
+                        Op::run(acc[2 * j], al, b0, b1);
+                        Op::run(acc[2 * j + 1], al, b2, b3);
+                    }
                 }
             }
         }
