@@ -164,6 +164,20 @@ def algorithmic_bytes(wl, split_kv: int) -> dict:
     return {"kv": kv, "q": q, "out": out, "ids": ids, "total": kv + q + out + ids}
 
 
+def causal_flops(wl) -> float:
+    """Useful flops of a step: 4*D per (query row, valid key) pair (QK^T and PV), masked work excluded."""
+    L = wl.seq_lens.astype(np.int64)
+    pairs = 0
+    for b in range(wl.B):
+        if wl.causal:
+            qoff = int(L[b]) - wl.Sq if wl.q_offset is None else int(wl.q_offset[b])
+            reach = np.clip(qoff + np.arange(wl.Sq) + 1, 0, int(L[b]))
+            pairs += int(reach.sum())
+        else:
+            pairs += int(L[b]) * wl.Sq
+    return 4.0 * wl.D * pairs * wl.Hq
+
+
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_201_gb300", "csrc")
@@ -288,7 +302,7 @@ def run_ours(args, ws, rank, local):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured"
     else:
         peak, peak_src = FALLBACK_HBM_GBS, "fallback"
-    kname = "paged_attn_mma_kernel" if args.variant != 1 else "paged_attn_simt_kernel"
+    kname = {1: "paged_attn_simt_kernel", 4: "paged_attn_tc05_kernel"}.get(args.variant, "paged_attn_mma_kernel")
     fwd_bytes = ab["total"]
     achieved = fwd_bytes / (fwd_ms * 1e-3) / 1e9
 
@@ -368,6 +382,8 @@ def run_ours(args, ws, rank, local):
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "kernel_ms": round(fwd_ms, 5), "traffic": recorded_traffic(kname, args.workload)},
+        "tflops": round(causal_flops(wl) * ws / (ms_step * 1e-3) / 1e12, 2),
+        "kernel_tflops": round(causal_flops(wl) / (fwd_ms * 1e-3) / 1e12, 2),
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": K * (2 if S > 1 else 1),

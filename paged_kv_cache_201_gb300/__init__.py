@@ -18,11 +18,11 @@ __all__ = [
     "PagedAttnError", "load_library", "library_path", "paged_attn_fwd", "paged_attn_fwd_variant",
     "paged_attn_combine", "paged_attn_plan", "paged_attn_debug_gather", "paged_attn_last_error_word",
     "paged_attn_strerror", "paged_attn_version", "attention", "PA_F32", "PA_F16", "PA_BF16",
-    "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL",
+    "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL", "VARIANT_TC05_PREFILL",
 ]
 
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
-VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA_DECODE, VARIANT_MMA_PREFILL = 0, 1, 2, 3
+VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA_DECODE, VARIANT_MMA_PREFILL, VARIANT_TC05_PREFILL = 0, 1, 2, 3, 4
 ERRBIT_PAGE_RANGE, ERRBIT_TIMEOUT, ERRBIT_SEQ_CLIPPED = 1, 2, 4
 
 

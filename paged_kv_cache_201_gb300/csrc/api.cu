@@ -68,23 +68,50 @@ int check_dims(const pa_dims *d) {
     return PA_OK;
 }
 
-// 4-D view of one pool for TMA: (d within a 64-element half, token, half, kv head),
-// box = (64, page_size, D/64, 1): one page of one kv head per copy.
-int make_pool_map(CUtensorMap *m, const void *base, const pa_dims *d) {
+CUtensorMapDataType tma_dtype(int dtype) {
+    return dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// 4-D view of one pool for TMA: (d within a 64-element half, token, half, kv head).
+// halves_per_box = D/64 copies a page's whole rows (decode kernel); 1 copies one half-row
+// (tcgen05 kernel, which keeps each half of a tile contiguous).
+int make_pool_map(CUtensorMap *m, const void *base, const pa_dims *d, int halves_per_box) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PA_ECUDA;
     const cuuint64_t esz = 2;
     const cuuint64_t D = (cuuint64_t)d->head_dim, Hkv = (cuuint64_t)d->num_kv_heads;
     const cuuint64_t dims[4] = {64, (cuuint64_t)d->num_pages * (cuuint64_t)d->page_size, D / 64, Hkv};
     const cuuint64_t strides[3] = {Hkv * D * esz, 64 * esz, D * esz};
-    const cuuint32_t box[4] = {64, (cuuint32_t)d->page_size, (cuuint32_t)(D / 64), 1};
+    const cuuint32_t box[4] = {64, (cuuint32_t)d->page_size, (cuuint32_t)halves_per_box, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUtensorMapDataType dt =
-        d->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUresult r = enc(m, dt, 4, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = enc(m, tma_dtype(d->dtype), 4, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
+}
+
+// 4-D view of q for the tcgen05 kernel: (d within a half, half, query head, token of B*Sq);
+// one box = one half of a 128-row tile: 128/G consecutive tokens x the G heads of a kv head.
+int make_q_map(CUtensorMap *m, const void *q, const pa_dims *d) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PA_ECUDA;
+    const cuuint64_t esz = 2;
+    const cuuint64_t D = (cuuint64_t)d->head_dim, Hq = (cuuint64_t)d->num_q_heads;
+    const int G = d->num_q_heads / d->num_kv_heads;
+    const cuuint64_t dims[4] = {64, D / 64, Hq, (cuuint64_t)d->batch * (cuuint64_t)d->q_len};
+    const cuuint64_t strides[3] = {64 * esz, D * esz, Hq * D * esz};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)G, (cuuint32_t)(128 / G)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, tma_dtype(d->dtype), 4, const_cast<void *>(q), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
+}
+
+bool tc05_supports(const pa_dims *d) {
+    const int G = d->num_q_heads / d->num_kv_heads;
+    return d->dtype != PA_F32 && d->head_dim == 128 && G <= 128 && (128 % G) == 0 &&
+           (int64_t)d->batch * d->q_len < ((int64_t)1 << 31);
 }
 
 int choose_variant(const pa_dims *d) {
@@ -126,6 +153,9 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
         case PA_VARIANT_MMA_PREFILL:
             if (dims->dtype == PA_F32) return PA_EUNSUPPORTED;
             break;
+        case PA_VARIANT_TC05_PREFILL:
+            if (!tc05_supports(dims)) return PA_EUNSUPPORTED;
+            break;
         default:
             return PA_EINVAL;
     }
@@ -164,10 +194,16 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
     cudaError_t e;
     if (variant == PA_VARIANT_SIMT) {
         e = pa::launch_simt(p, dims->dtype, st);
+    } else if (variant == PA_VARIANT_TC05_PREFILL) {
+        CUtensorMap tmq, tmk, tmv;
+        if ((rc = make_q_map(&tmq, q, dims)) != PA_OK) return rc;
+        if ((rc = make_pool_map(&tmk, k_cache, dims, 1)) != PA_OK) return rc;
+        if ((rc = make_pool_map(&tmv, v_cache, dims, 1)) != PA_OK) return rc;
+        e = pa::launch_tc05(p, dims->dtype, tmq, tmk, tmv, st);
     } else {
         CUtensorMap tmk, tmv;
-        if ((rc = make_pool_map(&tmk, k_cache, dims)) != PA_OK) return rc;
-        if ((rc = make_pool_map(&tmv, v_cache, dims)) != PA_OK) return rc;
+        if ((rc = make_pool_map(&tmk, k_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
+        if ((rc = make_pool_map(&tmv, v_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
         const int mode = variant == PA_VARIANT_MMA_DECODE ? pa::MODE_DECODE : pa::MODE_PREFILL;
         if (mode == pa::MODE_PREFILL) p.row_tiles = (rows + pa::kPrefillRows - 1) / pa::kPrefillRows;
         e = pa::launch_mma(p, mode, dims->dtype, tmk, tmv, st);

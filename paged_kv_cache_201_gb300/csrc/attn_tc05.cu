@@ -1,0 +1,402 @@
+// Paged attention on the 5th-generation tensor cores (tcgen05 + tensor memory), sm_103a.
+//
+// For query runs long enough to fill a 128-row tile (prefill, head_dim 128, bf16/f16).
+// One CTA = (sequence b, kv head, split s, tile of 128/G query tokens x the G query
+// heads of the kv head's group), so all 128 rows share every K/V tile:
+//   warp 0      TMA producer: the Q tile once; then, per 128-key tile, the block-table
+//               ids (32 pages per batch, never past the sequence's page count) and one
+//               2-D box per page, half-row and pool into a 2-stage ring.
+//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma from one thread:
+//               S_t = Q K_t^T into one of two S buffers (128 fp32 columns each), then
+//               O += Ph_{t-1} V_{t-1} + Pl_{t-1} V_{t-1} with P read from TMEM.
+//   warps 2-5   softmax, one TMEM lane (query row) per thread: mask (sequence length,
+//               split end, causal reach with q_offset), running max in the log2 domain,
+//               P = exp2(s - m) written back over S as a 16-bit high part and its
+//               rounding remainder.  O is rescaled in TMEM only when the running max
+//               grows by more than 2^8 (otherwise the stale max is kept), and the
+//               -inf - (-inf) and 0/0 guards of rocMLIR PR #2371 apply.
+#include <type_traits>
+
+#include "kernels.h"
+#include "tc05.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kT5Threads = 192;               // 6 warps
+constexpr int kT5Half = 128 * 128;            // bytes of one 64-column half of a 128-row tile
+constexpr int kT5Tile = 2 * kT5Half;          // a 128 x 128 bf16 tile (Q, K or V)
+constexpr int kT5Stages = 2;
+constexpr uint32_t kT5TmemCols = 512;
+constexpr uint32_t kColO = 256;
+constexpr float kRescaleLog2 = 8.f;           // rescale O only when the max grows by > 2^8
+
+// barrier slots
+enum { B_Q = 0, B_KF = 1, B_VF = 3, B_KVE = 5, B_SF = 7, B_PF = 9, B_OD = 11, B_COUNT = 12 };
+
+__device__ __forceinline__ long long t5_row_index(const FwdParams &p, int b, int kvh, int tok, int g) {
+    return ((long long)b * p.Sq + tok) * p.Hq + (long long)kvh * p.G + g;
+}
+
+template <typename T>
+__device__ __forceinline__ void t5_store_row(const FwdParams &p, int s, long long ridx, const float *v, float lse) {
+    if (p.split_kv == 1) {
+        T *o = reinterpret_cast<T *>(p.out) + ridx * 128;
+#pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+            uint4 w;
+            w.x = MmaOp<T>::pack(v[c + 0], v[c + 1]);
+            w.y = MmaOp<T>::pack(v[c + 2], v[c + 3]);
+            w.z = MmaOp<T>::pack(v[c + 4], v[c + 5]);
+            w.w = MmaOp<T>::pack(v[c + 6], v[c + 7]);
+            *reinterpret_cast<uint4 *>(o + c) = w;
+        }
+        if (p.lse) p.lse[ridx] = lse;
+    } else {
+        const long long rows_total = (long long)p.B * p.Sq * p.Hq;
+        float *o = reinterpret_cast<float *>(p.out) + ((long long)s * rows_total + ridx) * 128;
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) *reinterpret_cast<float4 *>(o + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+        p.lse[(long long)s * rows_total + ridx] = lse;
+    }
+}
+
+}  // namespace
+
+template <typename T>
+__global__ void __launch_bounds__(kT5Threads, 1)
+    paged_attn_tc05_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const FwdParams p, int tpt, int ps_shift,
+                           uint32_t idesc_qk, uint32_t idesc_pv) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[B_COUNT];
+    __shared__ uint32_t s_tmem;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ps = 1 << ps_shift;
+
+    int unit = blockIdx.x;
+    const int rt = unit % p.row_tiles;
+    unit /= p.row_tiles;
+    const int kvh = unit % p.Hkv;
+    unit /= p.Hkv;
+    const int s = unit % p.split_kv;
+    const int b = unit / p.split_kv;
+
+    int L = max(p.seq_lens[b], 0);
+    if (L > p.W * ps) {
+        if (threadIdx.x == 0) atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
+        L = p.W * ps;
+    }
+    int pg0, pg1;
+    split_pages(L, ps, p.split_kv, s, pg0, pg1);
+    const int k_lo = pg0 * ps;
+    const int k_hi_split = min(pg1 * ps, L);
+    const int tok0 = rt * tpt;
+    const int tok_end = min(tok0 + tpt, p.Sq);
+    const int k_hi = min(k_hi_split, row_key_limit(p, b, L, tok_end - 1));
+    const int n_tiles = k_hi > k_lo ? (k_hi - k_lo + 127) / 128 : 0;
+
+    if (n_tiles == 0) {  // every row of the unit is empty here: output 0, lse -inf
+        const int nrows = (tok_end - tok0) * p.G;
+        float zeros[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) zeros[c] = 0.f;
+        for (int r = threadIdx.x; r < nrows; r += kT5Threads)
+            t5_store_row<T>(p, s, t5_row_index(p, b, kvh, tok0 + r / p.G, r % p.G), zeros, kNegInf);
+        return;
+    }
+
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sQ = sbase;
+    auto sK = [&](int st) { return sbase + (uint32_t)kT5Tile + (uint32_t)(st * 2 * kT5Tile); };
+    auto sV = [&](int st) { return sbase + (uint32_t)(2 * kT5Tile) + (uint32_t)(st * 2 * kT5Tile); };
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B_Q), 1);
+        for (int st = 0; st < kT5Stages; ++st) {
+            mbar_init(bar(B_KF + st), 1);
+            mbar_init(bar(B_VF + st), 1);
+            mbar_init(bar(B_KVE + st), 1);
+            mbar_init(bar(B_SF + st), 1);
+            mbar_init(bar(B_PF + st), 128);
+        }
+        mbar_init(bar(B_OD), 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc05::tmem_alloc(smem_u32(&s_tmem), kT5TmemCols);
+        tc05::tmem_relinquish();
+    }
+    tc05::fence_before_sync();
+    __syncthreads();
+    tc05::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 0) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(bar(B_Q), (uint32_t)kT5Tile);
+            const int qtok = b * p.Sq + tok0;
+            tma_load_4d(sQ, &tmQ, bar(B_Q), 0, 0, kvh * p.G, qtok);
+            tma_load_4d(sQ + kT5Half, &tmQ, bar(B_Q), 0, 1, kvh * p.G, qtok);
+        }
+        const int ppt = 128 >> ps_shift;                     // pages per tile (divides 32)
+        const uint32_t box = (uint32_t)ps * 128u;            // bytes of one page half-row box
+        const int pg_end = (k_hi + ps - 1) >> ps_shift;
+        const int32_t *bt_row = p.block_table + (long long)b * p.W;
+        int batch = pg0;
+        int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
+        int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
+        bool bad = false;
+        int issued = 0;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t & 1;
+            if (t >= kT5Stages && !bad) {
+                const bool ok = mbar_wait(bar(B_KVE + st), ((t >> 1) - 1) & 1, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+            }
+            const int pg_first = pg0 + t * ppt;
+            if (pg_first >= batch + 32) {
+                batch += 32;
+                id_cur = id_next;
+                const int nx = batch + 32 + lane;
+                id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
+            }
+            const int id = __shfl_sync(0xffffffffu, id_cur, (pg_first + lane - batch) & 31);
+            if (bad) break;
+            const int nvalid = min(ppt, pg_end - pg_first);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(B_KF + st), (uint32_t)nvalid * 2u * box);
+                mbar_arrive_expect_tx(bar(B_VF + st), (uint32_t)nvalid * 2u * box);
+            }
+            __syncwarp();
+            if (lane < nvalid) {
+                int tok;
+                if (id < 0 || (long long)id >= p.num_pages) {
+                    atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
+                    tok = -ps;  // wholly outside the tensor: reads as zeros
+                } else {
+                    tok = id << ps_shift;
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t off = (uint32_t)h * kT5Half + (uint32_t)lane * box;
+                    tma_load_4d(sK(st) + off, &tmK, bar(B_KF + st), 0, tok, h, kvh);
+                    tma_load_4d(sV(st) + off, &tmV, bar(B_VF + st), 0, tok, h, kvh);
+                }
+            }
+            issued = t + 1;
+        }
+        for (int t = max(0, issued - kT5Stages); t < issued; ++t) {  // no copy may outlive the CTA
+            mbar_wait(bar(B_KF + (t & 1)), (t >> 1) & 1, p.err);
+            mbar_wait(bar(B_VF + (t & 1)), (t >> 1) & 1, p.err);
+        }
+        if (lane == 0) mbar_wait(bar(B_Q), 0, p.err);
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            bool bad = !mbar_wait(bar(B_Q), 0, p.err);
+            for (int t = 0; t <= n_tiles && !bad; ++t) {
+                if (t < n_tiles) {
+                    const int st = t & 1;
+                    if (!mbar_wait(bar(B_KF + st), (t >> 1) & 1, p.err)) { bad = true; break; }
+                    tc05::fence_after_sync();
+                    const uint32_t d = tmem + (st ? 128u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (uint32_t)(kk >> 2) * kT5Half + (uint32_t)(kk & 3) * 32u;
+                        tc05::mma_ss(d, tc05::smem_desc_sw128(sQ + off, 16, 1024),
+                                     tc05::smem_desc_sw128(sK(st) + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                    tc05::commit(bar(B_SF + st));
+                }
+                if (t >= 1) {
+                    const int u = t - 1, su = u & 1;
+                    if (!mbar_wait(bar(B_PF + su), (u >> 1) & 1, p.err)) { bad = true; break; }
+                    if (!mbar_wait(bar(B_VF + su), (u >> 1) & 1, p.err)) { bad = true; break; }
+                    tc05::fence_after_sync();
+                    const uint32_t pcol = tmem + (su ? 128u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t vd = tc05::smem_desc_sw128(sV(su) + (uint32_t)kk * 2048u, (uint32_t)kT5Half, 1024);
+                        tc05::mma_ts(tmem + kColO, pcol + (uint32_t)kk * 8u, vd, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
+                        tc05::mma_ts(tmem + kColO, pcol + 64u + (uint32_t)kk * 8u, vd, idesc_pv, 1u);
+                    }
+                    tc05::commit(bar(B_KVE + su));
+                    tc05::commit(bar(B_OD));
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================================================================ softmax (warps 2-5)
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane;                       // TMEM lane = query row of the tile
+        const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+        const int tk = tok0 + r / p.G;
+        const int g = r % p.G;
+        const bool row_valid = tk < tok_end;
+        const int lim = row_valid ? min(k_hi_split, row_key_limit(p, b, L, tk)) : k_lo;
+        float m_used = kNegInf, l = 0.f;
+        bool bad = false;
+        for (int t = 0; t < n_tiles && !bad; ++t) {
+            const int st = t & 1;
+            {
+                const bool ok = mbar_wait(bar(B_SF + st), (t >> 1) & 1, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+                if (bad) break;
+            }
+            tc05::fence_after_sync();
+            const uint32_t sbuf = tmem + lane_addr + (st ? 128u : 0u);
+            uint32_t u0[32], u1[32], u2[32], u3[32];
+            tc05::ld_32cols(sbuf + 0, u0);
+            tc05::ld_32cols(sbuf + 32, u1);
+            tc05::ld_32cols(sbuf + 64, u2);
+            tc05::ld_32cols(sbuf + 96, u3);
+            tc05::wait_ld();
+            float sc[128];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                sc[j] = __uint_as_float(u0[j]);
+                sc[32 + j] = __uint_as_float(u1[j]);
+                sc[64 + j] = __uint_as_float(u2[j]);
+                sc[96 + j] = __uint_as_float(u3[j]);
+            }
+            const int tile_k0 = k_lo + t * 128;
+            const int nvalid_row = lim - tile_k0;             // keys [0, nvalid_row) of the tile are valid here
+            float mx = kNegInf;
+#pragma unroll
+            for (int j = 0; j < 128; ++j) {
+                sc[j] = (j < nvalid_row) ? sc[j] * p.scale_log2 : kNegInf;
+                mx = fmaxf(mx, sc[j]);
+            }
+            const float m_new = fmaxf(m_used, mx);
+            const bool need = m_new > m_used + kRescaleLog2;  // also true when m_used is -inf and m_new is not
+            if (__any_sync(0xffffffffu, need)) {
+                const float alpha = need ? exp2f(m_used - m_new) : 1.f;
+                if (need) {
+                    l *= alpha;
+                    m_used = m_new;
+                }
+                if (t > 0) {
+                    // O holds P V of earlier tiles: wait for the last one, then rescale this row
+                    const bool ok = mbar_wait(bar(B_OD), (t - 1) & 1, p.err);
+                    bad = __any_sync(0xffffffffu, !ok);
+                    if (bad) break;
+                    tc05::fence_after_sync();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tc05::ld_32cols(tmem + lane_addr + kColO + 32u * c, o);
+                        tc05::wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        tc05::st_32cols(tmem + lane_addr + kColO + 32u * c, o);
+                    }
+                }
+            }
+            const float mu = (m_used == kNegInf) ? 0.f : m_used;  // -inf - (-inf) guard
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = exp2f(sc[32 * c + 2 * i] - mu);
+                    const float p1 = exp2f(sc[32 * c + 2 * i + 1] - mu);
+                    l += p0 + p1;
+                    hi[i] = MmaOp<T>::pack(p0, p1);
+                    const float2 h2 = MmaOp<T>::unpack(hi[i]);
+                    lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+                }
+                tc05::st_16cols(sbuf + 16u * c, hi);
+                tc05::st_16cols(sbuf + 64u + 16u * c, lo);
+            }
+            tc05::wait_st();
+            if (t == n_tiles - 1 && tile_k0 + 128 > k_hi) {
+                // Keys at or past k_hi (past the sequence or never loaded) may hold any bits:
+                // their weight is 0 but 0 * NaN is NaN, so zero those V rows before P V.
+                const bool ok = mbar_wait(bar(B_VF + st), (t >> 1) & 1, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+                if (!bad && tile_k0 + r >= k_hi) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t a = sV(st) + (uint32_t)h * kT5Half + (uint32_t)r * 128u;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a + 16u * c), "r"(0u)
+                                         : "memory");
+                    }
+                }
+                fence_proxy_async_smem();
+            }
+            tc05::fence_before_sync();
+            mbar_arrive(bar(B_PF + st));
+        }
+        if (!bad) {
+            const bool ok = mbar_wait(bar(B_OD), (n_tiles - 1) & 1, p.err);
+            bad = __any_sync(0xffffffffu, !ok);
+        }
+        if (!bad) {
+            tc05::fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float o[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t u[32];
+                tc05::ld_32cols(tmem + lane_addr + kColO + 32u * c, u);
+                tc05::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(u[j]) * inv;
+            }
+            if (row_valid)
+                t5_store_row<T>(p, s, t5_row_index(p, b, kvh, tk, g), o,
+                                l > 0.f ? m_used * kLn2 + logf(l) : kNegInf);
+        }
+    }
+
+    tc05::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc05::fence_after_sync();
+        tc05::tmem_dealloc(tmem, kT5TmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------ host side
+size_t tc05_smem_bytes() { return (size_t)(kT5Tile + kT5Stages * 2 * kT5Tile + 1024); }
+
+template <typename T>
+static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, const CUtensorMap &tmk,
+                                 const CUtensorMap &tmv, cudaStream_t stream) {
+    auto kern = paged_attn_tc05_kernel<T>;
+    const size_t smem = tc05_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int ps_shift = 0;
+    while ((1 << ps_shift) < p.ps) ++ps_shift;
+    const int tpt = 128 / p.G;
+    FwdParams q = p;
+    q.row_tiles = (p.Sq + tpt - 1) / tpt;
+    const long long units = (long long)p.B * p.split_kv * p.Hkv * q.row_tiles;
+    if (units <= 0) return cudaSuccess;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const bool bf = std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t iqk = tc05::idesc_f16(bf, false, 128, 128);
+    const uint32_t ipv = tc05::idesc_f16(bf, true, 128, 128);
+    kern<<<(unsigned)units, kT5Threads, smem, stream>>>(tmq, tmk, tmv, q, tpt, ps_shift, iqk, ipv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc05(const FwdParams &p, int dtype, const CUtensorMap &tmq, const CUtensorMap &tmk,
+                        const CUtensorMap &tmv, cudaStream_t stream) {
+    if (dtype == PA_BF16) return launch_tc05_t<__nv_bfloat16>(p, tmq, tmk, tmv, stream);
+    return launch_tc05_t<__half>(p, tmq, tmk, tmv, stream);
+}
+
+}  // namespace pa

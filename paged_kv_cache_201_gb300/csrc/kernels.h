@@ -23,6 +23,10 @@ size_t mma_smem_bytes(int head_dim, int stages);
 
 cudaError_t launch_mma(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
                        cudaStream_t stream);
+// tcgen05 prefill: bf16/f16, head_dim 128, (Hq/Hkv) dividing 128.
+size_t tc05_smem_bytes();
+cudaError_t launch_tc05(const FwdParams &p, int dtype, const CUtensorMap &tmq, const CUtensorMap &tmk,
+                        const CUtensorMap &tmv, cudaStream_t stream);
 cudaError_t launch_simt(const FwdParams &p, int dtype, cudaStream_t stream);
 cudaError_t launch_combine(const float *part_out, const float *part_lse, int S, long long rows, int D,
                            int out_dtype, void *out, float *lse, cudaStream_t stream);

@@ -1,0 +1,96 @@
+"""GPU parity of the tcgen05 (tensor-memory) kernel against the oracle: prefill and long query
+runs over paged K/V, causal with per-sequence offsets, GQA groups that divide 128, every page
+size, split partitions (including empty and fully masked ones), bf16 and f16."""
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_201_gb300 import workloads as W
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+TC05 = 4
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import paged_kv_cache_201_gb300 as pa
+    pa.load_library(build_if_missing=True)
+    return pa
+
+
+def _check(wl, S, what):
+    dw = _gpu.DeviceWorkload(wl)
+    res = _gpu.run(dw, S, TC05)
+    rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)
+    ref = oracle.workload_rows(wl, split_kv=S, row_bih=rows)
+    _gpu.compare_rows(res, ref, rows, wl, S, what)
+    return res
+
+
+@pytest.mark.parametrize("S", [1, 4, 16])
+def test_tc05_causal_prefill_small(pa, S):
+    qo = [0, 5, 40, -3]
+    Sq = 70
+    lens = [o + Sq for o in qo[:3]] + [50]
+    wl = W.make_custom(dtype="bf16", B=4, Sq=Sq, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=lens, causal=True,
+                       q_offset=qo, seed=205)
+    _check(wl, S, f"tc05 prefill-small S={S}")
+    assert pa.paged_attn_last_error_word() == 0
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+def test_tc05_gqa_groups(pa, G):
+    Hkv = 2
+    wl = W.make_custom(dtype="bf16", B=2, Sq=300 // G + 3, Hq=G * Hkv, Hkv=Hkv, D=128, page_size=16,
+                       seq_lens=[400, 333], causal=True, seed=206 + G)
+    _check(wl, 2, f"tc05 G={G}")
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tc05_page_sizes_dtypes(pa, page_size, dtype):
+    wl = W.make_custom(dtype=dtype, B=3, Sq=40, Hq=16, Hkv=4, D=128, page_size=page_size,
+                       seq_lens=[40, 170, 260], causal=True, q_offset=[0, 100, 220], seed=207 + page_size)
+    for S in (1, 3):
+        _check(wl, S, f"tc05 ps={page_size} {dtype} S={S}")
+
+
+def test_tc05_noncausal_and_decode_shapes(pa):
+    wl = W.make_custom(dtype="bf16", B=2, Sq=33, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=[33, 290],
+                       causal=False, seed=208)
+    _check(wl, 2, "tc05 noncausal")
+    wl = W.make_custom(dtype="bf16", B=5, Sq=1, Hq=16, Hkv=4, D=128, page_size=16, seq_lens=[0, 1, 17, 128, 513],
+                       seed=209)
+    res = _check(wl, 4, "tc05 decode shape")
+    assert np.all(res["lse"][0] == -np.inf)
+
+
+def test_tc05_causal_prefill_full(pa):
+    """The full causal prefill workload (B=4, Sq=1024, q_offset up to 3072, split 8) on sampled rows."""
+    wl = W.causal_prefill()
+    dw = _gpu.DeviceWorkload(wl)
+    toks = [0, 1, 2, 15, 16, 31, 32, 63, 64, 127, 128, 500, 777, 1000, 1023]
+    b, i, h = np.meshgrid(np.arange(wl.B), np.array(toks), np.arange(wl.Hq), indexing="ij")
+    rows = np.stack([b.ravel(), i.ravel(), h.ravel()], axis=1).astype(np.int32)
+    for S in (8, 1):
+        res = _gpu.run(dw, S, TC05)
+        ref = oracle.workload_rows(wl, split_kv=S, row_bih=rows)
+        _gpu.compare_rows(res, ref, rows, wl, S, f"tc05 full prefill S={S}")
+        assert not np.isnan(res["out"]).any()
+    assert pa.paged_attn_last_error_word() == 0
+
+
+def test_tc05_out_of_range_page(pa):
+    wl = W.make_custom(dtype="bf16", B=2, Sq=64, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=[100, 90], causal=True,
+                       num_pages=16, W=8, seed=210)
+    bt = wl.block_table.copy()
+    bt[0, 2] = 1 << 29
+    bad = W.Workload(**{**wl.__dict__, "block_table": bt})
+    assert pa.paged_attn_last_error_word() == 0
+    res = _gpu.run(_gpu.DeviceWorkload(bad), 1, TC05)
+    assert pa.paged_attn_last_error_word() & pa.ERRBIT_PAGE_RANGE
+    rows = oracle.all_rows(1, wl.Sq, wl.Hq)
+    rows[:, 0] = 1
+    ref = oracle.workload_rows(wl, split_kv=1, row_bih=rows)
+    _gpu.assert_close(res["out"][1].reshape(-1, wl.D), ref["out"], "bf16", "unaffected sequence")
