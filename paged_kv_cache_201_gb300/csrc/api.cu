@@ -119,6 +119,8 @@ int choose_variant(const pa_dims *d) {
     const int64_t rows = (int64_t)d->q_len * (d->num_q_heads / d->num_kv_heads);
     if (rows <= 1) return PA_VARIANT_SIMT;  // single-head decode: a 16-row tile would be 1/16 used
     if (rows <= pa::kDecodeRows) return PA_VARIANT_MMA_DECODE;
+    // 128-row tcgen05 tiles once at least half a tile of rows is real work
+    if (rows >= 64 && tc05_supports(d)) return PA_VARIANT_TC05_PREFILL;
     return PA_VARIANT_MMA_PREFILL;
 }
 

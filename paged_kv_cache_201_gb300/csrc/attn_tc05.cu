@@ -27,13 +27,13 @@ namespace {
 constexpr int kT5Threads = 192;               // 6 warps
 constexpr int kT5Half = 128 * 128;            // bytes of one 64-column half of a 128-row tile
 constexpr int kT5Tile = 2 * kT5Half;          // a 128 x 128 bf16 tile (Q, K or V)
-constexpr int kT5Stages = 2;
+constexpr int kT5Stages = 3;                  // K ring and V ring depth (tiles)
 constexpr uint32_t kT5TmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;           // rescale O only when the max grows by > 2^8
 
 // barrier slots
-enum { B_Q = 0, B_KF = 1, B_VF = 3, B_KVE = 5, B_SF = 7, B_PF = 9, B_OD = 11, B_COUNT = 12 };
+enum { B_Q = 0, B_KF = 1, B_VF = 4, B_KE = 7, B_VE = 10, B_SF = 13, B_PF = 15, B_OD = 17, B_COUNT = 18 };
 
 __device__ __forceinline__ long long t5_row_index(const FwdParams &p, int b, int kvh, int tok, int g) {
     return ((long long)b * p.Sq + tok) * p.Hq + (long long)kvh * p.G + g;
@@ -110,18 +110,22 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = sbase;
-    auto sK = [&](int st) { return sbase + (uint32_t)kT5Tile + (uint32_t)(st * 2 * kT5Tile); };
-    auto sV = [&](int st) { return sbase + (uint32_t)(2 * kT5Tile) + (uint32_t)(st * 2 * kT5Tile); };
+    // shared memory: Q | K ring (3 tiles) | V ring (3 tiles); K/V ring slot of tile t is t % 3
+    auto sK = [&](int ks) { return sbase + (uint32_t)kT5Tile * (1u + (uint32_t)ks); };
+    auto sV = [&](int ks) { return sbase + (uint32_t)kT5Tile * (1u + kT5Stages + (uint32_t)ks); };
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q), 1);
-        for (int st = 0; st < kT5Stages; ++st) {
-            mbar_init(bar(B_KF + st), 1);
-            mbar_init(bar(B_VF + st), 1);
-            mbar_init(bar(B_KVE + st), 1);
-            mbar_init(bar(B_SF + st), 1);
-            mbar_init(bar(B_PF + st), 128);
+        for (int ks = 0; ks < kT5Stages; ++ks) {
+            mbar_init(bar(B_KF + ks), 1);
+            mbar_init(bar(B_VF + ks), 1);
+            mbar_init(bar(B_KE + ks), 1);
+            mbar_init(bar(B_VE + ks), 1);
+        }
+        for (int sb = 0; sb < 2; ++sb) {
+            mbar_init(bar(B_SF + sb), 1);
+            mbar_init(bar(B_PF + sb), 128);
         }
         mbar_init(bar(B_OD), 1);
         fence_barrier_init();
@@ -154,13 +158,10 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
         int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
         bool bad = false;
-        int issued = 0;
+        int issued_k = 0, issued_v = 0;
         for (int t = 0; t < n_tiles; ++t) {
-            const int st = t & 1;
-            if (t >= kT5Stages && !bad) {
-                const bool ok = mbar_wait(bar(B_KVE + st), ((t >> 1) - 1) & 1, p.err);
-                bad = __any_sync(0xffffffffu, !ok);
-            }
+            const int ks = t % kT5Stages;
+            const uint32_t reuse_par = ((t / kT5Stages) - 1) & 1;
             const int pg_first = pg0 + t * ppt;
             if (pg_first >= batch + 32) {
                 batch += 32;
@@ -169,34 +170,52 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
             }
             const int id = __shfl_sync(0xffffffffu, id_cur, (pg_first + lane - batch) & 31);
-            if (bad) break;
             const int nvalid = min(ppt, pg_end - pg_first);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar(B_KF + st), (uint32_t)nvalid * 2u * box);
-                mbar_arrive_expect_tx(bar(B_VF + st), (uint32_t)nvalid * 2u * box);
-            }
-            __syncwarp();
+            int tok = 0;
             if (lane < nvalid) {
-                int tok;
                 if (id < 0 || (long long)id >= p.num_pages) {
                     atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
                     tok = -ps;  // wholly outside the tensor: reads as zeros
                 } else {
                     tok = id << ps_shift;
                 }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t off = (uint32_t)h * kT5Half + (uint32_t)lane * box;
-                    tma_load_4d(sK(st) + off, &tmK, bar(B_KF + st), 0, tok, h, kvh);
-                    tma_load_4d(sV(st) + off, &tmV, bar(B_VF + st), 0, tok, h, kvh);
-                }
             }
-            issued = t + 1;
+            // K slot: freed once Q K^T of tile t-3 has completed
+            if (t >= kT5Stages && !bad) {
+                const bool ok = mbar_wait(bar(B_KE + ks), reuse_par, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+            }
+            if (bad) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar(B_KF + ks), (uint32_t)nvalid * 2u * box);
+            __syncwarp();
+            if (lane < nvalid) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tma_load_4d(sK(ks) + (uint32_t)h * kT5Half + (uint32_t)lane * box, &tmK, bar(B_KF + ks), 0, tok, h,
+                                kvh);
+            }
+            issued_k = t + 1;
+            // V slot: freed once P V of tile t-3 has completed
+            if (t >= kT5Stages && !bad) {
+                const bool ok = mbar_wait(bar(B_VE + ks), reuse_par, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+            }
+            if (bad) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar(B_VF + ks), (uint32_t)nvalid * 2u * box);
+            __syncwarp();
+            if (lane < nvalid) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tma_load_4d(sV(ks) + (uint32_t)h * kT5Half + (uint32_t)lane * box, &tmV, bar(B_VF + ks), 0, tok, h,
+                                kvh);
+            }
+            issued_v = t + 1;
         }
-        for (int t = max(0, issued - kT5Stages); t < issued; ++t) {  // no copy may outlive the CTA
-            mbar_wait(bar(B_KF + (t & 1)), (t >> 1) & 1, p.err);
-            mbar_wait(bar(B_VF + (t & 1)), (t >> 1) & 1, p.err);
-        }
+        // no copy may outlive the CTA: wait (bounded) for the last phase armed on each slot
+        for (int t = max(0, issued_k - kT5Stages); t < issued_k; ++t)
+            mbar_wait(bar(B_KF + t % kT5Stages), (t / kT5Stages) & 1, p.err);
+        for (int t = max(0, issued_v - kT5Stages); t < issued_v; ++t)
+            mbar_wait(bar(B_VF + t % kT5Stages), (t / kT5Stages) & 1, p.err);
         if (lane == 0) mbar_wait(bar(B_Q), 0, p.err);
     } else if (warp == 1) {
         // ================================================================ MMA issuer
@@ -204,31 +223,33 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             bool bad = !mbar_wait(bar(B_Q), 0, p.err);
             for (int t = 0; t <= n_tiles && !bad; ++t) {
                 if (t < n_tiles) {
-                    const int st = t & 1;
-                    if (!mbar_wait(bar(B_KF + st), (t >> 1) & 1, p.err)) { bad = true; break; }
+                    const int sb = t & 1, ks = t % kT5Stages;
+                    if (!mbar_wait(bar(B_KF + ks), (t / kT5Stages) & 1, p.err)) { bad = true; break; }
                     tc05::fence_after_sync();
-                    const uint32_t d = tmem + (st ? 128u : 0u);
+                    const uint32_t d = tmem + (sb ? 128u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (uint32_t)(kk >> 2) * kT5Half + (uint32_t)(kk & 3) * 32u;
                         tc05::mma_ss(d, tc05::smem_desc_sw128(sQ + off, 16, 1024),
-                                     tc05::smem_desc_sw128(sK(st) + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                                     tc05::smem_desc_sw128(sK(ks) + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                     }
-                    tc05::commit(bar(B_SF + st));
+                    tc05::commit(bar(B_KE + ks));   // K slot reusable once this product is done
+                    tc05::commit(bar(B_SF + sb));
                 }
                 if (t >= 1) {
-                    const int u = t - 1, su = u & 1;
+                    const int u = t - 1, su = u & 1, ku = u % kT5Stages;
                     if (!mbar_wait(bar(B_PF + su), (u >> 1) & 1, p.err)) { bad = true; break; }
-                    if (!mbar_wait(bar(B_VF + su), (u >> 1) & 1, p.err)) { bad = true; break; }
+                    if (!mbar_wait(bar(B_VF + ku), (u / kT5Stages) & 1, p.err)) { bad = true; break; }
                     tc05::fence_after_sync();
                     const uint32_t pcol = tmem + (su ? 128u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t vd = tc05::smem_desc_sw128(sV(su) + (uint32_t)kk * 2048u, (uint32_t)kT5Half, 1024);
+                        const uint64_t vd =
+                            tc05::smem_desc_sw128(sV(ku) + (uint32_t)kk * 2048u, (uint32_t)kT5Half, 1024);
                         tc05::mma_ts(tmem + kColO, pcol + (uint32_t)kk * 8u, vd, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
                         tc05::mma_ts(tmem + kColO, pcol + 64u + (uint32_t)kk * 8u, vd, idesc_pv, 1u);
                     }
-                    tc05::commit(bar(B_KVE + su));
+                    tc05::commit(bar(B_VE + ku));
                     tc05::commit(bar(B_OD));
                 }
             }
@@ -321,12 +342,12 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             if (t == n_tiles - 1 && tile_k0 + 128 > k_hi) {
                 // Keys at or past k_hi (past the sequence or never loaded) may hold any bits:
                 // their weight is 0 but 0 * NaN is NaN, so zero those V rows before P V.
-                const bool ok = mbar_wait(bar(B_VF + st), (t >> 1) & 1, p.err);
+                const bool ok = mbar_wait(bar(B_VF + t % kT5Stages), (t / kT5Stages) & 1, p.err);
                 bad = __any_sync(0xffffffffu, !ok);
                 if (!bad && tile_k0 + r >= k_hi) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint32_t a = sV(st) + (uint32_t)h * kT5Half + (uint32_t)r * 128u;
+                        const uint32_t a = sV(t % kT5Stages) + (uint32_t)h * kT5Half + (uint32_t)r * 128u;
 #pragma unroll
                         for (int c = 0; c < 8; ++c)
                             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a + 16u * c), "r"(0u)
@@ -369,7 +390,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 }
 
 // ------------------------------------------------------------------------ host side
-size_t tc05_smem_bytes() { return (size_t)(kT5Tile + kT5Stages * 2 * kT5Tile + 1024); }
+size_t tc05_smem_bytes() { return (size_t)(kT5Tile * (1 + 2 * kT5Stages) + 1024); }
 
 template <typename T>
 static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, const CUtensorMap &tmk,
