@@ -246,8 +246,10 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t vd =
                             tc05::smem_desc_sw128(sV(ku) + (uint32_t)kk * 2048u, (uint32_t)kT5Half, 1024);
-                        tc05::mma_ts(tmem + kColO, pcol + (uint32_t)kk * 8u, vd, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
-                        tc05::mma_ts(tmem + kColO, pcol + 64u + (uint32_t)kk * 8u, vd, idesc_pv, 1u);
+                        // keys 16kk..16kk+15: chunk kk/2 of 32 keys; highs at +0, remainders at +16
+                        const uint32_t pa = pcol + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
+                        tc05::mma_ts(tmem + kColO, pa, vd, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
+                        tc05::mma_ts(tmem + kColO, pa + 16u, vd, idesc_pv, 1u);
                     }
                     tc05::commit(bar(B_VE + ku));
                     tc05::commit(bar(B_OD));
@@ -275,29 +277,25 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             }
             tc05::fence_after_sync();
             const uint32_t sbuf = tmem + lane_addr + (st ? 128u : 0u);
-            uint32_t u0[32], u1[32], u2[32], u3[32];
-            tc05::ld_32cols(sbuf + 0, u0);
-            tc05::ld_32cols(sbuf + 32, u1);
-            tc05::ld_32cols(sbuf + 64, u2);
-            tc05::ld_32cols(sbuf + 96, u3);
-            tc05::wait_ld();
-            float sc[128];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                sc[j] = __uint_as_float(u0[j]);
-                sc[32 + j] = __uint_as_float(u1[j]);
-                sc[64 + j] = __uint_as_float(u2[j]);
-                sc[96 + j] = __uint_as_float(u3[j]);
-            }
             const int tile_k0 = k_lo + t * 128;
             const int nvalid_row = lim - tile_k0;             // keys [0, nvalid_row) of the tile are valid here
+            // pass 1: maximum of this row's valid raw scores (scale > 0 commutes with max)
             float mx = kNegInf;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t u[32];
+                tc05::ld_32cols(sbuf + 32u * c, u);
+                tc05::wait_ld();
+                const int nv = nvalid_row - 32 * c;
+                if (nv >= 32) {
 #pragma unroll
-            for (int j = 0; j < 128; ++j) {
-                sc[j] = (j < nvalid_row) ? sc[j] * p.scale_log2 : kNegInf;
-                mx = fmaxf(mx, sc[j]);
+                    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(u[j]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) mx = (j < nv) ? fmaxf(mx, __uint_as_float(u[j])) : mx;
+                }
             }
-            const float m_new = fmaxf(m_used, mx);
+            const float m_new = fmaxf(m_used, mx * p.scale_log2);
             const bool need = m_new > m_used + kRescaleLog2;  // also true when m_used is -inf and m_new is not
             if (__any_sync(0xffffffffu, need)) {
                 const float alpha = need ? exp2f(m_used - m_new) : 1.f;
@@ -311,7 +309,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     bad = __any_sync(0xffffffffu, !ok);
                     if (bad) break;
                     tc05::fence_after_sync();
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
                         tc05::ld_32cols(tmem + lane_addr + kColO + 32u * c, o);
@@ -322,21 +320,29 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     }
                 }
             }
-            const float mu = (m_used == kNegInf) ? 0.f : m_used;  // -inf - (-inf) guard
-#pragma unroll
+            // pass 2: P = exp2(scale_log2 * s - m) for 32 keys at a time, stored over the same 32
+            // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs)
+            const float nmu = (m_used == kNegInf) ? 0.f : -m_used;  // -inf - (-inf) guard
+            const float c2 = p.scale_log2;
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
+                uint32_t u[32];
+                tc05::ld_32cols(sbuf + 32u * c, u);
+                tc05::wait_ld();
+                const int nv = nvalid_row - 32 * c;
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = exp2f(sc[32 * c + 2 * i] - mu);
-                    const float p1 = exp2f(sc[32 * c + 2 * i + 1] - mu);
+                    const float a0 = (2 * i < nv) ? fmaf(__uint_as_float(u[2 * i]), c2, nmu) : kNegInf;
+                    const float a1 = (2 * i + 1 < nv) ? fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu) : kNegInf;
+                    const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
                     l += p0 + p1;
                     hi[i] = MmaOp<T>::pack(p0, p1);
                     const float2 h2 = MmaOp<T>::unpack(hi[i]);
                     lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
                 }
-                tc05::st_16cols(sbuf + 16u * c, hi);
-                tc05::st_16cols(sbuf + 64u + 16u * c, lo);
+                tc05::st_16cols(sbuf + 32u * c, hi);
+                tc05::st_16cols(sbuf + 32u * c + 16u, lo);
             }
             tc05::wait_st();
             if (t == n_tiles - 1 && tile_k0 + 128 > k_hi) {

@@ -68,6 +68,13 @@ __device__ __forceinline__ int row_key_limit(const FwdParams &p, int b, int L, i
     return (int)(reach < L ? reach : L);
 }
 
+// 2^x by the hardware approximation (ex2.approx, subnormal results flushed to 0; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
