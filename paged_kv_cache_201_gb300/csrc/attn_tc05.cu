@@ -9,7 +9,7 @@
 //   warp 1      allocates 512 TMEM columns and issues tcgen05.mma from one thread:
 //               S_t = Q K_t^T into one of two S buffers (128 fp32 columns each), then
 //               O += Ph_{t-1} V_{t-1} + Pl_{t-1} V_{t-1} with P read from TMEM.
-//   warps 2-5   softmax, one TMEM lane (query row) per thread: mask (sequence length,
+//   warps 2-9   softmax, two threads per TMEM lane (query row), 64 columns each: mask (sequence length,
 //               split end, causal reach with q_offset), running max in the log2 domain,
 //               P = exp2(s - m) written back over S as a 16-bit high part and its
 //               rounding remainder.  O is rescaled in TMEM only when the running max
@@ -24,19 +24,45 @@ namespace pa {
 
 namespace {
 
-constexpr int kT5Threads = 192;               // 6 warps
+constexpr int kT5Threads = 320;               // 10 warps
 constexpr int kT5Half = 128 * 128;            // bytes of one 64-column half of a 128-row tile
 constexpr int kT5Tile = 2 * kT5Half;          // a 128 x 128 bf16 tile (Q, K or V)
-constexpr int kT5Stages = 3;                  // K ring and V ring depth (tiles)
+constexpr int kT5KStages = 3;                 // K ring depth (tiles)
+constexpr int kT5VStages = 2;                 // V ring depth (tiles)
 constexpr uint32_t kT5TmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;           // rescale O only when the max grows by > 2^8
 
 // barrier slots
-enum { B_Q = 0, B_KF = 1, B_VF = 4, B_KE = 7, B_VE = 10, B_SF = 13, B_PF = 15, B_OD = 17, B_COUNT = 18 };
+enum { B_Q = 0, B_KF = 1, B_KE = 4, B_VF = 7, B_VE = 9, B_SF = 11, B_PF = 13, B_OD = 15, B_COUNT = 16 };
 
 __device__ __forceinline__ long long t5_row_index(const FwdParams &p, int b, int kvh, int tok, int g) {
     return ((long long)b * p.Sq + tok) * p.Hq + (long long)kvh * p.G + g;
+}
+
+// Store output columns [64 hh, 64 hh + 64) of one row (and, from half 0, its lse).
+template <typename T>
+__device__ __forceinline__ void t5_store_half_row(const FwdParams &p, int s, long long ridx, int hh, const float *v,
+                                                  float lse) {
+    if (p.split_kv == 1) {
+        T *o = reinterpret_cast<T *>(p.out) + ridx * 128 + 64 * hh;
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+            uint4 w;
+            w.x = MmaOp<T>::pack(v[c + 0], v[c + 1]);
+            w.y = MmaOp<T>::pack(v[c + 2], v[c + 3]);
+            w.z = MmaOp<T>::pack(v[c + 4], v[c + 5]);
+            w.w = MmaOp<T>::pack(v[c + 6], v[c + 7]);
+            *reinterpret_cast<uint4 *>(o + c) = w;
+        }
+        if (p.lse && hh == 0) p.lse[ridx] = lse;
+    } else {
+        const long long rows_total = (long long)p.B * p.Sq * p.Hq;
+        float *o = reinterpret_cast<float *>(p.out) + ((long long)s * rows_total + ridx) * 128 + 64 * hh;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4 *>(o + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+        if (hh == 0) p.lse[(long long)s * rows_total + ridx] = lse;
+    }
 }
 
 template <typename T>
@@ -72,6 +98,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[B_COUNT];
     __shared__ uint32_t s_tmem;
+    __shared__ float s_xmax[2][2][128];   // [tile parity][column half][row]: partial row maxima
+    __shared__ float s_xsum[2][128];      // [column half][row]: partial row sums
+    __shared__ int s_xbad[2][128];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ps = 1 << ps_shift;
@@ -110,22 +139,24 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = sbase;
-    // shared memory: Q | K ring (3 tiles) | V ring (3 tiles); K/V ring slot of tile t is t % 3
+    // shared memory: Q | K ring (3 tiles, slot t % 3) | V ring (2 tiles, slot t % 2)
     auto sK = [&](int ks) { return sbase + (uint32_t)kT5Tile * (1u + (uint32_t)ks); };
-    auto sV = [&](int ks) { return sbase + (uint32_t)kT5Tile * (1u + kT5Stages + (uint32_t)ks); };
+    auto sV = [&](int vs) { return sbase + (uint32_t)kT5Tile * (1u + kT5KStages + (uint32_t)vs); };
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q), 1);
-        for (int ks = 0; ks < kT5Stages; ++ks) {
+        for (int ks = 0; ks < kT5KStages; ++ks) {
             mbar_init(bar(B_KF + ks), 1);
-            mbar_init(bar(B_VF + ks), 1);
             mbar_init(bar(B_KE + ks), 1);
-            mbar_init(bar(B_VE + ks), 1);
+        }
+        for (int vs = 0; vs < kT5VStages; ++vs) {
+            mbar_init(bar(B_VF + vs), 1);
+            mbar_init(bar(B_VE + vs), 1);
         }
         for (int sb = 0; sb < 2; ++sb) {
             mbar_init(bar(B_SF + sb), 1);
-            mbar_init(bar(B_PF + sb), 128);
+            mbar_init(bar(B_PF + sb), 256);
         }
         mbar_init(bar(B_OD), 1);
         fence_barrier_init();
@@ -160,8 +191,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         bool bad = false;
         int issued_k = 0, issued_v = 0;
         for (int t = 0; t < n_tiles; ++t) {
-            const int ks = t % kT5Stages;
-            const uint32_t reuse_par = ((t / kT5Stages) - 1) & 1;
+            const int ks = t % kT5KStages, vs = t % kT5VStages;
             const int pg_first = pg0 + t * ppt;
             if (pg_first >= batch + 32) {
                 batch += 32;
@@ -181,8 +211,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 }
             }
             // K slot: freed once Q K^T of tile t-3 has completed
-            if (t >= kT5Stages && !bad) {
-                const bool ok = mbar_wait(bar(B_KE + ks), reuse_par, p.err);
+            if (t >= kT5KStages && !bad) {
+                const bool ok = mbar_wait(bar(B_KE + ks), ((t / kT5KStages) - 1) & 1, p.err);
                 bad = __any_sync(0xffffffffu, !ok);
             }
             if (bad) break;
@@ -195,27 +225,27 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                                 kvh);
             }
             issued_k = t + 1;
-            // V slot: freed once P V of tile t-3 has completed
-            if (t >= kT5Stages && !bad) {
-                const bool ok = mbar_wait(bar(B_VE + ks), reuse_par, p.err);
+            // V slot: freed once P V of tile t-2 has completed
+            if (t >= kT5VStages && !bad) {
+                const bool ok = mbar_wait(bar(B_VE + vs), ((t / kT5VStages) - 1) & 1, p.err);
                 bad = __any_sync(0xffffffffu, !ok);
             }
             if (bad) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(B_VF + ks), (uint32_t)nvalid * 2u * box);
+            if (lane == 0) mbar_arrive_expect_tx(bar(B_VF + vs), (uint32_t)nvalid * 2u * box);
             __syncwarp();
             if (lane < nvalid) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sV(ks) + (uint32_t)h * kT5Half + (uint32_t)lane * box, &tmV, bar(B_VF + ks), 0, tok, h,
+                    tma_load_4d(sV(vs) + (uint32_t)h * kT5Half + (uint32_t)lane * box, &tmV, bar(B_VF + vs), 0, tok, h,
                                 kvh);
             }
             issued_v = t + 1;
         }
         // no copy may outlive the CTA: wait (bounded) for the last phase armed on each slot
-        for (int t = max(0, issued_k - kT5Stages); t < issued_k; ++t)
-            mbar_wait(bar(B_KF + t % kT5Stages), (t / kT5Stages) & 1, p.err);
-        for (int t = max(0, issued_v - kT5Stages); t < issued_v; ++t)
-            mbar_wait(bar(B_VF + t % kT5Stages), (t / kT5Stages) & 1, p.err);
+        for (int t = max(0, issued_k - kT5KStages); t < issued_k; ++t)
+            mbar_wait(bar(B_KF + t % kT5KStages), (t / kT5KStages) & 1, p.err);
+        for (int t = max(0, issued_v - kT5VStages); t < issued_v; ++t)
+            mbar_wait(bar(B_VF + t % kT5VStages), (t / kT5VStages) & 1, p.err);
         if (lane == 0) mbar_wait(bar(B_Q), 0, p.err);
     } else if (warp == 1) {
         // ================================================================ MMA issuer
@@ -223,8 +253,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             bool bad = !mbar_wait(bar(B_Q), 0, p.err);
             for (int t = 0; t <= n_tiles && !bad; ++t) {
                 if (t < n_tiles) {
-                    const int sb = t & 1, ks = t % kT5Stages;
-                    if (!mbar_wait(bar(B_KF + ks), (t / kT5Stages) & 1, p.err)) { bad = true; break; }
+                    const int sb = t & 1, ks = t % kT5KStages;
+                    if (!mbar_wait(bar(B_KF + ks), (t / kT5KStages) & 1, p.err)) { bad = true; break; }
                     tc05::fence_after_sync();
                     const uint32_t d = tmem + (sb ? 128u : 0u);
 #pragma unroll
@@ -237,9 +267,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     tc05::commit(bar(B_SF + sb));
                 }
                 if (t >= 1) {
-                    const int u = t - 1, su = u & 1, ku = u % kT5Stages;
+                    const int u = t - 1, su = u & 1, ku = u % kT5VStages;
                     if (!mbar_wait(bar(B_PF + su), (u >> 1) & 1, p.err)) { bad = true; break; }
-                    if (!mbar_wait(bar(B_VF + ku), (u / kT5Stages) & 1, p.err)) { bad = true; break; }
+                    if (!mbar_wait(bar(B_VF + ku), (u / kT5VStages) & 1, p.err)) { bad = true; break; }
                     tc05::fence_after_sync();
                     const uint32_t pcol = tmem + (su ? 128u : 0u);
 #pragma unroll
@@ -258,7 +288,13 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         }
         __syncwarp();
     } else {
-        // ================================================================ softmax (warps 2-5)
+        // ================================================================ softmax (warps 2-9)
+        // Two warpgroups share every row: group hh (warps 2-5: hh = 0, warps 6-9: hh = 1) owns
+        // score columns / keys [64 hh, 64 hh + 64) and output columns [64 hh, 64 hh + 64).  They
+        // exchange the row maximum once per tile and the row sum once at the end; both keep the
+        // same running maximum, so the rescale decisions agree.  Every named barrier is reached on
+        // every path (a warp that gave up on a wait still walks the loop), so none can hang.
+        const int hh = (warp - 2) >> 2;
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;                       // TMEM lane = query row of the tile
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
@@ -268,97 +304,114 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         const int lim = row_valid ? min(k_hi_split, row_key_limit(p, b, L, tk)) : k_lo;
         float m_used = kNegInf, l = 0.f;
         bool bad = false;
-        for (int t = 0; t < n_tiles && !bad; ++t) {
+        for (int t = 0; t < n_tiles; ++t) {
             const int st = t & 1;
-            {
+            if (!bad) {
                 const bool ok = mbar_wait(bar(B_SF + st), (t >> 1) & 1, p.err);
                 bad = __any_sync(0xffffffffu, !ok);
-                if (bad) break;
             }
             tc05::fence_after_sync();
             const uint32_t sbuf = tmem + lane_addr + (st ? 128u : 0u);
             const int tile_k0 = k_lo + t * 128;
-            const int nvalid_row = lim - tile_k0;             // keys [0, nvalid_row) of the tile are valid here
-            // pass 1: maximum of this row's valid raw scores (scale > 0 commutes with max)
+            const int nvalid_row = lim - tile_k0;           // keys [0, nvalid_row) of the tile are valid here
+            // pass 1: maximum of this row's valid raw scores in my 64 columns (scale > 0 commutes with max)
             float mx = kNegInf;
+            if (!bad) {
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t u[32];
-                tc05::ld_32cols(sbuf + 32u * c, u);
-                tc05::wait_ld();
-                const int nv = nvalid_row - 32 * c;
-                if (nv >= 32) {
+                for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
+                    uint32_t u[32];
+                    tc05::ld_32cols(sbuf + 32u * c, u);
+                    tc05::wait_ld();
+                    const int nv = nvalid_row - 32 * c;
+                    if (nv >= 32) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(u[j]));
-                } else {
+                        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(u[j]));
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) mx = (j < nv) ? fmaxf(mx, __uint_as_float(u[j])) : mx;
+                        for (int j = 0; j < 32; ++j) mx = (j < nv) ? fmaxf(mx, __uint_as_float(u[j])) : mx;
+                    }
                 }
             }
+            s_xmax[st][hh][r] = mx;
+            named_bar_sync(2, 256);
+            mx = fmaxf(mx, s_xmax[st][hh ^ 1][r]);
             const float m_new = fmaxf(m_used, mx * p.scale_log2);
             const bool need = m_new > m_used + kRescaleLog2;  // also true when m_used is -inf and m_new is not
-            if (__any_sync(0xffffffffu, need)) {
+            if (__any_sync(0xffffffffu, need) && !bad) {
                 const float alpha = need ? exp2f(m_used - m_new) : 1.f;
                 if (need) {
                     l *= alpha;
                     m_used = m_new;
                 }
                 if (t > 0) {
-                    // O holds P V of earlier tiles: wait for the last one, then rescale this row
+                    // O holds P V of earlier tiles: wait for the last one, then rescale my half of the row
                     const bool ok = mbar_wait(bar(B_OD), (t - 1) & 1, p.err);
                     bad = __any_sync(0xffffffffu, !ok);
-                    if (bad) break;
-                    tc05::fence_after_sync();
+                    if (!bad) {
+                        tc05::fence_after_sync();
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t o[32];
-                        tc05::ld_32cols(tmem + lane_addr + kColO + 32u * c, o);
-                        tc05::wait_ld();
+                        for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
+                            uint32_t o[32];
+                            tc05::ld_32cols(tmem + lane_addr + kColO + 32u * c, o);
+                            tc05::wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                        tc05::st_32cols(tmem + lane_addr + kColO + 32u * c, o);
+                            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                            tc05::st_32cols(tmem + lane_addr + kColO + 32u * c, o);
+                        }
                     }
                 }
             }
-            // pass 2: P = exp2(scale_log2 * s - m) for 32 keys at a time, stored over the same 32
-            // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs)
-            const float nmu = (m_used == kNegInf) ? 0.f : -m_used;  // -inf - (-inf) guard
-            const float c2 = p.scale_log2;
+            if (!bad) {
+                // pass 2: P = exp2(scale_log2 * s - m) for 32 keys at a time, stored over the same 32
+                // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs)
+                const float nmu = (m_used == kNegInf) ? 0.f : -m_used;  // -inf - (-inf) guard
+                const float c2 = p.scale_log2;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t u[32];
-                tc05::ld_32cols(sbuf + 32u * c, u);
-                tc05::wait_ld();
-                const int nv = nvalid_row - 32 * c;
-                uint32_t hi[16], lo[16];
+                for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
+                    uint32_t u[32];
+                    tc05::ld_32cols(sbuf + 32u * c, u);
+                    tc05::wait_ld();
+                    const int nv = nvalid_row - 32 * c;
+                    uint32_t hi[16], lo[16];
+                    if (nv >= 32) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float a0 = (2 * i < nv) ? fmaf(__uint_as_float(u[2 * i]), c2, nmu) : kNegInf;
-                    const float a1 = (2 * i + 1 < nv) ? fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu) : kNegInf;
-                    const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
-                    l += p0 + p1;
-                    hi[i] = MmaOp<T>::pack(p0, p1);
-                    const float2 h2 = MmaOp<T>::unpack(hi[i]);
-                    lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+                        for (int i = 0; i < 16; ++i) {
+                            const float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * i]), c2, nmu));
+                            const float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu));
+                            l += p0 + p1;
+                            hi[i] = MmaOp<T>::pack(p0, p1);
+                            const float2 h2 = MmaOp<T>::unpack(hi[i]);
+                            lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float a0 = (2 * i < nv) ? fmaf(__uint_as_float(u[2 * i]), c2, nmu) : kNegInf;
+                            const float a1 = (2 * i + 1 < nv) ? fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu) : kNegInf;
+                            const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+                            l += p0 + p1;
+                            hi[i] = MmaOp<T>::pack(p0, p1);
+                            const float2 h2 = MmaOp<T>::unpack(hi[i]);
+                            lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+                        }
+                    }
+                    tc05::st_16cols(sbuf + 32u * c, hi);
+                    tc05::st_16cols(sbuf + 32u * c + 16u, lo);
                 }
-                tc05::st_16cols(sbuf + 32u * c, hi);
-                tc05::st_16cols(sbuf + 32u * c + 16u, lo);
+                tc05::wait_st();
             }
-            tc05::wait_st();
             if (t == n_tiles - 1 && tile_k0 + 128 > k_hi) {
-                // Keys at or past k_hi (past the sequence or never loaded) may hold any bits:
-                // their weight is 0 but 0 * NaN is NaN, so zero those V rows before P V.
-                const bool ok = mbar_wait(bar(B_VF + t % kT5Stages), (t / kT5Stages) & 1, p.err);
-                bad = __any_sync(0xffffffffu, !ok);
+                // Keys at or past k_hi (past the sequence or never loaded) may hold any bits: their
+                // weight is 0 but 0 * NaN is NaN, so zero those V rows (my half of each) before P V.
+                if (!bad) {
+                    const bool ok = mbar_wait(bar(B_VF + t % kT5VStages), (t / kT5VStages) & 1, p.err);
+                    bad = __any_sync(0xffffffffu, !ok);
+                }
                 if (!bad && tile_k0 + r >= k_hi) {
+                    const uint32_t a = sV(t % kT5VStages) + (uint32_t)hh * kT5Half + (uint32_t)r * 128u;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t a = sV(t % kT5Stages) + (uint32_t)h * kT5Half + (uint32_t)r * 128u;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a + 16u * c), "r"(0u)
-                                         : "memory");
-                    }
+                    for (int c = 0; c < 8; ++c)
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a + 16u * c), "r"(0u) : "memory");
                 }
                 fence_proxy_async_smem();
             }
@@ -369,21 +422,25 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             const bool ok = mbar_wait(bar(B_OD), (n_tiles - 1) & 1, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
-        if (!bad) {
+        s_xsum[hh][r] = l;
+        s_xbad[hh][r] = bad ? 1 : 0;
+        named_bar_sync(2, 256);
+        const float l_tot = l + s_xsum[hh ^ 1][r];
+        if (!bad && !s_xbad[hh ^ 1][r]) {
             tc05::fence_after_sync();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            float o[128];
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            float o[64];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t u[32];
-                tc05::ld_32cols(tmem + lane_addr + kColO + 32u * c, u);
+                tc05::ld_32cols(tmem + lane_addr + kColO + 32u * (2 * hh + c), u);
                 tc05::wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(u[j]) * inv;
             }
             if (row_valid)
-                t5_store_row<T>(p, s, t5_row_index(p, b, kvh, tk, g), o,
-                                l > 0.f ? m_used * kLn2 + logf(l) : kNegInf);
+                t5_store_half_row<T>(p, s, t5_row_index(p, b, kvh, tk, g), hh, o,
+                                     l_tot > 0.f ? m_used * kLn2 + logf(l_tot) : kNegInf);
         }
     }
 
@@ -396,7 +453,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 }
 
 // ------------------------------------------------------------------------ host side
-size_t tc05_smem_bytes() { return (size_t)(kT5Tile * (1 + 2 * kT5Stages) + 1024); }
+size_t tc05_smem_bytes() { return (size_t)(kT5Tile * (1 + kT5KStages + kT5VStages) + 1024); }
 
 template <typename T>
 static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, const CUtensorMap &tmk,
