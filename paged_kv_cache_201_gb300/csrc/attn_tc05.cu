@@ -34,7 +34,10 @@ constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;           // rescale O only when the max grows by > 2^8
 
 // barrier slots
-enum { B_Q = 0, B_KF = 1, B_KE = 4, B_VF = 7, B_VE = 9, B_SF = 11, B_PF = 13, B_OD = 15, B_COUNT = 16 };
+// B_OD completes once per P V product; B_OF once, after the last one.  A parity wait on B_OD is
+// only unambiguous while it is at most one phase behind, which holds inside the tile loop (Q K^T of
+// tile t completing implies P V of tile t-2 has) but not after it, hence B_OF.
+enum { B_Q = 0, B_KF = 1, B_KE = 4, B_VF = 7, B_VE = 9, B_SF = 11, B_PF = 13, B_OD = 15, B_OF = 16, B_COUNT = 17 };
 
 __device__ __forceinline__ long long t5_row_index(const FwdParams &p, int b, int kvh, int tok, int g) {
     return ((long long)b * p.Sq + tok) * p.Hq + (long long)kvh * p.G + g;
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_init(bar(B_PF + sb), 256);
         }
         mbar_init(bar(B_OD), 1);
+        mbar_init(bar(B_OF), 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -283,6 +287,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     }
                     tc05::commit(bar(B_VE + ku));
                     tc05::commit(bar(B_OD));
+                    if (u == n_tiles - 1) tc05::commit(bar(B_OF));
                 }
             }
         }
@@ -419,7 +424,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_arrive(bar(B_PF + st));
         }
         if (!bad) {
-            const bool ok = mbar_wait(bar(B_OD), (n_tiles - 1) & 1, p.err);
+            const bool ok = mbar_wait(bar(B_OF), 0, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
         s_xsum[hh][r] = l;
