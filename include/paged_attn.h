@@ -137,6 +137,35 @@ int paged_attn_combine(const float *part_out, const float *part_lse, int split_k
                        int out_dtype, void *out, float *lse, void *stream);
 
 /*
+ * Workspace and automatic split (rocMLIR PR #2371, "device-memory-aware split-KV prefilter": the
+ * extra split-KV storage is bounded by a budget of device memory / 8, clamped to [1 GiB, 8 GiB]).
+ *
+ * paged_attn_auto_split — the split count paged_attn_fwd_splitkv uses for split_kv = 0: the smallest
+ *   S that gives at least two waves of work units over `num_sms` multiprocessors (units =
+ *   B * Hkv * S, times query-row tiles for long query runs), capped by bt_stride (no sequence
+ *   has more pages), by 256, and by the workspace budget for `device_bytes` of device memory.
+ *   Returns S >= 1, or a negative status for invalid dims.
+ * paged_attn_workspace_bytes — device bytes paged_attn_fwd_splitkv needs for split_kv partitions
+ *   (0 = the automatic choice for num_sms / device_bytes): 0 when S == 1, otherwise
+ *   S * B * Sq * Hq * (D + 1) * 4 rounded up to 256-byte blocks.  Negative status on error.
+ */
+int paged_attn_auto_split(const pa_dims *dims, int num_sms, int64_t device_bytes);
+int64_t paged_attn_workspace_bytes(const pa_dims *dims, int split_kv, int num_sms, int64_t device_bytes);
+
+/*
+ * paged_attn_fwd_splitkv — the whole path in one call: the split forward into `workspace` (fp32
+ * partial outputs and lse), then the fp32 combine into out [B, Sq, Hq, D] (dtype) and lse
+ * [B, Sq, Hq] (float32, or NULL).  split_kv = 0 picks paged_attn_auto_split(dims, num_sms,
+ * device_bytes); S == 1 writes out directly and touches no workspace.  `workspace` (device, 256-byte
+ * aligned, caller-owned) must hold paged_attn_workspace_bytes(...) bytes, else PA_EINVAL; its
+ * contents afterwards are unspecified.  Other arguments as paged_attn_fwd.
+ */
+int paged_attn_fwd_splitkv(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                           const int32_t *seq_lens, int causal, const int32_t *q_offset, int split_kv, float scale,
+                           void *out, float *lse, const pa_dims *dims, void *workspace, int64_t workspace_bytes,
+                           int num_sms, int64_t device_bytes, void *stream);
+
+/*
  * paged_attn_plan — the split plan as data: plan [batch, split_kv, 2] int32 =
  * {first page, one past the last page} of each run (see paged_attn_fwd).
  * seq_lens is a device pointer [batch]; negative lengths count as 0.

@@ -17,7 +17,8 @@ from . import build as _build
 __all__ = [
     "PagedAttnError", "load_library", "library_path", "paged_attn_fwd", "paged_attn_fwd_variant",
     "paged_attn_combine", "paged_attn_plan", "paged_attn_debug_gather", "paged_attn_last_error_word",
-    "paged_attn_strerror", "paged_attn_version", "attention", "PA_F32", "PA_F16", "PA_BF16",
+    "paged_attn_strerror", "paged_attn_version", "attention", "paged_attn_auto_split",
+    "paged_attn_workspace_bytes", "paged_attn_fwd_splitkv", "PA_F32", "PA_F16", "PA_BF16",
     "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL", "VARIANT_TC05_PREFILL",
 ]
 
@@ -63,6 +64,12 @@ def load_library(build_if_missing: bool = False):
     lib.paged_attn_fwd_variant.argtypes = [P, P, P, P, P, I32, P, I32, F, P, P, D, I32, P]
     lib.paged_attn_combine.argtypes = [P, P, I32, I64, I32, I32, P, P, P]
     lib.paged_attn_plan.argtypes = [P, I32, I32, I32, P, P]
+    lib.paged_attn_auto_split.argtypes = [D, I32, I64]
+    lib.paged_attn_auto_split.restype = ctypes.c_int
+    lib.paged_attn_workspace_bytes.argtypes = [D, I32, I32, I64]
+    lib.paged_attn_workspace_bytes.restype = ctypes.c_int64
+    lib.paged_attn_fwd_splitkv.argtypes = [P, P, P, P, P, I32, P, I32, F, P, P, D, P, I64, I32, I64, P]
+    lib.paged_attn_fwd_splitkv.restype = ctypes.c_int
     lib.paged_attn_debug_gather.argtypes = [P, P, P, D, I32, P, P]
     lib.paged_attn_last_error_word.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.paged_attn_strerror.argtypes = [I32]
@@ -154,6 +161,63 @@ def paged_attn_fwd(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset,
                    stream=None) -> None:
     paged_attn_fwd_variant(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale, out, lse,
                            VARIANT_AUTO, stream)
+
+
+def _device_info(device=None):
+    torch = _torch()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device() if device is None else device)
+    return int(props.multi_processor_count), int(props.total_memory)
+
+
+def paged_attn_auto_split(q, k_cache, block_table, num_sms=None, device_bytes=None) -> int:
+    """Split count the single-call forward picks for this shape (rocMLIR PR #2371 workspace budget)."""
+    dims = dims_of(q, k_cache, block_table)
+    if num_sms is None or device_bytes is None:
+        n, m = _device_info(q.device)
+        num_sms = n if num_sms is None else num_sms
+        device_bytes = m if device_bytes is None else device_bytes
+    rc = load_library().paged_attn_auto_split(ctypes.byref(dims), int(num_sms), int(device_bytes))
+    if rc < 0:
+        _raise(rc, "paged_attn_auto_split")
+    return rc
+
+
+def paged_attn_workspace_bytes(q, k_cache, block_table, split_kv: int = 0, num_sms=None, device_bytes=None) -> int:
+    dims = dims_of(q, k_cache, block_table)
+    if num_sms is None or device_bytes is None:
+        n, m = _device_info(q.device)
+        num_sms = n if num_sms is None else num_sms
+        device_bytes = m if device_bytes is None else device_bytes
+    v = load_library().paged_attn_workspace_bytes(ctypes.byref(dims), int(split_kv), int(num_sms), int(device_bytes))
+    if v < 0:
+        _raise(int(v), "paged_attn_workspace_bytes")
+    return int(v)
+
+
+def paged_attn_fwd_splitkv(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale, out, lse,
+                           workspace, num_sms=None, device_bytes=None, stream=None) -> None:
+    """Split forward + combine in one call; ``workspace`` is a uint8 CUDA tensor (may be None when S == 1)."""
+    torch = _torch()
+    _check(q, "q", ndim=4)
+    _check(k_cache, "k_cache", q.dtype, 4)
+    _check(v_cache, "v_cache", q.dtype, 4)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    _check(q_offset, "q_offset", torch.int32, 1)
+    _check(out, "out", q.dtype)
+    _check(lse, "lse", torch.float32)
+    _check(workspace, "workspace")
+    dims = dims_of(q, k_cache, block_table)
+    if num_sms is None or device_bytes is None:
+        n, m = _device_info(q.device)
+        num_sms = n if num_sms is None else num_sms
+        device_bytes = m if device_bytes is None else device_bytes
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().paged_attn_fwd_splitkv(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), int(bool(causal)), _ptr(q_offset),
+        int(split_kv), float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace), int(ws_bytes),
+        int(num_sms), int(device_bytes), _stream(stream))
+    _raise(rc, "paged_attn_fwd_splitkv")
 
 
 def paged_attn_combine(part_out, part_lse, out, lse=None, stream=None) -> None:

@@ -220,6 +220,74 @@ int paged_attn_fwd(const void *q, const void *k_cache, const void *v_cache, cons
                                   lse, dims, PA_VARIANT_AUTO, stream);
 }
 
+int paged_attn_auto_split(const pa_dims *dims, int num_sms, int64_t device_bytes) {
+    int rc = check_dims(dims);
+    if (rc != PA_OK) return rc;
+    if (num_sms < 1) return PA_EINVAL;
+    const int G = dims->num_q_heads / dims->num_kv_heads;
+    const int64_t rows = (int64_t)dims->q_len * G;
+    // query-row tiles per (sequence, kv head) of the kernel the planner would pick
+    const int64_t tile_rows = rows <= pa::kDecodeRows ? pa::kDecodeRows : 128;
+    const int64_t row_tiles = (rows + tile_rows - 1) / tile_rows;
+    const int64_t units1 = (int64_t)dims->batch * dims->num_kv_heads * (row_tiles > 0 ? row_tiles : 1);
+    const int64_t want = 2LL * num_sms;  // two waves of units
+    int64_t S = units1 > 0 ? (want + units1 - 1) / units1 : 1;
+    if (S > dims->bt_stride) S = dims->bt_stride;
+    if (S > 256) S = 256;
+    if (S < 1) S = 1;
+    // workspace budget: device memory / 8 clamped to [1 GiB, 8 GiB] (1.5 GiB when unknown)
+    int64_t budget = device_bytes > 0 ? device_bytes / 8 : (int64_t)3 << 29;
+    if (budget < ((int64_t)1 << 30)) budget = (int64_t)1 << 30;
+    if (budget > ((int64_t)8 << 30)) budget = (int64_t)8 << 30;
+    const int64_t per_split = (int64_t)dims->batch * dims->q_len * dims->num_q_heads * (dims->head_dim + 1) * 4;
+    while (S > 1 && S * per_split > budget) --S;
+    return (int)S;
+}
+
+int64_t paged_attn_workspace_bytes(const pa_dims *dims, int split_kv, int num_sms, int64_t device_bytes) {
+    int rc = check_dims(dims);
+    if (rc != PA_OK) return rc;
+    if (split_kv < 0 || split_kv > 65535) return PA_EINVAL;
+    if (split_kv == 0) {
+        split_kv = paged_attn_auto_split(dims, num_sms, device_bytes);
+        if (split_kv < 0) return split_kv;
+    }
+    if (split_kv == 1) return 0;
+    const int64_t rows = (int64_t)dims->batch * dims->q_len * dims->num_q_heads;
+    const int64_t out_b = ((int64_t)split_kv * rows * dims->head_dim * 4 + 255) / 256 * 256;
+    const int64_t lse_b = ((int64_t)split_kv * rows * 4 + 255) / 256 * 256;
+    return out_b + lse_b;
+}
+
+int paged_attn_fwd_splitkv(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                           const int32_t *seq_lens, int causal, const int32_t *q_offset, int split_kv, float scale,
+                           void *out, float *lse, const pa_dims *dims, void *workspace, int64_t workspace_bytes,
+                           int num_sms, int64_t device_bytes, void *stream) {
+    int rc = check_dims(dims);
+    if (rc != PA_OK) return rc;
+    if (split_kv < 0 || split_kv > 65535) return PA_EINVAL;
+    if (split_kv == 0) {
+        split_kv = paged_attn_auto_split(dims, num_sms, device_bytes);
+        if (split_kv < 0) return split_kv;
+    }
+    if (split_kv == 1)
+        return paged_attn_fwd(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, 1, scale, out, lse, dims,
+                              stream);
+    const int64_t need = paged_attn_workspace_bytes(dims, split_kv, num_sms, device_bytes);
+    if (need < 0) return (int)need;
+    const int64_t rows = (int64_t)dims->batch * dims->q_len * dims->num_q_heads;
+    if (rows == 0) return PA_OK;
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_EINVAL;
+    if (!out || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return PA_EINVAL;
+    float *part_out = static_cast<float *>(workspace);
+    float *part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                ((int64_t)split_kv * rows * dims->head_dim * 4 + 255) / 256 * 256);
+    rc = paged_attn_fwd(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale, part_out,
+                        part_lse, dims, stream);
+    if (rc != PA_OK) return rc;
+    return paged_attn_combine(part_out, part_lse, split_kv, rows, dims->head_dim, dims->dtype, out, lse, stream);
+}
+
 int paged_attn_combine(const float *part_out, const float *part_lse, int split_kv, int64_t rows, int head_dim,
                        int out_dtype, void *out, float *lse, void *stream) {
     if (out_dtype != PA_F32 && out_dtype != PA_F16 && out_dtype != PA_BF16) return PA_EDTYPE;

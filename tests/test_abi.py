@@ -110,3 +110,25 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(pa, "library_path", lambda: str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="not built"):
         pa.load_library()
+
+
+def test_auto_split_and_workspace_host_logic(lib):
+    """Split choice: two waves of units over the SMs, capped by bt_stride, 256 and the workspace budget
+    (device memory / 8 clamped to [1 GiB, 8 GiB], rocMLIR PR #2371 split-KV prefilter)."""
+    auto, wsb = lib.paged_attn_auto_split, lib.paged_attn_workspace_bytes
+    d = _dims(batch=256, q_len=1, num_q_heads=32, num_kv_heads=8, bt_stride=256)   # 2048 units already
+    assert auto(ctypes.byref(d), 152, 280 << 30) == 1
+    assert wsb(ctypes.byref(d), 0, 152, 280 << 30) == 0
+    d = _dims(batch=32, q_len=1, num_q_heads=64, num_kv_heads=4, bt_stride=63)     # 128 units -> ceil(304/128)
+    assert auto(ctypes.byref(d), 152, 280 << 30) == 3
+    # 3 splits x 2048 rows: out 3*2048*128*4 = 3145728 B, lse 3*2048*4 = 24576 B (256-B multiples)
+    assert wsb(ctypes.byref(d), 0, 152, 280 << 30) == 3145728 + 24576
+    d = _dims(batch=1, q_len=1, num_q_heads=32, num_kv_heads=8, bt_stride=20)      # capped by bt_stride
+    assert auto(ctypes.byref(d), 152, 280 << 30) == 20
+    d = _dims(batch=1024, q_len=1, num_q_heads=64, num_kv_heads=8, bt_stride=4096)
+    # per split 1024*64*129*4 = 33816576 B; 1 GiB budget -> 31 splits; 8 GiB -> the 245 of two waves stands
+    assert auto(ctypes.byref(d), 1000000, 8 << 30) == 31
+    assert auto(ctypes.byref(d), 1000000, 80 << 30) == 245
+    assert auto(ctypes.byref(d), 0, 8 << 30) == EINVAL
+    assert wsb(ctypes.byref(d), -1, 152, 8 << 30) == EINVAL
+    assert wsb(ctypes.byref(d), 1, 152, 8 << 30) == 0
