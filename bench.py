@@ -315,15 +315,15 @@ def run_ours(args, ws, rank, local):
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
 
-        ws_bytes = pa.paged_attn_workspace_bytes(q, k, bt, S)
-        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+        wsp_bytes = pa.paged_attn_workspace_bytes(q, k, bt, S)
+        wsp = torch.empty(max(wsp_bytes, 256), dtype=torch.uint8, device=dev)
 
         def e2e_step():
             # the single public call: split forward into the workspace, then the combine
             q.copy_(q_h, non_blocking=True)
             bt.copy_(bt_h, non_blocking=True)
             sl.copy_(sl_h, non_blocking=True)
-            pa.paged_attn_fwd_splitkv(q, k, v, bt, sl, wl.causal, qo, S, wl.scale, out, lse, ws, stream=stream)
+            pa.paged_attn_fwd_splitkv(q, k, v, bt, sl, wl.causal, qo, S, wl.scale, out, lse, wsp, stream=stream)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
 
