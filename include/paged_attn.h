@@ -166,6 +166,29 @@ int paged_attn_fwd_splitkv(const void *q, const void *k_cache, const void *v_cac
                            int num_sms, int64_t device_bytes, void *stream);
 
 /*
+ * paged_attn_fwd_splitkv_noalloc — paged_attn_fwd_splitkv for callers that cannot allocate device
+ * memory at call time (a plugin whose host framework owns every device byte, or a serving loop that
+ * must never reach cudaMalloc, which can synchronise the device).  The pages have no counterpart:
+ * this is a deployment convenience of this library, not part of the method.
+ *
+ * Same arguments and results as paged_attn_fwd_splitkv minus the workspace: the split partials go
+ * to a fixed array of PA_NOALLOC_SCRATCH_BYTES inside the library's device image, which every GPU
+ * that loads the library holds until the process exits.  Shapes whose partials need more than that
+ * (paged_attn_workspace_bytes > PA_NOALLOC_SCRATCH_BYTES) return PA_EINVAL and launch nothing;
+ * pass a smaller split_kv.  No call allocates device memory.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress);
+ *     make that first call before any stream capture on that device.
+ *   - All calls share the one array.  Calls that may overlap on the GPU (different streams, or
+ *     different host threads) race on it: serialise them.  Nothing in it needs clearing between
+ *     calls, because each call writes every partial it later reads.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (64ll * 1024 * 1024)
+int paged_attn_fwd_splitkv_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_table, const int32_t *seq_lens, int causal,
+                                   const int32_t *q_offset, int split_kv, float scale, void *out, float *lse,
+                                   const pa_dims *dims, int num_sms, int64_t device_bytes, void *stream);
+
+/*
  * paged_attn_plan — the split plan as data: plan [batch, split_kv, 2] int32 =
  * {first page, one past the last page} of each run (see paged_attn_fwd).
  * seq_lens is a device pointer [batch]; negative lengths count as 0.

@@ -18,7 +18,7 @@ __all__ = [
     "PagedAttnError", "load_library", "library_path", "paged_attn_fwd", "paged_attn_fwd_variant",
     "paged_attn_combine", "paged_attn_plan", "paged_attn_debug_gather", "paged_attn_last_error_word",
     "paged_attn_strerror", "paged_attn_version", "attention", "paged_attn_auto_split",
-    "paged_attn_workspace_bytes", "paged_attn_fwd_splitkv", "PA_F32", "PA_F16", "PA_BF16",
+    "paged_attn_workspace_bytes", "paged_attn_fwd_splitkv", "paged_attn_fwd_splitkv_noalloc", "PA_F32", "PA_F16", "PA_BF16",
     "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL", "VARIANT_TC05_PREFILL",
 ]
 
@@ -70,6 +70,8 @@ def load_library(build_if_missing: bool = False):
     lib.paged_attn_workspace_bytes.restype = ctypes.c_int64
     lib.paged_attn_fwd_splitkv.argtypes = [P, P, P, P, P, I32, P, I32, F, P, P, D, P, I64, I32, I64, P]
     lib.paged_attn_fwd_splitkv.restype = ctypes.c_int
+    lib.paged_attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I32, P, I32, F, P, P, D, I32, I64, P]
+    lib.paged_attn_fwd_splitkv_noalloc.restype = ctypes.c_int
     lib.paged_attn_debug_gather.argtypes = [P, P, P, D, I32, P, P]
     lib.paged_attn_last_error_word.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.paged_attn_strerror.argtypes = [I32]
@@ -218,6 +220,36 @@ def paged_attn_fwd_splitkv(q, k_cache, v_cache, block_table, seq_lens, causal, q
         int(split_kv), float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace), int(ws_bytes),
         int(num_sms), int(device_bytes), _stream(stream))
     _raise(rc, "paged_attn_fwd_splitkv")
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def paged_attn_fwd_splitkv_noalloc(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale,
+                                   out, lse, num_sms=None, device_bytes=None, stream=None) -> None:
+    """``paged_attn_fwd_splitkv`` without a workspace argument, for callers that cannot allocate device
+    memory when they run attention: the split partials use a fixed NOALLOC_SCRATCH_BYTES array inside
+    the library.  Calls that may overlap on the GPU share that array and must be serialised; the first
+    call on a device should come before any stream capture there."""
+    torch = _torch()
+    _check(q, "q", ndim=4)
+    _check(k_cache, "k_cache", q.dtype, 4)
+    _check(v_cache, "v_cache", q.dtype, 4)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    _check(q_offset, "q_offset", torch.int32, 1)
+    _check(out, "out", q.dtype)
+    _check(lse, "lse", torch.float32)
+    dims = dims_of(q, k_cache, block_table)
+    if num_sms is None or device_bytes is None:
+        n, m = _device_info(q.device)
+        num_sms = n if num_sms is None else num_sms
+        device_bytes = m if device_bytes is None else device_bytes
+    rc = load_library().paged_attn_fwd_splitkv_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), int(bool(causal)), _ptr(q_offset),
+        int(split_kv), float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), int(num_sms), int(device_bytes),
+        _stream(stream))
+    _raise(rc, "paged_attn_fwd_splitkv_noalloc")
 
 
 def paged_attn_combine(part_out, part_lse, out, lse=None, stream=None) -> None:
