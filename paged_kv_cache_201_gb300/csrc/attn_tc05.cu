@@ -1,20 +1,22 @@
 // Paged attention on the 5th-generation tensor cores (tcgen05 + tensor memory), sm_103a.
 //
 // For query runs long enough to fill a 128-row tile (prefill, head_dim 128, bf16/f16).
-// One CTA = (sequence b, kv head, split s, tile of 128/G query tokens x the G query
-// heads of the kv head's group), so all 128 rows share every K/V tile:
-//   warp 0      TMA producer: the Q tile once; then, per 128-key tile, the block-table
-//               ids (32 pages per batch, never past the sequence's page count) and one
-//               2-D box per page, half-row and pool into a 2-stage ring.
-//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma from one thread:
-//               S_t = Q K_t^T into one of two S buffers (128 fp32 columns each), then
-//               O += Ph_{t-1} V_{t-1} + Pl_{t-1} V_{t-1} with P read from TMEM.
-//   warps 2-9   softmax, two threads per TMEM lane (query row), 64 columns each: mask (sequence length,
-//               split end, causal reach with q_offset), running max in the log2 domain,
-//               P = exp2(s - m) written back over S as a 16-bit high part and its
-//               rounding remainder.  O is rescaled in TMEM only when the running max
-//               grows by more than 2^8 (otherwise the stale max is kept), and the
-//               -inf - (-inf) and 0/0 guards of rocMLIR PR #2371 apply.
+// A work unit = (sequence b, kv head, split s, tile of 128/G query tokens x the G query heads of
+// the kv head's group), so all 128 rows share every K/V tile.  The kernel is persistent: one CTA
+// per SM walks its units, with
+//   warp 0      TMA producer: each unit's Q tile (double-buffered), then per 128-key tile the
+//               block-table ids (32 pages per batch, never past the sequence's page count) and one
+//               box per page, half-row and pool into 2-slot K and V rings.
+//   warp 1      allocates all 512 TMEM columns and issues tcgen05.mma from one thread:
+//               S_g = Q K_g^T into one of two S buffers (128 fp32 columns each), then
+//               O += Ph_{g-1} V_{g-1} + Pl_{g-1} V_{g-1} with P read from TMEM into one of two O
+//               buffers (one per unit, alternating).
+//   warps 2-9   softmax, two threads per TMEM lane (query row), 64 columns each: mask (sequence
+//               length, split end, causal reach with q_offset), running max in the log2 domain,
+//               P = exp2(s - m) written back over S as a 16-bit high part and its rounding
+//               remainder.  O is rescaled in TMEM only when the running max grows by more than
+//               2^8 (otherwise the stale max is kept), and the -inf - (-inf) and 0/0 guards of
+//               rocMLIR PR #2371 apply.  They finish each unit by reading O out to global memory.
 #include <type_traits>
 
 #include "kernels.h"
@@ -27,17 +29,23 @@ namespace {
 constexpr int kT5Threads = 320;               // 10 warps
 constexpr int kT5Half = 128 * 128;            // bytes of one 64-column half of a 128-row tile
 constexpr int kT5Tile = 2 * kT5Half;          // a 128 x 128 bf16 tile (Q, K or V)
-constexpr int kT5KStages = 3;                 // K ring depth (tiles)
-constexpr int kT5VStages = 2;                 // V ring depth (tiles)
 constexpr uint32_t kT5TmemCols = 512;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = 256;               // O buffers at columns 256 and 384
 constexpr float kRescaleLog2 = 8.f;           // rescale O only when the max grows by > 2^8
 
-// barrier slots
-// B_OD completes once per P V product; B_OF once, after the last one.  A parity wait on B_OD is
-// only unambiguous while it is at most one phase behind, which holds inside the tile loop (Q K^T of
-// tile t completing implies P V of tile t-2 has) but not after it, hence B_OF.
-enum { B_Q = 0, B_KF = 1, B_KE = 4, B_VF = 7, B_VE = 9, B_SF = 11, B_PF = 13, B_OD = 15, B_OF = 16, B_COUNT = 17 };
+// barrier slots (pairs are indexed by buffer / ring slot)
+//   QF/QE  Q buffer full (TMA) / empty (after the unit's last Q K^T)
+//   KF/KE, VF/VE  K and V ring slots full (TMA) / empty (after the product that reads them)
+//   SF/PF  S buffer holds Q K^T / P written back over it (256 softmax threads arrive)
+//   OD     once per P V product; a parity wait on it is exact only while it is at most one
+//          phase behind, which holds inside a unit's tile loop (Q K^T of tile g done implies
+//          P V of tile g-2 done) but not after it, hence
+//   OF     once per use of an O buffer, after the unit's last P V
+//   OFREE  O buffer read out by the softmax threads (256 arrive)
+enum {
+    B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_PF = 14, B_OF = 16, B_OFREE = 18,
+    B_OD = 20, B_COUNT = 21
+};
 
 __device__ __forceinline__ long long t5_row_index(const FwdParams &p, int b, int kvh, int tok, int g) {
     return ((long long)b * p.Sq + tok) * p.Hq + (long long)kvh * p.G + g;
@@ -68,36 +76,42 @@ __device__ __forceinline__ void t5_store_half_row(const FwdParams &p, int s, lon
     }
 }
 
-template <typename T>
-__device__ __forceinline__ void t5_store_row(const FwdParams &p, int s, long long ridx, const float *v, float lse) {
-    if (p.split_kv == 1) {
-        T *o = reinterpret_cast<T *>(p.out) + ridx * 128;
-#pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-            uint4 w;
-            w.x = MmaOp<T>::pack(v[c + 0], v[c + 1]);
-            w.y = MmaOp<T>::pack(v[c + 2], v[c + 3]);
-            w.z = MmaOp<T>::pack(v[c + 4], v[c + 5]);
-            w.w = MmaOp<T>::pack(v[c + 6], v[c + 7]);
-            *reinterpret_cast<uint4 *>(o + c) = w;
-        }
-        if (p.lse) p.lse[ridx] = lse;
-    } else {
-        const long long rows_total = (long long)p.B * p.Sq * p.Hq;
-        float *o = reinterpret_cast<float *>(p.out) + ((long long)s * rows_total + ridx) * 128;
-#pragma unroll
-        for (int c = 0; c < 128; c += 4) *reinterpret_cast<float4 *>(o + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
-        p.lse[(long long)s * rows_total + ridx] = lse;
-    }
-}
-
 }  // namespace
 
+// Everything a role needs to know about one work unit; every role derives it the same way.
+struct T5Unit {
+    int b, kvh, s, L, k_lo, k_hi_split, k_hi, pg0, tok0, tok_end, n_tiles;
+};
+
+__device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, int unit, int tpt, int ps_shift) {
+    T5Unit U;
+    const int ps = 1 << ps_shift;
+    const int rt = unit % p.row_tiles;
+    unit /= p.row_tiles;
+    U.kvh = unit % p.Hkv;
+    unit /= p.Hkv;
+    U.s = unit % p.split_kv;
+    U.b = unit / p.split_kv;
+    U.L = min(max(p.seq_lens[U.b], 0), p.W * ps);
+    int pg1;
+    split_pages(U.L, ps, p.split_kv, U.s, U.pg0, pg1);
+    U.k_lo = U.pg0 * ps;
+    U.k_hi_split = min(pg1 * ps, U.L);
+    U.tok0 = rt * tpt;
+    U.tok_end = min(U.tok0 + tpt, p.Sq);
+    U.k_hi = min(U.k_hi_split, row_key_limit(p, U.b, U.L, U.tok_end - 1));
+    U.n_tiles = U.k_hi > U.k_lo ? (U.k_hi - U.k_lo + 127) / 128 : 0;
+    return U;
+}
+
+// Persistent: CTA c processes units c, c + gridDim.x, ...  Barrier phases and the K / V rings run
+// on the CTA's global tile counter g; Q and O are double-buffered by the CTA's count of non-empty
+// units n, so a unit's epilogue and the next unit's loads overlap its neighbours' work.
 template <typename T>
 __global__ void __launch_bounds__(kT5Threads, 1)
     paged_attn_tc05_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const FwdParams p, int tpt, int ps_shift,
-                           uint32_t idesc_qk, uint32_t idesc_pv) {
+                           uint32_t idesc_qk, uint32_t idesc_pv, int total_units) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[B_COUNT];
     __shared__ uint32_t s_tmem;
@@ -108,61 +122,27 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ps = 1 << ps_shift;
 
-    int unit = blockIdx.x;
-    const int rt = unit % p.row_tiles;
-    unit /= p.row_tiles;
-    const int kvh = unit % p.Hkv;
-    unit /= p.Hkv;
-    const int s = unit % p.split_kv;
-    const int b = unit / p.split_kv;
-
-    int L = max(p.seq_lens[b], 0);
-    if (L > p.W * ps) {
-        if (threadIdx.x == 0) atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
-        L = p.W * ps;
-    }
-    int pg0, pg1;
-    split_pages(L, ps, p.split_kv, s, pg0, pg1);
-    const int k_lo = pg0 * ps;
-    const int k_hi_split = min(pg1 * ps, L);
-    const int tok0 = rt * tpt;
-    const int tok_end = min(tok0 + tpt, p.Sq);
-    const int k_hi = min(k_hi_split, row_key_limit(p, b, L, tok_end - 1));
-    const int n_tiles = k_hi > k_lo ? (k_hi - k_lo + 127) / 128 : 0;
-
-    if (n_tiles == 0) {  // every row of the unit is empty here: output 0, lse -inf
-        const int nrows = (tok_end - tok0) * p.G;
-        float zeros[128];
-#pragma unroll
-        for (int c = 0; c < 128; ++c) zeros[c] = 0.f;
-        for (int r = threadIdx.x; r < nrows; r += kT5Threads)
-            t5_store_row<T>(p, s, t5_row_index(p, b, kvh, tok0 + r / p.G, r % p.G), zeros, kNegInf);
-        return;
-    }
-
+    // shared memory: Q x2 | K x2 | V x2 (128 x 128 tiles, two 64-column swizzled halves each)
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t sQ = sbase;
-    // shared memory: Q | K ring (3 tiles, slot t % 3) | V ring (2 tiles, slot t % 2)
-    auto sK = [&](int ks) { return sbase + (uint32_t)kT5Tile * (1u + (uint32_t)ks); };
-    auto sV = [&](int vs) { return sbase + (uint32_t)kT5Tile * (1u + kT5KStages + (uint32_t)vs); };
+    auto sQ = [&](int qb) { return sbase + (uint32_t)kT5Tile * (uint32_t)qb; };
+    auto sK = [&](int ks) { return sbase + (uint32_t)kT5Tile * (2u + (uint32_t)ks); };
+    auto sV = [&](int vs) { return sbase + (uint32_t)kT5Tile * (4u + (uint32_t)vs); };
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(B_Q), 1);
-        for (int ks = 0; ks < kT5KStages; ++ks) {
-            mbar_init(bar(B_KF + ks), 1);
-            mbar_init(bar(B_KE + ks), 1);
-        }
-        for (int vs = 0; vs < kT5VStages; ++vs) {
-            mbar_init(bar(B_VF + vs), 1);
-            mbar_init(bar(B_VE + vs), 1);
-        }
-        for (int sb = 0; sb < 2; ++sb) {
-            mbar_init(bar(B_SF + sb), 1);
-            mbar_init(bar(B_PF + sb), 256);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_QF + i), 1);
+            mbar_init(bar(B_QE + i), 1);
+            mbar_init(bar(B_KF + i), 1);
+            mbar_init(bar(B_KE + i), 1);
+            mbar_init(bar(B_VF + i), 1);
+            mbar_init(bar(B_VE + i), 1);
+            mbar_init(bar(B_SF + i), 1);
+            mbar_init(bar(B_PF + i), 256);
+            mbar_init(bar(B_OF + i), 1);
+            mbar_init(bar(B_OFREE + i), 256);
         }
         mbar_init(bar(B_OD), 1);
-        mbar_init(bar(B_OF), 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -180,272 +160,331 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            mbar_arrive_expect_tx(bar(B_Q), (uint32_t)kT5Tile);
-            const int qtok = b * p.Sq + tok0;
-            tma_load_4d(sQ, &tmQ, bar(B_Q), 0, 0, kvh * p.G, qtok);
-            tma_load_4d(sQ + kT5Half, &tmQ, bar(B_Q), 0, 1, kvh * p.G, qtok);
         }
         const int ppt = 128 >> ps_shift;                     // pages per tile (divides 32)
         const uint32_t box = (uint32_t)ps * 128u;            // bytes of one page half-row box
-        const int pg_end = (k_hi + ps - 1) >> ps_shift;
-        const int32_t *bt_row = p.block_table + (long long)b * p.W;
-        int batch = pg0;
-        int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
-        int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
         bool bad = false;
-        int issued_k = 0, issued_v = 0;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int ks = t % kT5KStages, vs = t % kT5VStages;
-            const int pg_first = pg0 + t * ppt;
-            if (pg_first >= batch + 32) {
-                batch += 32;
-                id_cur = id_next;
-                const int nx = batch + 32 + lane;
-                id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
+        int n = 0, g0 = 0;                                   // non-empty units so far, global tile base
+        for (int unit = blockIdx.x; unit < total_units && !bad; unit += gridDim.x) {
+            const T5Unit U = t5_unit(p, unit, tpt, ps_shift);
+            if (U.n_tiles == 0) continue;
+            const int qb = n & 1;
+            if (n >= 2) {  // Q buffer free once every Q K^T of unit n-2 is done
+                const bool ok = mbar_wait(bar(B_QE + qb), ((n >> 1) - 1) & 1, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+                if (bad) break;
             }
-            const int id = __shfl_sync(0xffffffffu, id_cur, (pg_first + lane - batch) & 31);
-            const int nvalid = min(ppt, pg_end - pg_first);
-            int tok = 0;
-            if (lane < nvalid) {
-                if (id < 0 || (long long)id >= p.num_pages) {
-                    atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
-                    tok = -ps;  // wholly outside the tensor: reads as zeros
-                } else {
-                    tok = id << ps_shift;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(B_QF + qb), (uint32_t)kT5Tile);
+                const int qtok = U.b * p.Sq + U.tok0;
+                tma_load_4d(sQ(qb), &tmQ, bar(B_QF + qb), 0, 0, U.kvh * p.G, qtok);
+                tma_load_4d(sQ(qb) + kT5Half, &tmQ, bar(B_QF + qb), 0, 1, U.kvh * p.G, qtok);
+            }
+            const int pg_end = (U.k_hi + ps - 1) >> ps_shift;
+            const int32_t *bt_row = p.block_table + (long long)U.b * p.W;
+            int batch = U.pg0;
+            int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
+            int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
+            for (int t = 0; t < U.n_tiles; ++t) {
+                const int g = g0 + t, slot = g & 1;
+                const int pg_first = U.pg0 + t * ppt;
+                if (pg_first >= batch + 32) {
+                    batch += 32;
+                    id_cur = id_next;
+                    const int nx = batch + 32 + lane;
+                    id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
+                }
+                const int id = __shfl_sync(0xffffffffu, id_cur, (pg_first + lane - batch) & 31);
+                const int nvalid = min(ppt, pg_end - pg_first);
+                int tok = 0;
+                if (lane < nvalid) {
+                    if (id < 0 || (long long)id >= p.num_pages) {
+                        atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
+                        tok = -ps;  // wholly outside the tensor: reads as zeros
+                    } else {
+                        tok = id << ps_shift;
+                    }
+                }
+                if (g >= 2) {  // K slot free once Q K^T of tile g-2 is done
+                    const bool ok = mbar_wait(bar(B_KE + slot), ((g >> 1) - 1) & 1, p.err);
+                    bad = __any_sync(0xffffffffu, !ok);
+                    if (bad) break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(bar(B_KF + slot), (uint32_t)nvalid * 2u * box);
+                __syncwarp();
+                if (lane < nvalid) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(sK(slot) + (uint32_t)h * kT5Half + (uint32_t)lane * box, &tmK, bar(B_KF + slot), 0,
+                                    tok, h, U.kvh);
+                }
+                if (g >= 2) {  // V slot free once P V of tile g-2 is done
+                    const bool ok = mbar_wait(bar(B_VE + slot), ((g >> 1) - 1) & 1, p.err);
+                    bad = __any_sync(0xffffffffu, !ok);
+                    if (bad) break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(bar(B_VF + slot), (uint32_t)nvalid * 2u * box);
+                __syncwarp();
+                if (lane < nvalid) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_4d(sV(slot) + (uint32_t)h * kT5Half + (uint32_t)lane * box, &tmV, bar(B_VF + slot), 0,
+                                    tok, h, U.kvh);
                 }
             }
-            // K slot: freed once Q K^T of tile t-3 has completed
-            if (t >= kT5KStages && !bad) {
-                const bool ok = mbar_wait(bar(B_KE + ks), ((t / kT5KStages) - 1) & 1, p.err);
-                bad = __any_sync(0xffffffffu, !ok);
-            }
-            if (bad) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(B_KF + ks), (uint32_t)nvalid * 2u * box);
-            __syncwarp();
-            if (lane < nvalid) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sK(ks) + (uint32_t)h * kT5Half + (uint32_t)lane * box, &tmK, bar(B_KF + ks), 0, tok, h,
-                                kvh);
-            }
-            issued_k = t + 1;
-            // V slot: freed once P V of tile t-2 has completed
-            if (t >= kT5VStages && !bad) {
-                const bool ok = mbar_wait(bar(B_VE + vs), ((t / kT5VStages) - 1) & 1, p.err);
-                bad = __any_sync(0xffffffffu, !ok);
-            }
-            if (bad) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(B_VF + vs), (uint32_t)nvalid * 2u * box);
-            __syncwarp();
-            if (lane < nvalid) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    tma_load_4d(sV(vs) + (uint32_t)h * kT5Half + (uint32_t)lane * box, &tmV, bar(B_VF + vs), 0, tok, h,
-                                kvh);
-            }
-            issued_v = t + 1;
+            g0 += U.n_tiles;
+            ++n;
         }
-        // no copy may outlive the CTA: wait (bounded) for the last phase armed on each slot
-        for (int t = max(0, issued_k - kT5KStages); t < issued_k; ++t)
-            mbar_wait(bar(B_KF + t % kT5KStages), (t / kT5KStages) & 1, p.err);
-        for (int t = max(0, issued_v - kT5VStages); t < issued_v; ++t)
-            mbar_wait(bar(B_VF + t % kT5VStages), (t / kT5VStages) & 1, p.err);
-        if (lane == 0) mbar_wait(bar(B_Q), 0, p.err);
+        // No copy may outlive the CTA: wait (bounded) for the last phase armed on every slot.  After a
+        // time-out some of these were never armed; their waits then give up too.
+        if (!bad) {
+            for (int g = max(0, g0 - 2); g < g0; ++g) {
+                mbar_wait(bar(B_KF + (g & 1)), (g >> 1) & 1, p.err);
+                mbar_wait(bar(B_VF + (g & 1)), (g >> 1) & 1, p.err);
+            }
+            for (int k = max(0, n - 2); k < n; ++k) mbar_wait(bar(B_QF + (k & 1)), (k >> 1) & 1, p.err);
+        }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0) {
-            bool bad = !mbar_wait(bar(B_Q), 0, p.err);
-            for (int t = 0; t <= n_tiles && !bad; ++t) {
-                if (t < n_tiles) {
-                    const int sb = t & 1, ks = t % kT5KStages;
-                    if (!mbar_wait(bar(B_KF + ks), (t / kT5KStages) & 1, p.err)) { bad = true; break; }
+            bool bad = false;
+            // P V of tile g is issued after Q K^T of tile g+1 (which may belong to the next unit)
+            bool pend = false;
+            int pg = 0, pn = 0;
+            bool pfirst = false, plast = false;
+            auto issue_pv = [&](int g, int un, bool first, bool last) -> bool {
+                const int slot = g & 1, ob = un & 1;
+                if (!mbar_wait(bar(B_PF + slot), (g >> 1) & 1, p.err)) return false;
+                if (!mbar_wait(bar(B_VF + slot), (g >> 1) & 1, p.err)) return false;
+                if (first && un >= 2 && !mbar_wait(bar(B_OFREE + ob), ((un >> 1) - 1) & 1, p.err)) return false;
+                tc05::fence_after_sync();
+                const uint32_t pcol = tmem + (slot ? 128u : 0u);
+                const uint32_t ocol = tmem + kColO + 128u * (uint32_t)ob;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t vd = tc05::smem_desc_sw128(sV(slot) + (uint32_t)kk * 2048u, (uint32_t)kT5Half, 1024);
+                    // keys 16kk..16kk+15: chunk kk/2 of 32 keys; highs at +0, remainders at +16
+                    const uint32_t pa = pcol + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
+                    tc05::mma_ts(ocol, pa, vd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                    tc05::mma_ts(ocol, pa + 16u, vd, idesc_pv, 1u);
+                }
+                tc05::commit(bar(B_VE + slot));
+                tc05::commit(bar(B_OD));
+                if (last) tc05::commit(bar(B_OF + ob));
+                return true;
+            };
+            int n = 0, g0 = 0;
+            for (int unit = blockIdx.x; unit < total_units && !bad; unit += gridDim.x) {
+                const T5Unit U = t5_unit(p, unit, tpt, ps_shift);
+                if (U.n_tiles == 0) continue;
+                const int qb = n & 1;
+                if (!mbar_wait(bar(B_QF + qb), (n >> 1) & 1, p.err)) { bad = true; break; }
+                for (int t = 0; t < U.n_tiles; ++t) {
+                    const int g = g0 + t, slot = g & 1;
+                    if (!mbar_wait(bar(B_KF + slot), (g >> 1) & 1, p.err)) { bad = true; break; }
                     tc05::fence_after_sync();
-                    const uint32_t d = tmem + (sb ? 128u : 0u);
+                    const uint32_t d = tmem + (slot ? 128u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (uint32_t)(kk >> 2) * kT5Half + (uint32_t)(kk & 3) * 32u;
-                        tc05::mma_ss(d, tc05::smem_desc_sw128(sQ + off, 16, 1024),
-                                     tc05::smem_desc_sw128(sK(ks) + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                        tc05::mma_ss(d, tc05::smem_desc_sw128(sQ(qb) + off, 16, 1024),
+                                     tc05::smem_desc_sw128(sK(slot) + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                     }
-                    tc05::commit(bar(B_KE + ks));   // K slot reusable once this product is done
-                    tc05::commit(bar(B_SF + sb));
+                    tc05::commit(bar(B_KE + slot));   // K slot reusable once this product is done
+                    tc05::commit(bar(B_SF + slot));
+                    if (t == U.n_tiles - 1) tc05::commit(bar(B_QE + qb));
+                    if (pend && !issue_pv(pg, pn, pfirst, plast)) { bad = true; break; }
+                    pend = true;
+                    pg = g;
+                    pn = n;
+                    pfirst = t == 0;
+                    plast = t == U.n_tiles - 1;
                 }
-                if (t >= 1) {
-                    const int u = t - 1, su = u & 1, ku = u % kT5VStages;
-                    if (!mbar_wait(bar(B_PF + su), (u >> 1) & 1, p.err)) { bad = true; break; }
-                    if (!mbar_wait(bar(B_VF + ku), (u / kT5VStages) & 1, p.err)) { bad = true; break; }
-                    tc05::fence_after_sync();
-                    const uint32_t pcol = tmem + (su ? 128u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t vd =
-                            tc05::smem_desc_sw128(sV(ku) + (uint32_t)kk * 2048u, (uint32_t)kT5Half, 1024);
-                        // keys 16kk..16kk+15: chunk kk/2 of 32 keys; highs at +0, remainders at +16
-                        const uint32_t pa = pcol + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
-                        tc05::mma_ts(tmem + kColO, pa, vd, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
-                        tc05::mma_ts(tmem + kColO, pa + 16u, vd, idesc_pv, 1u);
-                    }
-                    tc05::commit(bar(B_VE + ku));
-                    tc05::commit(bar(B_OD));
-                    if (u == n_tiles - 1) tc05::commit(bar(B_OF));
-                }
+                g0 += U.n_tiles;
+                ++n;
             }
+            if (!bad && pend) issue_pv(pg, pn, pfirst, plast);
         }
         __syncwarp();
     } else {
         // ================================================================ softmax (warps 2-9)
         // Two warpgroups share every row: group hh (warps 2-5: hh = 0, warps 6-9: hh = 1) owns
         // score columns / keys [64 hh, 64 hh + 64) and output columns [64 hh, 64 hh + 64).  They
-        // exchange the row maximum once per tile and the row sum once at the end; both keep the
-        // same running maximum, so the rescale decisions agree.  Every named barrier is reached on
-        // every path (a warp that gave up on a wait still walks the loop), so none can hang.
+        // exchange the row maximum once per tile and the row sum once per unit; both keep the same
+        // running maximum, so the rescale decisions agree.  Every named barrier is reached on every
+        // path (a warp that gave up on a wait still walks the loops), so none can hang.
         const int hh = (warp - 2) >> 2;
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;                       // TMEM lane = query row of the tile
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-        const int tk = tok0 + r / p.G;
-        const int g = r % p.G;
-        const bool row_valid = tk < tok_end;
-        const int lim = row_valid ? min(k_hi_split, row_key_limit(p, b, L, tk)) : k_lo;
-        float m_used = kNegInf, l = 0.f;
         bool bad = false;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int st = t & 1;
-            if (!bad) {
-                const bool ok = mbar_wait(bar(B_SF + st), (t >> 1) & 1, p.err);
+        int n = 0, g0 = 0;
+        for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x) {
+            const T5Unit U = t5_unit(p, unit, tpt, ps_shift);
+            if (threadIdx.x == 64 && U.s == 0 && U.tok0 == 0 && p.seq_lens[U.b] > p.W * ps)
+                atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
+            const int tk = U.tok0 + r / p.G;
+            const int gq = r % p.G;
+            const bool row_valid = tk < U.tok_end;
+            if (U.n_tiles == 0) {  // no valid key for any row of the unit: output 0, lse -inf
+                if (row_valid) {
+                    float zeros[64];
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) zeros[c] = 0.f;
+                    t5_store_half_row<T>(p, U.s, t5_row_index(p, U.b, U.kvh, tk, gq), hh, zeros, kNegInf);
+                }
+                continue;
+            }
+            const int ob = n & 1;
+            const uint32_t ocol = kColO + 128u * (uint32_t)ob;
+            const int lim = row_valid ? min(U.k_hi_split, row_key_limit(p, U.b, U.L, tk)) : U.k_lo;
+            float m_used = kNegInf, l = 0.f;
+            for (int t = 0; t < U.n_tiles; ++t) {
+                const int g = g0 + t, st = g & 1;
+                if (!bad) {
+                    const bool ok = mbar_wait(bar(B_SF + st), (g >> 1) & 1, p.err);
+                    bad = __any_sync(0xffffffffu, !ok);
+                }
+                tc05::fence_after_sync();
+                const uint32_t sbuf = tmem + lane_addr + (st ? 128u : 0u);
+                const int tile_k0 = U.k_lo + t * 128;
+                const int nvalid_row = lim - tile_k0;       // keys [0, nvalid_row) of the tile are valid here
+                // pass 1: maximum of this row's valid raw scores in my 64 columns (scale > 0 commutes with max)
+                float mx = kNegInf;
+                if (!bad) {
+#pragma unroll 1
+                    for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
+                        uint32_t u[32];
+                        tc05::ld_32cols(sbuf + 32u * c, u);
+                        tc05::wait_ld();
+                        const int nv = nvalid_row - 32 * c;
+                        if (nv >= 32) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(u[j]));
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) mx = (j < nv) ? fmaxf(mx, __uint_as_float(u[j])) : mx;
+                        }
+                    }
+                }
+                s_xmax[st][hh][r] = mx;
+                named_bar_sync(2, 256);
+                mx = fmaxf(mx, s_xmax[st][hh ^ 1][r]);
+                const float m_new = fmaxf(m_used, mx * p.scale_log2);
+                const bool need = m_new > m_used + kRescaleLog2;  // also true when m_used is -inf and m_new is not
+                if (__any_sync(0xffffffffu, need) && !bad) {
+                    const float alpha = need ? exp2f(m_used - m_new) : 1.f;
+                    if (need) {
+                        l *= alpha;
+                        m_used = m_new;
+                    }
+                    if (t > 0) {
+                        // O holds P V of this unit's earlier tiles: wait for the last one (tile g-1; Q K^T
+                        // of tile g having completed, P V of g-2 has, so the parity wait is exact), then
+                        // rescale my half of the row
+                        const bool ok = mbar_wait(bar(B_OD), (g - 1) & 1, p.err);
+                        bad = __any_sync(0xffffffffu, !ok);
+                        if (!bad) {
+                            tc05::fence_after_sync();
+#pragma unroll 1
+                            for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
+                                uint32_t o[32];
+                                tc05::ld_32cols(tmem + lane_addr + ocol + 32u * c, o);
+                                tc05::wait_ld();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                                tc05::st_32cols(tmem + lane_addr + ocol + 32u * c, o);
+                            }
+                        }
+                    }
+                }
+                if (!bad) {
+                    // pass 2: P = exp2(scale_log2 * s - m) for 32 keys at a time, stored over the same 32
+                    // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs)
+                    const float nmu = (m_used == kNegInf) ? 0.f : -m_used;  // -inf - (-inf) guard
+                    const float c2 = p.scale_log2;
+#pragma unroll 1
+                    for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
+                        uint32_t u[32];
+                        tc05::ld_32cols(sbuf + 32u * c, u);
+                        tc05::wait_ld();
+                        const int nv = nvalid_row - 32 * c;
+                        uint32_t hi[16], lo[16];
+                        if (nv >= 32) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * i]), c2, nmu));
+                                const float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu));
+                                l += p0 + p1;
+                                hi[i] = MmaOp<T>::pack(p0, p1);
+                                const float2 h2 = MmaOp<T>::unpack(hi[i]);
+                                lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float a0 = (2 * i < nv) ? fmaf(__uint_as_float(u[2 * i]), c2, nmu) : kNegInf;
+                                const float a1 =
+                                    (2 * i + 1 < nv) ? fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu) : kNegInf;
+                                const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+                                l += p0 + p1;
+                                hi[i] = MmaOp<T>::pack(p0, p1);
+                                const float2 h2 = MmaOp<T>::unpack(hi[i]);
+                                lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+                            }
+                        }
+                        tc05::st_16cols(sbuf + 32u * c, hi);
+                        tc05::st_16cols(sbuf + 32u * c + 16u, lo);
+                    }
+                    tc05::wait_st();
+                }
+                if (t == U.n_tiles - 1 && tile_k0 + 128 > U.k_hi) {
+                    // Keys at or past k_hi (past the sequence or never loaded) may hold any bits: their
+                    // weight is 0 but 0 * NaN is NaN, so zero those V rows (my half of each) before P V.
+                    if (!bad) {
+                        const bool ok = mbar_wait(bar(B_VF + st), (g >> 1) & 1, p.err);
+                        bad = __any_sync(0xffffffffu, !ok);
+                    }
+                    if (!bad && tile_k0 + r >= U.k_hi) {
+                        const uint32_t a = sV(st) + (uint32_t)hh * kT5Half + (uint32_t)r * 128u;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a + 16u * c), "r"(0u)
+                                         : "memory");
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc05::fence_before_sync();
+                mbar_arrive(bar(B_PF + st));
+            }
+            if (!bad) {  // the unit's last P V (a dedicated barrier: exact whatever B_OD's phase)
+                const bool ok = mbar_wait(bar(B_OF + ob), (n >> 1) & 1, p.err);
                 bad = __any_sync(0xffffffffu, !ok);
             }
-            tc05::fence_after_sync();
-            const uint32_t sbuf = tmem + lane_addr + (st ? 128u : 0u);
-            const int tile_k0 = k_lo + t * 128;
-            const int nvalid_row = lim - tile_k0;           // keys [0, nvalid_row) of the tile are valid here
-            // pass 1: maximum of this row's valid raw scores in my 64 columns (scale > 0 commutes with max)
-            float mx = kNegInf;
-            if (!bad) {
-#pragma unroll 1
-                for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
-                    uint32_t u[32];
-                    tc05::ld_32cols(sbuf + 32u * c, u);
-                    tc05::wait_ld();
-                    const int nv = nvalid_row - 32 * c;
-                    if (nv >= 32) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(u[j]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) mx = (j < nv) ? fmaxf(mx, __uint_as_float(u[j])) : mx;
-                    }
-                }
-            }
-            s_xmax[st][hh][r] = mx;
+            s_xsum[hh][r] = l;
+            s_xbad[hh][r] = bad ? 1 : 0;
             named_bar_sync(2, 256);
-            mx = fmaxf(mx, s_xmax[st][hh ^ 1][r]);
-            const float m_new = fmaxf(m_used, mx * p.scale_log2);
-            const bool need = m_new > m_used + kRescaleLog2;  // also true when m_used is -inf and m_new is not
-            if (__any_sync(0xffffffffu, need) && !bad) {
-                const float alpha = need ? exp2f(m_used - m_new) : 1.f;
-                if (need) {
-                    l *= alpha;
-                    m_used = m_new;
-                }
-                if (t > 0) {
-                    // O holds P V of earlier tiles: wait for the last one, then rescale my half of the row
-                    const bool ok = mbar_wait(bar(B_OD), (t - 1) & 1, p.err);
-                    bad = __any_sync(0xffffffffu, !ok);
-                    if (!bad) {
-                        tc05::fence_after_sync();
-#pragma unroll 1
-                        for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
-                            uint32_t o[32];
-                            tc05::ld_32cols(tmem + lane_addr + kColO + 32u * c, o);
-                            tc05::wait_ld();
+            const float l_tot = l + s_xsum[hh ^ 1][r];
+            if (!bad && !s_xbad[hh ^ 1][r]) {
+                tc05::fence_after_sync();
+                const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                float o[64];
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                            tc05::st_32cols(tmem + lane_addr + kColO + 32u * c, o);
-                        }
-                    }
-                }
-            }
-            if (!bad) {
-                // pass 2: P = exp2(scale_log2 * s - m) for 32 keys at a time, stored over the same 32
-                // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs)
-                const float nmu = (m_used == kNegInf) ? 0.f : -m_used;  // -inf - (-inf) guard
-                const float c2 = p.scale_log2;
-#pragma unroll 1
-                for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t u[32];
-                    tc05::ld_32cols(sbuf + 32u * c, u);
+                    tc05::ld_32cols(tmem + lane_addr + ocol + 32u * (2 * hh + c), u);
                     tc05::wait_ld();
-                    const int nv = nvalid_row - 32 * c;
-                    uint32_t hi[16], lo[16];
-                    if (nv >= 32) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * i]), c2, nmu));
-                            const float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu));
-                            l += p0 + p1;
-                            hi[i] = MmaOp<T>::pack(p0, p1);
-                            const float2 h2 = MmaOp<T>::unpack(hi[i]);
-                            lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float a0 = (2 * i < nv) ? fmaf(__uint_as_float(u[2 * i]), c2, nmu) : kNegInf;
-                            const float a1 = (2 * i + 1 < nv) ? fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu) : kNegInf;
-                            const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
-                            l += p0 + p1;
-                            hi[i] = MmaOp<T>::pack(p0, p1);
-                            const float2 h2 = MmaOp<T>::unpack(hi[i]);
-                            lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
-                        }
-                    }
-                    tc05::st_16cols(sbuf + 32u * c, hi);
-                    tc05::st_16cols(sbuf + 32u * c + 16u, lo);
+                    for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(u[j]) * inv;
                 }
-                tc05::wait_st();
-            }
-            if (t == n_tiles - 1 && tile_k0 + 128 > k_hi) {
-                // Keys at or past k_hi (past the sequence or never loaded) may hold any bits: their
-                // weight is 0 but 0 * NaN is NaN, so zero those V rows (my half of each) before P V.
-                if (!bad) {
-                    const bool ok = mbar_wait(bar(B_VF + t % kT5VStages), (t / kT5VStages) & 1, p.err);
-                    bad = __any_sync(0xffffffffu, !ok);
-                }
-                if (!bad && tile_k0 + r >= k_hi) {
-                    const uint32_t a = sV(t % kT5VStages) + (uint32_t)hh * kT5Half + (uint32_t)r * 128u;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a + 16u * c), "r"(0u) : "memory");
-                }
-                fence_proxy_async_smem();
+                if (row_valid)
+                    t5_store_half_row<T>(p, U.s, t5_row_index(p, U.b, U.kvh, tk, gq), hh, o,
+                                         l_tot > 0.f ? m_used * kLn2 + logf(l_tot) : kNegInf);
             }
             tc05::fence_before_sync();
-            mbar_arrive(bar(B_PF + st));
-        }
-        if (!bad) {
-            const bool ok = mbar_wait(bar(B_OF), 0, p.err);
-            bad = __any_sync(0xffffffffu, !ok);
-        }
-        s_xsum[hh][r] = l;
-        s_xbad[hh][r] = bad ? 1 : 0;
-        named_bar_sync(2, 256);
-        const float l_tot = l + s_xsum[hh ^ 1][r];
-        if (!bad && !s_xbad[hh ^ 1][r]) {
-            tc05::fence_after_sync();
-            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-            float o[64];
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t u[32];
-                tc05::ld_32cols(tmem + lane_addr + kColO + 32u * (2 * hh + c), u);
-                tc05::wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(u[j]) * inv;
-            }
-            if (row_valid)
-                t5_store_half_row<T>(p, s, t5_row_index(p, b, kvh, tk, g), hh, o,
-                                     l_tot > 0.f ? m_used * kLn2 + logf(l_tot) : kNegInf);
+            mbar_arrive(bar(B_OFREE + ob));  // O buffer ob may take unit n+2's products
+            g0 += U.n_tiles;
+            ++n;
         }
     }
 
@@ -458,7 +497,19 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 }
 
 // ------------------------------------------------------------------------ host side
-size_t tc05_smem_bytes() { return (size_t)(kT5Tile * (1 + kT5KStages + kT5VStages) + 1024); }
+size_t tc05_smem_bytes() { return (size_t)(kT5Tile * 6 + 1024); }
+
+static int num_sms_of_current_device() {
+    static int cached[128];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+    if (!cached[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
 
 template <typename T>
 static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, const CUtensorMap &tmk,
@@ -475,10 +526,13 @@ static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, con
     const long long units = (long long)p.B * p.split_kv * p.Hkv * q.row_tiles;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int sms = num_sms_of_current_device();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = (int)(units < sms ? units : sms);
     const bool bf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t iqk = tc05::idesc_f16(bf, false, 128, 128);
     const uint32_t ipv = tc05::idesc_f16(bf, true, 128, 128);
-    kern<<<(unsigned)units, kT5Threads, smem, stream>>>(tmq, tmk, tmv, q, tpt, ps_shift, iqk, ipv);
+    kern<<<grid, kT5Threads, smem, stream>>>(tmq, tmk, tmv, q, tpt, ps_shift, iqk, ipv, (int)units);
     return cudaGetLastError();
 }
 

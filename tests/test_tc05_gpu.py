@@ -94,3 +94,17 @@ def test_tc05_out_of_range_page(pa):
     rows[:, 0] = 1
     ref = oracle.workload_rows(wl, split_kv=1, row_bih=rows)
     _gpu.assert_close(res["out"][1].reshape(-1, wl.D), ref["out"], "bf16", "unaffected sequence")
+
+
+def test_tc05_many_units_per_cta(pa):
+    """More work units than SMs: each persistent CTA walks several units (ragged causal lengths,
+    empty and partial splits), so the cross-unit pipeline (Q and O double buffers) is exercised."""
+    rng = np.random.default_rng(211)
+    B, Sq = 8, 256
+    qo = rng.integers(0, 300, size=B).tolist()
+    lens = [o + Sq for o in qo]
+    wl = W.make_custom(dtype="bf16", B=B, Sq=Sq, Hq=16, Hkv=2, D=128, page_size=16, seq_lens=lens, causal=True,
+                       q_offset=qo, seed=212)
+    for S in (4, 1):
+        _check(wl, S, f"tc05 many units S={S}")
+    assert pa.paged_attn_last_error_word() == 0
