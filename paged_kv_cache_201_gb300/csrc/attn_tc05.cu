@@ -78,6 +78,39 @@ __device__ __forceinline__ void t5_store_half_row(const FwdParams &p, int s, lon
 
 }  // namespace
 
+// P for 32 keys of one row: p = exp2(s * c2 + nmu) for the nv (may be <= 0 or >= 32) valid keys, 0
+// for the rest; l accumulates the p; the 32 columns at `taddr` receive [16 columns of high parts |
+// 16 columns of remainders] (bf16/f16 pairs).
+template <typename T>
+__device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], int nv, float c2, float nmu, float &l,
+                                             uint32_t taddr) {
+    uint32_t hi[16], lo[16];
+    if (nv >= 32) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * i]), c2, nmu));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu));
+            l += p0 + p1;
+            hi[i] = MmaOp<T>::pack(p0, p1);
+            const float2 h2 = MmaOp<T>::unpack(hi[i]);
+            lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float a0 = (2 * i < nv) ? fmaf(__uint_as_float(u[2 * i]), c2, nmu) : kNegInf;
+            const float a1 = (2 * i + 1 < nv) ? fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu) : kNegInf;
+            const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+            l += p0 + p1;
+            hi[i] = MmaOp<T>::pack(p0, p1);
+            const float2 h2 = MmaOp<T>::unpack(hi[i]);
+            lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+        }
+    }
+    tc05::st_16cols(taddr, hi);
+    tc05::st_16cols(taddr + 16u, lo);
+}
+
 // Everything a role needs to know about one work unit; every role derives it the same way.
 struct T5Unit {
     int b, kvh, s, L, k_lo, k_hi_split, k_hi, pg0, tok0, tok_end, n_tiles;
@@ -349,21 +382,23 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 const uint32_t sbuf = tmem + lane_addr + (st ? 128u : 0u);
                 const int tile_k0 = U.k_lo + t * 128;
                 const int nvalid_row = lim - tile_k0;       // keys [0, nvalid_row) of the tile are valid here
-                // pass 1: maximum of this row's valid raw scores in my 64 columns (scale > 0 commutes with max)
+                // my 64 score columns: two 32-column loads, one wait; kept in registers for both passes
+                uint32_t ua[32], ub[32];
                 float mx = kNegInf;
                 if (!bad) {
-#pragma unroll 1
-                    for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
-                        uint32_t u[32];
-                        tc05::ld_32cols(sbuf + 32u * c, u);
-                        tc05::wait_ld();
-                        const int nv = nvalid_row - 32 * c;
-                        if (nv >= 32) {
+                    tc05::ld_32cols(sbuf + 64u * hh, ua);
+                    tc05::ld_32cols(sbuf + 64u * hh + 32u, ub);
+                    tc05::wait_ld();
+                    // pass 1: maximum of this row's valid raw scores (scale > 0 commutes with max)
+                    const int nv = nvalid_row - 64 * hh;
+                    if (nv >= 64) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(u[j]));
-                        } else {
+                        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fmaxf(__uint_as_float(ua[j]), __uint_as_float(ub[j])));
+                    } else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) mx = (j < nv) ? fmaxf(mx, __uint_as_float(u[j])) : mx;
+                        for (int j = 0; j < 32; ++j) {
+                            mx = (j < nv) ? fmaxf(mx, __uint_as_float(ua[j])) : mx;
+                            mx = (j + 32 < nv) ? fmaxf(mx, __uint_as_float(ub[j])) : mx;
                         }
                     }
                 }
@@ -403,39 +438,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs)
                     const float nmu = (m_used == kNegInf) ? 0.f : -m_used;  // -inf - (-inf) guard
                     const float c2 = p.scale_log2;
-#pragma unroll 1
-                    for (int c = 2 * hh; c < 2 * hh + 2; ++c) {
-                        uint32_t u[32];
-                        tc05::ld_32cols(sbuf + 32u * c, u);
-                        tc05::wait_ld();
-                        const int nv = nvalid_row - 32 * c;
-                        uint32_t hi[16], lo[16];
-                        if (nv >= 32) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * i]), c2, nmu));
-                                const float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu));
-                                l += p0 + p1;
-                                hi[i] = MmaOp<T>::pack(p0, p1);
-                                const float2 h2 = MmaOp<T>::unpack(hi[i]);
-                                lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float a0 = (2 * i < nv) ? fmaf(__uint_as_float(u[2 * i]), c2, nmu) : kNegInf;
-                                const float a1 =
-                                    (2 * i + 1 < nv) ? fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu) : kNegInf;
-                                const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
-                                l += p0 + p1;
-                                hi[i] = MmaOp<T>::pack(p0, p1);
-                                const float2 h2 = MmaOp<T>::unpack(hi[i]);
-                                lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
-                            }
-                        }
-                        tc05::st_16cols(sbuf + 32u * c, hi);
-                        tc05::st_16cols(sbuf + 32u * c + 16u, lo);
-                    }
+                    t5_exp_chunk<T>(ua, nvalid_row - 64 * hh, c2, nmu, l, sbuf + 64u * hh);
+                    t5_exp_chunk<T>(ub, nvalid_row - 64 * hh - 32, c2, nmu, l, sbuf + 64u * hh + 32u);
                     tc05::wait_st();
                 }
                 if (t == U.n_tiles - 1 && tile_k0 + 128 > U.k_hi) {
