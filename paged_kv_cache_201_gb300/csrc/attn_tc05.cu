@@ -85,12 +85,13 @@ template <typename T>
 __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], int nv, float c2, float nmu, float &l,
                                              uint32_t taddr) {
     uint32_t hi[16], lo[16];
+    float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
     if (nv >= 32) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * i]), c2, nmu));
             const float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu));
-            l += p0 + p1;
+            l4[i & 3] += p0 + p1;
             hi[i] = MmaOp<T>::pack(p0, p1);
             const float2 h2 = MmaOp<T>::unpack(hi[i]);
             lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
@@ -101,12 +102,13 @@ __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], int nv, fl
             const float a0 = (2 * i < nv) ? fmaf(__uint_as_float(u[2 * i]), c2, nmu) : kNegInf;
             const float a1 = (2 * i + 1 < nv) ? fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu) : kNegInf;
             const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
-            l += p0 + p1;
+            l4[i & 3] += p0 + p1;
             hi[i] = MmaOp<T>::pack(p0, p1);
             const float2 h2 = MmaOp<T>::unpack(hi[i]);
             lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
         }
     }
+    l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
     tc05::st_16cols(taddr, hi);
     tc05::st_16cols(taddr + 16u, lo);
 }
@@ -390,17 +392,22 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     tc05::ld_32cols(sbuf + 64u * hh + 32u, ub);
                     tc05::wait_ld();
                     // pass 1: maximum of this row's valid raw scores (scale > 0 commutes with max)
+                    // four independent running maxima (max is exact, so the grouping does not matter)
                     const int nv = nvalid_row - 64 * hh;
+                    float m4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
                     if (nv >= 64) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fmaxf(__uint_as_float(ua[j]), __uint_as_float(ub[j])));
+                        for (int j = 0; j < 32; ++j)
+                            m4[j & 3] = fmaxf(m4[j & 3], fmaxf(__uint_as_float(ua[j]), __uint_as_float(ub[j])));
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            mx = (j < nv) ? fmaxf(mx, __uint_as_float(ua[j])) : mx;
-                            mx = (j + 32 < nv) ? fmaxf(mx, __uint_as_float(ub[j])) : mx;
+                            const float a = (j < nv) ? __uint_as_float(ua[j]) : kNegInf;
+                            const float c = (j + 32 < nv) ? __uint_as_float(ub[j]) : kNegInf;
+                            m4[j & 3] = fmaxf(m4[j & 3], fmaxf(a, c));
                         }
                     }
+                    mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 }
                 s_xmax[st][hh][r] = mx;
                 named_bar_sync(2, 256);
