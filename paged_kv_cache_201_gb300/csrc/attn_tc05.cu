@@ -200,9 +200,26 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         const uint32_t box = (uint32_t)ps * 128u;            // bytes of one page half-row box
         bool bad = false;
         int n = 0, g0 = 0;                                   // non-empty units so far, global tile base
-        for (int unit = blockIdx.x; unit < total_units && !bad; unit += gridDim.x) {
+        // The first id batch of the next non-empty unit is loaded one unit ahead, so its latency
+        // hides behind the current unit's copies.
+        auto next_unit = [&](int from) {
+            int u = from;
+            while (u < total_units && t5_unit(p, u, tpt, ps_shift).n_tiles == 0) u += gridDim.x;
+            return u;
+        };
+        auto first_ids = [&](int u) {
+            if (u >= total_units) return 0;
+            const T5Unit V = t5_unit(p, u, tpt, ps_shift);
+            const int pe = (V.k_hi + ps - 1) >> ps_shift;
+            return (V.pg0 + lane < pe) ? __ldg(p.block_table + (long long)V.b * p.W + V.pg0 + lane) : 0;
+        };
+        int unit = next_unit(blockIdx.x);
+        int ids_pref = first_ids(unit);
+        for (; unit < total_units && !bad;) {
             const T5Unit U = t5_unit(p, unit, tpt, ps_shift);
-            if (U.n_tiles == 0) continue;
+            const int unit_next = next_unit(unit + gridDim.x);
+            const int ids_now = ids_pref;
+            ids_pref = first_ids(unit_next);
             const int qb = n & 1;
             if (n >= 2) {  // Q buffer free once every Q K^T of unit n-2 is done
                 const bool ok = mbar_wait(bar(B_QE + qb), ((n >> 1) - 1) & 1, p.err);
@@ -218,7 +235,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             const int pg_end = (U.k_hi + ps - 1) >> ps_shift;
             const int32_t *bt_row = p.block_table + (long long)U.b * p.W;
             int batch = U.pg0;
-            int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
+            int id_cur = ids_now;
             int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
             for (int t = 0; t < U.n_tiles; ++t) {
                 const int g = g0 + t, slot = g & 1;
@@ -269,6 +286,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             }
             g0 += U.n_tiles;
             ++n;
+            unit = unit_next;
         }
         // No copy may outlive the CTA: wait (bounded) for the last phase armed on every slot.  After a
         // time-out some of these were never armed; their waits then give up too.
@@ -335,10 +353,13 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     pfirst = t == 0;
                     plast = t == U.n_tiles - 1;
                 }
+                // The unit's last P V goes out now rather than behind the next unit's first Q K^T,
+                // which may still be waiting for its loads: the softmax read-out of this unit waits on it.
+                if (!bad && pend && !issue_pv(pg, pn, pfirst, plast)) bad = true;
+                pend = false;
                 g0 += U.n_tiles;
                 ++n;
             }
-            if (!bad && pend) issue_pv(pg, pn, pfirst, plast);
         }
         __syncwarp();
     } else {
