@@ -32,6 +32,7 @@ constexpr int kT5Tile = 2 * kT5Half;          // a 128 x 128 bf16 tile (Q, K or 
 constexpr uint32_t kT5TmemCols = 512;
 constexpr uint32_t kColO = 256;               // O buffers at columns 256 and 384
 constexpr float kRescaleLog2 = 8.f;           // rescale O only when the max grows by > 2^8
+constexpr int kT5StageLens = 1024;            // batches up to this size keep seq_lens / q_offset in smem
 
 // barrier slots (pairs are indexed by buffer / ring slot)
 //   QF/QE  Q buffer full (TMA) / empty (after the unit's last Q K^T)
@@ -118,7 +119,21 @@ struct T5Unit {
     int b, kvh, s, L, k_lo, k_hi_split, k_hi, pg0, tok0, tok_end, n_tiles;
 };
 
-__device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, int unit, int tpt, int ps_shift) {
+// seq_lens / q_offset as staged by the CTA (shared memory when the batch fits, else global).
+struct T5Lens {
+    const int32_t *seq_lens;
+    const int32_t *q_offset;  // null: seq_lens[b] - Sq
+};
+
+__device__ __forceinline__ int t5_key_limit(const FwdParams &p, const T5Lens &ln, int b, int L, int i) {
+    if (!p.causal) return L;
+    const long long qoff = ln.q_offset ? (long long)ln.q_offset[b] : (long long)L - p.Sq;
+    long long reach = qoff + i + 1;
+    reach = reach < 0 ? 0 : reach;
+    return (int)(reach < L ? reach : L);
+}
+
+__device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, const T5Lens &ln, int unit, int tpt, int ps_shift) {
     T5Unit U;
     const int ps = 1 << ps_shift;
     const int rt = unit % p.row_tiles;
@@ -127,14 +142,14 @@ __device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, int unit, int tpt,
     unit /= p.Hkv;
     U.s = unit % p.split_kv;
     U.b = unit / p.split_kv;
-    U.L = min(max(p.seq_lens[U.b], 0), p.W * ps);
+    U.L = min(max(ln.seq_lens[U.b], 0), p.W * ps);
     int pg1;
     split_pages(U.L, ps, p.split_kv, U.s, U.pg0, pg1);
     U.k_lo = U.pg0 * ps;
     U.k_hi_split = min(pg1 * ps, U.L);
     U.tok0 = rt * tpt;
     U.tok_end = min(U.tok0 + tpt, p.Sq);
-    U.k_hi = min(U.k_hi_split, row_key_limit(p, U.b, U.L, U.tok_end - 1));
+    U.k_hi = min(U.k_hi_split, t5_key_limit(p, ln, U.b, U.L, U.tok_end - 1));
     U.n_tiles = U.k_hi > U.k_lo ? (U.k_hi - U.k_lo + 127) / 128 : 0;
     return U;
 }
@@ -153,9 +168,22 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     __shared__ float s_xmax[2][2][128];   // [tile parity][column half][row]: partial row maxima
     __shared__ float s_xsum[2][128];      // [column half][row]: partial row sums
     __shared__ int s_xbad[2][128];
+    __shared__ int32_t s_seqlen[kT5StageLens], s_qoff[kT5StageLens];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ps = 1 << ps_shift;
+
+    // Every role walks every unit of this CTA and derives its bounds from seq_lens / q_offset: stage
+    // them in shared memory once, so no unit waits on a global load for them.
+    T5Lens ln{p.seq_lens, p.q_offset};
+    if (p.B <= kT5StageLens) {
+        for (int i = threadIdx.x; i < p.B; i += kT5Threads) {
+            s_seqlen[i] = p.seq_lens[i];
+            if (p.q_offset) s_qoff[i] = p.q_offset[i];
+        }
+        ln.seq_lens = s_seqlen;
+        ln.q_offset = p.q_offset ? s_qoff : nullptr;
+    }
 
     // shared memory: Q x2 | K x2 | V x2 (128 x 128 tiles, two 64-column swizzled halves each)
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -204,19 +232,19 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         // hides behind the current unit's copies.
         auto next_unit = [&](int from) {
             int u = from;
-            while (u < total_units && t5_unit(p, u, tpt, ps_shift).n_tiles == 0) u += gridDim.x;
+            while (u < total_units && t5_unit(p, ln, u, tpt, ps_shift).n_tiles == 0) u += gridDim.x;
             return u;
         };
         auto first_ids = [&](int u) {
             if (u >= total_units) return 0;
-            const T5Unit V = t5_unit(p, u, tpt, ps_shift);
+            const T5Unit V = t5_unit(p, ln, u, tpt, ps_shift);
             const int pe = (V.k_hi + ps - 1) >> ps_shift;
             return (V.pg0 + lane < pe) ? __ldg(p.block_table + (long long)V.b * p.W + V.pg0 + lane) : 0;
         };
         int unit = next_unit(blockIdx.x);
         int ids_pref = first_ids(unit);
         for (; unit < total_units && !bad;) {
-            const T5Unit U = t5_unit(p, unit, tpt, ps_shift);
+            const T5Unit U = t5_unit(p, ln, unit, tpt, ps_shift);
             const int unit_next = next_unit(unit + gridDim.x);
             const int ids_now = ids_pref;
             ids_pref = first_ids(unit_next);
@@ -328,7 +356,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             };
             int n = 0, g0 = 0;
             for (int unit = blockIdx.x; unit < total_units && !bad; unit += gridDim.x) {
-                const T5Unit U = t5_unit(p, unit, tpt, ps_shift);
+                const T5Unit U = t5_unit(p, ln, unit, tpt, ps_shift);
                 if (U.n_tiles == 0) continue;
                 const int qb = n & 1;
                 if (!mbar_wait(bar(B_QF + qb), (n >> 1) & 1, p.err)) { bad = true; break; }
@@ -353,13 +381,10 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     pfirst = t == 0;
                     plast = t == U.n_tiles - 1;
                 }
-                // The unit's last P V goes out now rather than behind the next unit's first Q K^T,
-                // which may still be waiting for its loads: the softmax read-out of this unit waits on it.
-                if (!bad && pend && !issue_pv(pg, pn, pfirst, plast)) bad = true;
-                pend = false;
                 g0 += U.n_tiles;
                 ++n;
             }
+            if (!bad && pend) issue_pv(pg, pn, pfirst, plast);
         }
         __syncwarp();
     } else {
@@ -376,7 +401,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         bool bad = false;
         int n = 0, g0 = 0;
         for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x) {
-            const T5Unit U = t5_unit(p, unit, tpt, ps_shift);
+            const T5Unit U = t5_unit(p, ln, unit, tpt, ps_shift);
             if (threadIdx.x == 64 && U.s == 0 && U.tok0 == 0 && p.seq_lens[U.b] > p.W * ps)
                 atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
             const int tk = U.tok0 + r / p.G;
@@ -393,7 +418,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             }
             const int ob = n & 1;
             const uint32_t ocol = kColO + 128u * (uint32_t)ob;
-            const int lim = row_valid ? min(U.k_hi_split, row_key_limit(p, U.b, U.L, tk)) : U.k_lo;
+            const int lim = row_valid ? min(U.k_hi_split, t5_key_limit(p, ln, U.b, U.L, tk)) : U.k_lo;
             float m_used = kNegInf, l = 0.f;
             for (int t = 0; t < U.n_tiles; ++t) {
                 const int g = g0 + t, st = g & 1;
