@@ -4,7 +4,7 @@
 // A work unit = (sequence b, kv head, split s, tile of 128/G query tokens x the G query heads of
 // the kv head's group), so all 128 rows share every K/V tile.  The kernel is persistent: one CTA
 // per SM walks its units, with
-//   warp 0      TMA producer: each unit's Q tile (double-buffered), then per 128-key tile the
+//   warps 0,10  TMA producers (0: Q and K, 10: V): each unit's Q tile (double-buffered), then per 128-key tile the
 //               block-table ids (32 pages per batch, never past the sequence's page count) and one
 //               box per page, half-row and pool into 2-slot K and V rings.
 //   warp 1      allocates all 512 TMEM columns and issues tcgen05.mma from one thread:
@@ -26,7 +26,7 @@ namespace pa {
 
 namespace {
 
-constexpr int kT5Threads = 320;               // 10 warps
+constexpr int kT5Threads = 352;               // 11 warps
 constexpr int kT5Half = 128 * 128;            // bytes of one 64-column half of a 128-row tile
 constexpr int kT5Tile = 2 * kT5Half;          // a 128 x 128 bf16 tile (Q, K or V)
 constexpr uint32_t kT5TmemCols = 512;
@@ -217,12 +217,18 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     tc05::fence_after_sync();
     const uint32_t tmem = s_tmem;
 
-    if (warp == 0) {
-        // ================================================================ TMA producer
+    if (warp == 0 || warp == 10) {
+        // ================================================================ TMA producers
+        // warp 0 loads Q and K, warp 10 loads V: the two rings free at different times (K after
+        // Q K^T, V after P V), so one must not wait behind the other.
+        const bool kq = warp == 0;
         if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
+            if (kq) {
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+            } else {
+                tma_prefetch_desc(&tmV);
+            }
         }
         const int ppt = 128 >> ps_shift;                     // pages per tile (divides 32)
         const uint32_t box = (uint32_t)ps * 128u;            // bytes of one page half-row box
@@ -249,12 +255,12 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             const int ids_now = ids_pref;
             ids_pref = first_ids(unit_next);
             const int qb = n & 1;
-            if (n >= 2) {  // Q buffer free once every Q K^T of unit n-2 is done
+            if (kq && n >= 2) {  // Q buffer free once every Q K^T of unit n-2 is done
                 const bool ok = mbar_wait(bar(B_QE + qb), ((n >> 1) - 1) & 1, p.err);
                 bad = __any_sync(0xffffffffu, !ok);
                 if (bad) break;
             }
-            if (lane == 0) {
+            if (kq && lane == 0) {
                 mbar_arrive_expect_tx(bar(B_QF + qb), (uint32_t)kT5Tile);
                 const int qtok = U.b * p.Sq + U.tok0;
                 tma_load_4d(sQ(qb), &tmQ, bar(B_QF + qb), 0, 0, U.kvh * p.G, qtok);
@@ -285,31 +291,21 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                         tok = id << ps_shift;
                     }
                 }
-                if (g >= 2) {  // K slot free once Q K^T of tile g-2 is done
-                    const bool ok = mbar_wait(bar(B_KE + slot), ((g >> 1) - 1) & 1, p.err);
+                // K slot free once Q K^T of tile g-2 is done; V slot once P V of tile g-2 is done
+                const int b_empty = kq ? B_KE : B_VE, b_full = kq ? B_KF : B_VF;
+                if (g >= 2) {
+                    const bool ok = mbar_wait(bar(b_empty + slot), ((g >> 1) - 1) & 1, p.err);
                     bad = __any_sync(0xffffffffu, !ok);
                     if (bad) break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(bar(B_KF + slot), (uint32_t)nvalid * 2u * box);
+                if (lane == 0) mbar_arrive_expect_tx(bar(b_full + slot), (uint32_t)nvalid * 2u * box);
                 __syncwarp();
                 if (lane < nvalid) {
+                    const uint32_t dst = (kq ? sK(slot) : sV(slot)) + (uint32_t)lane * box;
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
-                        tma_load_4d(sK(slot) + (uint32_t)h * kT5Half + (uint32_t)lane * box, &tmK, bar(B_KF + slot), 0,
-                                    tok, h, U.kvh);
-                }
-                if (g >= 2) {  // V slot free once P V of tile g-2 is done
-                    const bool ok = mbar_wait(bar(B_VE + slot), ((g >> 1) - 1) & 1, p.err);
-                    bad = __any_sync(0xffffffffu, !ok);
-                    if (bad) break;
-                }
-                if (lane == 0) mbar_arrive_expect_tx(bar(B_VF + slot), (uint32_t)nvalid * 2u * box);
-                __syncwarp();
-                if (lane < nvalid) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_4d(sV(slot) + (uint32_t)h * kT5Half + (uint32_t)lane * box, &tmV, bar(B_VF + slot), 0,
-                                    tok, h, U.kvh);
+                        tma_load_4d(dst + (uint32_t)h * kT5Half, kq ? &tmK : &tmV, bar(b_full + slot), 0, tok, h,
+                                    U.kvh);
                 }
             }
             g0 += U.n_tiles;
@@ -319,11 +315,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         // No copy may outlive the CTA: wait (bounded) for the last phase armed on every slot.  After a
         // time-out some of these were never armed; their waits then give up too.
         if (!bad) {
-            for (int g = max(0, g0 - 2); g < g0; ++g) {
-                mbar_wait(bar(B_KF + (g & 1)), (g >> 1) & 1, p.err);
-                mbar_wait(bar(B_VF + (g & 1)), (g >> 1) & 1, p.err);
-            }
-            for (int k = max(0, n - 2); k < n; ++k) mbar_wait(bar(B_QF + (k & 1)), (k >> 1) & 1, p.err);
+            for (int g = max(0, g0 - 2); g < g0; ++g) mbar_wait(bar((kq ? B_KF : B_VF) + (g & 1)), (g >> 1) & 1, p.err);
+            if (kq)
+                for (int k = max(0, n - 2); k < n; ++k) mbar_wait(bar(B_QF + (k & 1)), (k >> 1) & 1, p.err);
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
