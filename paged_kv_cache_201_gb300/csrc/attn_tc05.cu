@@ -393,6 +393,43 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         const int r = q4 * 32 + lane;                       // TMEM lane = query row of the tile
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
         bool bad = false;
+        // A unit's read-out of O waits for its last P V, which the MMA thread issues after the next
+        // unit's first Q K^T; it is done after this thread's first tile of the next unit, so the
+        // wait overlaps useful work.  O is double-buffered, so the buffer is not needed earlier.
+        struct Pending {
+            bool valid, row_valid;
+            int s, ob, n;
+            long long ridx;
+            float l, m;
+        } pend{false, false, 0, 0, 0, 0, 0.f, kNegInf};
+        auto epilogue = [&](const Pending &e) {
+            if (!bad) {  // the unit's last P V (a dedicated barrier: exact whatever B_OD's phase)
+                const bool ok = mbar_wait(bar(B_OF + e.ob), (e.n >> 1) & 1, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+            }
+            s_xsum[hh][r] = e.l;
+            s_xbad[hh][r] = bad ? 1 : 0;
+            named_bar_sync(2, 256);
+            const float l_tot = e.l + s_xsum[hh ^ 1][r];
+            if (!bad && !s_xbad[hh ^ 1][r]) {
+                tc05::fence_after_sync();
+                const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                const uint32_t ocol = kColO + 128u * (uint32_t)e.ob;
+                float o[64];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t u[32];
+                    tc05::ld_32cols(tmem + lane_addr + ocol + 32u * (2 * hh + c), u);
+                    tc05::wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(u[j]) * inv;
+                }
+                if (e.row_valid)
+                    t5_store_half_row<T>(p, e.s, e.ridx, hh, o, l_tot > 0.f ? e.m * kLn2 + logf(l_tot) : kNegInf);
+            }
+            tc05::fence_before_sync();
+            mbar_arrive(bar(B_OFREE + e.ob));  // O buffer may take unit e.n + 2's products
+        };
         int n = 0, g0 = 0;
         for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x) {
             const T5Unit U = t5_unit(p, ln, unit, tpt, ps_shift);
@@ -507,36 +544,16 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 }
                 tc05::fence_before_sync();
                 mbar_arrive(bar(B_PF + st));
-            }
-            if (!bad) {  // the unit's last P V (a dedicated barrier: exact whatever B_OD's phase)
-                const bool ok = mbar_wait(bar(B_OF + ob), (n >> 1) & 1, p.err);
-                bad = __any_sync(0xffffffffu, !ok);
-            }
-            s_xsum[hh][r] = l;
-            s_xbad[hh][r] = bad ? 1 : 0;
-            named_bar_sync(2, 256);
-            const float l_tot = l + s_xsum[hh ^ 1][r];
-            if (!bad && !s_xbad[hh ^ 1][r]) {
-                tc05::fence_after_sync();
-                const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-                float o[64];
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t u[32];
-                    tc05::ld_32cols(tmem + lane_addr + ocol + 32u * (2 * hh + c), u);
-                    tc05::wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(u[j]) * inv;
+                if (t == 0 && pend.valid) {
+                    epilogue(pend);
+                    pend.valid = false;
                 }
-                if (row_valid)
-                    t5_store_half_row<T>(p, U.s, t5_row_index(p, U.b, U.kvh, tk, gq), hh, o,
-                                         l_tot > 0.f ? m_used * kLn2 + logf(l_tot) : kNegInf);
             }
-            tc05::fence_before_sync();
-            mbar_arrive(bar(B_OFREE + ob));  // O buffer ob may take unit n+2's products
+            pend = Pending{true, row_valid, U.s, ob, n, t5_row_index(p, U.b, U.kvh, tk, gq), l, m_used};
             g0 += U.n_tiles;
             ++n;
         }
+        if (pend.valid) epilogue(pend);
     }
 
     tc05::fence_before_sync();
