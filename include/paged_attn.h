@@ -216,6 +216,9 @@ int paged_attn_last_error_word(uint32_t *flags);
 /* Human-readable text for a status code (static storage). */
 const char *paged_attn_strerror(int code);
 
+/* Text of the CUDA error behind the calling thread's most recent PA_ECUDA ("no error" if none). */
+const char *paged_attn_cuda_error_string(void);
+
 /* Library version as an integer, major * 10000 + minor * 100 + patch. */
 int paged_attn_version(void);
 

@@ -36,7 +36,10 @@ class PaDims(ctypes.Structure):
 class PagedAttnError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: status {code} ({paged_attn_strerror(code)})")
+        msg = f"{where}: status {code} ({paged_attn_strerror(code)})"
+        if code == -4:
+            msg += f": {load_library().paged_attn_cuda_error_string().decode()}"
+        super().__init__(msg)
 
 
 _lib = None
@@ -77,6 +80,8 @@ def load_library(build_if_missing: bool = False):
     lib.paged_attn_strerror.argtypes = [I32]
     lib.paged_attn_strerror.restype = ctypes.c_char_p
     lib.paged_attn_version.argtypes = []
+    lib.paged_attn_cuda_error_string.argtypes = []
+    lib.paged_attn_cuda_error_string.restype = ctypes.c_char_p
     for name in ("paged_attn_fwd", "paged_attn_fwd_variant", "paged_attn_combine", "paged_attn_plan",
                  "paged_attn_debug_gather", "paged_attn_last_error_word", "paged_attn_version"):
         getattr(lib, name).restype = ctypes.c_int

@@ -48,6 +48,15 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+// PA_OK, or PA_ECUDA after remembering e for paged_attn_cuda_error_string.
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return PA_OK;
+    t_last_cuda_error = e;
+    return PA_ECUDA;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int esize_of(int dtype) { return dtype == PA_F32 ? 4 : 2; }
@@ -210,7 +219,7 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
         if (mode == pa::MODE_PREFILL) p.row_tiles = (rows + pa::kPrefillRows - 1) / pa::kPrefillRows;
         e = pa::launch_mma(p, mode, dims->dtype, tmk, tmv, st);
     }
-    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+    return cuda_status(e);
 }
 
 int paged_attn_fwd(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
@@ -300,7 +309,7 @@ int paged_attn_combine(const float *part_out, const float *part_lse, int split_k
         return PA_EINVAL;
     cudaError_t e = pa::launch_combine(part_out, part_lse, split_kv, (long long)rows, head_dim, out_dtype, out, lse,
                                        static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+    return cuda_status(e);
 }
 
 int paged_attn_plan(const int32_t *seq_lens, int batch, int page_size, int split_kv, int32_t *plan, void *stream) {
@@ -308,7 +317,7 @@ int paged_attn_plan(const int32_t *seq_lens, int batch, int page_size, int split
     if (batch == 0) return PA_OK;
     if (!seq_lens || !plan) return PA_EINVAL;
     cudaError_t e = pa::launch_plan(seq_lens, batch, page_size, split_kv, plan, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+    return cuda_status(e);
 }
 
 int paged_attn_debug_gather(const void *cache, const int32_t *block_table, const int32_t *seq_lens,
@@ -324,7 +333,7 @@ int paged_attn_debug_gather(const void *cache, const int32_t *block_table, const
     cudaError_t e = pa::launch_gather(cache, block_table, seq_lens, dims->batch, dims->bt_stride, dims->page_size,
                                       dims->num_kv_heads, dims->head_dim, esize_of(dims->dtype), dims->num_pages,
                                       out_tokens, out, err, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? PA_OK : PA_ECUDA;
+    return cuda_status(e);
 }
 
 int paged_attn_last_error_word(uint32_t *flags) {
@@ -350,5 +359,7 @@ const char *paged_attn_strerror(int code) {
 }
 
 int paged_attn_version(void) { return 100; }
+
+const char *paged_attn_cuda_error_string(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 }  // extern "C"

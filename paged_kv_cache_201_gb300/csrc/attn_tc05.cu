@@ -211,7 +211,7 @@ __device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, const T5Lens &ln, 
 // on the CTA's global tile counter g; Q and O are double-buffered by the CTA's count of non-empty
 // units n, so a unit's epilogue and the next unit's loads overlap its neighbours' work.
 template <typename T>
-__global__ void __maxnreg__(176)
+__global__ void __launch_bounds__(kT5Threads, 1)
     paged_attn_tc05_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const FwdParams p, int tpt, int ps_shift,
                            uint32_t idesc_qk, uint32_t idesc_pv, int total_units) {
