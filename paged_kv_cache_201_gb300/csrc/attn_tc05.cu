@@ -32,8 +32,7 @@ constexpr int kT5Tile = 2 * kT5Half;          // a 128 x 128 bf16 tile (Q, K or 
 constexpr uint32_t kT5TmemCols = 512;
 constexpr uint32_t kColO = 256;               // O buffers at columns 256 and 384
 constexpr float kRescaleLog2 = 8.f;           // rescale O only when the max grows by > 2^8
-constexpr int kT5StageLens = 512;             // batches up to this size keep seq_lens / q_offset in smem
-constexpr int kT5StageRow = 272;              // bytes per staged output half-row (256 + 16 pad)
+constexpr int kT5StageLens = 1024;            // batches up to this size keep seq_lens / q_offset in smem
 
 // barrier slots (pairs are indexed by buffer / ring slot)
 //   QF/QE  Q buffer full (TMA) / empty (after the unit's last Q K^T)
@@ -51,58 +50,6 @@ enum {
 
 __device__ __forceinline__ long long t5_row_index(const FwdParams &p, int b, int kvh, int tok, int g) {
     return ((long long)b * p.Sq + tok) * p.Hq + (long long)kvh * p.G + g;
-}
-
-// Store output columns [64 hh, 64 hh + 64) of the warp's 32 rows (one per lane), coalesced: rows go
-// 8 at a time through the warp's shared staging area and leave as whole half-rows (256 B of fp32
-// partials or 128 B of T), so one store instruction covers 2 or 4 rows instead of 32 scattered
-// pieces.  From half 0 each lane also writes its row's lse.
-template <typename T>
-__device__ __forceinline__ void t5_store_rows(const FwdParams &p, int s, long long ridx, bool valid, int hh,
-                                              const float *v, float lse, uint8_t *stage, int lane) {
-    const bool partial = p.split_kv > 1;
-    const long long rows_total = (long long)p.B * p.Sq * p.Hq;
-    const int chunks = partial ? 16 : 8;                     // 16-byte chunks per half-row
-    uint8_t *dst_base = partial ? reinterpret_cast<uint8_t *>(reinterpret_cast<float *>(p.out) +
-                                                              (long long)s * rows_total * 128 + 64 * hh)
-                                : reinterpret_cast<uint8_t *>(reinterpret_cast<T *>(p.out) + 64 * hh);
-    const long long row_bytes = partial ? 128 * 4 : 128 * (long long)sizeof(T);
-#pragma unroll 1
-    for (int j = 0; j < 4; ++j) {
-        if ((lane >> 3) == j) {
-            uint4 *st = reinterpret_cast<uint4 *>(stage + (lane & 7) * kT5StageRow);
-            if (partial) {
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    st[c] = make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
-                                       __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
-            } else {
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st[c] = make_uint4(MmaOp<T>::pack(v[8 * c], v[8 * c + 1]), MmaOp<T>::pack(v[8 * c + 2], v[8 * c + 3]),
-                                       MmaOp<T>::pack(v[8 * c + 4], v[8 * c + 5]),
-                                       MmaOp<T>::pack(v[8 * c + 6], v[8 * c + 7]));
-            }
-        }
-        __syncwarp();
-        for (int item = lane; item < 8 * chunks; item += 32) {
-            const int row = item / chunks, c = item % chunks;
-            const int src = 8 * j + row;
-            const long long rid = __shfl_sync(0xffffffffu, ridx, src);
-            const bool ok = __shfl_sync(0xffffffffu, valid ? 1 : 0, src) != 0;
-            if (ok) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(stage + row * kT5StageRow + 16 * c);
-                *reinterpret_cast<uint4 *>(dst_base + rid * row_bytes + 16 * c) = w;
-            }
-        }
-        __syncwarp();
-    }
-    if (valid && hh == 0) {
-        if (partial)
-            p.lse[(long long)s * rows_total + ridx] = lse;
-        else if (p.lse)
-            p.lse[ridx] = lse;
-    }
 }
 
 // Store output columns [64 hh, 64 hh + 64) of one row (and, from half 0, its lse).
@@ -222,7 +169,6 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     __shared__ float s_xsum[2][128];      // [column half][row]: partial row sums
     __shared__ int s_xbad[2][128];
     __shared__ int32_t s_seqlen[kT5StageLens], s_qoff[kT5StageLens];
-    __shared__ __align__(16) uint8_t s_stage[8][8 * kT5StageRow];  // per softmax warp: 8 output half-rows
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ps = 1 << ps_shift;
@@ -478,8 +424,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(u[j]) * inv;
                 }
-                t5_store_rows<T>(p, e.s, e.ridx, e.row_valid, hh, o, l_tot > 0.f ? e.m * kLn2 + logf(l_tot) : kNegInf,
-                                 s_stage[warp - 2], lane);
+                if (e.row_valid)
+                    t5_store_half_row<T>(p, e.s, e.ridx, hh, o, l_tot > 0.f ? e.m * kLn2 + logf(l_tot) : kNegInf);
             }
             tc05::fence_before_sync();
             mbar_arrive(bar(B_OFREE + e.ob));  // O buffer may take unit e.n + 2's products
