@@ -22,6 +22,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+KV_FP8E4M3 = 3
 OK, EINVAL, EBOUNDS, ENOMEM = 0, -1, -5, -6
 
 
@@ -68,6 +69,12 @@ def load(path: str = _LIB_PATH, rebuild_if_stale: bool = True):
                                 ctypes.c_int32, P, P, P, ctypes.c_int64, ctypes.c_int32,
                                 P, P, P, P, P, P]
     lib.oracle_rows.restype = ctypes.c_int
+    lib.oracle_rows_kvq.argtypes = [P, P, P, ctypes.c_int32, P, P, P, P, P, ctypes.c_int32, ctypes.POINTER(Dims),
+                                    ctypes.c_double, ctypes.c_int32, P, P, P, ctypes.c_int64, ctypes.c_int32,
+                                    P, P, P, P, P, P]
+    lib.oracle_rows_kvq.restype = ctypes.c_int
+    lib.oracle_gather_kvq.argtypes = [P, ctypes.c_int32, P, P, P, ctypes.POINTER(Dims), ctypes.c_int32, P]
+    lib.oracle_gather_kvq.restype = ctypes.c_int
     _lib_cache[path] = lib
     return lib
 
@@ -194,3 +201,65 @@ def workload_rows(wl, split_kv: int = 1, row_bih=None, n_threads: int = 0, want_
                 seq_lens=wl.seq_lens, q_offset=wl.q_offset, causal=wl.causal, dims=dims_of(wl),
                 scale=wl.scale, split_kv=split_kv, row_bih=row_bih, n_threads=n_threads,
                 want_split=want_split, lib=lib)
+
+
+# ----------------------------------------------------------------------------- quantized pools
+def gather_kvq(cache_bits: np.ndarray, scales: np.ndarray, block_table, seq_lens, dims: Dims, b: int,
+               lib=None) -> np.ndarray:
+    """Dequantized logical rows of sequence b from an FP8 E4M3 pool (uint8 bits) with
+    [num_pages, Hkv] float32 scales: float64 [L_b, Hkv, D]."""
+    lib = lib or load()
+    c = np.ascontiguousarray(cache_bits, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    L = max(int(sl[b]), 0)
+    out = np.zeros((L, dims.Hkv, dims.D), dtype=np.float64)
+    rc = lib.oracle_gather_kvq(_ptr(c), KV_FP8E4M3, _ptr(sc), _ptr(bt), _ptr(sl), ctypes.byref(dims), b, _ptr(out))
+    if rc != OK:
+        raise ValueError(f"oracle_gather_kvq failed: {rc}")
+    return out
+
+
+def rows_kvq(*, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, causal: bool, dims: Dims,
+             scale: float, split_kv: int = 1, row_bih: Optional[np.ndarray] = None, n_threads: int = 0,
+             want_split: bool = True, lib=None) -> dict:
+    """``rows`` with FP8 E4M3 K/V pools (uint8 bits) and [num_pages, Hkv] float32 scales per pool;
+    q is float32 / uint16 bits of dims.dtype as in ``rows``."""
+    lib = lib or load()
+    dt = {v: k for k, v in DTYPE_CODE.items()}[dims.dtype]
+    qe = _elems(q, dt)
+    ke = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    ve = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qo = None if q_offset is None else np.ascontiguousarray(q_offset, dtype=np.int32)
+    if row_bih is None:
+        row_bih = all_rows(dims.B, dims.Sq, dims.Hq)
+    row_bih = np.ascontiguousarray(row_bih, dtype=np.int32)
+    rb, ri, rh = (np.ascontiguousarray(row_bih[:, k]) for k in range(3))
+    n, D, S = row_bih.shape[0], dims.D, split_kv
+    res = {"out": np.zeros((n, D)), "lse": np.zeros((n,))}
+    if want_split:
+        res.update(part_out=np.zeros((n, S, D)), part_lse=np.zeros((n, S)), comb_out=np.zeros((n, D)),
+                   comb_lse=np.zeros((n,)))
+    rc = lib.oracle_rows_kvq(_ptr(qe), _ptr(ke), _ptr(ve), KV_FP8E4M3, _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl),
+                             _ptr(qo), int(causal), ctypes.byref(dims), float(scale), S, _ptr(rb), _ptr(ri),
+                             _ptr(rh), n, n_threads, _ptr(res["out"]), _ptr(res["lse"]), _ptr(res.get("part_out")),
+                             _ptr(res.get("part_lse")), _ptr(res.get("comb_out")), _ptr(res.get("comb_lse")))
+    if rc != OK:
+        raise ValueError(f"oracle_rows_kvq failed: {rc}")
+    return res
+
+
+def workload_rows_kvq(wl, split_kv: int = 1, row_bih=None, n_threads: int = 0, want_split: bool = True,
+                      k_cache=None, v_cache=None, k_scale=None, v_scale=None, lib=None) -> dict:
+    """``rows_kvq`` on an object with the workload attributes (pools as uint8 E4M3 bits + scales)."""
+    return rows_kvq(q=wl.q, k_cache=wl.k_cache if k_cache is None else k_cache,
+                    v_cache=wl.v_cache if v_cache is None else v_cache,
+                    k_scale=wl.k_scale if k_scale is None else k_scale,
+                    v_scale=wl.v_scale if v_scale is None else v_scale, block_table=wl.block_table,
+                    seq_lens=wl.seq_lens, q_offset=wl.q_offset, causal=wl.causal, dims=dims_of(wl), scale=wl.scale,
+                    split_kv=split_kv, row_bih=row_bih, n_threads=n_threads, want_split=want_split, lib=lib)

@@ -29,7 +29,10 @@
  *   - GQA: query head h reads kv head h / (Hq / Hkv);
  *   - lse is the natural log of the sum of exp(scaled score);
  *   - a split's partial output is normalised by its own sum; a split with no
- *     valid key yields output 0 and lse -inf.
+ *     valid key yields output 0 and lse -inf;
+ *   - quantized pools (the pages' sweeps include i8 attention: rocMLIR PR #2222,
+ *     reviewed files; rocMLIR PR #2371, Motivation) are read as FP8 E4M3
+ *     elements with one float scale per (page, kv head): value = element x scale.
  *
  * Everything is evaluated from the definition: scores in double, the maximum
  * over all valid keys, then exp, sum and weighted sum.  No online rescaling,
@@ -43,7 +46,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_FP8E4M3 = 3 };
 enum { ORACLE_OK = 0, ORACLE_EINVAL = -1, ORACLE_EBOUNDS = -5, ORACLE_ENOMEM = -6 };
 
 /* Shape of one problem.  Layouts (all dense, row-major):
@@ -83,8 +86,27 @@ static double bf16_bits_to_double(uint16_t h)
     return (double)f;
 }
 
+/* FP8 E4M3 (OCP "fn" variant: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent
+ * 1111 with mantissa 111 is NaN; no infinities) -> double, exactly, from the format's definition. */
+static double e4m3_bits_to_double(uint8_t h)
+{
+    int sign = (h >> 7) & 1;
+    int e = (h >> 3) & 0xF;
+    int m = h & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);          /* m/8 * 2^(1-7) */
+    else
+        v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
 static double widen(const void *base, int dtype, int64_t idx)
 {
+    if (dtype == ORACLE_FP8E4M3)
+        return e4m3_bits_to_double(((const uint8_t *)base)[idx]);
     if (dtype == ORACLE_F32)
         return (double)((const float *)base)[idx];
     if (dtype == ORACLE_BF16)
@@ -102,6 +124,14 @@ static int dims_ok(const oracle_dims *d)
         return 0;
     return d->num_pages >= 0 && d->bt_stride >= 0;
 }
+
+/* The K and V pools as stored: element type, and for quantized pools one float scale per
+ * (page, kv head), [num_pages, Hkv]; a stored element times its page's scale is the value. */
+typedef struct {
+    const void *k_cache, *v_cache;
+    int kv_dtype;
+    const float *k_scale, *v_scale;  /* NULL: no scaling */
+} oracle_kv;
 
 /* ---------------------------------------------------------------- split plan */
 
@@ -135,10 +165,15 @@ int oracle_plan(const int32_t *seq_lens, int32_t B, int32_t page_size, int32_t s
  * block_table[b][j / page_size]; inside the page the token sits at row
  * j % page_size and the kv head adds kvh * D.  Returns the flat index or -1 if
  * the page id is not a page of the pool. */
+static int32_t table_page(const oracle_dims *d, const int32_t *block_table, int32_t b, int64_t j)
+{
+    return block_table[(int64_t)b * d->bt_stride + j / d->page_size];
+}
+
 static int64_t logical_index(const oracle_dims *d, const int32_t *block_table, int32_t b, int64_t j,
                              int32_t kvh, int32_t e)
 {
-    int32_t page = block_table[(int64_t)b * d->bt_stride + j / d->page_size];
+    int32_t page = table_page(d, block_table, b, j);
     if (page < 0 || (int64_t)page >= d->num_pages)
         return -1;
     int64_t tok = (int64_t)page * d->page_size + j % d->page_size;
@@ -192,7 +227,21 @@ int64_t oracle_key_limit(const int32_t *seq_lens, const int32_t *q_offset, int32
 
 /* softmax(scale * q.k_j) . v_j over the keys j in [lo, hi), from the definition.
  * No keys: out = 0, lse = -inf.  scratch has room for hi - lo doubles. */
-static int attend_keys(const oracle_dims *d, const double *qrow, const void *k_cache, const void *v_cache,
+/* Value of element (token j, kv head kvh, dim e) of sequence b in pool k (which = 0) or v (1). */
+/* Value of the element at flat index idx (token j, kv head kvh of sequence b) in pool k
+ * (which = 0) or v (1): the stored element, times its (page, kv head) scale for quantized pools. */
+static double kv_value(const oracle_dims *d, const oracle_kv *kv, int which, const int32_t *block_table, int32_t b,
+                       int64_t j, int32_t kvh, int64_t idx)
+{
+    const void *cache = which ? kv->v_cache : kv->k_cache;
+    double x = widen(cache, kv->kv_dtype, idx);
+    const float *sc = which ? kv->v_scale : kv->k_scale;
+    if (sc)
+        x *= (double)sc[(int64_t)table_page(d, block_table, b, j) * d->Hkv + kvh];
+    return x;
+}
+
+static int attend_keys(const oracle_dims *d, const double *qrow, const oracle_kv *kv,
                        const int32_t *block_table, int32_t b, int32_t kvh, int64_t lo, int64_t hi,
                        double scale, double *scratch, double *out, double *lse)
 {
@@ -210,7 +259,7 @@ static int attend_keys(const oracle_dims *d, const double *qrow, const void *k_c
             int64_t idx = logical_index(d, block_table, b, j, kvh, e);
             if (idx < 0)
                 return ORACLE_EBOUNDS;
-            s += qrow[e] * widen(k_cache, d->dtype, idx);
+            s += qrow[e] * kv_value(d, kv, 0, block_table, b, j, kvh, idx);
         }
         s *= scale;
         scratch[j - lo] = s;
@@ -223,7 +272,7 @@ static int attend_keys(const oracle_dims *d, const double *qrow, const void *k_c
         l += p;
         for (int32_t e = 0; e < D; ++e) {
             int64_t idx = logical_index(d, block_table, b, j, kvh, e);
-            out[e] += p * widen(v_cache, d->dtype, idx);
+            out[e] += p * kv_value(d, kv, 1, block_table, b, j, kvh, idx);
         }
     }
     for (int32_t e = 0; e < D; ++e)
@@ -288,11 +337,11 @@ int oracle_num_threads(void)
  * Any of the split outputs may be NULL (then split_kv is only used for them).
  * n_threads <= 0 uses the OpenMP default.  Returns ORACLE_EBOUNDS if a page id
  * inside a sequence's first ceil(L_b / page_size) table slots is not a pool page. */
-int oracle_rows(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
-                const int32_t *seq_lens, const int32_t *q_offset, int32_t causal, const oracle_dims *d,
-                double scale, int32_t split_kv, const int32_t *row_b, const int32_t *row_i,
-                const int32_t *row_h, int64_t n_rows, int32_t n_threads, double *out, double *lse,
-                double *part_out, double *part_lse, double *comb_out, double *comb_lse)
+static int rows_impl(const void *q, const oracle_kv *kv, const int32_t *block_table,
+                     const int32_t *seq_lens, const int32_t *q_offset, int32_t causal, const oracle_dims *d,
+                     double scale, int32_t split_kv, const int32_t *row_b, const int32_t *row_i,
+                     const int32_t *row_h, int64_t n_rows, int32_t n_threads, double *out, double *lse,
+                     double *part_out, double *part_lse, double *comb_out, double *comb_lse)
 {
     if (!dims_ok(d) || split_kv <= 0 || n_rows < 0)
         return ORACLE_EINVAL;
@@ -341,8 +390,7 @@ int oracle_rows(const void *q, const void *k_cache, const void *v_cache, const i
                 int st = ORACLE_OK;
                 double tlse;
                 if (out && lse) {
-                    st = attend_keys(d, qrow, k_cache, v_cache, block_table, b, kvh, 0, lim, scale, scratch,
-                                     out + r * D, lse + r);
+                    st = attend_keys(d, qrow, kv, block_table, b, kvh, 0, lim, scale, scratch, out + r * D, lse + r);
                 }
                 if (st == ORACLE_OK && (part_out || comb_out)) {
                     const int64_t L = seq_lens[b] > 0 ? seq_lens[b] : 0;
@@ -352,7 +400,7 @@ int oracle_rows(const void *q, const void *k_cache, const void *v_cache, const i
                         if (hi > L) hi = L;
                         if (hi > lim) hi = lim;   /* causal reach inside the split */
                         if (lo > hi) lo = hi;
-                        st = attend_keys(d, qrow, k_cache, v_cache, block_table, b, kvh, lo, hi, scale, scratch,
+                        st = attend_keys(d, qrow, kv, block_table, b, kvh, lo, hi, scale, scratch,
                                          pout + (int64_t)s * D, &tlse);
                         plse[s] = tlse;
                     }
@@ -379,4 +427,55 @@ int oracle_rows(const void *q, const void *k_cache, const void *v_cache, const i
     }
     free(plan);
     return status;
+}
+
+/* Attention for the chosen rows with K/V pools of element type dtype (see oracle_rows). */
+int oracle_rows(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                const int32_t *seq_lens, const int32_t *q_offset, int32_t causal, const oracle_dims *d,
+                double scale, int32_t split_kv, const int32_t *row_b, const int32_t *row_i,
+                const int32_t *row_h, int64_t n_rows, int32_t n_threads, double *out, double *lse,
+                double *part_out, double *part_lse, double *comb_out, double *comb_lse)
+{
+    if (!dims_ok(d))
+        return ORACLE_EINVAL;
+    const oracle_kv kv = {k_cache, v_cache, d->dtype, NULL, NULL};
+    return rows_impl(q, &kv, block_table, seq_lens, q_offset, causal, d, scale, split_kv, row_b, row_i, row_h,
+                     n_rows, n_threads, out, lse, part_out, part_lse, comb_out, comb_lse);
+}
+
+/* The same with quantized K/V pools: elements of kv_dtype (ORACLE_FP8E4M3) times the float scale
+ * of their (page, kv head), k_scale / v_scale [num_pages, Hkv]; q and the results as in oracle_rows. */
+int oracle_rows_kvq(const void *q, const void *k_cache, const void *v_cache, int32_t kv_dtype,
+                    const float *k_scale, const float *v_scale, const int32_t *block_table,
+                    const int32_t *seq_lens, const int32_t *q_offset, int32_t causal, const oracle_dims *d,
+                    double scale, int32_t split_kv, const int32_t *row_b, const int32_t *row_i,
+                    const int32_t *row_h, int64_t n_rows, int32_t n_threads, double *out, double *lse,
+                    double *part_out, double *part_lse, double *comb_out, double *comb_lse)
+{
+    if (!dims_ok(d) || kv_dtype != ORACLE_FP8E4M3 || !k_scale || !v_scale)
+        return ORACLE_EINVAL;
+    const oracle_kv kv = {k_cache, v_cache, kv_dtype, k_scale, v_scale};
+    return rows_impl(q, &kv, block_table, seq_lens, q_offset, causal, d, scale, split_kv, row_b, row_i, row_h,
+                     n_rows, n_threads, out, lse, part_out, part_lse, comb_out, comb_lse);
+}
+
+/* Dequantized logical gather of one quantized pool: out[L_b, Hkv, D] (see oracle_gather). */
+int oracle_gather_kvq(const void *cache, int32_t kv_dtype, const float *scales, const int32_t *block_table,
+                      const int32_t *seq_lens, const oracle_dims *d, int32_t b, double *out)
+{
+    if (!dims_ok(d) || b < 0 || b >= d->B || kv_dtype != ORACLE_FP8E4M3 || !scales)
+        return ORACLE_EINVAL;
+    const oracle_kv kv = {cache, cache, kv_dtype, scales, scales};
+    int64_t L = seq_lens[b] > 0 ? seq_lens[b] : 0;
+    if ((L + d->page_size - 1) / d->page_size > d->bt_stride)
+        return ORACLE_EINVAL;
+    for (int64_t j = 0; j < L; ++j)
+        for (int32_t kvh = 0; kvh < d->Hkv; ++kvh)
+            for (int32_t e = 0; e < d->D; ++e) {
+                int64_t idx = logical_index(d, block_table, b, j, kvh, e);
+                if (idx < 0)
+                    return ORACLE_EBOUNDS;
+                out[(j * d->Hkv + kvh) * d->D + e] = kv_value(d, &kv, 0, block_table, b, j, kvh, idx);
+            }
+    return ORACLE_OK;
 }

@@ -82,6 +82,9 @@ class Workload:
     k_cache: Optional[np.ndarray] = None    # [P, ps, Hkv, D] (host) or None if device-drawn
     v_cache: Optional[np.ndarray] = None
     device_cache_seed: Optional[int] = None  # set when the pools are drawn on the device
+    kv_dtype: Optional[str] = None           # "fp8e4m3": pools hold E4M3 bits (uint8) with per-page scales
+    k_scale: Optional[np.ndarray] = None     # float32 [num_pages, Hkv] (quantized pools only)
+    v_scale: Optional[np.ndarray] = None
 
     @property
     def G(self) -> int:
@@ -106,6 +109,10 @@ class Workload:
 
     def host_cache_available(self) -> bool:
         return self.k_cache is not None
+
+    @property
+    def kv_esize(self) -> int:
+        return 1 if self.kv_dtype == "fp8e4m3" else ESIZE[self.dtype]
 
 
 def _pack_tables(B: int, W: int, nblk: Sequence[int], pages: np.ndarray, tail: int) -> np.ndarray:
@@ -297,3 +304,73 @@ def fill_device_cache(wl: Workload, device="cuda", chunk: int = 1 << 27):
             flat[s:e].copy_(torch.randn(e - s, generator=g, device=device, dtype=torch.float32))
         out.append(t)
     return out[0], out[1]
+
+
+# ----------------------------------------------------------------------------- quantized pools
+E4M3_MAX = 448.0
+
+
+def quantize_pool_e4m3(x: np.ndarray):
+    """Quantize a float32 pool [P, ps, Hkv, D] to FP8 E4M3 with one scale per (page, kv head):
+    scale = max |x| / 448 over the page's rows of that head (1 where the block is all zero), and
+    the stored element is x / scale rounded to E4M3 (round to nearest even, torch's cast).
+    Returns (uint8 bits [P, ps, Hkv, D], float32 scales [P, Hkv])."""
+    import torch
+    amax = np.abs(x).max(axis=(1, 3))                            # [P, Hkv]
+    scale = np.where(amax > 0, amax / E4M3_MAX, 1.0).astype(np.float32)
+    y = x / scale[:, None, :, None]
+    bits = torch.from_numpy(np.ascontiguousarray(y, dtype=np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    return bits.numpy().copy(), scale
+
+
+def e4m3_bits_to_float(bits: np.ndarray) -> np.ndarray:
+    """E4M3 bits -> float64 values by torch's conversion (a library routine)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def make_custom_fp8(**kw) -> Workload:
+    """``make_custom`` (bf16 or f16 queries) whose K/V pools are then quantized to FP8 E4M3 with
+    per-(page, kv head) scales (``quantize_pool_e4m3``) from the same N(0,1) draws, in float32."""
+    dtype = kw.pop("dtype", "bf16")
+    assert dtype in ("bf16", "f16")
+    wl = make_custom(dtype="f32", **kw)
+    rng = np.random.default_rng(kw.get("seed", 0) + 7919)
+    q = _normal_elems(rng, wl.q.size, dtype).reshape(wl.q.shape)
+    kb, ks = quantize_pool_e4m3(wl.k_cache)
+    vb, vs = quantize_pool_e4m3(wl.v_cache)
+    return Workload(**{**wl.__dict__, "name": kw.get("name", "custom_fp8"), "dtype": dtype, "q": q,
+                       "k_cache": kb, "v_cache": vb, "kv_dtype": "fp8e4m3", "k_scale": ks, "v_scale": vs})
+
+
+def llama8b_decode_fp8(seed: int = 1006, B: int = 256) -> Workload:
+    """The Llama-3-8B-shaped decode with FP8 E4M3 pools (1 GiB each) and per-(page, kv head) scales;
+    pools and scales are drawn on the device (``fill_device_cache_fp8``)."""
+    wl = llama8b_decode(seed=seed, B=B)
+    return Workload(**{**wl.__dict__, "name": "llama8b_decode_fp8", "kv_dtype": "fp8e4m3"})
+
+
+CONFIGS["llama8b_decode_fp8"] = llama8b_decode_fp8
+
+
+def fill_device_cache_fp8(wl: Workload, device="cuda", pages_per_chunk: int = 4096):
+    """Draw the K and V pools on the device (seeded torch.randn, float32) and quantize them to E4M3
+    with per-(page, kv head) scales max|x| / 448.  Returns (k_bits, v_bits, k_scale, v_scale)."""
+    import torch
+    assert wl.device_cache_seed is not None and wl.kv_dtype == "fp8e4m3"
+    out = []
+    for which in (0, 1):
+        g = torch.Generator(device=device)
+        g.manual_seed(int(wl.device_cache_seed) * 2 + which)
+        bits = torch.empty(wl.cache_shape, dtype=torch.uint8, device=device)
+        scales = torch.empty((wl.num_pages, wl.Hkv), dtype=torch.float32, device=device)
+        for p0 in range(0, wl.num_pages, pages_per_chunk):
+            p1 = min(wl.num_pages, p0 + pages_per_chunk)
+            x = torch.randn((p1 - p0,) + wl.cache_shape[1:], generator=g, device=device, dtype=torch.float32)
+            amax = x.abs().amax(dim=(1, 3))
+            sc = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+            bits[p0:p1] = (x / sc[:, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+            scales[p0:p1] = sc
+        out += [bits, scales]
+    return out[0], out[2], out[1], out[3]

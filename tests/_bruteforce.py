@@ -12,6 +12,8 @@ import numpy as np
 
 
 def widen(arr: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f64":
+        return np.asarray(arr, dtype=np.float64)
     if dtype == "f32":
         return np.asarray(arr, dtype=np.float32).astype(np.float64)
     bits = np.asarray(arr).view(np.uint16)
@@ -28,9 +30,11 @@ def logical_kv(cache: np.ndarray, block_table: np.ndarray, L: int, page_size: in
     return c[pages, j % page_size]
 
 
-def attention(wl, q=None, k_cache=None, v_cache=None):
-    """Returns (out [B, Sq, Hq, D], lse [B, Sq, Hq]) in float64."""
+def attention(wl, q=None, k_cache=None, v_cache=None, kv_dtype=None):
+    """Returns (out [B, Sq, Hq, D], lse [B, Sq, Hq]) in float64.  ``kv_dtype`` ("f64" for
+    already-dequantized pools) defaults to the query dtype."""
     q = wl.q if q is None else q
+    kvd = wl.dtype if kv_dtype is None else kv_dtype
     k_cache = wl.k_cache if k_cache is None else k_cache
     v_cache = wl.v_cache if v_cache is None else v_cache
     qd = widen(q, wl.dtype)
@@ -41,8 +45,8 @@ def attention(wl, q=None, k_cache=None, v_cache=None):
         L = int(wl.seq_lens[b])
         if L <= 0:
             continue
-        K = np.repeat(logical_kv(k_cache, wl.block_table[b], L, wl.page_size, wl.dtype), G, axis=1)  # [L, Hq, D]
-        V = np.repeat(logical_kv(v_cache, wl.block_table[b], L, wl.page_size, wl.dtype), G, axis=1)
+        K = np.repeat(logical_kv(k_cache, wl.block_table[b], L, wl.page_size, kvd), G, axis=1)  # [L, Hq, D]
+        V = np.repeat(logical_kv(v_cache, wl.block_table[b], L, wl.page_size, kvd), G, axis=1)
         s = np.einsum("ihd,jhd->hij", qd[b], K) * wl.scale                                 # [Hq, Sq, L]
         if wl.causal:
             qoff = (L - wl.Sq) if wl.q_offset is None else int(wl.q_offset[b])

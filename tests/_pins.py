@@ -307,4 +307,73 @@ def pin_rejects_bad_page(lib):
     raise AssertionError("out-of-pool page id was accepted")
 
 
+# ----------------------------------------------------------------------------- quantized pools
+def pin_e4m3_all_codes(lib):
+    """Every FP8 E4M3 code decodes as the format defines (library cast for reference; hand-checked
+    anchors: 0x38 = 1, 0x7E = 448, 0x08 = 2^-6, 0x01 = 2^-9, 0xB8 = -1, 0x80 = -0, 0x7F = NaN)."""
+    codes = np.arange(256, dtype=np.uint8)
+    d = oracle.make_dims(B=1, Sq=1, Hq=1, Hkv=1, D=1, page_size=1, bt_stride=256, dtype="bf16", num_pages=256)
+    got = oracle.gather_kvq(codes.reshape(256, 1, 1, 1), np.ones((256, 1), np.float32),
+                            np.arange(256, dtype=np.int32).reshape(1, -1), np.array([256], dtype=np.int32), d, 0,
+                            lib=lib)[:, 0, 0]
+    want = W.e4m3_bits_to_float(codes)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan]) and np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+    for code, val in ((0x38, 1.0), (0x7E, 448.0), (0x08, 2.0 ** -6), (0x01, 2.0 ** -9), (0xB8, -1.0)):
+        assert got[code] == val, (hex(code), got[code])
+    assert got[0x80] == 0.0 and np.signbit(got[0x80]) and np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+
+
+def _fp8_small(seed=91, **kw):
+    base = dict(B=3, Sq=2, Hq=8, Hkv=2, D=16, page_size=4, seq_lens=[13, 4, 21], num_pages=16, W=6,
+                causal=True, seed=seed)
+    base.update(kw)
+    return W.make_custom_fp8(**base)
+
+
+def pin_kvq_unit_scale_equals_unquantized(lib):
+    """With every scale 1, quantized pools give bit-identical results to bf16 pools holding the same
+    (exactly representable) values."""
+    wl = _fp8_small()
+    ones = np.ones_like(wl.k_scale)
+    rq = oracle.workload_rows_kvq(wl, split_kv=3, k_scale=ones, v_scale=ones, lib=lib)
+    kb = W.bf16_bits_rne(W.e4m3_bits_to_float(wl.k_cache).astype(np.float32))
+    vb = W.bf16_bits_rne(W.e4m3_bits_to_float(wl.v_cache).astype(np.float32))
+    plain = W.Workload(**{**wl.__dict__, "k_cache": kb, "v_cache": vb, "kv_dtype": None})
+    rp = oracle.workload_rows(plain, split_kv=3, lib=lib)
+    for key in rq:
+        assert np.array_equal(rq[key], rp[key]), key
+
+
+def pin_kvq_bruteforce(lib):
+    """Quantized pools with per-(page, kv head) scales on shuffled pages agree with dense fp64
+    attention on the dequantized pools (1e-12)."""
+    for wl in (_fp8_small(), _fp8_small(seed=92, B=2, Sq=1, Hq=6, Hkv=3, D=8, seq_lens=[9, 16], causal=False,
+                                         num_pages=7, W=4)):
+        kd = W.e4m3_bits_to_float(wl.k_cache) * wl.k_scale[:, None, :, None].astype(np.float64)
+        vd = W.e4m3_bits_to_float(wl.v_cache) * wl.v_scale[:, None, :, None].astype(np.float64)
+        ref_out, ref_lse = bf.attention(wl, k_cache=kd, v_cache=vd, kv_dtype="f64")
+        r = oracle.workload_rows_kvq(wl, split_kv=1, want_split=False, lib=lib)
+        np.testing.assert_allclose(r["out"].reshape(ref_out.shape), ref_out, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(r["lse"].reshape(ref_lse.shape), ref_lse, rtol=1e-12, atol=1e-12)
+        assert len(np.unique(wl.k_scale)) > 4
+
+
+def pin_kvq_power_of_two_scales(lib):
+    """Power-of-two scales are exact: quantized results equal those of f32 pools holding value x scale."""
+    wl = _fp8_small(seed=93)
+    rng = np.random.default_rng(94)
+    ks = (2.0 ** rng.integers(-6, 7, size=wl.k_scale.shape)).astype(np.float32)
+    vs = (2.0 ** rng.integers(-6, 7, size=wl.v_scale.shape)).astype(np.float32)
+    rq = oracle.workload_rows_kvq(wl, split_kv=2, k_scale=ks, v_scale=vs, lib=lib)
+    kf = (W.e4m3_bits_to_float(wl.k_cache) * ks[:, None, :, None]).astype(np.float32)
+    vf = (W.e4m3_bits_to_float(wl.v_cache) * vs[:, None, :, None]).astype(np.float32)
+    qf = bf.widen(wl.q, wl.dtype).astype(np.float32)
+    plain = W.Workload(**{**wl.__dict__, "dtype": "f32", "q": qf, "k_cache": kf, "v_cache": vf, "kv_dtype": None})
+    rp = oracle.workload_rows(plain, split_kv=2, lib=lib)
+    for key in rq:
+        assert np.array_equal(rq[key], rp[key]), key
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -54,6 +54,16 @@ MUTATIONS = {
     # split partial range starts at the split's end page
     "split_range_start": ("int64_t lo = (int64_t)plan[((int64_t)b * S + s) * 2 + 0] * d->page_size;",
                           "int64_t lo = (int64_t)plan[((int64_t)b * S + s) * 2 + 0] * d->page_size + 1;"),
+    # quantized pools: scale looked up by logical page instead of the physical page
+    "kvq_scale_logical_page": ("x *= (double)sc[(int64_t)table_page(d, block_table, b, j) * d->Hkv + kvh];",
+                               "x *= (double)sc[(int64_t)(j / d->page_size) * d->Hkv + kvh];"),
+    # quantized pools: K and V scales swapped
+    "kvq_scales_swapped": ("const float *sc = which ? kv->v_scale : kv->k_scale;",
+                           "const float *sc = which ? kv->k_scale : kv->v_scale;"),
+    # E4M3 exponent bias off by one
+    "e4m3_bias": ("v = ldexp((double)(8 + m), e - 10);", "v = ldexp((double)(8 + m), e - 11);"),
+    # E4M3 subnormals scaled wrong
+    "e4m3_subnormal": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
     # page ids not range checked
     "no_page_range_check": ("if (page < 0 || (int64_t)page >= d->num_pages)", "if (page < 0)"),
 }
