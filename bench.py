@@ -40,7 +40,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode",
-                    choices=["llama8b_decode", "over2gib_decode", "ragged_decode", "causal_prefill"])
+                    choices=["llama8b_decode", "over2gib_decode", "ragged_decode", "causal_prefill",
+                             "llama8b_decode_fp8"])
     ap.add_argument("--split-kv", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences (llama8b/over2gib workloads only; smaller pools for profiling)")
@@ -156,13 +157,15 @@ def measured_peaks():
 
 
 def algorithmic_bytes(wl, split_kv: int) -> dict:
-    """Bytes a decode step must move: valid K and V tokens, q, out, block-table ids, seq_lens."""
+    """Bytes a decode step must move: valid K and V tokens, q, out, block-table ids, seq_lens, and
+    for quantized pools the K and V scale of every (page read, kv head)."""
     L = wl.seq_lens.astype(np.int64)
-    kv = int(L.sum()) * wl.Hkv * wl.D * wl.esize * 2
+    kv = int(L.sum()) * wl.Hkv * wl.D * wl.kv_esize * 2
     q = wl.B * wl.Sq * wl.Hq * wl.D * wl.esize
     out = q
     ids = int(wl.nblk().sum()) * 4 + wl.B * 4
-    return {"kv": kv, "q": q, "out": out, "ids": ids, "total": kv + q + out + ids}
+    scales = int(wl.nblk().sum()) * wl.Hkv * 4 * 2 if wl.kv_dtype == "fp8e4m3" else 0
+    return {"kv": kv, "q": q, "out": out, "ids": ids, "scales": scales, "total": kv + q + out + ids + scales}
 
 
 def causal_flops(wl) -> float:
@@ -180,7 +183,8 @@ def causal_flops(wl) -> float:
 
 
 KERNEL_SOURCES = {
-    "paged_attn_mma_kernel": ("attn_mma.cu", "common.cuh", "kernels.h"),
+    "paged_attn_mma_kernel": ("attn_mma.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
+    "paged_attn_mma_kvq_kernel": ("attn_mma_kvq.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
     "paged_attn_tc05_kernel": ("attn_tc05.cu", "tc05.cuh", "common.cuh", "kernels.h"),
     "paged_attn_simt_kernel": ("attn_simt.cu", "common.cuh", "kernels.h"),
 }
@@ -213,7 +217,7 @@ def recorded_traffic(kernel: str, workload: str):
 
 def build_workload(name, batch=None):
     from paged_kv_cache_201_gb300 import workloads as W
-    if batch is not None and name in ("llama8b_decode", "over2gib_decode"):
+    if batch is not None and name in ("llama8b_decode", "over2gib_decode", "llama8b_decode_fp8"):
         return W.make(name, B=batch)
     return W.make(name)
 
@@ -225,16 +229,44 @@ def cpu_sample_rows(wl, n_seq: int):
     return rows
 
 
-def time_oracle(wl, k_host, v_host, split_kv: int, n_seq: int):
-    """Run the oracle on the first n_seq sequences; return (seconds, kv_bytes_processed, threads)."""
+def time_oracle(wl, k_host, v_host, split_kv: int, n_seq: int, scales=None):
+    """Run the oracle on the first n_seq sequences; return (seconds, kv_bytes_processed, threads).
+    ``scales`` = (k_scale, v_scale) host arrays for quantized pools."""
     import oracle
     rows = cpu_sample_rows(wl, n_seq)
     t0 = time.perf_counter()
-    oracle.workload_rows(wl, split_kv=split_kv, row_bih=rows, k_cache=k_host, v_cache=v_host,
-                         want_split=split_kv > 1)
+    if wl.kv_dtype == "fp8e4m3":
+        oracle.workload_rows_kvq(wl, split_kv=split_kv, row_bih=rows, k_cache=k_host, v_cache=v_host,
+                                 k_scale=scales[0], v_scale=scales[1], want_split=split_kv > 1)
+    else:
+        oracle.workload_rows(wl, split_kv=split_kv, row_bih=rows, k_cache=k_host, v_cache=v_host,
+                             want_split=split_kv > 1)
     dt = time.perf_counter() - t0
-    kv = int(wl.seq_lens[:n_seq].astype(np.int64).sum()) * wl.Hkv * wl.D * wl.esize * 2
+    kv = int(wl.seq_lens[:n_seq].astype(np.int64).sum()) * wl.Hkv * wl.D * wl.kv_esize * 2
     return dt, kv, oracle.num_threads()
+
+
+def host_pools(wl, k, v):
+    """Device pools -> host element arrays for the oracle (uint16 bits, float32, or uint8 E4M3 bits)."""
+    import torch
+    if wl.kv_dtype == "fp8e4m3":
+        return k.cpu().numpy(), v.cpu().numpy()
+    if wl.dtype == "f32":
+        return k.cpu().numpy(), v.cpu().numpy()
+    return k.view(torch.int16).cpu().numpy().view(np.uint16), v.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def data_text(wl) -> str:
+    if wl.kv_dtype == "fp8e4m3":
+        return ("synthetic (seeded N(0,1) K/V quantized to FP8 E4M3 with per-(page, kv head) scales "
+                "max|x|/448; N(0,1) q rounded to bf16; shuffled pages)")
+    return f"synthetic (seeded N(0,1) rounded to {wl.dtype}; shuffled pages)"
+
+
+def l2_text(wl) -> str:
+    pool = wl.num_pages * wl.page_size * wl.Hkv * wl.D * wl.kv_esize
+    rel = "larger" if pool > 129 * 2 ** 20 else "smaller"
+    return f"inputs (2 x {pool / 2 ** 30:.2f} GiB pools) {rel} than L2"
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -249,7 +281,15 @@ def run_ours(args, ws, rank, local):
     wl = build_workload(args.workload, args.batch)
     S = args.split_kv or wl.split_kv[0]
     q = W.host_to_torch(wl.q, wl.dtype).to(dev)
-    if wl.k_cache is not None:
+    kvq = wl.kv_dtype == "fp8e4m3"
+    ks = vs = None
+    if kvq:
+        if wl.k_cache is not None:
+            k, v = torch.from_numpy(wl.k_cache).to(dev), torch.from_numpy(wl.v_cache).to(dev)
+            ks, vs = torch.from_numpy(wl.k_scale).to(dev), torch.from_numpy(wl.v_scale).to(dev)
+        else:
+            k, v, ks, vs = W.fill_device_cache_fp8(wl, dev)
+    elif wl.k_cache is not None:
         k = W.host_to_torch(wl.k_cache, wl.dtype).to(dev)
         v = W.host_to_torch(wl.v_cache, wl.dtype).to(dev)
     else:
@@ -265,10 +305,11 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     def fwd():
-        if S == 1:
-            pa.paged_attn_fwd_variant(q, k, v, bt, sl, wl.causal, qo, 1, wl.scale, out, lse, args.variant, stream)
+        o, l = (out, lse) if S == 1 else (po, pl)
+        if kvq:
+            pa.paged_attn_fwd_kvq(q, k, v, ks, vs, bt, sl, wl.causal, qo, S, wl.scale, o, l, stream)
         else:
-            pa.paged_attn_fwd_variant(q, k, v, bt, sl, wl.causal, qo, S, wl.scale, po, pl, args.variant, stream)
+            pa.paged_attn_fwd_variant(q, k, v, bt, sl, wl.causal, qo, S, wl.scale, o, l, args.variant, stream)
 
     def step():
         fwd()
@@ -312,7 +353,9 @@ def run_ours(args, ws, rank, local):
     else:
         peak, peak_src = FALLBACK_HBM_GBS, "fallback"
     prefill = wl.Sq * wl.G > 16
-    if args.variant:
+    if kvq:
+        kname = "paged_attn_mma_kvq_kernel"
+    elif args.variant:
         kname = {1: "paged_attn_simt_kernel", 4: "paged_attn_tc05_kernel"}.get(args.variant, "paged_attn_mma_kernel")
     else:  # what the planner picks for this shape
         kname = "paged_attn_tc05_kernel" if (prefill and wl.Sq * wl.G >= 64 and wl.D == 128 and 128 % wl.G == 0
@@ -353,7 +396,12 @@ def run_ours(args, ws, rank, local):
             q.copy_(q_h, non_blocking=True)
             bt.copy_(bt_h, non_blocking=True)
             sl.copy_(sl_h, non_blocking=True)
-            pa.paged_attn_fwd_splitkv(q, k, v, bt, sl, wl.causal, qo, S, wl.scale, out, lse, wsp, stream=stream)
+            if kvq:
+                pa.paged_attn_fwd_kvq_splitkv(q, k, v, ks, vs, bt, sl, wl.causal, qo, S, wl.scale, out, lse, wsp,
+                                              stream=stream)
+            else:
+                pa.paged_attn_fwd_splitkv(q, k, v, bt, sl, wl.causal, qo, S, wl.scale, out, lse, wsp,
+                                          stream=stream)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
 
@@ -374,19 +422,20 @@ def run_ours(args, ws, rank, local):
         db = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
         e2e = {"value": round(job_throughput(ab["total"], ws, e2e_ms), 1), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(hb), "d2h_bytes_per_step": int(db),
-               "api": "paged_attn_fwd_splitkv (host q / block table / seq_lens in, host out / lse back)"}
+               "api": ("paged_attn_fwd_kvq_splitkv" if kvq else "paged_attn_fwd_splitkv") +
+                      " (host q / block table / seq_lens in, host out / lse back)"}
 
     # ---- CPU baseline: the oracle on a bounded sample of the same workload (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        k_h = k.view(torch.int16).cpu().numpy().view(np.uint16) if wl.dtype != "f32" else k.cpu().numpy()
-        v_h = v.view(torch.int16).cpu().numpy().view(np.uint16) if wl.dtype != "f32" else v.cpu().numpy()
+        k_h, v_h = host_pools(wl, k, v)
+        sc_h = (ks.cpu().numpy(), vs.cpu().numpy()) if kvq else None
         # one pass over the whole batch calibrates; then whole-batch passes until >= 10 s (cap 30 s)
-        dt1, kv1, thr = time_oracle(wl, k_h, v_h, S, wl.B)
+        dt1, kv1, thr = time_oracle(wl, k_h, v_h, S, wl.B, sc_h)
         reps = int(min(max(1, np.ceil(10.0 / max(dt1, 1e-3))), max(1, 30.0 // max(dt1, 1e-3))))
         dt, kvb = 0.0, 0
         for _ in range(reps):
-            d_, k_, thr = time_oracle(wl, k_h, v_h, S, wl.B)
+            d_, k_, thr = time_oracle(wl, k_h, v_h, S, wl.B, sc_h)
             dt += d_
             kvb += k_
         cpu = {"value": round(kvb / dt / 1e9, 3), "unit": "GB/s", "cores": thr, "kind": "oracle",
@@ -407,10 +456,11 @@ def run_ours(args, ws, rank, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": wl.dtype,
-        "data": "synthetic (seeded N(0,1) rounded to bf16; shuffled pages)",
+        "data": data_text(wl),
         "config": {"workload": args.workload, "B": wl.B, "Sq": wl.Sq, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
                    "page_size": wl.page_size, "num_pages": wl.num_pages, "seq_len": int(wl.seq_lens.max()),
-                   "split_kv": S, "variant": args.variant, "l2": "inputs (2 x 2 GiB pools) larger than L2",
+                   "kv_dtype": wl.kv_dtype or wl.dtype, "split_kv": S, "variant": args.variant,
+                   "l2": l2_text(wl),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "pct_of_peak": round(100.0 * value / ws / peak, 2),
         "bytes_per_step": ab,
@@ -436,6 +486,7 @@ def run_reference(args, ws, rank, local):
 
     wl = build_workload(args.workload, args.batch)
     S = args.split_kv or wl.split_kv[0]
+    sc_h = (wl.k_scale, wl.v_scale) if wl.kv_dtype == "fp8e4m3" else None
     if wl.k_cache is not None:
         k_h, v_h = wl.k_cache, wl.v_cache
     else:
@@ -443,15 +494,19 @@ def run_reference(args, ws, rank, local):
         if dev is None:
             print(json.dumps({"impl": "reference", "unavailable": "the 2-GiB pools are drawn on a CUDA device"}))
             return
-        k, v = W.fill_device_cache(wl, dev)
-        k_h = k.view(torch.int16).cpu().numpy().view(np.uint16)
-        v_h = v.view(torch.int16).cpu().numpy().view(np.uint16)
+        if wl.kv_dtype == "fp8e4m3":
+            k, v, ks, vs = W.fill_device_cache_fp8(wl, dev)
+            sc_h = (ks.cpu().numpy(), vs.cpu().numpy())
+            del ks, vs
+        else:
+            k, v = W.fill_device_cache(wl, dev)
+        k_h, v_h = host_pools(wl, k, v)
         del k, v
     n_seq = min(wl.B, 4)
-    time_oracle(wl, k_h, v_h, S, 1)  # warm-up: page in the pools and the library
+    time_oracle(wl, k_h, v_h, S, 1, sc_h)  # warm-up: page in the pools and the library
     times, kv = [], 0
     for _ in range(min(args.steps, 20)):
-        dt, kv, thr = time_oracle(wl, k_h, v_h, S, n_seq)
+        dt, kv, thr = time_oracle(wl, k_h, v_h, S, n_seq, sc_h)
         times.append(dt)
     ms = float(np.mean(times)) * 1e3
     value = kv / (ms * 1e-3) / 1e9
@@ -468,7 +523,7 @@ def run_reference(args, ws, rank, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) rounded to bf16; shuffled pages)",
+        "data": data_text(wl),
         "config": {"workload": args.workload, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
                    "page_size": wl.page_size, "split_kv": S, "sample_sequences": n_seq},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",

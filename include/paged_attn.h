@@ -42,8 +42,8 @@
 extern "C" {
 #endif
 
-/* element types */
-enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 };
+/* element types (PA_FP8_E4M3: quantized K/V pools only, see paged_attn_fwd_kvq) */
+enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 };
 
 /* status codes */
 enum {
@@ -187,6 +187,35 @@ int paged_attn_fwd_splitkv_noalloc(const void *q, const void *k_cache, const voi
                                    const int32_t *block_table, const int32_t *seq_lens, int causal,
                                    const int32_t *q_offset, int split_kv, float scale, void *out, float *lse,
                                    const pa_dims *dims, int num_sms, int64_t device_bytes, void *stream);
+
+/*
+ * paged_attn_fwd_kvq — paged_attn_fwd over quantized K/V pools.  The pages' sweeps include i8
+ * attention (rocMLIR PR #2371, Motivation; rocMLIR PR #2222, reviewed files); this library reads a
+ * quantized pool as FP8 E4M3 elements (OCP "fn" encoding: bias 7, no infinities, S.1111.111 is
+ * NaN) with one float32 scale per (page, kv head):
+ *   value of K element (page, t, kvh, e) = e4m3(k_cache[page, t, kvh, e]) * k_scale[page, kvh]
+ * and the same for V with v_scale.
+ *   k_cache, v_cache  [num_pages, page_size, num_kv_heads, head_dim] bytes (E4M3 bits), 16-byte aligned
+ *   k_scale, v_scale  [num_pages, num_kv_heads] float32, 4-byte aligned
+ *   kv_dtype          PA_FP8_E4M3 (anything else: PA_EDTYPE)
+ * q, out and dims->dtype are PA_BF16 or PA_F16 (PA_F32: PA_EDTYPE).  Every other argument, the
+ * split semantics and the outputs are those of paged_attn_fwd.  A page id outside [0, num_pages)
+ * reads as zeros with scale 0 and sets PA_ERRBIT_PAGE_RANGE.  The scaled score is
+ * scale * k_scale * q.k_stored and the weight of a V row p * v_scale, each a float32 product;
+ * the stored elements enter the tensor cores unchanged.
+ */
+int paged_attn_fwd_kvq(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                       const float *v_scale, int kv_dtype, const int32_t *block_table, const int32_t *seq_lens,
+                       int causal, const int32_t *q_offset, int split_kv, float scale, void *out, float *lse,
+                       const pa_dims *dims, void *stream);
+
+/* paged_attn_fwd_splitkv over quantized pools: paged_attn_fwd_kvq into `workspace`, then
+ * paged_attn_combine; workspace rules and split_kv = 0 as paged_attn_fwd_splitkv. */
+int paged_attn_fwd_kvq_splitkv(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                               const float *v_scale, int kv_dtype, const int32_t *block_table,
+                               const int32_t *seq_lens, int causal, const int32_t *q_offset, int split_kv,
+                               float scale, void *out, float *lse, const pa_dims *dims, void *workspace,
+                               int64_t workspace_bytes, int num_sms, int64_t device_bytes, void *stream);
 
 /*
  * paged_attn_plan — the split plan as data: plan [batch, split_kv, 2] int32 =

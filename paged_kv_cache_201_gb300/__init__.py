@@ -18,11 +18,12 @@ __all__ = [
     "PagedAttnError", "load_library", "library_path", "paged_attn_fwd", "paged_attn_fwd_variant",
     "paged_attn_combine", "paged_attn_plan", "paged_attn_debug_gather", "paged_attn_last_error_word",
     "paged_attn_strerror", "paged_attn_version", "attention", "paged_attn_auto_split",
-    "paged_attn_workspace_bytes", "paged_attn_fwd_splitkv", "paged_attn_fwd_splitkv_noalloc", "PA_F32", "PA_F16", "PA_BF16",
+    "paged_attn_workspace_bytes", "paged_attn_fwd_splitkv", "paged_attn_fwd_splitkv_noalloc", "paged_attn_fwd_kvq",
+    "paged_attn_fwd_kvq_splitkv", "attention_kvq", "PA_F32", "PA_F16", "PA_BF16", "PA_FP8_E4M3",
     "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL", "VARIANT_TC05_PREFILL",
 ]
 
-PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA_DECODE, VARIANT_MMA_PREFILL, VARIANT_TC05_PREFILL = 0, 1, 2, 3, 4
 ERRBIT_PAGE_RANGE, ERRBIT_TIMEOUT, ERRBIT_SEQ_CLIPPED = 1, 2, 4
 
@@ -75,6 +76,10 @@ def load_library(build_if_missing: bool = False):
     lib.paged_attn_fwd_splitkv.restype = ctypes.c_int
     lib.paged_attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I32, P, I32, F, P, P, D, I32, I64, P]
     lib.paged_attn_fwd_splitkv_noalloc.restype = ctypes.c_int
+    lib.paged_attn_fwd_kvq.argtypes = [P, P, P, P, P, I32, P, P, I32, P, I32, F, P, P, D, P]
+    lib.paged_attn_fwd_kvq.restype = ctypes.c_int
+    lib.paged_attn_fwd_kvq_splitkv.argtypes = [P, P, P, P, P, I32, P, P, I32, P, I32, F, P, P, D, P, I64, I32, I64, P]
+    lib.paged_attn_fwd_kvq_splitkv.restype = ctypes.c_int
     lib.paged_attn_debug_gather.argtypes = [P, P, P, D, I32, P, P]
     lib.paged_attn_last_error_word.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.paged_attn_strerror.argtypes = [I32]
@@ -257,6 +262,66 @@ def paged_attn_fwd_splitkv_noalloc(q, k_cache, v_cache, block_table, seq_lens, c
     _raise(rc, "paged_attn_fwd_splitkv_noalloc")
 
 
+def _check_e4m3_pool(t, name):
+    """An FP8 E4M3 pool: uint8 bits or torch.float8_e4m3fn, [P, ps, Hkv, D]."""
+    torch = _torch()
+    _check(t, name, ndim=4)
+    if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        raise TypeError(f"{name} must be uint8 (E4M3 bits) or float8_e4m3fn, got {t.dtype}")
+
+
+def _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, out, lse):
+    torch = _torch()
+    _check(q, "q", ndim=4)
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"q must be bf16 or f16 with FP8 pools, got {q.dtype}")
+    _check_e4m3_pool(k_cache, "k_cache")
+    _check_e4m3_pool(v_cache, "v_cache")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    P, _, Hkv, _ = k_cache.shape
+    for t, name in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _check(t, name, torch.float32, 2)
+        if tuple(t.shape) != (P, Hkv):
+            raise ValueError(f"{name} must be [num_pages, num_kv_heads] = {(P, Hkv)}, got {tuple(t.shape)}")
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    _check(q_offset, "q_offset", torch.int32, 1)
+    _check(out, "out")
+    _check(lse, "lse", torch.float32)
+    return dims_of(q, k_cache, block_table)
+
+
+def paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, causal, q_offset, split_kv,
+                       scale, out, lse, stream=None) -> None:
+    """Forward over FP8 E4M3 pools with [num_pages, Hkv] float32 scales; see ``paged_attn_fwd_kvq`` in
+    include/paged_attn.h.  Outputs as ``paged_attn_fwd``."""
+    dims = _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, out, lse)
+    rc = load_library().paged_attn_fwd_kvq(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), PA_FP8_E4M3, _ptr(block_table),
+        _ptr(seq_lens), int(bool(causal)), _ptr(q_offset), int(split_kv), float(scale), _ptr(out), _ptr(lse),
+        ctypes.byref(dims), _stream(stream))
+    _raise(rc, "paged_attn_fwd_kvq")
+
+
+def paged_attn_fwd_kvq_splitkv(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, causal, q_offset,
+                               split_kv, scale, out, lse, workspace, num_sms=None, device_bytes=None,
+                               stream=None) -> None:
+    """``paged_attn_fwd_splitkv`` over FP8 E4M3 pools (split forward + combine in one call)."""
+    dims = _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, out, lse)
+    _check(workspace, "workspace")
+    if num_sms is None or device_bytes is None:
+        n, m = _device_info(q.device)
+        num_sms = n if num_sms is None else num_sms
+        device_bytes = m if device_bytes is None else device_bytes
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().paged_attn_fwd_kvq_splitkv(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), PA_FP8_E4M3, _ptr(block_table),
+        _ptr(seq_lens), int(bool(causal)), _ptr(q_offset), int(split_kv), float(scale), _ptr(out), _ptr(lse),
+        ctypes.byref(dims), _ptr(workspace), int(ws_bytes), int(num_sms), int(device_bytes), _stream(stream))
+    _raise(rc, "paged_attn_fwd_kvq_splitkv")
+
+
 def paged_attn_combine(part_out, part_lse, out, lse=None, stream=None) -> None:
     """Merge split partials: part_out [S, ..., D] f32, part_lse [S, ...] f32 -> out [..., D], lse [...]."""
     torch = _torch()
@@ -344,5 +409,27 @@ def attention(q, k_cache, v_cache, block_table, seq_lens, *, causal: bool = Fals
             po, pl = partials
         paged_attn_fwd_variant(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale, po,
                                pl, variant, stream)
+        paged_attn_combine(po, pl, out, lse, stream)
+    return (out, lse) if want_lse else out
+
+
+def attention_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, *, causal: bool = False,
+                  q_offset=None, split_kv: int = 1, scale: Optional[float] = None, want_lse: bool = False,
+                  stream=None):
+    """``attention`` over FP8 E4M3 pools with per-(page, kv head) scales."""
+    torch = _torch()
+    B, Sq, Hq, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device) if (want_lse or split_kv > 1) else None
+    if split_kv == 1:
+        paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, causal, q_offset, 1, scale,
+                           out, lse, stream)
+    else:
+        po = torch.empty((split_kv, B, Sq, Hq, D), dtype=torch.float32, device=q.device)
+        pl = torch.empty((split_kv, B, Sq, Hq), dtype=torch.float32, device=q.device)
+        paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, causal, q_offset, split_kv,
+                           scale, po, pl, stream)
         paged_attn_combine(po, pl, out, lse, stream)
     return (out, lse) if want_lse else out

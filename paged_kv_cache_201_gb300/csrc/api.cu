@@ -99,6 +99,22 @@ int make_pool_map(CUtensorMap *m, const void *base, const pa_dims *d, int halves
     return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
 }
 
+// 3-D view of one E4M3 pool for TMA: (byte within a row, token, kv head); one box = the page_size
+// rows of one page and one kv head, copied as they are (no swizzle: the consumers read whole rows).
+int make_pool_map_e4m3(CUtensorMap *m, const void *base, const pa_dims *d) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PA_ECUDA;
+    const cuuint64_t D = (cuuint64_t)d->head_dim, Hkv = (cuuint64_t)d->num_kv_heads;
+    const cuuint64_t dims[3] = {D, (cuuint64_t)d->num_pages * (cuuint64_t)d->page_size, Hkv};
+    const cuuint64_t strides[2] = {Hkv * D, D};
+    const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)d->page_size, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
+}
+
 // 4-D view of q for the tcgen05 kernel: (d within a half, half, query head, token of B*Sq);
 // one box = one half of a 128-row tile: 128/G consecutive tokens x the G heads of a kv head.
 int make_q_map(CUtensorMap *m, const void *q, const pa_dims *d) {
@@ -133,6 +149,74 @@ int choose_variant(const pa_dims *d) {
     return PA_VARIANT_MMA_PREFILL;
 }
 
+// Pointer and alignment checks shared by the forward entry points.
+int check_fwd_pointers(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                       const int32_t *seq_lens, const int32_t *q_offset, int split_kv, const void *out,
+                       const float *lse) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PA_EINVAL;
+    if (split_kv > 1 && !lse) return PA_EINVAL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(q_offset) & 3u))
+        return PA_EINVAL;
+    return PA_OK;
+}
+
+pa::FwdParams fill_params(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                          const int32_t *seq_lens, int causal, const int32_t *q_offset, int split_kv, float scale,
+                          void *out, float *lse, const pa_dims *dims, unsigned int *err) {
+    pa::FwdParams p{};
+    p.q = q;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.q_offset = q_offset;
+    p.out = out;
+    p.lse = lse;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.err = err;
+    p.num_pages = dims->num_pages;
+    p.B = dims->batch;
+    p.Sq = dims->q_len;
+    p.Hq = dims->num_q_heads;
+    p.Hkv = dims->num_kv_heads;
+    p.D = dims->head_dim;
+    p.ps = dims->page_size;
+    p.W = dims->bt_stride;
+    p.G = dims->num_q_heads / dims->num_kv_heads;
+    p.rows = dims->q_len * p.G;
+    p.causal = causal ? 1 : 0;
+    p.split_kv = split_kv;
+    p.scale_log2 = scale * pa::kLog2e;
+    p.row_tiles = 1;
+    return p;
+}
+
+// Split forward into a workspace, then the fp32 combine (rocMLIR PR #2371): the body of the
+// single-call entry points.  fwd(S, part_out, part_lse) runs the forward with S partitions.
+template <typename Fwd>
+int splitkv_call(const pa_dims *dims, int split_kv, void *out, float *lse, void *workspace, int64_t workspace_bytes,
+                 int num_sms, int64_t device_bytes, void *stream, Fwd fwd) {
+    if (split_kv < 0 || split_kv > 65535) return PA_EINVAL;
+    if (split_kv == 0) {
+        split_kv = paged_attn_auto_split(dims, num_sms, device_bytes);
+        if (split_kv < 0) return split_kv;
+    }
+    if (split_kv == 1) return fwd(1, out, lse);
+    const int64_t need = paged_attn_workspace_bytes(dims, split_kv, num_sms, device_bytes);
+    if (need < 0) return (int)need;
+    const int64_t rows = (int64_t)dims->batch * dims->q_len * dims->num_q_heads;
+    if (rows == 0) return PA_OK;
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_EINVAL;
+    if (!out || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return PA_EINVAL;
+    float *part_out = static_cast<float *>(workspace);
+    float *part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                ((int64_t)split_kv * rows * dims->head_dim * 4 + 255) / 256 * 256);
+    int rc = fwd(split_kv, part_out, part_lse);
+    if (rc != PA_OK) return rc;
+    return paged_attn_combine(part_out, part_lse, split_kv, rows, dims->head_dim, dims->dtype, out, lse, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -146,12 +230,8 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
     if (!isfinite(scale)) return PA_EINVAL;
     const int64_t nrows = (int64_t)dims->batch * dims->q_len * dims->num_q_heads;
     if (nrows == 0) return PA_OK;
-    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PA_EINVAL;
-    if (split_kv > 1 && !lse) return PA_EINVAL;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_EINVAL;
-    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
-        (reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(q_offset) & 3u))
-        return PA_EINVAL;
+    rc = check_fwd_pointers(q, k_cache, v_cache, block_table, seq_lens, q_offset, split_kv, out, lse);
+    if (rc != PA_OK) return rc;
     if (variant == PA_VARIANT_AUTO) variant = choose_variant(dims);
     const int G = dims->num_q_heads / dims->num_kv_heads;
     const int rows = dims->q_len * G;
@@ -176,30 +256,8 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
     rc = error_word_ptr(&err);
     if (rc != PA_OK) return rc;
 
-    pa::FwdParams p{};
-    p.q = q;
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
-    p.q_offset = q_offset;
-    p.out = out;
-    p.lse = lse;
-    p.k_cache = k_cache;
-    p.v_cache = v_cache;
-    p.err = err;
-    p.num_pages = dims->num_pages;
-    p.B = dims->batch;
-    p.Sq = dims->q_len;
-    p.Hq = dims->num_q_heads;
-    p.Hkv = dims->num_kv_heads;
-    p.D = dims->head_dim;
-    p.ps = dims->page_size;
-    p.W = dims->bt_stride;
-    p.G = G;
-    p.rows = rows;
-    p.causal = causal ? 1 : 0;
-    p.split_kv = split_kv;
-    p.scale_log2 = scale * pa::kLog2e;
-    p.row_tiles = 1;
+    pa::FwdParams p = fill_params(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale,
+                                  out, lse, dims, err);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -274,27 +332,58 @@ int paged_attn_fwd_splitkv(const void *q, const void *k_cache, const void *v_cac
                            int num_sms, int64_t device_bytes, void *stream) {
     int rc = check_dims(dims);
     if (rc != PA_OK) return rc;
-    if (split_kv < 0 || split_kv > 65535) return PA_EINVAL;
-    if (split_kv == 0) {
-        split_kv = paged_attn_auto_split(dims, num_sms, device_bytes);
-        if (split_kv < 0) return split_kv;
-    }
-    if (split_kv == 1)
-        return paged_attn_fwd(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, 1, scale, out, lse, dims,
-                              stream);
-    const int64_t need = paged_attn_workspace_bytes(dims, split_kv, num_sms, device_bytes);
-    if (need < 0) return (int)need;
-    const int64_t rows = (int64_t)dims->batch * dims->q_len * dims->num_q_heads;
-    if (rows == 0) return PA_OK;
-    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_EINVAL;
-    if (!out || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return PA_EINVAL;
-    float *part_out = static_cast<float *>(workspace);
-    float *part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                                ((int64_t)split_kv * rows * dims->head_dim * 4 + 255) / 256 * 256);
-    rc = paged_attn_fwd(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale, part_out,
-                        part_lse, dims, stream);
+    return splitkv_call(dims, split_kv, out, lse, workspace, workspace_bytes, num_sms, device_bytes, stream,
+                        [&](int S, void *o, float *l) {
+                            return paged_attn_fwd(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, S,
+                                                  scale, o, l, dims, stream);
+                        });
+}
+
+int paged_attn_fwd_kvq(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                       const float *v_scale, int kv_dtype, const int32_t *block_table, const int32_t *seq_lens,
+                       int causal, const int32_t *q_offset, int split_kv, float scale, void *out, float *lse,
+                       const pa_dims *dims, void *stream) {
+    int rc = check_dims(dims);
     if (rc != PA_OK) return rc;
-    return paged_attn_combine(part_out, part_lse, split_kv, rows, dims->head_dim, dims->dtype, out, lse, stream);
+    if (dims->dtype == PA_F32 || kv_dtype != PA_FP8_E4M3) return PA_EDTYPE;
+    if (split_kv < 1 || split_kv > 65535) return PA_EINVAL;
+    if (!isfinite(scale)) return PA_EINVAL;
+    const int64_t nrows = (int64_t)dims->batch * dims->q_len * dims->num_q_heads;
+    if (nrows == 0) return PA_OK;
+    rc = check_fwd_pointers(q, k_cache, v_cache, block_table, seq_lens, q_offset, split_kv, out, lse);
+    if (rc != PA_OK) return rc;
+    if (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+        return PA_EINVAL;
+
+    unsigned int *err = nullptr;
+    rc = error_word_ptr(&err);
+    if (rc != PA_OK) return rc;
+    pa::FwdParams p = fill_params(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale,
+                                  out, lse, dims, err);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    CUtensorMap tmk, tmv;
+    if ((rc = make_pool_map_e4m3(&tmk, k_cache, dims)) != PA_OK) return rc;
+    if ((rc = make_pool_map_e4m3(&tmv, v_cache, dims)) != PA_OK) return rc;
+    const int mode = p.rows <= pa::kDecodeRows ? pa::MODE_DECODE : pa::MODE_PREFILL;
+    if (mode == pa::MODE_PREFILL) p.row_tiles = (p.rows + pa::kPrefillRows - 1) / pa::kPrefillRows;
+    return cuda_status(pa::launch_mma_kvq(p, mode, dims->dtype, tmk, tmv, static_cast<cudaStream_t>(stream)));
+}
+
+int paged_attn_fwd_kvq_splitkv(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                               const float *v_scale, int kv_dtype, const int32_t *block_table,
+                               const int32_t *seq_lens, int causal, const int32_t *q_offset, int split_kv,
+                               float scale, void *out, float *lse, const pa_dims *dims, void *workspace,
+                               int64_t workspace_bytes, int num_sms, int64_t device_bytes, void *stream) {
+    int rc = check_dims(dims);
+    if (rc != PA_OK) return rc;
+    if (dims->dtype == PA_F32 || kv_dtype != PA_FP8_E4M3) return PA_EDTYPE;
+    return splitkv_call(dims, split_kv, out, lse, workspace, workspace_bytes, num_sms, device_bytes, stream,
+                        [&](int S, void *o, float *l) {
+                            return paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, block_table,
+                                                      seq_lens, causal, q_offset, S, scale, o, l, dims, stream);
+                        });
 }
 
 int paged_attn_combine(const float *part_out, const float *part_lse, int split_kv, int64_t rows, int head_dim,

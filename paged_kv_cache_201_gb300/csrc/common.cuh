@@ -28,6 +28,8 @@ struct FwdParams {
     float *lse;                // S == 1: [B,Sq,Hq] or null; S > 1: [S,B,Sq,Hq]
     const void *k_cache;       // raw pools (used by the CUDA-core kernel)
     const void *v_cache;
+    const float *k_scale;      // FP8 pools: [num_pages, Hkv] per-(page, kv head) scales; else null
+    const float *v_scale;
     unsigned int *err;         // device error word
     long long num_pages;
     int B, Sq, Hq, Hkv, D, ps, W;
@@ -132,6 +134,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, 
         "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+// 3-D tiled load global -> shared, completion counted on `bar` (bytes).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int c1,
+                                            int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
 

@@ -16,7 +16,17 @@ class DeviceWorkload:
         import torch
         self.wl = wl
         self.q = W.host_to_torch(wl.q, wl.dtype).to(device)
-        if wl.k_cache is not None:
+        self.kvq = getattr(wl, "kv_dtype", None) == "fp8e4m3"
+        self.ks = self.vs = None
+        if self.kvq:
+            if wl.k_cache is not None:
+                self.k = torch.from_numpy(np.ascontiguousarray(wl.k_cache, dtype=np.uint8)).to(device)
+                self.v = torch.from_numpy(np.ascontiguousarray(wl.v_cache, dtype=np.uint8)).to(device)
+                self.ks = torch.from_numpy(np.ascontiguousarray(wl.k_scale, dtype=np.float32)).to(device)
+                self.vs = torch.from_numpy(np.ascontiguousarray(wl.v_scale, dtype=np.float32)).to(device)
+            else:
+                self.k, self.v, self.ks, self.vs = W.fill_device_cache_fp8(wl, device)
+        elif wl.k_cache is not None:
             self.k = W.host_to_torch(wl.k_cache, wl.dtype).to(device)
             self.v = W.host_to_torch(wl.v_cache, wl.dtype).to(device)
         else:
@@ -26,8 +36,14 @@ class DeviceWorkload:
         self.qo = None if wl.q_offset is None else torch.from_numpy(np.ascontiguousarray(wl.q_offset)).to(device)
 
     def host_pools(self):
-        """The device pools as host element arrays (uint16 bits or float32), for the oracle."""
+        """The device pools as host element arrays (uint16 bits or float32; uint8 E4M3 bits for
+        quantized pools), for the oracle."""
+        if self.kvq:
+            return self.k.cpu().numpy(), self.v.cpu().numpy()
         return to_host_elems(self.k, self.wl.dtype), to_host_elems(self.v, self.wl.dtype)
+
+    def host_scales(self):
+        return self.ks.cpu().numpy(), self.vs.cpu().numpy()
 
 
 def to_host_elems(t, dtype):
@@ -53,15 +69,22 @@ def run(dw: DeviceWorkload, split_kv: int, variant: int = 0):
     wl = dw.wl
     B, Sq, Hq, D = wl.B, wl.Sq, wl.Hq, wl.D
     res = {}
+
+    def fwd(S, o, l):
+        if dw.kvq:
+            assert variant == 0
+            pa.paged_attn_fwd_kvq(dw.q, dw.k, dw.v, dw.ks, dw.vs, dw.bt, dw.sl, wl.causal, dw.qo, S, wl.scale, o, l)
+        else:
+            pa.paged_attn_fwd_variant(dw.q, dw.k, dw.v, dw.bt, dw.sl, wl.causal, dw.qo, S, wl.scale, o, l, variant)
+
     if split_kv == 1:
         out = torch.empty_like(dw.q)
         lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=dw.q.device)
-        pa.paged_attn_fwd_variant(dw.q, dw.k, dw.v, dw.bt, dw.sl, wl.causal, dw.qo, 1, wl.scale, out, lse, variant)
+        fwd(1, out, lse)
     else:
         po = torch.empty((split_kv, B, Sq, Hq, D), dtype=torch.float32, device=dw.q.device)
         pl = torch.empty((split_kv, B, Sq, Hq), dtype=torch.float32, device=dw.q.device)
-        pa.paged_attn_fwd_variant(dw.q, dw.k, dw.v, dw.bt, dw.sl, wl.causal, dw.qo, split_kv, wl.scale, po, pl,
-                                  variant)
+        fwd(split_kv, po, pl)
         out = torch.empty_like(dw.q)
         lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=dw.q.device)
         pa.paged_attn_combine(po, pl, out, lse)

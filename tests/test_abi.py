@@ -132,3 +132,29 @@ def test_auto_split_and_workspace_host_logic(lib):
     assert auto(ctypes.byref(d), 0, 8 << 30) == EINVAL
     assert wsb(ctypes.byref(d), -1, 152, 8 << 30) == EINVAL
     assert wsb(ctypes.byref(d), 1, 152, 8 << 30) == 0
+
+
+def _kvq(lib, dims, kv_dtype=pa.PA_FP8_E4M3, split=1, k_scale=FAKE, v_scale=FAKE, lse=FAKE, k=FAKE):
+    return lib.paged_attn_fwd_kvq(FAKE, k, FAKE, k_scale, v_scale, kv_dtype, FAKE, FAKE, 0, None, split, 0.1, FAKE,
+                                  lse, None if dims is None else ctypes.byref(dims), None)
+
+
+def test_fwd_kvq_validation(lib):
+    """FP8-pool entry points: element types, scales and the shared checks, all before any launch."""
+    assert _kvq(lib, None) == EINVAL
+    assert _kvq(lib, _dims(dtype=pa.PA_F32)) == EDTYPE              # f32 queries are not read against FP8 pools
+    assert _kvq(lib, _dims(), kv_dtype=pa.PA_BF16) == EDTYPE       # pools must be E4M3
+    assert _kvq(lib, _dims(head_dim=96)) == EUNSUP
+    assert _kvq(lib, _dims(), split=0) == EINVAL
+    assert _kvq(lib, _dims(), k_scale=None) == EINVAL
+    assert _kvq(lib, _dims(), v_scale=FAKE + 2) == EINVAL
+    assert _kvq(lib, _dims(), k=FAKE + 8) == EINVAL                # pools 16-byte aligned
+    assert _kvq(lib, _dims(), split=2, lse=None) == EINVAL
+    assert _kvq(lib, _dims(batch=0), k_scale=None) == OK            # no rows: nothing to check further
+    f = lib.paged_attn_fwd_kvq_splitkv
+    d = _dims()
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, pa.PA_F16, FAKE, FAKE, 0, None, 2, 0.1, FAKE, FAKE, ctypes.byref(d),
+             FAKE, 1 << 20, 152, 280 << 30, None) == EDTYPE
+    # split 2 needs 2 * 16 rows * (128 + 1) * 4 bytes rounded up: a 16-byte workspace is too small
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, pa.PA_FP8_E4M3, FAKE, FAKE, 0, None, 2, 0.1, FAKE, FAKE, ctypes.byref(d),
+             FAKE, 16, 152, 280 << 30, None) == EINVAL
