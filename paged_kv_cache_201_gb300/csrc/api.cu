@@ -100,7 +100,8 @@ int make_pool_map(CUtensorMap *m, const void *base, const pa_dims *d, int halves
 }
 
 // 3-D view of one E4M3 pool for TMA: (byte within a row, token, kv head); one box = the page_size
-// rows of one page and one kv head, copied as they are (no swizzle: the consumers read whole rows).
+// rows of one page and one kv head.  128-byte rows (head_dim 128) land with the 128-byte swizzle,
+// which the kernel's conflict-free operand loads rely on; 64-byte rows land as they are.
 int make_pool_map_e4m3(CUtensorMap *m, const void *base, const pa_dims *d) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PA_ECUDA;
@@ -109,8 +110,9 @@ int make_pool_map_e4m3(CUtensorMap *m, const void *base, const pa_dims *d) {
     const cuuint64_t strides[2] = {Hkv * D, D};
     const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)d->page_size, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle swz = d->head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
 }

@@ -10,14 +10,21 @@
 //     head: one 3-D TMA box, half the bytes of a 16-bit page) into a ring of 64-key stages, and
 //     with the page ids it loads the pages' K and V scales, which it leaves in shared memory
 //     beside the stage before arming the stage's barriers.
-//   * consumer warp w widens keys [16w, 16w + 16) of each stage to 16-bit rows (K to the query's
-//     type, V to bf16).  Both are exact: every E4M3 value is an f16 and a bf16 number.  The warp
-//     then releases the ring stage at once, so the next pages stream in while it computes.
-//     Decode mode reads only its own 16 keys; prefill mode (each warp owning 16 query rows over
-//     all 64 keys) meets the other warps at a named barrier first.
-//   * the scale of key j's page enters its score (scale x k_scale x q.k) and the weight of its
-//     V row (p_j x v_scale); the softmax sum takes the unscaled p_j.  The tensor-core operands
-//     are the stored values, so the only rounding added is that of these float products.
+//   * Q K^T runs in f16 straight from the ring: a lane converts the E4M3 bytes of its key into the
+//     MMA operand registers (one conversion per element pair, exact: every E4M3 value is an f16
+//     number).  The head dimension is visited in a permuted order, the same for Q and K, so that
+//     a lane's operand bytes are 16 contiguous bytes of one row (one conflict-free shared load);
+//     a dot product does not depend on the order of its terms.  bf16 queries enter as f16 after
+//     multiplying each query row by a power of two that puts its largest element in [2^14, 2^15);
+//     the score is scaled back by the inverse power exactly.
+//   * V rows are widened to f16 in shared memory (exact) for the transposing ldmatrix; warp w
+//     widens keys [16w, 16w + 16) of the stage.  Decode mode reads only its own 16 keys; prefill
+//     mode (each warp owning 16 query rows over all 64 keys) meets the other warps at a named
+//     barrier first.
+//   * the scale of key j's page multiplies its score (scale x k_scale x q.k), and each 16-key step
+//     of P V is accumulated separately and added to O times that step's page v_scale (a 16-key
+//     step never crosses a page).  P itself is the unscaled softmax weight in [0, 1], split into
+//     an f16 high part and its rounding remainder.
 #include <type_traits>
 
 #include "mma_common.cuh"
@@ -67,6 +74,21 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
 // 16-bit rows at `wide` (bf16 when TO_BF16, else f16).  Keys at or past key_end (relative to the
 // stage) become zero rows: they hold whatever the ring held before, and a zero V row keeps
 // 0 x NaN out of the output.
+// Shared address of 16-byte chunk c of key row k in an E4M3 ring stage: rows of D bytes; for
+// D = 128 the TMA wrote them with the 128-byte swizzle (chunk c at position c XOR (k % 8)).
+template <int D>
+__device__ __forceinline__ uint32_t ring_chunk_addr(uint32_t stage, int k, int c) {
+    const int pc = (D == 128) ? (c ^ (k & 7)) : c;
+    return stage + (uint32_t)(k * D + (pc << 4));
+}
+
+__device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t (&w)[4]) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
 template <int D, bool TO_BF16>
 __device__ __forceinline__ void widen_keys(uint32_t ring, uint32_t wide, int kw0, int key_end, int lane) {
     constexpr int C8 = D / 16;  // 16-byte E4M3 chunks per row
@@ -77,15 +99,12 @@ __device__ __forceinline__ void widen_keys(uint32_t ring, uint32_t wide, int kw0
         const int c8 = idx % C8;
         uint32_t w[8];
         if (key < key_end) {
-            uint32_t x0, x1, x2, x3;
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                         : "r"(ring + (uint32_t)(key * D + c8 * 16))
-                         : "memory");
-            e4m3x4_to_f16x4(x0, w[0], w[1]);
-            e4m3x4_to_f16x4(x1, w[2], w[3]);
-            e4m3x4_to_f16x4(x2, w[4], w[5]);
-            e4m3x4_to_f16x4(x3, w[6], w[7]);
+            uint32_t x[4];
+            lds_v4(ring_chunk_addr<D>(ring, key, c8), x);
+            e4m3x4_to_f16x4(x[0], w[0], w[1]);
+            e4m3x4_to_f16x4(x[1], w[2], w[3]);
+            e4m3x4_to_f16x4(x[2], w[4], w[5]);
+            e4m3x4_to_f16x4(x[3], w[6], w[7]);
             if (TO_BF16) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) w[i] = f16x2_to_bf16x2(w[i]);
@@ -104,17 +123,49 @@ __device__ __forceinline__ void widen_keys(uint32_t ring, uint32_t wide, int kw0
     }
 }
 
+// Power of two that brings a row whose largest magnitude is amax into f16 with amax x scale in
+// [2^14, 2^15) (clamped to 2^[-113, 100], so both it and its inverse are normal floats); the inverse
+// goes to inv.  Elements below 2^-28 amax become f16 subnormals: their terms of a dot product are
+// below 2^-28 of its largest term.
+__device__ __forceinline__ float f16_row_scale(float amax, float &inv) {
+    const int e = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;  // amax in [2^e, 2^(e+1))
+    const int s = max(-113, min(14 - e, 100));
+    inv = __uint_as_float((uint32_t)(127 - s) << 23);
+    return __uint_as_float((uint32_t)(127 + s) << 23);
+}
+
+// bf16 pair x (power of two) -> f16 pair, round to nearest even (exact for normal f16 results:
+// a bf16 number has 8 significant bits).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(w << 16) * sc, __uint_as_float(w & 0xffff0000u) * sc);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// K operand of one n-tile (8 keys) for every MMA step: this lane's key row `k`, bytes
+// [tq D/4, (tq + 1) D/4) of it, as f16 pairs.  Step kk takes bytes tq D/4 + 4 kk + {0, 1} (b0)
+// and + {2, 3} (b1); the query fragments use the same head-dim order.  For D = 128 the lane's two
+// chunks are 2 tq and 2 tq + 1: with the swizzle, the two keys of a load phase then read
+// chunks of opposite parity, so the 8 lanes of a phase hit 8 different banks.
+template <int D>
+__device__ __forceinline__ void load_k_frags(uint32_t stage, int k, int tq, uint32_t (&bk)[D / 16][2]) {
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+        uint32_t w[4];
+        lds_v4(ring_chunk_addr<D>(stage, k, (D / 64) * tq + h), w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) e4m3x4_to_f16x4(w[i], bk[4 * h + i][0], bk[4 * h + i][1]);
+    }
+}
+
 }  // namespace
 
 template <typename T, int D, int MODE, int NSTAGE>
 __global__ void __launch_bounds__(kMmaThreads, 2)
     paged_attn_mma_kvq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                               const FwdParams p, int ps_shift) {
-    using Op = MmaOp<T>;                  // Q K^T in the query's type
-    using OpV = MmaOp<__nv_bfloat16>;     // P V in bf16 (P x v_scale keeps bf16's exponent range)
-    constexpr bool kKBf16 = std::is_same<T, __nv_bfloat16>::value;
+    using Op = MmaOp<__half>;  // Q K^T and P V both in f16
+    constexpr bool kQBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr int kStage8 = Geo8<D>::kStage8;
-    constexpr int kWide = Geo8<D>::kWide;
     constexpr int KB = (MODE == MODE_DECODE) ? 16 : 32;   // keys per softmax block
     constexpr int SUBS = (MODE == MODE_DECODE) ? 1 : 2;   // blocks a warp handles per stage
     constexpr int NTB = KB / 8;                           // score n-tiles per block
@@ -163,8 +214,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
-    const uint32_t wideK = sbase + (uint32_t)(NSTAGE * 2 * kStage8);
-    const uint32_t wideV = wideK + (uint32_t)kWide;
+    const uint32_t wideV = sbase + (uint32_t)(NSTAGE * 2 * kStage8);
     const uint32_t bar_fk = smem_u32(&bars[0]);
     const uint32_t bar_fv = smem_u32(&bars[NSTAGE]);
     const uint32_t bar_em = smem_u32(&bars[2 * NSTAGE]);
@@ -280,31 +330,64 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     const int tq = lane & 3;
     const int rbase = (MODE == MODE_DECODE) ? 0 : row0 + warp * 16;
     const int ra = rbase + g, rb = rbase + g + 8;
-    const int kw0 = warp * 16;  // the stage keys this warp widens (and, in decode mode, reads)
+    const int kw0 = warp * 16;  // the stage keys whose V rows this warp widens (decode mode: its keys)
 
+    // Q fragments in f16 over the permuted head-dim order: lane tq holds elements
+    // [tq D/4, (tq + 1) D/4) of rows ra and rb, and step kk takes elements tq D/4 + 4 kk + {0, 1}
+    // (a0 / a1) and + {2, 3} (a2 / a3).  q_inv_* undoes the power-of-two scaling of bf16 rows.
     uint32_t qf[D / 16][4];
+    float q_inv_a = 1.f, q_inv_b = 1.f;
     {
+        constexpr int NW = D / 8;  // element pairs a lane holds per row
+        uint32_t wa[NW], wb[NW];
         const T *q = reinterpret_cast<const T *>(p.q);
         const bool va = ra < p.rows, vb = rb < p.rows;
-        const T *qa = q + (va ? out_row_index(p, b, kvh, ra) * D : 0);
-        const T *qb = q + (vb ? out_row_index(p, b, kvh, rb) * D : 0);
+        const uint4 *qa = reinterpret_cast<const uint4 *>(q + (va ? out_row_index(p, b, kvh, ra) * D : 0) + tq * (D / 4));
+        const uint4 *qb = reinterpret_cast<const uint4 *>(q + (vb ? out_row_index(p, b, kvh, rb) * D : 0) + tq * (D / 4));
+#pragma unroll
+        for (int i = 0; i < NW / 4; ++i) {
+            const uint4 xa = va ? __ldg(qa + i) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 xb = vb ? __ldg(qb + i) : make_uint4(0u, 0u, 0u, 0u);
+            wa[4 * i] = xa.x, wa[4 * i + 1] = xa.y, wa[4 * i + 2] = xa.z, wa[4 * i + 3] = xa.w;
+            wb[4 * i] = xb.x, wb[4 * i + 1] = xb.y, wb[4 * i + 2] = xb.z, wb[4 * i + 3] = xb.w;
+        }
+        if (kQBf16) {
+            float am_a = 0.f, am_b = 0.f;
+#pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                am_a = fmaxf(am_a, fmaxf(fabsf(__uint_as_float(wa[i] << 16)), fabsf(__uint_as_float(wa[i] & 0xffff0000u))));
+                am_b = fmaxf(am_b, fmaxf(fabsf(__uint_as_float(wb[i] << 16)), fabsf(__uint_as_float(wb[i] & 0xffff0000u))));
+            }
+            am_a = fmaxf(am_a, __shfl_xor_sync(0xffffffffu, am_a, 1));
+            am_a = fmaxf(am_a, __shfl_xor_sync(0xffffffffu, am_a, 2));
+            am_b = fmaxf(am_b, __shfl_xor_sync(0xffffffffu, am_b, 1));
+            am_b = fmaxf(am_b, __shfl_xor_sync(0xffffffffu, am_b, 2));
+            const float sc_a = f16_row_scale(am_a, q_inv_a), sc_b = f16_row_scale(am_b, q_inv_b);
+#pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                wa[i] = bf16x2_to_f16x2_scaled(wa[i], sc_a);
+                wb[i] = bf16x2_to_f16x2_scaled(wb[i], sc_b);
+            }
+        }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const int c0 = kk * 16 + 2 * tq;
-            qf[kk][0] = va ? __ldg(reinterpret_cast<const uint32_t *>(qa + c0)) : 0u;
-            qf[kk][1] = vb ? __ldg(reinterpret_cast<const uint32_t *>(qb + c0)) : 0u;
-            qf[kk][2] = va ? __ldg(reinterpret_cast<const uint32_t *>(qa + c0 + 8)) : 0u;
-            qf[kk][3] = vb ? __ldg(reinterpret_cast<const uint32_t *>(qb + c0 + 8)) : 0u;
+            qf[kk][0] = wa[2 * kk];
+            qf[kk][1] = wb[2 * kk];
+            qf[kk][2] = wa[2 * kk + 1];
+            qf[kk][3] = wb[2 * kk + 1];
         }
     }
     const int lim_a = ra < p.rows ? min(k_hi_split, row_key_limit(p, b, L, ra / p.G)) : k_lo;
     const int lim_b = rb < p.rows ? min(k_hi_split, row_key_limit(p, b, L, rb / p.G)) : k_lo;
+    // scale x log2(e) x the rows' inverse query scaling; times k_scale of the key's page below
+    const float srow_a = p.scale_log2 * q_inv_a, srow_b = p.scale_log2 * q_inv_b;
 
     float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;
     float acc[D / 8][4];
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
     const int warp_lim = __reduce_max_sync(0xffffffffu, (unsigned)max(lim_a, lim_b));
+    const int mi = lane >> 3, rr = lane & 7;
 
     bool bad = false;
     for (int t = 0; t < n_tiles; ++t) {
@@ -314,116 +397,128 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
         const uint32_t kring = sbase + (uint32_t)(st * 2 * kStage8);
         const uint32_t vring = kring + (uint32_t)kStage8;
         const int tile_k0 = k_lo + t * kMmaTileKeys;
-        // decode mode reads only this warp's keys, prefill mode every warp's
-        const bool widen = (MODE == MODE_PREFILL) || (tile_k0 + kw0 < min(k_hi, warp_lim));
 
-        if (MODE == MODE_PREFILL) named_bar_sync(1, kMmaConsumerWarps * 32);  // previous rows read by all
         if (!bad) {
             const bool ok = mbar_wait(bar_fk + 8 * st, par, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
-        if (!bad && widen) widen_keys<D, kKBf16>(kring, wideK, kw0, k_hi - tile_k0, lane);
-        if (!bad) {
-            const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
-            bad = __any_sync(0xffffffffu, !ok);
+        if (MODE == MODE_PREFILL) {
+            named_bar_sync(1, kMmaConsumerWarps * 32);  // every warp is done with the previous V rows
+            if (!bad) {
+                const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+            }
+            if (!bad) widen_keys<D, false>(vring, wideV, kw0, k_hi - tile_k0, lane);
+            named_bar_sync(1, kMmaConsumerWarps * 32);  // the stage's V rows are complete
         }
-        if (!bad && widen) widen_keys<D, true>(vring, wideV, kw0, k_hi - tile_k0, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_em + 8 * st);  // the ring stage is widened: free it
-        if (MODE == MODE_PREFILL)
-            named_bar_sync(1, kMmaConsumerWarps * 32);
-        else
-            __syncwarp();
 
 #pragma unroll
         for (int sb = 0; sb < SUBS; ++sb) {
             const int kb0 = ((MODE == MODE_DECODE) ? kw0 : 0) + sb * KB;  // first key (in the stage) of the block
             const bool active = tile_k0 + kb0 < min(k_hi, warp_lim);   // warp-uniform
-            if (bad || !active) continue;
-            float sc[NTB][4];
-#pragma unroll
-            for (int n = 0; n < NTB; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-            // ---- S = Q K^T over the block's KB keys
-            const int mi = lane >> 3, rr = lane & 7;
-#pragma unroll
-            for (int np = 0; np < NTB / 2; ++np) {
-                const int key = kb0 + np * 16 + rr + ((mi >> 1) << 3);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(wide_addr<D>(wideK, key, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-                    Op::run(sc[2 * np], qf[kk], b0, b1);
-                    Op::run(sc[2 * np + 1], qf[kk], b2, b3);
-                }
-            }
-            // ---- mask, scale x k_scale of the key's page (log2 domain)
-            float vsn[NTB];
-            float mx_a = kNegInf, mx_b = kNegInf;
-#pragma unroll
-            for (int n = 0; n < NTB; ++n) {
-                const int pis = (kb0 + n * 8) >> ps_shift;  // page within the stage (8 keys share one)
-                const float kq = p.scale_log2 * s_ks[slot][pis];
-                vsn[n] = s_vs[slot][pis];
-                const int j = tile_k0 + kb0 + n * 8 + 2 * tq;
-                sc[n][0] = (j < lim_a) ? sc[n][0] * kq : kNegInf;
-                sc[n][1] = (j + 1 < lim_a) ? sc[n][1] * kq : kNegInf;
-                sc[n][2] = (j < lim_b) ? sc[n][2] * kq : kNegInf;
-                sc[n][3] = (j + 1 < lim_b) ? sc[n][3] * kq : kNegInf;
-                mx_a = fmaxf(mx_a, fmaxf(sc[n][0], sc[n][1]));
-                mx_b = fmaxf(mx_b, fmaxf(sc[n][2], sc[n][3]));
-            }
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-            const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-            // -inf - (-inf) guard: an all-masked row keeps max -inf and uses 0 as its offset
-            const float mu_a = (mn_a == kNegInf) ? 0.f : mn_a;
-            const float mu_b = (mn_b == kNegInf) ? 0.f : mn_b;
-            const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
-            m_a = mn_a;
-            m_b = mn_b;
-            // P x v_scale split into a bf16 high part and the rounding remainder (see attn_mma.cu)
             uint32_t ph[NTB][2], pl[NTB][2];
-            float rs_a = 0.f, rs_b = 0.f;
+            if (!bad && active) {
+                // ---- S = Q K^T over the block's KB keys, K converted from the ring
+                float sc[NTB][4];
 #pragma unroll
-            for (int n = 0; n < NTB; ++n) {
-                const float p0 = exp2f(sc[n][0] - mu_a), p1 = exp2f(sc[n][1] - mu_a);
-                const float p2 = exp2f(sc[n][2] - mu_b), p3 = exp2f(sc[n][3] - mu_b);
-                rs_a += p0 + p1;
-                rs_b += p2 + p3;
-                const float w0 = p0 * vsn[n], w1 = p1 * vsn[n], w2 = p2 * vsn[n], w3 = p3 * vsn[n];
-                ph[n][0] = OpV::pack(w0, w1);
-                ph[n][1] = OpV::pack(w2, w3);
-                const float2 ha = OpV::unpack(ph[n][0]), hb = OpV::unpack(ph[n][1]);
-                pl[n][0] = OpV::pack(w0 - ha.x, w1 - ha.y);
-                pl[n][1] = OpV::pack(w2 - hb.x, w3 - hb.y);
-            }
-            l_a = l_a * al_a + rs_a;
-            l_b = l_b * al_b + rs_b;
+                for (int n = 0; n < NTB; ++n) {
+                    sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+                    uint32_t bk[D / 16][2];
+                    load_k_frags<D>(kring, kb0 + n * 8 + g, tq, bk);
 #pragma unroll
-            for (int n = 0; n < D / 8; ++n) {
-                acc[n][0] *= al_a;
-                acc[n][1] *= al_a;
-                acc[n][2] *= al_b;
-                acc[n][3] *= al_b;
-            }
-            // ---- O += (Ph + Pl) V
+                    for (int kk = 0; kk < D / 16; ++kk) Op::run(sc[n], qf[kk], bk[kk][0], bk[kk][1]);
+                }
+                // ---- mask; scale x k_scale of the key's page (log2 domain)
+                float mx_a = kNegInf, mx_b = kNegInf;
 #pragma unroll
-            for (int ks = 0; ks < KB / 16; ++ks) {
-                const uint32_t ah[4] = {ph[2 * ks][0], ph[2 * ks][1], ph[2 * ks + 1][0], ph[2 * ks + 1][1]};
-                const uint32_t al[4] = {pl[2 * ks][0], pl[2 * ks][1], pl[2 * ks + 1][0], pl[2 * ks + 1][1]};
-                const int key = kb0 + ks * 16 + rr + ((mi & 1) << 3);
+                for (int n = 0; n < NTB; ++n) {
+                    const float ksc = s_ks[slot][(kb0 + n * 8) >> ps_shift];  // 8 keys share a page
+                    const float fa = srow_a * ksc, fb = srow_b * ksc;
+                    const int j = tile_k0 + kb0 + n * 8 + 2 * tq;
+                    sc[n][0] = (j < lim_a) ? sc[n][0] * fa : kNegInf;
+                    sc[n][1] = (j + 1 < lim_a) ? sc[n][1] * fa : kNegInf;
+                    sc[n][2] = (j < lim_b) ? sc[n][2] * fb : kNegInf;
+                    sc[n][3] = (j + 1 < lim_b) ? sc[n][3] * fb : kNegInf;
+                    mx_a = fmaxf(mx_a, fmaxf(sc[n][0], sc[n][1]));
+                    mx_b = fmaxf(mx_b, fmaxf(sc[n][2], sc[n][3]));
+                }
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+                const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+                // -inf - (-inf) guard: an all-masked row keeps max -inf and uses 0 as its offset
+                const float mu_a = (mn_a == kNegInf) ? 0.f : mn_a;
+                const float mu_b = (mn_b == kNegInf) ? 0.f : mn_b;
+                const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
+                m_a = mn_a;
+                m_b = mn_b;
+                // P split into an f16 high part and its rounding remainder: ~2^-22 relative
+                float rs_a = 0.f, rs_b = 0.f;
 #pragma unroll
-                for (int j = 0; j < D / 16; ++j) {
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4_trans(wide_addr<D>(wideV, key, 2 * j + (mi >> 1)), b0, b1, b2, b3);
-                    OpV::run(acc[2 * j], ah, b0, b1);
-                    OpV::run(acc[2 * j + 1], ah, b2, b3);
-                    OpV::run(acc[2 * j], al, b0, b1);
-                    OpV::run(acc[2 * j + 1], al, b2, b3);
+                for (int n = 0; n < NTB; ++n) {
+                    const float p0 = exp2f(sc[n][0] - mu_a), p1 = exp2f(sc[n][1] - mu_a);
+                    const float p2 = exp2f(sc[n][2] - mu_b), p3 = exp2f(sc[n][3] - mu_b);
+                    rs_a += p0 + p1;
+                    rs_b += p2 + p3;
+                    ph[n][0] = Op::pack(p0, p1);
+                    ph[n][1] = Op::pack(p2, p3);
+                    const float2 ha = Op::unpack(ph[n][0]), hb = Op::unpack(ph[n][1]);
+                    pl[n][0] = Op::pack(p0 - ha.x, p1 - ha.y);
+                    pl[n][1] = Op::pack(p2 - hb.x, p3 - hb.y);
+                }
+                l_a = l_a * al_a + rs_a;
+                l_b = l_b * al_b + rs_b;
+                if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {  // the running max moved
+#pragma unroll
+                    for (int n = 0; n < D / 8; ++n) {
+                        acc[n][0] *= al_a;
+                        acc[n][1] *= al_a;
+                        acc[n][2] *= al_b;
+                        acc[n][3] *= al_b;
+                    }
                 }
             }
+
+            if (MODE == MODE_DECODE) {
+                if (!bad) {
+                    const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
+                    bad = __any_sync(0xffffffffu, !ok);
+                }
+                if (!bad && active) widen_keys<D, false>(vring, wideV, kw0, k_hi - tile_k0, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_em + 8 * st);  // K read above, V widened: free the stage
+            }
+
+            if (!bad && active) {
+                // ---- O += v_scale x (Ph + Pl) V, one 16-key step (one page) at a time
+#pragma unroll
+                for (int kst = 0; kst < KB / 16; ++kst) {
+                    const float vsc = s_vs[slot][(kb0 + kst * 16) >> ps_shift];
+                    const uint32_t ah[4] = {ph[2 * kst][0], ph[2 * kst][1], ph[2 * kst + 1][0], ph[2 * kst + 1][1]};
+                    const uint32_t al[4] = {pl[2 * kst][0], pl[2 * kst][1], pl[2 * kst + 1][0], pl[2 * kst + 1][1]};
+                    const int key = kb0 + kst * 16 + rr + ((mi & 1) << 3);
+#pragma unroll
+                    for (int j = 0; j < D / 16; ++j) {
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4_trans(wide_addr<D>(wideV, key, 2 * j + (mi >> 1)), b0, b1, b2, b3);
+                        float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+                        Op::run(t0, ah, b0, b1);
+                        Op::run(t1, ah, b2, b3);
+                        Op::run(t0, al, b0, b1);
+                        Op::run(t1, al, b2, b3);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            acc[2 * j][e] = fmaf(vsc, t0[e], acc[2 * j][e]);
+                            acc[2 * j + 1][e] = fmaf(vsc, t1[e], acc[2 * j + 1][e]);
+                        }
+                    }
+                }
+            }
+        }
+        if (MODE == MODE_PREFILL) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_em + 8 * st);  // K of the whole stage read, V widened
         }
     }
 
@@ -446,14 +541,14 @@ static constexpr int kvq_stages(int head_dim) { return head_dim == 128 ? 4 : 6; 
 
 static size_t kvq_smem_bytes(int head_dim) {
     const int n = kvq_stages(head_dim);
-    return (size_t)n * 2 * kMmaTileKeys * head_dim + 2 * (size_t)kMmaTileKeys * head_dim * 2 + 1024;
+    return (size_t)n * 2 * kMmaTileKeys * head_dim + (size_t)kMmaTileKeys * head_dim * 2 + 1024;
 }
 
 template <typename T, int D, int MODE>
 static cudaError_t launch_kvq_t(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 cudaStream_t stream) {
     constexpr int NSTAGE = kvq_stages(D);
-    static_assert(merge_scratch_bytes(D) <= (size_t)NSTAGE * 2 * Geo8<D>::kStage8 + 2 * Geo8<D>::kWide,
+    static_assert(merge_scratch_bytes(D) <= (size_t)NSTAGE * 2 * Geo8<D>::kStage8 + Geo8<D>::kWide,
                   "decode merge scratch must fit in the ring and the widened rows");
     auto kern = paged_attn_mma_kvq_kernel<T, D, MODE, NSTAGE>;
     const size_t smem = kvq_smem_bytes(D);
