@@ -184,7 +184,8 @@ def causal_flops(wl) -> float:
 
 KERNEL_SOURCES = {
     "paged_attn_mma_kernel": ("attn_mma.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
-    "paged_attn_mma_kvq_kernel": ("attn_mma_kvq.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
+    "paged_attn_kvq_decode_kernel": ("attn_mma_kvq.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
+    "paged_attn_kvq_prefill_kernel": ("attn_mma_kvq.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
     "paged_attn_tc05_kernel": ("attn_tc05.cu", "tc05.cuh", "common.cuh", "kernels.h"),
     "paged_attn_simt_kernel": ("attn_simt.cu", "common.cuh", "kernels.h"),
 }
@@ -354,7 +355,7 @@ def run_ours(args, ws, rank, local):
         peak, peak_src = FALLBACK_HBM_GBS, "fallback"
     prefill = wl.Sq * wl.G > 16
     if kvq:
-        kname = "paged_attn_mma_kvq_kernel"
+        kname = "paged_attn_kvq_prefill_kernel" if wl.Sq * wl.G > 16 else "paged_attn_kvq_decode_kernel"
     elif args.variant:
         kname = {1: "paged_attn_simt_kernel", 4: "paged_attn_tc05_kernel"}.get(args.variant, "paged_attn_mma_kernel")
     else:  # what the planner picks for this shape

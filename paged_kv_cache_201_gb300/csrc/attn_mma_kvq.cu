@@ -5,26 +5,28 @@
 // reviewed files); a quantized pool here holds E4M3 elements whose value is element x scale of
 // the element's (page, kv head).
 //
-// Units, producer warp and online softmax follow the 16-bit kernel (attn_mma.cu).  What differs:
+// Units (one CTA per (sequence, kv head, split[, 64-row query tile])), the producer warp and the
+// online softmax with its guards follow the 16-bit kernel (attn_mma.cu).  What differs:
 //   * the producer copies each page's raw E4M3 rows (page_size tokens x head_dim bytes of one kv
 //     head: one 3-D TMA box, half the bytes of a 16-bit page) into a ring of 64-key stages, and
 //     with the page ids it loads the pages' K and V scales, which it leaves in shared memory
 //     beside the stage before arming the stage's barriers.
-//   * Q K^T runs in f16 straight from the ring: a lane converts the E4M3 bytes of its key into the
-//     MMA operand registers (one conversion per element pair, exact: every E4M3 value is an f16
-//     number).  The head dimension is visited in a permuted order, the same for Q and K, so that
-//     a lane's operand bytes are 16 contiguous bytes of one row (one conflict-free shared load);
-//     a dot product does not depend on the order of its terms.  bf16 queries enter as f16 after
-//     multiplying each query row by a power of two that puts its largest element in [2^14, 2^15);
-//     the score is scaled back by the inverse power exactly.
-//   * V rows are widened to f16 in shared memory (exact) for the transposing ldmatrix; warp w
-//     widens keys [16w, 16w + 16) of the stage.  Decode mode reads only its own 16 keys; prefill
-//     mode (each warp owning 16 query rows over all 64 keys) meets the other warps at a named
-//     barrier first.
-//   * the scale of key j's page multiplies its score (scale x k_scale x q.k), and each 16-key step
-//     of P V is accumulated separately and added to O times that step's page v_scale (a 16-key
-//     step never crosses a page).  P itself is the unscaled softmax weight in [0, 1], split into
-//     an f16 high part and its rounding remainder.
+//   * K enters the tensor cores in f16 straight from the ring: a lane converts the E4M3 bytes of
+//     its key into MMA operand registers (one conversion per element pair, exact: every E4M3 value
+//     is an f16 number).  The head dimension is visited in a permuted order, the same for Q and K,
+//     so that a lane's operand bytes are 16 contiguous bytes of one row (one conflict-free shared
+//     load); a dot product does not depend on the order of its terms.  bf16 queries enter as f16
+//     after multiplying each query row by a power of two that puts its largest element in
+//     [2^14, 2^15); the score is scaled back by the inverse power exactly.
+//   * V rows are widened to f16 in shared memory (exact) for the transposing ldmatrix.
+//   * the scale of key j's page multiplies its score (scale x k_scale x q.k); each 16-key step of
+//     P V (one page: page_size >= 16) is accumulated on its own and added to O times the page's
+//     v_scale.  P is the unscaled softmax weight in [0, 1], split into an f16 high part and its
+//     rounding remainder.
+//   * decode (at most 16 query rows per unit) computes the transposed products S^T = K Q^T and
+//     O^T = V^T P^T: keys and head dimension fill the MMA's 16-row side, the GQA group its 8-wide
+//     side, so a group of 4 or 8 heads does not pay for 16 rows; P^T is turned into the second
+//     operand's layout with movmatrix.  Prefill keeps S = Q K^T over 64-row query tiles.
 #include <type_traits>
 
 #include "mma_common.cuh"
@@ -40,7 +42,6 @@ constexpr int kMaxPagesPerStage = kMmaTileKeys / 16;  // page_size >= 16
 template <int D>
 struct Geo8 {
     static constexpr int kStage8 = kMmaTileKeys * D;     // bytes of one K (or V) stage, E4M3
-    static constexpr int kWide = kMmaTileKeys * D * 2;   // the same 64 keys widened to 16 bits
 };
 
 // Widened rows: [4 warps][D/64 halves][16 keys][64 elements].  A row is 128 bytes; its 16-byte
@@ -157,20 +158,186 @@ __device__ __forceinline__ void load_k_frags(uint32_t stage, int k, int tq, uint
     }
 }
 
+
+// One query row as f16 operand pairs in the permuted head-dim order: this lane's elements
+// [tq D/4, (tq + 1) D/4), pair i = elements tq D/4 + 2 i and + 1.  bf16 rows are multiplied by the
+// f16_row_scale power of two of the whole row (the 4 lanes of a quad hold one row) and inv gets
+// its inverse; f16 rows are taken as they are (inv = 1).  A row that is not valid reads as zeros.
+template <typename T, int D>
+__device__ __forceinline__ void load_q_row(const T *row, bool valid, int tq, uint32_t (&w)[D / 8], float &inv) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(row + tq * (D / 4));
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+        const uint4 x = valid ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * i] = x.x;
+        w[4 * i + 1] = x.y;
+        w[4 * i + 2] = x.z;
+        w[4 * i + 3] = x.w;
+    }
+    inv = 1.f;
+    if (std::is_same<T, __nv_bfloat16>::value) {
+        float am = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i)
+            am = fmaxf(am, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xffff0000u))));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+        const float sc = f16_row_scale(am, inv);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) w[i] = bf16x2_to_f16x2_scaled(w[i], sc);
+    }
+}
+
+// Transpose of an 8 x 8 matrix of 16-bit elements held one row pair per lane (lane 4 r + c holds
+// elements (r, 2c) and (r, 2c + 1)); returns the same lane's pair of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// The producer warp of one unit.  Page ids come 32 at a time, one per lane, never past the unit's
+// pages; each lane also holds its page's K and V scales (an id outside [0, num_pages) gets scale 0
+// and its rows read as zeros).  Per 64-key stage t it writes the stage's page scales into slot
+// t % (2 NSTAGE), arms the stage's barriers and issues one 3-D TMA box per page and pool into
+// ring stage t % NSTAGE.
+template <int D, int NSTAGE>
+__device__ __forceinline__ void kvq_produce(const CUtensorMap *tmK, const CUtensorMap *tmV, const FwdParams &p,
+                                            int b, int kvh, int pg0, int k_hi, int n_tiles, int ps_shift,
+                                            uint32_t sbase, uint32_t bar_fk, uint32_t bar_fv, uint32_t bar_em,
+                                            float (*s_ks)[kMaxPagesPerStage], float (*s_vs)[kMaxPagesPerStage],
+                                            int lane) {
+    constexpr int kStage8 = Geo8<D>::kStage8;
+    constexpr int kSlots = 2 * NSTAGE;
+    if (lane == 0) {
+        tma_prefetch_desc(tmK);
+        tma_prefetch_desc(tmV);
+    }
+    const int ps = 1 << ps_shift;
+    const int pps = kMmaTileKeys >> ps_shift;       // pages per stage (1, 2 or 4)
+    const uint32_t box_bytes = (uint32_t)(ps * D);  // one page of one kv head, E4M3
+    const int pg_end = (k_hi + ps - 1) >> ps_shift;
+    const int32_t *bt_row = p.block_table + (long long)b * p.W;
+    auto scale_of = [&](const float *sc, int id) -> float {
+        return (id >= 0 && (long long)id < p.num_pages) ? __ldg(sc + (long long)id * p.Hkv + kvh) : 0.f;
+    };
+    int batch = pg0;
+    int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
+    int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
+    float ks_cur = 0.f, vs_cur = 0.f, ks_next = 0.f, vs_next = 0.f;
+    if (batch + lane < pg_end) {
+        ks_cur = scale_of(p.k_scale, id_cur);
+        vs_cur = scale_of(p.v_scale, id_cur);
+    }
+    bool pend = true;  // scales of id_next not loaded yet
+    bool bad = false;
+    int issued = 0;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % NSTAGE;
+        const int slot = t % kSlots;
+        if (t >= NSTAGE && !bad) {
+            const bool ok = mbar_wait(bar_em + 8 * st, ((t / NSTAGE) - 1) & 1, p.err);
+            bad = __any_sync(0xffffffffu, !ok);
+        }
+        const int pg_first = pg0 + t * pps;
+        if (pg_first >= batch + 32) {
+            if (pend && batch + 32 + lane < pg_end) {
+                ks_next = scale_of(p.k_scale, id_next);
+                vs_next = scale_of(p.v_scale, id_next);
+            }
+            batch += 32;
+            id_cur = id_next;
+            ks_cur = ks_next;
+            vs_cur = vs_next;
+            const int nx = batch + 32 + lane;
+            id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
+            ks_next = vs_next = 0.f;
+            pend = true;
+        }
+        const int src = (pg_first + lane - batch) & 31;
+        const int id = __shfl_sync(0xffffffffu, id_cur, src);
+        const float ks = __shfl_sync(0xffffffffu, ks_cur, src);
+        const float vs = __shfl_sync(0xffffffffu, vs_cur, src);
+        if (bad) break;
+        const int nvalid = min(pps, pg_end - pg_first);
+        // Slot t % (2 NSTAGE) was last read for stage t - 2 NSTAGE; every consumer warp has
+        // finished that stage once it released stage t - NSTAGE, which the wait above saw.
+        if (lane < pps) {
+            s_ks[slot][lane] = ks;
+            s_vs[slot][lane] = vs;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_fk + 8 * st, (uint32_t)nvalid * box_bytes);
+            mbar_arrive_expect_tx(bar_fv + 8 * st, (uint32_t)nvalid * box_bytes);
+        }
+        __syncwarp();
+        if (lane < nvalid) {
+            int tok;
+            if (id < 0 || (long long)id >= p.num_pages) {
+                atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
+                tok = -ps;  // wholly out of the tensor: the box reads as zeros
+            } else {
+                tok = id << ps_shift;
+            }
+            const uint32_t kdst = sbase + (uint32_t)(st * 2 * kStage8) + (uint32_t)lane * box_bytes;
+            tma_load_3d(kdst, tmK, bar_fk + 8 * st, 0, tok, kvh);
+            tma_load_3d(kdst + kStage8, tmV, bar_fv + 8 * st, 0, tok, kvh);
+        }
+        issued = t + 1;
+        if (pend) {  // after this stage's copies are on their way
+            if (batch + 32 + lane < pg_end) {
+                ks_next = scale_of(p.k_scale, id_next);
+                vs_next = scale_of(p.v_scale, id_next);
+            }
+            pend = false;
+        }
+    }
+    // every copy must have landed before the CTA may exit
+    for (int t = max(0, issued - NSTAGE); t < issued; ++t) {
+        const int st = t % NSTAGE;
+        const uint32_t par = (t / NSTAGE) & 1;
+        mbar_wait(bar_fk + 8 * st, par, p.err);
+        mbar_wait(bar_fv + 8 * st, par, p.err);
+    }
+}
+
+// Unit bounds shared by both kernels: sequence length clipped to the block-table row, the
+// split's key range [k_lo, k_hi_split) and its 64-key stage count up to key k_hi.
+struct KvqUnit {
+    int L, pg0, k_lo, k_hi_split;
+};
+
+__device__ __forceinline__ KvqUnit kvq_unit(const FwdParams &p, int b, int s, int ps_shift) {
+    KvqUnit u;
+    const int ps = 1 << ps_shift;
+    u.L = max(p.seq_lens[b], 0);
+    if (u.L > p.W * ps) {  // never read past the sequence's block-table row
+        if (threadIdx.x == 0) atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
+        u.L = p.W * ps;
+    }
+    int pg1;
+    split_pages(u.L, ps, p.split_kv, s, u.pg0, pg1);
+    u.k_lo = u.pg0 * ps;
+    u.k_hi_split = min(pg1 * ps, u.L);
+    return u;
+}
+
 }  // namespace
 
-template <typename T, int D, int MODE, int NSTAGE>
-__global__ void __launch_bounds__(kMmaThreads, 2)
-    paged_attn_mma_kvq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                              const FwdParams p, int ps_shift) {
-    using Op = MmaOp<__half>;  // Q K^T and P V both in f16
-    constexpr bool kQBf16 = std::is_same<T, __nv_bfloat16>::value;
+// ============================================================================ decode
+// At most 16 query rows per (sequence, kv head): the kernel computes S^T = K Q^T and O^T = V^T P^T,
+// so that keys and head dimension fill the MMA's 16-row side and the few query rows (GQA group x
+// query tokens, padded to NR x 8) its 8-column side.  Warp w reads keys [16 w, 16 w + 16) of every
+// stage (one page: page_size >= 16); the four warps' softmax states are merged at the end.
+template <typename T, int D, int NR, int NSTAGE>
+__global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
+    paged_attn_kvq_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                                 const FwdParams p, int ps_shift) {
+    using Op = MmaOp<__half>;
     constexpr int kStage8 = Geo8<D>::kStage8;
-    constexpr int KB = (MODE == MODE_DECODE) ? 16 : 32;   // keys per softmax block
-    constexpr int SUBS = (MODE == MODE_DECODE) ? 1 : 2;   // blocks a warp handles per stage
-    constexpr int NTB = KB / 8;                           // score n-tiles per block
-    constexpr int CTA_ROWS = (MODE == MODE_DECODE) ? kDecodeRows : kPrefillRows;
-    constexpr int kSlots = 2 * NSTAGE;                    // scale slots (see the producer)
+    constexpr int kSlots = 2 * NSTAGE;
+    constexpr int MT = D / 16;  // 16-wide head-dim tiles of O^T
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[3 * NSTAGE];
@@ -179,36 +346,17 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int ps = 1 << ps_shift;
-
-    // ---- unit coordinates
     int unit = blockIdx.x;
-    int rt = 0;
-    if (MODE == MODE_PREFILL) {
-        rt = unit % p.row_tiles;
-        unit /= p.row_tiles;
-    }
     const int kvh = unit % p.Hkv;
     unit /= p.Hkv;
     const int s = unit % p.split_kv;
     const int b = unit / p.split_kv;
-
-    int L = max(p.seq_lens[b], 0);
-    if (L > p.W * ps) {  // never read past the sequence's block-table row
-        if (threadIdx.x == 0) atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
-        L = p.W * ps;
-    }
-    int pg0, pg1;
-    split_pages(L, ps, p.split_kv, s, pg0, pg1);
-    const int k_lo = pg0 * ps;
-    const int k_hi_split = min(pg1 * ps, L);
-    const int row0 = rt * CTA_ROWS;
-    const int row_end = min(row0 + CTA_ROWS, p.rows);
-    const int k_hi = min(k_hi_split, row_key_limit(p, b, L, (row_end - 1) / p.G));
-    const int n_tiles = k_hi > k_lo ? (k_hi - k_lo + kMmaTileKeys - 1) / kMmaTileKeys : 0;
-
+    const KvqUnit u = kvq_unit(p, b, s, ps_shift);
+    const int rows = p.rows;  // <= 8 NR
+    const int k_hi = min(u.k_hi_split, row_key_limit(p, b, u.L, (rows - 1) / p.G));
+    const int n_tiles = k_hi > u.k_lo ? (k_hi - u.k_lo + kMmaTileKeys - 1) / kMmaTileKeys : 0;
     if (n_tiles == 0) {
-        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, b, kvh, s, row0, row_end);
+        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, b, kvh, s, 0, rows);
         return;
     }
 
@@ -218,7 +366,6 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     const uint32_t bar_fk = smem_u32(&bars[0]);
     const uint32_t bar_fv = smem_u32(&bars[NSTAGE]);
     const uint32_t bar_em = smem_u32(&bars[2 * NSTAGE]);
-
     if (threadIdx.x == 0) {
         for (int st = 0; st < NSTAGE; ++st) {
             mbar_init(bar_fk + 8 * st, 1);
@@ -230,145 +377,288 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     __syncthreads();
 
     if (warp == kMmaConsumerWarps) {
-        // ================================================================ producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-        }
-        const int pps = kMmaTileKeys >> ps_shift;       // pages per stage (1, 2 or 4)
-        const uint32_t box_bytes = (uint32_t)(ps * D);  // one page of one kv head, E4M3
-        const int pg_end = (k_hi + ps - 1) >> ps_shift;
-        const int32_t *bt_row = p.block_table + (long long)b * p.W;
-        // Page ids come 32 at a time, one per lane; each lane also holds its page's two scales.
-        // An id outside [0, num_pages) gets scale 0 (its rows read as zeros).
-        auto scale_of = [&](const float *sc, int id) -> float {
-            return (id >= 0 && (long long)id < p.num_pages) ? __ldg(sc + (long long)id * p.Hkv + kvh) : 0.f;
-        };
-        int batch = pg0;
-        int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
-        int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
-        float ks_cur = 0.f, vs_cur = 0.f, ks_next = 0.f, vs_next = 0.f;
-        if (batch + lane < pg_end) {
-            ks_cur = scale_of(p.k_scale, id_cur);
-            vs_cur = scale_of(p.v_scale, id_cur);
-        }
-        bool pend = true;  // scales of id_next not loaded yet
-        bool bad = false;
-        int issued = 0;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int st = t % NSTAGE;
-            const int slot = t % kSlots;
-            if (t >= NSTAGE && !bad) {
-                const bool ok = mbar_wait(bar_em + 8 * st, ((t / NSTAGE) - 1) & 1, p.err);
-                bad = __any_sync(0xffffffffu, !ok);
-            }
-            const int pg_first = pg0 + t * pps;
-            if (pg_first >= batch + 32) {
-                if (pend && batch + 32 + lane < pg_end) {
-                    ks_next = scale_of(p.k_scale, id_next);
-                    vs_next = scale_of(p.v_scale, id_next);
-                }
-                batch += 32;
-                id_cur = id_next;
-                ks_cur = ks_next;
-                vs_cur = vs_next;
-                const int nx = batch + 32 + lane;
-                id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
-                ks_next = vs_next = 0.f;
-                pend = true;
-            }
-            const int src = (pg_first + lane - batch) & 31;
-            const int id = __shfl_sync(0xffffffffu, id_cur, src);
-            const float ks = __shfl_sync(0xffffffffu, ks_cur, src);
-            const float vs = __shfl_sync(0xffffffffu, vs_cur, src);
-            if (bad) break;
-            const int nvalid = min(pps, pg_end - pg_first);
-            // Slot t % (2 NSTAGE) was last read for stage t - 2 NSTAGE; every consumer warp has
-            // finished that stage once it released stage t - NSTAGE, which the wait above saw.
-            if (lane < pps) {
-                s_ks[slot][lane] = ks;
-                s_vs[slot][lane] = vs;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar_fk + 8 * st, (uint32_t)nvalid * box_bytes);
-                mbar_arrive_expect_tx(bar_fv + 8 * st, (uint32_t)nvalid * box_bytes);
-            }
-            __syncwarp();
-            if (lane < nvalid) {
-                int tok;
-                if (id < 0 || (long long)id >= p.num_pages) {
-                    atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
-                    tok = -ps;  // wholly out of the tensor: the box reads as zeros
-                } else {
-                    tok = id << ps_shift;
-                }
-                const uint32_t kdst = sbase + (uint32_t)(st * 2 * kStage8) + (uint32_t)lane * box_bytes;
-                tma_load_3d(kdst, &tmK, bar_fk + 8 * st, 0, tok, kvh);
-                tma_load_3d(kdst + kStage8, &tmV, bar_fv + 8 * st, 0, tok, kvh);
-            }
-            issued = t + 1;
-            if (pend) {  // after this stage's copies are on their way
-                if (batch + 32 + lane < pg_end) {
-                    ks_next = scale_of(p.k_scale, id_next);
-                    vs_next = scale_of(p.v_scale, id_next);
-                }
-                pend = false;
-            }
-        }
-        for (int t = max(0, issued - NSTAGE); t < issued; ++t) {
-            const int st = t % NSTAGE;
-            const uint32_t par = (t / NSTAGE) & 1;
-            mbar_wait(bar_fk + 8 * st, par, p.err);
-            mbar_wait(bar_fv + 8 * st, par, p.err);
-        }
+        kvq_produce<D, NSTAGE>(&tmK, &tmV, p, b, kvh, u.pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk, bar_fv, bar_em,
+                               s_ks, s_vs, lane);
         return;
     }
 
     // ==================================================================== consumers
     const int g = lane >> 2;
     const int tq = lane & 3;
-    const int rbase = (MODE == MODE_DECODE) ? 0 : row0 + warp * 16;
-    const int ra = rbase + g, rb = rbase + g + 8;
-    const int kw0 = warp * 16;  // the stage keys whose V rows this warp widens (decode mode: its keys)
+    const int kw0 = warp * 16;  // this warp's keys in every stage
+    // Q^T operands: row-tile nr, this lane's row 8 nr + g.  The score and output fragments hold
+    // rows 8 nr + 2 tq + e (e = 0, 1): their inverse query scalings come from lanes 4 (2 tq + e).
+    uint32_t qb[NR][D / 16][2];
+    float srow[NR][2];
+    int lim[NR][2];
+    int lmax = u.k_lo;
+#pragma unroll
+    for (int nr = 0; nr < NR; ++nr) {
+        const int r = nr * 8 + g;
+        const bool valid = r < rows;
+        const T *qrow = reinterpret_cast<const T *>(p.q) + (valid ? out_row_index(p, b, kvh, r) * D : 0);
+        uint32_t w[D / 8];
+        float inv;
+        load_q_row<T, D>(qrow, valid, tq, w, inv);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qb[nr][kk][0] = w[2 * kk];
+            qb[nr][kk][1] = w[2 * kk + 1];
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int rc = nr * 8 + 2 * tq + e;
+            srow[nr][e] = p.scale_log2 * __shfl_sync(0xffffffffu, inv, 4 * (2 * tq + e));
+            lim[nr][e] = rc < rows ? min(u.k_hi_split, row_key_limit(p, b, u.L, rc / p.G)) : u.k_lo;
+            lmax = max(lmax, lim[nr][e]);
+        }
+    }
+    // keys at or past the furthest limit of the unit's rows are masked for all of them
+    const int key_lim = min(k_hi, (int)__reduce_max_sync(0xffffffffu, (unsigned)lmax));
 
-    // Q fragments in f16 over the permuted head-dim order: lane tq holds elements
-    // [tq D/4, (tq + 1) D/4) of rows ra and rb, and step kk takes elements tq D/4 + 4 kk + {0, 1}
-    // (a0 / a1) and + {2, 3} (a2 / a3).  q_inv_* undoes the power-of-two scaling of bf16 rows.
-    uint32_t qf[D / 16][4];
-    float q_inv_a = 1.f, q_inv_b = 1.f;
+    float m[NR][2], l[NR][2];
+    float acc[NR][MT][4];
+#pragma unroll
+    for (int nr = 0; nr < NR; ++nr) {
+        m[nr][0] = m[nr][1] = kNegInf;
+        l[nr][0] = l[nr][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) acc[nr][mt][0] = acc[nr][mt][1] = acc[nr][mt][2] = acc[nr][mt][3] = 0.f;
+    }
+    const int mi = lane >> 3, rr = lane & 7;
+
+    bool bad = false;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % NSTAGE;
+        const uint32_t par = (t / NSTAGE) & 1;
+        const int slot = t % kSlots;
+        const uint32_t kring = sbase + (uint32_t)(st * 2 * kStage8);
+        const uint32_t vring = kring + (uint32_t)kStage8;
+        const int tile_k0 = u.k_lo + t * kMmaTileKeys;
+        const bool active = tile_k0 + kw0 < key_lim;  // warp-uniform
+
+        if (!bad) {
+            const bool ok = mbar_wait(bar_fk + 8 * st, par, p.err);
+            bad = __any_sync(0xffffffffu, !ok);
+        }
+        uint32_t pb[NR][2][2];  // P^T operands: [row tile][high / low part][keys 0-7 / 8-15]
+        if (!bad && active) {
+            // ---- S^T = K Q^T: keys g and g + 8 of the warp's 16, two partial sums over the steps
+            float sc[NR][2][4];
+#pragma unroll
+            for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) sc[nr][c][0] = sc[nr][c][1] = sc[nr][c][2] = sc[nr][c][3] = 0.f;
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+                uint32_t wg[4], w8[4];
+                lds_v4(ring_chunk_addr<D>(kring, kw0 + g, (D / 64) * tq + h), wg);
+                lds_v4(ring_chunk_addr<D>(kring, kw0 + g + 8, (D / 64) * tq + h), w8);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int kk = 4 * h + i;
+                    uint32_t a[4];
+                    e4m3x4_to_f16x4(wg[i], a[0], a[2]);
+                    e4m3x4_to_f16x4(w8[i], a[1], a[3]);
+#pragma unroll
+                    for (int nr = 0; nr < NR; ++nr) Op::run(sc[nr][i & 1], a, qb[nr][kk][0], qb[nr][kk][1]);
+                }
+            }
+            // ---- mask; scale x k_scale of the warp's page (log2 domain); online softmax per row
+            const float ksc = s_ks[slot][kw0 >> ps_shift];
+            const int j0 = tile_k0 + kw0 + g;  // key of fragment elements 0-1; j0 + 8 for 2-3
+            float al[NR][2], pv[NR][2][2];
+            bool moved = false;
+#pragma unroll
+            for (int nr = 0; nr < NR; ++nr) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float f = srow[nr][e] * ksc;
+                    float x0 = sc[nr][0][e] + sc[nr][1][e];
+                    float x1 = sc[nr][0][2 + e] + sc[nr][1][2 + e];
+                    x0 = (j0 < lim[nr][e]) ? x0 * f : kNegInf;
+                    x1 = (j0 + 8 < lim[nr][e]) ? x1 * f : kNegInf;
+                    float mx = fmaxf(x0, x1);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float mn = fmaxf(m[nr][e], mx);
+                    // -inf - (-inf) guard: an all-masked row keeps max -inf and uses 0 as its offset
+                    const float mu = (mn == kNegInf) ? 0.f : mn;
+                    al[nr][e] = exp2f(m[nr][e] - mu);
+                    m[nr][e] = mn;
+                    pv[nr][e][0] = exp2f(x0 - mu);
+                    pv[nr][e][1] = exp2f(x1 - mu);
+                    l[nr][e] = l[nr][e] * al[nr][e] + (pv[nr][e][0] + pv[nr][e][1]);
+                    moved |= al[nr][e] != 1.f;
+                }
+                // P^T tiles (rows: keys g / g + 8; columns: rows 2 tq, 2 tq + 1), high f16 part and
+                // remainder, transposed into the B operand layout (keys along k)
+                const uint32_t h0 = Op::pack(pv[nr][0][0], pv[nr][1][0]);
+                const uint32_t h1 = Op::pack(pv[nr][0][1], pv[nr][1][1]);
+                const float2 u0 = Op::unpack(h0), u1 = Op::unpack(h1);
+                const uint32_t r0 = Op::pack(pv[nr][0][0] - u0.x, pv[nr][1][0] - u0.y);
+                const uint32_t r1 = Op::pack(pv[nr][0][1] - u1.x, pv[nr][1][1] - u1.y);
+                pb[nr][0][0] = movmatrix_trans(h0);
+                pb[nr][0][1] = movmatrix_trans(h1);
+                pb[nr][1][0] = movmatrix_trans(r0);
+                pb[nr][1][1] = movmatrix_trans(r1);
+            }
+            if (__any_sync(0xffffffffu, moved)) {  // a running max moved: rescale O
+#pragma unroll
+                for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        acc[nr][mt][0] *= al[nr][0];
+                        acc[nr][mt][1] *= al[nr][1];
+                        acc[nr][mt][2] *= al[nr][0];
+                        acc[nr][mt][3] *= al[nr][1];
+                    }
+            }
+        }
+        if (!bad) {
+            const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
+            bad = __any_sync(0xffffffffu, !ok);
+        }
+        if (!bad && active) widen_keys<D, false>(vring, wideV, kw0, k_hi - tile_k0, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_em + 8 * st);  // K read above, V widened: free the stage
+        if (!bad && active) {
+            // ---- O^T += v_scale x V^T (Ph + Pl)^T over the warp's 16 keys
+            const float vsc = s_vs[slot][kw0 >> ps_shift];
+            const int key = kw0 + rr + ((mi >> 1) << 3);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                uint32_t a[4];
+                ldmatrix_x4_trans(wide_addr<D>(wideV, key, 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                for (int nr = 0; nr < NR; ++nr) {
+                    float tt[4] = {0.f, 0.f, 0.f, 0.f};
+                    Op::run(tt, a, pb[nr][0][0], pb[nr][0][1]);
+                    Op::run(tt, a, pb[nr][1][0], pb[nr][1][1]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[nr][mt][e] = fmaf(vsc, tt[e], acc[nr][mt][e]);
+                }
+            }
+        }
+    }
+
+    // row sums over the 8 key lanes of each row
+#pragma unroll
+    for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            l[nr][e] += __shfl_xor_sync(0xffffffffu, l[nr][e], 4);
+            l[nr][e] += __shfl_xor_sync(0xffffffffu, l[nr][e], 8);
+            l[nr][e] += __shfl_xor_sync(0xffffffffu, l[nr][e], 16);
+        }
+    // ---- merge the four warps' states through shared memory (reuses the ring and the rows)
+    constexpr int ACC_STRIDE = D + 4;
+    float *sm = reinterpret_cast<float *>(smem_raw + (sbase - raw));
+    named_bar_sync(1, kMmaConsumerWarps * 32);  // every warp is done reading the ring and the rows
     {
-        constexpr int NW = D / 8;  // element pairs a lane holds per row
-        uint32_t wa[NW], wb[NW];
+        float *wa = sm + warp * 16 * ACC_STRIDE;
+        float *s_m = sm + kMmaConsumerWarps * 16 * ACC_STRIDE;
+        float *s_l = s_m + kMmaConsumerWarps * 16;
+#pragma unroll
+        for (int nr = 0; nr < NR; ++nr) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = nr * 8 + 2 * tq + e;
+                    wa[r * ACC_STRIDE + 16 * mt + g] = acc[nr][mt][e];
+                    wa[r * ACC_STRIDE + 16 * mt + g + 8] = acc[nr][mt][2 + e];
+                }
+            if (g == 0) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    s_m[warp * 16 + nr * 8 + 2 * tq + e] = m[nr][e];
+                    s_l[warp * 16 + nr * 8 + 2 * tq + e] = l[nr][e];
+                }
+            }
+        }
+    }
+    named_bar_sync(1, kMmaConsumerWarps * 32);
+    if (!bad) decode_merge_store<T, D>(p, sm, b, kvh, s, rows);
+}
+
+// ============================================================================ prefill
+// More than 16 query rows: 64-row tiles, each consumer warp owning 16 rows over all 64 keys of a
+// stage (S = Q K^T, O = P V); V rows are widened once per stage by the four warps together.
+template <typename T, int D, int NSTAGE>
+__global__ void __launch_bounds__(kMmaThreads, 2)
+    paged_attn_kvq_prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                                  const FwdParams p, int ps_shift) {
+    using Op = MmaOp<__half>;
+    constexpr int kStage8 = Geo8<D>::kStage8;
+    constexpr int KB = 32;      // keys per softmax block
+    constexpr int SUBS = 2;     // blocks per stage
+    constexpr int NTB = KB / 8; // score n-tiles per block
+    constexpr int kSlots = 2 * NSTAGE;
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[3 * NSTAGE];
+    __shared__ float s_ks[kSlots][kMaxPagesPerStage];
+    __shared__ float s_vs[kSlots][kMaxPagesPerStage];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int unit = blockIdx.x;
+    const int rt = unit % p.row_tiles;
+    unit /= p.row_tiles;
+    const int kvh = unit % p.Hkv;
+    unit /= p.Hkv;
+    const int s = unit % p.split_kv;
+    const int b = unit / p.split_kv;
+    const KvqUnit u = kvq_unit(p, b, s, ps_shift);
+    const int row0 = rt * kPrefillRows;
+    const int row_end = min(row0 + kPrefillRows, p.rows);
+    // causal reach grows with the query index, so the tile's last row reaches furthest
+    const int k_hi = min(u.k_hi_split, row_key_limit(p, b, u.L, (row_end - 1) / p.G));
+    const int n_tiles = k_hi > u.k_lo ? (k_hi - u.k_lo + kMmaTileKeys - 1) / kMmaTileKeys : 0;
+    if (n_tiles == 0) {
+        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, b, kvh, s, row0, row_end);
+        return;
+    }
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    const uint32_t wideV = sbase + (uint32_t)(NSTAGE * 2 * kStage8);
+    const uint32_t bar_fk = smem_u32(&bars[0]);
+    const uint32_t bar_fv = smem_u32(&bars[NSTAGE]);
+    const uint32_t bar_em = smem_u32(&bars[2 * NSTAGE]);
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < NSTAGE; ++st) {
+            mbar_init(bar_fk + 8 * st, 1);
+            mbar_init(bar_fv + 8 * st, 1);
+            mbar_init(bar_em + 8 * st, kMmaConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kMmaConsumerWarps) {
+        kvq_produce<D, NSTAGE>(&tmK, &tmV, p, b, kvh, u.pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk, bar_fv, bar_em,
+                               s_ks, s_vs, lane);
+        return;
+    }
+
+    // ==================================================================== consumers
+    const int g = lane >> 2;
+    const int tq = lane & 3;
+    const int ra = row0 + warp * 16 + g, rb = ra + 8;
+    const int kw0 = warp * 16;  // the stage keys whose V rows this warp widens
+    // Q fragments (A operand) in f16 over the permuted head-dim order: step kk takes elements
+    // tq D/4 + 4 kk + {0, 1} (a0 / a1) and + {2, 3} (a2 / a3) of rows ra / rb.
+    uint32_t qf[D / 16][4];
+    float q_inv_a, q_inv_b;
+    {
+        uint32_t wa[D / 8], wb[D / 8];
         const T *q = reinterpret_cast<const T *>(p.q);
         const bool va = ra < p.rows, vb = rb < p.rows;
-        const uint4 *qa = reinterpret_cast<const uint4 *>(q + (va ? out_row_index(p, b, kvh, ra) * D : 0) + tq * (D / 4));
-        const uint4 *qb = reinterpret_cast<const uint4 *>(q + (vb ? out_row_index(p, b, kvh, rb) * D : 0) + tq * (D / 4));
-#pragma unroll
-        for (int i = 0; i < NW / 4; ++i) {
-            const uint4 xa = va ? __ldg(qa + i) : make_uint4(0u, 0u, 0u, 0u);
-            const uint4 xb = vb ? __ldg(qb + i) : make_uint4(0u, 0u, 0u, 0u);
-            wa[4 * i] = xa.x, wa[4 * i + 1] = xa.y, wa[4 * i + 2] = xa.z, wa[4 * i + 3] = xa.w;
-            wb[4 * i] = xb.x, wb[4 * i + 1] = xb.y, wb[4 * i + 2] = xb.z, wb[4 * i + 3] = xb.w;
-        }
-        if (kQBf16) {
-            float am_a = 0.f, am_b = 0.f;
-#pragma unroll
-            for (int i = 0; i < NW; ++i) {
-                am_a = fmaxf(am_a, fmaxf(fabsf(__uint_as_float(wa[i] << 16)), fabsf(__uint_as_float(wa[i] & 0xffff0000u))));
-                am_b = fmaxf(am_b, fmaxf(fabsf(__uint_as_float(wb[i] << 16)), fabsf(__uint_as_float(wb[i] & 0xffff0000u))));
-            }
-            am_a = fmaxf(am_a, __shfl_xor_sync(0xffffffffu, am_a, 1));
-            am_a = fmaxf(am_a, __shfl_xor_sync(0xffffffffu, am_a, 2));
-            am_b = fmaxf(am_b, __shfl_xor_sync(0xffffffffu, am_b, 1));
-            am_b = fmaxf(am_b, __shfl_xor_sync(0xffffffffu, am_b, 2));
-            const float sc_a = f16_row_scale(am_a, q_inv_a), sc_b = f16_row_scale(am_b, q_inv_b);
-#pragma unroll
-            for (int i = 0; i < NW; ++i) {
-                wa[i] = bf16x2_to_f16x2_scaled(wa[i], sc_a);
-                wb[i] = bf16x2_to_f16x2_scaled(wb[i], sc_b);
-            }
-        }
+        load_q_row<T, D>(q + (va ? out_row_index(p, b, kvh, ra) * D : 0), va, tq, wa, q_inv_a);
+        load_q_row<T, D>(q + (vb ? out_row_index(p, b, kvh, rb) * D : 0), vb, tq, wb, q_inv_b);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             qf[kk][0] = wa[2 * kk];
@@ -377,8 +667,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
             qf[kk][3] = wb[2 * kk + 1];
         }
     }
-    const int lim_a = ra < p.rows ? min(k_hi_split, row_key_limit(p, b, L, ra / p.G)) : k_lo;
-    const int lim_b = rb < p.rows ? min(k_hi_split, row_key_limit(p, b, L, rb / p.G)) : k_lo;
+    const int lim_a = ra < p.rows ? min(u.k_hi_split, row_key_limit(p, b, u.L, ra / p.G)) : u.k_lo;
+    const int lim_b = rb < p.rows ? min(u.k_hi_split, row_key_limit(p, b, u.L, rb / p.G)) : u.k_lo;
     // scale x log2(e) x the rows' inverse query scaling; times k_scale of the key's page below
     const float srow_a = p.scale_log2 * q_inv_a, srow_b = p.scale_log2 * q_inv_b;
 
@@ -396,188 +686,183 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
         const int slot = t % kSlots;
         const uint32_t kring = sbase + (uint32_t)(st * 2 * kStage8);
         const uint32_t vring = kring + (uint32_t)kStage8;
-        const int tile_k0 = k_lo + t * kMmaTileKeys;
+        const int tile_k0 = u.k_lo + t * kMmaTileKeys;
 
         if (!bad) {
             const bool ok = mbar_wait(bar_fk + 8 * st, par, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
-        if (MODE == MODE_PREFILL) {
-            named_bar_sync(1, kMmaConsumerWarps * 32);  // every warp is done with the previous V rows
-            if (!bad) {
-                const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
-                bad = __any_sync(0xffffffffu, !ok);
-            }
-            if (!bad) widen_keys<D, false>(vring, wideV, kw0, k_hi - tile_k0, lane);
-            named_bar_sync(1, kMmaConsumerWarps * 32);  // the stage's V rows are complete
+        named_bar_sync(1, kMmaConsumerWarps * 32);  // every warp is done with the previous V rows
+        if (!bad) {
+            const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
+            bad = __any_sync(0xffffffffu, !ok);
         }
+        if (!bad) widen_keys<D, false>(vring, wideV, kw0, k_hi - tile_k0, lane);
+        named_bar_sync(1, kMmaConsumerWarps * 32);  // the stage's V rows are complete
 
 #pragma unroll
         for (int sb = 0; sb < SUBS; ++sb) {
-            const int kb0 = ((MODE == MODE_DECODE) ? kw0 : 0) + sb * KB;  // first key (in the stage) of the block
+            const int kb0 = sb * KB;                                   // first key (in the stage) of the block
             const bool active = tile_k0 + kb0 < min(k_hi, warp_lim);   // warp-uniform
+            if (bad || !active) continue;
+            // ---- S = Q K^T over the block's KB keys, K converted from the ring
+            float sc[NTB][4];
+#pragma unroll
+            for (int n = 0; n < NTB; ++n) {
+                sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+                uint32_t bk[D / 16][2];
+                load_k_frags<D>(kring, kb0 + n * 8 + g, tq, bk);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) Op::run(sc[n], qf[kk], bk[kk][0], bk[kk][1]);
+            }
+            // ---- mask; scale x k_scale of the key's page (log2 domain)
+            float mx_a = kNegInf, mx_b = kNegInf;
+#pragma unroll
+            for (int n = 0; n < NTB; ++n) {
+                const float ksc = s_ks[slot][(kb0 + n * 8) >> ps_shift];  // 8 keys share a page
+                const float fa = srow_a * ksc, fb = srow_b * ksc;
+                const int j = tile_k0 + kb0 + n * 8 + 2 * tq;
+                sc[n][0] = (j < lim_a) ? sc[n][0] * fa : kNegInf;
+                sc[n][1] = (j + 1 < lim_a) ? sc[n][1] * fa : kNegInf;
+                sc[n][2] = (j < lim_b) ? sc[n][2] * fb : kNegInf;
+                sc[n][3] = (j + 1 < lim_b) ? sc[n][3] * fb : kNegInf;
+                mx_a = fmaxf(mx_a, fmaxf(sc[n][0], sc[n][1]));
+                mx_b = fmaxf(mx_b, fmaxf(sc[n][2], sc[n][3]));
+            }
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+            const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+            // -inf - (-inf) guard: an all-masked row keeps max -inf and uses 0 as its offset
+            const float mu_a = (mn_a == kNegInf) ? 0.f : mn_a;
+            const float mu_b = (mn_b == kNegInf) ? 0.f : mn_b;
+            const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
+            m_a = mn_a;
+            m_b = mn_b;
+            // P split into an f16 high part and its rounding remainder
             uint32_t ph[NTB][2], pl[NTB][2];
-            if (!bad && active) {
-                // ---- S = Q K^T over the block's KB keys, K converted from the ring
-                float sc[NTB][4];
+            float rs_a = 0.f, rs_b = 0.f;
 #pragma unroll
-                for (int n = 0; n < NTB; ++n) {
-                    sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-                    uint32_t bk[D / 16][2];
-                    load_k_frags<D>(kring, kb0 + n * 8 + g, tq, bk);
+            for (int n = 0; n < NTB; ++n) {
+                const float p0 = exp2f(sc[n][0] - mu_a), p1 = exp2f(sc[n][1] - mu_a);
+                const float p2 = exp2f(sc[n][2] - mu_b), p3 = exp2f(sc[n][3] - mu_b);
+                rs_a += p0 + p1;
+                rs_b += p2 + p3;
+                ph[n][0] = Op::pack(p0, p1);
+                ph[n][1] = Op::pack(p2, p3);
+                const float2 ha = Op::unpack(ph[n][0]), hb = Op::unpack(ph[n][1]);
+                pl[n][0] = Op::pack(p0 - ha.x, p1 - ha.y);
+                pl[n][1] = Op::pack(p2 - hb.x, p3 - hb.y);
+            }
+            l_a = l_a * al_a + rs_a;
+            l_b = l_b * al_b + rs_b;
+            if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {  // a running max moved
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) Op::run(sc[n], qf[kk], bk[kk][0], bk[kk][1]);
-                }
-                // ---- mask; scale x k_scale of the key's page (log2 domain)
-                float mx_a = kNegInf, mx_b = kNegInf;
-#pragma unroll
-                for (int n = 0; n < NTB; ++n) {
-                    const float ksc = s_ks[slot][(kb0 + n * 8) >> ps_shift];  // 8 keys share a page
-                    const float fa = srow_a * ksc, fb = srow_b * ksc;
-                    const int j = tile_k0 + kb0 + n * 8 + 2 * tq;
-                    sc[n][0] = (j < lim_a) ? sc[n][0] * fa : kNegInf;
-                    sc[n][1] = (j + 1 < lim_a) ? sc[n][1] * fa : kNegInf;
-                    sc[n][2] = (j < lim_b) ? sc[n][2] * fb : kNegInf;
-                    sc[n][3] = (j + 1 < lim_b) ? sc[n][3] * fb : kNegInf;
-                    mx_a = fmaxf(mx_a, fmaxf(sc[n][0], sc[n][1]));
-                    mx_b = fmaxf(mx_b, fmaxf(sc[n][2], sc[n][3]));
-                }
-                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-                const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-                // -inf - (-inf) guard: an all-masked row keeps max -inf and uses 0 as its offset
-                const float mu_a = (mn_a == kNegInf) ? 0.f : mn_a;
-                const float mu_b = (mn_b == kNegInf) ? 0.f : mn_b;
-                const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
-                m_a = mn_a;
-                m_b = mn_b;
-                // P split into an f16 high part and its rounding remainder: ~2^-22 relative
-                float rs_a = 0.f, rs_b = 0.f;
-#pragma unroll
-                for (int n = 0; n < NTB; ++n) {
-                    const float p0 = exp2f(sc[n][0] - mu_a), p1 = exp2f(sc[n][1] - mu_a);
-                    const float p2 = exp2f(sc[n][2] - mu_b), p3 = exp2f(sc[n][3] - mu_b);
-                    rs_a += p0 + p1;
-                    rs_b += p2 + p3;
-                    ph[n][0] = Op::pack(p0, p1);
-                    ph[n][1] = Op::pack(p2, p3);
-                    const float2 ha = Op::unpack(ph[n][0]), hb = Op::unpack(ph[n][1]);
-                    pl[n][0] = Op::pack(p0 - ha.x, p1 - ha.y);
-                    pl[n][1] = Op::pack(p2 - hb.x, p3 - hb.y);
-                }
-                l_a = l_a * al_a + rs_a;
-                l_b = l_b * al_b + rs_b;
-                if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {  // the running max moved
-#pragma unroll
-                    for (int n = 0; n < D / 8; ++n) {
-                        acc[n][0] *= al_a;
-                        acc[n][1] *= al_a;
-                        acc[n][2] *= al_b;
-                        acc[n][3] *= al_b;
-                    }
+                for (int n = 0; n < D / 8; ++n) {
+                    acc[n][0] *= al_a;
+                    acc[n][1] *= al_a;
+                    acc[n][2] *= al_b;
+                    acc[n][3] *= al_b;
                 }
             }
-
-            if (MODE == MODE_DECODE) {
-                if (!bad) {
-                    const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
-                    bad = __any_sync(0xffffffffu, !ok);
-                }
-                if (!bad && active) widen_keys<D, false>(vring, wideV, kw0, k_hi - tile_k0, lane);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_em + 8 * st);  // K read above, V widened: free the stage
-            }
-
-            if (!bad && active) {
-                // ---- O += v_scale x (Ph + Pl) V, one 16-key step (one page) at a time
+            // ---- O += v_scale x (Ph + Pl) V, one 16-key step (one page) at a time
 #pragma unroll
-                for (int kst = 0; kst < KB / 16; ++kst) {
-                    const float vsc = s_vs[slot][(kb0 + kst * 16) >> ps_shift];
-                    const uint32_t ah[4] = {ph[2 * kst][0], ph[2 * kst][1], ph[2 * kst + 1][0], ph[2 * kst + 1][1]};
-                    const uint32_t al[4] = {pl[2 * kst][0], pl[2 * kst][1], pl[2 * kst + 1][0], pl[2 * kst + 1][1]};
-                    const int key = kb0 + kst * 16 + rr + ((mi & 1) << 3);
+            for (int kst = 0; kst < KB / 16; ++kst) {
+                const float vsc = s_vs[slot][(kb0 + kst * 16) >> ps_shift];
+                const uint32_t ah[4] = {ph[2 * kst][0], ph[2 * kst][1], ph[2 * kst + 1][0], ph[2 * kst + 1][1]};
+                const uint32_t al[4] = {pl[2 * kst][0], pl[2 * kst][1], pl[2 * kst + 1][0], pl[2 * kst + 1][1]};
+                const int key = kb0 + kst * 16 + rr + ((mi & 1) << 3);
 #pragma unroll
-                    for (int j = 0; j < D / 16; ++j) {
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4_trans(wide_addr<D>(wideV, key, 2 * j + (mi >> 1)), b0, b1, b2, b3);
-                        float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-                        Op::run(t0, ah, b0, b1);
-                        Op::run(t1, ah, b2, b3);
-                        Op::run(t0, al, b0, b1);
-                        Op::run(t1, al, b2, b3);
+                for (int j = 0; j < D / 16; ++j) {
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(wide_addr<D>(wideV, key, 2 * j + (mi >> 1)), b0, b1, b2, b3);
+                    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+                    Op::run(t0, ah, b0, b1);
+                    Op::run(t1, ah, b2, b3);
+                    Op::run(t0, al, b0, b1);
+                    Op::run(t1, al, b2, b3);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            acc[2 * j][e] = fmaf(vsc, t0[e], acc[2 * j][e]);
-                            acc[2 * j + 1][e] = fmaf(vsc, t1[e], acc[2 * j + 1][e]);
-                        }
+                    for (int e = 0; e < 4; ++e) {
+                        acc[2 * j][e] = fmaf(vsc, t0[e], acc[2 * j][e]);
+                        acc[2 * j + 1][e] = fmaf(vsc, t1[e], acc[2 * j + 1][e]);
                     }
                 }
             }
         }
-        if (MODE == MODE_PREFILL) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_em + 8 * st);  // K of the whole stage read, V widened
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_em + 8 * st);  // K of the whole stage read, V widened
     }
 
+    // quad sums of the row sums (alpha is uniform across a quad)
     l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
     l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-
-    if (MODE == MODE_PREFILL) {
-        if (!bad) finish_prefill_rows<T, D>(p, b, kvh, s, ra, rb, row_end, tq, m_a, m_b, l_a, l_b, acc);
-        return;
-    }
-    // decode: merge the four warps' states through shared memory (reuses the ring and the rows)
-    decode_merge<T, D>(p, reinterpret_cast<float *>(smem_raw + (sbase - raw)), b, kvh, s, row_end, warp, lane, m_a,
-                       m_b, l_a, l_b, acc, bad);
+    if (!bad) finish_prefill_rows<T, D>(p, b, kvh, s, ra, rb, row_end, tq, m_a, m_b, l_a, l_b, acc);
 }
 
 // ------------------------------------------------------------------------ host side
-static constexpr int kvq_stages(int head_dim) { return head_dim == 128 ? 4 : 6; }
+static constexpr int kvq_decode_stages(int D, int NR) { return D == 128 ? (NR == 1 ? 3 : 4) : 6; }
+static constexpr int kvq_prefill_stages(int D) { return D == 128 ? 4 : 6; }
 
-static size_t kvq_smem_bytes(int head_dim) {
-    const int n = kvq_stages(head_dim);
-    return (size_t)n * 2 * kMmaTileKeys * head_dim + (size_t)kMmaTileKeys * head_dim * 2 + 1024;
+static constexpr size_t kvq_smem_bytes(int D, int nstage) {
+    return (size_t)nstage * 2 * kMmaTileKeys * D + (size_t)kMmaTileKeys * D * 2 + 1024;  // ring, V rows, alignment
 }
 
-template <typename T, int D, int MODE>
-static cudaError_t launch_kvq_t(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                cudaStream_t stream) {
-    constexpr int NSTAGE = kvq_stages(D);
-    static_assert(merge_scratch_bytes(D) <= (size_t)NSTAGE * 2 * Geo8<D>::kStage8 + Geo8<D>::kWide,
-                  "decode merge scratch must fit in the ring and the widened rows");
-    auto kern = paged_attn_mma_kvq_kernel<T, D, MODE, NSTAGE>;
-    const size_t smem = kvq_smem_bytes(D);
+static int ps_shift_of(int ps) {
+    int sh = 0;
+    while ((1 << sh) < ps) ++sh;
+    return sh;
+}
+
+template <typename T, int D, int NR>
+static cudaError_t launch_kvq_decode(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                     cudaStream_t stream) {
+    constexpr int NSTAGE = kvq_decode_stages(D, NR);
+    constexpr size_t smem = kvq_smem_bytes(D, NSTAGE);
+    static_assert(merge_scratch_bytes(D) + 1024 <= smem, "decode merge scratch must fit in the ring and the rows");
+    auto kern = paged_attn_kvq_decode_kernel<T, D, NR, NSTAGE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    int ps_shift = 0;
-    while ((1 << ps_shift) < p.ps) ++ps_shift;
-    const long long units = (long long)p.B * p.split_kv * p.Hkv * (MODE == MODE_PREFILL ? p.row_tiles : 1);
+    const long long units = (long long)p.B * p.split_kv * p.Hkv;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)units, kMmaThreads, smem, stream>>>(tmk, tmv, p, ps_shift);
+    kern<<<(unsigned)units, kMmaThreads, smem, stream>>>(tmk, tmv, p, ps_shift_of(p.ps));
     return cudaGetLastError();
 }
 
-template <typename T>
-static cudaError_t launch_kvq_dt(const FwdParams &p, int mode, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                 cudaStream_t stream) {
-    if (p.D == 128) {
-        return mode == MODE_DECODE ? launch_kvq_t<T, 128, MODE_DECODE>(p, tmk, tmv, stream)
-                                   : launch_kvq_t<T, 128, MODE_PREFILL>(p, tmk, tmv, stream);
-    }
-    return mode == MODE_DECODE ? launch_kvq_t<T, 64, MODE_DECODE>(p, tmk, tmv, stream)
-                               : launch_kvq_t<T, 64, MODE_PREFILL>(p, tmk, tmv, stream);
+template <typename T, int D>
+static cudaError_t launch_kvq_prefill(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                      cudaStream_t stream) {
+    constexpr int NSTAGE = kvq_prefill_stages(D);
+    constexpr size_t smem = kvq_smem_bytes(D, NSTAGE);
+    auto kern = paged_attn_kvq_prefill_kernel<T, D, NSTAGE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long units = (long long)p.B * p.split_kv * p.Hkv * p.row_tiles;
+    if (units <= 0) return cudaSuccess;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)units, kMmaThreads, smem, stream>>>(tmk, tmv, p, ps_shift_of(p.ps));
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t launch_kvq_d(const FwdParams &p, int mode, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                cudaStream_t stream) {
+    if (mode == MODE_PREFILL) return launch_kvq_prefill<T, D>(p, tmk, tmv, stream);
+    return p.rows <= 8 ? launch_kvq_decode<T, D, 1>(p, tmk, tmv, stream)
+                       : launch_kvq_decode<T, D, 2>(p, tmk, tmv, stream);
 }
 
 cudaError_t launch_mma_kvq(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            cudaStream_t stream) {
-    if (dtype == PA_BF16) return launch_kvq_dt<__nv_bfloat16>(p, mode, tmk, tmv, stream);
-    return launch_kvq_dt<__half>(p, mode, tmk, tmv, stream);
+    if (dtype == PA_BF16) {
+        return p.D == 128 ? launch_kvq_d<__nv_bfloat16, 128>(p, mode, tmk, tmv, stream)
+                          : launch_kvq_d<__nv_bfloat16, 64>(p, mode, tmk, tmv, stream);
+    }
+    return p.D == 128 ? launch_kvq_d<__half, 128>(p, mode, tmk, tmv, stream)
+                      : launch_kvq_d<__half, 64>(p, mode, tmk, tmv, stream);
 }
 
 }  // namespace pa

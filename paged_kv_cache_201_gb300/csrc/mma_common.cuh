@@ -98,34 +98,16 @@ __host__ __device__ constexpr size_t merge_scratch_bytes(int D) {
     return (size_t)kMmaConsumerWarps * 16 * (D + 4) * 4 + 2 * kMmaConsumerWarps * 16 * 4;
 }
 
+// Second half of the decode merge: shared memory `sm` holds, for each consumer warp w, rows
+// [w][16][D + 4] of unnormalised outputs, then maxima [w][16] and sums [w][16] (log2 domain).
+// Each row is combined over the warps (0/0 guard: l == 0 stores 0, lse -inf) and stored.
 template <typename T, int D>
-__device__ __forceinline__ void decode_merge(const FwdParams &p, float *sm, int b, int kvh, int s, int row_end,
-                                             int warp, int lane, float m_a, float m_b, float l_a, float l_b,
-                                             const float (&acc)[D / 8][4], bool bad) {
+__device__ __forceinline__ void decode_merge_store(const FwdParams &p, const float *sm, int b, int kvh, int s,
+                                                   int row_end) {
     constexpr int ACC_STRIDE = D + 4;
-    const int g = lane >> 2;
-    const int tq = lane & 3;
-    float *s_acc = sm;                                            // [4][16][ACC_STRIDE]
-    float *s_m = sm + kMmaConsumerWarps * 16 * ACC_STRIDE;        // [4][16]
-    float *s_l = s_m + kMmaConsumerWarps * 16;                    // [4][16]
-    named_bar_sync(1, kMmaConsumerWarps * 32);  // every warp is done reading the buffers below
-    {
-        float *wa = s_acc + (warp * 16) * ACC_STRIDE;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-            const int col = n * 8 + 2 * tq;
-            *reinterpret_cast<float2 *>(wa + g * ACC_STRIDE + col) = make_float2(acc[n][0], acc[n][1]);
-            *reinterpret_cast<float2 *>(wa + (g + 8) * ACC_STRIDE + col) = make_float2(acc[n][2], acc[n][3]);
-        }
-        if (tq == 0) {
-            s_m[warp * 16 + g] = m_a;
-            s_m[warp * 16 + g + 8] = m_b;
-            s_l[warp * 16 + g] = l_a;
-            s_l[warp * 16 + g + 8] = l_b;
-        }
-    }
-    named_bar_sync(1, kMmaConsumerWarps * 32);
-    if (bad) return;
+    const float *s_acc = sm;
+    const float *s_m = sm + kMmaConsumerWarps * 16 * ACC_STRIDE;
+    const float *s_l = s_m + kMmaConsumerWarps * 16;
     const int tid = threadIdx.x;  // 0..127
     const int r = tid >> 3;       // 16 rows x 8 column groups
     const int cg = tid & 7;
@@ -157,6 +139,36 @@ __device__ __forceinline__ void decode_merge(const FwdParams &p, float *sm, int 
         }
         if (cg == 0) store_lse(p, s, ridx, Lsum > 0.f ? M * kLn2 + logf(Lsum) : kNegInf);
     }
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void decode_merge(const FwdParams &p, float *sm, int b, int kvh, int s, int row_end,
+                                             int warp, int lane, float m_a, float m_b, float l_a, float l_b,
+                                             const float (&acc)[D / 8][4], bool bad) {
+    constexpr int ACC_STRIDE = D + 4;
+    const int g = lane >> 2;
+    const int tq = lane & 3;
+    float *s_acc = sm;                                            // [4][16][ACC_STRIDE]
+    float *s_m = sm + kMmaConsumerWarps * 16 * ACC_STRIDE;        // [4][16]
+    float *s_l = s_m + kMmaConsumerWarps * 16;                    // [4][16]
+    named_bar_sync(1, kMmaConsumerWarps * 32);  // every warp is done reading the buffers below
+    {
+        float *wa = s_acc + (warp * 16) * ACC_STRIDE;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+            const int col = n * 8 + 2 * tq;
+            *reinterpret_cast<float2 *>(wa + g * ACC_STRIDE + col) = make_float2(acc[n][0], acc[n][1]);
+            *reinterpret_cast<float2 *>(wa + (g + 8) * ACC_STRIDE + col) = make_float2(acc[n][2], acc[n][3]);
+        }
+        if (tq == 0) {
+            s_m[warp * 16 + g] = m_a;
+            s_m[warp * 16 + g + 8] = m_b;
+            s_l[warp * 16 + g] = l_a;
+            s_l[warp * 16 + g + 8] = l_b;
+        }
+    }
+    named_bar_sync(1, kMmaConsumerWarps * 32);
+    if (!bad) decode_merge_store<T, D>(p, sm, b, kvh, s, row_end);
 }
 
 }  // namespace mmac
