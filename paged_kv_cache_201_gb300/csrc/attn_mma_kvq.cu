@@ -18,7 +18,8 @@
 //     load); a dot product does not depend on the order of its terms.  bf16 queries enter as f16
 //     after multiplying each query row by a power of two that puts its largest element in
 //     [2^14, 2^15); the score is scaled back by the inverse power exactly.
-//   * V rows are widened to f16 in shared memory (exact) for the transposing ldmatrix.
+//   * decode converts V from the ring the same way and transposes it in registers (movmatrix);
+//     prefill widens V rows to f16 in shared memory (exact) for the transposing ldmatrix.
 //   * the scale of key j's page multiplies its score (scale x k_scale x q.k); each 16-key step of
 //     P V (one page: page_size >= 16) is accumulated on its own and added to O times the page's
 //     v_scale.  P is the unscaled softmax weight in [0, 1], split into an f16 high part and its
@@ -362,7 +363,6 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
-    const uint32_t wideV = sbase + (uint32_t)(NSTAGE * 2 * kStage8);
     const uint32_t bar_fk = smem_u32(&bars[0]);
     const uint32_t bar_fv = smem_u32(&bars[NSTAGE]);
     const uint32_t bar_em = smem_u32(&bars[2 * NSTAGE]);
@@ -425,7 +425,6 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) acc[nr][mt][0] = acc[nr][mt][1] = acc[nr][mt][2] = acc[nr][mt][3] = 0.f;
     }
-    const int mi = lane >> 3, rr = lane & 7;
 
     bool bad = false;
     for (int t = 0; t < n_tiles; ++t) {
@@ -485,10 +484,10 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
                     const float mn = fmaxf(m[nr][e], mx);
                     // -inf - (-inf) guard: an all-masked row keeps max -inf and uses 0 as its offset
                     const float mu = (mn == kNegInf) ? 0.f : mn;
-                    al[nr][e] = exp2f(m[nr][e] - mu);
+                    al[nr][e] = fast_exp2(m[nr][e] - mu);
                     m[nr][e] = mn;
-                    pv[nr][e][0] = exp2f(x0 - mu);
-                    pv[nr][e][1] = exp2f(x1 - mu);
+                    pv[nr][e][0] = fast_exp2(x0 - mu);
+                    pv[nr][e][1] = fast_exp2(x1 - mu);
                     l[nr][e] = l[nr][e] * al[nr][e] + (pv[nr][e][0] + pv[nr][e][1]);
                     moved |= al[nr][e] != 1.f;
                 }
@@ -520,17 +519,40 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
             const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
-        if (!bad && active) widen_keys<D, false>(vring, wideV, kw0, k_hi - tile_k0, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_em + 8 * st);  // K read above, V widened: free the stage
+        // V bytes of keys g and g + 8 (this lane's D/4 bytes of each, as for K) into registers
+        uint32_t vw[2][D / 16];
         if (!bad && active) {
-            // ---- O^T += v_scale x V^T (Ph + Pl)^T over the warp's 16 keys
+#pragma unroll
+            for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h) {
+                    uint32_t w[4];
+                    lds_v4(ring_chunk_addr<D>(vring, kw0 + g + 8 * kh, (D / 64) * tq + h), w);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) vw[kh][4 * h + i] = w[i];
+                }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_em + 8 * st);  // K and V of the stage are read: free it
+        if (!bad && active) {
+            // Keys at or past k_hi hold whatever the ring held before: zero V rows keep 0 x NaN out.
+#pragma unroll
+            for (int kh = 0; kh < 2; ++kh)
+                if (tile_k0 + kw0 + g + 8 * kh >= k_hi)
+#pragma unroll
+                    for (int i = 0; i < D / 16; ++i) vw[kh][i] = 0u;
+            // ---- O^T += v_scale x V^T (Ph + Pl)^T over the warp's 16 keys.  Head-dim tile mt takes
+            // this lane's bytes 4 mt + {0..3} of keys g and g + 8: four 8 x 8 blocks (keys x 2-byte
+            // d slots) which movmatrix turns into the A operand (d x keys), so output row m of the
+            // tile is head-dim index out_d(mt, m) (see the merge below).
             const float vsc = s_vs[slot][kw0 >> ps_shift];
-            const int key = kw0 + rr + ((mi >> 1) << 3);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                uint32_t a[4];
-                ldmatrix_x4_trans(wide_addr<D>(wideV, key, 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+                uint32_t x00, x01, x10, x11;  // [key half][d slot half]
+                e4m3x4_to_f16x4(vw[0][mt], x00, x01);
+                e4m3x4_to_f16x4(vw[1][mt], x10, x11);
+                const uint32_t a[4] = {movmatrix_trans(x00), movmatrix_trans(x01), movmatrix_trans(x10),
+                                       movmatrix_trans(x11)};
 #pragma unroll
                 for (int nr = 0; nr < NR; ++nr) {
                     float tt[4] = {0.f, 0.f, 0.f, 0.f};
@@ -566,9 +588,12 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
+                    // tile row g holds head-dim index out_d(mt, g) = (g / 2) D/4 + 4 mt + (g % 2),
+                    // tile row g + 8 the index two above it
                     const int r = nr * 8 + 2 * tq + e;
-                    wa[r * ACC_STRIDE + 16 * mt + g] = acc[nr][mt][e];
-                    wa[r * ACC_STRIDE + 16 * mt + g + 8] = acc[nr][mt][2 + e];
+                    const int d0 = (g >> 1) * (D / 4) + 4 * mt + (g & 1);
+                    wa[r * ACC_STRIDE + d0] = acc[nr][mt][e];
+                    wa[r * ACC_STRIDE + d0 + 2] = acc[nr][mt][2 + e];
                 }
             if (g == 0) {
 #pragma unroll
@@ -803,11 +828,12 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
 }
 
 // ------------------------------------------------------------------------ host side
-static constexpr int kvq_decode_stages(int D, int NR) { return D == 128 ? (NR == 1 ? 3 : 4) : 6; }
+static constexpr int kvq_decode_stages(int D, int NR) { return D == 128 ? 4 : 8; }
 static constexpr int kvq_prefill_stages(int D) { return D == 128 ? 4 : 6; }
 
-static constexpr size_t kvq_smem_bytes(int D, int nstage) {
-    return (size_t)nstage * 2 * kMmaTileKeys * D + (size_t)kMmaTileKeys * D * 2 + 1024;  // ring, V rows, alignment
+// ring (+ the widened V rows of the prefill kernel) + alignment slack
+static constexpr size_t kvq_smem_bytes(int D, int nstage, bool wide_v) {
+    return (size_t)nstage * 2 * kMmaTileKeys * D + (wide_v ? (size_t)kMmaTileKeys * D * 2 : 0) + 1024;
 }
 
 static int ps_shift_of(int ps) {
@@ -820,7 +846,7 @@ template <typename T, int D, int NR>
 static cudaError_t launch_kvq_decode(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                      cudaStream_t stream) {
     constexpr int NSTAGE = kvq_decode_stages(D, NR);
-    constexpr size_t smem = kvq_smem_bytes(D, NSTAGE);
+    constexpr size_t smem = kvq_smem_bytes(D, NSTAGE, false);
     static_assert(merge_scratch_bytes(D) + 1024 <= smem, "decode merge scratch must fit in the ring and the rows");
     auto kern = paged_attn_kvq_decode_kernel<T, D, NR, NSTAGE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -836,7 +862,7 @@ template <typename T, int D>
 static cudaError_t launch_kvq_prefill(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                       cudaStream_t stream) {
     constexpr int NSTAGE = kvq_prefill_stages(D);
-    constexpr size_t smem = kvq_smem_bytes(D, NSTAGE);
+    constexpr size_t smem = kvq_smem_bytes(D, NSTAGE, true);
     auto kern = paged_attn_kvq_prefill_kernel<T, D, NSTAGE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
