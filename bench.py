@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode",
                     choices=["llama8b_decode", "over2gib_decode", "ragged_decode", "causal_prefill",
-                             "llama8b_decode_fp8"])
+                             "llama8b_decode_fp8", "mixed_decode_prefill"])
     ap.add_argument("--split-kv", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences (llama8b/over2gib workloads only; smaller pools for profiling)")
@@ -186,6 +186,7 @@ KERNEL_SOURCES = {
     "paged_attn_mma_kernel": ("attn_mma.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
     "paged_attn_kvq_decode_kernel": ("attn_mma_kvq.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
     "paged_attn_kvq_prefill_kernel": ("attn_mma_kvq.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
+    "paged_attn_mma_varlen_kernel": ("attn_mma.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
     "paged_attn_tc05_kernel": ("attn_tc05.cu", "tc05.cuh", "common.cuh", "kernels.h"),
     "paged_attn_simt_kernel": ("attn_simt.cu", "common.cuh", "kernels.h"),
 }
@@ -477,6 +478,199 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- variable-length batch
+def varlen_bytes(wl) -> dict:
+    """Bytes a mixed step must move at least: every valid K and V token once per kv head, q, out,
+    page ids, q_start."""
+    L = wl.seq_lens.astype(np.int64)
+    kv = int(L.sum()) * wl.Hkv * wl.D * wl.esize * 2
+    q = wl.Sq * wl.Hq * wl.D * wl.esize
+    ids = int(wl.nblk().sum()) * 4 + (2 * wl.B + 1) * 4
+    return {"kv": kv, "q": q, "out": q, "ids": ids, "total": kv + 2 * q + ids}
+
+
+def varlen_flops(wl) -> float:
+    """Useful flops: 4 D per (query row, valid key) pair, causal reach with each sequence's offset."""
+    pairs = 0
+    for b in range(wl.B):
+        n = int(wl.q_start[b + 1] - wl.q_start[b])
+        L = int(wl.seq_lens[b])
+        qoff = (L - n) if wl.q_offset is None else int(wl.q_offset[b])
+        reach = np.clip(qoff + np.arange(n) + 1, 0, L) if wl.causal else np.full(n, L)
+        pairs += int(reach.sum())
+    return 4.0 * wl.D * pairs * wl.Hq
+
+
+def run_varlen(args, ws, rank, local):
+    """The mixed decode + prefill batch through paged_attn_fwd_varlen (one grid); for context the
+    same batch as two uniform launches (decode kernel + tcgen05 prefill) is timed too."""
+    import torch
+    import paged_kv_cache_201_gb300 as pa
+    from paged_kv_cache_201_gb300 import workloads as W
+    import oracle
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa.load_library()
+    wl = build_workload(args.workload)
+    S = args.split_kv or 1
+    q = W.host_to_torch(wl.q, wl.dtype).to(dev)
+    k, v = W.fill_device_cache(wl, dev)
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    sl = torch.from_numpy(wl.seq_lens).to(dev)
+    qs = torch.from_numpy(wl.q_start).to(dev)
+    qo = torch.from_numpy(wl.q_offset).to(dev)
+    T, Hq, D = wl.Sq, wl.Hq, wl.D
+    out = torch.empty_like(q)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    po = torch.empty((S, T, Hq, D), dtype=torch.float32, device=dev) if S > 1 else None
+    pl = torch.empty((S, T, Hq), dtype=torch.float32, device=dev) if S > 1 else None
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if S == 1:
+            pa.paged_attn_fwd_varlen(q, k, v, bt, sl, qs, wl.causal, qo, 1, wl.scale, out, lse, stream)
+        else:
+            pa.paged_attn_fwd_varlen(q, k, v, bt, sl, qs, wl.causal, qo, S, wl.scale, po, pl, stream)
+            pa.paged_attn_combine(po, pl, out, lse, stream)
+
+    def timed(fn, K):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b_) / K
+
+    K = args.steps
+    with ClockSampler(local, enabled=not args.no_clocks) as clk:
+        ms_local = timed(step, K)
+    ms_step = max_over_ranks(ms_local, ws, dev)
+    flags = pa.paged_attn_last_error_word()
+    if flags:
+        raise RuntimeError(f"device error word {flags:#x} during the bench")
+
+    # the same batch as two uniform launches: decode sequences (one token) and prefill chunks
+    pre = np.nonzero(np.diff(wl.q_start) > 1)[0]
+    dec = np.nonzero(np.diff(wl.q_start) == 1)[0]
+    assert len(pre) + len(dec) == wl.B and (len(pre) == 0 or pre.max() < dec.min())
+    n_pre = len(pre)
+    sq_pre = int(wl.q_start[1] - wl.q_start[0]) if n_pre else 0
+    assert all(int(wl.q_start[b + 1] - wl.q_start[b]) == sq_pre for b in pre)
+    t_pre = n_pre * sq_pre
+    q_pre = q[:t_pre].view(n_pre, sq_pre, Hq, D)
+    q_dec = q[t_pre:].view(len(dec), 1, Hq, D)
+    o_pre = out[:t_pre].view(n_pre, sq_pre, Hq, D)
+    o_dec = out[t_pre:].view(len(dec), 1, Hq, D)
+    l_pre = lse[:t_pre].view(n_pre, sq_pre, Hq)
+    l_dec = lse[t_pre:].view(len(dec), 1, Hq)
+
+    def two_launch():
+        pa.paged_attn_fwd(q_pre, k, v, bt[:n_pre], sl[:n_pre], wl.causal, qo[:n_pre], 1, wl.scale, o_pre, l_pre, stream)
+        pa.paged_attn_fwd(q_dec, k, v, bt[n_pre:], sl[n_pre:], wl.causal, qo[n_pre:], 1, wl.scale, o_dec, l_dec, stream)
+
+    ms_two = timed(two_launch, max(10, K // 4)) if S == 1 else None
+
+    ab = varlen_bytes(wl)
+    fl = varlen_flops(wl)
+    peaks = measured_peaks()
+    if peaks and peaks.get("hbm_gbs"):
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    else:
+        peak, peak_src = FALLBACK_HBM_GBS, "fallback"
+    achieved = ab["total"] / (ms_local * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "paged_attn_mma_varlen_kernel", "achieved": round(achieved, 1),
+                "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "kernel_ms": round(ms_local, 5), "traffic": recorded_traffic("paged_attn_mma_varlen_kernel",
+                                                                             args.workload),
+                "tensor_side": {"achieved_tflops": round(fl / (ms_local * 1e-3) / 1e12, 1)}}
+
+    e2e = None
+    if not args.no_e2e:
+        q_h = q.cpu().pin_memory()
+        small = [t.cpu().pin_memory() for t in (bt, sl, qs, qo)]
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+        def e2e_step():
+            q.copy_(q_h, non_blocking=True)
+            for dst, src in zip((bt, sl, qs, qo), small):
+                dst.copy_(src, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        e2e_ms = max_over_ranks(timed(e2e_step, max(10, K // 4)), ws, dev)
+        hb = q_h.numel() * q_h.element_size() + sum(t.numel() * 4 for t in small)
+        db = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+        e2e = {"value": round(job_throughput(ab["total"], ws, e2e_ms), 1), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(hb), "d2h_bytes_per_step": int(db),
+               "api": "paged_attn_fwd_varlen (host q / block table / seq_lens / q_start / q_offset in, "
+                      "host out / lse back)"}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        # the oracle on the decode sequences (each a batch of one), repeated to >= 10 s (cap 30 s)
+        k_h, v_h = host_pools(wl, k, v)
+        dims = oracle.make_dims(B=len(dec), Sq=1, Hq=Hq, Hkv=wl.Hkv, D=D, page_size=wl.page_size,
+                                bt_stride=wl.W, dtype=wl.dtype, num_pages=wl.num_pages)
+        qd = wl.q[t_pre:].reshape(len(dec), 1, Hq, D)
+
+        def one_pass():
+            t0 = time.perf_counter()
+            oracle.rows(q=qd, k_cache=k_h, v_cache=v_h, block_table=wl.block_table[n_pre:],
+                        seq_lens=wl.seq_lens[n_pre:], q_offset=wl.q_offset[n_pre:], causal=wl.causal, dims=dims,
+                        scale=wl.scale, split_kv=1, want_split=False)
+            return time.perf_counter() - t0
+
+        dt1 = one_pass()
+        reps = int(min(max(1, np.ceil(10.0 / max(dt1, 1e-3))), max(1, 30.0 // max(dt1, 1e-3))))
+        dt = sum(one_pass() for _ in range(reps))
+        kvb = reps * int(wl.seq_lens[n_pre:].astype(np.int64).sum()) * wl.Hkv * D * wl.esize * 2
+        cpu = {"value": round(kvb / dt / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{reps} pass(es) over the {len(dec)} decode sequences of the batch, every head; "
+                         f"{dt:.1f} s fp64", "seconds": round(dt, 3)}
+
+    line = {
+        "metric": METRIC,
+        "value": round(job_throughput(ab["total"], ws, ms_step), 1),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(ms_step * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": data_text(wl),
+        "config": {"workload": args.workload, "B": wl.B, "prefill_sequences": n_pre, "prefill_tokens": sq_pre,
+                   "decode_sequences": len(dec), "total_query_tokens": T, "Hq": Hq, "Hkv": wl.Hkv, "D": D,
+                   "page_size": wl.page_size, "num_pages": wl.num_pages, "split_kv": S, "l2": l2_text(wl),
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "bytes_per_step": ab,
+        "flops_per_step": fl,
+        "roofline": roofline,
+        "two_launch": None if ms_two is None else {
+            "ms_per_step": round(ms_two, 5),
+            "how": "the same batch as paged_attn_fwd on the prefill chunks (tcgen05 kernel) then on the "
+                   "decode sequences (decode kernel), same stream"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * (2 if S > 1 else 1),
+        "clocks": clk.summary() if not args.no_clocks else None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- reference arm (the oracle)
 def run_reference(args, ws, rank, local):
     if rank != 0:
@@ -503,6 +697,13 @@ def run_reference(args, ws, rank, local):
             k, v = W.fill_device_cache(wl, dev)
         k_h, v_h = host_pools(wl, k, v)
         del k, v
+    if wl.q_start is not None:
+        # a variable-length batch: sample its first 4 one-token (decode) sequences, each a batch of one
+        dec = np.nonzero(np.diff(wl.q_start) == 1)[0][:4]
+        t0s = wl.q_start[dec]
+        wl = W.Workload(**{**wl.__dict__, "B": len(dec), "Sq": 1, "q": wl.q[t0s].reshape(len(dec), 1, wl.Hq, wl.D),
+                           "seq_lens": wl.seq_lens[dec], "block_table": wl.block_table[dec],
+                           "q_offset": wl.q_offset[dec], "q_start": None})
     n_seq = min(wl.B, 4)
     time_oracle(wl, k_h, v_h, S, 1, sc_h)  # warm-up: page in the pools and the library
     times, kv = [], 0
@@ -539,6 +740,8 @@ def main():
     ws, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, ws, rank, local)
+    elif args.workload == "mixed_decode_prefill":
+        run_varlen(args, ws, rank, local)
     else:
         run_ours(args, ws, rank, local)
     if ws > 1:

@@ -59,7 +59,8 @@ enum {
 enum {
     PA_ERRBIT_PAGE_RANGE = 1u,   /* a block-table page id used by a sequence was outside [0, num_pages) */
     PA_ERRBIT_TIMEOUT = 2u,      /* a pipeline wait gave up after its time limit (results invalid) */
-    PA_ERRBIT_SEQ_CLIPPED = 4u   /* seq_lens[b] needed more pages than bt_stride holds; clipped to bt_stride pages */
+    PA_ERRBIT_SEQ_CLIPPED = 4u,  /* seq_lens[b] needed more pages than bt_stride holds; clipped to bt_stride pages */
+    PA_ERRBIT_QSTART = 8u        /* paged_attn_fwd_varlen: a q_start entry out of [0, total tokens] or decreasing */
 };
 
 /* kernel variants (paged_attn_fwd_variant) */
@@ -187,6 +188,30 @@ int paged_attn_fwd_splitkv_noalloc(const void *q, const void *k_cache, const voi
                                    const int32_t *block_table, const int32_t *seq_lens, int causal,
                                    const int32_t *q_offset, int split_kv, float scale, void *out, float *lse,
                                    const pa_dims *dims, int num_sms, int64_t device_bytes, void *stream);
+
+/*
+ * paged_attn_fwd_varlen — one launch over a batch whose sequences have different numbers of query
+ * tokens: decode sequences (one new token) next to prefill chunks.  The pages' rocKE entry point
+ * serves such batches ("run_unified_attention_torch", rocm-libraries PR #14349, Performance); the
+ * layout below is this library's.
+ *   q        [T, Hq, D] (dtype): every sequence's query tokens packed; sequence b's are rows
+ *            [q_start[b], q_start[b + 1]).  T = dims->q_len (the total, not a per-sequence count).
+ *   q_start  [B + 1] int32, device: q_start[0] = 0, nondecreasing, q_start[B] = T.  A sequence with
+ *            no query token (q_start[b] == q_start[b + 1]) is skipped.
+ *   seq_lens[b] counts sequence b's K/V tokens including its query tokens; q_offset[b] places its
+ *            first query token (NULL: seq_lens[b] - its query count).
+ *   out      S == 1: [T, Hq, D] (dtype); S > 1: float32 [S, T, Hq, D] partials, merged by
+ *            paged_attn_combine with rows = T * Hq.  lse [T, Hq] or [S, T, Hq] (as paged_attn_fwd).
+ * dims->dtype is PA_BF16 or PA_F16 (PA_F32: PA_EDTYPE); every other rule is paged_attn_fwd's.
+ * Sequences of at most 16 query rows (tokens x Hq/Hkv) run as decode units and longer ones as
+ * 64-row tiles of the same grid.  If q_start[b] or q_start[b + 1] lies outside [0, T], or
+ * q_start[b + 1] < q_start[b], sequence b is skipped (its rows are not written) and
+ * PA_ERRBIT_QSTART is set; other malformed arrays give unspecified values but no access outside
+ * the buffers.
+ */
+int paged_attn_fwd_varlen(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                          const int32_t *seq_lens, const int32_t *q_start, int causal, const int32_t *q_offset,
+                          int split_kv, float scale, void *out, float *lse, const pa_dims *dims, void *stream);
 
 /*
  * paged_attn_fwd_kvq — paged_attn_fwd over quantized K/V pools.  The pages' sweeps include i8

@@ -263,3 +263,42 @@ def workload_rows_kvq(wl, split_kv: int = 1, row_bih=None, n_threads: int = 0, w
                     v_scale=wl.v_scale if v_scale is None else v_scale, block_table=wl.block_table,
                     seq_lens=wl.seq_lens, q_offset=wl.q_offset, causal=wl.causal, dims=dims_of(wl), scale=wl.scale,
                     split_kv=split_kv, row_bih=row_bih, n_threads=n_threads, want_split=want_split, lib=lib)
+
+
+# ----------------------------------------------------------------------------- variable-length batches
+def rows_varlen(*, q, k_cache, v_cache, block_table, seq_lens, q_start, q_offset, causal: bool, dims: Dims,
+                scale: float, split_kv: int = 1, n_threads: int = 0, want_split: bool = True, lib=None) -> dict:
+    """A batch whose sequences have different query counts.  q holds every sequence's query tokens
+    packed, [T, Hq, D] (dims.Sq = T); sequence b's tokens are rows q_start[b] .. q_start[b+1] - 1.
+    Each sequence is the uniform case with a batch of one (its own query count, block-table row,
+    length and offset; without an offset its queries are its last tokens), evaluated by ``rows``.
+
+    Returns float64 arrays over the packed rows: ``out`` [T, Hq, D], ``lse`` [T, Hq] and, with
+    ``want_split``, ``part_out`` [S, T, Hq, D], ``part_lse`` [S, T, Hq], ``comb_out`` / ``comb_lse``.
+    """
+    qs = np.asarray(q_start, dtype=np.int64)
+    B = int(qs.shape[0]) - 1
+    T, Hq, D, S = int(dims.Sq), int(dims.Hq), int(dims.D), split_kv
+    assert B == dims.B and qs[0] == 0 and qs[-1] == T and np.all(np.diff(qs) >= 0)
+    res = {"out": np.zeros((T, Hq, D)), "lse": np.full((T, Hq), -np.inf)}
+    if want_split:
+        res.update(part_out=np.zeros((S, T, Hq, D)), part_lse=np.full((S, T, Hq), -np.inf),
+                   comb_out=np.zeros((T, Hq, D)), comb_lse=np.full((T, Hq), -np.inf))
+    bt = np.ascontiguousarray(block_table)
+    for b in range(B):
+        a, e = int(qs[b]), int(qs[b + 1])
+        if e == a:
+            continue
+        sub = Dims(1, e - a, Hq, dims.Hkv, D, dims.page_size, dims.bt_stride, dims.dtype, dims.num_pages)
+        r = rows(q=np.ascontiguousarray(q[a:e])[None], k_cache=k_cache, v_cache=v_cache, block_table=bt[b:b + 1],
+                 seq_lens=np.asarray(seq_lens)[b:b + 1], q_offset=None if q_offset is None else np.asarray(q_offset)[b:b + 1],
+                 causal=causal, dims=sub, scale=scale, split_kv=split_kv, n_threads=n_threads, want_split=want_split,
+                 lib=lib)
+        res["out"][a:e] = r["out"].reshape(e - a, Hq, D)
+        res["lse"][a:e] = r["lse"].reshape(e - a, Hq)
+        if want_split:
+            res["part_out"][:, a:e] = np.moveaxis(r["part_out"].reshape(e - a, Hq, S, D), 2, 0)
+            res["part_lse"][:, a:e] = np.moveaxis(r["part_lse"].reshape(e - a, Hq, S), 2, 0)
+            res["comb_out"][a:e] = r["comb_out"].reshape(e - a, Hq, D)
+            res["comb_lse"][a:e] = r["comb_lse"].reshape(e - a, Hq)
+    return res

@@ -19,13 +19,13 @@ __all__ = [
     "paged_attn_combine", "paged_attn_plan", "paged_attn_debug_gather", "paged_attn_last_error_word",
     "paged_attn_strerror", "paged_attn_version", "attention", "paged_attn_auto_split",
     "paged_attn_workspace_bytes", "paged_attn_fwd_splitkv", "paged_attn_fwd_splitkv_noalloc", "paged_attn_fwd_kvq",
-    "paged_attn_fwd_kvq_splitkv", "attention_kvq", "PA_F32", "PA_F16", "PA_BF16", "PA_FP8_E4M3",
+    "paged_attn_fwd_kvq_splitkv", "attention_kvq", "paged_attn_fwd_varlen", "attention_varlen", "PA_F32", "PA_F16", "PA_BF16", "PA_FP8_E4M3",
     "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL", "VARIANT_TC05_PREFILL",
 ]
 
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA_DECODE, VARIANT_MMA_PREFILL, VARIANT_TC05_PREFILL = 0, 1, 2, 3, 4
-ERRBIT_PAGE_RANGE, ERRBIT_TIMEOUT, ERRBIT_SEQ_CLIPPED = 1, 2, 4
+ERRBIT_PAGE_RANGE, ERRBIT_TIMEOUT, ERRBIT_SEQ_CLIPPED, ERRBIT_QSTART = 1, 2, 4, 8
 
 
 class PaDims(ctypes.Structure):
@@ -80,6 +80,8 @@ def load_library(build_if_missing: bool = False):
     lib.paged_attn_fwd_kvq.restype = ctypes.c_int
     lib.paged_attn_fwd_kvq_splitkv.argtypes = [P, P, P, P, P, I32, P, P, I32, P, I32, F, P, P, D, P, I64, I32, I64, P]
     lib.paged_attn_fwd_kvq_splitkv.restype = ctypes.c_int
+    lib.paged_attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I32, P, I32, F, P, P, D, P]
+    lib.paged_attn_fwd_varlen.restype = ctypes.c_int
     lib.paged_attn_debug_gather.argtypes = [P, P, P, D, I32, P, P]
     lib.paged_attn_last_error_word.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.paged_attn_strerror.argtypes = [I32]
@@ -322,6 +324,35 @@ def paged_attn_fwd_kvq_splitkv(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     _raise(rc, "paged_attn_fwd_kvq_splitkv")
 
 
+def paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, split_kv, scale,
+                          out, lse, stream=None) -> None:
+    """Forward over a batch with a different query count per sequence; see ``paged_attn_fwd_varlen``
+    in include/paged_attn.h.  q [T, Hq, D] packed, q_start int32 [B + 1]; out [T, Hq, D] (S = 1) or
+    float32 [S, T, Hq, D]; lse [T, Hq] or [S, T, Hq]."""
+    torch = _torch()
+    _check(q, "q", ndim=3)
+    _check(k_cache, "k_cache", q.dtype, 4)
+    _check(v_cache, "v_cache", q.dtype, 4)
+    _check(block_table, "block_table", torch.int32, 2)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    _check(q_start, "q_start", torch.int32, 1)
+    _check(q_offset, "q_offset", torch.int32, 1)
+    _check(out, "out")
+    _check(lse, "lse", torch.float32)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    T, Hq, D = q.shape
+    P, ps, Hkv, D2 = k_cache.shape
+    B = block_table.shape[0]
+    if D2 != D or q_start.shape[0] != B + 1 or seq_lens.shape[0] != B:
+        raise ValueError("q / k_cache / block_table / q_start / seq_lens shapes disagree")
+    dims = PaDims(B, T, Hq, Hkv, D, ps, P, block_table.shape[1], _dtype_code(q))
+    rc = load_library().paged_attn_fwd_varlen(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(q_start), int(bool(causal)),
+        _ptr(q_offset), int(split_kv), float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _stream(stream))
+    _raise(rc, "paged_attn_fwd_varlen")
+
+
 def paged_attn_combine(part_out, part_lse, out, lse=None, stream=None) -> None:
     """Merge split partials: part_out [S, ..., D] f32, part_lse [S, ...] f32 -> out [..., D], lse [...]."""
     torch = _torch()
@@ -431,5 +462,26 @@ def attention_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, 
         pl = torch.empty((split_kv, B, Sq, Hq), dtype=torch.float32, device=q.device)
         paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, causal, q_offset, split_kv,
                            scale, po, pl, stream)
+        paged_attn_combine(po, pl, out, lse, stream)
+    return (out, lse) if want_lse else out
+
+
+def attention_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, *, causal: bool = False, q_offset=None,
+                     split_kv: int = 1, scale: Optional[float] = None, want_lse: bool = False, stream=None):
+    """``attention`` for a packed variable-length batch: q [T, Hq, D], q_start [B + 1]."""
+    torch = _torch()
+    T, Hq, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    out = torch.empty_like(q)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if (want_lse or split_kv > 1) else None
+    if split_kv == 1:
+        paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, 1, scale, out,
+                              lse, stream)
+    else:
+        po = torch.empty((split_kv, T, Hq, D), dtype=torch.float32, device=q.device)
+        pl = torch.empty((split_kv, T, Hq), dtype=torch.float32, device=q.device)
+        paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, split_kv,
+                              scale, po, pl, stream)
         paged_attn_combine(po, pl, out, lse, stream)
     return (out, lse) if want_lse else out

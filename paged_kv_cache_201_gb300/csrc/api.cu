@@ -191,6 +191,7 @@ pa::FwdParams fill_params(const void *q, const void *k_cache, const void *v_cach
     p.split_kv = split_kv;
     p.scale_log2 = scale * pa::kLog2e;
     p.row_tiles = 1;
+    p.rows_total = (long long)dims->batch * dims->q_len * dims->num_q_heads;
     return p;
 }
 
@@ -386,6 +387,35 @@ int paged_attn_fwd_kvq_splitkv(const void *q, const void *k_cache, const void *v
                             return paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, block_table,
                                                       seq_lens, causal, q_offset, S, scale, o, l, dims, stream);
                         });
+}
+
+int paged_attn_fwd_varlen(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                          const int32_t *seq_lens, const int32_t *q_start, int causal, const int32_t *q_offset,
+                          int split_kv, float scale, void *out, float *lse, const pa_dims *dims, void *stream) {
+    int rc = check_dims(dims);
+    if (rc != PA_OK) return rc;
+    if (dims->dtype == PA_F32) return PA_EDTYPE;
+    if (split_kv < 1 || split_kv > 65535) return PA_EINVAL;
+    if (!isfinite(scale)) return PA_EINVAL;
+    if (dims->batch == 0 || dims->q_len == 0) return PA_OK;  // no query token
+    rc = check_fwd_pointers(q, k_cache, v_cache, block_table, seq_lens, q_offset, split_kv, out, lse);
+    if (rc != PA_OK) return rc;
+    if (!q_start || (reinterpret_cast<uintptr_t>(q_start) & 3u)) return PA_EINVAL;
+    unsigned int *err = nullptr;
+    rc = error_word_ptr(&err);
+    if (rc != PA_OK) return rc;
+    pa::FwdParams p = fill_params(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, split_kv, scale,
+                                  out, lse, dims, err);
+    // q_len is the total packed token count T; per-sequence counts come from q_start
+    p.q_start = q_start;
+    p.Sq = 0;
+    p.rows = 0;
+    p.rows_total = (long long)dims->q_len * dims->num_q_heads;
+    CUtensorMap tmk, tmv;
+    if ((rc = make_pool_map(&tmk, k_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
+    if ((rc = make_pool_map(&tmv, v_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
+    return cuda_status(
+        pa::launch_mma_varlen(p, dims->q_len, dims->dtype, tmk, tmv, static_cast<cudaStream_t>(stream)));
 }
 
 int paged_attn_combine(const float *part_out, const float *part_lse, int split_kv, int64_t rows, int head_dim,

@@ -23,10 +23,12 @@ namespace pa {
 
 using namespace mmac;
 
+// One unit: sequence b, whose query tokens are `sq` (rows = sq.Sq x G query rows), kv head kvh,
+// split s and, in prefill mode, 64-row query tile rt.  Every thread of the CTA calls it.
 template <typename T, int D, int MODE, int NSTAGE>
-__global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
-    paged_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                          const FwdParams p, int ps_shift) {
+__device__ __forceinline__ void mma_unit(const CUtensorMap *tmK, const CUtensorMap *tmV, const FwdParams &p, int b,
+                                         const SeqRows &sq, int rows, int kvh, int s, int rt, int ps_shift,
+                                         uint8_t *smem_raw, uint64_t *bars) {
     using Op = MmaOp<T>;
     constexpr int kStage = Geo<D>::kStageBytes;
     constexpr int kChunks = Geo<D>::kChunks;
@@ -35,24 +37,9 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
     constexpr int NTB = KB / 8;                           // score n-tiles per block
     constexpr int CTA_ROWS = (MODE == MODE_DECODE) ? kDecodeRows : kPrefillRows;
 
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[3 * NSTAGE];
-
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int ps = 1 << ps_shift;
-
-    // ---- unit coordinates
-    int unit = blockIdx.x;
-    int rt = 0;
-    if (MODE == MODE_PREFILL) {
-        rt = unit % p.row_tiles;
-        unit /= p.row_tiles;
-    }
-    const int kvh = unit % p.Hkv;
-    unit /= p.Hkv;
-    const int s = unit % p.split_kv;
-    const int b = unit / p.split_kv;
 
     int L = max(p.seq_lens[b], 0);
     if (L > p.W * ps) {  // never read past the sequence's block-table row
@@ -64,14 +51,14 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
     const int k_lo = pg0 * ps;
     const int k_hi_split = min(pg1 * ps, L);
     const int row0 = rt * CTA_ROWS;
-    const int row_end = min(row0 + CTA_ROWS, p.rows);
+    const int row_end = min(row0 + CTA_ROWS, rows);
     // causal reach grows with the query index, so the CTA's last row reaches furthest
-    const int k_hi = min(k_hi_split, row_key_limit(p, b, L, (row_end - 1) / p.G));
+    const int k_hi = min(k_hi_split, row_key_limit(p, b, L, (row_end - 1) / p.G, sq.Sq));
     const int n_tiles = k_hi > k_lo ? (k_hi - k_lo + kMmaTileKeys - 1) / kMmaTileKeys : 0;
 
     if (n_tiles == 0) {
         // no valid key for any row of this unit: output 0, lse -inf
-        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, b, kvh, s, row0, row_end);
+        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, sq, kvh, s, row0, row_end);
         return;
     }
 
@@ -94,8 +81,8 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
     if (warp == kMmaConsumerWarps) {
         // ================================================================ producer
         if (lane == 0) {
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
+            tma_prefetch_desc(tmK);
+            tma_prefetch_desc(tmV);
         }
         const int pps = kMmaTileKeys >> ps_shift;                 // pages per stage (divides 32)
         const uint32_t box_bytes = (uint32_t)(Geo<D>::NH * ps * 128);
@@ -138,8 +125,8 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
                 }
                 const uint32_t off = (uint32_t)lane * box_bytes;
                 const uint32_t kdst = sbase + (uint32_t)(st * 2 * kStage) + off;
-                tma_load_4d(kdst, &tmK, bar_fk + 8 * st, 0, tok, 0, kvh);
-                tma_load_4d(kdst + kStage, &tmV, bar_fv + 8 * st, 0, tok, 0, kvh);
+                tma_load_4d(kdst, tmK, bar_fk + 8 * st, 0, tok, 0, kvh);
+                tma_load_4d(kdst + kStage, tmV, bar_fv + 8 * st, 0, tok, 0, kvh);
             }
             issued = t + 1;
         }
@@ -165,9 +152,9 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
     uint32_t qf[D / 16][4];
     {
         const T *q = reinterpret_cast<const T *>(p.q);
-        const bool va = ra < p.rows, vb = rb < p.rows;
-        const T *qa = q + (va ? out_row_index(p, b, kvh, ra) * D : 0);
-        const T *qb = q + (vb ? out_row_index(p, b, kvh, rb) * D : 0);
+        const bool va = ra < rows, vb = rb < rows;
+        const T *qa = q + (va ? out_row_index(p, sq, kvh, ra) * D : 0);
+        const T *qb = q + (vb ? out_row_index(p, sq, kvh, rb) * D : 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int c0 = kk * 16 + 2 * tq;
@@ -178,8 +165,8 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
         }
     }
     // exclusive key bounds of the two rows (pad rows see nothing)
-    const int lim_a = ra < p.rows ? min(k_hi_split, row_key_limit(p, b, L, ra / p.G)) : k_lo;
-    const int lim_b = rb < p.rows ? min(k_hi_split, row_key_limit(p, b, L, rb / p.G)) : k_lo;
+    const int lim_a = ra < rows ? min(k_hi_split, row_key_limit(p, b, L, ra / p.G, sq.Sq)) : k_lo;
+    const int lim_b = rb < rows ? min(k_hi_split, row_key_limit(p, b, L, rb / p.G, sq.Sq)) : k_lo;
 
     float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;
     float acc[D / 8][4];
@@ -328,12 +315,89 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
 
     if (MODE == MODE_PREFILL) {
         // each warp owns its rows: finalise and store
-        if (!bad) finish_prefill_rows<T, D>(p, b, kvh, s, ra, rb, row_end, tq, m_a, m_b, l_a, l_b, acc);
+        if (!bad) finish_prefill_rows<T, D>(p, sq, kvh, s, ra, rb, row_end, tq, m_a, m_b, l_a, l_b, acc);
         return;
     }
     // decode: merge the four warps' (m, l, acc) through shared memory (reuses the ring)
-    decode_merge<T, D>(p, reinterpret_cast<float *>(smem_raw + (sbase - raw)), b, kvh, s, row_end, warp, lane, m_a,
+    decode_merge<T, D>(p, reinterpret_cast<float *>(smem_raw + (sbase - raw)), sq, kvh, s, row_end, warp, lane, m_a,
                        m_b, l_a, l_b, acc, bad);
+}
+
+
+template <typename T, int D, int MODE, int NSTAGE>
+__global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
+    paged_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const FwdParams p, int ps_shift) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[3 * NSTAGE];
+    int unit = blockIdx.x;
+    int rt = 0;
+    if (MODE == MODE_PREFILL) {
+        rt = unit % p.row_tiles;
+        unit /= p.row_tiles;
+    }
+    const int kvh = unit % p.Hkv;
+    unit /= p.Hkv;
+    const int s = unit % p.split_kv;
+    const int b = unit / p.split_kv;
+    mma_unit<T, D, MODE, NSTAGE>(&tmK, &tmV, p, b, uniform_seq(p, b), p.rows, kvh, s, rt, ps_shift, smem_raw, bars);
+}
+
+// ---------------------------------------------------------------- variable-length batches
+// Sequence b's query tokens are packed rows [q_start[b], q_start[b + 1]) of q and out.  The grid
+// enumerates blocks of the packed rows: sequence b owns blocks [first_block(b), first_block(b + 1))
+// with first_block(b) = floor(q_start[b] G / 64) + b, at least as many as its 64-row tiles (and
+// one decode unit when it has at most 16 rows); blocks beyond what it needs exit at once.
+__device__ __forceinline__ long long varlen_first_block(const FwdParams &p, int b) {
+    return (long long)__ldg(p.q_start + b) * p.G / kPrefillRows + b;
+}
+
+// The sequence owning block t: the largest b in [0, B) with first_block(b) <= t, by a 32-way
+// search of one warp (first_block is strictly increasing for a valid q_start).
+__device__ __forceinline__ int varlen_sequence(const FwdParams &p, long long t, int lane) {
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+        const int stride = (hi - lo + 32) / 32;
+        const int idx = min(lo + lane * stride, hi);
+        const unsigned ok = __ballot_sync(0xffffffffu, varlen_first_block(p, idx) <= t);
+        const int last = ok ? 31 - __clz((int)ok) : 0;
+        lo = min(lo + last * stride, hi);
+        hi = stride == 1 ? lo : min(lo + stride - 1, hi);
+    }
+    return lo;
+}
+
+// Mixed decode and prefill sequences in one grid: each CTA finds its sequence, then runs a
+// 16-row decode unit (sequences with at most 16 query rows) or a 64-row prefill tile.  Units are
+// visited in the order u -> u * p.row_tiles mod gridDim.x (p.row_tiles coprime to the grid), which
+// spreads each sequence's units over the whole launch: the prefill tiles (tensor-bound) then run
+// beside the decode units (HBM-bound) instead of in a phase of their own.
+template <typename T, int D, int NSTAGE>
+__global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
+    paged_attn_mma_varlen_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                                 const FwdParams p, int ps_shift) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[3 * NSTAGE];
+    int unit = (int)(((unsigned long long)blockIdx.x * (unsigned)p.row_tiles) % gridDim.x);
+    const int kvh = unit % p.Hkv;
+    unit /= p.Hkv;
+    const int s = unit % p.split_kv;
+    const long long t = unit / p.split_kv;
+    const int b = varlen_sequence(p, t, threadIdx.x & 31);
+    const int q0 = __ldg(p.q_start + b), q1 = __ldg(p.q_start + b + 1);
+    if (q0 < 0 || q1 < q0 || (long long)q1 * p.Hq > p.rows_total) {
+        if (threadIdx.x == 0) atomicOr(p.err, (unsigned int)PA_ERRBIT_QSTART);
+        return;
+    }
+    const SeqRows sq{q0, q1 - q0};
+    const int rows = sq.Sq * p.G;
+    const long long j = t - varlen_first_block(p, b);  // block within the sequence
+    if (rows == 0 || j < 0) return;
+    if (rows <= kDecodeRows) {
+        if (j == 0) mma_unit<T, D, MODE_DECODE, NSTAGE>(&tmK, &tmV, p, b, sq, rows, kvh, s, 0, ps_shift, smem_raw, bars);
+    } else if (j < (rows + kPrefillRows - 1) / kPrefillRows) {
+        mma_unit<T, D, MODE_PREFILL, NSTAGE>(&tmK, &tmV, p, b, sq, rows, kvh, s, (int)j, ps_shift, smem_raw, bars);
+    }
 }
 
 // ------------------------------------------------------------------------ host side
@@ -370,6 +434,40 @@ static cudaError_t launch_mma_dt(const FwdParams &p, int mode, const CUtensorMap
     }
     return mode == MODE_DECODE ? launch_mma_t<T, 64, MODE_DECODE, 4>(p, tmk, tmv, stream)
                                : launch_mma_t<T, 64, MODE_PREFILL, 4>(p, tmk, tmv, stream);
+}
+
+template <typename T, int D, int NSTAGE>
+static cudaError_t launch_varlen_t(const FwdParams &p, long long blocks, const CUtensorMap &tmk,
+                                   const CUtensorMap &tmv, cudaStream_t stream) {
+    auto kern = paged_attn_mma_varlen_kernel<T, D, NSTAGE>;
+    const size_t smem = mma_smem_bytes(D, NSTAGE);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int ps_shift = 0;
+    while ((1 << ps_shift) < p.ps) ++ps_shift;
+    const long long units = blocks * p.split_kv * p.Hkv;
+    if (units <= 0) return cudaSuccess;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // visiting stride: the first value >= 0.618 units that is coprime to units (1 for tiny grids)
+    FwdParams q = p;
+    long long stride = units > 2 ? (units * 618) / 1000 : 1;
+    auto gcd = [](long long a, long long b) { while (b) { const long long r = a % b; a = b; b = r; } return a; };
+    while (stride > 1 && gcd(stride, units) != 1) ++stride;
+    q.row_tiles = (int)(stride < 1 ? 1 : stride);
+    kern<<<(unsigned)units, kMmaThreads, smem, stream>>>(tmk, tmv, q, ps_shift);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mma_varlen(const FwdParams &p, long long total_q, int dtype, const CUtensorMap &tmk,
+                              const CUtensorMap &tmv, cudaStream_t stream) {
+    // blocks of the packed rows: floor(T G / 64) + B (see varlen_first_block)
+    const long long blocks = total_q * p.G / kPrefillRows + p.B;
+    if (dtype == PA_BF16) {
+        return p.D == 128 ? launch_varlen_t<__nv_bfloat16, 128, 3>(p, blocks, tmk, tmv, stream)
+                          : launch_varlen_t<__nv_bfloat16, 64, 4>(p, blocks, tmk, tmv, stream);
+    }
+    return p.D == 128 ? launch_varlen_t<__half, 128, 3>(p, blocks, tmk, tmv, stream)
+                      : launch_varlen_t<__half, 64, 4>(p, blocks, tmk, tmv, stream);
 }
 
 cudaError_t launch_mma(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,

@@ -353,11 +353,12 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
     const int s = unit % p.split_kv;
     const int b = unit / p.split_kv;
     const KvqUnit u = kvq_unit(p, b, s, ps_shift);
+    const SeqRows sq = uniform_seq(p, b);
     const int rows = p.rows;  // <= 8 NR
     const int k_hi = min(u.k_hi_split, row_key_limit(p, b, u.L, (rows - 1) / p.G));
     const int n_tiles = k_hi > u.k_lo ? (k_hi - u.k_lo + kMmaTileKeys - 1) / kMmaTileKeys : 0;
     if (n_tiles == 0) {
-        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, b, kvh, s, 0, rows);
+        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, sq, kvh, s, 0, rows);
         return;
     }
 
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
     for (int nr = 0; nr < NR; ++nr) {
         const int r = nr * 8 + g;
         const bool valid = r < rows;
-        const T *qrow = reinterpret_cast<const T *>(p.q) + (valid ? out_row_index(p, b, kvh, r) * D : 0);
+        const T *qrow = reinterpret_cast<const T *>(p.q) + (valid ? out_row_index(p, sq, kvh, r) * D : 0);
         uint32_t w[D / 8];
         float inv;
         load_q_row<T, D>(qrow, valid, tq, w, inv);
@@ -605,7 +606,7 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
         }
     }
     named_bar_sync(1, kMmaConsumerWarps * 32);
-    if (!bad) decode_merge_store<T, D>(p, sm, b, kvh, s, rows);
+    if (!bad) decode_merge_store<T, D>(p, sm, sq, kvh, s, rows);
 }
 
 // ============================================================================ prefill
@@ -637,13 +638,14 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     const int s = unit % p.split_kv;
     const int b = unit / p.split_kv;
     const KvqUnit u = kvq_unit(p, b, s, ps_shift);
+    const SeqRows sq = uniform_seq(p, b);
     const int row0 = rt * kPrefillRows;
     const int row_end = min(row0 + kPrefillRows, p.rows);
     // causal reach grows with the query index, so the tile's last row reaches furthest
     const int k_hi = min(u.k_hi_split, row_key_limit(p, b, u.L, (row_end - 1) / p.G));
     const int n_tiles = k_hi > u.k_lo ? (k_hi - u.k_lo + kMmaTileKeys - 1) / kMmaTileKeys : 0;
     if (n_tiles == 0) {
-        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, b, kvh, s, row0, row_end);
+        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, sq, kvh, s, row0, row_end);
         return;
     }
 
@@ -682,8 +684,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
         uint32_t wa[D / 8], wb[D / 8];
         const T *q = reinterpret_cast<const T *>(p.q);
         const bool va = ra < p.rows, vb = rb < p.rows;
-        load_q_row<T, D>(q + (va ? out_row_index(p, b, kvh, ra) * D : 0), va, tq, wa, q_inv_a);
-        load_q_row<T, D>(q + (vb ? out_row_index(p, b, kvh, rb) * D : 0), vb, tq, wb, q_inv_b);
+        load_q_row<T, D>(q + (va ? out_row_index(p, sq, kvh, ra) * D : 0), va, tq, wa, q_inv_a);
+        load_q_row<T, D>(q + (vb ? out_row_index(p, sq, kvh, rb) * D : 0), vb, tq, wb, q_inv_b);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             qf[kk][0] = wa[2 * kk];
@@ -824,7 +826,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-    if (!bad) finish_prefill_rows<T, D>(p, b, kvh, s, ra, rb, row_end, tq, m_a, m_b, l_a, l_b, acc);
+    if (!bad) finish_prefill_rows<T, D>(p, sq, kvh, s, ra, rb, row_end, tq, m_a, m_b, l_a, l_b, acc);
 }
 
 // ------------------------------------------------------------------------ host side

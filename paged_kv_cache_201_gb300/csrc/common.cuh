@@ -30,6 +30,8 @@ struct FwdParams {
     const void *v_cache;
     const float *k_scale;      // FP8 pools: [num_pages, Hkv] per-(page, kv head) scales; else null
     const float *v_scale;
+    const int32_t *q_start;    // variable-length batches: [B + 1] first packed query token per sequence; else null
+    long long rows_total;      // query rows (tokens x heads) of the whole batch: the stride of one split's partials
     unsigned int *err;         // device error word
     long long num_pages;
     int B, Sq, Hq, Hkv, D, ps, W;
@@ -61,13 +63,18 @@ __device__ __forceinline__ void split_pages(int L, int ps, int S, int s, int &p0
     p1 = (int)(e < nblk ? e : nblk);
 }
 
-// Exclusive key bound for query row i of sequence b (causal reach incl. q_offset).
-__device__ __forceinline__ int row_key_limit(const FwdParams &p, int b, int L, int i) {
+// Exclusive key bound for query row i of sequence b, which has Sq query tokens (causal reach
+// incl. q_offset; without one the queries are the sequence's last Sq tokens).
+__device__ __forceinline__ int row_key_limit(const FwdParams &p, int b, int L, int i, int Sq) {
     if (!p.causal) return L;
-    const long long qoff = p.q_offset ? (long long)p.q_offset[b] : (long long)L - p.Sq;
+    const long long qoff = p.q_offset ? (long long)p.q_offset[b] : (long long)L - Sq;
     long long reach = qoff + i + 1;
     reach = reach < 0 ? 0 : reach;
     return (int)(reach < L ? reach : L);
+}
+
+__device__ __forceinline__ int row_key_limit(const FwdParams &p, int b, int L, int i) {
+    return row_key_limit(p, b, L, i, p.Sq);
 }
 
 // 2^x by the hardware approximation (ex2.approx, subnormal results flushed to 0; 2^-inf = 0).

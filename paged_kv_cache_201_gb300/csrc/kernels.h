@@ -23,6 +23,9 @@ size_t mma_smem_bytes(int head_dim, int stages);
 
 cudaError_t launch_mma(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
                        cudaStream_t stream);
+// Variable-length batch (p.q_start set, p.B sequences, total_q packed query tokens).
+cudaError_t launch_mma_varlen(const FwdParams &p, long long total_q, int dtype, const CUtensorMap &tmk,
+                              const CUtensorMap &tmv, cudaStream_t stream);
 // FP8 E4M3 pools with per-(page, kv head) scales in p.k_scale / p.v_scale; bf16/f16 queries.
 cudaError_t launch_mma_kvq(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
                            cudaStream_t stream);

@@ -25,10 +25,20 @@ __device__ __forceinline__ uint32_t kv_chunk_addr(uint32_t base, int k, int c, i
     return base + (uint32_t)(row << 7) + (uint32_t)((((c & 7) ^ (k & 7))) << 4);
 }
 
-__device__ __forceinline__ long long out_row_index(const FwdParams &p, int b, int kvh, int r) {
+// The query tokens of one sequence: its first token in the packed [tokens, Hq, D] layout
+// (b * Sq for a uniform batch) and its token count.
+struct SeqRows {
+    long long q0;
+    int Sq;
+};
+
+__device__ __forceinline__ SeqRows uniform_seq(const FwdParams &p, int b) { return {(long long)b * p.Sq, p.Sq}; }
+
+// Packed row (token x Hq + head) of unit row r (query token r / G, head kvh G + r % G).
+__device__ __forceinline__ long long out_row_index(const FwdParams &p, const SeqRows &sq, int kvh, int r) {
     const int i = r / p.G;
     const int h = kvh * p.G + (r - i * p.G);
-    return ((long long)b * p.Sq + i) * p.Hq + h;
+    return (sq.q0 + i) * p.Hq + h;
 }
 
 // Write two adjacent output columns of one row.
@@ -39,9 +49,8 @@ __device__ __forceinline__ void store_pair(const FwdParams &p, int s, long long 
         o[0] = from_float<T>(v0);
         o[1] = from_float<T>(v1);
     } else {
-        const long long rows_total = (long long)p.B * p.Sq * p.Hq;
         float2 *o = reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.out) +
-                                               ((long long)s * rows_total + ridx) * p.D + col);
+                                               ((long long)s * p.rows_total + ridx) * p.D + col);
         *o = make_float2(v0, v1);
     }
 }
@@ -50,19 +59,19 @@ __device__ __forceinline__ void store_lse(const FwdParams &p, int s, long long r
     if (p.split_kv == 1) {
         if (p.lse) p.lse[ridx] = v;
     } else {
-        const long long rows_total = (long long)p.B * p.Sq * p.Hq;
-        p.lse[(long long)s * rows_total + ridx] = v;
+        p.lse[(long long)s * p.rows_total + ridx] = v;
     }
 }
 
 // A unit with no valid key for any of its rows: output 0, lse -inf (consumer warps only).
 template <typename T, int D>
-__device__ __forceinline__ void store_empty_unit(const FwdParams &p, int b, int kvh, int s, int row0, int row_end) {
+__device__ __forceinline__ void store_empty_unit(const FwdParams &p, const SeqRows &sq, int kvh, int s, int row0,
+                                                 int row_end) {
     const int nrows = row_end - row0;
     for (int idx = threadIdx.x; idx < nrows * (D / 2); idx += kMmaConsumerWarps * 32) {
         const int r = row0 + idx / (D / 2);
         const int col = (idx % (D / 2)) * 2;
-        const long long ridx = out_row_index(p, b, kvh, r);
+        const long long ridx = out_row_index(p, sq, kvh, r);
         store_pair<T>(p, s, ridx, col, 0.f, 0.f);
         if (col == 0) store_lse(p, s, ridx, kNegInf);
     }
@@ -71,14 +80,14 @@ __device__ __forceinline__ void store_empty_unit(const FwdParams &p, int b, int 
 // Prefill epilogue: each warp owns rows ra / rb (fragment rows g, g + 8 of its m16 tile);
 // l_a / l_b are already summed over the quad.  0/0 guard: a row with l == 0 stores 0, lse -inf.
 template <typename T, int D>
-__device__ __forceinline__ void finish_prefill_rows(const FwdParams &p, int b, int kvh, int s, int ra, int rb,
+__device__ __forceinline__ void finish_prefill_rows(const FwdParams &p, const SeqRows &sq, int kvh, int s, int ra, int rb,
                                                     int row_end, int tq, float m_a, float m_b, float l_a,
                                                     float l_b, const float (&acc)[D / 8][4]) {
     const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f;
     const float inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
     const bool va = ra < row_end, vb = rb < row_end;
-    const long long ia = va ? out_row_index(p, b, kvh, ra) : 0;
-    const long long ib = vb ? out_row_index(p, b, kvh, rb) : 0;
+    const long long ia = va ? out_row_index(p, sq, kvh, ra) : 0;
+    const long long ib = vb ? out_row_index(p, sq, kvh, rb) : 0;
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) {
         const int col = n * 8 + 2 * tq;
@@ -102,8 +111,8 @@ __host__ __device__ constexpr size_t merge_scratch_bytes(int D) {
 // [w][16][D + 4] of unnormalised outputs, then maxima [w][16] and sums [w][16] (log2 domain).
 // Each row is combined over the warps (0/0 guard: l == 0 stores 0, lse -inf) and stored.
 template <typename T, int D>
-__device__ __forceinline__ void decode_merge_store(const FwdParams &p, const float *sm, int b, int kvh, int s,
-                                                   int row_end) {
+__device__ __forceinline__ void decode_merge_store(const FwdParams &p, const float *sm, const SeqRows &sq, int kvh,
+                                                   int s, int row_end) {
     constexpr int ACC_STRIDE = D + 4;
     const float *s_acc = sm;
     const float *s_m = sm + kMmaConsumerWarps * 16 * ACC_STRIDE;
@@ -124,7 +133,7 @@ __device__ __forceinline__ void decode_merge_store(const FwdParams &p, const flo
             Lsum += wsc[w] * s_l[w * 16 + r];
         }
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-        const long long ridx = out_row_index(p, b, kvh, r);
+        const long long ridx = out_row_index(p, sq, kvh, r);
 #pragma unroll
         for (int c = 0; c < COLS; c += 2) {
             const int col = cg * COLS + c;
@@ -142,7 +151,7 @@ __device__ __forceinline__ void decode_merge_store(const FwdParams &p, const flo
 }
 
 template <typename T, int D>
-__device__ __forceinline__ void decode_merge(const FwdParams &p, float *sm, int b, int kvh, int s, int row_end,
+__device__ __forceinline__ void decode_merge(const FwdParams &p, float *sm, const SeqRows &sq, int kvh, int s, int row_end,
                                              int warp, int lane, float m_a, float m_b, float l_a, float l_b,
                                              const float (&acc)[D / 8][4], bool bad) {
     constexpr int ACC_STRIDE = D + 4;
@@ -168,7 +177,7 @@ __device__ __forceinline__ void decode_merge(const FwdParams &p, float *sm, int 
         }
     }
     named_bar_sync(1, kMmaConsumerWarps * 32);
-    if (!bad) decode_merge_store<T, D>(p, sm, b, kvh, s, row_end);
+    if (!bad) decode_merge_store<T, D>(p, sm, sq, kvh, s, row_end);
 }
 
 }  // namespace mmac

@@ -85,6 +85,9 @@ class Workload:
     kv_dtype: Optional[str] = None           # "fp8e4m3": pools hold E4M3 bits (uint8) with per-page scales
     k_scale: Optional[np.ndarray] = None     # float32 [num_pages, Hkv] (quantized pools only)
     v_scale: Optional[np.ndarray] = None
+    # variable-length batches: q is [T, Hq, D] packed and Sq = T; sequence b's query tokens are
+    # rows q_start[b] .. q_start[b+1] - 1
+    q_start: Optional[np.ndarray] = None     # int32 [B + 1]
 
     @property
     def G(self) -> int:
@@ -374,3 +377,54 @@ def fill_device_cache_fp8(wl: Workload, device="cuda", pages_per_chunk: int = 40
             scales[p0:p1] = sc
         out += [bits, scales]
     return out[0], out[2], out[1], out[3]
+
+
+# ----------------------------------------------------------------------------- variable-length batches
+def make_varlen(*, name: str = "varlen", dtype: str = "bf16", q_lens: Sequence[int], seq_lens: Sequence[int],
+                Hq: int, Hkv: int, D: int, page_size: int, causal: bool = True,
+                q_offset: Optional[Sequence[int]] = None, num_pages: Optional[int] = None, W: Optional[int] = None,
+                split_kv: Sequence[int] = (1,), seed: int = 0, tail: int = SENTINEL_MAX) -> Workload:
+    """A host-resident batch whose sequences have their own query counts ``q_lens`` (0 allowed),
+    packed into q [T, Hq, D].  Values and pages are drawn as in ``make_custom``."""
+    q_lens = np.asarray(q_lens, dtype=np.int64)
+    B = int(q_lens.shape[0])
+    T = int(q_lens.sum())
+    wl = make_custom(name=name, dtype=dtype, B=B, Sq=1, Hq=Hq, Hkv=Hkv, D=D, page_size=page_size,
+                     seq_lens=seq_lens, num_pages=num_pages, W=W, causal=causal, q_offset=q_offset,
+                     split_kv=split_kv, seed=seed, tail=tail)
+    rng = np.random.default_rng(seed + 104729)
+    q = _normal_elems(rng, T * Hq * D, dtype).reshape(T, Hq, D)
+    q_start = np.zeros(B + 1, dtype=np.int32)
+    q_start[1:] = np.cumsum(q_lens)
+    return Workload(**{**wl.__dict__, "Sq": T, "q": q, "q_start": q_start})
+
+
+def mixed_decode_prefill(seed: int = 1007, n_decode: int = 256, n_prefill: int = 4) -> Workload:
+    """One batch mixing the Llama-3-8B decode (n_decode sequences, one query token, L=4096) and the
+    causal prefill (n_prefill sequences, 1024 query tokens, q_offset~U[0,3072], L = q_offset + 1024):
+    Hq=32, Hkv=8, D=128, bf16, page_size 16, prefill sequences first in the packed order.  Pools are
+    drawn on the device (``fill_device_cache``): 65536 pages for the decode sequences plus the
+    prefill sequences' pages, shuffled together."""
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D, ps, L = 32, 8, 128, 16, 4096
+    pre_off = rng.integers(0, 3072 + 1, size=n_prefill).astype(np.int64)
+    q_lens = np.array([1024] * n_prefill + [1] * n_decode, dtype=np.int64)
+    seq_lens = np.concatenate([pre_off + 1024, np.full(n_decode, L)]).astype(np.int32)
+    q_offset = (seq_lens.astype(np.int64) - q_lens).astype(np.int32)
+    q_offset[:n_prefill] = pre_off
+    B = n_prefill + n_decode
+    nblk = (seq_lens.astype(np.int64) + ps - 1) // ps
+    P = int(nblk.sum())
+    W = int(nblk.max())
+    T = int(q_lens.sum())
+    q = _normal_elems(rng, T * Hq * D, "bf16").reshape(T, Hq, D)
+    perm = rng.permutation(P)
+    bt = _pack_tables(B, W, nblk, perm, SENTINEL_MAX)
+    q_start = np.zeros(B + 1, dtype=np.int32)
+    q_start[1:] = np.cumsum(q_lens)
+    return Workload(name="mixed_decode_prefill", dtype="bf16", B=B, Sq=T, Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
+                    num_pages=P, causal=True, scale=1.0 / math.sqrt(D), split_kv=(1,), seq_lens=seq_lens,
+                    block_table=bt, q=q, q_offset=q_offset, device_cache_seed=seed, q_start=q_start)
+
+
+CONFIGS["mixed_decode_prefill"] = mixed_decode_prefill

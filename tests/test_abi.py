@@ -158,3 +158,20 @@ def test_fwd_kvq_validation(lib):
     # split 2 needs 2 * 16 rows * (128 + 1) * 4 bytes rounded up: a 16-byte workspace is too small
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, pa.PA_FP8_E4M3, FAKE, FAKE, 0, None, 2, 0.1, FAKE, FAKE, ctypes.byref(d),
              FAKE, 16, 152, 280 << 30, None) == EINVAL
+
+
+def test_fwd_varlen_validation(lib):
+    """Variable-length entry point: element type, q_start and the shared checks before any launch."""
+    f = lib.paged_attn_fwd_varlen
+
+    def call(dims, q_start=FAKE, split=1, lse=FAKE):
+        return f(FAKE, FAKE, FAKE, FAKE, FAKE, q_start, 1, None, split, 0.1, FAKE, lse,
+                 None if dims is None else ctypes.byref(dims), None)
+    assert call(None) == EINVAL
+    assert call(_dims(q_len=40, dtype=pa.PA_F32)) == EDTYPE
+    assert call(_dims(q_len=40), q_start=None) == EINVAL
+    assert call(_dims(q_len=40), q_start=FAKE + 2) == EINVAL
+    assert call(_dims(q_len=40), split=0) == EINVAL
+    assert call(_dims(q_len=40), split=2, lse=None) == EINVAL
+    assert call(_dims(q_len=40, head_dim=96)) == EUNSUP
+    assert call(_dims(q_len=0), q_start=None) == OK   # no query token: nothing to do

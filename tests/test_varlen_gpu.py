@@ -1,0 +1,189 @@
+"""GPU parity of the variable-length entry point (decode and prefill sequences in one grid) against
+the oracle's variable-length evaluation (each sequence as a batch of one).
+
+Bars as everywhere: bf16/f16 atol=2e-3, rtol=2^-8, -inf patterns exact, no NaN.  On a batch whose
+sequences all have the same query count, the unified launch runs the same per-unit code as the
+uniform entry point's tensor-core kernel, so the two agree bit for bit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_201_gb300 import workloads as W
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import paged_kv_cache_201_gb300 as pa
+    pa.load_library(build_if_missing=True)
+    return pa
+
+
+def _device(wl, k=None, v=None):
+    import torch
+    dw = _gpu.DeviceWorkload(wl) if k is None else None
+    d = {"q": W.host_to_torch(wl.q, wl.dtype).cuda(),
+         "k": dw.k if dw else k, "v": dw.v if dw else v,
+         "bt": torch.from_numpy(np.ascontiguousarray(wl.block_table)).cuda(),
+         "sl": torch.from_numpy(np.ascontiguousarray(wl.seq_lens)).cuda(),
+         "qs": torch.from_numpy(np.ascontiguousarray(wl.q_start)).cuda(),
+         "qo": None if wl.q_offset is None else torch.from_numpy(np.ascontiguousarray(wl.q_offset)).cuda()}
+    return d
+
+
+def _run(pa, wl, d, S):
+    """Returns float64 numpy out [T, Hq, D], lse [T, Hq] (+ part_out / part_lse for S > 1)."""
+    import torch
+    T, Hq, D = wl.Sq, wl.Hq, wl.D
+    res = {}
+    if S == 1:
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+        pa.paged_attn_fwd_varlen(d["q"], d["k"], d["v"], d["bt"], d["sl"], d["qs"], wl.causal, d["qo"], 1, wl.scale,
+                                 out, lse)
+    else:
+        po = torch.empty((S, T, Hq, D), dtype=torch.float32, device="cuda")
+        pl = torch.empty((S, T, Hq), dtype=torch.float32, device="cuda")
+        pa.paged_attn_fwd_varlen(d["q"], d["k"], d["v"], d["bt"], d["sl"], d["qs"], wl.causal, d["qo"], S, wl.scale,
+                                 po, pl)
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+        pa.paged_attn_combine(po, pl, out, lse)
+        res["part_out"], res["part_lse"] = _gpu.to_f64(po, "f32"), _gpu.to_f64(pl, "f32")
+    torch.cuda.synchronize()
+    res["out"], res["lse"] = _gpu.to_f64(out, wl.dtype), _gpu.to_f64(lse, "f32")
+    return res
+
+
+def _oracle(wl, S, k=None, v=None):
+    dims = oracle.make_dims(B=wl.B, Sq=wl.Sq, Hq=wl.Hq, Hkv=wl.Hkv, D=wl.D, page_size=wl.page_size,
+                            bt_stride=int(wl.block_table.shape[1]), dtype=wl.dtype, num_pages=wl.num_pages)
+    return oracle.rows_varlen(q=wl.q, k_cache=wl.k_cache if k is None else k, v_cache=wl.v_cache if v is None else v,
+                              block_table=wl.block_table, seq_lens=wl.seq_lens, q_start=wl.q_start,
+                              q_offset=wl.q_offset, causal=wl.causal, dims=dims, scale=wl.scale, split_kv=S)
+
+
+def _compare(res, ref, wl, S, what, rows=None):
+    sel = slice(None) if rows is None else rows
+    dt = wl.dtype
+    if S == 1:
+        _gpu.assert_close(res["out"][sel], ref["out"][sel], dt, f"{what} out")
+        _gpu.assert_close(res["lse"][sel], ref["lse"][sel], dt, f"{what} lse")
+    else:
+        _gpu.assert_close(res["out"][sel], ref["comb_out"][sel], dt, f"{what} combined out")
+        _gpu.assert_close(res["lse"][sel], ref["comb_lse"][sel], dt, f"{what} combined lse")
+        _gpu.assert_close(res["part_out"][:, sel], ref["part_out"][:, sel], dt, f"{what} partial out")
+        _gpu.assert_close(res["part_lse"][:, sel], ref["part_lse"][:, sel], dt, f"{what} partial lse")
+
+
+# ----------------------------------------------------------------------------- mixed small batches
+MIXED = dict(q_lens=[1, 0, 4, 1, 40, 3, 17, 1, 100], seq_lens=[300, 50, 4, 1000, 600, 70, 17, 1, 333])
+
+
+@pytest.mark.parametrize("dtype,D,Hq,Hkv", [("bf16", 128, 32, 8), ("f16", 64, 16, 2), ("bf16", 128, 16, 16)])
+@pytest.mark.parametrize("S", [1, 3])
+def test_mixed_batch(pa, dtype, D, Hq, Hkv, S):
+    """Decode sequences (1-4 tokens), empty ones and prefill chunks (17-100 tokens) in one launch,
+    causal with the default offsets (queries are each sequence's newest tokens)."""
+    wl = W.make_varlen(dtype=dtype, Hq=Hq, Hkv=Hkv, D=D, page_size=16, seed=40 + D + Hq, **MIXED)
+    res = _run(pa, wl, _device(wl), S)
+    ref = _oracle(wl, S)
+    _compare(res, ref, wl, S, f"mixed {dtype} D={D} G={Hq // Hkv} S={S}")
+    assert pa.paged_attn_last_error_word() == 0
+
+
+def test_mixed_batch_offsets_and_noncausal(pa):
+    """Explicit offsets (one hides every key from the first rows) and a non-causal batch."""
+    qo = [299, 10, 0, 999, -3, 67, 0, 0, 200]
+    wl = W.make_varlen(dtype="bf16", Hq=32, Hkv=8, D=128, page_size=32, q_offset=qo, seed=77, **MIXED)
+    res = _run(pa, wl, _device(wl), 2)
+    ref = _oracle(wl, 2)
+    _compare(res, ref, wl, 2, "offsets")
+    a = int(wl.q_start[4])
+    assert np.isneginf(res["lse"][a:a + 3]).all()  # reach <= 0 for the first 3 rows of sequence 4
+    wl2 = W.Workload(**{**wl.__dict__, "causal": False, "q_offset": None})
+    res = _run(pa, wl2, _device(wl2), 1)
+    _compare(res, _oracle(wl2, 1), wl2, 1, "non-causal")
+    assert pa.paged_attn_last_error_word() == 0
+
+
+@pytest.mark.parametrize("q_len,variant", [(1, 2), (3, 2), (37, 3)])
+def test_uniform_batch_bit_identical(pa, q_len, variant):
+    """Every sequence with the same query count: the unified launch equals the uniform tensor-core
+    kernel (16-row decode units, or 64-row tiles) bit for bit."""
+    import torch
+    wl = W.make_custom(dtype="bf16", B=5, Sq=q_len, Hq=32, Hkv=8, D=128, page_size=16,
+                       seq_lens=[64, 200, 500, 37, 1000], causal=True, seed=9)
+    dw = _gpu.DeviceWorkload(wl)
+    want = _gpu.run(dw, 2, variant=variant)
+    T = wl.B * q_len
+    packed = W.Workload(**{**wl.__dict__, "Sq": T, "q": wl.q.reshape(T, wl.Hq, wl.D),
+                           "q_start": np.arange(0, T + 1, q_len, dtype=np.int32)})
+    got = _run(pa, packed, _device(packed, dw.k, dw.v), 2)
+    assert np.array_equal(got["out"], want["out"].reshape(T, wl.Hq, wl.D))
+    assert np.array_equal(got["lse"], want["lse"].reshape(T, wl.Hq))
+    assert np.array_equal(got["part_out"], want["part_out"].reshape(2, T, wl.Hq, wl.D))
+    del torch
+
+
+def test_bad_q_start_is_reported(pa):
+    """A q_start entry past the packed tokens: that sequence is skipped (its rows untouched), the
+    others are exact, and the error word says so."""
+    import torch
+    wl = W.make_varlen(dtype="bf16", Hq=8, Hkv=2, D=64, page_size=16, seed=3, q_lens=[2, 3, 4],
+                       seq_lens=[40, 50, 60])
+    d = _device(wl)
+    bad = d["qs"].clone()
+    bad[2] = 1000  # sequence 1 ends, and sequence 2 starts, past T = 9
+    out = torch.full_like(d["q"], 7.0)
+    lse = torch.empty((wl.Sq, wl.Hq), dtype=torch.float32, device="cuda")
+    pa.paged_attn_fwd_varlen(d["q"], d["k"], d["v"], d["bt"], d["sl"], bad, True, None, 1, wl.scale, out, lse)
+    torch.cuda.synchronize()
+    assert pa.paged_attn_last_error_word() & pa.ERRBIT_QSTART
+    ref = _oracle(wl, 1)
+    got = _gpu.to_f64(out, "bf16")
+    _gpu.assert_close(got[0:2], ref["out"][0:2], "bf16", "sequence 0")
+    assert np.all(got[2:] == 7.0)
+
+
+# ----------------------------------------------------------------------------- full size
+@pytest.fixture(scope="module")
+def mixed_full():
+    wl = W.mixed_decode_prefill()
+    dw = _gpu.DeviceWorkload(W.Workload(**{**wl.__dict__, "q": wl.q[:1].reshape(1, 1, wl.Hq, wl.D)}))
+    k, v = dw.host_pools()
+    return wl, dw.k, dw.v, k, v
+
+
+def test_mixed_decode_prefill_full(pa, mixed_full):
+    """The benchmarked mixed batch (4 causal prefill chunks of 1024 tokens + 256 decode sequences of
+    4096 keys, 2 x 2 GiB pools) on sampled rows: 8 tokens of each prefill chunk and 8 decode
+    sequences, every head."""
+    wl, kd, vd, k, v = mixed_full
+    res = _run(pa, wl, _device(wl, kd, vd), 1)
+    assert not np.isnan(res["out"]).any() and np.isfinite(res["lse"]).all()
+    toks = []
+    for b in range(4):
+        a = int(wl.q_start[b])
+        toks += [a + i for i in (0, 1, 63, 64, 511, 777, 1022, 1023)]
+    toks += [int(wl.q_start[b]) for b in (4, 5, 77, 128, 200, 255, 258, 259)]
+    sel = np.array(toks)
+    # oracle only on the sampled tokens: a batch of the sampled sequences with those tokens
+    ref_out, ref_lse = [], []
+    for tok in toks:
+        b = int(np.searchsorted(wl.q_start, tok, side="right")) - 1
+        i = tok - int(wl.q_start[b])
+        one = W.Workload(**{**wl.__dict__, "B": 1, "Sq": int(wl.q_start[b + 1] - wl.q_start[b]),
+                            "q": wl.q[int(wl.q_start[b]):int(wl.q_start[b + 1])][None],
+                            "seq_lens": wl.seq_lens[b:b + 1], "block_table": wl.block_table[b:b + 1],
+                            "q_offset": wl.q_offset[b:b + 1], "q_start": None})
+        rows = np.stack([np.zeros(wl.Hq), np.full(wl.Hq, i), np.arange(wl.Hq)], axis=1).astype(np.int32)
+        r = oracle.workload_rows(one, split_kv=1, row_bih=rows, k_cache=k, v_cache=v, want_split=False)
+        ref_out.append(r["out"])
+        ref_lse.append(r["lse"])
+    _gpu.assert_close(res["out"][sel], np.stack(ref_out), "bf16", "mixed full out")
+    _gpu.assert_close(res["lse"][sel], np.stack(ref_lse), "bf16", "mixed full lse")
+    assert pa.paged_attn_last_error_word() == 0
