@@ -69,8 +69,10 @@ enum {
     PA_VARIANT_SIMT = 1,         /* CUDA-core kernel: any dtype, any head grouping */
     PA_VARIANT_MMA_DECODE = 2,   /* tensor-core decode: Sq * (Hq/Hkv) <= 16 rows, keys split across warps */
     PA_VARIANT_MMA_PREFILL = 3,  /* warp-level tensor cores, 64-row query tiles (prefill / long query runs) */
-    PA_VARIANT_TC05_PREFILL = 4  /* tcgen05 + tensor memory, 128-row query tiles; bf16/f16, head_dim 128,
+    PA_VARIANT_TC05_PREFILL = 4, /* tcgen05 + tensor memory, 128-row query tiles; bf16/f16, head_dim 128,
                                     Hq/Hkv dividing 128 */
+    PA_VARIANT_MMA_T = 5         /* tensor cores, transposed products (keys and head dim as MMA rows), 8-row
+                                    units; bf16/f16, head_dim 256 (the only 16-bit variant there) */
 };
 
 /*
@@ -83,7 +85,8 @@ enum {
  *                q_len newest tokens
  *   q_offset     [batch] int32 or NULL: position of query row 0 of sequence b
  *                inside its K/V sequence (NULL means seq_lens[b] - q_len)
- * Supported: dtype in {PA_F32, PA_F16, PA_BF16}; head_dim in {64, 128};
+ * Supported: dtype in {PA_F32, PA_F16, PA_BF16}; head_dim in {64, 128, 256} (256: not for the FP8 and
+ * variable-length entry points);
  * page_size in {16, 32, 64}; num_q_heads a multiple of num_kv_heads;
  * num_pages * page_size < 2^31 tokens (each pool may exceed 2^31 bytes).
  */

@@ -68,7 +68,7 @@ int check_dims(const pa_dims *d) {
     if (d->batch < 0 || d->q_len < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->bt_stride < 0)
         return PA_EINVAL;
     if (d->num_q_heads % d->num_kv_heads != 0) return PA_EINVAL;
-    if (d->head_dim != 64 && d->head_dim != 128) return PA_EUNSUPPORTED;
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return PA_EUNSUPPORTED;
     if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64) return PA_EUNSUPPORTED;
     if (d->num_pages < 1) return PA_EINVAL;
     if (d->num_pages * (int64_t)d->page_size >= (int64_t)1 << 31) return PA_EUNSUPPORTED;
@@ -145,6 +145,7 @@ int choose_variant(const pa_dims *d) {
     if (d->dtype == PA_F32) return PA_VARIANT_SIMT;
     const int64_t rows = (int64_t)d->q_len * (d->num_q_heads / d->num_kv_heads);
     if (rows <= 1) return PA_VARIANT_SIMT;  // single-head decode: a 16-row tile would be 1/16 used
+    if (d->head_dim == 256) return PA_VARIANT_MMA_T;
     if (rows <= pa::kDecodeRows) return PA_VARIANT_MMA_DECODE;
     // 128-row tcgen05 tiles once at least half a tile of rows is real work
     if (rows >= 64 && tc05_supports(d)) return PA_VARIANT_TC05_PREFILL;
@@ -242,10 +243,13 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
         case PA_VARIANT_SIMT:
             break;
         case PA_VARIANT_MMA_DECODE:
-            if (dims->dtype == PA_F32 || rows > pa::kDecodeRows) return PA_EUNSUPPORTED;
+            if (dims->dtype == PA_F32 || rows > pa::kDecodeRows || dims->head_dim == 256) return PA_EUNSUPPORTED;
             break;
         case PA_VARIANT_MMA_PREFILL:
-            if (dims->dtype == PA_F32) return PA_EUNSUPPORTED;
+            if (dims->dtype == PA_F32 || dims->head_dim == 256) return PA_EUNSUPPORTED;
+            break;
+        case PA_VARIANT_MMA_T:
+            if (dims->dtype == PA_F32 || dims->head_dim != 256) return PA_EUNSUPPORTED;
             break;
         case PA_VARIANT_TC05_PREFILL:
             if (!tc05_supports(dims)) return PA_EUNSUPPORTED;
@@ -266,6 +270,11 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
     cudaError_t e;
     if (variant == PA_VARIANT_SIMT) {
         e = pa::launch_simt(p, dims->dtype, st);
+    } else if (variant == PA_VARIANT_MMA_T) {
+        CUtensorMap tmk, tmv;
+        if ((rc = make_pool_map(&tmk, k_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
+        if ((rc = make_pool_map(&tmv, v_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
+        e = pa::launch_mma_t(p, dims->dtype, tmk, tmv, st);
     } else if (variant == PA_VARIANT_TC05_PREFILL) {
         CUtensorMap tmq, tmk, tmv;
         if ((rc = make_q_map(&tmq, q, dims)) != PA_OK) return rc;
@@ -297,7 +306,7 @@ int paged_attn_auto_split(const pa_dims *dims, int num_sms, int64_t device_bytes
     const int G = dims->num_q_heads / dims->num_kv_heads;
     const int64_t rows = (int64_t)dims->q_len * G;
     // query-row tiles per (sequence, kv head) of the kernel the planner would pick
-    const int64_t tile_rows = rows <= pa::kDecodeRows ? pa::kDecodeRows : 128;
+    const int64_t tile_rows = dims->head_dim == 256 ? 8 : (rows <= pa::kDecodeRows ? pa::kDecodeRows : 128);
     const int64_t row_tiles = (rows + tile_rows - 1) / tile_rows;
     const int64_t units1 = (int64_t)dims->batch * dims->num_kv_heads * (row_tiles > 0 ? row_tiles : 1);
     const int64_t want = 2LL * num_sms;  // two waves of units
@@ -349,6 +358,7 @@ int paged_attn_fwd_kvq(const void *q, const void *k_cache, const void *v_cache, 
     int rc = check_dims(dims);
     if (rc != PA_OK) return rc;
     if (dims->dtype == PA_F32 || kv_dtype != PA_FP8_E4M3) return PA_EDTYPE;
+    if (dims->head_dim == 256) return PA_EUNSUPPORTED;
     if (split_kv < 1 || split_kv > 65535) return PA_EINVAL;
     if (!isfinite(scale)) return PA_EINVAL;
     const int64_t nrows = (int64_t)dims->batch * dims->q_len * dims->num_q_heads;
@@ -395,6 +405,7 @@ int paged_attn_fwd_varlen(const void *q, const void *k_cache, const void *v_cach
     int rc = check_dims(dims);
     if (rc != PA_OK) return rc;
     if (dims->dtype == PA_F32) return PA_EDTYPE;
+    if (dims->head_dim == 256) return PA_EUNSUPPORTED;
     if (split_kv < 1 || split_kv > 65535) return PA_EINVAL;
     if (!isfinite(scale)) return PA_EINVAL;
     if (dims->batch == 0 || dims->q_len == 0) return PA_OK;  // no query token
@@ -422,7 +433,7 @@ int paged_attn_combine(const float *part_out, const float *part_lse, int split_k
                        int out_dtype, void *out, float *lse, void *stream) {
     if (out_dtype != PA_F32 && out_dtype != PA_F16 && out_dtype != PA_BF16) return PA_EDTYPE;
     if (split_kv < 1 || split_kv > 65535 || rows < 0) return PA_EINVAL;
-    if (head_dim != 64 && head_dim != 128) return PA_EUNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_EUNSUPPORTED;
     if (rows == 0) return PA_OK;
     if (!part_out || !part_lse || !out) return PA_EINVAL;
     if (!aligned16(part_out) || !aligned16(out) || (reinterpret_cast<uintptr_t>(part_lse) & 3u) ||

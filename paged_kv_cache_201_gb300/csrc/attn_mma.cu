@@ -79,65 +79,8 @@ __device__ __forceinline__ void mma_unit(const CUtensorMap *tmK, const CUtensorM
     __syncthreads();
 
     if (warp == kMmaConsumerWarps) {
-        // ================================================================ producer
-        if (lane == 0) {
-            tma_prefetch_desc(tmK);
-            tma_prefetch_desc(tmV);
-        }
-        const int pps = kMmaTileKeys >> ps_shift;                 // pages per stage (divides 32)
-        const uint32_t box_bytes = (uint32_t)(Geo<D>::NH * ps * 128);
-        const int pg_end = (k_hi + ps - 1) >> ps_shift;          // pages this unit reads
-        const int32_t *bt_row = p.block_table + (long long)b * p.W;
-        int batch = pg0;                                           // page held by lane 0 of id_cur
-        int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
-        int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
-        bool bad = false;
-        int issued = 0;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int st = t % NSTAGE;
-            if (t >= NSTAGE && !bad) {
-                const bool ok = mbar_wait(bar_em + 8 * st, ((t / NSTAGE) - 1) & 1, p.err);
-                bad = __any_sync(0xffffffffu, !ok);
-            }
-            const int pg_first = pg0 + t * pps;
-            if (pg_first >= batch + 32) {
-                batch += 32;
-                id_cur = id_next;
-                const int nx = batch + 32 + lane;
-                id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
-            }
-            const int my_pg = pg_first + lane;
-            const int id = __shfl_sync(0xffffffffu, id_cur, (my_pg - batch) & 31);
-            if (bad) break;
-            const int nvalid = min(pps, pg_end - pg_first);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar_fk + 8 * st, (uint32_t)nvalid * box_bytes);
-                mbar_arrive_expect_tx(bar_fv + 8 * st, (uint32_t)nvalid * box_bytes);
-            }
-            __syncwarp();
-            if (lane < nvalid) {
-                int tok;
-                if (id < 0 || (long long)id >= p.num_pages) {
-                    atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
-                    tok = -ps;  // wholly out of the tensor: the box reads as zeros
-                } else {
-                    tok = id << ps_shift;
-                }
-                const uint32_t off = (uint32_t)lane * box_bytes;
-                const uint32_t kdst = sbase + (uint32_t)(st * 2 * kStage) + off;
-                tma_load_4d(kdst, tmK, bar_fk + 8 * st, 0, tok, 0, kvh);
-                tma_load_4d(kdst + kStage, tmV, bar_fv + 8 * st, 0, tok, 0, kvh);
-            }
-            issued = t + 1;
-        }
-        // Every copy must have landed before the CTA may exit: wait (bounded) for the
-        // last phase of each stage that was armed.
-        for (int t = max(0, issued - NSTAGE); t < issued; ++t) {
-            const int st = t % NSTAGE;
-            const uint32_t par = (t / NSTAGE) & 1;
-            mbar_wait(bar_fk + 8 * st, par, p.err);
-            mbar_wait(bar_fv + 8 * st, par, p.err);
-        }
+        produce_pages16<D, NSTAGE>(tmK, tmV, p, b, kvh, pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk, bar_fv, bar_em,
+                                   lane);
         return;
     }
 

@@ -606,7 +606,7 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
         }
     }
     named_bar_sync(1, kMmaConsumerWarps * 32);
-    if (!bad) decode_merge_store<T, D>(p, sm, sq, kvh, s, rows);
+    if (!bad) decode_merge_store<T, D>(p, sm, sq, kvh, s, 0, rows);
 }
 
 // ============================================================================ prefill

@@ -67,9 +67,14 @@ __global__ void __launch_bounds__(kSimtWarps * 32) paged_attn_simt_kernel(const 
     constexpr int CPR = D / EPV;             // 16-byte chunks per key row
     constexpr int KS = D + 1;                // padded smem row (conflict-free column walks)
     constexpr int DPL = D / 32;              // output columns per lane
-    __shared__ float s_k[kSimtKeys * KS];
-    __shared__ float s_v[kSimtKeys * KS];
-    __shared__ float s_q[kSimtRows * D];
+    // K, V and Q staging: static for D <= 128; D = 256 (74 KiB) takes dynamic shared memory
+    constexpr bool kDyn = D > 128;
+    constexpr int kFloats = 2 * kSimtKeys * KS + kSimtRows * D;
+    __shared__ float s_static[kDyn ? 1 : kFloats];
+    extern __shared__ float s_dynamic[];
+    float *const s_k = kDyn ? s_dynamic : s_static;
+    float *const s_v = s_k + kSimtKeys * KS;
+    float *const s_q = s_v + kSimtKeys * KS;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int unit = blockIdx.x;
@@ -209,10 +214,17 @@ static cudaError_t launch_simt_t(const FwdParams &p, cudaStream_t stream) {
     const long long units = (long long)p.B * p.split_kv * p.Hkv * q.row_tiles;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (p.D == 128)
+    if (p.D == 256) {
+        constexpr size_t smem = (size_t)(2 * kSimtKeys * 257 + kSimtRows * 256) * 4;
+        auto kern = paged_attn_simt_kernel<T, 256>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<(unsigned)units, kSimtWarps * 32, smem, stream>>>(q);
+    } else if (p.D == 128) {
         paged_attn_simt_kernel<T, 128><<<(unsigned)units, kSimtWarps * 32, 0, stream>>>(q);
-    else
+    } else {
         paged_attn_simt_kernel<T, 64><<<(unsigned)units, kSimtWarps * 32, 0, stream>>>(q);
+    }
     return cudaGetLastError();
 }
 

@@ -35,12 +35,15 @@ __global__ void __launch_bounds__(256) paged_attn_combine_kernel(const float *__
             wsum += w;
             if (w != 0.f) {
                 const float *src = part_out + ((long long)s * rows + row) * D + lane * DPL;
-                if constexpr (DPL == 4) {
-                    const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
-                    acc[0] = fmaf(w, v.x, acc[0]);
-                    acc[1] = fmaf(w, v.y, acc[1]);
-                    acc[2] = fmaf(w, v.z, acc[2]);
-                    acc[3] = fmaf(w, v.w, acc[3]);
+                if constexpr (DPL % 4 == 0) {
+#pragma unroll
+                    for (int c4 = 0; c4 < DPL; c4 += 4) {
+                        const float4 v = __ldg(reinterpret_cast<const float4 *>(src + c4));
+                        acc[c4] = fmaf(w, v.x, acc[c4]);
+                        acc[c4 + 1] = fmaf(w, v.y, acc[c4 + 1]);
+                        acc[c4 + 2] = fmaf(w, v.z, acc[c4 + 2]);
+                        acc[c4 + 3] = fmaf(w, v.w, acc[c4 + 3]);
+                    }
                 } else {
                     const float2 v = __ldg(reinterpret_cast<const float2 *>(src));
                     acc[0] = fmaf(w, v.x, acc[0]);
@@ -63,7 +66,10 @@ static cudaError_t launch_combine_t(const float *po, const float *pl, int S, lon
     const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (D == 128)
+    if (D == 256)
+        paged_attn_combine_kernel<TO, 256>
+            <<<(unsigned)blocks, kRowsPerBlock * 32, 0, stream>>>(po, pl, S, rows, static_cast<TO *>(out), lse);
+    else if (D == 128)
         paged_attn_combine_kernel<TO, 128>
             <<<(unsigned)blocks, kRowsPerBlock * 32, 0, stream>>>(po, pl, S, rows, static_cast<TO *>(out), lse);
     else

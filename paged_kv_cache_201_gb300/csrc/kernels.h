@@ -34,6 +34,9 @@ size_t tc05_smem_bytes();
 cudaError_t launch_tc05(const FwdParams &p, int dtype, const CUtensorMap &tmq, const CUtensorMap &tmk,
                         const CUtensorMap &tmv, cudaStream_t stream);
 cudaError_t launch_simt(const FwdParams &p, int dtype, cudaStream_t stream);
+// head_dim 256, bf16/f16: transposed products, 8-row units.
+cudaError_t launch_mma_t(const FwdParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                         cudaStream_t stream);
 cudaError_t launch_combine(const float *part_out, const float *part_lse, int S, long long rows, int D,
                            int out_dtype, void *out, float *lse, cudaStream_t stream);
 cudaError_t launch_plan(const int32_t *seq_lens, int B, int ps, int S, int32_t *plan, cudaStream_t stream);

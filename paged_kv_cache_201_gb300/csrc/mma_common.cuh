@@ -63,6 +63,79 @@ __device__ __forceinline__ void store_lse(const FwdParams &p, int s, long long r
     }
 }
 
+// The producer warp of a unit over 16-bit pools: page ids 32 at a time (one per lane, never past
+// the unit's pages), then per 64-key stage t one 4-D TMA box per page and pool (page_size tokens
+// x one kv head x head_dim, 128-byte swizzled) into ring stage t % NSTAGE, armed on the stage's K
+// and V full barriers once the consumers have released it (rocm-libraries PR #14349, Technical
+// Details: page ids loaded once per tile).  An id outside [0, num_pages) is not dereferenced: its
+// box starts before the tensor and reads as zeros, and PA_ERRBIT_PAGE_RANGE is set.
+template <int D, int NSTAGE>
+__device__ __forceinline__ void produce_pages16(const CUtensorMap *tmK, const CUtensorMap *tmV, const FwdParams &p,
+                                                int b, int kvh, int pg0, int k_hi, int n_tiles, int ps_shift,
+                                                uint32_t sbase, uint32_t bar_fk, uint32_t bar_fv, uint32_t bar_em,
+                                                int lane) {
+    constexpr int kStage = Geo<D>::kStageBytes;
+    const int ps = 1 << ps_shift;
+    if (lane == 0) {
+        tma_prefetch_desc(tmK);
+        tma_prefetch_desc(tmV);
+    }
+    const int pps = kMmaTileKeys >> ps_shift;                 // pages per stage (divides 32)
+    const uint32_t box_bytes = (uint32_t)(Geo<D>::NH * ps * 128);
+    const int pg_end = (k_hi + ps - 1) >> ps_shift;          // pages this unit reads
+    const int32_t *bt_row = p.block_table + (long long)b * p.W;
+    int batch = pg0;                                           // page held by lane 0 of id_cur
+    int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
+    int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
+    bool bad = false;
+    int issued = 0;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % NSTAGE;
+        if (t >= NSTAGE && !bad) {
+            const bool ok = mbar_wait(bar_em + 8 * st, ((t / NSTAGE) - 1) & 1, p.err);
+            bad = __any_sync(0xffffffffu, !ok);
+        }
+        const int pg_first = pg0 + t * pps;
+        if (pg_first >= batch + 32) {
+            batch += 32;
+            id_cur = id_next;
+            const int nx = batch + 32 + lane;
+            id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
+        }
+        const int my_pg = pg_first + lane;
+        const int id = __shfl_sync(0xffffffffu, id_cur, (my_pg - batch) & 31);
+        if (bad) break;
+        const int nvalid = min(pps, pg_end - pg_first);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_fk + 8 * st, (uint32_t)nvalid * box_bytes);
+            mbar_arrive_expect_tx(bar_fv + 8 * st, (uint32_t)nvalid * box_bytes);
+        }
+        __syncwarp();
+        if (lane < nvalid) {
+            int tok;
+            if (id < 0 || (long long)id >= p.num_pages) {
+                atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
+                tok = -ps;  // wholly out of the tensor: the box reads as zeros
+            } else {
+                tok = id << ps_shift;
+            }
+            const uint32_t off = (uint32_t)lane * box_bytes;
+            const uint32_t kdst = sbase + (uint32_t)(st * 2 * kStage) + off;
+            tma_load_4d(kdst, tmK, bar_fk + 8 * st, 0, tok, 0, kvh);
+            tma_load_4d(kdst + kStage, tmV, bar_fv + 8 * st, 0, tok, 0, kvh);
+        }
+        issued = t + 1;
+    }
+    // Every copy must have landed before the CTA may exit: wait (bounded) for the
+    // last phase of each stage that was armed.
+    for (int t = max(0, issued - NSTAGE); t < issued; ++t) {
+        const int st = t % NSTAGE;
+        const uint32_t par = (t / NSTAGE) & 1;
+        mbar_wait(bar_fk + 8 * st, par, p.err);
+        mbar_wait(bar_fv + 8 * st, par, p.err);
+    }
+}
+
 // A unit with no valid key for any of its rows: output 0, lse -inf (consumer warps only).
 template <typename T, int D>
 __device__ __forceinline__ void store_empty_unit(const FwdParams &p, const SeqRows &sq, int kvh, int s, int row0,
@@ -108,11 +181,12 @@ __host__ __device__ constexpr size_t merge_scratch_bytes(int D) {
 }
 
 // Second half of the decode merge: shared memory `sm` holds, for each consumer warp w, rows
-// [w][16][D + 4] of unnormalised outputs, then maxima [w][16] and sums [w][16] (log2 domain).
-// Each row is combined over the warps (0/0 guard: l == 0 stores 0, lse -inf) and stored.
+// [w][16][D + 4] of unnormalised outputs, then maxima [w][16] and sums [w][16] (log2 domain), for
+// unit rows row0 .. row0 + 15.  Each row below row_end is combined over the warps (0/0 guard:
+// l == 0 stores 0, lse -inf) and stored.
 template <typename T, int D>
 __device__ __forceinline__ void decode_merge_store(const FwdParams &p, const float *sm, const SeqRows &sq, int kvh,
-                                                   int s, int row_end) {
+                                                   int s, int row0, int row_end) {
     constexpr int ACC_STRIDE = D + 4;
     const float *s_acc = sm;
     const float *s_m = sm + kMmaConsumerWarps * 16 * ACC_STRIDE;
@@ -121,7 +195,7 @@ __device__ __forceinline__ void decode_merge_store(const FwdParams &p, const flo
     const int r = tid >> 3;       // 16 rows x 8 column groups
     const int cg = tid & 7;
     constexpr int COLS = D / 8;
-    if (r < row_end) {
+    if (row0 + r < row_end) {
         float M = kNegInf;
 #pragma unroll
         for (int w = 0; w < kMmaConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + r]);
@@ -133,7 +207,7 @@ __device__ __forceinline__ void decode_merge_store(const FwdParams &p, const flo
             Lsum += wsc[w] * s_l[w * 16 + r];
         }
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-        const long long ridx = out_row_index(p, sq, kvh, r);
+        const long long ridx = out_row_index(p, sq, kvh, row0 + r);
 #pragma unroll
         for (int c = 0; c < COLS; c += 2) {
             const int col = cg * COLS + c;
@@ -177,7 +251,7 @@ __device__ __forceinline__ void decode_merge(const FwdParams &p, float *sm, cons
         }
     }
     named_bar_sync(1, kMmaConsumerWarps * 32);
-    if (!bad) decode_merge_store<T, D>(p, sm, sq, kvh, s, row_end);
+    if (!bad) decode_merge_store<T, D>(p, sm, sq, kvh, s, 0, row_end);
 }
 
 }  // namespace mmac

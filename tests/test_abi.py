@@ -74,6 +74,10 @@ def _fwd(lib, dims, split=1, scale=0.1, lse=FAKE, q=FAKE, out=FAKE, variant=0):
     ({}, 1, 0.1, dict(q=FAKE + 2), EINVAL),
     ({}, 1, 0.1, dict(q=None), EINVAL),
     (dict(dtype=pa.PA_F32), 1, 0.1, dict(variant=2), EUNSUP),
+    (dict(head_dim=256), 1, 0.1, dict(variant=2), EUNSUP),
+    (dict(head_dim=256), 1, 0.1, dict(variant=3), EUNSUP),
+    (dict(head_dim=128), 1, 0.1, dict(variant=5), EUNSUP),
+    (dict(head_dim=256, dtype=pa.PA_F32), 1, 0.1, dict(variant=5), EUNSUP),
     (dict(q_len=2, num_q_heads=32), 1, 0.1, dict(variant=2), EUNSUP),
     ({}, 1, 0.1, dict(variant=9), EINVAL),
     (dict(batch=0), 1, 0.1, {}, OK),
@@ -145,6 +149,7 @@ def test_fwd_kvq_validation(lib):
     assert _kvq(lib, _dims(dtype=pa.PA_F32)) == EDTYPE              # f32 queries are not read against FP8 pools
     assert _kvq(lib, _dims(), kv_dtype=pa.PA_BF16) == EDTYPE       # pools must be E4M3
     assert _kvq(lib, _dims(head_dim=96)) == EUNSUP
+    assert _kvq(lib, _dims(head_dim=256)) == EUNSUP
     assert _kvq(lib, _dims(), split=0) == EINVAL
     assert _kvq(lib, _dims(), k_scale=None) == EINVAL
     assert _kvq(lib, _dims(), v_scale=FAKE + 2) == EINVAL
@@ -175,3 +180,4 @@ def test_fwd_varlen_validation(lib):
     assert call(_dims(q_len=40), split=2, lse=None) == EINVAL
     assert call(_dims(q_len=40, head_dim=96)) == EUNSUP
     assert call(_dims(q_len=0), q_start=None) == OK   # no query token: nothing to do
+    assert call(_dims(q_len=40, head_dim=256)) == EUNSUP
