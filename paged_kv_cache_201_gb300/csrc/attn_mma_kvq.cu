@@ -38,7 +38,7 @@ using namespace mmac;
 
 namespace {
 
-constexpr int kMaxPagesPerStage = kMmaTileKeys / 16;  // page_size >= 16
+constexpr int kMaxPagesPerStage = kMmaTileKeys / 16;  // prefill stages: page_size >= 16
 
 template <int D>
 struct Geo8 {
@@ -199,23 +199,22 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 
 // The producer warp of one unit.  Page ids come 32 at a time, one per lane, never past the unit's
 // pages; each lane also holds its page's K and V scales (an id outside [0, num_pages) gets scale 0
-// and its rows read as zeros).  Per 64-key stage t it writes the stage's page scales into slot
+// and its rows read as zeros).  Per SK-key stage t it writes the stage's page scales into slot
 // t % (2 NSTAGE), arms the stage's barriers and issues one 3-D TMA box per page and pool into
 // ring stage t % NSTAGE.
-template <int D, int NSTAGE>
+template <int D, int NSTAGE, int SK>
 __device__ __forceinline__ void kvq_produce(const CUtensorMap *tmK, const CUtensorMap *tmV, const FwdParams &p,
                                             int b, int kvh, int pg0, int k_hi, int n_tiles, int ps_shift,
                                             uint32_t sbase, uint32_t bar_fk, uint32_t bar_fv, uint32_t bar_em,
-                                            float (*s_ks)[kMaxPagesPerStage], float (*s_vs)[kMaxPagesPerStage],
-                                            int lane) {
-    constexpr int kStage8 = Geo8<D>::kStage8;
+                                            float (*s_ks)[SK / 16], float (*s_vs)[SK / 16], int lane) {
+    constexpr int kStage8 = SK * D;  // bytes of one K (or V) stage of SK keys
     constexpr int kSlots = 2 * NSTAGE;
     if (lane == 0) {
         tma_prefetch_desc(tmK);
         tma_prefetch_desc(tmV);
     }
     const int ps = 1 << ps_shift;
-    const int pps = kMmaTileKeys >> ps_shift;       // pages per stage (1, 2 or 4)
+    const int pps = SK >> ps_shift;                 // pages per stage (page_size >= 16: at most SK / 16)
     const uint32_t box_bytes = (uint32_t)(ps * D);  // one page of one kv head, E4M3
     const int pg_end = (k_hi + ps - 1) >> ps_shift;
     const int32_t *bt_row = p.block_table + (long long)b * p.W;
@@ -331,19 +330,21 @@ __device__ __forceinline__ KvqUnit kvq_unit(const FwdParams &p, int b, int s, in
 // so that keys and head dimension fill the MMA's 16-row side and the few query rows (GQA group x
 // query tokens, padded to NR x 8) its 8-column side.  Warp w reads keys [16 w, 16 w + 16) of every
 // stage (one page: page_size >= 16); the four warps' softmax states are merged at the end.
-template <typename T, int D, int NR, int NSTAGE>
-__global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
+template <typename T, int D, int NR, int NSTAGE, int KPW, int MINB>
+__global__ void __launch_bounds__(kMmaThreads, MINB)
     paged_attn_kvq_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                                  const FwdParams p, int ps_shift) {
     using Op = MmaOp<__half>;
-    constexpr int kStage8 = Geo8<D>::kStage8;
+    constexpr int SK = kMmaConsumerWarps * KPW;  // keys per stage
+    constexpr int NB = KPW / 16;                 // 16-key blocks per warp and stage (one page each)
+    constexpr int kStage8 = SK * D;              // bytes of one K (or V) stage
     constexpr int kSlots = 2 * NSTAGE;
-    constexpr int MT = D / 16;  // 16-wide head-dim tiles of O^T
+    constexpr int MT = D / 16;                   // 16-wide head-dim tiles of O^T
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[3 * NSTAGE];
-    __shared__ float s_ks[kSlots][kMaxPagesPerStage];
-    __shared__ float s_vs[kSlots][kMaxPagesPerStage];
+    __shared__ float s_ks[kSlots][SK / 16];
+    __shared__ float s_vs[kSlots][SK / 16];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
     const SeqRows sq = uniform_seq(p, b);
     const int rows = p.rows;  // <= 8 NR
     const int k_hi = min(u.k_hi_split, row_key_limit(p, b, u.L, (rows - 1) / p.G));
-    const int n_tiles = k_hi > u.k_lo ? (k_hi - u.k_lo + kMmaTileKeys - 1) / kMmaTileKeys : 0;
+    const int n_tiles = k_hi > u.k_lo ? (k_hi - u.k_lo + SK - 1) / SK : 0;
     if (n_tiles == 0) {
         if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, sq, kvh, s, 0, rows);
         return;
@@ -378,15 +379,15 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
     __syncthreads();
 
     if (warp == kMmaConsumerWarps) {
-        kvq_produce<D, NSTAGE>(&tmK, &tmV, p, b, kvh, u.pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk, bar_fv, bar_em,
-                               s_ks, s_vs, lane);
+        kvq_produce<D, NSTAGE, SK>(&tmK, &tmV, p, b, kvh, u.pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk, bar_fv,
+                                   bar_em, s_ks, s_vs, lane);
         return;
     }
 
     // ==================================================================== consumers
     const int g = lane >> 2;
     const int tq = lane & 3;
-    const int kw0 = warp * 16;  // this warp's keys in every stage
+    const int kw0 = warp * KPW;  // this warp's keys in every stage: NB blocks of 16
     // Q^T operands: row-tile nr, this lane's row 8 nr + g.  The score and output fragments hold
     // rows 8 nr + 2 tq + e (e = 0, 1): their inverse query scalings come from lanes 4 (2 tq + e).
     uint32_t qb[NR][D / 16][2];
@@ -434,51 +435,64 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
         const int slot = t % kSlots;
         const uint32_t kring = sbase + (uint32_t)(st * 2 * kStage8);
         const uint32_t vring = kring + (uint32_t)kStage8;
-        const int tile_k0 = u.k_lo + t * kMmaTileKeys;
+        const int tile_k0 = u.k_lo + t * SK;
         const bool active = tile_k0 + kw0 < key_lim;  // warp-uniform
 
         if (!bad) {
             const bool ok = mbar_wait(bar_fk + 8 * st, par, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
-        uint32_t pb[NR][2][2];  // P^T operands: [row tile][high / low part][keys 0-7 / 8-15]
+        uint32_t pb[NB][NR][2][2];  // P^T operands: [block][row tile][high / low part][keys 0-7 / 8-15]
         if (!bad && active) {
-            // ---- S^T = K Q^T: keys g and g + 8 of the warp's 16, two partial sums over the steps
-            float sc[NR][2][4];
+            // ---- S^T = K Q^T: keys g and g + 8 of each of the warp's blocks, two partial sums each
+            float sc[NB][NR][2][4];
 #pragma unroll
-            for (int nr = 0; nr < NR; ++nr)
+            for (int hb = 0; hb < NB; ++hb)
 #pragma unroll
-                for (int c = 0; c < 2; ++c) sc[nr][c][0] = sc[nr][c][1] = sc[nr][c][2] = sc[nr][c][3] = 0.f;
+                for (int nr = 0; nr < NR; ++nr)
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-                uint32_t wg[4], w8[4];
-                lds_v4(ring_chunk_addr<D>(kring, kw0 + g, (D / 64) * tq + h), wg);
-                lds_v4(ring_chunk_addr<D>(kring, kw0 + g + 8, (D / 64) * tq + h), w8);
+                    for (int c = 0; c < 2; ++c) sc[hb][nr][c][0] = sc[hb][nr][c][1] = sc[hb][nr][c][2] = sc[hb][nr][c][3] = 0.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int kk = 4 * h + i;
-                    uint32_t a[4];
-                    e4m3x4_to_f16x4(wg[i], a[0], a[2]);
-                    e4m3x4_to_f16x4(w8[i], a[1], a[3]);
+            for (int hb = 0; hb < NB; ++hb) {
 #pragma unroll
-                    for (int nr = 0; nr < NR; ++nr) Op::run(sc[nr][i & 1], a, qb[nr][kk][0], qb[nr][kk][1]);
+                for (int h = 0; h < D / 64; ++h) {
+                    uint32_t wg[4], w8[4];
+                    lds_v4(ring_chunk_addr<D>(kring, kw0 + 16 * hb + g, (D / 64) * tq + h), wg);
+                    lds_v4(ring_chunk_addr<D>(kring, kw0 + 16 * hb + g + 8, (D / 64) * tq + h), w8);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int kk = 4 * h + i;
+                        uint32_t a[4];
+                        e4m3x4_to_f16x4(wg[i], a[0], a[2]);
+                        e4m3x4_to_f16x4(w8[i], a[1], a[3]);
+#pragma unroll
+                        for (int nr = 0; nr < NR; ++nr) Op::run(sc[hb][nr][i & 1], a, qb[nr][kk][0], qb[nr][kk][1]);
+                    }
                 }
             }
-            // ---- mask; scale x k_scale of the warp's page (log2 domain); online softmax per row
-            const float ksc = s_ks[slot][kw0 >> ps_shift];
-            const int j0 = tile_k0 + kw0 + g;  // key of fragment elements 0-1; j0 + 8 for 2-3
-            float al[NR][2], pv[NR][2][2];
+            // ---- mask; scale x k_scale of each block's page (log2 domain); one online-softmax step
+            // per row over the warp's KPW keys
+            float ksc[NB];
+#pragma unroll
+            for (int hb = 0; hb < NB; ++hb) ksc[hb] = s_ks[slot][(kw0 + 16 * hb) >> ps_shift];
+            float al[NR][2], pv[NB][NR][2][2];
             bool moved = false;
 #pragma unroll
             for (int nr = 0; nr < NR; ++nr) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const float f = srow[nr][e] * ksc;
-                    float x0 = sc[nr][0][e] + sc[nr][1][e];
-                    float x1 = sc[nr][0][2 + e] + sc[nr][1][2 + e];
-                    x0 = (j0 < lim[nr][e]) ? x0 * f : kNegInf;
-                    x1 = (j0 + 8 < lim[nr][e]) ? x1 * f : kNegInf;
-                    float mx = fmaxf(x0, x1);
+                    float x[NB][2];
+                    float mx = kNegInf;
+#pragma unroll
+                    for (int hb = 0; hb < NB; ++hb) {
+                        const float f = srow[nr][e] * ksc[hb];
+                        const int j0 = tile_k0 + kw0 + 16 * hb + g;  // key of elements 0-1; j0 + 8 for 2-3
+                        const float x0 = sc[hb][nr][0][e] + sc[hb][nr][1][e];
+                        const float x1 = sc[hb][nr][0][2 + e] + sc[hb][nr][1][2 + e];
+                        x[hb][0] = (j0 < lim[nr][e]) ? x0 * f : kNegInf;
+                        x[hb][1] = (j0 + 8 < lim[nr][e]) ? x1 * f : kNegInf;
+                        mx = fmaxf(mx, fmaxf(x[hb][0], x[hb][1]));
+                    }
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -487,23 +501,33 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
                     const float mu = (mn == kNegInf) ? 0.f : mn;
                     al[nr][e] = fast_exp2(m[nr][e] - mu);
                     m[nr][e] = mn;
-                    pv[nr][e][0] = fast_exp2(x0 - mu);
-                    pv[nr][e][1] = fast_exp2(x1 - mu);
-                    l[nr][e] = l[nr][e] * al[nr][e] + (pv[nr][e][0] + pv[nr][e][1]);
+                    float rs = 0.f;
+#pragma unroll
+                    for (int hb = 0; hb < NB; ++hb) {
+                        pv[hb][nr][e][0] = fast_exp2(x[hb][0] - mu);
+                        pv[hb][nr][e][1] = fast_exp2(x[hb][1] - mu);
+                        rs += pv[hb][nr][e][0] + pv[hb][nr][e][1];
+                    }
+                    l[nr][e] = l[nr][e] * al[nr][e] + rs;
                     moved |= al[nr][e] != 1.f;
                 }
-                // P^T tiles (rows: keys g / g + 8; columns: rows 2 tq, 2 tq + 1), high f16 part and
-                // remainder, transposed into the B operand layout (keys along k)
-                const uint32_t h0 = Op::pack(pv[nr][0][0], pv[nr][1][0]);
-                const uint32_t h1 = Op::pack(pv[nr][0][1], pv[nr][1][1]);
-                const float2 u0 = Op::unpack(h0), u1 = Op::unpack(h1);
-                const uint32_t r0 = Op::pack(pv[nr][0][0] - u0.x, pv[nr][1][0] - u0.y);
-                const uint32_t r1 = Op::pack(pv[nr][0][1] - u1.x, pv[nr][1][1] - u1.y);
-                pb[nr][0][0] = movmatrix_trans(h0);
-                pb[nr][0][1] = movmatrix_trans(h1);
-                pb[nr][1][0] = movmatrix_trans(r0);
-                pb[nr][1][1] = movmatrix_trans(r1);
             }
+            // P^T tiles (rows: keys g / g + 8; columns: rows 2 tq, 2 tq + 1), high f16 part and
+            // remainder, transposed into the B operand layout (keys along k)
+#pragma unroll
+            for (int hb = 0; hb < NB; ++hb)
+#pragma unroll
+                for (int nr = 0; nr < NR; ++nr) {
+                    const uint32_t h0 = Op::pack(pv[hb][nr][0][0], pv[hb][nr][1][0]);
+                    const uint32_t h1 = Op::pack(pv[hb][nr][0][1], pv[hb][nr][1][1]);
+                    const float2 u0 = Op::unpack(h0), u1 = Op::unpack(h1);
+                    const uint32_t r0 = Op::pack(pv[hb][nr][0][0] - u0.x, pv[hb][nr][1][0] - u0.y);
+                    const uint32_t r1 = Op::pack(pv[hb][nr][0][1] - u1.x, pv[hb][nr][1][1] - u1.y);
+                    pb[hb][nr][0][0] = movmatrix_trans(h0);
+                    pb[hb][nr][0][1] = movmatrix_trans(h1);
+                    pb[hb][nr][1][0] = movmatrix_trans(r0);
+                    pb[hb][nr][1][1] = movmatrix_trans(r1);
+                }
             if (__any_sync(0xffffffffu, moved)) {  // a running max moved: rescale O
 #pragma unroll
                 for (int nr = 0; nr < NR; ++nr)
@@ -520,47 +544,52 @@ __global__ void __launch_bounds__(kMmaThreads, NR == 1 ? 3 : 2)
             const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
-        // V bytes of keys g and g + 8 (this lane's D/4 bytes of each, as for K) into registers
-        uint32_t vw[2][D / 16];
+        // V bytes of keys g and g + 8 of each block (this lane's D/4 bytes of each, as for K)
+        uint32_t vw[NB][2][D / 16];
         if (!bad && active) {
 #pragma unroll
-            for (int kh = 0; kh < 2; ++kh)
+            for (int hb = 0; hb < NB; ++hb)
 #pragma unroll
-                for (int h = 0; h < D / 64; ++h) {
-                    uint32_t w[4];
-                    lds_v4(ring_chunk_addr<D>(vring, kw0 + g + 8 * kh, (D / 64) * tq + h), w);
+                for (int kh = 0; kh < 2; ++kh)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) vw[kh][4 * h + i] = w[i];
-                }
+                    for (int h = 0; h < D / 64; ++h) {
+                        uint32_t w[4];
+                        lds_v4(ring_chunk_addr<D>(vring, kw0 + 16 * hb + g + 8 * kh, (D / 64) * tq + h), w);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) vw[hb][kh][4 * h + i] = w[i];
+                    }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_em + 8 * st);  // K and V of the stage are read: free it
         if (!bad && active) {
-            // Keys at or past k_hi hold whatever the ring held before: zero V rows keep 0 x NaN out.
 #pragma unroll
-            for (int kh = 0; kh < 2; ++kh)
-                if (tile_k0 + kw0 + g + 8 * kh >= k_hi)
+            for (int hb = 0; hb < NB; ++hb) {
+                // Keys at or past k_hi hold whatever the ring held before: zero V rows keep 0 x NaN out.
 #pragma unroll
-                    for (int i = 0; i < D / 16; ++i) vw[kh][i] = 0u;
-            // ---- O^T += v_scale x V^T (Ph + Pl)^T over the warp's 16 keys.  Head-dim tile mt takes
-            // this lane's bytes 4 mt + {0..3} of keys g and g + 8: four 8 x 8 blocks (keys x 2-byte
-            // d slots) which movmatrix turns into the A operand (d x keys), so output row m of the
-            // tile is head-dim index out_d(mt, m) (see the merge below).
-            const float vsc = s_vs[slot][kw0 >> ps_shift];
+                for (int kh = 0; kh < 2; ++kh)
+                    if (tile_k0 + kw0 + 16 * hb + g + 8 * kh >= k_hi)
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                uint32_t x00, x01, x10, x11;  // [key half][d slot half]
-                e4m3x4_to_f16x4(vw[0][mt], x00, x01);
-                e4m3x4_to_f16x4(vw[1][mt], x10, x11);
-                const uint32_t a[4] = {movmatrix_trans(x00), movmatrix_trans(x01), movmatrix_trans(x10),
-                                       movmatrix_trans(x11)};
+                        for (int i = 0; i < D / 16; ++i) vw[hb][kh][i] = 0u;
+                // ---- O^T += v_scale x V^T (Ph + Pl)^T over the block's 16 keys.  Head-dim tile mt takes
+                // this lane's bytes 4 mt + {0..3} of keys g and g + 8: four 8 x 8 blocks (keys x 2-byte
+                // d slots) which movmatrix turns into the A operand (d x keys), so output row m of the
+                // tile is head-dim index out_d(mt, m) (see the merge below).
+                const float vsc = s_vs[slot][(kw0 + 16 * hb) >> ps_shift];
 #pragma unroll
-                for (int nr = 0; nr < NR; ++nr) {
-                    float tt[4] = {0.f, 0.f, 0.f, 0.f};
-                    Op::run(tt, a, pb[nr][0][0], pb[nr][0][1]);
-                    Op::run(tt, a, pb[nr][1][0], pb[nr][1][1]);
+                for (int mt = 0; mt < MT; ++mt) {
+                    uint32_t x00, x01, x10, x11;  // [key half][d slot half]
+                    e4m3x4_to_f16x4(vw[hb][0][mt], x00, x01);
+                    e4m3x4_to_f16x4(vw[hb][1][mt], x10, x11);
+                    const uint32_t a[4] = {movmatrix_trans(x00), movmatrix_trans(x01), movmatrix_trans(x10),
+                                           movmatrix_trans(x11)};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[nr][mt][e] = fmaf(vsc, tt[e], acc[nr][mt][e]);
+                    for (int nr = 0; nr < NR; ++nr) {
+                        float tt[4] = {0.f, 0.f, 0.f, 0.f};
+                        Op::run(tt, a, pb[hb][nr][0][0], pb[hb][nr][0][1]);
+                        Op::run(tt, a, pb[hb][nr][1][0], pb[hb][nr][1][1]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[nr][mt][e] = fmaf(vsc, tt[e], acc[nr][mt][e]);
+                    }
                 }
             }
         }
@@ -666,8 +695,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     __syncthreads();
 
     if (warp == kMmaConsumerWarps) {
-        kvq_produce<D, NSTAGE>(&tmK, &tmV, p, b, kvh, u.pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk, bar_fv, bar_em,
-                               s_ks, s_vs, lane);
+        kvq_produce<D, NSTAGE, kMmaTileKeys>(&tmK, &tmV, p, b, kvh, u.pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk,
+                                             bar_fv, bar_em, s_ks, s_vs, lane);
         return;
     }
 
@@ -830,7 +859,6 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
 }
 
 // ------------------------------------------------------------------------ host side
-static constexpr int kvq_decode_stages(int D, int NR) { return D == 128 ? 4 : 8; }
 static constexpr int kvq_prefill_stages(int D) { return D == 128 ? 4 : 6; }
 
 // ring (+ the widened V rows of the prefill kernel) + alignment slack
@@ -844,13 +872,14 @@ static int ps_shift_of(int ps) {
     return sh;
 }
 
-template <typename T, int D, int NR>
+// Decode shape: KPW keys per consumer warp and stage (stages of 4 KPW keys), NSTAGE-deep ring,
+// MINB CTAs per SM.
+template <typename T, int D, int NR, int KPW, int NSTAGE, int MINB>
 static cudaError_t launch_kvq_decode(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                      cudaStream_t stream) {
-    constexpr int NSTAGE = kvq_decode_stages(D, NR);
-    constexpr size_t smem = kvq_smem_bytes(D, NSTAGE, false);
-    static_assert(merge_scratch_bytes(D) + 1024 <= smem, "decode merge scratch must fit in the ring and the rows");
-    auto kern = paged_attn_kvq_decode_kernel<T, D, NR, NSTAGE>;
+    constexpr size_t smem = (size_t)NSTAGE * 2 * kMmaConsumerWarps * KPW * D + 1024;
+    static_assert(merge_scratch_bytes(D) + 1024 <= smem, "decode merge scratch must fit in the ring");
+    auto kern = paged_attn_kvq_decode_kernel<T, D, NR, NSTAGE, KPW, MINB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long units = (long long)p.B * p.split_kv * p.Hkv;
@@ -879,8 +908,11 @@ template <typename T, int D>
 static cudaError_t launch_kvq_d(const FwdParams &p, int mode, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 cudaStream_t stream) {
     if (mode == MODE_PREFILL) return launch_kvq_prefill<T, D>(p, tmk, tmv, stream);
-    return p.rows <= 8 ? launch_kvq_decode<T, D, 1>(p, tmk, tmv, stream)
-                       : launch_kvq_decode<T, D, 2>(p, tmk, tmv, stream);
+    // 16 keys per warp and stage, 4 (D = 128) or 8 (D = 64) 64-key stages: 65 KiB, so 3 CTAs per SM
+    // for <= 8 rows.  Measured on the FP8 Llama-3-8B decode: 32 keys per warp (two blocks sharing one
+    // softmax step) with 2 or 3 stages, and 6 stages at 2 CTAs per SM, were no faster.
+    if (p.rows <= 8) return launch_kvq_decode<T, D, 1, 16, (D == 128 ? 4 : 8), 3>(p, tmk, tmv, stream);
+    return launch_kvq_decode<T, D, 2, 16, (D == 128 ? 4 : 8), 2>(p, tmk, tmv, stream);
 }
 
 cudaError_t launch_mma_kvq(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
