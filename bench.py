@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode",
                     choices=["llama8b_decode", "over2gib_decode", "ragged_decode", "causal_prefill",
-                             "llama8b_decode_fp8", "mixed_decode_prefill", "d256_decode"])
+                             "llama8b_decode_fp8", "mixed_decode_prefill", "d256_decode", "mha_decode"])
     ap.add_argument("--split-kv", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences (llama8b/over2gib workloads only; smaller pools for profiling)")
@@ -190,6 +190,7 @@ KERNEL_SOURCES = {
     "paged_attn_mma_t_kernel": ("attn_mma_t.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
     "paged_attn_tc05_kernel": ("attn_tc05.cu", "tc05.cuh", "common.cuh", "kernels.h"),
     "paged_attn_simt_kernel": ("attn_simt.cu", "common.cuh", "kernels.h"),
+    "paged_attn_simt_decode_kernel": ("attn_simt_decode.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
 }
 
 
@@ -220,7 +221,8 @@ def recorded_traffic(kernel: str, workload: str):
 
 def build_workload(name, batch=None):
     from paged_kv_cache_201_gb300 import workloads as W
-    if batch is not None and name in ("llama8b_decode", "over2gib_decode", "llama8b_decode_fp8", "d256_decode"):
+    if batch is not None and name in ("llama8b_decode", "over2gib_decode", "llama8b_decode_fp8", "d256_decode",
+                                      "mha_decode"):
         return W.make(name, B=batch)
     return W.make(name)
 
@@ -360,6 +362,8 @@ def run_ours(args, ws, rank, local):
         kname = "paged_attn_kvq_prefill_kernel" if wl.Sq * wl.G > 16 else "paged_attn_kvq_decode_kernel"
     elif wl.D == 256 and wl.dtype != "f32" and wl.Sq * wl.G > 1 and args.variant in (0, 5):
         kname = "paged_attn_mma_t_kernel"
+    elif wl.Sq * wl.G == 1 and wl.dtype != "f32" and wl.D != 256 and args.variant in (0, 1):
+        kname = "paged_attn_simt_decode_kernel"
     elif args.variant:
         kname = {1: "paged_attn_simt_kernel", 4: "paged_attn_tc05_kernel"}.get(args.variant, "paged_attn_mma_kernel")
     else:  # what the planner picks for this shape

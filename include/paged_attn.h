@@ -66,7 +66,8 @@ enum {
 /* kernel variants (paged_attn_fwd_variant) */
 enum {
     PA_VARIANT_AUTO = 0,         /* planner's choice */
-    PA_VARIANT_SIMT = 1,         /* CUDA-core kernel: any dtype, any head grouping */
+    PA_VARIANT_SIMT = 1,         /* CUDA cores: any dtype, any head grouping (a single query row per kv head
+                                    in bf16/f16 at head_dim 64/128 streams K/V through a TMA ring) */
     PA_VARIANT_MMA_DECODE = 2,   /* tensor-core decode: Sq * (Hq/Hkv) <= 16 rows, keys split across warps */
     PA_VARIANT_MMA_PREFILL = 3,  /* warp-level tensor cores, 64-row query tiles (prefill / long query runs) */
     PA_VARIANT_TC05_PREFILL = 4, /* tcgen05 + tensor memory, 128-row query tiles; bf16/f16, head_dim 128,

@@ -268,7 +268,13 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (variant == PA_VARIANT_SIMT) {
+    if (variant == PA_VARIANT_SIMT && rows == 1 && dims->dtype != PA_F32 && dims->head_dim != 256) {
+        // single-row decode: the CUDA-core kernel over the TMA ring
+        CUtensorMap tmk, tmv;
+        if ((rc = make_pool_map(&tmk, k_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
+        if ((rc = make_pool_map(&tmv, v_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
+        e = pa::launch_simt_decode(p, dims->dtype, tmk, tmv, st);
+    } else if (variant == PA_VARIANT_SIMT) {
         e = pa::launch_simt(p, dims->dtype, st);
     } else if (variant == PA_VARIANT_MMA_T) {
         CUtensorMap tmk, tmv;

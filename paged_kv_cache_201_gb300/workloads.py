@@ -447,3 +447,21 @@ def d256_decode(seed: int = 1008, B: int = 128) -> Workload:
 
 
 CONFIGS["d256_decode"] = d256_decode
+
+
+def mha_decode(seed: int = 1009, B: int = 64) -> Workload:
+    """Single-head-group decode (no GQA): Hq=Hkv=32, D=128, L=4096, bf16, page_size 16, B * 256 pages
+    per pool (2 GiB each at B=64) in a seeded permutation; pools drawn on the device."""
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D, ps, L = 32, 32, 128, 16, 4096
+    per_seq = L // ps
+    P = B * per_seq
+    q = _normal_elems(rng, B * Hq * D, "bf16").reshape(B, 1, Hq, D)
+    perm = rng.permutation(P).astype(np.int64)
+    bt = perm[:B * per_seq].reshape(B, per_seq).astype(np.int32)
+    return Workload(name="mha_decode", dtype="bf16", B=B, Sq=1, Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
+                    num_pages=P, causal=False, scale=1.0 / math.sqrt(D), split_kv=(1,),
+                    seq_lens=np.full(B, L, dtype=np.int32), block_table=bt, q=q, device_cache_seed=seed)
+
+
+CONFIGS["mha_decode"] = mha_decode
