@@ -265,6 +265,15 @@ int paged_attn_debug_gather(const void *cache, const int32_t *block_table, const
                             const pa_dims *dims, int out_tokens, void *out, void *stream);
 
 /*
+ * paged_attn_debug_wait_timeout — check of the kernels' failure path: one warp waits, with the same
+ * bounded pipeline wait the kernels use, on a barrier that nothing completes.  After limit_us
+ * microseconds (1 .. 2 000 000; PA_EINVAL otherwise) the wait gives up, sets PA_ERRBIT_TIMEOUT in the
+ * device error word and the kernel returns, leaving the context usable: the way a stalled pipeline
+ * ends instead of hanging the GPU.  Asynchronous on `stream`.
+ */
+int paged_attn_debug_wait_timeout(uint32_t limit_us, void *stream);
+
+/*
  * paged_attn_last_error_word — synchronise the current device, then read and
  * clear its error word (PA_ERRBIT_* bits accumulated by every call since the
  * last read).  Returns PA_OK, or PA_ECUDA if the read failed.

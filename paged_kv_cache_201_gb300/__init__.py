@@ -84,6 +84,8 @@ def load_library(build_if_missing: bool = False):
     lib.paged_attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I32, P, I32, F, P, P, D, P]
     lib.paged_attn_fwd_varlen.restype = ctypes.c_int
     lib.paged_attn_debug_gather.argtypes = [P, P, P, D, I32, P, P]
+    lib.paged_attn_debug_wait_timeout.argtypes = [ctypes.c_uint32, P]
+    lib.paged_attn_debug_wait_timeout.restype = ctypes.c_int
     lib.paged_attn_last_error_word.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.paged_attn_strerror.argtypes = [I32]
     lib.paged_attn_strerror.restype = ctypes.c_char_p
@@ -399,6 +401,12 @@ def paged_attn_debug_gather(cache, block_table, seq_lens, out_tokens: int, out=N
                                                 int(out_tokens), _ptr(out), _stream(stream))
     _raise(rc, "paged_attn_debug_gather")
     return out
+
+
+def paged_attn_debug_wait_timeout(limit_us: int, stream=None) -> None:
+    """Run the kernels' bounded pipeline wait on a barrier nothing completes; it gives up after
+    ``limit_us`` and sets ERRBIT_TIMEOUT (see include/paged_attn.h)."""
+    _raise(load_library().paged_attn_debug_wait_timeout(int(limit_us), _stream(stream)), "paged_attn_debug_wait_timeout")
 
 
 def paged_attn_last_error_word() -> int:

@@ -474,6 +474,14 @@ int paged_attn_debug_gather(const void *cache, const int32_t *block_table, const
     return cuda_status(e);
 }
 
+int paged_attn_debug_wait_timeout(uint32_t limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 2000000) return PA_EINVAL;
+    unsigned int *err = nullptr;
+    int rc = error_word_ptr(&err);
+    if (rc != PA_OK) return rc;
+    return cuda_status(pa::launch_wait_probe(err, 1000ull * limit_us, static_cast<cudaStream_t>(stream)));
+}
+
 int paged_attn_last_error_word(uint32_t *flags) {
     if (!flags) return PA_EINVAL;
     if (cudaDeviceSynchronize() != cudaSuccess) return PA_ECUDA;

@@ -153,4 +153,24 @@ cudaError_t launch_gather(const void *cache, const int32_t *block_table, const i
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------- bounded wait check
+// One warp waits, with the kernels' bounded wait, on an mbarrier that nothing arrives at: after
+// limit_ns the wait gives up and records PA_ERRBIT_TIMEOUT in the error word, as a stalled
+// pipeline would.  Lets a test see the time-out path end and leave the context usable.
+__global__ void paged_attn_wait_probe_kernel(unsigned int *err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    mbar_wait(b, 0, err, limit_ns);  // phase 0 never completes
+}
+
+cudaError_t launch_wait_probe(unsigned int *err, unsigned long long limit_ns, cudaStream_t stream) {
+    paged_attn_wait_probe_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+    return cudaGetLastError();
+}
+
 }  // namespace pa

@@ -114,15 +114,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity; gives up after kWaitLimitNs and
-// records PA_ERRBIT_TIMEOUT.  Returns false on time-out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int *err) {
+// Wait for the phase with the given parity; gives up after limit_ns (kWaitLimitNs in every
+// kernel) and records PA_ERRBIT_TIMEOUT.  Returns false on time-out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int *err,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
         for (int k = 0; k < 64; ++k)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             atomicOr(err, (unsigned int)PA_ERRBIT_TIMEOUT);
             return false;
         }

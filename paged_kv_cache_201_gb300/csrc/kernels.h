@@ -43,6 +43,7 @@ cudaError_t launch_mma_t(const FwdParams &p, int dtype, const CUtensorMap &tmk, 
 cudaError_t launch_combine(const float *part_out, const float *part_lse, int S, long long rows, int D,
                            int out_dtype, void *out, float *lse, cudaStream_t stream);
 cudaError_t launch_plan(const int32_t *seq_lens, int B, int ps, int S, int32_t *plan, cudaStream_t stream);
+cudaError_t launch_wait_probe(unsigned int *err, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_gather(const void *cache, const int32_t *block_table, const int32_t *seq_lens, int B, int W,
                           int ps, int Hkv, int D, int esize, long long num_pages, int out_tokens, void *out,
                           unsigned int *err, cudaStream_t stream);

@@ -181,3 +181,8 @@ def test_fwd_varlen_validation(lib):
     assert call(_dims(q_len=40, head_dim=96)) == EUNSUP
     assert call(_dims(q_len=0), q_start=None) == OK   # no query token: nothing to do
     assert call(_dims(q_len=40, head_dim=256)) == EUNSUP
+
+
+def test_debug_wait_timeout_validation(lib):
+    assert lib.paged_attn_debug_wait_timeout(0, None) == EINVAL
+    assert lib.paged_attn_debug_wait_timeout(2_000_001, None) == EINVAL

@@ -203,3 +203,23 @@ def test_api_errors(pa):
         pa.paged_attn_fwd_variant(q32, dw.k.float(), dw.v.float(), dw.bt, dw.sl, False, None, 1, 0.1,
                                   torch.empty_like(q32), None, 2)
     assert e.value.code == -3
+
+
+def test_bounded_wait_gives_up_and_context_survives(pa):
+    """Failure path without a fault: a pipeline wait on a barrier nothing completes gives up after
+    its limit (here 50 ms), sets the time-out bit, and the next attention call still runs exactly."""
+    import time
+    import torch
+    assert pa.paged_attn_last_error_word() == 0
+    t0 = time.perf_counter()
+    pa.paged_attn_debug_wait_timeout(50_000)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert 0.04 < dt < 5.0
+    assert pa.paged_attn_last_error_word() == pa.ERRBIT_TIMEOUT
+    assert pa.paged_attn_last_error_word() == 0  # read and cleared
+    wl = W.make_custom(dtype="bf16", B=2, Sq=1, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=[33, 90], seed=77)
+    res = _gpu.run(_gpu.DeviceWorkload(wl), 2)
+    rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)
+    _gpu.compare_rows(res, oracle.workload_rows(wl, split_kv=2, row_bih=rows), rows, wl, 2, "after time-out")
+    assert pa.paged_attn_last_error_word() == 0
