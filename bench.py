@@ -41,7 +41,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode",
                     choices=["llama8b_decode", "over2gib_decode", "ragged_decode", "causal_prefill",
-                             "llama8b_decode_fp8", "mixed_decode_prefill", "d256_decode", "mha_decode"])
+                             "llama8b_decode_fp8", "mixed_decode_prefill", "d256_decode", "mha_decode",
+                             "causal_prefill_f16"])
     ap.add_argument("--split-kv", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences (llama8b/over2gib workloads only; smaller pools for profiling)")

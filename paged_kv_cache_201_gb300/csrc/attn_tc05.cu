@@ -79,9 +79,14 @@ __device__ __forceinline__ void t5_store_half_row(const FwdParams &p, int s, lon
 
 }  // namespace
 
+// P V with P split into a 16-bit high part and its rounding remainder (two products) for bf16; f16
+// rounds P to 2^-11 relative (p in [0, 1]), well inside the tolerance, so one product is enough.
+template <typename T>
+__host__ __device__ constexpr bool t5_split_p() { return !std::is_same<T, __half>::value; }
+
 // P for 32 keys of one row: p = exp2(s * c2 + nmu) for the nv (may be <= 0 or >= 32) valid keys, 0
 // for the rest; l accumulates the p; the 32 columns at `taddr` receive [16 columns of high parts |
-// 16 columns of remainders] (bf16/f16 pairs).
+// 16 columns of remainders] (bf16/f16 pairs; the remainders only when t5_split_p<T>()).
 template <typename T>
 __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], int nv, float c2, float nmu, float &l,
                                              uint32_t taddr) {
@@ -94,8 +99,10 @@ __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], int nv, fl
             const float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu));
             l4[i & 3] += p0 + p1;
             hi[i] = MmaOp<T>::pack(p0, p1);
-            const float2 h2 = MmaOp<T>::unpack(hi[i]);
-            lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+            if (t5_split_p<T>()) {
+                const float2 h2 = MmaOp<T>::unpack(hi[i]);
+                lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+            }
         }
     } else {
 #pragma unroll
@@ -105,13 +112,15 @@ __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], int nv, fl
             const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
             l4[i & 3] += p0 + p1;
             hi[i] = MmaOp<T>::pack(p0, p1);
-            const float2 h2 = MmaOp<T>::unpack(hi[i]);
-            lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+            if (t5_split_p<T>()) {
+                const float2 h2 = MmaOp<T>::unpack(hi[i]);
+                lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+            }
         }
     }
     l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
     tc05::st_16cols(taddr, hi);
-    tc05::st_16cols(taddr + 16u, lo);
+    if (t5_split_p<T>()) tc05::st_16cols(taddr + 16u, lo);
 }
 
 // Everything a role needs to know about one work unit; every role derives it the same way.
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     // keys 16kk..16kk+15: chunk kk/2 of 32 keys; highs at +0, remainders at +16
                     const uint32_t pa = pcol + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
                     tc05::mma_ts(ocol, pa, vd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                    tc05::mma_ts(ocol, pa + 16u, vd, idesc_pv, 1u);
+                    if (t5_split_p<T>()) tc05::mma_ts(ocol, pa + 16u, vd, idesc_pv, 1u);
                 }
                 tc05::commit(bar(B_VE + slot));
                 tc05::commit(bar(B_OD));

@@ -465,3 +465,16 @@ def mha_decode(seed: int = 1009, B: int = 64) -> Workload:
 
 
 CONFIGS["mha_decode"] = mha_decode
+
+
+def causal_prefill_f16(seed: int = 1010) -> Workload:
+    """The causal prefill shape (B=4, Sq=1024, Hq=32, Hkv=8, D=128, q_offset~U[0,3072]) in f16."""
+    wl = causal_prefill(seed=seed)
+    def to16(bits):  # bf16 bits -> the same values as f16 bits (exact for these N(0,1) draws)
+        f32 = (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+        return f32.astype(np.float16).view(np.uint16)
+    return Workload(**{**wl.__dict__, "name": "causal_prefill_f16", "dtype": "f16", "q": to16(wl.q),
+                       "k_cache": to16(wl.k_cache), "v_cache": to16(wl.v_cache)})
+
+
+CONFIGS["causal_prefill_f16"] = causal_prefill_f16

@@ -108,3 +108,18 @@ def test_tc05_many_units_per_cta(pa):
     for S in (4, 1):
         _check(wl, S, f"tc05 many units S={S}")
     assert pa.paged_attn_last_error_word() == 0
+
+
+@pytest.mark.parametrize("scale_mult", [1.0, 8.0])
+def test_tc05_f16_single_product(pa, scale_mult):
+    """f16 runs P V as one product with P rounded to f16: causal prefill rows including peaky
+    softmaxes (scores scaled up 8x, so a few keys carry the weight), every row against the oracle."""
+    lens = [70, 333, 1000]
+    wl = W.make_custom(dtype="f16", B=3, Sq=64, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=lens, causal=True,
+                       seed=880, scale=scale_mult / np.sqrt(128))
+    for S in (1, 3):
+        res = _gpu.run(_gpu.DeviceWorkload(wl), S, variant=4)
+        rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)
+        ref = oracle.workload_rows(wl, split_kv=S, row_bih=rows)
+        _gpu.compare_rows(res, ref, rows, wl, S, f"f16 tc05 x{scale_mult} S={S}")
+    assert pa.paged_attn_last_error_word() == 0
