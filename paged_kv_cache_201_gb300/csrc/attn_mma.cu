@@ -17,6 +17,9 @@
 //   * online softmax in the log2 domain with the rocMLIR PR #2371 guards: a
 //     running max of -inf is replaced by 0 before exp2 (so -inf - (-inf)
 //     never appears), and a row whose sum is 0 stores 0 / lse -inf.
+// The unit body is one device function; the uniform kernel gives it the units
+// of a batch with one query count, and the variable-length kernel (below) the
+// decode units and 64-row tiles of a batch whose sequences differ in it.
 #include "mma_common.cuh"
 
 namespace pa {
@@ -344,7 +347,6 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
 }
 
 // ------------------------------------------------------------------------ host side
-int mma_stages(int head_dim) { return head_dim == 128 ? 3 : 4; }
 
 size_t mma_smem_bytes(int head_dim, int stages) {
     return (size_t)stages * 2 * kMmaTileKeys * head_dim * 2 + 1024;

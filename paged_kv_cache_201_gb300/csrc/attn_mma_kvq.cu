@@ -65,15 +65,8 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t four, uint32_t &lo, uin
         : "r"(four));
 }
 
-// An f16 pair holding E4M3 values -> the same values as a bf16 pair (exact: 4 significant bits).
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-    const __nv_bfloat162 v = __floats2bfloat162_rn(f.x, f.y);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-
 // Widen keys [kw0, kw0 + 16) of one E4M3 stage (rows of D bytes, as the TMA left them) into
-// 16-bit rows at `wide` (bf16 when TO_BF16, else f16).  Keys at or past key_end (relative to the
+// f16 rows at `wide`.  Keys at or past key_end (relative to the
 // stage) become zero rows: they hold whatever the ring held before, and a zero V row keeps
 // 0 x NaN out of the output.
 // Shared address of 16-byte chunk c of key row k in an E4M3 ring stage: rows of D bytes; for
@@ -91,7 +84,7 @@ __device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t (&w)[4]) {
                  : "memory");
 }
 
-template <int D, bool TO_BF16>
+template <int D>
 __device__ __forceinline__ void widen_keys(uint32_t ring, uint32_t wide, int kw0, int key_end, int lane) {
     constexpr int C8 = D / 16;  // 16-byte E4M3 chunks per row
 #pragma unroll
@@ -107,10 +100,6 @@ __device__ __forceinline__ void widen_keys(uint32_t ring, uint32_t wide, int kw0
             e4m3x4_to_f16x4(x[1], w[2], w[3]);
             e4m3x4_to_f16x4(x[2], w[4], w[5]);
             e4m3x4_to_f16x4(x[3], w[6], w[7]);
-            if (TO_BF16) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = f16x2_to_bf16x2(w[i]);
-            }
         } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) w[i] = 0u;
@@ -753,7 +742,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
             const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
-        if (!bad) widen_keys<D, false>(vring, wideV, kw0, k_hi - tile_k0, lane);
+        if (!bad) widen_keys<D>(vring, wideV, kw0, k_hi - tile_k0, lane);
         named_bar_sync(1, kMmaConsumerWarps * 32);  // the stage's V rows are complete
 
 #pragma unroll

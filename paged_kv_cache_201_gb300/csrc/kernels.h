@@ -17,8 +17,7 @@ constexpr int kMmaThreads = (kMmaConsumerWarps + 1) * 32;
 constexpr int kDecodeRows = 16;       // query rows of one decode CTA (one m16 tile)
 constexpr int kPrefillRows = 64;      // query rows of one prefill CTA (4 warps x 16)
 
-// Pipeline depth and the matching dynamic shared-memory size.
-int mma_stages(int head_dim);
+// Dynamic shared memory of the tensor-core kernel for a pipeline depth.
 size_t mma_smem_bytes(int head_dim, int stages);
 
 cudaError_t launch_mma(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
