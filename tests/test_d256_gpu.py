@@ -82,3 +82,19 @@ def test_d256_bad_page_reads_zero(pa):
     ref = oracle.workload_rows(wl, split_kv=1, row_bih=rows)
     _gpu.assert_close(res["out"][1, 0], ref["out"], "bf16", "sequence 1")
     assert np.isfinite(res["out"][0]).all()
+
+
+def test_d256_decode_full(pa):
+    """The benchmarked head-dim-256 decode (B=128, L=4096, Hq=16, Hkv=8, 2 x 2 GiB pools drawn on the
+    device) in its bench launch (split 1) on sampled sequences, every head."""
+    wl = W.d256_decode()
+    dw = _gpu.DeviceWorkload(wl)
+    k, v = dw.host_pools()
+    res = _gpu.run(dw, 1)
+    assert not np.isnan(res["out"]).any() and np.isfinite(res["lse"]).all()
+    seqs = [0, 1, 63, 64, 100, 127]
+    b, h = np.meshgrid(np.asarray(seqs), np.arange(wl.Hq), indexing="ij")
+    rows = np.stack([b.ravel(), np.zeros(b.size, dtype=np.int64), h.ravel()], axis=1).astype(np.int32)
+    ref = oracle.workload_rows(wl, split_kv=1, row_bih=rows, k_cache=k, v_cache=v)
+    _gpu.compare_rows(res, ref, rows, wl, 1, "d256 full")
+    assert pa.paged_attn_last_error_word() == 0

@@ -68,3 +68,19 @@ def test_single_row_bad_page(pa):
     ref = oracle.workload_rows(wl, split_kv=1, row_bih=rows)
     _gpu.assert_close(res["out"][1, 0], ref["out"], "bf16", "sequence 1")
     assert np.isfinite(res["out"][0]).all()
+
+
+def test_mha_decode_full(pa):
+    """The benchmarked single-head decode (B=64, L=4096, Hq=Hkv=32, 2 x 2 GiB pools drawn on the
+    device) in its bench launch (split 1) on sampled sequences, every head."""
+    wl = W.mha_decode()
+    dw = _gpu.DeviceWorkload(wl)
+    k, v = dw.host_pools()
+    res = _gpu.run(dw, 1)
+    assert not np.isnan(res["out"]).any() and np.isfinite(res["lse"]).all()
+    seqs = [0, 1, 31, 32, 62, 63]
+    b, h = np.meshgrid(np.asarray(seqs), np.arange(wl.Hq), indexing="ij")
+    rows = np.stack([b.ravel(), np.zeros(b.size, dtype=np.int64), h.ravel()], axis=1).astype(np.int32)
+    ref = oracle.workload_rows(wl, split_kv=1, row_bih=rows, k_cache=k, v_cache=v)
+    _gpu.compare_rows(res, ref, rows, wl, 1, "mha full")
+    assert pa.paged_attn_last_error_word() == 0
