@@ -71,7 +71,8 @@ enum {
     PA_VARIANT_MMA_DECODE = 2,   /* tensor-core decode: Sq * (Hq/Hkv) <= 16 rows, keys split across warps */
     PA_VARIANT_MMA_PREFILL = 3,  /* warp-level tensor cores, 64-row query tiles (prefill / long query runs) */
     PA_VARIANT_TC05_PREFILL = 4, /* tcgen05 + tensor memory, 128-row query tiles; bf16/f16, head_dim 128,
-                                    Hq/Hkv dividing 128 */
+                                    Hq/Hkv dividing 128, scale > 0 (the planner sends scale <= 0 to
+                                    PA_VARIANT_MMA_PREFILL) */
     PA_VARIANT_MMA_T = 5         /* tensor cores, transposed products (keys and head dim as MMA rows), 8-row
                                     units; bf16/f16, head_dim 256 (the only 16-bit variant there) */
 };

@@ -135,6 +135,28 @@ int make_q_map(CUtensorMap *m, const void *q, const pa_dims *d) {
     return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
 }
 
+// 4-D view of the tcgen05 kernel's output for TMA stores: (d, query head, token, sequence) for the
+// final rows (split_kv = 1, q's element type) or (d, query head, token, split x B + sequence) for
+// the fp32 partials.  One box = one epilogue warp's 32 rows (min(G, 32) heads x max(32 / G, 1)
+// tokens) x 128 bytes of columns, 128-byte swizzled; tokens past Sq fall outside and are clipped.
+int make_tc05_out_map(CUtensorMap *m, void *out, const pa_dims *d, int split_kv) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PA_ECUDA;
+    const bool part = split_kv > 1;
+    const cuuint64_t esz = part ? 4 : 2;
+    const cuuint64_t D = (cuuint64_t)d->head_dim, Hq = (cuuint64_t)d->num_q_heads, Sq = (cuuint64_t)d->q_len;
+    const int G = d->num_q_heads / d->num_kv_heads;
+    const cuuint64_t dims[4] = {D, Hq, Sq, (cuuint64_t)d->batch * (cuuint64_t)(part ? split_kv : 1)};
+    const cuuint64_t strides[3] = {D * esz, Hq * D * esz, Sq * Hq * D * esz};
+    const cuuint32_t bh = (cuuint32_t)(G < 32 ? G : 32), bt = (cuuint32_t)(G < 32 ? 32 / G : 1);
+    const cuuint32_t box[4] = {(cuuint32_t)(128 / esz), bh, bt, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType ty = part ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : tma_dtype(d->dtype);
+    CUresult r = enc(m, ty, 4, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
+}
+
 bool tc05_supports(const pa_dims *d) {
     const int G = d->num_q_heads / d->num_kv_heads;
     return d->dtype != PA_F32 && d->head_dim == 128 && G <= 128 && (128 % G) == 0 &&
@@ -236,7 +258,11 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
     if (nrows == 0) return PA_OK;
     rc = check_fwd_pointers(q, k_cache, v_cache, block_table, seq_lens, q_offset, split_kv, out, lse);
     if (rc != PA_OK) return rc;
-    if (variant == PA_VARIANT_AUTO) variant = choose_variant(dims);
+    if (variant == PA_VARIANT_AUTO) {
+        variant = choose_variant(dims);
+        // the tcgen05 kernel takes its row maximum over unscaled scores, which needs scale > 0
+        if (variant == PA_VARIANT_TC05_PREFILL && !(scale > 0.f)) variant = PA_VARIANT_MMA_PREFILL;
+    }
     const int G = dims->num_q_heads / dims->num_kv_heads;
     const int rows = dims->q_len * G;
     switch (variant) {
@@ -252,7 +278,7 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
             if (dims->dtype == PA_F32 || dims->head_dim != 256) return PA_EUNSUPPORTED;
             break;
         case PA_VARIANT_TC05_PREFILL:
-            if (!tc05_supports(dims)) return PA_EUNSUPPORTED;
+            if (!tc05_supports(dims) || !(scale > 0.f)) return PA_EUNSUPPORTED;
             break;
         default:
             return PA_EINVAL;
@@ -282,11 +308,12 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
         if ((rc = make_pool_map(&tmv, v_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
         e = pa::launch_mma_t(p, dims->dtype, tmk, tmv, st);
     } else if (variant == PA_VARIANT_TC05_PREFILL) {
-        CUtensorMap tmq, tmk, tmv;
+        CUtensorMap tmq, tmk, tmv, tmo;
         if ((rc = make_q_map(&tmq, q, dims)) != PA_OK) return rc;
         if ((rc = make_pool_map(&tmk, k_cache, dims, 1)) != PA_OK) return rc;
         if ((rc = make_pool_map(&tmv, v_cache, dims, 1)) != PA_OK) return rc;
-        e = pa::launch_tc05(p, dims->dtype, tmq, tmk, tmv, st);
+        if ((rc = make_tc05_out_map(&tmo, out, dims, split_kv)) != PA_OK) return rc;
+        e = pa::launch_tc05(p, dims->dtype, tmq, tmk, tmv, tmo, st);
     } else {
         CUtensorMap tmk, tmv;
         if ((rc = make_pool_map(&tmk, k_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;

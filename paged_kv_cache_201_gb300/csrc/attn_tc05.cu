@@ -3,20 +3,28 @@
 // For query runs long enough to fill a 128-row tile (prefill, head_dim 128, bf16/f16).
 // A work unit = (sequence b, kv head, split s, tile of 128/G query tokens x the G query heads of
 // the kv head's group), so all 128 rows share every K/V tile.  The kernel is persistent: one CTA
-// per SM walks its units, with
-//   warps 0,10  TMA producers (0: Q and K, 10: V): each unit's Q tile (double-buffered), then per 128-key tile the
-//               block-table ids (32 pages per batch, never past the sequence's page count) and one
-//               box per page, half-row and pool into 2-slot K and V rings.
+// per SM walks its units, with four warpgroups:
+//   warps 0,2   TMA producers (0: Q and K, 2: V): each unit's Q tile (double-buffered), then per 128-key
+//               tile the block-table ids (32 pages per batch, never past the sequence's page count)
+//               and one box per page, half-row and pool into 2-slot K and V rings.
 //   warp 1      allocates all 512 TMEM columns and issues tcgen05.mma from one thread:
 //               S_g = Q K_g^T into one of two S buffers (128 fp32 columns each), then
 //               O += Ph_{g-1} V_{g-1} + Pl_{g-1} V_{g-1} with P read from TMEM into one of two O
 //               buffers (one per unit, alternating).
-//   warps 2-9   softmax, two threads per TMEM lane (query row), 64 columns each: mask (sequence
+//   warp 3      V gate: clears the V rows of a unit's last tile that lie past its last valid key
+//               (they may hold any bits, and a zero weight times NaN is NaN), then releases the slot
+//               to the P V product.
+//   warps 4-11  softmax, two threads per TMEM lane (query row), 64 columns each: mask (sequence
 //               length, split end, causal reach with q_offset), running max in the log2 domain,
 //               P = exp2(s - m) written back over S as a 16-bit high part and its rounding
 //               remainder.  O is rescaled in TMEM only when the running max grows by more than
-//               2^8 (otherwise the stale max is kept), and the -inf - (-inf) and 0/0 guards of
-//               rocMLIR PR #2371 apply.  They finish each unit by reading O out to global memory.
+//               2^8 (otherwise the stale max is kept), and the -inf - (-inf) guard of rocMLIR
+//               PR #2371 applies.  At a unit's end they hand its row maximum and sum over.
+//   warps 12-15 epilogue: one thread per query row reads the unit's O out of TMEM, divides by the
+//               row sum (0/0 guard), and stores the output row and its log-sum-exp, while the
+//               softmax warps already work on the next unit.
+// The register file is split with setmaxnreg: 64 per thread for warps 0-3, 176 for the softmax
+// warpgroups, 96 for the epilogue (128 x (64 + 2 x 176 + 96) = the 65536 of a 512 x 128 launch).
 #include <type_traits>
 
 #include "kernels.h"
@@ -26,9 +34,14 @@ namespace pa {
 
 namespace {
 
-constexpr int kT5Threads = 352;               // 11 warps
+constexpr int kT5Threads = 512;               // 16 warps, four warpgroups
+constexpr uint32_t kRegLoad = 64, kRegSoftmax = 176, kRegEpilogue = 96;  // per thread, see above
+constexpr int kT5LaunchRegs = 128;            // registers per thread the launch must hold
+static_assert(128 * (kRegLoad + 2 * kRegSoftmax + kRegEpilogue) <= kT5Threads * kT5LaunchRegs,
+              "the register split must fit the launch");
 constexpr int kT5Half = 128 * 128;            // bytes of one 64-column half of a 128-row tile
 constexpr int kT5Tile = 2 * kT5Half;          // a 128 x 128 bf16 tile (Q, K or V)
+constexpr int kT5Stage = 32 * 128;            // one epilogue warp's output staging: 32 rows x 128 bytes
 constexpr uint32_t kT5TmemCols = 512;
 constexpr uint32_t kColO = 256;               // O buffers at columns 256 and 384
 constexpr float kRescaleLog2 = 8.f;           // rescale O only when the max grows by > 2^8
@@ -37,43 +50,30 @@ constexpr int kT5StageLens = 1024;            // batches up to this size keep se
 // barrier slots (pairs are indexed by buffer / ring slot)
 //   QF/QE  Q buffer full (TMA) / empty (after the unit's last Q K^T)
 //   KF/KE, VF/VE  K and V ring slots full (TMA) / empty (after the product that reads them)
+//   VZ     V ring slot cleared past the unit's last key, where needed (32 V-gate threads arrive)
 //   SF/PF  S buffer holds Q K^T / P written back over it (256 softmax threads arrive)
 //   OD     once per P V product; a parity wait on it is exact only while it is at most one
 //          phase behind, which holds inside a unit's tile loop (Q K^T of tile g done implies
 //          P V of tile g-2 done) but not after it, hence
 //   OF     once per use of an O buffer, after the unit's last P V
-//   OFREE  O buffer read out by the softmax threads (256 arrive)
+//   OFREE  O buffer read out by the epilogue threads (128 arrive)
+//   LF/LE  a unit's row maxima and sums handed to the epilogue (256 softmax threads arrive) / read
+//          by it (128 epilogue threads arrive); indexed like the O buffers
 enum {
     B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_PF = 14, B_OF = 16, B_OFREE = 18,
-    B_OD = 20, B_COUNT = 21
+    B_OD = 20, B_VZ = 21, B_LF = 23, B_LE = 25, B_COUNT = 27
 };
 
 __device__ __forceinline__ long long t5_row_index(const FwdParams &p, int b, int kvh, int tok, int g) {
     return ((long long)b * p.Sq + tok) * p.Hq + (long long)kvh * p.G + g;
 }
 
-// Store output columns [64 hh, 64 hh + 64) of one row (and, from half 0, its lse).
-template <typename T>
-__device__ __forceinline__ void t5_store_half_row(const FwdParams &p, int s, long long ridx, int hh, const float *v,
-                                                  float lse) {
+// The log-sum-exp of one row: the final one (split_kv = 1, if wanted) or split s's.
+__device__ __forceinline__ void t5_store_lse(const FwdParams &p, int s, long long ridx, float lse) {
     if (p.split_kv == 1) {
-        T *o = reinterpret_cast<T *>(p.out) + ridx * 128 + 64 * hh;
-#pragma unroll
-        for (int c = 0; c < 64; c += 8) {
-            uint4 w;
-            w.x = MmaOp<T>::pack(v[c + 0], v[c + 1]);
-            w.y = MmaOp<T>::pack(v[c + 2], v[c + 3]);
-            w.z = MmaOp<T>::pack(v[c + 4], v[c + 5]);
-            w.w = MmaOp<T>::pack(v[c + 6], v[c + 7]);
-            *reinterpret_cast<uint4 *>(o + c) = w;
-        }
-        if (p.lse && hh == 0) p.lse[ridx] = lse;
+        if (p.lse) p.lse[ridx] = lse;
     } else {
-        const long long rows_total = (long long)p.B * p.Sq * p.Hq;
-        float *o = reinterpret_cast<float *>(p.out) + ((long long)s * rows_total + ridx) * 128 + 64 * hh;
-#pragma unroll
-        for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4 *>(o + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
-        if (hh == 0) p.lse[(long long)s * rows_total + ridx] = lse;
+        p.lse[(long long)s * ((long long)p.B * p.Sq * p.Hq) + ridx] = lse;
     }
 }
 
@@ -84,38 +84,23 @@ __device__ __forceinline__ void t5_store_half_row(const FwdParams &p, int s, lon
 template <typename T>
 __host__ __device__ constexpr bool t5_split_p() { return !std::is_same<T, __half>::value; }
 
-// P for 32 keys of one row: p = exp2(s * c2 + nmu) for the nv (may be <= 0 or >= 32) valid keys, 0
-// for the rest; l accumulates the p; the 32 columns at `taddr` receive [16 columns of high parts |
-// 16 columns of remainders] (bf16/f16 pairs; the remainders only when t5_split_p<T>()).
+// P for 32 keys of one row: p = exp2(s * c2 + nmu), where the caller has set the scores of masked
+// keys to -inf (c2 > 0, so their p is exactly 0: one code path for every tile keeps the loop small
+// in the instruction cache); l accumulates the p; the 32 columns at `taddr` receive [16 columns of
+// high parts | 16 columns of remainders] (bf16/f16 pairs; the remainders only when t5_split_p<T>()).
 template <typename T>
-__device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], int nv, float c2, float nmu, float &l,
-                                             uint32_t taddr) {
+__device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], float c2, float nmu, float &l, uint32_t taddr) {
     uint32_t hi[16], lo[16];
     float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
-    if (nv >= 32) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * i]), c2, nmu));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu));
-            l4[i & 3] += p0 + p1;
-            hi[i] = MmaOp<T>::pack(p0, p1);
-            if (t5_split_p<T>()) {
-                const float2 h2 = MmaOp<T>::unpack(hi[i]);
-                lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float a0 = (2 * i < nv) ? fmaf(__uint_as_float(u[2 * i]), c2, nmu) : kNegInf;
-            const float a1 = (2 * i + 1 < nv) ? fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu) : kNegInf;
-            const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
-            l4[i & 3] += p0 + p1;
-            hi[i] = MmaOp<T>::pack(p0, p1);
-            if (t5_split_p<T>()) {
-                const float2 h2 = MmaOp<T>::unpack(hi[i]);
-                lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
-            }
+    for (int i = 0; i < 16; ++i) {
+        const float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * i]), c2, nmu));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu));
+        l4[i & 3] += p0 + p1;
+        hi[i] = MmaOp<T>::pack(p0, p1);
+        if (t5_split_p<T>()) {
+            const float2 h2 = MmaOp<T>::unpack(hi[i]);
+            lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
         }
     }
     l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
@@ -142,18 +127,54 @@ __device__ __forceinline__ int t5_key_limit(const FwdParams &p, const T5Lens &ln
     return (int)(reach < L ? reach : L);
 }
 
-__device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, const T5Lens &ln, int unit, int tpt, int ps_shift) {
+// A unit's place in the order unit = ((b * split_kv + s) * Hkv + kvh) * row_tiles + rt.  Every role
+// walks its CTA's units c, c + gridDim.x, ... by adding gridDim.x's own digits with one carry per
+// digit (no division per unit: the per-unit code stays small, so it does not push the softmax's
+// loop out of the instruction cache).
+struct T5Pos {
+    int rt, kvh, s, b;
+};
+
+__device__ __forceinline__ T5Pos t5_pos(const FwdParams &p, int unit) {
+    T5Pos u;
+    u.rt = unit % p.row_tiles;
+    unit /= p.row_tiles;
+    u.kvh = unit % p.Hkv;
+    unit /= p.Hkv;
+    u.s = unit % p.split_kv;
+    u.b = unit / p.split_kv;
+    return u;
+}
+
+// u += d, for d's digits each below its radix; u.b >= p.B past the last unit.
+__device__ __forceinline__ void t5_advance(const FwdParams &p, T5Pos &u, const T5Pos &d) {
+    u.rt += d.rt;
+    int c = u.rt >= p.row_tiles;
+    if (c) u.rt -= p.row_tiles;
+    u.kvh += d.kvh + c;
+    c = u.kvh >= p.Hkv;
+    if (c) u.kvh -= p.Hkv;
+    u.s += d.s + c;
+    c = u.s >= p.split_kv;
+    if (c) u.s -= p.split_kv;
+    u.b += d.b + c;
+}
+
+__device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, const T5Lens &ln, const T5Pos &q, int tpt,
+                                          int ps_shift) {
     T5Unit U;
     const int ps = 1 << ps_shift;
-    const int rt = unit % p.row_tiles;
-    unit /= p.row_tiles;
-    U.kvh = unit % p.Hkv;
-    unit /= p.Hkv;
-    U.s = unit % p.split_kv;
-    U.b = unit / p.split_kv;
+    const int rt = q.rt;
+    U.kvh = q.kvh;
+    U.s = q.s;
+    U.b = q.b;
     U.L = min(max(ln.seq_lens[U.b], 0), p.W * ps);
-    int pg1;
-    split_pages(U.L, ps, p.split_kv, U.s, U.pg0, pg1);
+    // the split plan of split_pages, with the page count by shift
+    const int nblk = (U.L + ps - 1) >> ps_shift;
+    const int per = (nblk + p.split_kv - 1) / p.split_kv;
+    const long long a = (long long)U.s * per, e = (long long)(U.s + 1) * per;
+    U.pg0 = (int)(a < nblk ? a : nblk);
+    const int pg1 = (int)(e < nblk ? e : nblk);
     U.k_lo = U.pg0 * ps;
     U.k_hi_split = min(pg1 * ps, U.L);
     U.tok0 = rt * tpt;
@@ -165,18 +186,19 @@ __device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, const T5Lens &ln, 
 
 // Persistent: CTA c processes units c, c + gridDim.x, ...  Barrier phases and the K / V rings run
 // on the CTA's global tile counter g; Q and O are double-buffered by the CTA's count of non-empty
-// units n, so a unit's epilogue and the next unit's loads overlap its neighbours' work.
+// units n, so a unit's read-out and the next unit's loads overlap its neighbours' work.
 template <typename T>
 __global__ void __launch_bounds__(kT5Threads, 1)
     paged_attn_tc05_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                           const __grid_constant__ CUtensorMap tmV, const FwdParams p, int tpt, int ps_shift,
-                           uint32_t idesc_qk, uint32_t idesc_pv, int total_units) {
+                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                           const FwdParams p, int tpt, int ps_shift,
+                           uint32_t idesc_qk, uint32_t idesc_pv) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[B_COUNT];
     __shared__ uint32_t s_tmem;
     __shared__ float s_xmax[2][2][128];   // [tile parity][column half][row]: partial row maxima
-    __shared__ float s_xsum[2][128];      // [column half][row]: partial row sums
-    __shared__ int s_xbad[2][128];
+    __shared__ float s_lsum[2][2][128];   // [O buffer][column half][row]: a unit's partial row sums
+    __shared__ float s_lmax[2][128];      // [O buffer][row]: a unit's running row maximum (log2 domain)
     __shared__ int32_t s_seqlen[kT5StageLens], s_qoff[kT5StageLens];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -212,7 +234,10 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_init(bar(B_SF + i), 1);
             mbar_init(bar(B_PF + i), 256);
             mbar_init(bar(B_OF + i), 1);
-            mbar_init(bar(B_OFREE + i), 256);
+            mbar_init(bar(B_OFREE + i), 128);
+            mbar_init(bar(B_VZ + i), 32);
+            mbar_init(bar(B_LF + i), 256);
+            mbar_init(bar(B_LE + i), 128);
         }
         mbar_init(bar(B_OD), 1);
         fence_barrier_init();
@@ -225,237 +250,233 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     __syncthreads();
     tc05::fence_after_sync();
     const uint32_t tmem = s_tmem;
+    const int wg = warp >> 2;
+    const T5Pos step = t5_pos(p, gridDim.x);  // gridDim.x <= the unit count, so b < B here
 
-    if (warp == 0 || warp == 10) {
-        // ================================================================ TMA producers
-        // warp 0 loads Q and K, warp 10 loads V: the two rings free at different times (K after
-        // Q K^T, V after P V), so one must not wait behind the other.
-        const bool kq = warp == 0;
-        if (lane == 0) {
-            if (kq) {
-                tma_prefetch_desc(&tmQ);
-                tma_prefetch_desc(&tmK);
-            } else {
-                tma_prefetch_desc(&tmV);
-            }
-        }
-        const int ppt = 128 >> ps_shift;                     // pages per tile (divides 32)
-        const uint32_t box = (uint32_t)ps * 128u;            // bytes of one page half-row box
-        bool bad = false;
-        int n = 0, g0 = 0;                                   // non-empty units so far, global tile base
-        // The first id batch of the next non-empty unit is loaded one unit ahead, so its latency
-        // hides behind the current unit's copies.
-        auto next_unit = [&](int from) {
-            int u = from;
-            while (u < total_units && t5_unit(p, ln, u, tpt, ps_shift).n_tiles == 0) u += gridDim.x;
-            return u;
-        };
-        auto first_ids = [&](int u) {
-            if (u >= total_units) return 0;
-            const T5Unit V = t5_unit(p, ln, u, tpt, ps_shift);
-            const int pe = (V.k_hi + ps - 1) >> ps_shift;
-            return (V.pg0 + lane < pe) ? __ldg(p.block_table + (long long)V.b * p.W + V.pg0 + lane) : 0;
-        };
-        int unit = next_unit(blockIdx.x);
-        int ids_pref = first_ids(unit);
-        for (; unit < total_units && !bad;) {
-            const T5Unit U = t5_unit(p, ln, unit, tpt, ps_shift);
-            const int unit_next = next_unit(unit + gridDim.x);
-            const int ids_now = ids_pref;
-            ids_pref = first_ids(unit_next);
-            const int qb = n & 1;
-            if (kq && n >= 2) {  // Q buffer free once every Q K^T of unit n-2 is done
-                const bool ok = mbar_wait(bar(B_QE + qb), ((n >> 1) - 1) & 1, p.err);
-                bad = __any_sync(0xffffffffu, !ok);
-                if (bad) break;
-            }
-            if (kq && lane == 0) {
-                mbar_arrive_expect_tx(bar(B_QF + qb), (uint32_t)kT5Tile);
-                const int qtok = U.b * p.Sq + U.tok0;
-                tma_load_4d(sQ(qb), &tmQ, bar(B_QF + qb), 0, 0, U.kvh * p.G, qtok);
-                tma_load_4d(sQ(qb) + kT5Half, &tmQ, bar(B_QF + qb), 0, 1, U.kvh * p.G, qtok);
-            }
-            const int pg_end = (U.k_hi + ps - 1) >> ps_shift;
-            const int32_t *bt_row = p.block_table + (long long)U.b * p.W;
-            int batch = U.pg0;
-            int id_cur = ids_now;
-            int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
-            for (int t = 0; t < U.n_tiles; ++t) {
-                const int g = g0 + t, slot = g & 1;
-                const int pg_first = U.pg0 + t * ppt;
-                if (pg_first >= batch + 32) {
-                    batch += 32;
-                    id_cur = id_next;
-                    const int nx = batch + 32 + lane;
-                    id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
+    if (wg == 0) {
+        tc05::setmaxnreg_dec<kRegLoad>();
+        if (warp == 0 || warp == 2) {
+            // ================================================================ TMA producers
+            // warp 0 loads Q and K, warp 2 loads V: the two rings free at different times (K after
+            // Q K^T, V after P V), so one must not wait behind the other.
+            const bool kq = warp == 0;
+            if (lane == 0) {
+                if (kq) {
+                    tma_prefetch_desc(&tmQ);
+                    tma_prefetch_desc(&tmK);
+                } else {
+                    tma_prefetch_desc(&tmV);
                 }
-                const int id = __shfl_sync(0xffffffffu, id_cur, (pg_first + lane - batch) & 31);
-                const int nvalid = min(ppt, pg_end - pg_first);
-                int tok = 0;
-                if (lane < nvalid) {
-                    if (id < 0 || (long long)id >= p.num_pages) {
-                        atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
-                        tok = -ps;  // wholly outside the tensor: reads as zeros
-                    } else {
-                        tok = id << ps_shift;
-                    }
+            }
+            const int ppt = 128 >> ps_shift;                     // pages per tile (divides 32)
+            const uint32_t box = (uint32_t)ps * 128u;            // bytes of one page half-row box
+            bool bad = false;
+            int n = 0, g0 = 0;                                   // non-empty units so far, global tile base
+            // The first id batch of the next non-empty unit is loaded one unit ahead, so its latency
+            // hides behind the current unit's copies.
+            // the first unit with key tiles at or after position q (q.b >= p.B: none), into V
+            auto next_unit = [&](T5Pos q, T5Unit &V) {
+                for (; q.b < p.B; t5_advance(p, q, step)) {
+                    V = t5_unit(p, ln, q, tpt, ps_shift);
+                    if (V.n_tiles > 0) break;
                 }
-                // K slot free once Q K^T of tile g-2 is done; V slot once P V of tile g-2 is done
-                const int b_empty = kq ? B_KE : B_VE, b_full = kq ? B_KF : B_VF;
-                if (g >= 2) {
-                    const bool ok = mbar_wait(bar(b_empty + slot), ((g >> 1) - 1) & 1, p.err);
+                return q;
+            };
+            auto first_ids = [&](const T5Pos &q, const T5Unit &V) {
+                if (q.b >= p.B) return 0;
+                const int pe = (V.k_hi + ps - 1) >> ps_shift;
+                return (V.pg0 + lane < pe) ? __ldg(p.block_table + (long long)V.b * p.W + V.pg0 + lane) : 0;
+            };
+            T5Unit Un{};
+            T5Pos pos = next_unit(t5_pos(p, blockIdx.x), Un);
+            int ids_pref = first_ids(pos, Un);
+            while (pos.b < p.B && !bad) {
+                const T5Unit U = Un;
+                T5Pos nxt = pos;
+                t5_advance(p, nxt, step);
+                nxt = next_unit(nxt, Un);
+                const int ids_now = ids_pref;
+                ids_pref = first_ids(nxt, Un);
+                const int qb = n & 1;
+                if (kq && n >= 2) {  // Q buffer free once every Q K^T of unit n-2 is done
+                    const bool ok = mbar_wait(bar(B_QE + qb), ((n >> 1) - 1) & 1, p.err);
                     bad = __any_sync(0xffffffffu, !ok);
                     if (bad) break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(bar(b_full + slot), (uint32_t)nvalid * 2u * box);
-                __syncwarp();
-                if (lane < nvalid) {
-                    const uint32_t dst = (kq ? sK(slot) : sV(slot)) + (uint32_t)lane * box;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_4d(dst + (uint32_t)h * kT5Half, kq ? &tmK : &tmV, bar(b_full + slot), 0, tok, h,
-                                    U.kvh);
+                if (kq && lane == 0) {
+                    mbar_arrive_expect_tx(bar(B_QF + qb), (uint32_t)kT5Tile);
+                    const int qtok = U.b * p.Sq + U.tok0;
+                    tma_load_4d(sQ(qb), &tmQ, bar(B_QF + qb), 0, 0, U.kvh * p.G, qtok);
+                    tma_load_4d(sQ(qb) + kT5Half, &tmQ, bar(B_QF + qb), 0, 1, U.kvh * p.G, qtok);
                 }
-            }
-            g0 += U.n_tiles;
-            ++n;
-            unit = unit_next;
-        }
-        // No copy may outlive the CTA: wait (bounded) for the last phase armed on every slot.  After a
-        // time-out some of these were never armed; their waits then give up too.
-        if (!bad) {
-            for (int g = max(0, g0 - 2); g < g0; ++g) mbar_wait(bar((kq ? B_KF : B_VF) + (g & 1)), (g >> 1) & 1, p.err);
-            if (kq)
-                for (int k = max(0, n - 2); k < n; ++k) mbar_wait(bar(B_QF + (k & 1)), (k >> 1) & 1, p.err);
-        }
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
-        if (lane == 0) {
-            bool bad = false;
-            // P V of tile g is issued after Q K^T of tile g+1 (which may belong to the next unit)
-            bool pend = false;
-            int pg = 0, pn = 0;
-            bool pfirst = false, plast = false;
-            auto issue_pv = [&](int g, int un, bool first, bool last) -> bool {
-                const int slot = g & 1, ob = un & 1;
-                if (!mbar_wait(bar(B_PF + slot), (g >> 1) & 1, p.err)) return false;
-                if (!mbar_wait(bar(B_VF + slot), (g >> 1) & 1, p.err)) return false;
-                if (first && un >= 2 && !mbar_wait(bar(B_OFREE + ob), ((un >> 1) - 1) & 1, p.err)) return false;
-                tc05::fence_after_sync();
-                const uint32_t pcol = tmem + (slot ? 128u : 0u);
-                const uint32_t ocol = tmem + kColO + 128u * (uint32_t)ob;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t vd = tc05::smem_desc_sw128(sV(slot) + (uint32_t)kk * 2048u, (uint32_t)kT5Half, 1024);
-                    // keys 16kk..16kk+15: chunk kk/2 of 32 keys; highs at +0, remainders at +16
-                    const uint32_t pa = pcol + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
-                    tc05::mma_ts(ocol, pa, vd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                    if (t5_split_p<T>()) tc05::mma_ts(ocol, pa + 16u, vd, idesc_pv, 1u);
-                }
-                tc05::commit(bar(B_VE + slot));
-                tc05::commit(bar(B_OD));
-                if (last) tc05::commit(bar(B_OF + ob));
-                return true;
-            };
-            int n = 0, g0 = 0;
-            for (int unit = blockIdx.x; unit < total_units && !bad; unit += gridDim.x) {
-                const T5Unit U = t5_unit(p, ln, unit, tpt, ps_shift);
-                if (U.n_tiles == 0) continue;
-                const int qb = n & 1;
-                if (!mbar_wait(bar(B_QF + qb), (n >> 1) & 1, p.err)) { bad = true; break; }
+                const int pg_end = (U.k_hi + ps - 1) >> ps_shift;
+                const int32_t *bt_row = p.block_table + (long long)U.b * p.W;
+                int batch = U.pg0;
+                int id_cur = ids_now;
+                int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
                 for (int t = 0; t < U.n_tiles; ++t) {
                     const int g = g0 + t, slot = g & 1;
-                    if (!mbar_wait(bar(B_KF + slot), (g >> 1) & 1, p.err)) { bad = true; break; }
-                    tc05::fence_after_sync();
-                    const uint32_t d = tmem + (slot ? 128u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (uint32_t)(kk >> 2) * kT5Half + (uint32_t)(kk & 3) * 32u;
-                        tc05::mma_ss(d, tc05::smem_desc_sw128(sQ(qb) + off, 16, 1024),
-                                     tc05::smem_desc_sw128(sK(slot) + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    const int pg_first = U.pg0 + t * ppt;
+                    if (pg_first >= batch + 32) {
+                        batch += 32;
+                        id_cur = id_next;
+                        const int nx = batch + 32 + lane;
+                        id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
                     }
-                    tc05::commit(bar(B_KE + slot));   // K slot reusable once this product is done
-                    tc05::commit(bar(B_SF + slot));
-                    if (t == U.n_tiles - 1) tc05::commit(bar(B_QE + qb));
-                    if (pend && !issue_pv(pg, pn, pfirst, plast)) { bad = true; break; }
-                    pend = true;
-                    pg = g;
-                    pn = n;
-                    pfirst = t == 0;
-                    plast = t == U.n_tiles - 1;
+                    const int id = __shfl_sync(0xffffffffu, id_cur, (pg_first + lane - batch) & 31);
+                    const int nvalid = min(ppt, pg_end - pg_first);
+                    int tok = 0;
+                    if (lane < nvalid) {
+                        if (id < 0 || (long long)id >= p.num_pages) {
+                            atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
+                            tok = -ps;  // wholly outside the tensor: reads as zeros
+                        } else {
+                            tok = id << ps_shift;
+                        }
+                    }
+                    // K slot free once Q K^T of tile g-2 is done; V slot once P V of tile g-2 is done
+                    const int b_empty = kq ? B_KE : B_VE, b_full = kq ? B_KF : B_VF;
+                    if (g >= 2) {
+                        const bool ok = mbar_wait(bar(b_empty + slot), ((g >> 1) - 1) & 1, p.err);
+                        bad = __any_sync(0xffffffffu, !ok);
+                        if (bad) break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(bar(b_full + slot), (uint32_t)nvalid * 2u * box);
+                    __syncwarp();
+                    if (lane < nvalid) {
+                        const uint32_t dst = (kq ? sK(slot) : sV(slot)) + (uint32_t)lane * box;
+    #pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_4d(dst + (uint32_t)h * kT5Half, kq ? &tmK : &tmV, bar(b_full + slot), 0, tok, h,
+                                        U.kvh);
+                    }
                 }
                 g0 += U.n_tiles;
                 ++n;
+                pos = nxt;
             }
-            if (!bad && pend) issue_pv(pg, pn, pfirst, plast);
+            // No copy may outlive the CTA: wait (bounded) for the last phase armed on every slot.  After a
+            // time-out some of these were never armed; their waits then give up too.
+            if (!bad) {
+                for (int g = max(0, g0 - 2); g < g0; ++g)
+                    mbar_wait(bar((kq ? B_KF : B_VF) + (g & 1)), (g >> 1) & 1, p.err);
+                if (kq)
+                    for (int k = max(0, n - 2); k < n; ++k) mbar_wait(bar(B_QF + (k & 1)), (k >> 1) & 1, p.err);
+            }
+        } else if (warp == 1) {
+            // ================================================================ MMA issuer
+            if (lane == 0) {
+                bool bad = false;
+                // P V of tile g is issued after Q K^T of tile g+1 (which may belong to the next unit)
+                bool pend = false;
+                int pg = 0, pn = 0;
+                bool pfirst = false, plast = false;
+                auto issue_pv = [&](int g, int un, bool first, bool last) -> bool {
+                    const int slot = g & 1, ob = un & 1;
+                    if (!mbar_wait(bar(B_PF + slot), (g >> 1) & 1, p.err)) return false;
+                    if (!mbar_wait(bar(B_VZ + slot), (g >> 1) & 1, p.err)) return false;
+                    if (first && un >= 2 && !mbar_wait(bar(B_OFREE + ob), ((un >> 1) - 1) & 1, p.err)) return false;
+                    tc05::fence_after_sync();
+                    const uint32_t pcol = tmem + (slot ? 128u : 0u);
+                    const uint32_t ocol = tmem + kColO + 128u * (uint32_t)ob;
+    #pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t vd =
+                            tc05::smem_desc_sw128(sV(slot) + (uint32_t)kk * 2048u, (uint32_t)kT5Half, 1024);
+                        // keys 16kk..16kk+15: chunk kk/2 of 32 keys; highs at +0, remainders at +16
+                        const uint32_t pa = pcol + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
+                        tc05::mma_ts(ocol, pa, vd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                        if (t5_split_p<T>()) tc05::mma_ts(ocol, pa + 16u, vd, idesc_pv, 1u);
+                    }
+                    tc05::commit(bar(B_VE + slot));
+                    tc05::commit(bar(B_OD));
+                    if (last) tc05::commit(bar(B_OF + ob));
+                    return true;
+                };
+                int n = 0, g0 = 0;
+                for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < p.B && !bad; t5_advance(p, pos, step)) {
+                    const T5Unit U = t5_unit(p, ln, pos, tpt, ps_shift);
+                    if (U.n_tiles == 0) continue;
+                    const int qb = n & 1;
+                    if (!mbar_wait(bar(B_QF + qb), (n >> 1) & 1, p.err)) { bad = true; break; }
+                    for (int t = 0; t < U.n_tiles; ++t) {
+                        const int g = g0 + t, slot = g & 1;
+                        if (!mbar_wait(bar(B_KF + slot), (g >> 1) & 1, p.err)) { bad = true; break; }
+                        tc05::fence_after_sync();
+                        const uint32_t d = tmem + (slot ? 128u : 0u);
+    #pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (uint32_t)(kk >> 2) * kT5Half + (uint32_t)(kk & 3) * 32u;
+                            tc05::mma_ss(d, tc05::smem_desc_sw128(sQ(qb) + off, 16, 1024),
+                                         tc05::smem_desc_sw128(sK(slot) + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        tc05::commit(bar(B_KE + slot));   // K slot reusable once this product is done
+                        tc05::commit(bar(B_SF + slot));
+                        if (t == U.n_tiles - 1) tc05::commit(bar(B_QE + qb));
+                        if (pend && !issue_pv(pg, pn, pfirst, plast)) { bad = true; break; }
+                        pend = true;
+                        pg = g;
+                        pn = n;
+                        pfirst = t == 0;
+                        plast = t == U.n_tiles - 1;
+                    }
+                    g0 += U.n_tiles;
+                    ++n;
+                }
+                if (!bad && pend) issue_pv(pg, pn, pfirst, plast);
+            }
+            __syncwarp();
+        } else if (warp == 3) {
+            // ================================================================ V gate
+            // Keys at or past the unit's k_hi (past the sequence, past the split, past every row's causal
+            // reach, or never loaded) sit in the V rows of the unit's last tile with any bits: their
+            // weight is 0, but 0 * NaN is NaN, so those rows are cleared before P V reads the slot.
+            // Every tile passes through here (the P V product waits on VZ, not VF), so the phases
+            // stay in step with the ring.
+            bool bad = false;
+            int g0 = 0;
+            for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < p.B; t5_advance(p, pos, step)) {
+                const T5Unit U = t5_unit(p, ln, pos, tpt, ps_shift);
+                for (int t = 0; t < U.n_tiles; ++t) {
+                    const int g = g0 + t, st = g & 1;
+                    if (!bad) {
+                        const bool ok = mbar_wait(bar(B_VF + st), (g >> 1) & 1, p.err);
+                        bad = __any_sync(0xffffffffu, !ok);
+                    }
+                    const int z0 = U.k_hi - (U.k_lo + t * 128);  // first row to clear (< 128 on the last tile only)
+                    if (!bad && z0 < 128) {
+                        // (128 - z0) rows x 2 halves x 8 16-byte chunks; a quarter warp covers one 128-byte row half
+                        for (int i = lane; i < (128 - z0) * 16; i += 32) {
+                            const uint32_t a = sV(st) + (uint32_t)((i >> 3) & 1) * kT5Half +
+                                               (uint32_t)(z0 + (i >> 4)) * 128u + 16u * (uint32_t)(i & 7);
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    mbar_arrive(bar(B_VZ + st));
+                }
+                g0 += U.n_tiles;
+            }
         }
-        __syncwarp();
-    } else {
-        // ================================================================ softmax (warps 2-9)
-        // Two warpgroups share every row: group hh (warps 2-5: hh = 0, warps 6-9: hh = 1) owns
-        // score columns / keys [64 hh, 64 hh + 64) and output columns [64 hh, 64 hh + 64).  They
-        // exchange the row maximum once per tile and the row sum once per unit; both keep the same
-        // running maximum, so the rescale decisions agree.  Every named barrier is reached on every
-        // path (a warp that gave up on a wait still walks the loops), so none can hang.
-        const int hh = (warp - 2) >> 2;
+    } else if (wg == 1 || wg == 2) {
+        tc05::setmaxnreg_inc<kRegSoftmax>();
+        // ================================================================ softmax (warps 4-11)
+        // Two warpgroups share every row: group hh (warps 4-7: hh = 0, warps 8-11: hh = 1) owns
+        // score columns / keys [64 hh, 64 hh + 64).  They exchange the row maximum once per tile;
+        // both keep the same running maximum, so the rescale decisions agree.  Every named barrier
+        // is reached on every path (a warp that gave up on a wait still walks the loops), so none
+        // can hang.
+        const int hh = wg - 1;
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;                       // TMEM lane = query row of the tile
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
         bool bad = false;
-        // A unit's read-out of O waits for its last P V, which the MMA thread issues after the next
-        // unit's first Q K^T; it is done after this thread's first tile of the next unit, so the
-        // wait overlaps useful work.  O is double-buffered, so the buffer is not needed earlier.
-        struct Pending {
-            bool valid, row_valid;
-            int s, ob, n;
-            long long ridx;
-            float l, m;
-        } pend{false, false, 0, 0, 0, 0, 0.f, kNegInf};
-        auto epilogue = [&](const Pending &e) {
-            if (!bad) {  // the unit's last P V (a dedicated barrier: exact whatever B_OD's phase)
-                const bool ok = mbar_wait(bar(B_OF + e.ob), (e.n >> 1) & 1, p.err);
-                bad = __any_sync(0xffffffffu, !ok);
-            }
-            s_xsum[hh][r] = e.l;
-            s_xbad[hh][r] = bad ? 1 : 0;
-            named_bar_sync(2, 256);
-            const float l_tot = e.l + s_xsum[hh ^ 1][r];
-            if (!bad && !s_xbad[hh ^ 1][r]) {
-                tc05::fence_after_sync();
-                const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-                const uint32_t ocol = kColO + 128u * (uint32_t)e.ob;
-                float o[64];
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t u[32];
-                    tc05::ld_32cols(tmem + lane_addr + ocol + 32u * (2 * hh + c), u);
-                    tc05::wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) o[32 * c + j] = __uint_as_float(u[j]) * inv;
-                }
-                if (e.row_valid)
-                    t5_store_half_row<T>(p, e.s, e.ridx, hh, o, l_tot > 0.f ? e.m * kLn2 + logf(l_tot) : kNegInf);
-            }
-            tc05::fence_before_sync();
-            mbar_arrive(bar(B_OFREE + e.ob));  // O buffer may take unit e.n + 2's products
-        };
         int n = 0, g0 = 0;
-        for (int unit = blockIdx.x; unit < total_units; unit += gridDim.x) {
-            const T5Unit U = t5_unit(p, ln, unit, tpt, ps_shift);
-            if (threadIdx.x == 64 && U.s == 0 && U.tok0 == 0 && p.seq_lens[U.b] > p.W * ps)
-                atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
+        for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < p.B; t5_advance(p, pos, step)) {
+            const T5Unit U = t5_unit(p, ln, pos, tpt, ps_shift);
+            if (U.n_tiles == 0) continue;  // the epilogue warps write its rows
             const int tk = U.tok0 + r / p.G;
-            const int gq = r % p.G;
             const bool row_valid = tk < U.tok_end;
-            if (U.n_tiles == 0) {  // no valid key for any row of the unit: output 0, lse -inf
-                if (row_valid) {
-                    float zeros[64];
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) zeros[c] = 0.f;
-                    t5_store_half_row<T>(p, U.s, t5_row_index(p, U.b, U.kvh, tk, gq), hh, zeros, kNegInf);
-                }
-                continue;
-            }
             const int ob = n & 1;
             const uint32_t ocol = kColO + 128u * (uint32_t)ob;
             const int lim = row_valid ? min(U.k_hi_split, t5_key_limit(p, ln, U.b, U.L, tk)) : U.k_lo;
@@ -477,22 +498,21 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     tc05::ld_32cols(sbuf + 64u * hh, ua);
                     tc05::ld_32cols(sbuf + 64u * hh + 32u, ub);
                     tc05::wait_ld();
-                    // pass 1: maximum of this row's valid raw scores (scale > 0 commutes with max)
+                    // pass 1: maximum of this row's valid raw scores (scale > 0, which the host
+                    // checks, commutes with max)
                     // four independent running maxima (max is exact, so the grouping does not matter)
                     const int nv = nvalid_row - 64 * hh;
-                    float m4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-                    if (nv >= 64) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            m4[j & 3] = fmaxf(m4[j & 3], fmaxf(__uint_as_float(ua[j]), __uint_as_float(ub[j])));
-                    } else {
+                    if (nv < 64) {  // keys past this row's limit become -inf: weight exactly 0 below
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const float a = (j < nv) ? __uint_as_float(ua[j]) : kNegInf;
-                            const float c = (j + 32 < nv) ? __uint_as_float(ub[j]) : kNegInf;
-                            m4[j & 3] = fmaxf(m4[j & 3], fmaxf(a, c));
+                            if (j >= nv) ua[j] = 0xff800000u;
+                            if (j + 32 >= nv) ub[j] = 0xff800000u;
                         }
                     }
+                    float m4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        m4[j & 3] = fmaxf(m4[j & 3], fmaxf(__uint_as_float(ua[j]), __uint_as_float(ub[j])));
                     mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 }
                 s_xmax[st][hh][r] = mx;
@@ -531,38 +551,127 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs)
                     const float nmu = (m_used == kNegInf) ? 0.f : -m_used;  // -inf - (-inf) guard
                     const float c2 = p.scale_log2;
-                    t5_exp_chunk<T>(ua, nvalid_row - 64 * hh, c2, nmu, l, sbuf + 64u * hh);
-                    t5_exp_chunk<T>(ub, nvalid_row - 64 * hh - 32, c2, nmu, l, sbuf + 64u * hh + 32u);
+                    t5_exp_chunk<T>(ua, c2, nmu, l, sbuf + 64u * hh);
+                    t5_exp_chunk<T>(ub, c2, nmu, l, sbuf + 64u * hh + 32u);
                     tc05::wait_st();
-                }
-                if (t == U.n_tiles - 1 && tile_k0 + 128 > U.k_hi) {
-                    // Keys at or past k_hi (past the sequence or never loaded) may hold any bits: their
-                    // weight is 0 but 0 * NaN is NaN, so zero those V rows (my half of each) before P V.
-                    if (!bad) {
-                        const bool ok = mbar_wait(bar(B_VF + st), (g >> 1) & 1, p.err);
-                        bad = __any_sync(0xffffffffu, !ok);
-                    }
-                    if (!bad && tile_k0 + r >= U.k_hi) {
-                        const uint32_t a = sV(st) + (uint32_t)hh * kT5Half + (uint32_t)r * 128u;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a + 16u * c), "r"(0u)
-                                         : "memory");
-                    }
-                    fence_proxy_async_smem();
                 }
                 tc05::fence_before_sync();
                 mbar_arrive(bar(B_PF + st));
-                if (t == 0 && pend.valid) {
-                    epilogue(pend);
-                    pend.valid = false;
-                }
             }
-            pend = Pending{true, row_valid, U.s, ob, n, t5_row_index(p, U.b, U.kvh, tk, gq), l, m_used};
+            // hand the row's maximum and partial sum to the epilogue (the slot of unit n-2 read first)
+            if (!bad && n >= 2) {
+                const bool ok = mbar_wait(bar(B_LE + ob), ((n >> 1) - 1) & 1, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+            }
+            s_lsum[ob][hh][r] = l;
+            if (hh == 0) s_lmax[ob][r] = m_used;
+            mbar_arrive(bar(B_LF + ob));
             g0 += U.n_tiles;
             ++n;
         }
-        if (pend.valid) epilogue(pend);
+    } else {
+        tc05::setmaxnreg_dec<kRegEpilogue>();
+        // ================================================================ epilogue (warps 12-15)
+        // One thread per query row: wait for the unit's last P V and its row statistics, read the
+        // 128 output columns out of TMEM, scale by 1 / l (0 when l = 0: a row with no valid key),
+        // and free the O buffer for unit n + 2.  The rows leave through shared memory: each warp
+        // stages its 32 rows x 128 bytes of columns (128-byte swizzle: conflict-free) and one
+        // lane stores the box with TMA, so no warp issues a store per row; tokens past Sq fall
+        // outside the tensor and are clipped.  The log-sum-exp goes out with plain stores.
+        const int q4 = warp & 3;
+        const int r = q4 * 32 + lane, r0 = q4 * 32;
+        const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+        const uint32_t stage = sbase + (uint32_t)kT5Tile * 6u + (uint32_t)q4 * (uint32_t)kT5Stage;
+        const uint32_t srow = stage + (uint32_t)lane * 128u, sw = (uint32_t)(lane & 7);
+        const bool part = p.split_kv > 1;
+        const int nch = part ? 4 : 2;  // 128-byte column chunks of a row: 32 fp32 or 64 16-bit values
+        auto put16 = [&](int j, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {  // 16-byte chunk j of my row
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(srow + 16u * ((uint32_t)j ^ sw)), "r"(a),
+                         "r"(b), "r"(c), "r"(d)
+                         : "memory");
+        };
+        auto stage_free = [&]() {  // the previous box has been read out of the staging rows
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+        };
+        auto store_box = [&](const T5Unit &U, int ch) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_4d(&tmO, stage, part ? 32 * ch : 64 * ch, U.kvh * p.G + r0 % p.G, U.tok0 + r0 / p.G,
+                             part ? U.s * p.B + U.b : U.b);
+                bulk_commit_group();
+            }
+        };
+        bool bad = false;
+        int n = 0;
+        for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < p.B; t5_advance(p, pos, step)) {
+            const T5Unit U = t5_unit(p, ln, pos, tpt, ps_shift);
+            if (threadIdx.x == 384 && U.s == 0 && U.tok0 == 0 && p.seq_lens[U.b] > p.W * ps)
+                atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
+            const int tk = U.tok0 + r / p.G;
+            const bool row_valid = tk < U.tok_end;
+            const long long ridx = row_valid ? t5_row_index(p, U.b, U.kvh, tk, r % p.G) : 0;
+            if (U.n_tiles == 0) {  // no valid key for any row of the unit: output 0, lse -inf
+                stage_free();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) put16(j, 0u, 0u, 0u, 0u);
+#pragma unroll 1
+                for (int ch = 0; ch < nch; ++ch) store_box(U, ch);
+                if (row_valid) t5_store_lse(p, U.s, ridx, kNegInf);
+                continue;
+            }
+            const int ob = n & 1;
+            if (!bad) {
+                bool ok = mbar_wait(bar(B_LF + ob), (n >> 1) & 1, p.err);
+                ok = ok && mbar_wait(bar(B_OF + ob), (n >> 1) & 1, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+            }
+            const float l_tot = s_lsum[ob][0][r] + s_lsum[ob][1][r];
+            const float m = s_lmax[ob][r];
+            mbar_arrive(bar(B_LE + ob));
+            if (!bad) {
+                tc05::fence_after_sync();
+                const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                const uint32_t ocol = tmem + lane_addr + kColO + 128u * (uint32_t)ob;
+#pragma unroll 1
+                for (int ch = 0; ch < nch; ++ch) {
+                    if (part) {
+                        uint32_t u[32];
+                        tc05::ld_32cols(ocol + 32u * (uint32_t)ch, u);
+                        stage_free();
+                        tc05::wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            put16(j, __float_as_uint(__uint_as_float(u[4 * j]) * inv),
+                                  __float_as_uint(__uint_as_float(u[4 * j + 1]) * inv),
+                                  __float_as_uint(__uint_as_float(u[4 * j + 2]) * inv),
+                                  __float_as_uint(__uint_as_float(u[4 * j + 3]) * inv));
+                    } else {
+                        stage_free();
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            uint32_t u[32];
+                            tc05::ld_32cols(ocol + 64u * (uint32_t)ch + 32u * (uint32_t)hf, u);
+                            tc05::wait_ld();
+                            auto pk = [&](int i) {
+                                return MmaOp<T>::pack(__uint_as_float(u[i]) * inv, __uint_as_float(u[i + 1]) * inv);
+                            };
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                put16(4 * hf + j, pk(8 * j), pk(8 * j + 2), pk(8 * j + 4), pk(8 * j + 6));
+                        }
+                    }
+                    store_box(U, ch);
+                }
+                if (row_valid) t5_store_lse(p, U.s, ridx, l_tot > 0.f ? m * kLn2 + logf(l_tot) : kNegInf);
+            }
+            tc05::fence_before_sync();
+            mbar_arrive(bar(B_OFREE + ob));  // O buffer may take unit n + 2's products
+            ++n;
+        }
+        if (lane == 0) bulk_wait_all();  // no store may outlive the CTA's shared memory
+        __syncwarp();
     }
 
     tc05::fence_before_sync();
@@ -574,7 +683,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 }
 
 // ------------------------------------------------------------------------ host side
-size_t tc05_smem_bytes() { return (size_t)(kT5Tile * 6 + 1024); }
+size_t tc05_smem_bytes() { return (size_t)(kT5Tile * 6 + 4 * kT5Stage + 1024); }
 
 static int num_sms_of_current_device() {
     static int cached[128];
@@ -590,11 +699,21 @@ static int num_sms_of_current_device() {
 
 template <typename T>
 static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, const CUtensorMap &tmk,
-                                 const CUtensorMap &tmv, cudaStream_t stream) {
+                                 const CUtensorMap &tmv, const CUtensorMap &tmo, cudaStream_t stream) {
     auto kern = paged_attn_tc05_kernel<T>;
     const size_t smem = tc05_smem_bytes();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    // The softmax warpgroups' setmaxnreg increase is served from what the launch holds: a build
+    // that gave the kernel fewer registers per thread would leave them waiting, so refuse it.
+    static int launch_regs = 0;
+    if (!launch_regs) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        launch_regs = fa.numRegs;
+    }
+    if (launch_regs < kT5LaunchRegs) return cudaErrorInvalidConfiguration;
     int ps_shift = 0;
     while ((1 << ps_shift) < p.ps) ++ps_shift;
     const int tpt = 128 / p.G;
@@ -609,14 +728,14 @@ static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, con
     const bool bf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t iqk = tc05::idesc_f16(bf, false, 128, 128);
     const uint32_t ipv = tc05::idesc_f16(bf, true, 128, 128);
-    kern<<<grid, kT5Threads, smem, stream>>>(tmq, tmk, tmv, q, tpt, ps_shift, iqk, ipv, (int)units);
+    kern<<<grid, kT5Threads, smem, stream>>>(tmq, tmk, tmv, tmo, q, tpt, ps_shift, iqk, ipv);
     return cudaGetLastError();
 }
 
 cudaError_t launch_tc05(const FwdParams &p, int dtype, const CUtensorMap &tmq, const CUtensorMap &tmk,
-                        const CUtensorMap &tmv, cudaStream_t stream) {
-    if (dtype == PA_BF16) return launch_tc05_t<__nv_bfloat16>(p, tmq, tmk, tmv, stream);
-    return launch_tc05_t<__half>(p, tmq, tmk, tmv, stream);
+                        const CUtensorMap &tmv, const CUtensorMap &tmo, cudaStream_t stream) {
+    if (dtype == PA_BF16) return launch_tc05_t<__nv_bfloat16>(p, tmq, tmk, tmv, tmo, stream);
+    return launch_tc05_t<__half>(p, tmq, tmk, tmv, tmo, stream);
 }
 
 }  // namespace pa

@@ -31,7 +31,7 @@ cudaError_t launch_mma_kvq(const FwdParams &p, int mode, int dtype, const CUtens
 // tcgen05 prefill: bf16/f16, head_dim 128, (Hq/Hkv) dividing 128.
 size_t tc05_smem_bytes();
 cudaError_t launch_tc05(const FwdParams &p, int dtype, const CUtensorMap &tmq, const CUtensorMap &tmk,
-                        const CUtensorMap &tmv, cudaStream_t stream);
+                        const CUtensorMap &tmv, const CUtensorMap &tmo, cudaStream_t stream);
 cudaError_t launch_simt(const FwdParams &p, int dtype, cudaStream_t stream);
 // One query row per (sequence, kv head), bf16/f16, head_dim 64/128: CUDA cores over the TMA ring.
 cudaError_t launch_simt_decode(const FwdParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,

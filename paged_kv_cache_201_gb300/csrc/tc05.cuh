@@ -101,5 +101,13 @@ __device__ __forceinline__ void st_32cols(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Per-warpgroup register budget (all four warps of the warpgroup execute the same instruction).
+// An increase draws on what the block was launched with (threads x registers per thread), so the
+// launch must hold the sum of every warpgroup's target.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+
 }  // namespace tc05
 }  // namespace pa

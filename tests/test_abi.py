@@ -80,6 +80,8 @@ def _fwd(lib, dims, split=1, scale=0.1, lse=FAKE, q=FAKE, out=FAKE, variant=0):
     (dict(head_dim=256, dtype=pa.PA_F32), 1, 0.1, dict(variant=5), EUNSUP),
     (dict(q_len=2, num_q_heads=32), 1, 0.1, dict(variant=2), EUNSUP),
     ({}, 1, 0.1, dict(variant=9), EINVAL),
+    (dict(q_len=128), 1, 0.0, dict(variant=4), EUNSUP),   # tcgen05 prefill takes scale > 0 only
+    (dict(q_len=128), 1, -0.1, dict(variant=4), EUNSUP),
     (dict(batch=0), 1, 0.1, {}, OK),
     (dict(q_len=0), 4, 0.1, dict(lse=None), OK),
     (dict(q_len=0), 4, 0.1, {}, OK),
