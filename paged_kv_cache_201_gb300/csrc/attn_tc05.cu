@@ -69,8 +69,9 @@ __device__ __forceinline__ long long t5_row_index(const FwdParams &p, int b, int
 }
 
 // The log-sum-exp of one row: the final one (split_kv = 1, if wanted) or split s's.
+template <bool PART>
 __device__ __forceinline__ void t5_store_lse(const FwdParams &p, int s, long long ridx, float lse) {
-    if (p.split_kv == 1) {
+    if constexpr (!PART) {
         if (p.lse) p.lse[ridx] = lse;
     } else {
         p.lse[(long long)s * ((long long)p.B * p.Sq * p.Hq) + ridx] = lse;
@@ -88,22 +89,55 @@ __host__ __device__ constexpr bool t5_split_p() { return !std::is_same<T, __half
 // keys to -inf (c2 > 0, so their p is exactly 0: one code path for every tile keeps the loop small
 // in the instruction cache); l accumulates the p; the 32 columns at `taddr` receive [16 columns of
 // high parts | 16 columns of remainders] (bf16/f16 pairs; the remainders only when t5_split_p<T>()).
+// Packed pairs of fp32 (the f32x2 arithmetic of sm_100-family cores: one instruction per pair,
+// each lane rounded as its scalar counterpart).
+__device__ __forceinline__ uint64_t f2_pack(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 template <typename T>
 __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], float c2, float nmu, float &l, uint32_t taddr) {
     uint32_t hi[16], lo[16];
-    float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
+    const uint64_t c2x2 = f2_pack(c2, c2), nmux2 = f2_pack(nmu, nmu);
+    uint64_t l2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};  // two pair sums: short dependency chains
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const float p0 = fast_exp2(fmaf(__uint_as_float(u[2 * i]), c2, nmu));
-        const float p1 = fast_exp2(fmaf(__uint_as_float(u[2 * i + 1]), c2, nmu));
-        l4[i & 3] += p0 + p1;
+        const uint64_t sc = f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+        const float2 x = f2_unpack(f2_fma(sc, c2x2, nmux2));
+        const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+        const uint64_t pp = f2_pack(p0, p1);
+        l2[i & 1] = f2_add(l2[i & 1], pp);
         hi[i] = MmaOp<T>::pack(p0, p1);
         if (t5_split_p<T>()) {
             const float2 h2 = MmaOp<T>::unpack(hi[i]);
-            lo[i] = MmaOp<T>::pack(p0 - h2.x, p1 - h2.y);
+            const float2 d = f2_unpack(f2_sub(pp, f2_pack(h2.x, h2.y)));
+            lo[i] = MmaOp<T>::pack(d.x, d.y);
         }
     }
-    l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+    const float2 ls = f2_unpack(f2_add(l2[0], l2[1]));
+    l += ls.x + ls.y;
     tc05::st_16cols(taddr, hi);
     if (t5_split_p<T>()) tc05::st_16cols(taddr + 16u, lo);
 }
@@ -186,13 +220,15 @@ __device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, const T5Lens &ln, 
 
 // Persistent: CTA c processes units c, c + gridDim.x, ...  Barrier phases and the K / V rings run
 // on the CTA's global tile counter g; Q and O are double-buffered by the CTA's count of non-empty
-// units n, so a unit's read-out and the next unit's loads overlap its neighbours' work.
-template <typename T>
+// units n, so a unit's read-out and the next unit's loads overlap its neighbours' work.  PART: the
+// output is split_kv > 1's fp32 partials (else the final rows in T); one store path per kernel keeps
+// the code the SM must hold small.  G = 2^g_shift (it divides 128).
+template <typename T, bool PART>
 __global__ void __launch_bounds__(kT5Threads, 1)
     paged_attn_tc05_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                           const FwdParams p, int tpt, int ps_shift,
-                           uint32_t idesc_qk, uint32_t idesc_pv) {
+                           const FwdParams p, int tpt, int ps_shift, int g_shift, uint32_t idesc_qk,
+                           uint32_t idesc_pv) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[B_COUNT];
     __shared__ uint32_t s_tmem;
@@ -475,7 +511,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < p.B; t5_advance(p, pos, step)) {
             const T5Unit U = t5_unit(p, ln, pos, tpt, ps_shift);
             if (U.n_tiles == 0) continue;  // the epilogue warps write its rows
-            const int tk = U.tok0 + r / p.G;
+            const int tk = U.tok0 + (r >> g_shift);
             const bool row_valid = tk < U.tok_end;
             const int ob = n & 1;
             const uint32_t ocol = kColO + 128u * (uint32_t)ob;
@@ -551,8 +587,15 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs)
                     const float nmu = (m_used == kNegInf) ? 0.f : -m_used;  // -inf - (-inf) guard
                     const float c2 = p.scale_log2;
-                    t5_exp_chunk<T>(ua, c2, nmu, l, sbuf + 64u * hh);
-                    t5_exp_chunk<T>(ub, c2, nmu, l, sbuf + 64u * hh + 32u);
+                    // one copy of the chunk's code, run twice (the second 32 scores moved into ua)
+#pragma unroll 1
+                    for (int c = 0; c < 2; ++c) {
+                        t5_exp_chunk<T>(ua, c2, nmu, l, sbuf + 64u * hh + 32u * (uint32_t)c);
+                        if (c == 0) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) ua[j] = ub[j];
+                        }
+                    }
                     tc05::wait_st();
                 }
                 tc05::fence_before_sync();
@@ -583,8 +626,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
         const uint32_t stage = sbase + (uint32_t)kT5Tile * 6u + (uint32_t)q4 * (uint32_t)kT5Stage;
         const uint32_t srow = stage + (uint32_t)lane * 128u, sw = (uint32_t)(lane & 7);
-        const bool part = p.split_kv > 1;
-        const int nch = part ? 4 : 2;  // 128-byte column chunks of a row: 32 fp32 or 64 16-bit values
+        constexpr int nch = PART ? 4 : 2;  // 128-byte column chunks of a row: 32 fp32 or 64 16-bit values
         auto put16 = [&](int j, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {  // 16-byte chunk j of my row
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(srow + 16u * ((uint32_t)j ^ sw)), "r"(a),
                          "r"(b), "r"(c), "r"(d)
@@ -598,8 +640,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_4d(&tmO, stage, part ? 32 * ch : 64 * ch, U.kvh * p.G + r0 % p.G, U.tok0 + r0 / p.G,
-                             part ? U.s * p.B + U.b : U.b);
+                tma_store_4d(&tmO, stage, PART ? 32 * ch : 64 * ch, U.kvh * p.G + (r0 & (p.G - 1)),
+                             U.tok0 + (r0 >> g_shift), PART ? U.s * p.B + U.b : U.b);
                 bulk_commit_group();
             }
         };
@@ -609,16 +651,16 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             const T5Unit U = t5_unit(p, ln, pos, tpt, ps_shift);
             if (threadIdx.x == 384 && U.s == 0 && U.tok0 == 0 && p.seq_lens[U.b] > p.W * ps)
                 atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
-            const int tk = U.tok0 + r / p.G;
+            const int tk = U.tok0 + (r >> g_shift);
             const bool row_valid = tk < U.tok_end;
-            const long long ridx = row_valid ? t5_row_index(p, U.b, U.kvh, tk, r % p.G) : 0;
+            const long long ridx = row_valid ? t5_row_index(p, U.b, U.kvh, tk, r & (p.G - 1)) : 0;
             if (U.n_tiles == 0) {  // no valid key for any row of the unit: output 0, lse -inf
                 stage_free();
 #pragma unroll
                 for (int j = 0; j < 8; ++j) put16(j, 0u, 0u, 0u, 0u);
 #pragma unroll 1
                 for (int ch = 0; ch < nch; ++ch) store_box(U, ch);
-                if (row_valid) t5_store_lse(p, U.s, ridx, kNegInf);
+                if (row_valid) t5_store_lse<PART>(p, U.s, ridx, kNegInf);
                 continue;
             }
             const int ob = n & 1;
@@ -636,7 +678,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 const uint32_t ocol = tmem + lane_addr + kColO + 128u * (uint32_t)ob;
 #pragma unroll 1
                 for (int ch = 0; ch < nch; ++ch) {
-                    if (part) {
+                    if constexpr (PART) {
                         uint32_t u[32];
                         tc05::ld_32cols(ocol + 32u * (uint32_t)ch, u);
                         stage_free();
@@ -664,7 +706,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     }
                     store_box(U, ch);
                 }
-                if (row_valid) t5_store_lse(p, U.s, ridx, l_tot > 0.f ? m * kLn2 + logf(l_tot) : kNegInf);
+                if (row_valid) t5_store_lse<PART>(p, U.s, ridx, l_tot > 0.f ? m * kLn2 + logf(l_tot) : kNegInf);
             }
             tc05::fence_before_sync();
             mbar_arrive(bar(B_OFREE + ob));  // O buffer may take unit n + 2's products
@@ -697,10 +739,10 @@ static int num_sms_of_current_device() {
     return cached[dev];
 }
 
-template <typename T>
+template <typename T, bool PART>
 static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, const CUtensorMap &tmk,
                                  const CUtensorMap &tmv, const CUtensorMap &tmo, cudaStream_t stream) {
-    auto kern = paged_attn_tc05_kernel<T>;
+    auto kern = paged_attn_tc05_kernel<T, PART>;
     const size_t smem = tc05_smem_bytes();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -714,9 +756,11 @@ static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, con
         launch_regs = fa.numRegs;
     }
     if (launch_regs < kT5LaunchRegs) return cudaErrorInvalidConfiguration;
-    int ps_shift = 0;
+    int ps_shift = 0, g_shift = 0;
     while ((1 << ps_shift) < p.ps) ++ps_shift;
-    const int tpt = 128 / p.G;
+    while ((1 << g_shift) < p.G) ++g_shift;
+    if ((1 << g_shift) != p.G || g_shift > 7) return cudaErrorInvalidValue;  // G must divide 128
+    const int tpt = 128 >> g_shift;
     FwdParams q = p;
     q.row_tiles = (p.Sq + tpt - 1) / tpt;
     const long long units = (long long)p.B * p.split_kv * p.Hkv * q.row_tiles;
@@ -728,14 +772,18 @@ static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, con
     const bool bf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t iqk = tc05::idesc_f16(bf, false, 128, 128);
     const uint32_t ipv = tc05::idesc_f16(bf, true, 128, 128);
-    kern<<<grid, kT5Threads, smem, stream>>>(tmq, tmk, tmv, tmo, q, tpt, ps_shift, iqk, ipv);
+    kern<<<grid, kT5Threads, smem, stream>>>(tmq, tmk, tmv, tmo, q, tpt, ps_shift, g_shift, iqk, ipv);
     return cudaGetLastError();
 }
 
 cudaError_t launch_tc05(const FwdParams &p, int dtype, const CUtensorMap &tmq, const CUtensorMap &tmk,
                         const CUtensorMap &tmv, const CUtensorMap &tmo, cudaStream_t stream) {
-    if (dtype == PA_BF16) return launch_tc05_t<__nv_bfloat16>(p, tmq, tmk, tmv, tmo, stream);
-    return launch_tc05_t<__half>(p, tmq, tmk, tmv, tmo, stream);
+    const bool part = p.split_kv > 1;
+    if (dtype == PA_BF16)
+        return part ? launch_tc05_t<__nv_bfloat16, true>(p, tmq, tmk, tmv, tmo, stream)
+                    : launch_tc05_t<__nv_bfloat16, false>(p, tmq, tmk, tmv, tmo, stream);
+    return part ? launch_tc05_t<__half, true>(p, tmq, tmk, tmv, tmo, stream)
+                : launch_tc05_t<__half, false>(p, tmq, tmk, tmv, tmo, stream);
 }
 
 }  // namespace pa
