@@ -206,15 +206,16 @@ def kernel_source_digest(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel sources."""
+def recorded_traffic(kernel: str, workload: str, split_kv: int):
+    """DRAM bytes per launch from a committed ncu summary of this kernel, workload and split_kv, if it
+    was taken on the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    ent = rec.get(f"{kernel}/{workload}")
+    ent = rec.get(f"{kernel}/{workload}/split{split_kv}")
     if not ent or ent.get("source_digest") != kernel_source_digest(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
@@ -403,11 +404,11 @@ def run_ours(args, ws, rank, local):
             tpeak, tpeak_src = FALLBACK_BF16_TFLOPS, "fallback"
         roofline = {"bound": "tensor", "kernel": kname, "achieved": round(tf_achieved, 1), "peak": tpeak,
                     "peak_source": tpeak_src, "unit": "TFLOP/s", "frac": round(tf_achieved / tpeak, 4),
-                    "kernel_ms": round(fwd_ms, 5), "traffic": recorded_traffic(kname, args.workload)}
+                    "kernel_ms": round(fwd_ms, 5), "traffic": recorded_traffic(kname, args.workload, S)}
     else:
         roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                    "kernel_ms": round(fwd_ms, 5), "traffic": recorded_traffic(kname, args.workload)}
+                    "kernel_ms": round(fwd_ms, 5), "traffic": recorded_traffic(kname, args.workload, S)}
 
     # ---- end to end through the public API: host inputs in, host result out, every step
     e2e = None
@@ -616,7 +617,7 @@ def run_varlen(args, ws, rank, local):
     roofline = {"bound": "hbm", "kernel": "paged_attn_mma_varlen_kernel", "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "kernel_ms": round(ms_local, 5), "traffic": recorded_traffic("paged_attn_mma_varlen_kernel",
-                                                                             args.workload),
+                                                                             args.workload, S),
                 "tensor_side": {"achieved_tflops": round(fl / (ms_local * 1e-3) / 1e12, 1)}}
 
     e2e = None
