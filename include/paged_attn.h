@@ -73,8 +73,13 @@ enum {
     PA_VARIANT_TC05_PREFILL = 4, /* tcgen05 + tensor memory, 128-row query tiles; bf16/f16, head_dim 128,
                                     Hq/Hkv dividing 128, scale > 0 (the planner sends scale <= 0 to
                                     PA_VARIANT_MMA_PREFILL) */
-    PA_VARIANT_MMA_T = 5         /* tensor cores, transposed products (keys and head dim as MMA rows), 8-row
+    PA_VARIANT_MMA_T = 5,        /* tensor cores, transposed products (keys and head dim as MMA rows), 8-row
                                     units; bf16/f16, head_dim 256 (the only 16-bit variant there) */
+    PA_VARIANT_MMA_SPLIT_GROUP = 6 /* tensor-core decode (Sq * (Hq/Hkv) <= 16 rows, head_dim 64/128, bf16/f16)
+                                    with short splits: a CTA per four consecutive splits, one warp per split;
+                                    every split at most 8 pages (ceil(bt_stride / split_kv) <= 8).  The
+                                    planner takes it when that holds and one CTA per split would need more
+                                    than two CTAs per multiprocessor */
 };
 
 /*

@@ -21,11 +21,12 @@ __all__ = [
     "paged_attn_workspace_bytes", "paged_attn_fwd_splitkv", "paged_attn_fwd_splitkv_noalloc", "paged_attn_fwd_kvq",
     "paged_attn_fwd_kvq_splitkv", "attention_kvq", "paged_attn_fwd_varlen", "attention_varlen", "PA_F32", "PA_F16", "PA_BF16", "PA_FP8_E4M3",
     "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL", "VARIANT_TC05_PREFILL",
-    "VARIANT_MMA_T",
+    "VARIANT_MMA_T", "VARIANT_MMA_SPLIT_GROUP",
 ]
 
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA_DECODE, VARIANT_MMA_PREFILL, VARIANT_TC05_PREFILL, VARIANT_MMA_T = 0, 1, 2, 3, 4, 5
+VARIANT_MMA_SPLIT_GROUP = 6
 ERRBIT_PAGE_RANGE, ERRBIT_TIMEOUT, ERRBIT_SEQ_CLIPPED, ERRBIT_QSTART = 1, 2, 4, 8
 
 

@@ -157,6 +157,25 @@ int make_tc05_out_map(CUtensorMap *m, void *out, const pa_dims *d, int split_kv)
     return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
 }
 
+// The split-group decode kernel needs every split within kGroupSplitPages pages; W (bt_stride)
+// pages bound every sequence's page count.
+bool split_group_fits(const pa_dims *d, int split_kv) {
+    return split_kv >= 1 && ((int64_t)d->bt_stride + split_kv - 1) / split_kv <= pa::kGroupSplitPages;
+}
+
+// Multiprocessor count of the current device (cached per device; 152 if it cannot be read).
+int device_sm_count() {
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (!cached[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 152;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
 bool tc05_supports(const pa_dims *d) {
     const int G = d->num_q_heads / d->num_kv_heads;
     return d->dtype != PA_F32 && d->head_dim == 128 && G <= 128 && (128 % G) == 0 &&
@@ -258,7 +277,8 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
     if (nrows == 0) return PA_OK;
     rc = check_fwd_pointers(q, k_cache, v_cache, block_table, seq_lens, q_offset, split_kv, out, lse);
     if (rc != PA_OK) return rc;
-    if (variant == PA_VARIANT_AUTO) {
+    const bool planned = variant == PA_VARIANT_AUTO;
+    if (planned) {
         variant = choose_variant(dims);
         // the tcgen05 kernel takes its row maximum over unscaled scores, which needs scale > 0
         if (variant == PA_VARIANT_TC05_PREFILL && !(scale > 0.f)) variant = PA_VARIANT_MMA_PREFILL;
@@ -276,6 +296,11 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
             break;
         case PA_VARIANT_MMA_T:
             if (dims->dtype == PA_F32 || dims->head_dim != 256) return PA_EUNSUPPORTED;
+            break;
+        case PA_VARIANT_MMA_SPLIT_GROUP:
+            if (dims->dtype == PA_F32 || rows > pa::kDecodeRows || dims->head_dim == 256 ||
+                !split_group_fits(dims, split_kv))
+                return PA_EUNSUPPORTED;
             break;
         case PA_VARIANT_TC05_PREFILL:
             if (!tc05_supports(dims) || !(scale > 0.f)) return PA_EUNSUPPORTED;
@@ -318,8 +343,15 @@ int paged_attn_fwd_variant(const void *q, const void *k_cache, const void *v_cac
         CUtensorMap tmk, tmv;
         if ((rc = make_pool_map(&tmk, k_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
         if ((rc = make_pool_map(&tmv, v_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
-        const int mode = variant == PA_VARIANT_MMA_DECODE ? pa::MODE_DECODE : pa::MODE_PREFILL;
+        int mode = variant == PA_VARIANT_MMA_PREFILL ? pa::MODE_PREFILL : pa::MODE_DECODE;
         if (mode == pa::MODE_PREFILL) p.row_tiles = (rows + pa::kPrefillRows - 1) / pa::kPrefillRows;
+        // Short splits in more CTAs than two per SM hold at once: a CTA per four splits, one warp
+        // per split.  With fewer units the one-CTA-per-split launch is already a single wave, and
+        // its four warps sharing each split's keys finish sooner.
+        if (variant == PA_VARIANT_MMA_SPLIT_GROUP ||
+            (planned && mode == pa::MODE_DECODE && split_kv >= 2 && split_group_fits(dims, split_kv) &&
+             (int64_t)dims->batch * split_kv * dims->num_kv_heads > 2LL * device_sm_count()))
+            mode = pa::MODE_SPLITS;
         e = pa::launch_mma(p, mode, dims->dtype, tmk, tmv, st);
     }
     return cuda_status(e);

@@ -13,7 +13,11 @@
 //     mma.m16n8k16 (fp32 accumulate).  Decode mode: the 16 rows are the GQA
 //     group (x query tokens) and the 4 warps split each stage's 64 keys, then
 //     merge their softmax states once at the end.  Prefill mode: each warp owns
-//     16 query rows and reads all 64 keys of the stage.
+//     16 query rows and reads all 64 keys of the stage.  Split-group mode
+//     (decode with short splits): the CTA takes 4 consecutive splits, each warp
+//     owns one of them (the same 16 rows, all 64 keys of each of its stages) and
+//     stores its own partial, so short splits need neither a key split nor a
+//     merge, and a quarter as many CTAs.
 //   * online softmax in the log2 domain with the rocMLIR PR #2371 guards: a
 //     running max of -inf is replaced by 0 before exp2 (so -inf - (-inf)
 //     never appears), and a row whose sum is 0 stores 0 / lse -inf.
@@ -27,7 +31,8 @@ namespace pa {
 using namespace mmac;
 
 // One unit: sequence b, whose query tokens are `sq` (rows = sq.Sq x G query rows), kv head kvh,
-// split s and, in prefill mode, 64-row query tile rt.  Every thread of the CTA calls it.
+// split s (in split-group mode the group: splits 4 s .. 4 s + 3) and, in prefill mode, 64-row
+// query tile rt.  Every thread of the CTA calls it.
 template <typename T, int D, int MODE, int NSTAGE>
 __device__ __forceinline__ void mma_unit(const CUtensorMap *tmK, const CUtensorMap *tmV, const FwdParams &p, int b,
                                          const SeqRows &sq, int rows, int kvh, int s, int rt, int ps_shift,
@@ -35,10 +40,12 @@ __device__ __forceinline__ void mma_unit(const CUtensorMap *tmK, const CUtensorM
     using Op = MmaOp<T>;
     constexpr int kStage = Geo<D>::kStageBytes;
     constexpr int kChunks = Geo<D>::kChunks;
-    constexpr int KB = (MODE == MODE_DECODE) ? 16 : 32;   // keys per softmax block
-    constexpr int SUBS = (MODE == MODE_DECODE) ? 1 : 2;   // blocks a warp handles per stage
+    constexpr int NW = kMmaConsumerWarps;
+    constexpr bool GROUP = MODE == MODE_SPLITS;
+    constexpr int KB = (MODE == MODE_PREFILL) ? 32 : 16;  // keys per softmax block
+    constexpr int SUBS = (MODE == MODE_DECODE) ? 1 : kMmaTileKeys / KB;  // blocks a warp handles per stage
     constexpr int NTB = KB / 8;                           // score n-tiles per block
-    constexpr int CTA_ROWS = (MODE == MODE_DECODE) ? kDecodeRows : kPrefillRows;
+    constexpr int CTA_ROWS = (MODE == MODE_PREFILL) ? kPrefillRows : kDecodeRows;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -49,50 +56,110 @@ __device__ __forceinline__ void mma_unit(const CUtensorMap *tmK, const CUtensorM
         if (threadIdx.x == 0) atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
         L = p.W * ps;
     }
-    int pg0, pg1;
-    split_pages(L, ps, p.split_kv, s, pg0, pg1);
-    const int k_lo = pg0 * ps;
-    const int k_hi_split = min(pg1 * ps, L);
     const int row0 = rt * CTA_ROWS;
     const int row_end = min(row0 + CTA_ROWS, rows);
     // causal reach grows with the query index, so the CTA's last row reaches furthest
-    const int k_hi = min(k_hi_split, row_key_limit(p, b, L, (row_end - 1) / p.G, sq.Sq));
-    const int n_tiles = k_hi > k_lo ? (k_hi - k_lo + kMmaTileKeys - 1) / kMmaTileKeys : 0;
-
-    if (n_tiles == 0) {
-        // no valid key for any row of this unit: output 0, lse -inf
-        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, sq, kvh, s, row0, row_end);
-        return;
+    const int reach = row_key_limit(p, b, L, (row_end - 1) / p.G, sq.Sq);
+    int pg0, pg1;
+    int k_lo, k_hi_split, k_hi, n_tiles;
+    // split-group mode: every thread knows the four splits' pages and tiles, and warp w takes
+    // split 4 s + w (a split past the last has no pages)
+    int gpg0[NW], gpe[NW], gnt[NW];
+    int my_s = s;
+    if constexpr (GROUP) {
+        const int nblk = (L + ps - 1) >> ps_shift;
+        int any = 0;
+        n_tiles = 0;
+        k_lo = k_hi_split = k_hi = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const int sw = s * NW + w;
+            int a = nblk, e = nblk;
+            if (sw < p.split_kv) split_pages(L, ps, p.split_kv, sw, a, e);
+            const int kl = a * ps, khs = min(e * ps, L), kh = min(khs, reach);
+            gpg0[w] = a;
+            gnt[w] = kh > kl ? (kh - kl + kMmaTileKeys - 1) / kMmaTileKeys : 0;
+            gpe[w] = gnt[w] > 0 ? (kh + ps - 1) >> ps_shift : a;
+            any += gnt[w];
+            if (w == warp) {
+                my_s = sw;
+                k_lo = kl;
+                k_hi_split = khs;
+                k_hi = kh;
+                n_tiles = gnt[w];
+            }
+        }
+        if (any == 0) {
+            // no valid key for any row of the group's splits: output 0, lse -inf
+            if (warp < NW && my_s < p.split_kv) store_empty_unit<T, D>(p, sq, kvh, my_s, row0, row_end, true);
+            return;
+        }
+    } else {
+        split_pages(L, ps, p.split_kv, s, pg0, pg1);
+        k_lo = pg0 * ps;
+        k_hi_split = min(pg1 * ps, L);
+        k_hi = min(k_hi_split, reach);
+        n_tiles = k_hi > k_lo ? (k_hi - k_lo + kMmaTileKeys - 1) / kMmaTileKeys : 0;
+        if (n_tiles == 0) {
+            // no valid key for any row of this unit: output 0, lse -inf
+            if (warp < NW) store_empty_unit<T, D>(p, sq, kvh, s, row0, row_end);
+            return;
+        }
     }
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
+    // full barriers: one per ring slot, or in split-group mode one per stage (kGroupMaxStages)
+    constexpr int NFULL = GROUP ? kGroupMaxStages : NSTAGE;
     const uint32_t bar_fk = smem_u32(&bars[0]);
-    const uint32_t bar_fv = smem_u32(&bars[NSTAGE]);
-    const uint32_t bar_em = smem_u32(&bars[2 * NSTAGE]);
+    const uint32_t bar_fv = smem_u32(&bars[NFULL]);
+    const uint32_t bar_em = smem_u32(&bars[2 * NFULL]);
 
     if (threadIdx.x == 0) {
-        for (int st = 0; st < NSTAGE; ++st) {
-            mbar_init(bar_fk + 8 * st, 1);
-            mbar_init(bar_fv + 8 * st, 1);
-            mbar_init(bar_em + 8 * st, kMmaConsumerWarps);
+        for (int i = 0; i < NFULL; ++i) {
+            mbar_init(bar_fk + 8 * i, 1);
+            mbar_init(bar_fv + 8 * i, 1);
         }
+        for (int st = 0; st < NSTAGE; ++st) mbar_init(bar_em + 8 * st, GROUP ? 1 : NW);  // a group's stage: one warp
         fence_barrier_init();
     }
     __syncthreads();
 
-    if (warp == kMmaConsumerWarps) {
-        produce_pages16<D, NSTAGE>(tmK, tmV, p, b, kvh, pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk, bar_fv, bar_em,
-                                   lane);
+    if (warp == NW) {
+        if constexpr (GROUP)
+            produce_split_group<D, NSTAGE>(tmK, tmV, p, b, kvh, gpg0, gpe, gnt, ps_shift, sbase, bar_fk, bar_fv, bar_em,
+                                           lane);
+        else
+            produce_pages16<D, NSTAGE>(tmK, tmV, p, b, kvh, pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk, bar_fv,
+                                       bar_em, lane);
         return;
+    }
+    if constexpr (GROUP) {
+        if (my_s >= p.split_kv) return;  // no fourth (or third ...) split in the last group
+        if (n_tiles == 0) {              // this warp's split has no valid key: output 0, lse -inf
+            store_empty_unit<T, D>(p, sq, kvh, my_s, row0, row_end, true);
+            return;
+        }
     }
 
     // ==================================================================== consumers
     const int g = lane >> 2;
     const int tq = lane & 3;
-    const int rbase = (MODE == MODE_DECODE) ? 0 : row0 + warp * 16;
+    const int rbase = (MODE == MODE_PREFILL) ? row0 + warp * 16 : 0;
     const int ra = rbase + g, rb = rbase + g + 8;
     const int kw0 = (MODE == MODE_DECODE) ? warp * 16 : 0;  // first key (in the stage) of this warp
+    // split-group mode: this warp's tile t is stage (tiles of earlier rounds, all splits) + (tile t
+    // of earlier splits), the producer's interleaved order
+    auto stage_of = [&](int t) {
+        int k = 0;
+        if constexpr (GROUP) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) k += min(t, gnt[w]) + ((w < warp && gnt[w] > t) ? 1 : 0);
+        } else {
+            k = t;
+        }
+        return k;
+    };
 
     // Q fragments (A operand, row-major 16 x D): rows ra / rb, zero beyond the unit's rows
     uint32_t qf[D / 16][4];
@@ -124,14 +191,16 @@ __device__ __forceinline__ void mma_unit(const CUtensorMap *tmK, const CUtensorM
 
     bool bad = false;
     for (int t = 0; t < n_tiles; ++t) {
-        const int st = t % NSTAGE;
-        const uint32_t par = (t / NSTAGE) & 1;
+        const int kst = stage_of(t);
+        const int st = kst % NSTAGE;
+        const uint32_t par = GROUP ? 0u : (uint32_t)(kst / NSTAGE) & 1;  // group: the stage's own barriers
+        const uint32_t bk = GROUP ? (uint32_t)kst : (uint32_t)st;            // full-barrier index
         const uint32_t kbuf = sbase + (uint32_t)(st * 2 * kStage);
         const uint32_t vbuf = kbuf + kStage;
         const int tile_k0 = k_lo + t * kMmaTileKeys;
 
         if (!bad) {
-            const bool ok = mbar_wait(bar_fk + 8 * st, par, p.err);
+            const bool ok = mbar_wait(bar_fk + 8 * bk, par, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
 #pragma unroll
@@ -207,14 +276,15 @@ __device__ __forceinline__ void mma_unit(const CUtensorMap *tmK, const CUtensorM
 
             if (sb == 0) {
                 if (!bad) {
-                    const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
+                    const bool ok = mbar_wait(bar_fv + 8 * bk, par, p.err);
                     bad = __any_sync(0xffffffffu, !ok);
                 }
                 if (tile_k0 + kMmaTileKeys > k_hi) {
                     // Last stage: keys at or past k_hi (past the sequence, or pages never loaded)
-                    // may hold any bits.  Their weight is 0, but 0 * NaN is NaN, so zero those V rows.
-                    const int kz0 = (MODE == MODE_DECODE) ? kw0 : warp * 16;
-                    for (int idx = lane; idx < 16 * kChunks; idx += 32) {
+                    // may hold any bits.  Their weight is 0, but 0 * NaN is NaN, so zero those V rows
+                    // (the warp's own 16 keys; a split-group warp owns all 64 of the stage).
+                    const int kz0 = (MODE == MODE_DECODE) ? kw0 : (GROUP ? 0 : warp * 16);
+                    for (int idx = lane; idx < (GROUP ? 64 : 16) * kChunks; idx += 32) {
                         const int key = kz0 + idx / kChunks;
                         if (tile_k0 + key >= k_hi) {
                             const uint32_t a = kv_chunk_addr<D>(vbuf, key, idx % kChunks, ps_shift);
@@ -222,7 +292,7 @@ __device__ __forceinline__ void mma_unit(const CUtensorMap *tmK, const CUtensorM
                         }
                     }
                     fence_proxy_async_smem();
-                    if (MODE == MODE_DECODE)
+                    if (MODE != MODE_PREFILL)
                         __syncwarp();
                     else
                         named_bar_sync(1, kMmaConsumerWarps * 32);
@@ -259,9 +329,9 @@ __device__ __forceinline__ void mma_unit(const CUtensorMap *tmK, const CUtensorM
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
 
-    if (MODE == MODE_PREFILL) {
-        // each warp owns its rows: finalise and store
-        if (!bad) finish_prefill_rows<T, D>(p, sq, kvh, s, ra, rb, row_end, tq, m_a, m_b, l_a, l_b, acc);
+    if (MODE != MODE_DECODE) {
+        // each warp owns its rows (prefill) or its split (split group): finalise and store
+        if (!bad) finish_prefill_rows<T, D>(p, sq, kvh, my_s, ra, rb, row_end, tq, m_a, m_b, l_a, l_b, acc);
         return;
     }
     // decode: merge the four warps' (m, l, acc) through shared memory (reuses the ring)
@@ -275,7 +345,7 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
     paged_attn_mma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           const FwdParams p, int ps_shift) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[3 * NSTAGE];
+    __shared__ __align__(8) uint64_t bars[MODE == MODE_SPLITS ? 2 * kGroupMaxStages + NSTAGE : 3 * NSTAGE];
     int unit = blockIdx.x;
     int rt = 0;
     if (MODE == MODE_PREFILL) {
@@ -284,8 +354,10 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
     }
     const int kvh = unit % p.Hkv;
     unit /= p.Hkv;
-    const int s = unit % p.split_kv;
-    const int b = unit / p.split_kv;
+    // split-group mode: s indexes groups of kMmaConsumerWarps splits
+    const int ns = MODE == MODE_SPLITS ? (p.split_kv + kMmaConsumerWarps - 1) / kMmaConsumerWarps : p.split_kv;
+    const int s = unit % ns;
+    const int b = unit / ns;
     mma_unit<T, D, MODE, NSTAGE>(&tmK, &tmV, p, b, uniform_seq(p, b), p.rows, kvh, s, rt, ps_shift, smem_raw, bars);
 }
 
@@ -363,7 +435,8 @@ static cudaError_t launch_mma_t(const FwdParams &p, const CUtensorMap &tmk, cons
     if (e != cudaSuccess) return e;
     int ps_shift = 0;
     while ((1 << ps_shift) < p.ps) ++ps_shift;
-    const long long units = (long long)p.B * p.split_kv * p.Hkv * (MODE == MODE_PREFILL ? p.row_tiles : 1);
+    const long long ns = MODE == MODE_SPLITS ? (p.split_kv + kMmaConsumerWarps - 1) / kMmaConsumerWarps : p.split_kv;
+    const long long units = (long long)p.B * ns * p.Hkv * (MODE == MODE_PREFILL ? p.row_tiles : 1);
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)units, kMmaThreads, smem, stream>>>(tmk, tmv, p, ps_shift);
@@ -374,9 +447,11 @@ template <typename T>
 static cudaError_t launch_mma_dt(const FwdParams &p, int mode, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                  cudaStream_t stream) {
     if (p.D == 128) {
+        if (mode == MODE_SPLITS) return launch_mma_t<T, 128, MODE_SPLITS, 3>(p, tmk, tmv, stream);
         return mode == MODE_DECODE ? launch_mma_t<T, 128, MODE_DECODE, 3>(p, tmk, tmv, stream)
                                    : launch_mma_t<T, 128, MODE_PREFILL, 3>(p, tmk, tmv, stream);
     }
+    if (mode == MODE_SPLITS) return launch_mma_t<T, 64, MODE_SPLITS, 4>(p, tmk, tmv, stream);
     return mode == MODE_DECODE ? launch_mma_t<T, 64, MODE_DECODE, 4>(p, tmk, tmv, stream)
                                : launch_mma_t<T, 64, MODE_PREFILL, 4>(p, tmk, tmv, stream);
 }

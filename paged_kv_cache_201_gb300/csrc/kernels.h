@@ -9,13 +9,21 @@
 namespace pa {
 
 // Tensor-core kernel modes.
-enum { MODE_DECODE = 0, MODE_PREFILL = 1 };
+enum { MODE_DECODE = 0, MODE_PREFILL = 1, MODE_SPLITS = 2 };
 
 constexpr int kMmaTileKeys = 64;      // keys per pipeline stage
 constexpr int kMmaConsumerWarps = 4;  // warps doing QK / softmax / PV
 constexpr int kMmaThreads = (kMmaConsumerWarps + 1) * 32;
 constexpr int kDecodeRows = 16;       // query rows of one decode CTA (one m16 tile)
 constexpr int kPrefillRows = 64;      // query rows of one prefill CTA (4 warps x 16)
+// MODE_SPLITS: decode whose splits are short.  A CTA takes kMmaConsumerWarps consecutive splits
+// of one (sequence, kv head) and each consumer warp owns one of them; every split is at most
+// kGroupSplitPages pages, so a group's page ids fit one warp-wide load.
+constexpr int kGroupSplitPages = 32 / kMmaConsumerWarps;
+// Stages of one group at most: four splits of kGroupSplitPages pages of up to 64 tokens, 64-key
+// stages.  Each has its own full barriers (waited once, at phase 0): the warps consume the ring's
+// slots out of step with one another, so a per-slot parity could be two phases behind.
+constexpr int kGroupMaxStages = kMmaConsumerWarps * kGroupSplitPages;
 
 // Dynamic shared memory of the tensor-core kernel for a pipeline depth.
 size_t mma_smem_bytes(int head_dim, int stages);

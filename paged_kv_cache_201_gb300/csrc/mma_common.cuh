@@ -136,12 +136,90 @@ __device__ __forceinline__ void produce_pages16(const CUtensorMap *tmK, const CU
     }
 }
 
-// A unit with no valid key for any of its rows: output 0, lse -inf (consumer warps only).
+// Producer of a split group (MODE_SPLITS): split w of the group reads pages [pg0[w], pe[w]) in
+// nt[w] 64-key tiles; the group's pages are consecutive from pg0[0] and at most 32, so one id per
+// lane covers them.  Stages go out interleaved, round t holding tile t of every split that has
+// one (in split order), and stage k lands in ring slot k % NSTAGE, so the four consumer warps
+// work on their own splits at once.  Stage k completes on its own full barriers bar_fk / bar_fv
+// + 8 k (used once); slot st frees on bar_em + 8 st, which only this warp waits on, in order.
+template <int D, int NSTAGE>
+__device__ __forceinline__ void produce_split_group(const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                                    const FwdParams &p, int b, int kvh,
+                                                    const int (&pg0)[kMmaConsumerWarps],
+                                                    const int (&pe)[kMmaConsumerWarps],
+                                                    const int (&nt)[kMmaConsumerWarps], int ps_shift, uint32_t sbase,
+                                                    uint32_t bar_fk, uint32_t bar_fv, uint32_t bar_em, int lane) {
+    constexpr int kStage = Geo<D>::kStageBytes;
+    constexpr int NW = kMmaConsumerWarps;
+    const int ps = 1 << ps_shift;
+    if (lane == 0) {
+        tma_prefetch_desc(tmK);
+        tma_prefetch_desc(tmV);
+    }
+    const int pps = kMmaTileKeys >> ps_shift;  // pages per stage
+    const uint32_t box_bytes = (uint32_t)(Geo<D>::NH * ps * 128);
+    // lane i: the id of page pg0[0] + i, loaded only when one of the splits reads that page
+    const int my_page = pg0[0] + lane;
+    bool read = false;
+    int max_nt = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        read |= my_page >= pg0[w] && my_page < pe[w];
+        max_nt = max(max_nt, nt[w]);
+    }
+    const int id_lane = read ? __ldg(p.block_table + (long long)b * p.W + my_page) : 0;
+    bool bad = false;
+    int k = 0;  // stages issued
+    for (int t = 0; t < max_nt && !bad; ++t) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            if (t >= nt[w] || bad) continue;  // warp-uniform
+            const int st = k % NSTAGE;
+            if (k >= NSTAGE) {
+                const bool ok = mbar_wait(bar_em + 8 * st, ((k / NSTAGE) - 1) & 1, p.err);
+                bad = __any_sync(0xffffffffu, !ok);
+                if (bad) break;
+            }
+            const int pg_first = pg0[w] + t * pps;
+            const int nvalid = min(pps, pe[w] - pg_first);
+            const int id = __shfl_sync(0xffffffffu, id_lane, (pg_first - pg0[0] + lane) & 31);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar_fk + 8 * k, (uint32_t)nvalid * box_bytes);
+                mbar_arrive_expect_tx(bar_fv + 8 * k, (uint32_t)nvalid * box_bytes);
+            }
+            __syncwarp();
+            if (lane < nvalid) {
+                int tok;
+                if (id < 0 || (long long)id >= p.num_pages) {
+                    atomicOr(p.err, (unsigned int)PA_ERRBIT_PAGE_RANGE);
+                    tok = -ps;  // wholly out of the tensor: the box reads as zeros
+                } else {
+                    tok = id << ps_shift;
+                }
+                const uint32_t kdst = sbase + (uint32_t)(st * 2 * kStage) + (uint32_t)lane * box_bytes;
+                tma_load_4d(kdst, tmK, bar_fk + 8 * k, 0, tok, 0, kvh);
+                tma_load_4d(kdst + kStage, tmV, bar_fv + 8 * k, 0, tok, 0, kvh);
+            }
+            ++k;
+        }
+    }
+    // Every copy must have landed before the CTA may exit: the last NSTAGE stages' barriers
+    // (bounded waits; earlier stages were consumed before their slots were reused).
+    for (int kk = max(0, k - NSTAGE); kk < k; ++kk) {
+        mbar_wait(bar_fk + 8 * kk, 0, p.err);
+        mbar_wait(bar_fv + 8 * kk, 0, p.err);
+    }
+}
+
+// A unit with no valid key for any of its rows: output 0, lse -inf (every consumer thread, or
+// with one_warp the 32 threads of one warp).
 template <typename T, int D>
 __device__ __forceinline__ void store_empty_unit(const FwdParams &p, const SeqRows &sq, int kvh, int s, int row0,
-                                                 int row_end) {
+                                                 int row_end, bool one_warp = false) {
     const int nrows = row_end - row0;
-    for (int idx = threadIdx.x; idx < nrows * (D / 2); idx += kMmaConsumerWarps * 32) {
+    const int i0 = one_warp ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
+    const int stride = one_warp ? 32 : kMmaConsumerWarps * 32;
+    for (int idx = i0; idx < nrows * (D / 2); idx += stride) {
         const int r = row0 + idx / (D / 2);
         const int col = (idx % (D / 2)) * 2;
         const long long ridx = out_row_index(p, sq, kvh, r);

@@ -81,6 +81,10 @@ def _fwd(lib, dims, split=1, scale=0.1, lse=FAKE, q=FAKE, out=FAKE, variant=0):
     (dict(q_len=2, num_q_heads=32), 1, 0.1, dict(variant=2), EUNSUP),
     ({}, 1, 0.1, dict(variant=9), EINVAL),
     (dict(q_len=128), 1, 0.0, dict(variant=4), EUNSUP),   # tcgen05 prefill takes scale > 0 only
+    (dict(bt_stride=17), 2, 0.1, dict(variant=6), EUNSUP),   # split group: a split past 8 pages
+    (dict(q_len=5), 4, 0.1, dict(variant=6), EUNSUP),        # split group: 20 rows > 16
+    (dict(head_dim=256), 4, 0.1, dict(variant=6), EUNSUP),
+    (dict(dtype=pa.PA_F32), 4, 0.1, dict(variant=6), EUNSUP),
     (dict(q_len=128), 1, -0.1, dict(variant=4), EUNSUP),
     (dict(batch=0), 1, 0.1, {}, OK),
     (dict(q_len=0), 4, 0.1, dict(lse=None), OK),

@@ -223,3 +223,20 @@ def test_bounded_wait_gives_up_and_context_survives(pa):
     rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)
     _gpu.compare_rows(res, oracle.workload_rows(wl, split_kv=2, row_bih=rows), rows, wl, 2, "after time-out")
     assert pa.paged_attn_last_error_word() == 0
+
+
+@pytest.mark.parametrize("S", [2, 3, 5, 8, 13])
+@pytest.mark.parametrize("ps,D,dtype", [(16, 128, "bf16"), (32, 64, "f16"), (64, 128, "f16")])
+def test_split_group_decode(pa, S, ps, D, dtype):
+    """Decode with short splits (every split at most 8 pages), forced: one CTA per four consecutive
+    splits, one warp per split (the planner takes it for config 3's 1024 splits).  Partial last groups, empty splits inside a group, sentinel tails, 1-3
+    query tokens with causal offsets, every row against the oracle."""
+    lens = [0, 1, 15, ps, ps + 1, 3 * ps - 1, 5 * ps + 3, 8 * ps * S // 2 + 7]
+    width = max(-(-max(lens) // ps), 1)
+    assert -(-width // S) <= 8
+    for Sq, Hq, Hkv in [(1, 16, 1), (3, 8, 2)]:
+        qo = [max(L - Sq, 0) for L in lens] if Sq > 1 else None
+        wl = W.make_custom(dtype=dtype, B=len(lens), Sq=Sq, Hq=Hq, Hkv=Hkv, D=D, page_size=ps, seq_lens=lens,
+                           W=width, causal=Sq > 1, q_offset=qo, seed=140 + S + ps + Sq)
+        _full_check(wl, S, pa.VARIANT_MMA_SPLIT_GROUP, f"split group S={S} ps={ps} D={D} Sq={Sq}")
+    assert pa.paged_attn_last_error_word() == 0
