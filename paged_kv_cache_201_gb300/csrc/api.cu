@@ -117,15 +117,17 @@ int make_pool_map_e4m3(CUtensorMap *m, const void *base, const pa_dims *d) {
     return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
 }
 
-// 4-D view of q for the tcgen05 kernel: (d within a half, half, query head, token of B*Sq);
-// one box = one half of a 128-row tile: 128/G consecutive tokens x the G heads of a kv head.
-int make_q_map(CUtensorMap *m, const void *q, const pa_dims *d) {
+// 4-D view of q for the tcgen05 kernel: (d within a half, half, query head, token of B*Sq, or of
+// the T packed tokens of a variable-length batch); one box = one half of a 128-row tile: 128/G
+// consecutive tokens x the G heads of a kv head.
+int make_q_map(CUtensorMap *m, const void *q, const pa_dims *d, bool varlen = false) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PA_ECUDA;
     const cuuint64_t esz = 2;
     const cuuint64_t D = (cuuint64_t)d->head_dim, Hq = (cuuint64_t)d->num_q_heads;
     const int G = d->num_q_heads / d->num_kv_heads;
-    const cuuint64_t dims[4] = {64, D / 64, Hq, (cuuint64_t)d->batch * (cuuint64_t)d->q_len};
+    const cuuint64_t tokens = varlen ? (cuuint64_t)d->q_len : (cuuint64_t)d->batch * (cuuint64_t)d->q_len;
+    const cuuint64_t dims[4] = {64, D / 64, Hq, tokens};
     const cuuint64_t strides[3] = {64 * esz, D * esz, Hq * D * esz};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)G, (cuuint32_t)(128 / G)};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -137,16 +139,19 @@ int make_q_map(CUtensorMap *m, const void *q, const pa_dims *d) {
 
 // 4-D view of the tcgen05 kernel's output for TMA stores: (d, query head, token, sequence) for the
 // final rows (split_kv = 1, q's element type) or (d, query head, token, split x B + sequence) for
-// the fp32 partials.  One box = one epilogue warp's 32 rows (min(G, 32) heads x max(32 / G, 1)
-// tokens) x 128 bytes of columns, 128-byte swizzled; tokens past Sq fall outside and are clipped.
-int make_tc05_out_map(CUtensorMap *m, void *out, const pa_dims *d, int split_kv) {
+// the fp32 partials; for a variable-length batch (d, query head, packed token, split).  One box =
+// one epilogue warp's 32 rows (min(G, 32) heads x max(32 / G, 1) tokens) x 128 bytes of columns,
+// 128-byte swizzled; tokens past Sq fall outside and are clipped (a variable-length batch's
+// kernel stores rows that run past their sequence itself).
+int make_tc05_out_map(CUtensorMap *m, void *out, const pa_dims *d, int split_kv, bool varlen = false) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PA_ECUDA;
     const bool part = split_kv > 1;
     const cuuint64_t esz = part ? 4 : 2;
     const cuuint64_t D = (cuuint64_t)d->head_dim, Hq = (cuuint64_t)d->num_q_heads, Sq = (cuuint64_t)d->q_len;
     const int G = d->num_q_heads / d->num_kv_heads;
-    const cuuint64_t dims[4] = {D, Hq, Sq, (cuuint64_t)d->batch * (cuuint64_t)(part ? split_kv : 1)};
+    const cuuint64_t nsp = (cuuint64_t)(part ? split_kv : 1);
+    const cuuint64_t dims[4] = {D, Hq, Sq, varlen ? nsp : (cuuint64_t)d->batch * nsp};
     const cuuint64_t strides[3] = {D * esz, Hq * D * esz, Sq * Hq * D * esz};
     const cuuint32_t bh = (cuuint32_t)(G < 32 ? G : 32), bt = (cuuint32_t)(G < 32 ? 32 / G : 1);
     const cuuint32_t box[4] = {(cuuint32_t)(128 / esz), bh, bt, 1};
@@ -487,11 +492,23 @@ int paged_attn_fwd_varlen(const void *q, const void *k_cache, const void *v_cach
     p.Sq = 0;
     p.rows = 0;
     p.rows_total = (long long)dims->q_len * dims->num_q_heads;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Sequences of at least 64 query rows go to the tcgen05 kernel when it takes the shape (it
+    // finds them on the device, from q_start); the one-grid kernel takes the rest, or everything.
+    if (tc05_supports(dims) && scale > 0.f && dims->batch <= pa::kTc05VarlenMaxBatch) {
+        CUtensorMap tmq, tmk5, tmv5, tmo;
+        if ((rc = make_q_map(&tmq, q, dims, true)) != PA_OK) return rc;
+        if ((rc = make_pool_map(&tmk5, k_cache, dims, 1)) != PA_OK) return rc;
+        if ((rc = make_pool_map(&tmv5, v_cache, dims, 1)) != PA_OK) return rc;
+        if ((rc = make_tc05_out_map(&tmo, out, dims, split_kv, true)) != PA_OK) return rc;
+        rc = cuda_status(pa::launch_tc05_varlen(p, dims->q_len, dims->dtype, tmq, tmk5, tmv5, tmo, st));
+        if (rc != PA_OK) return rc;
+        p.varlen_rows_cap = 64;
+    }
     CUtensorMap tmk, tmv;
     if ((rc = make_pool_map(&tmk, k_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
     if ((rc = make_pool_map(&tmv, v_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
-    return cuda_status(
-        pa::launch_mma_varlen(p, dims->q_len, dims->dtype, tmk, tmv, static_cast<cudaStream_t>(stream)));
+    return cuda_status(pa::launch_mma_varlen(p, dims->q_len, dims->dtype, tmk, tmv, st));
 }
 
 int paged_attn_combine(const float *part_out, const float *part_lse, int split_kv, int64_t rows, int head_dim,

@@ -401,7 +401,9 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
     unit /= p.Hkv;
     const int s = unit % p.split_kv;
     const long long t = unit / p.split_kv;
-    const int b = varlen_sequence(p, t, threadIdx.x & 31);
+    // with a row cap, every sequence this kernel takes fits one block: block t is sequence t
+    const bool capped = p.varlen_rows_cap > 0;
+    const int b = capped ? (int)t : varlen_sequence(p, t, threadIdx.x & 31);
     const int q0 = __ldg(p.q_start + b), q1 = __ldg(p.q_start + b + 1);
     if (q0 < 0 || q1 < q0 || (long long)q1 * p.Hq > p.rows_total) {
         if (threadIdx.x == 0) atomicOr(p.err, (unsigned int)PA_ERRBIT_QSTART);
@@ -409,8 +411,9 @@ __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
     }
     const SeqRows sq{q0, q1 - q0};
     const int rows = sq.Sq * p.G;
-    const long long j = t - varlen_first_block(p, b);  // block within the sequence
+    const long long j = capped ? 0 : t - varlen_first_block(p, b);  // block within the sequence
     if (rows == 0 || j < 0) return;
+    if (p.varlen_rows_cap > 0 && rows >= p.varlen_rows_cap) return;  // the tcgen05 kernel's
     if (rows <= kDecodeRows) {
         if (j == 0) mma_unit<T, D, MODE_DECODE, NSTAGE>(&tmK, &tmV, p, b, sq, rows, kvh, s, 0, ps_shift, smem_raw, bars);
     } else if (j < (rows + kPrefillRows - 1) / kPrefillRows) {
@@ -468,9 +471,11 @@ static cudaError_t launch_varlen_t(const FwdParams &p, long long blocks, const C
     const long long units = blocks * p.split_kv * p.Hkv;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    // visiting stride: the first value >= 0.618 units that is coprime to units (1 for tiny grids)
+    // visiting stride: the first value >= 0.618 units that is coprime to units (1 for tiny grids),
+    // which mixes prefill tiles into the decode units; with a row cap (the tcgen05 kernel has the
+    // prefill sequences) 1, so neighbouring CTAs read the kv heads of the same pages
     FwdParams q = p;
-    long long stride = units > 2 ? (units * 618) / 1000 : 1;
+    long long stride = (units > 2 && p.varlen_rows_cap == 0) ? (units * 618) / 1000 : 1;
     auto gcd = [](long long a, long long b) { while (b) { const long long r = a % b; a = b; b = r; } return a; };
     while (stride > 1 && gcd(stride, units) != 1) ++stride;
     q.row_tiles = (int)(stride < 1 ? 1 : stride);
@@ -480,8 +485,10 @@ static cudaError_t launch_varlen_t(const FwdParams &p, long long blocks, const C
 
 cudaError_t launch_mma_varlen(const FwdParams &p, long long total_q, int dtype, const CUtensorMap &tmk,
                               const CUtensorMap &tmv, cudaStream_t stream) {
-    // blocks of the packed rows: floor(T G / 64) + B (see varlen_first_block)
-    const long long blocks = total_q * p.G / kPrefillRows + p.B;
+    // blocks of the packed rows: floor(T G / 64) + B (see varlen_first_block); with a row cap of at
+    // most 64 rows, one per sequence
+    const long long blocks =
+        (p.varlen_rows_cap > 0 && p.varlen_rows_cap <= kPrefillRows) ? p.B : total_q * p.G / kPrefillRows + p.B;
     if (dtype == PA_BF16) {
         return p.D == 128 ? launch_varlen_t<__nv_bfloat16, 128, 3>(p, blocks, tmk, tmv, stream)
                           : launch_varlen_t<__nv_bfloat16, 64, 4>(p, blocks, tmk, tmv, stream);

@@ -64,8 +64,9 @@ enum {
     B_OD = 20, B_VZ = 21, B_LF = 23, B_LE = 25, B_COUNT = 27
 };
 
-__device__ __forceinline__ long long t5_row_index(const FwdParams &p, int b, int kvh, int tok, int g) {
-    return ((long long)b * p.Sq + tok) * p.Hq + (long long)kvh * p.G + g;
+// Output row of query token tok (of the sequence whose first packed token is q0) and head kvh G + g.
+__device__ __forceinline__ long long t5_row_index(const FwdParams &p, int q0, int kvh, int tok, int g) {
+    return ((long long)q0 + tok) * p.Hq + (long long)kvh * p.G + g;
 }
 
 // The log-sum-exp of one row: the final one (split_kv = 1, if wanted) or split s's.
@@ -74,7 +75,7 @@ __device__ __forceinline__ void t5_store_lse(const FwdParams &p, int s, long lon
     if constexpr (!PART) {
         if (p.lse) p.lse[ridx] = lse;
     } else {
-        p.lse[(long long)s * ((long long)p.B * p.Sq * p.Hq) + ridx] = lse;
+        p.lse[(long long)s * p.rows_total + ridx] = lse;
     }
 }
 
@@ -143,8 +144,11 @@ __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], float c2, 
 }
 
 // Everything a role needs to know about one work unit; every role derives it the same way.
+// q0: the sequence's first packed query token, Sq its query count; skip: a unit of the
+// variable-length launch that is not this kernel's (no loads, no product, no output).
 struct T5Unit {
-    int b, kvh, s, L, k_lo, k_hi_split, k_hi, pg0, tok0, tok_end, n_tiles;
+    int b, kvh, s, L, k_lo, k_hi_split, k_hi, pg0, tok0, tok_end, n_tiles, q0, Sq;
+    bool skip;
 };
 
 // seq_lens / q_offset as staged by the CTA (shared memory when the batch fits, else global).
@@ -153,9 +157,9 @@ struct T5Lens {
     const int32_t *q_offset;  // null: seq_lens[b] - Sq
 };
 
-__device__ __forceinline__ int t5_key_limit(const FwdParams &p, const T5Lens &ln, int b, int L, int i) {
+__device__ __forceinline__ int t5_key_limit(const FwdParams &p, const T5Lens &ln, int b, int L, int Sq, int i) {
     if (!p.causal) return L;
-    const long long qoff = ln.q_offset ? (long long)ln.q_offset[b] : (long long)L - p.Sq;
+    const long long qoff = ln.q_offset ? (long long)ln.q_offset[b] : (long long)L - Sq;
     long long reach = qoff + i + 1;
     reach = reach < 0 ? 0 : reach;
     return (int)(reach < L ? reach : L);
@@ -180,7 +184,7 @@ __device__ __forceinline__ T5Pos t5_pos(const FwdParams &p, int unit) {
     return u;
 }
 
-// u += d, for d's digits each below its radix; u.b >= p.B past the last unit.
+// u += d, for d's digits each below its radix; u.b at or past the b digit's count past the last unit.
 __device__ __forceinline__ void t5_advance(const FwdParams &p, T5Pos &u, const T5Pos &d) {
     u.rt += d.rt;
     int c = u.rt >= p.row_tiles;
@@ -194,14 +198,54 @@ __device__ __forceinline__ void t5_advance(const FwdParams &p, T5Pos &u, const T
     u.b += d.b + c;
 }
 
+// Variable-length batches (at most kT5StageLens sequences): q_start staged in shared memory by
+// the CTA (a fixed address, so reading it costs the softmax warps no pointer register).
+__shared__ int32_t t5_qstart[kT5StageLens + 1];
+static_assert(kTc05VarlenMaxBatch <= kT5StageLens, "the host's variable-length batch limit must fit the stage");
+
+// The packed rows are cut into blocks, sequence b's first being floor(q_start[b] G / 128) + b
+// (strictly increasing, and at least as many blocks as the sequence has 128-row tiles before the
+// next one starts).  Block blk belongs to the largest such b.
+__device__ __forceinline__ long long t5_first_block(int b, int g_shift) {
+    return (((long long)t5_qstart[b]) << g_shift >> 7) + b;
+}
+
+template <bool VARLEN>
 __device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, const T5Lens &ln, const T5Pos &q, int tpt,
-                                          int ps_shift) {
+                                          int ps_shift, int g_shift) {
     T5Unit U;
     const int ps = 1 << ps_shift;
-    const int rt = q.rt;
+    int rt;
     U.kvh = q.kvh;
     U.s = q.s;
-    U.b = q.b;
+    U.skip = false;
+    if constexpr (VARLEN) {
+        // the b digit is the block: find its sequence (binary search on the first blocks)
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (t5_first_block(mid, g_shift) <= q.b) lo = mid;
+            else hi = mid - 1;
+        }
+        U.b = lo;
+        U.q0 = t5_qstart[lo];
+        const int q1 = t5_qstart[lo + 1];
+        U.Sq = q1 - U.q0;
+        rt = (int)(q.b - t5_first_block(lo, g_shift));
+        // an invalid q_start entry (the one-grid kernel flags it), a sequence of fewer than 64
+        // query rows (the one-grid kernel takes it) or a block past the sequence's tiles
+        U.skip = U.q0 < 0 || U.Sq < 0 || (long long)q1 * p.Hq > p.rows_total || (U.Sq << g_shift) < 64 || rt < 0 ||
+                 rt >= ((U.Sq + tpt - 1) >> (7 - g_shift));
+        if (U.skip) {
+            U.n_tiles = 0;
+            return U;
+        }
+    } else {
+        rt = q.rt;
+        U.b = q.b;
+        U.Sq = p.Sq;
+        U.q0 = q.b * p.Sq;
+    }
     U.L = min(max(ln.seq_lens[U.b], 0), p.W * ps);
     // the split plan of split_pages, with the page count by shift
     const int nblk = (U.L + ps - 1) >> ps_shift;
@@ -212,8 +256,8 @@ __device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, const T5Lens &ln, 
     U.k_lo = U.pg0 * ps;
     U.k_hi_split = min(pg1 * ps, U.L);
     U.tok0 = rt * tpt;
-    U.tok_end = min(U.tok0 + tpt, p.Sq);
-    U.k_hi = min(U.k_hi_split, t5_key_limit(p, ln, U.b, U.L, U.tok_end - 1));
+    U.tok_end = min(U.tok0 + tpt, U.Sq);
+    U.k_hi = min(U.k_hi_split, t5_key_limit(p, ln, U.b, U.L, U.Sq, U.tok_end - 1));
     U.n_tiles = U.k_hi > U.k_lo ? (U.k_hi - U.k_lo + 127) / 128 : 0;
     return U;
 }
@@ -222,13 +266,15 @@ __device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, const T5Lens &ln, 
 // on the CTA's global tile counter g; Q and O are double-buffered by the CTA's count of non-empty
 // units n, so a unit's read-out and the next unit's loads overlap its neighbours' work.  PART: the
 // output is split_kv > 1's fp32 partials (else the final rows in T); one store path per kernel keeps
-// the code the SM must hold small.  G = 2^g_shift (it divides 128).
-template <typename T, bool PART>
+// the code the SM must hold small.  G = 2^g_shift (it divides 128).  VARLEN: a variable-length
+// batch (q_start), whose sequences of at least 64 query rows this kernel takes; the unit order's
+// b digit is then the block of the packed rows (nb of them), and row_tiles is 1.
+template <typename T, bool PART, bool VARLEN>
 __global__ void __launch_bounds__(kT5Threads, 1)
     paged_attn_tc05_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                            const FwdParams p, int tpt, int ps_shift, int g_shift, uint32_t idesc_qk,
-                           uint32_t idesc_pv) {
+                           uint32_t idesc_pv, int nb) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[B_COUNT];
     __shared__ uint32_t s_tmem;
@@ -251,6 +297,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         ln.seq_lens = s_seqlen;
         ln.q_offset = p.q_offset ? s_qoff : nullptr;
     }
+    if constexpr (VARLEN)  // the host launches this kernel only for B <= kT5StageLens
+        for (int i = threadIdx.x; i <= p.B; i += kT5Threads) t5_qstart[i] = p.q_start[i];
 
     // shared memory: Q x2 | K x2 | V x2 (128 x 128 tiles, two 64-column swizzled halves each)
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -287,7 +335,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     tc05::fence_after_sync();
     const uint32_t tmem = s_tmem;
     const int wg = warp >> 2;
-    const T5Pos step = t5_pos(p, gridDim.x);  // gridDim.x <= the unit count, so b < B here
+    const T5Pos step = t5_pos(p, gridDim.x);  // gridDim.x <= the unit count, so b < nb here
 
     if (wg == 0) {
         tc05::setmaxnreg_dec<kRegLoad>();
@@ -310,23 +358,23 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             int n = 0, g0 = 0;                                   // non-empty units so far, global tile base
             // The first id batch of the next non-empty unit is loaded one unit ahead, so its latency
             // hides behind the current unit's copies.
-            // the first unit with key tiles at or after position q (q.b >= p.B: none), into V
+            // the first unit with key tiles at or after position q (q.b >= nb: none), into V
             auto next_unit = [&](T5Pos q, T5Unit &V) {
-                for (; q.b < p.B; t5_advance(p, q, step)) {
-                    V = t5_unit(p, ln, q, tpt, ps_shift);
+                for (; q.b < nb; t5_advance(p, q, step)) {
+                    V = t5_unit<VARLEN>(p, ln, q, tpt, ps_shift, g_shift);
                     if (V.n_tiles > 0) break;
                 }
                 return q;
             };
             auto first_ids = [&](const T5Pos &q, const T5Unit &V) {
-                if (q.b >= p.B) return 0;
+                if (q.b >= nb) return 0;
                 const int pe = (V.k_hi + ps - 1) >> ps_shift;
                 return (V.pg0 + lane < pe) ? __ldg(p.block_table + (long long)V.b * p.W + V.pg0 + lane) : 0;
             };
             T5Unit Un{};
             T5Pos pos = next_unit(t5_pos(p, blockIdx.x), Un);
             int ids_pref = first_ids(pos, Un);
-            while (pos.b < p.B && !bad) {
+            while (pos.b < nb && !bad) {
                 const T5Unit U = Un;
                 T5Pos nxt = pos;
                 t5_advance(p, nxt, step);
@@ -341,7 +389,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 }
                 if (kq && lane == 0) {
                     mbar_arrive_expect_tx(bar(B_QF + qb), (uint32_t)kT5Tile);
-                    const int qtok = U.b * p.Sq + U.tok0;
+                    const int qtok = U.q0 + U.tok0;
                     tma_load_4d(sQ(qb), &tmQ, bar(B_QF + qb), 0, 0, U.kvh * p.G, qtok);
                     tma_load_4d(sQ(qb) + kT5Half, &tmQ, bar(B_QF + qb), 0, 1, U.kvh * p.G, qtok);
                 }
@@ -430,8 +478,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     return true;
                 };
                 int n = 0, g0 = 0;
-                for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < p.B && !bad; t5_advance(p, pos, step)) {
-                    const T5Unit U = t5_unit(p, ln, pos, tpt, ps_shift);
+                for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < nb && !bad; t5_advance(p, pos, step)) {
+                    const T5Unit U = t5_unit<VARLEN>(p, ln, pos, tpt, ps_shift, g_shift);
                     if (U.n_tiles == 0) continue;
                     const int qb = n & 1;
                     if (!mbar_wait(bar(B_QF + qb), (n >> 1) & 1, p.err)) { bad = true; break; }
@@ -471,8 +519,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             // stay in step with the ring.
             bool bad = false;
             int g0 = 0;
-            for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < p.B; t5_advance(p, pos, step)) {
-                const T5Unit U = t5_unit(p, ln, pos, tpt, ps_shift);
+            for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < nb; t5_advance(p, pos, step)) {
+                const T5Unit U = t5_unit<VARLEN>(p, ln, pos, tpt, ps_shift, g_shift);
                 for (int t = 0; t < U.n_tiles; ++t) {
                     const int g = g0 + t, st = g & 1;
                     if (!bad) {
@@ -508,14 +556,14 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
         bool bad = false;
         int n = 0, g0 = 0;
-        for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < p.B; t5_advance(p, pos, step)) {
-            const T5Unit U = t5_unit(p, ln, pos, tpt, ps_shift);
+        for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < nb; t5_advance(p, pos, step)) {
+            const T5Unit U = t5_unit<VARLEN>(p, ln, pos, tpt, ps_shift, g_shift);
             if (U.n_tiles == 0) continue;  // the epilogue warps write its rows
             const int tk = U.tok0 + (r >> g_shift);
             const bool row_valid = tk < U.tok_end;
             const int ob = n & 1;
             const uint32_t ocol = kColO + 128u * (uint32_t)ob;
-            const int lim = row_valid ? min(U.k_hi_split, t5_key_limit(p, ln, U.b, U.L, tk)) : U.k_lo;
+            const int lim = row_valid ? min(U.k_hi_split, t5_key_limit(p, ln, U.b, U.L, U.Sq, tk)) : U.k_lo;
             float m_used = kNegInf, l = 0.f;
             for (int t = 0; t < U.n_tiles; ++t) {
                 const int g = g0 + t, st = g & 1;
@@ -620,7 +668,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         // and free the O buffer for unit n + 2.  The rows leave through shared memory: each warp
         // stages its 32 rows x 128 bytes of columns (128-byte swizzle: conflict-free) and one
         // lane stores the box with TMA, so no warp issues a store per row; tokens past Sq fall
-        // outside the tensor and are clipped.  The log-sum-exp goes out with plain stores.
+        // outside the tensor and are clipped.  In a variable-length batch the next sequence's rows
+        // follow, so a warp whose rows run past its sequence's last token stores its valid rows
+        // itself (one per lane).  The log-sum-exp goes out with plain stores.
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane, r0 = q4 * 32;
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
@@ -632,34 +682,58 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                          "r"(b), "r"(c), "r"(d)
                          : "memory");
         };
+        // 16-byte chunk j of column chunk ch of my row, straight to global memory
+        auto gput16 = [&](const T5Unit &U, long long ridx, int ch, int j, uint32_t a, uint32_t b, uint32_t c,
+                          uint32_t d) {
+            uint4 *dst;
+            if constexpr (PART)
+                dst = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.out) +
+                                                ((long long)U.s * p.rows_total + ridx) * 128 + 32 * ch) + j;
+            else
+                dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + ridx * 128 + 64 * ch) + j;
+            *dst = make_uint4(a, b, c, d);
+        };
         auto stage_free = [&]() {  // the previous box has been read out of the staging rows
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
         };
-        auto store_box = [&](const T5Unit &U, int ch) {
+        auto store_box = [&](const T5Unit &U, int ch, bool direct) {
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                tma_store_4d(&tmO, stage, PART ? 32 * ch : 64 * ch, U.kvh * p.G + (r0 & (p.G - 1)),
-                             U.tok0 + (r0 >> g_shift), PART ? U.s * p.B + U.b : U.b);
+            if (lane == 0 && !direct) {
+                if constexpr (VARLEN)  // map (D, Hq, T, S): packed tokens
+                    tma_store_4d(&tmO, stage, PART ? 32 * ch : 64 * ch, U.kvh * p.G + (r0 & (p.G - 1)),
+                                 U.q0 + U.tok0 + (r0 >> g_shift), PART ? U.s : 0);
+                else  // map (D, Hq, Sq, B x S)
+                    tma_store_4d(&tmO, stage, PART ? 32 * ch : 64 * ch, U.kvh * p.G + (r0 & (p.G - 1)),
+                                 U.tok0 + (r0 >> g_shift), PART ? U.s * p.B + U.b : U.b);
                 bulk_commit_group();
             }
         };
         bool bad = false;
         int n = 0;
-        for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < p.B; t5_advance(p, pos, step)) {
-            const T5Unit U = t5_unit(p, ln, pos, tpt, ps_shift);
+        for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < nb; t5_advance(p, pos, step)) {
+            const T5Unit U = t5_unit<VARLEN>(p, ln, pos, tpt, ps_shift, g_shift);
+            if (U.skip) continue;  // another kernel's unit (variable-length batches)
             if (threadIdx.x == 384 && U.s == 0 && U.tok0 == 0 && p.seq_lens[U.b] > p.W * ps)
                 atomicOr(p.err, (unsigned int)PA_ERRBIT_SEQ_CLIPPED);
             const int tk = U.tok0 + (r >> g_shift);
             const bool row_valid = tk < U.tok_end;
-            const long long ridx = row_valid ? t5_row_index(p, U.b, U.kvh, tk, r & (p.G - 1)) : 0;
+            const long long ridx = row_valid ? t5_row_index(p, U.q0, U.kvh, tk, r & (p.G - 1)) : 0;
+            // variable-length batches: this warp's rows run past the sequence (warp-uniform)
+            const bool direct = VARLEN && U.tok0 + ((r0 + 31) >> g_shift) >= U.tok_end;
+            auto emit16 = [&](int ch, int j, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+                if (!direct) put16(j, a, b, c, d);
+                else if (row_valid) gput16(U, ridx, ch, j, a, b, c, d);
+            };
             if (U.n_tiles == 0) {  // no valid key for any row of the unit: output 0, lse -inf
-                stage_free();
-#pragma unroll
-                for (int j = 0; j < 8; ++j) put16(j, 0u, 0u, 0u, 0u);
 #pragma unroll 1
-                for (int ch = 0; ch < nch; ++ch) store_box(U, ch);
+                for (int ch = 0; ch < nch; ++ch) {
+                    stage_free();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) emit16(ch, j, 0u, 0u, 0u, 0u);
+                    store_box(U, ch, direct);
+                }
                 if (row_valid) t5_store_lse<PART>(p, U.s, ridx, kNegInf);
                 continue;
             }
@@ -685,7 +759,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                         tc05::wait_ld();
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            put16(j, __float_as_uint(__uint_as_float(u[4 * j]) * inv),
+                            emit16(ch, j, __float_as_uint(__uint_as_float(u[4 * j]) * inv),
                                   __float_as_uint(__uint_as_float(u[4 * j + 1]) * inv),
                                   __float_as_uint(__uint_as_float(u[4 * j + 2]) * inv),
                                   __float_as_uint(__uint_as_float(u[4 * j + 3]) * inv));
@@ -701,10 +775,10 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                             };
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                put16(4 * hf + j, pk(8 * j), pk(8 * j + 2), pk(8 * j + 4), pk(8 * j + 6));
+                                emit16(ch, 4 * hf + j, pk(8 * j), pk(8 * j + 2), pk(8 * j + 4), pk(8 * j + 6));
                         }
                     }
-                    store_box(U, ch);
+                    store_box(U, ch, direct);
                 }
                 if (row_valid) t5_store_lse<PART>(p, U.s, ridx, l_tot > 0.f ? m * kLn2 + logf(l_tot) : kNegInf);
             }
@@ -739,10 +813,11 @@ static int num_sms_of_current_device() {
     return cached[dev];
 }
 
-template <typename T, bool PART>
-static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, const CUtensorMap &tmk,
-                                 const CUtensorMap &tmv, const CUtensorMap &tmo, cudaStream_t stream) {
-    auto kern = paged_attn_tc05_kernel<T, PART>;
+template <typename T, bool PART, bool VARLEN>
+static cudaError_t launch_tc05_t(const FwdParams &p, long long total_q, const CUtensorMap &tmq,
+                                 const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmo,
+                                 cudaStream_t stream) {
+    auto kern = paged_attn_tc05_kernel<T, PART, VARLEN>;
     const size_t smem = tc05_smem_bytes();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -762,8 +837,16 @@ static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, con
     if ((1 << g_shift) != p.G || g_shift > 7) return cudaErrorInvalidValue;  // G must divide 128
     const int tpt = 128 >> g_shift;
     FwdParams q = p;
-    q.row_tiles = (p.Sq + tpt - 1) / tpt;
-    const long long units = (long long)p.B * p.split_kv * p.Hkv * q.row_tiles;
+    long long nb;  // values of the unit order's b digit
+    if (VARLEN && p.B > kT5StageLens) return cudaErrorInvalidValue;  // q_start must fit its stage
+    if (VARLEN) {
+        q.row_tiles = 1;
+        nb = (total_q << g_shift >> 7) + p.B;  // blocks of the packed rows (t5_first_block)
+    } else {
+        q.row_tiles = (p.Sq + tpt - 1) / tpt;
+        nb = p.B;
+    }
+    const long long units = nb * p.split_kv * p.Hkv * q.row_tiles;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int sms = num_sms_of_current_device();
@@ -772,18 +855,31 @@ static cudaError_t launch_tc05_t(const FwdParams &p, const CUtensorMap &tmq, con
     const bool bf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t iqk = tc05::idesc_f16(bf, false, 128, 128);
     const uint32_t ipv = tc05::idesc_f16(bf, true, 128, 128);
-    kern<<<grid, kT5Threads, smem, stream>>>(tmq, tmk, tmv, tmo, q, tpt, ps_shift, g_shift, iqk, ipv);
+    kern<<<grid, kT5Threads, smem, stream>>>(tmq, tmk, tmv, tmo, q, tpt, ps_shift, g_shift, iqk, ipv, (int)nb);
     return cudaGetLastError();
+}
+
+template <bool VARLEN>
+static cudaError_t launch_tc05_any(const FwdParams &p, long long total_q, int dtype, const CUtensorMap &tmq,
+                                   const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmo,
+                                   cudaStream_t stream) {
+    const bool part = p.split_kv > 1;
+    if (dtype == PA_BF16)
+        return part ? launch_tc05_t<__nv_bfloat16, true, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, stream)
+                    : launch_tc05_t<__nv_bfloat16, false, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, stream);
+    return part ? launch_tc05_t<__half, true, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, stream)
+                : launch_tc05_t<__half, false, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, stream);
 }
 
 cudaError_t launch_tc05(const FwdParams &p, int dtype, const CUtensorMap &tmq, const CUtensorMap &tmk,
                         const CUtensorMap &tmv, const CUtensorMap &tmo, cudaStream_t stream) {
-    const bool part = p.split_kv > 1;
-    if (dtype == PA_BF16)
-        return part ? launch_tc05_t<__nv_bfloat16, true>(p, tmq, tmk, tmv, tmo, stream)
-                    : launch_tc05_t<__nv_bfloat16, false>(p, tmq, tmk, tmv, tmo, stream);
-    return part ? launch_tc05_t<__half, true>(p, tmq, tmk, tmv, tmo, stream)
-                : launch_tc05_t<__half, false>(p, tmq, tmk, tmv, tmo, stream);
+    return launch_tc05_any<false>(p, 0, dtype, tmq, tmk, tmv, tmo, stream);
+}
+
+cudaError_t launch_tc05_varlen(const FwdParams &p, long long total_q, int dtype, const CUtensorMap &tmq,
+                               const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmo,
+                               cudaStream_t stream) {
+    return launch_tc05_any<true>(p, total_q, dtype, tmq, tmk, tmv, tmo, stream);
 }
 
 }  // namespace pa

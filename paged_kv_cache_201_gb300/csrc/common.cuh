@@ -40,6 +40,8 @@ struct FwdParams {
     int causal, split_kv;
     float scale_log2;          // scale * log2(e)
     int row_tiles;             // query-row tiles per (sequence, kv head, split)
+    int varlen_rows_cap;       // variable-length one-grid kernel: skip sequences with at least this many
+                               // query rows (another kernel takes them); 0: take every sequence
 };
 
 // ------------------------------------------------------------------ small helpers

@@ -110,10 +110,11 @@ def test_mixed_batch_offsets_and_noncausal(pa):
     assert pa.paged_attn_last_error_word() == 0
 
 
-@pytest.mark.parametrize("q_len,variant", [(1, 2), (3, 2), (37, 3)])
+@pytest.mark.parametrize("q_len,variant", [(1, 2), (3, 2), (37, 4)])
 def test_uniform_batch_bit_identical(pa, q_len, variant):
-    """Every sequence with the same query count: the unified launch equals the uniform tensor-core
-    kernel (16-row decode units, or 64-row tiles) bit for bit."""
+    """Every sequence with the same query count: the variable-length launch equals the uniform
+    kernel bit for bit (16-row decode units for 4-12 rows; the tcgen05 kernel's 128-row tiles for
+    148 rows, whose last tile runs past each sequence)."""
     import torch
     wl = W.make_custom(dtype="bf16", B=5, Sq=q_len, Hq=32, Hkv=8, D=128, page_size=16,
                        seq_lens=[64, 200, 500, 37, 1000], causal=True, seed=9)
@@ -129,15 +130,17 @@ def test_uniform_batch_bit_identical(pa, q_len, variant):
     del torch
 
 
-def test_bad_q_start_is_reported(pa):
+@pytest.mark.parametrize("D,q_lens", [(64, [2, 3, 4]), (128, [20, 30, 40])])
+def test_bad_q_start_is_reported(pa, D, q_lens):
     """A q_start entry past the packed tokens: that sequence is skipped (its rows untouched), the
-    others are exact, and the error word says so."""
+    others are exact, and the error word says so (short sequences: one-grid kernel; 80-160 rows at
+    head dim 128: tcgen05 kernel)."""
     import torch
-    wl = W.make_varlen(dtype="bf16", Hq=8, Hkv=2, D=64, page_size=16, seed=3, q_lens=[2, 3, 4],
-                       seq_lens=[40, 50, 60])
+    wl = W.make_varlen(dtype="bf16", Hq=8, Hkv=2, D=D, page_size=16, seed=3, q_lens=q_lens,
+                       seq_lens=[q + 40 for q in q_lens])
     d = _device(wl)
     bad = d["qs"].clone()
-    bad[2] = 1000  # sequence 1 ends, and sequence 2 starts, past T = 9
+    bad[2] = 1000  # sequence 1 ends, and sequence 2 starts, past T
     out = torch.full_like(d["q"], 7.0)
     lse = torch.empty((wl.Sq, wl.Hq), dtype=torch.float32, device="cuda")
     pa.paged_attn_fwd_varlen(d["q"], d["k"], d["v"], d["bt"], d["sl"], bad, True, None, 1, wl.scale, out, lse)
@@ -145,8 +148,28 @@ def test_bad_q_start_is_reported(pa):
     assert pa.paged_attn_last_error_word() & pa.ERRBIT_QSTART
     ref = _oracle(wl, 1)
     got = _gpu.to_f64(out, "bf16")
-    _gpu.assert_close(got[0:2], ref["out"][0:2], "bf16", "sequence 0")
-    assert np.all(got[2:] == 7.0)
+    q0 = q_lens[0]
+    _gpu.assert_close(got[0:q0], ref["out"][0:q0], "bf16", "sequence 0")
+    assert np.all(got[q0:] == 7.0)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (16, 16), (64, 4)])
+@pytest.mark.parametrize("S", [1, 3])
+def test_long_sequences_on_tcgen05(pa, Hq, Hkv, S):
+    """Head dim 128, bf16: sequences of at least 64 query rows run on the tcgen05 kernel, the rest on
+    the one-grid kernel.  Row counts on both sides of 64, last tiles that end inside an epilogue
+    warp's rows (those rows are stored one per lane), sequences spanning several tiles, an empty
+    sequence, explicit offsets that hide every key from the first rows of one sequence."""
+    G = Hq // Hkv
+    q_lens = [64 // G, 64 // G - 1, 1, 0, 333 // G + 5, 129, 5, 2 * (128 // G) + 1]
+    qo = [40, 7, 300, 0, -3, 500, 12, 64]
+    seq_lens = [max(o, 0) + q for o, q in zip(qo, q_lens)]
+    wl = W.make_varlen(dtype="bf16", Hq=Hq, Hkv=Hkv, D=128, page_size=16, q_offset=qo, seed=90 + G + S,
+                       q_lens=q_lens, seq_lens=seq_lens)
+    res = _run(pa, wl, _device(wl), S)
+    ref = _oracle(wl, S)
+    _compare(res, ref, wl, S, f"tcgen05 varlen G={G} S={S}")
+    assert pa.paged_attn_last_error_word() == 0
 
 
 # ----------------------------------------------------------------------------- full size
