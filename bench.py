@@ -187,7 +187,9 @@ KERNEL_SOURCES = {
     "paged_attn_mma_kernel": ("attn_mma.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
     "paged_attn_kvq_decode_kernel": ("attn_mma_kvq.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
     "paged_attn_kvq_prefill_kernel": ("attn_mma_kvq.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
-    "paged_attn_mma_varlen_kernel": ("attn_mma.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
+    # the variable-length call: the tcgen05 kernel (long sequences) and the one-grid kernel
+    "paged_attn_mma_varlen_kernel": ("attn_mma.cu", "mma_common.cuh", "attn_tc05.cu", "tc05.cuh", "common.cuh",
+                                     "kernels.h"),
     "paged_attn_mma_t_kernel": ("attn_mma_t.cu", "mma_common.cuh", "common.cuh", "kernels.h"),
     "paged_attn_tc05_kernel": ("attn_tc05.cu", "tc05.cuh", "common.cuh", "kernels.h"),
     "paged_attn_simt_kernel": ("attn_simt.cu", "common.cuh", "kernels.h"),
