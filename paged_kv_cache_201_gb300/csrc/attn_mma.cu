@@ -389,7 +389,9 @@ __device__ __forceinline__ int varlen_sequence(const FwdParams &p, long long t, 
 // 16-row decode unit (sequences with at most 16 query rows) or a 64-row prefill tile.  Units are
 // visited in the order u -> u * p.row_tiles mod gridDim.x (p.row_tiles coprime to the grid), which
 // spreads each sequence's units over the whole launch: the prefill tiles (tensor-bound) then run
-// beside the decode units (HBM-bound) instead of in a phase of their own.
+// beside the decode units (HBM-bound) instead of in a phase of their own.  With a row cap
+// (p.varlen_rows_cap: the tcgen05 kernel takes the sequences of that many rows or more) every
+// sequence left fits one block, block t is sequence t, and the order is plain (row_tiles = 1).
 template <typename T, int D, int NSTAGE>
 __global__ void __launch_bounds__(kMmaThreads, (NSTAGE <= 3 ? 2 : 1))
     paged_attn_mma_varlen_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
