@@ -200,7 +200,7 @@ int paged_attn_fwd_splitkv_noalloc(const void *q, const void *k_cache, const voi
                                    const pa_dims *dims, int num_sms, int64_t device_bytes, void *stream);
 
 /*
- * paged_attn_fwd_varlen — one launch over a batch whose sequences have different numbers of query
+ * paged_attn_fwd_varlen — one call over a batch whose sequences have different numbers of query
  * tokens: decode sequences (one new token) next to prefill chunks.  The pages' rocKE entry point
  * serves such batches ("run_unified_attention_torch", rocm-libraries PR #14349, Performance); the
  * layout below is this library's.
@@ -214,7 +214,10 @@ int paged_attn_fwd_splitkv_noalloc(const void *q, const void *k_cache, const voi
  *            paged_attn_combine with rows = T * Hq.  lse [T, Hq] or [S, T, Hq] (as paged_attn_fwd).
  * dims->dtype is PA_BF16 or PA_F16 (PA_F32: PA_EDTYPE); every other rule is paged_attn_fwd's.
  * Sequences of at most 16 query rows (tokens x Hq/Hkv) run as decode units and longer ones as
- * 64-row tiles of the same grid.  If q_start[b] or q_start[b + 1] lies outside [0, T], or
+ * 64-row tiles of the same grid; at head_dim 128 with Hq/Hkv dividing 128, scale > 0 and at most
+ * 1024 sequences, those of 64 query rows or more run instead in 128-row tcgen05 tiles, a second
+ * launch on the same stream (both kernels find their sequences from q_start on the device, so
+ * the host never reads it).  If q_start[b] or q_start[b + 1] lies outside [0, T], or
  * q_start[b + 1] < q_start[b], sequence b is skipped (its rows are not written) and
  * PA_ERRBIT_QSTART is set; other malformed arrays give unspecified values but no access outside
  * the buffers.
