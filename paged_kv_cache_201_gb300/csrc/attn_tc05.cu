@@ -21,10 +21,14 @@
 //               2^8 (otherwise the stale max is kept), and the -inf - (-inf) guard of rocMLIR
 //               PR #2371 applies.  At a unit's end they hand its row maximum and sum over.
 //   warps 12-15 epilogue: one thread per query row reads the unit's O out of TMEM, divides by the
-//               row sum (0/0 guard), and stores the output row and its log-sum-exp, while the
-//               softmax warps already work on the next unit.
+//               row sum (0/0 guard), stages the rows in shared memory and stores them with TMA (the
+//               log-sum-exp with plain stores), while the softmax warps already work on the next
+//               unit.
 // The register file is split with setmaxnreg: 64 per thread for warps 0-3, 176 for the softmax
 // warpgroups, 96 for the epilogue (128 x (64 + 2 x 176 + 96) = the 65536 of a 512 x 128 launch).
+// Instantiations: PART (split_kv > 1's fp32 partials, or the final rows) x VARLEN (a batch of
+// sequences with their own query counts, whose units are blocks of the packed rows).  The row
+// maximum is taken over unscaled scores, so the host launches this kernel only for scale > 0.
 #include <type_traits>
 
 #include "kernels.h"
