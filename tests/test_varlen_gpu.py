@@ -1,9 +1,10 @@
-"""GPU parity of the variable-length entry point (decode and prefill sequences in one grid) against
+"""GPU parity of the variable-length entry point (decode and prefill sequences in one call) against
 the oracle's variable-length evaluation (each sequence as a batch of one).
 
 Bars as everywhere: bf16/f16 atol=2e-3, rtol=2^-8, -inf patterns exact, no NaN.  On a batch whose
-sequences all have the same query count, the unified launch runs the same per-unit code as the
-uniform entry point's tensor-core kernel, so the two agree bit for bit.
+sequences all have the same query count, the variable-length call runs the same per-unit code as
+the uniform entry point's kernel for that shape (the tcgen05 kernel for 64 rows or more, the
+tensor-core decode units below), so the two agree bit for bit.
 """
 import numpy as np
 import pytest
@@ -86,7 +87,7 @@ MIXED = dict(q_lens=[1, 0, 4, 1, 40, 3, 17, 1, 100], seq_lens=[300, 50, 4, 1000,
 @pytest.mark.parametrize("dtype,D,Hq,Hkv", [("bf16", 128, 32, 8), ("f16", 64, 16, 2), ("bf16", 128, 16, 16)])
 @pytest.mark.parametrize("S", [1, 3])
 def test_mixed_batch(pa, dtype, D, Hq, Hkv, S):
-    """Decode sequences (1-4 tokens), empty ones and prefill chunks (17-100 tokens) in one launch,
+    """Decode sequences (1-4 tokens), empty ones and prefill chunks (17-100 tokens) in one call,
     causal with the default offsets (queries are each sequence's newest tokens)."""
     wl = W.make_varlen(dtype=dtype, Hq=Hq, Hkv=Hkv, D=D, page_size=16, seed=40 + D + Hq, **MIXED)
     res = _run(pa, wl, _device(wl), S)
