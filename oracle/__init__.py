@@ -23,6 +23,8 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
 KV_FP8E4M3 = 3
+KV_INT8 = 4
+KV_CODE = {"fp8e4m3": KV_FP8E4M3, "int8": KV_INT8}
 OK, EINVAL, EBOUNDS, ENOMEM = 0, -1, -5, -6
 
 
@@ -205,9 +207,9 @@ def workload_rows(wl, split_kv: int = 1, row_bih=None, n_threads: int = 0, want_
 
 # ----------------------------------------------------------------------------- quantized pools
 def gather_kvq(cache_bits: np.ndarray, scales: np.ndarray, block_table, seq_lens, dims: Dims, b: int,
-               lib=None) -> np.ndarray:
-    """Dequantized logical rows of sequence b from an FP8 E4M3 pool (uint8 bits) with
-    [num_pages, Hkv] float32 scales: float64 [L_b, Hkv, D]."""
+               lib=None, kv_dtype: str = "fp8e4m3") -> np.ndarray:
+    """Dequantized logical rows of sequence b from a quantized pool (uint8 bits of FP8 E4M3 or
+    int8 elements, ``kv_dtype``) with [num_pages, Hkv] float32 scales: float64 [L_b, Hkv, D]."""
     lib = lib or load()
     c = np.ascontiguousarray(cache_bits, dtype=np.uint8)
     sc = np.ascontiguousarray(scales, dtype=np.float32)
@@ -215,7 +217,7 @@ def gather_kvq(cache_bits: np.ndarray, scales: np.ndarray, block_table, seq_lens
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     L = max(int(sl[b]), 0)
     out = np.zeros((L, dims.Hkv, dims.D), dtype=np.float64)
-    rc = lib.oracle_gather_kvq(_ptr(c), KV_FP8E4M3, _ptr(sc), _ptr(bt), _ptr(sl), ctypes.byref(dims), b, _ptr(out))
+    rc = lib.oracle_gather_kvq(_ptr(c), KV_CODE[kv_dtype], _ptr(sc), _ptr(bt), _ptr(sl), ctypes.byref(dims), b, _ptr(out))
     if rc != OK:
         raise ValueError(f"oracle_gather_kvq failed: {rc}")
     return out
@@ -223,9 +225,9 @@ def gather_kvq(cache_bits: np.ndarray, scales: np.ndarray, block_table, seq_lens
 
 def rows_kvq(*, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, causal: bool, dims: Dims,
              scale: float, split_kv: int = 1, row_bih: Optional[np.ndarray] = None, n_threads: int = 0,
-             want_split: bool = True, lib=None) -> dict:
-    """``rows`` with FP8 E4M3 K/V pools (uint8 bits) and [num_pages, Hkv] float32 scales per pool;
-    q is float32 / uint16 bits of dims.dtype as in ``rows``."""
+             want_split: bool = True, lib=None, kv_dtype: str = "fp8e4m3") -> dict:
+    """``rows`` with quantized K/V pools (uint8 bits of FP8 E4M3 or int8 elements, ``kv_dtype``) and
+    [num_pages, Hkv] float32 scales per pool; q is float32 / uint16 bits of dims.dtype as in ``rows``."""
     lib = lib or load()
     dt = {v: k for k, v in DTYPE_CODE.items()}[dims.dtype]
     qe = _elems(q, dt)
@@ -245,7 +247,7 @@ def rows_kvq(*, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_
     if want_split:
         res.update(part_out=np.zeros((n, S, D)), part_lse=np.zeros((n, S)), comb_out=np.zeros((n, D)),
                    comb_lse=np.zeros((n,)))
-    rc = lib.oracle_rows_kvq(_ptr(qe), _ptr(ke), _ptr(ve), KV_FP8E4M3, _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl),
+    rc = lib.oracle_rows_kvq(_ptr(qe), _ptr(ke), _ptr(ve), KV_CODE[kv_dtype], _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl),
                              _ptr(qo), int(causal), ctypes.byref(dims), float(scale), S, _ptr(rb), _ptr(ri),
                              _ptr(rh), n, n_threads, _ptr(res["out"]), _ptr(res["lse"]), _ptr(res.get("part_out")),
                              _ptr(res.get("part_lse")), _ptr(res.get("comb_out")), _ptr(res.get("comb_lse")))
@@ -256,13 +258,15 @@ def rows_kvq(*, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_
 
 def workload_rows_kvq(wl, split_kv: int = 1, row_bih=None, n_threads: int = 0, want_split: bool = True,
                       k_cache=None, v_cache=None, k_scale=None, v_scale=None, lib=None) -> dict:
-    """``rows_kvq`` on an object with the workload attributes (pools as uint8 E4M3 bits + scales)."""
+    """``rows_kvq`` on an object with the workload attributes (pools as uint8 bits + scales; the
+    element format is the workload's ``kv_dtype``)."""
     return rows_kvq(q=wl.q, k_cache=wl.k_cache if k_cache is None else k_cache,
                     v_cache=wl.v_cache if v_cache is None else v_cache,
                     k_scale=wl.k_scale if k_scale is None else k_scale,
                     v_scale=wl.v_scale if v_scale is None else v_scale, block_table=wl.block_table,
                     seq_lens=wl.seq_lens, q_offset=wl.q_offset, causal=wl.causal, dims=dims_of(wl), scale=wl.scale,
-                    split_kv=split_kv, row_bih=row_bih, n_threads=n_threads, want_split=want_split, lib=lib)
+                    split_kv=split_kv, row_bih=row_bih, n_threads=n_threads, want_split=want_split, lib=lib,
+                    kv_dtype=wl.kv_dtype)
 
 
 # ----------------------------------------------------------------------------- variable-length batches

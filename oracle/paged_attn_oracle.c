@@ -31,8 +31,9 @@
  *   - a split's partial output is normalised by its own sum; a split with no
  *     valid key yields output 0 and lse -inf;
  *   - quantized pools (the pages' sweeps include i8 attention: rocMLIR PR #2222,
- *     reviewed files; rocMLIR PR #2371, Motivation) are read as FP8 E4M3
- *     elements with one float scale per (page, kv head): value = element x scale.
+ *     reviewed files; rocMLIR PR #2371, Motivation) are read as FP8 E4M3 or as
+ *     two's-complement int8 elements with one float scale per (page, kv head):
+ *     value = element x scale.
  *
  * Everything is evaluated from the definition: scores in double, the maximum
  * over all valid keys, then exp, sum and weighted sum.  No online rescaling,
@@ -46,7 +47,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_FP8E4M3 = 3 };
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_FP8E4M3 = 3, ORACLE_INT8 = 4 };
 enum { ORACLE_OK = 0, ORACLE_EINVAL = -1, ORACLE_EBOUNDS = -5, ORACLE_ENOMEM = -6 };
 
 /* Shape of one problem.  Layouts (all dense, row-major):
@@ -103,8 +104,16 @@ static double e4m3_bits_to_double(uint8_t h)
     return sign ? -v : v;
 }
 
+/* int8 (two's complement: bit 7 weighs -128) -> double. */
+static double int8_bits_to_double(uint8_t h)
+{
+    return (double)(h & 0x7F) - ((h & 0x80) ? 128.0 : 0.0);
+}
+
 static double widen(const void *base, int dtype, int64_t idx)
 {
+    if (dtype == ORACLE_INT8)
+        return int8_bits_to_double(((const uint8_t *)base)[idx]);
     if (dtype == ORACLE_FP8E4M3)
         return e4m3_bits_to_double(((const uint8_t *)base)[idx]);
     if (dtype == ORACLE_F32)
@@ -443,7 +452,7 @@ int oracle_rows(const void *q, const void *k_cache, const void *v_cache, const i
                      n_rows, n_threads, out, lse, part_out, part_lse, comb_out, comb_lse);
 }
 
-/* The same with quantized K/V pools: elements of kv_dtype (ORACLE_FP8E4M3) times the float scale
+/* The same with quantized K/V pools: elements of kv_dtype (ORACLE_FP8E4M3 or ORACLE_INT8) times the float scale
  * of their (page, kv head), k_scale / v_scale [num_pages, Hkv]; q and the results as in oracle_rows. */
 int oracle_rows_kvq(const void *q, const void *k_cache, const void *v_cache, int32_t kv_dtype,
                     const float *k_scale, const float *v_scale, const int32_t *block_table,
@@ -452,7 +461,7 @@ int oracle_rows_kvq(const void *q, const void *k_cache, const void *v_cache, int
                     const int32_t *row_h, int64_t n_rows, int32_t n_threads, double *out, double *lse,
                     double *part_out, double *part_lse, double *comb_out, double *comb_lse)
 {
-    if (!dims_ok(d) || kv_dtype != ORACLE_FP8E4M3 || !k_scale || !v_scale)
+    if (!dims_ok(d) || (kv_dtype != ORACLE_FP8E4M3 && kv_dtype != ORACLE_INT8) || !k_scale || !v_scale)
         return ORACLE_EINVAL;
     const oracle_kv kv = {k_cache, v_cache, kv_dtype, k_scale, v_scale};
     return rows_impl(q, &kv, block_table, seq_lens, q_offset, causal, d, scale, split_kv, row_b, row_i, row_h,
@@ -463,7 +472,7 @@ int oracle_rows_kvq(const void *q, const void *k_cache, const void *v_cache, int
 int oracle_gather_kvq(const void *cache, int32_t kv_dtype, const float *scales, const int32_t *block_table,
                       const int32_t *seq_lens, const oracle_dims *d, int32_t b, double *out)
 {
-    if (!dims_ok(d) || b < 0 || b >= d->B || kv_dtype != ORACLE_FP8E4M3 || !scales)
+    if (!dims_ok(d) || b < 0 || b >= d->B || (kv_dtype != ORACLE_FP8E4M3 && kv_dtype != ORACLE_INT8) || !scales)
         return ORACLE_EINVAL;
     const oracle_kv kv = {cache, cache, kv_dtype, scales, scales};
     int64_t L = seq_lens[b] > 0 ? seq_lens[b] : 0;

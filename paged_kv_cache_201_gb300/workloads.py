@@ -82,7 +82,8 @@ class Workload:
     k_cache: Optional[np.ndarray] = None    # [P, ps, Hkv, D] (host) or None if device-drawn
     v_cache: Optional[np.ndarray] = None
     device_cache_seed: Optional[int] = None  # set when the pools are drawn on the device
-    kv_dtype: Optional[str] = None           # "fp8e4m3": pools hold E4M3 bits (uint8) with per-page scales
+    kv_dtype: Optional[str] = None           # "fp8e4m3" / "int8": pools hold 8-bit elements (uint8 bits)
+                                             # with per-(page, kv head) scales
     k_scale: Optional[np.ndarray] = None     # float32 [num_pages, Hkv] (quantized pools only)
     v_scale: Optional[np.ndarray] = None
     # variable-length batches: q is [T, Hq, D] packed and Sq = T; sequence b's query tokens are
@@ -115,7 +116,7 @@ class Workload:
 
     @property
     def kv_esize(self) -> int:
-        return 1 if self.kv_dtype == "fp8e4m3" else ESIZE[self.dtype]
+        return 1 if self.kv_dtype in QUANT_KV else ESIZE[self.dtype]
 
 
 def _pack_tables(B: int, W: int, nblk: Sequence[int], pages: np.ndarray, tail: int) -> np.ndarray:
@@ -310,7 +311,9 @@ def fill_device_cache(wl: Workload, device="cuda", chunk: int = 1 << 27):
 
 
 # ----------------------------------------------------------------------------- quantized pools
+QUANT_KV = ("fp8e4m3", "int8")  # 8-bit pool element formats
 E4M3_MAX = 448.0
+INT8_MAX = 127.0
 
 
 def quantize_pool_e4m3(x: np.ndarray):
@@ -326,6 +329,28 @@ def quantize_pool_e4m3(x: np.ndarray):
     return bits.numpy().copy(), scale
 
 
+def quantize_pool_int8(x: np.ndarray):
+    """Quantize a float32 pool [P, ps, Hkv, D] to int8 with one scale per (page, kv head):
+    scale = max |x| / 127 over the page's rows of that head (1 where the block is all zero), and
+    the stored element is x / scale rounded to the nearest integer (ties to even), within
+    [-127, 127].  Returns (uint8 bits [P, ps, Hkv, D], float32 scales [P, Hkv])."""
+    amax = np.abs(x).max(axis=(1, 3))                            # [P, Hkv]
+    scale = np.where(amax > 0, amax / INT8_MAX, 1.0).astype(np.float32)
+    y = np.rint(x.astype(np.float32) / scale[:, None, :, None])
+    q = np.clip(y, -INT8_MAX, INT8_MAX).astype(np.int8)
+    return q.view(np.uint8).copy(), scale
+
+
+def int8_bits_to_float(bits: np.ndarray) -> np.ndarray:
+    """int8 bits (uint8 storage) -> float64 values by numpy's reinterpretation (a library routine)."""
+    return np.ascontiguousarray(bits, dtype=np.uint8).view(np.int8).astype(np.float64)
+
+
+def q8_bits_to_float(bits: np.ndarray, kv_dtype: str) -> np.ndarray:
+    """Element values of a quantized pool's bits (without the scales)."""
+    return e4m3_bits_to_float(bits) if kv_dtype == "fp8e4m3" else int8_bits_to_float(bits)
+
+
 def e4m3_bits_to_float(bits: np.ndarray) -> np.ndarray:
     """E4M3 bits -> float64 values by torch's conversion (a library routine)."""
     import torch
@@ -333,18 +358,31 @@ def e4m3_bits_to_float(bits: np.ndarray) -> np.ndarray:
     return t.to(torch.float64).numpy()
 
 
-def make_custom_fp8(**kw) -> Workload:
-    """``make_custom`` (bf16 or f16 queries) whose K/V pools are then quantized to FP8 E4M3 with
-    per-(page, kv head) scales (``quantize_pool_e4m3``) from the same N(0,1) draws, in float32."""
+def make_custom_q8(kv_dtype: str = "fp8e4m3", **kw) -> Workload:
+    """``make_custom`` (bf16 or f16 queries) whose K/V pools are then quantized to ``kv_dtype``
+    (FP8 E4M3 or int8) with per-(page, kv head) scales (``quantize_pool_e4m3`` /
+    ``quantize_pool_int8``) from the same N(0,1) draws, in float32."""
+    assert kv_dtype in QUANT_KV
     dtype = kw.pop("dtype", "bf16")
     assert dtype in ("bf16", "f16")
     wl = make_custom(dtype="f32", **kw)
     rng = np.random.default_rng(kw.get("seed", 0) + 7919)
     q = _normal_elems(rng, wl.q.size, dtype).reshape(wl.q.shape)
-    kb, ks = quantize_pool_e4m3(wl.k_cache)
-    vb, vs = quantize_pool_e4m3(wl.v_cache)
-    return Workload(**{**wl.__dict__, "name": kw.get("name", "custom_fp8"), "dtype": dtype, "q": q,
-                       "k_cache": kb, "v_cache": vb, "kv_dtype": "fp8e4m3", "k_scale": ks, "v_scale": vs})
+    quant = quantize_pool_e4m3 if kv_dtype == "fp8e4m3" else quantize_pool_int8
+    kb, ks = quant(wl.k_cache)
+    vb, vs = quant(wl.v_cache)
+    return Workload(**{**wl.__dict__, "name": kw.get("name", f"custom_{kv_dtype}"), "dtype": dtype, "q": q,
+                       "k_cache": kb, "v_cache": vb, "kv_dtype": kv_dtype, "k_scale": ks, "v_scale": vs})
+
+
+def make_custom_fp8(**kw) -> Workload:
+    """``make_custom_q8`` with FP8 E4M3 pools."""
+    return make_custom_q8("fp8e4m3", **kw)
+
+
+def make_custom_int8(**kw) -> Workload:
+    """``make_custom_q8`` with int8 pools."""
+    return make_custom_q8("int8", **kw)
 
 
 def llama8b_decode_fp8(seed: int = 1006, B: int = 256) -> Workload:
@@ -357,11 +395,24 @@ def llama8b_decode_fp8(seed: int = 1006, B: int = 256) -> Workload:
 CONFIGS["llama8b_decode_fp8"] = llama8b_decode_fp8
 
 
-def fill_device_cache_fp8(wl: Workload, device="cuda", pages_per_chunk: int = 4096):
-    """Draw the K and V pools on the device (seeded torch.randn, float32) and quantize them to E4M3
-    with per-(page, kv head) scales max|x| / 448.  Returns (k_bits, v_bits, k_scale, v_scale)."""
+def llama8b_decode_int8(seed: int = 1011, B: int = 256) -> Workload:
+    """The Llama-3-8B-shaped decode with int8 pools (1 GiB each) and per-(page, kv head) scales;
+    pools and scales are drawn on the device (``fill_device_cache_q8``)."""
+    wl = llama8b_decode(seed=seed, B=B)
+    return Workload(**{**wl.__dict__, "name": "llama8b_decode_int8", "kv_dtype": "int8"})
+
+
+CONFIGS["llama8b_decode_int8"] = llama8b_decode_int8
+
+
+def fill_device_cache_q8(wl: Workload, device="cuda", pages_per_chunk: int = 4096):
+    """Draw the K and V pools on the device (seeded torch.randn, float32) and quantize them to the
+    workload's 8-bit format with per-(page, kv head) scales: max|x| / 448 and torch's E4M3 cast, or
+    max|x| / 127 and rounding to the nearest integer (ties to even).  Returns (k_bits, v_bits,
+    k_scale, v_scale)."""
     import torch
-    assert wl.device_cache_seed is not None and wl.kv_dtype == "fp8e4m3"
+    assert wl.device_cache_seed is not None and wl.kv_dtype in QUANT_KV
+    fp8 = wl.kv_dtype == "fp8e4m3"
     out = []
     for which in (0, 1):
         g = torch.Generator(device=device)
@@ -372,8 +423,12 @@ def fill_device_cache_fp8(wl: Workload, device="cuda", pages_per_chunk: int = 40
             p1 = min(wl.num_pages, p0 + pages_per_chunk)
             x = torch.randn((p1 - p0,) + wl.cache_shape[1:], generator=g, device=device, dtype=torch.float32)
             amax = x.abs().amax(dim=(1, 3))
-            sc = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
-            bits[p0:p1] = (x / sc[:, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+            sc = torch.where(amax > 0, amax / (E4M3_MAX if fp8 else INT8_MAX), torch.ones_like(amax))
+            y = x / sc[:, None, :, None]
+            if fp8:
+                bits[p0:p1] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+            else:
+                bits[p0:p1] = torch.round(y).clamp_(-INT8_MAX, INT8_MAX).to(torch.int8).view(torch.uint8)
             scales[p0:p1] = sc
         out += [bits, scales]
     return out[0], out[2], out[1], out[3]

@@ -376,4 +376,56 @@ def pin_kvq_power_of_two_scales(lib):
         assert np.array_equal(rq[key], rp[key]), key
 
 
+def pin_int8_all_codes(lib):
+    """Every int8 code decodes as two's complement (numpy's reinterpretation for reference;
+    hand-checked anchors: 0x00 = 0, 0x01 = 1, 0x7F = 127, 0x80 = -128, 0x81 = -127, 0xFF = -1)."""
+    codes = np.arange(256, dtype=np.uint8)
+    d = oracle.make_dims(B=1, Sq=1, Hq=1, Hkv=1, D=1, page_size=1, bt_stride=256, dtype="bf16", num_pages=256)
+    got = oracle.gather_kvq(codes.reshape(256, 1, 1, 1), np.ones((256, 1), np.float32),
+                            np.arange(256, dtype=np.int32).reshape(1, -1), np.array([256], dtype=np.int32), d, 0,
+                            lib=lib, kv_dtype="int8")[:, 0, 0]
+    assert np.array_equal(got, W.int8_bits_to_float(codes))
+    for code, val in ((0x00, 0.0), (0x01, 1.0), (0x7F, 127.0), (0x80, -128.0), (0x81, -127.0), (0xFF, -1.0)):
+        assert got[code] == val, (hex(code), got[code])
+
+
+def _int8_small(seed=95, **kw):
+    base = dict(B=3, Sq=2, Hq=8, Hkv=2, D=16, page_size=4, seq_lens=[13, 4, 21], num_pages=16, W=6,
+                causal=True, seed=seed)
+    base.update(kw)
+    return W.make_custom_int8(**base)
+
+
+def pin_int8_power_of_two_scales_equal_unquantized(lib):
+    """int8 pools with power-of-two scales give bit-identical results to bf16 pools holding
+    element x scale (every such value is a bf16 number: at most 8 significant bits)."""
+    wl = _int8_small()
+    rng = np.random.default_rng(96)
+    ks = (2.0 ** rng.integers(-6, 7, size=wl.k_scale.shape)).astype(np.float32)
+    vs = (2.0 ** rng.integers(-6, 7, size=wl.v_scale.shape)).astype(np.float32)
+    rq = oracle.workload_rows_kvq(wl, split_kv=3, k_scale=ks, v_scale=vs, lib=lib)
+    kb = W.bf16_bits_rne((W.int8_bits_to_float(wl.k_cache) * ks[:, None, :, None]).astype(np.float32))
+    vb = W.bf16_bits_rne((W.int8_bits_to_float(wl.v_cache) * vs[:, None, :, None]).astype(np.float32))
+    assert np.array_equal(bf.widen(kb, "bf16"), W.int8_bits_to_float(wl.k_cache) * ks[:, None, :, None])
+    assert (W.int8_bits_to_float(wl.k_cache) < 0).any() and (W.int8_bits_to_float(wl.v_cache) < 0).any()
+    plain = W.Workload(**{**wl.__dict__, "k_cache": kb, "v_cache": vb, "kv_dtype": None})
+    rp = oracle.workload_rows(plain, split_kv=3, lib=lib)
+    for key in rq:
+        assert np.array_equal(rq[key], rp[key]), key
+
+
+def pin_int8_bruteforce(lib):
+    """int8 pools with per-(page, kv head) scales on shuffled pages agree with dense fp64 attention
+    on the dequantized pools (1e-12)."""
+    for wl in (_int8_small(), _int8_small(seed=97, B=2, Sq=1, Hq=6, Hkv=3, D=8, seq_lens=[9, 16], causal=False,
+                                          num_pages=7, W=4)):
+        kd = W.int8_bits_to_float(wl.k_cache) * wl.k_scale[:, None, :, None].astype(np.float64)
+        vd = W.int8_bits_to_float(wl.v_cache) * wl.v_scale[:, None, :, None].astype(np.float64)
+        ref_out, ref_lse = bf.attention(wl, k_cache=kd, v_cache=vd, kv_dtype="f64")
+        r = oracle.workload_rows_kvq(wl, split_kv=1, want_split=False, lib=lib)
+        np.testing.assert_allclose(r["out"].reshape(ref_out.shape), ref_out, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(r["lse"].reshape(ref_lse.shape), ref_lse, rtol=1e-12, atol=1e-12)
+        assert len(np.unique(wl.k_scale)) > 4
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

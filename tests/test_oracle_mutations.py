@@ -64,6 +64,15 @@ MUTATIONS = {
     "e4m3_bias": ("v = ldexp((double)(8 + m), e - 10);", "v = ldexp((double)(8 + m), e - 11);"),
     # E4M3 subnormals scaled wrong
     "e4m3_subnormal": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    # int8 read as unsigned
+    "int8_unsigned": ("return (double)(h & 0x7F) - ((h & 0x80) ? 128.0 : 0.0);",
+                      "return (double)(h & 0x7F) + ((h & 0x80) ? 128.0 : 0.0);"),
+    # int8 read as sign-magnitude
+    "int8_sign_magnitude": ("return (double)(h & 0x7F) - ((h & 0x80) ? 128.0 : 0.0);",
+                            "return (h & 0x80) ? -(double)(h & 0x7F) : (double)(h & 0x7F);"),
+    # int8 pools decoded as E4M3
+    "int8_as_e4m3": ("return int8_bits_to_double(((const uint8_t *)base)[idx]);",
+                     "return e4m3_bits_to_double(((const uint8_t *)base)[idx]);"),
     # page ids not range checked
     "no_page_range_check": ("if (page < 0 || (int64_t)page >= d->num_pages)", "if (page < 0)"),
 }
