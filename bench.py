@@ -41,8 +41,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode",
                     choices=["llama8b_decode", "over2gib_decode", "ragged_decode", "causal_prefill", "tiny_decode_f32",
-                             "llama8b_decode_fp8", "mixed_decode_prefill", "d256_decode", "mha_decode",
-                             "causal_prefill_f16"])
+                             "llama8b_decode_fp8", "llama8b_decode_int8", "mixed_decode_prefill", "d256_decode",
+                             "mha_decode", "causal_prefill_f16"])
     ap.add_argument("--split-kv", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences (llama8b/over2gib workloads only; smaller pools for profiling)")
@@ -165,7 +165,7 @@ def algorithmic_bytes(wl, split_kv: int) -> dict:
     q = wl.B * wl.Sq * wl.Hq * wl.D * wl.esize
     out = q
     ids = int(wl.nblk().sum()) * 4 + wl.B * 4
-    scales = int(wl.nblk().sum()) * wl.Hkv * 4 * 2 if wl.kv_dtype == "fp8e4m3" else 0
+    scales = int(wl.nblk().sum()) * wl.Hkv * 4 * 2 if wl.kv_dtype is not None else 0
     return {"kv": kv, "q": q, "out": out, "ids": ids, "scales": scales, "total": kv + q + out + ids + scales}
 
 
@@ -225,8 +225,8 @@ def recorded_traffic(kernel: str, workload: str, split_kv: int):
 
 def build_workload(name, batch=None):
     from paged_kv_cache_201_gb300 import workloads as W
-    if batch is not None and name in ("llama8b_decode", "over2gib_decode", "llama8b_decode_fp8", "d256_decode",
-                                      "mha_decode"):
+    if batch is not None and name in ("llama8b_decode", "over2gib_decode", "llama8b_decode_fp8",
+                                      "llama8b_decode_int8", "d256_decode", "mha_decode"):
         return W.make(name, B=batch)
     return W.make(name)
 
@@ -244,7 +244,7 @@ def time_oracle(wl, k_host, v_host, split_kv: int, n_seq: int, scales=None):
     import oracle
     rows = cpu_sample_rows(wl, n_seq)
     t0 = time.perf_counter()
-    if wl.kv_dtype == "fp8e4m3":
+    if wl.kv_dtype is not None:
         oracle.workload_rows_kvq(wl, split_kv=split_kv, row_bih=rows, k_cache=k_host, v_cache=v_host,
                                  k_scale=scales[0], v_scale=scales[1], want_split=split_kv > 1)
     else:
@@ -256,9 +256,10 @@ def time_oracle(wl, k_host, v_host, split_kv: int, n_seq: int, scales=None):
 
 
 def host_pools(wl, k, v):
-    """Device pools -> host element arrays for the oracle (uint16 bits, float32, or uint8 E4M3 bits)."""
+    """Device pools -> host element arrays for the oracle (uint16 bits, float32, or uint8 bits of
+    8-bit elements)."""
     import torch
-    if wl.kv_dtype == "fp8e4m3":
+    if wl.kv_dtype is not None:
         return k.cpu().numpy(), v.cpu().numpy()
     if wl.dtype == "f32":
         return k.cpu().numpy(), v.cpu().numpy()
@@ -269,6 +270,9 @@ def data_text(wl) -> str:
     if wl.kv_dtype == "fp8e4m3":
         return ("synthetic (seeded N(0,1) K/V quantized to FP8 E4M3 with per-(page, kv head) scales "
                 "max|x|/448; N(0,1) q rounded to bf16; shuffled pages)")
+    if wl.kv_dtype == "int8":
+        return ("synthetic (seeded N(0,1) K/V quantized to int8 with per-(page, kv head) scales "
+                "max|x|/127, round to nearest even; N(0,1) q rounded to bf16; shuffled pages)")
     return f"synthetic (seeded N(0,1) rounded to {wl.dtype}; shuffled pages)"
 
 
@@ -299,14 +303,15 @@ def run_ours(args, ws, rank, local):
     wl = build_workload(args.workload, args.batch)
     S = args.split_kv or wl.split_kv[0]
     q = W.host_to_torch(wl.q, wl.dtype).to(dev)
-    kvq = wl.kv_dtype == "fp8e4m3"
+    kvq = wl.kv_dtype is not None
+    kv_code = {"fp8e4m3": pa.PA_FP8_E4M3, "int8": pa.PA_INT8}.get(wl.kv_dtype)
     ks = vs = None
     if kvq:
         if wl.k_cache is not None:
             k, v = torch.from_numpy(wl.k_cache).to(dev), torch.from_numpy(wl.v_cache).to(dev)
             ks, vs = torch.from_numpy(wl.k_scale).to(dev), torch.from_numpy(wl.v_scale).to(dev)
         else:
-            k, v, ks, vs = W.fill_device_cache_fp8(wl, dev)
+            k, v, ks, vs = W.fill_device_cache_q8(wl, dev)
     elif wl.k_cache is not None:
         k = W.host_to_torch(wl.k_cache, wl.dtype).to(dev)
         v = W.host_to_torch(wl.v_cache, wl.dtype).to(dev)
@@ -325,7 +330,7 @@ def run_ours(args, ws, rank, local):
     def fwd():
         o, l = (out, lse) if S == 1 else (po, pl)
         if kvq:
-            pa.paged_attn_fwd_kvq(q, k, v, ks, vs, bt, sl, wl.causal, qo, S, wl.scale, o, l, stream)
+            pa.paged_attn_fwd_kvq(q, k, v, ks, vs, bt, sl, wl.causal, qo, S, wl.scale, o, l, stream, kv_code)
         else:
             pa.paged_attn_fwd_variant(q, k, v, bt, sl, wl.causal, qo, S, wl.scale, o, l, args.variant, stream)
 
@@ -431,7 +436,7 @@ def run_ours(args, ws, rank, local):
             sl.copy_(sl_h, non_blocking=True)
             if kvq:
                 pa.paged_attn_fwd_kvq_splitkv(q, k, v, ks, vs, bt, sl, wl.causal, qo, S, wl.scale, out, lse, wsp,
-                                              stream=stream)
+                                              stream=stream, kv_dtype=kv_code)
             else:
                 pa.paged_attn_fwd_splitkv(q, k, v, bt, sl, wl.causal, qo, S, wl.scale, out, lse, wsp,
                                           stream=stream)
@@ -712,7 +717,7 @@ def run_reference(args, ws, rank, local):
 
     wl = build_workload(args.workload, args.batch)
     S = args.split_kv or wl.split_kv[0]
-    sc_h = (wl.k_scale, wl.v_scale) if wl.kv_dtype == "fp8e4m3" else None
+    sc_h = (wl.k_scale, wl.v_scale) if wl.kv_dtype is not None else None
     if wl.k_cache is not None:
         k_h, v_h = wl.k_cache, wl.v_cache
     else:
@@ -720,8 +725,8 @@ def run_reference(args, ws, rank, local):
         if dev is None:
             print(json.dumps({"impl": "reference", "unavailable": "the 2-GiB pools are drawn on a CUDA device"}))
             return
-        if wl.kv_dtype == "fp8e4m3":
-            k, v, ks, vs = W.fill_device_cache_fp8(wl, dev)
+        if wl.kv_dtype is not None:
+            k, v, ks, vs = W.fill_device_cache_q8(wl, dev)
             sc_h = (ks.cpu().numpy(), vs.cpu().numpy())
             del ks, vs
         else:

@@ -42,8 +42,8 @@
 extern "C" {
 #endif
 
-/* element types (PA_FP8_E4M3: quantized K/V pools only, see paged_attn_fwd_kvq) */
-enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 };
+/* element types (PA_FP8_E4M3, PA_INT8: quantized K/V pools only, see paged_attn_fwd_kvq) */
+enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3, PA_INT8 = 4 };
 
 /* status codes */
 enum {
@@ -229,13 +229,14 @@ int paged_attn_fwd_varlen(const void *q, const void *k_cache, const void *v_cach
 /*
  * paged_attn_fwd_kvq — paged_attn_fwd over quantized K/V pools.  The pages' sweeps include i8
  * attention (rocMLIR PR #2371, Motivation; rocMLIR PR #2222, reviewed files); this library reads a
- * quantized pool as FP8 E4M3 elements (OCP "fn" encoding: bias 7, no infinities, S.1111.111 is
- * NaN) with one float32 scale per (page, kv head):
- *   value of K element (page, t, kvh, e) = e4m3(k_cache[page, t, kvh, e]) * k_scale[page, kvh]
- * and the same for V with v_scale.
- *   k_cache, v_cache  [num_pages, page_size, num_kv_heads, head_dim] bytes (E4M3 bits), 16-byte aligned
+ * quantized pool as 8-bit elements with one float32 scale per (page, kv head):
+ *   value of K element (page, t, kvh, e) = elem(k_cache[page, t, kvh, e]) * k_scale[page, kvh]
+ * and the same for V with v_scale, where elem() decodes a byte as
+ *   PA_FP8_E4M3  an FP8 E4M3 number (OCP "fn" encoding: bias 7, no infinities, S.1111.111 is NaN)
+ *   PA_INT8      a two's-complement integer in [-128, 127]
+ *   k_cache, v_cache  [num_pages, page_size, num_kv_heads, head_dim] bytes, 16-byte aligned
  *   k_scale, v_scale  [num_pages, num_kv_heads] float32, 4-byte aligned
- *   kv_dtype          PA_FP8_E4M3 (anything else: PA_EDTYPE)
+ *   kv_dtype          PA_FP8_E4M3 or PA_INT8, both pools (anything else: PA_EDTYPE)
  * q, out and dims->dtype are PA_BF16 or PA_F16 (PA_F32: PA_EDTYPE).  Every other argument, the
  * split semantics and the outputs are those of paged_attn_fwd.  A page id outside [0, num_pages)
  * reads as zeros with scale 0 and sets PA_ERRBIT_PAGE_RANGE.  The scaled score is

@@ -20,11 +20,12 @@ __all__ = [
     "paged_attn_strerror", "paged_attn_version", "attention", "paged_attn_auto_split",
     "paged_attn_workspace_bytes", "paged_attn_fwd_splitkv", "paged_attn_fwd_splitkv_noalloc", "paged_attn_fwd_kvq",
     "paged_attn_fwd_kvq_splitkv", "attention_kvq", "paged_attn_fwd_varlen", "attention_varlen", "PA_F32", "PA_F16", "PA_BF16", "PA_FP8_E4M3",
+    "PA_INT8",
     "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL", "VARIANT_TC05_PREFILL",
     "VARIANT_MMA_T", "VARIANT_MMA_SPLIT_GROUP",
 ]
 
-PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_INT8 = 0, 1, 2, 3, 4
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA_DECODE, VARIANT_MMA_PREFILL, VARIANT_TC05_PREFILL, VARIANT_MMA_T = 0, 1, 2, 3, 4, 5
 VARIANT_MMA_SPLIT_GROUP = 6
 ERRBIT_PAGE_RANGE, ERRBIT_TIMEOUT, ERRBIT_SEQ_CLIPPED, ERRBIT_QSTART = 1, 2, 4, 8
@@ -268,21 +269,32 @@ def paged_attn_fwd_splitkv_noalloc(q, k_cache, v_cache, block_table, seq_lens, c
     _raise(rc, "paged_attn_fwd_splitkv_noalloc")
 
 
-def _check_e4m3_pool(t, name):
-    """An FP8 E4M3 pool: uint8 bits or torch.float8_e4m3fn, [P, ps, Hkv, D]."""
+def _check_q8_pool(t, name, kv_dtype):
+    """An 8-bit pool [P, ps, Hkv, D]: uint8 bits of either format, torch.float8_e4m3fn for
+    PA_FP8_E4M3 or torch.int8 for PA_INT8."""
     torch = _torch()
     _check(t, name, ndim=4)
-    if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
-        raise TypeError(f"{name} must be uint8 (E4M3 bits) or float8_e4m3fn, got {t.dtype}")
+    typed = {PA_FP8_E4M3: getattr(torch, "float8_e4m3fn", torch.uint8), PA_INT8: torch.int8}
+    if kv_dtype not in typed:
+        raise ValueError(f"kv_dtype must be PA_FP8_E4M3 or PA_INT8, got {kv_dtype}")
+    if t.dtype not in (torch.uint8, typed[kv_dtype]):
+        raise TypeError(f"{name} must be uint8 bits or {typed[kv_dtype]} for kv_dtype {kv_dtype}, got {t.dtype}")
 
 
-def _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, out, lse):
+def _kv_dtype_of(k_cache, kv_dtype):
+    """kv_dtype as given, else PA_INT8 for an int8 pool and PA_FP8_E4M3 otherwise."""
+    if kv_dtype is not None:
+        return int(kv_dtype)
+    return PA_INT8 if k_cache.dtype == _torch().int8 else PA_FP8_E4M3
+
+
+def _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, out, lse, kv_dtype):
     torch = _torch()
     _check(q, "q", ndim=4)
     if q.dtype not in (torch.bfloat16, torch.float16):
-        raise TypeError(f"q must be bf16 or f16 with FP8 pools, got {q.dtype}")
-    _check_e4m3_pool(k_cache, "k_cache")
-    _check_e4m3_pool(v_cache, "v_cache")
+        raise TypeError(f"q must be bf16 or f16 with 8-bit pools, got {q.dtype}")
+    _check_q8_pool(k_cache, "k_cache", kv_dtype)
+    _check_q8_pool(v_cache, "v_cache", kv_dtype)
     if k_cache.shape != v_cache.shape:
         raise ValueError("k_cache and v_cache shapes differ")
     P, _, Hkv, _ = k_cache.shape
@@ -299,12 +311,14 @@ def _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_of
 
 
 def paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, causal, q_offset, split_kv,
-                       scale, out, lse, stream=None) -> None:
-    """Forward over FP8 E4M3 pools with [num_pages, Hkv] float32 scales; see ``paged_attn_fwd_kvq`` in
+                       scale, out, lse, stream=None, kv_dtype=None) -> None:
+    """Forward over 8-bit pools (``kv_dtype`` PA_FP8_E4M3 or PA_INT8; by default PA_INT8 for int8
+    tensors, else PA_FP8_E4M3) with [num_pages, Hkv] float32 scales; see ``paged_attn_fwd_kvq`` in
     include/paged_attn.h.  Outputs as ``paged_attn_fwd``."""
-    dims = _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, out, lse)
+    kv_dtype = _kv_dtype_of(k_cache, kv_dtype)
+    dims = _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, out, lse, kv_dtype)
     rc = load_library().paged_attn_fwd_kvq(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), PA_FP8_E4M3, _ptr(block_table),
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kv_dtype, _ptr(block_table),
         _ptr(seq_lens), int(bool(causal)), _ptr(q_offset), int(split_kv), float(scale), _ptr(out), _ptr(lse),
         ctypes.byref(dims), _stream(stream))
     _raise(rc, "paged_attn_fwd_kvq")
@@ -312,9 +326,11 @@ def paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_l
 
 def paged_attn_fwd_kvq_splitkv(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, causal, q_offset,
                                split_kv, scale, out, lse, workspace, num_sms=None, device_bytes=None,
-                               stream=None) -> None:
-    """``paged_attn_fwd_splitkv`` over FP8 E4M3 pools (split forward + combine in one call)."""
-    dims = _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, out, lse)
+                               stream=None, kv_dtype=None) -> None:
+    """``paged_attn_fwd_splitkv`` over 8-bit pools (split forward + combine in one call); ``kv_dtype``
+    as in ``paged_attn_fwd_kvq``."""
+    kv_dtype = _kv_dtype_of(k_cache, kv_dtype)
+    dims = _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, out, lse, kv_dtype)
     _check(workspace, "workspace")
     if num_sms is None or device_bytes is None:
         n, m = _device_info(q.device)
@@ -322,7 +338,7 @@ def paged_attn_fwd_kvq_splitkv(q, k_cache, v_cache, k_scale, v_scale, block_tabl
         device_bytes = m if device_bytes is None else device_bytes
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().paged_attn_fwd_kvq_splitkv(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), PA_FP8_E4M3, _ptr(block_table),
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kv_dtype, _ptr(block_table),
         _ptr(seq_lens), int(bool(causal)), _ptr(q_offset), int(split_kv), float(scale), _ptr(out), _ptr(lse),
         ctypes.byref(dims), _ptr(workspace), int(ws_bytes), int(num_sms), int(device_bytes), _stream(stream))
     _raise(rc, "paged_attn_fwd_kvq_splitkv")
@@ -456,8 +472,9 @@ def attention(q, k_cache, v_cache, block_table, seq_lens, *, causal: bool = Fals
 
 def attention_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, *, causal: bool = False,
                   q_offset=None, split_kv: int = 1, scale: Optional[float] = None, want_lse: bool = False,
-                  stream=None):
-    """``attention`` over FP8 E4M3 pools with per-(page, kv head) scales."""
+                  stream=None, kv_dtype=None):
+    """``attention`` over 8-bit pools with per-(page, kv head) scales; ``kv_dtype`` as in
+    ``paged_attn_fwd_kvq``."""
     torch = _torch()
     B, Sq, Hq, D = q.shape
     if scale is None:
@@ -466,12 +483,12 @@ def attention_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, 
     lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device) if (want_lse or split_kv > 1) else None
     if split_kv == 1:
         paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, causal, q_offset, 1, scale,
-                           out, lse, stream)
+                           out, lse, stream, kv_dtype)
     else:
         po = torch.empty((split_kv, B, Sq, Hq, D), dtype=torch.float32, device=q.device)
         pl = torch.empty((split_kv, B, Sq, Hq), dtype=torch.float32, device=q.device)
         paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, causal, q_offset, split_kv,
-                           scale, po, pl, stream)
+                           scale, po, pl, stream, kv_dtype)
         paged_attn_combine(po, pl, out, lse, stream)
     return (out, lse) if want_lse else out
 

@@ -99,10 +99,10 @@ int make_pool_map(CUtensorMap *m, const void *base, const pa_dims *d, int halves
     return r == CUDA_SUCCESS ? PA_OK : PA_ECUDA;
 }
 
-// 3-D view of one E4M3 pool for TMA: (byte within a row, token, kv head); one box = the page_size
+// 3-D view of one 8-bit pool (E4M3 or int8 elements) for TMA: (byte within a row, token, kv head); one box = the page_size
 // rows of one page and one kv head.  128-byte rows (head_dim 128) land with the 128-byte swizzle,
 // which the kernel's conflict-free operand loads rely on; 64-byte rows land as they are.
-int make_pool_map_e4m3(CUtensorMap *m, const void *base, const pa_dims *d) {
+int make_pool_map_q8(CUtensorMap *m, const void *base, const pa_dims *d) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PA_ECUDA;
     const cuuint64_t D = (cuuint64_t)d->head_dim, Hkv = (cuuint64_t)d->num_kv_heads;
@@ -427,7 +427,7 @@ int paged_attn_fwd_kvq(const void *q, const void *k_cache, const void *v_cache, 
                        const pa_dims *dims, void *stream) {
     int rc = check_dims(dims);
     if (rc != PA_OK) return rc;
-    if (dims->dtype == PA_F32 || kv_dtype != PA_FP8_E4M3) return PA_EDTYPE;
+    if (dims->dtype == PA_F32 || (kv_dtype != PA_FP8_E4M3 && kv_dtype != PA_INT8)) return PA_EDTYPE;
     if (dims->head_dim == 256) return PA_EUNSUPPORTED;
     if (split_kv < 1 || split_kv > 65535) return PA_EINVAL;
     if (!isfinite(scale)) return PA_EINVAL;
@@ -447,11 +447,11 @@ int paged_attn_fwd_kvq(const void *q, const void *k_cache, const void *v_cache, 
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     CUtensorMap tmk, tmv;
-    if ((rc = make_pool_map_e4m3(&tmk, k_cache, dims)) != PA_OK) return rc;
-    if ((rc = make_pool_map_e4m3(&tmv, v_cache, dims)) != PA_OK) return rc;
+    if ((rc = make_pool_map_q8(&tmk, k_cache, dims)) != PA_OK) return rc;
+    if ((rc = make_pool_map_q8(&tmv, v_cache, dims)) != PA_OK) return rc;
     const int mode = p.rows <= pa::kDecodeRows ? pa::MODE_DECODE : pa::MODE_PREFILL;
     if (mode == pa::MODE_PREFILL) p.row_tiles = (p.rows + pa::kPrefillRows - 1) / pa::kPrefillRows;
-    return cuda_status(pa::launch_mma_kvq(p, mode, dims->dtype, tmk, tmv, static_cast<cudaStream_t>(stream)));
+    return cuda_status(pa::launch_mma_kvq(p, mode, dims->dtype, kv_dtype, tmk, tmv, static_cast<cudaStream_t>(stream)));
 }
 
 int paged_attn_fwd_kvq_splitkv(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
@@ -461,7 +461,7 @@ int paged_attn_fwd_kvq_splitkv(const void *q, const void *k_cache, const void *v
                                int64_t workspace_bytes, int num_sms, int64_t device_bytes, void *stream) {
     int rc = check_dims(dims);
     if (rc != PA_OK) return rc;
-    if (dims->dtype == PA_F32 || kv_dtype != PA_FP8_E4M3) return PA_EDTYPE;
+    if (dims->dtype == PA_F32 || (kv_dtype != PA_FP8_E4M3 && kv_dtype != PA_INT8)) return PA_EDTYPE;
     return splitkv_call(dims, split_kv, out, lse, workspace, workspace_bytes, num_sms, device_bytes, stream,
                         [&](int S, void *o, float *l) {
                             return paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, block_table,

@@ -1,21 +1,22 @@
-// Tensor-core paged attention over FP8 E4M3 K/V pools with one float scale per (page, kv head),
-// for bf16 / f16 queries, head_dim 64 or 128 (sm_103a).
+// Tensor-core paged attention over 8-bit K/V pools (FP8 E4M3 or int8 elements) with one float
+// scale per (page, kv head), for bf16 / f16 queries, head_dim 64 or 128 (sm_103a).
 //
 // The pages' sweeps include i8 attention (rocMLIR PR #2371, Motivation; rocMLIR PR #2222, the
-// reviewed files); a quantized pool here holds E4M3 elements whose value is element x scale of
-// the element's (page, kv head).
+// reviewed files); a quantized pool here holds E4M3 or two's-complement int8 elements whose value
+// is element x scale of the element's (page, kv head).  Both formats convert exactly to f16 (every
+// E4M3 value and every integer in [-128, 127] is an f16 number), so one kernel body serves both;
+// the element format is a template parameter (FMT) that picks the conversion.
 //
 // Units (one CTA per (sequence, kv head, split[, 64-row query tile])), the producer warp and the
 // online softmax with its guards follow the 16-bit kernel (attn_mma.cu).  What differs:
-//   * the producer copies each page's raw E4M3 rows (page_size tokens x head_dim bytes of one kv
+//   * the producer copies each page's raw 8-bit rows (page_size tokens x head_dim bytes of one kv
 //     head: one 3-D TMA box, half the bytes of a 16-bit page) into a ring of 64-key stages, and
 //     with the page ids it loads the pages' K and V scales, which it leaves in shared memory
 //     beside the stage before arming the stage's barriers.
-//   * K enters the tensor cores in f16 straight from the ring: a lane converts the E4M3 bytes of
-//     its key into MMA operand registers (one conversion per element pair, exact: every E4M3 value
-//     is an f16 number).  The head dimension is visited in a permuted order, the same for Q and K,
-//     so that a lane's operand bytes are 16 contiguous bytes of one row (one conflict-free shared
-//     load); a dot product does not depend on the order of its terms.  bf16 queries enter as f16
+//   * K enters the tensor cores in f16 straight from the ring: a lane converts the 8-bit bytes of
+//     its key into MMA operand registers (exact).  The head dimension is visited in a permuted
+//     order, the same for Q and K, so that a lane's operand bytes are 16 contiguous bytes of one
+//     row (one conflict-free shared load); a dot product does not depend on the order of its terms.  bf16 queries enter as f16
 //     after multiplying each query row by a power of two that puts its largest element in
 //     [2^14, 2^15); the score is scaled back by the inverse power exactly.
 //   * decode converts V from the ring the same way and transposes it in registers (movmatrix);
@@ -42,7 +43,7 @@ constexpr int kMaxPagesPerStage = kMmaTileKeys / 16;  // prefill stages: page_si
 
 template <int D>
 struct Geo8 {
-    static constexpr int kStage8 = kMmaTileKeys * D;     // bytes of one K (or V) stage, E4M3
+    static constexpr int kStage8 = kMmaTileKeys * D;     // bytes of one K (or V) stage, 8-bit elements
 };
 
 // Widened rows: [4 warps][D/64 halves][16 keys][64 elements].  A row is 128 bytes; its 16-byte
@@ -65,11 +66,33 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t four, uint32_t &lo, uin
         : "r"(four));
 }
 
-// Widen keys [kw0, kw0 + 16) of one E4M3 stage (rows of D bytes, as the TMA left them) into
+// Four int8 bytes (element 0 in the low byte) -> two f16 pairs, exactly.  Byte XOR 0x80 is v + 128
+// in [0, 255]; placed as the low mantissa byte of an f16 with biased exponent 25 (0x64 in the high
+// byte: the binade [1024, 2048), whose spacing is 1) it reads 1024 + v + 128, and subtracting 1152
+// (0x6480) leaves v.
+__device__ __forceinline__ void s8x4_to_f16x4(uint32_t four, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = four ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);  // bytes u0, 0x64, u1, 0x64
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);  // bytes u2, 0x64, u3, 0x64
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+constexpr int kFmtE4M3 = 0, kFmtInt8 = 1;  // element formats of a quantized pool
+
+template <int FMT>
+__device__ __forceinline__ void q8x4_to_f16x4(uint32_t four, uint32_t &lo, uint32_t &hi) {
+    if constexpr (FMT == kFmtInt8)
+        s8x4_to_f16x4(four, lo, hi);
+    else
+        e4m3x4_to_f16x4(four, lo, hi);
+}
+
+// Widen keys [kw0, kw0 + 16) of one 8-bit stage (rows of D bytes, as the TMA left them) into
 // f16 rows at `wide`.  Keys at or past key_end (relative to the
 // stage) become zero rows: they hold whatever the ring held before, and a zero V row keeps
 // 0 x NaN out of the output.
-// Shared address of 16-byte chunk c of key row k in an E4M3 ring stage: rows of D bytes; for
+// Shared address of 16-byte chunk c of key row k in an 8-bit ring stage: rows of D bytes; for
 // D = 128 the TMA wrote them with the 128-byte swizzle (chunk c at position c XOR (k % 8)).
 template <int D>
 __device__ __forceinline__ uint32_t ring_chunk_addr(uint32_t stage, int k, int c) {
@@ -84,9 +107,9 @@ __device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t (&w)[4]) {
                  : "memory");
 }
 
-template <int D>
+template <int FMT, int D>
 __device__ __forceinline__ void widen_keys(uint32_t ring, uint32_t wide, int kw0, int key_end, int lane) {
-    constexpr int C8 = D / 16;  // 16-byte E4M3 chunks per row
+    constexpr int C8 = D / 16;  // 16-byte chunks of 8-bit elements per row
 #pragma unroll
     for (int it = 0; it < 16 * C8 / 32; ++it) {
         const int idx = it * 32 + lane;
@@ -96,10 +119,10 @@ __device__ __forceinline__ void widen_keys(uint32_t ring, uint32_t wide, int kw0
         if (key < key_end) {
             uint32_t x[4];
             lds_v4(ring_chunk_addr<D>(ring, key, c8), x);
-            e4m3x4_to_f16x4(x[0], w[0], w[1]);
-            e4m3x4_to_f16x4(x[1], w[2], w[3]);
-            e4m3x4_to_f16x4(x[2], w[4], w[5]);
-            e4m3x4_to_f16x4(x[3], w[6], w[7]);
+            q8x4_to_f16x4<FMT>(x[0], w[0], w[1]);
+            q8x4_to_f16x4<FMT>(x[1], w[2], w[3]);
+            q8x4_to_f16x4<FMT>(x[2], w[4], w[5]);
+            q8x4_to_f16x4<FMT>(x[3], w[6], w[7]);
         } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) w[i] = 0u;
@@ -137,14 +160,14 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc)
 // and + {2, 3} (b1); the query fragments use the same head-dim order.  For D = 128 the lane's two
 // chunks are 2 tq and 2 tq + 1: with the swizzle, the two keys of a load phase then read
 // chunks of opposite parity, so the 8 lanes of a phase hit 8 different banks.
-template <int D>
+template <int FMT, int D>
 __device__ __forceinline__ void load_k_frags(uint32_t stage, int k, int tq, uint32_t (&bk)[D / 16][2]) {
 #pragma unroll
     for (int h = 0; h < D / 64; ++h) {
         uint32_t w[4];
         lds_v4(ring_chunk_addr<D>(stage, k, (D / 64) * tq + h), w);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) e4m3x4_to_f16x4(w[i], bk[4 * h + i][0], bk[4 * h + i][1]);
+        for (int i = 0; i < 4; ++i) q8x4_to_f16x4<FMT>(w[i], bk[4 * h + i][0], bk[4 * h + i][1]);
     }
 }
 
@@ -204,7 +227,7 @@ __device__ __forceinline__ void kvq_produce(const CUtensorMap *tmK, const CUtens
     }
     const int ps = 1 << ps_shift;
     const int pps = SK >> ps_shift;                 // pages per stage (page_size >= 16: at most SK / 16)
-    const uint32_t box_bytes = (uint32_t)(ps * D);  // one page of one kv head, E4M3
+    const uint32_t box_bytes = (uint32_t)(ps * D);  // one page of one kv head, 8-bit elements
     const int pg_end = (k_hi + ps - 1) >> ps_shift;
     const int32_t *bt_row = p.block_table + (long long)b * p.W;
     auto scale_of = [&](const float *sc, int id) -> float {
@@ -319,7 +342,7 @@ __device__ __forceinline__ KvqUnit kvq_unit(const FwdParams &p, int b, int s, in
 // so that keys and head dimension fill the MMA's 16-row side and the few query rows (GQA group x
 // query tokens, padded to NR x 8) its 8-column side.  Warp w reads keys [16 w, 16 w + 16) of every
 // stage (one page: page_size >= 16); the four warps' softmax states are merged at the end.
-template <typename T, int D, int NR, int NSTAGE, int KPW, int MINB>
+template <typename T, int FMT, int D, int NR, int NSTAGE, int KPW, int MINB>
 __global__ void __launch_bounds__(kMmaThreads, MINB)
     paged_attn_kvq_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                                  const FwdParams p, int ps_shift) {
@@ -452,8 +475,8 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
                     for (int i = 0; i < 4; ++i) {
                         const int kk = 4 * h + i;
                         uint32_t a[4];
-                        e4m3x4_to_f16x4(wg[i], a[0], a[2]);
-                        e4m3x4_to_f16x4(w8[i], a[1], a[3]);
+                        q8x4_to_f16x4<FMT>(wg[i], a[0], a[2]);
+                        q8x4_to_f16x4<FMT>(w8[i], a[1], a[3]);
 #pragma unroll
                         for (int nr = 0; nr < NR; ++nr) Op::run(sc[hb][nr][i & 1], a, qb[nr][kk][0], qb[nr][kk][1]);
                     }
@@ -567,8 +590,8 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     uint32_t x00, x01, x10, x11;  // [key half][d slot half]
-                    e4m3x4_to_f16x4(vw[hb][0][mt], x00, x01);
-                    e4m3x4_to_f16x4(vw[hb][1][mt], x10, x11);
+                    q8x4_to_f16x4<FMT>(vw[hb][0][mt], x00, x01);
+                    q8x4_to_f16x4<FMT>(vw[hb][1][mt], x10, x11);
                     const uint32_t a[4] = {movmatrix_trans(x00), movmatrix_trans(x01), movmatrix_trans(x10),
                                            movmatrix_trans(x11)};
 #pragma unroll
@@ -630,7 +653,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
 // ============================================================================ prefill
 // More than 16 query rows: 64-row tiles, each consumer warp owning 16 rows over all 64 keys of a
 // stage (S = Q K^T, O = P V); V rows are widened once per stage by the four warps together.
-template <typename T, int D, int NSTAGE>
+template <typename T, int FMT, int D, int NSTAGE>
 __global__ void __launch_bounds__(kMmaThreads, 2)
     paged_attn_kvq_prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                                   const FwdParams p, int ps_shift) {
@@ -742,7 +765,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
             const bool ok = mbar_wait(bar_fv + 8 * st, par, p.err);
             bad = __any_sync(0xffffffffu, !ok);
         }
-        if (!bad) widen_keys<D>(vring, wideV, kw0, k_hi - tile_k0, lane);
+        if (!bad) widen_keys<FMT, D>(vring, wideV, kw0, k_hi - tile_k0, lane);
         named_bar_sync(1, kMmaConsumerWarps * 32);  // the stage's V rows are complete
 
 #pragma unroll
@@ -756,7 +779,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
             for (int n = 0; n < NTB; ++n) {
                 sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
                 uint32_t bk[D / 16][2];
-                load_k_frags<D>(kring, kb0 + n * 8 + g, tq, bk);
+                load_k_frags<FMT, D>(kring, kb0 + n * 8 + g, tq, bk);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) Op::run(sc[n], qf[kk], bk[kk][0], bk[kk][1]);
             }
@@ -863,12 +886,12 @@ static int ps_shift_of(int ps) {
 
 // Decode shape: KPW keys per consumer warp and stage (stages of 4 KPW keys), NSTAGE-deep ring,
 // MINB CTAs per SM.
-template <typename T, int D, int NR, int KPW, int NSTAGE, int MINB>
+template <typename T, int FMT, int D, int NR, int KPW, int NSTAGE, int MINB>
 static cudaError_t launch_kvq_decode(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                      cudaStream_t stream) {
     constexpr size_t smem = (size_t)NSTAGE * 2 * kMmaConsumerWarps * KPW * D + 1024;
     static_assert(merge_scratch_bytes(D) + 1024 <= smem, "decode merge scratch must fit in the ring");
-    auto kern = paged_attn_kvq_decode_kernel<T, D, NR, NSTAGE, KPW, MINB>;
+    auto kern = paged_attn_kvq_decode_kernel<T, FMT, D, NR, NSTAGE, KPW, MINB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long units = (long long)p.B * p.split_kv * p.Hkv;
@@ -878,12 +901,12 @@ static cudaError_t launch_kvq_decode(const FwdParams &p, const CUtensorMap &tmk,
     return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int FMT, int D>
 static cudaError_t launch_kvq_prefill(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                       cudaStream_t stream) {
     constexpr int NSTAGE = kvq_prefill_stages(D);
     constexpr size_t smem = kvq_smem_bytes(D, NSTAGE, true);
-    auto kern = paged_attn_kvq_prefill_kernel<T, D, NSTAGE>;
+    auto kern = paged_attn_kvq_prefill_kernel<T, FMT, D, NSTAGE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long units = (long long)p.B * p.split_kv * p.Hkv * p.row_tiles;
@@ -893,25 +916,32 @@ static cudaError_t launch_kvq_prefill(const FwdParams &p, const CUtensorMap &tmk
     return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int FMT, int D>
 static cudaError_t launch_kvq_d(const FwdParams &p, int mode, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 cudaStream_t stream) {
-    if (mode == MODE_PREFILL) return launch_kvq_prefill<T, D>(p, tmk, tmv, stream);
+    if (mode == MODE_PREFILL) return launch_kvq_prefill<T, FMT, D>(p, tmk, tmv, stream);
     // 16 keys per warp and stage, 4 (D = 128) or 8 (D = 64) 64-key stages: 65 KiB, so 3 CTAs per SM
     // for <= 8 rows.  Measured on the FP8 Llama-3-8B decode: 32 keys per warp (two blocks sharing one
     // softmax step) with 2 or 3 stages, and 6 stages at 2 CTAs per SM, were no faster.
-    if (p.rows <= 8) return launch_kvq_decode<T, D, 1, 16, (D == 128 ? 4 : 8), 3>(p, tmk, tmv, stream);
-    return launch_kvq_decode<T, D, 2, 16, (D == 128 ? 4 : 8), 2>(p, tmk, tmv, stream);
+    if (p.rows <= 8) return launch_kvq_decode<T, FMT, D, 1, 16, (D == 128 ? 4 : 8), 3>(p, tmk, tmv, stream);
+    return launch_kvq_decode<T, FMT, D, 2, 16, (D == 128 ? 4 : 8), 2>(p, tmk, tmv, stream);
 }
 
-cudaError_t launch_mma_kvq(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                           cudaStream_t stream) {
+template <int FMT>
+static cudaError_t launch_kvq_fmt(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk,
+                                  const CUtensorMap &tmv, cudaStream_t stream) {
     if (dtype == PA_BF16) {
-        return p.D == 128 ? launch_kvq_d<__nv_bfloat16, 128>(p, mode, tmk, tmv, stream)
-                          : launch_kvq_d<__nv_bfloat16, 64>(p, mode, tmk, tmv, stream);
+        return p.D == 128 ? launch_kvq_d<__nv_bfloat16, FMT, 128>(p, mode, tmk, tmv, stream)
+                          : launch_kvq_d<__nv_bfloat16, FMT, 64>(p, mode, tmk, tmv, stream);
     }
-    return p.D == 128 ? launch_kvq_d<__half, 128>(p, mode, tmk, tmv, stream)
-                      : launch_kvq_d<__half, 64>(p, mode, tmk, tmv, stream);
+    return p.D == 128 ? launch_kvq_d<__half, FMT, 128>(p, mode, tmk, tmv, stream)
+                      : launch_kvq_d<__half, FMT, 64>(p, mode, tmk, tmv, stream);
+}
+
+cudaError_t launch_mma_kvq(const FwdParams &p, int mode, int dtype, int kv_dtype, const CUtensorMap &tmk,
+                           const CUtensorMap &tmv, cudaStream_t stream) {
+    if (kv_dtype == PA_INT8) return launch_kvq_fmt<kFmtInt8>(p, mode, dtype, tmk, tmv, stream);
+    return launch_kvq_fmt<kFmtE4M3>(p, mode, dtype, tmk, tmv, stream);
 }
 
 }  // namespace pa

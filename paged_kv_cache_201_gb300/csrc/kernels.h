@@ -33,9 +33,10 @@ cudaError_t launch_mma(const FwdParams &p, int mode, int dtype, const CUtensorMa
 // Variable-length batch (p.q_start set, p.B sequences, total_q packed query tokens).
 cudaError_t launch_mma_varlen(const FwdParams &p, long long total_q, int dtype, const CUtensorMap &tmk,
                               const CUtensorMap &tmv, cudaStream_t stream);
-// FP8 E4M3 pools with per-(page, kv head) scales in p.k_scale / p.v_scale; bf16/f16 queries.
-cudaError_t launch_mma_kvq(const FwdParams &p, int mode, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                           cudaStream_t stream);
+// 8-bit pools (kv_dtype PA_FP8_E4M3 or PA_INT8) with per-(page, kv head) scales in p.k_scale /
+// p.v_scale; bf16/f16 queries.
+cudaError_t launch_mma_kvq(const FwdParams &p, int mode, int dtype, int kv_dtype, const CUtensorMap &tmk,
+                           const CUtensorMap &tmv, cudaStream_t stream);
 // tcgen05 prefill: bf16/f16, head_dim 128, (Hq/Hkv) dividing 128.
 size_t tc05_smem_bytes();
 cudaError_t launch_tc05(const FwdParams &p, int dtype, const CUtensorMap &tmq, const CUtensorMap &tmk,

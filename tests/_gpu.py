@@ -16,7 +16,8 @@ class DeviceWorkload:
         import torch
         self.wl = wl
         self.q = W.host_to_torch(wl.q, wl.dtype).to(device)
-        self.kvq = getattr(wl, "kv_dtype", None) == "fp8e4m3"
+        self.kvq = getattr(wl, "kv_dtype", None) in W.QUANT_KV
+        self.kv_code = {"fp8e4m3": 3, "int8": 4}.get(getattr(wl, "kv_dtype", None))  # PA_FP8_E4M3 / PA_INT8
         self.ks = self.vs = None
         if self.kvq:
             if wl.k_cache is not None:
@@ -25,7 +26,7 @@ class DeviceWorkload:
                 self.ks = torch.from_numpy(np.ascontiguousarray(wl.k_scale, dtype=np.float32)).to(device)
                 self.vs = torch.from_numpy(np.ascontiguousarray(wl.v_scale, dtype=np.float32)).to(device)
             else:
-                self.k, self.v, self.ks, self.vs = W.fill_device_cache_fp8(wl, device)
+                self.k, self.v, self.ks, self.vs = W.fill_device_cache_q8(wl, device)
         elif wl.k_cache is not None:
             self.k = W.host_to_torch(wl.k_cache, wl.dtype).to(device)
             self.v = W.host_to_torch(wl.v_cache, wl.dtype).to(device)
@@ -36,7 +37,7 @@ class DeviceWorkload:
         self.qo = None if wl.q_offset is None else torch.from_numpy(np.ascontiguousarray(wl.q_offset)).to(device)
 
     def host_pools(self):
-        """The device pools as host element arrays (uint16 bits or float32; uint8 E4M3 bits for
+        """The device pools as host element arrays (uint16 bits or float32; uint8 bits for
         quantized pools), for the oracle."""
         if self.kvq:
             return self.k.cpu().numpy(), self.v.cpu().numpy()
@@ -73,7 +74,8 @@ def run(dw: DeviceWorkload, split_kv: int, variant: int = 0):
     def fwd(S, o, l):
         if dw.kvq:
             assert variant == 0
-            pa.paged_attn_fwd_kvq(dw.q, dw.k, dw.v, dw.ks, dw.vs, dw.bt, dw.sl, wl.causal, dw.qo, S, wl.scale, o, l)
+            pa.paged_attn_fwd_kvq(dw.q, dw.k, dw.v, dw.ks, dw.vs, dw.bt, dw.sl, wl.causal, dw.qo, S, wl.scale, o, l,
+                                  kv_dtype=dw.kv_code)
         else:
             pa.paged_attn_fwd_variant(dw.q, dw.k, dw.v, dw.bt, dw.sl, wl.causal, dw.qo, S, wl.scale, o, l, variant)
 

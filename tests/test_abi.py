@@ -150,10 +150,15 @@ def _kvq(lib, dims, kv_dtype=pa.PA_FP8_E4M3, split=1, k_scale=FAKE, v_scale=FAKE
 
 
 def test_fwd_kvq_validation(lib):
-    """FP8-pool entry points: element types, scales and the shared checks, all before any launch."""
+    """8-bit-pool entry points: element types, scales and the shared checks, all before any launch."""
     assert _kvq(lib, None) == EINVAL
-    assert _kvq(lib, _dims(dtype=pa.PA_F32)) == EDTYPE              # f32 queries are not read against FP8 pools
-    assert _kvq(lib, _dims(), kv_dtype=pa.PA_BF16) == EDTYPE       # pools must be E4M3
+    assert _kvq(lib, _dims(dtype=pa.PA_F32)) == EDTYPE              # f32 queries are not read against 8-bit pools
+    assert _kvq(lib, _dims(), kv_dtype=pa.PA_BF16) == EDTYPE       # pools must be E4M3 or int8
+    assert _kvq(lib, _dims(), kv_dtype=5) == EDTYPE
+    assert _kvq(lib, _dims(), kv_dtype=-1) == EDTYPE
+    for kvd in (pa.PA_FP8_E4M3, pa.PA_INT8):                       # both formats pass the type check
+        assert _kvq(lib, _dims(), kv_dtype=kvd, k_scale=None) == EINVAL
+        assert _kvq(lib, _dims(batch=0), kv_dtype=kvd, k_scale=None) == OK
     assert _kvq(lib, _dims(head_dim=96)) == EUNSUP
     assert _kvq(lib, _dims(head_dim=256)) == EUNSUP
     assert _kvq(lib, _dims(), split=0) == EINVAL
