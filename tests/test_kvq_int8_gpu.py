@@ -76,17 +76,40 @@ def test_causal_prefill_int8(pa, dtype):
 
 
 # ----------------------------------------------------------------------------- edge cases
-def test_int8_every_code_and_extreme_scales(pa):
-    """Pools drawn from all 256 codes (-128 included, which the quantizer never writes) with scales
-    from 1e-30 to 1e+30 across pages: the scores and weights stay in float32 range as the products say."""
+def _int8_pools(wl, rng, v_codes):
+    k = rng.integers(0, 256, size=wl.k_cache.shape).astype(np.uint8)
+    v = rng.choice(v_codes, size=wl.v_cache.shape).astype(np.uint8)
+    k.reshape(-1)[:256] = np.arange(256, dtype=np.uint8)
+    return k, v
+
+
+def test_int8_every_code(pa):
+    """K and V pools drawn from all 256 codes (-128 included, which the quantizer never writes), each
+    code present, with scales of the quantizer's size (10^-2 .. 10^-0.5)."""
     lens = [256, 130]
     wl = W.make_custom_int8(name="int8_codes", dtype="bf16", B=2, Sq=1, Hq=8, Hkv=2, D=128, page_size=16,
                             seq_lens=lens, seed=6)
     rng = np.random.default_rng(10)
-    k = rng.integers(0, 256, size=wl.k_cache.shape).astype(np.uint8)
-    v = rng.integers(0, 256, size=wl.v_cache.shape).astype(np.uint8)
-    k.reshape(-1)[:256] = np.arange(256, dtype=np.uint8)
+    k, v = _int8_pools(wl, rng, np.arange(256))
     v.reshape(-1)[:256] = np.arange(256, dtype=np.uint8)
+    ks = (10.0 ** rng.uniform(-2, -0.5, size=wl.k_scale.shape)).astype(np.float32)
+    vs = (10.0 ** rng.uniform(-2, -0.5, size=wl.v_scale.shape)).astype(np.float32)
+    wl = W.Workload(**{**wl.__dict__, "k_cache": k, "v_cache": v, "k_scale": ks, "v_scale": vs})
+    _full(wl, 1)
+    _full(wl, 2)
+    _check_clean(pa)
+
+
+def test_int8_extreme_scales(pa):
+    """Scales from 1e-30 to 1e+30 across pages: the scores and weights stay in float32 range as the
+    products say.  V holds codes 0..127 here: with both signs, a page whose keys have nearly equal
+    weights can cancel to 1e-9 of its terms, and at a scale of 1e19 that residue is below what any
+    float32 sum of the terms resolves (the same holds for the oracle's value in float32)."""
+    lens = [256, 130]
+    wl = W.make_custom_int8(name="int8_scales", dtype="bf16", B=2, Sq=1, Hq=8, Hkv=2, D=128, page_size=16,
+                            seq_lens=lens, seed=7)
+    rng = np.random.default_rng(11)
+    k, v = _int8_pools(wl, rng, np.arange(128))
     ks = (10.0 ** rng.uniform(-30, -2, size=wl.k_scale.shape)).astype(np.float32)   # scores stay moderate
     vs = (10.0 ** rng.uniform(-30, 30, size=wl.v_scale.shape)).astype(np.float32)
     wl = W.Workload(**{**wl.__dict__, "k_cache": k, "v_cache": v, "k_scale": ks, "v_scale": vs})
