@@ -48,6 +48,8 @@ def parse():
                     help="sequences (llama8b/over2gib workloads only; smaller pools for profiling)")
     ap.add_argument("--variant", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="variable-length batches: the plain call (its two kernels one after the other)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     return ap.parse_args()
@@ -538,8 +540,11 @@ def varlen_flops(wl) -> float:
 
 
 def run_varlen(args, ws, rank, local):
-    """The mixed decode + prefill batch through paged_attn_fwd_varlen (one grid); for context the
-    same batch as two uniform launches (decode kernel + tcgen05 prefill) is timed too."""
+    """The mixed decode + prefill batch through paged_attn_fwd_varlen_overlap: the host-side hint
+    (the batch's work split, from its host arrays as a serving scheduler holds them) lets the tcgen05
+    kernel (prefill chunks) and the one-grid kernel (decode sequences) run side by side.  For
+    context the plain call (the two kernels one after the other) and the same batch as two uniform
+    launches are timed too."""
     import torch
     import paged_kv_cache_201_gb300 as pa
     from paged_kv_cache_201_gb300 import workloads as W
@@ -563,11 +568,17 @@ def run_varlen(args, ws, rank, local):
     pl = torch.empty((S, T, Hq), dtype=torch.float32, device=dev) if S > 1 else None
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def make_hint():
+        return pa.paged_attn_varlen_hint(wl.q_start, wl.seq_lens, wl.q_offset, wl.causal, Hq, wl.Hkv, D,
+                                         pa.PA_BF16 if wl.dtype == "bf16" else pa.PA_F16)
+
+    hint = None if args.no_overlap else make_hint()
+
+    def step(h=hint):
         if S == 1:
-            pa.paged_attn_fwd_varlen(q, k, v, bt, sl, qs, wl.causal, qo, 1, wl.scale, out, lse, stream)
+            pa.paged_attn_fwd_varlen(q, k, v, bt, sl, qs, wl.causal, qo, 1, wl.scale, out, lse, stream, hint=h)
         else:
-            pa.paged_attn_fwd_varlen(q, k, v, bt, sl, qs, wl.causal, qo, S, wl.scale, po, pl, stream)
+            pa.paged_attn_fwd_varlen(q, k, v, bt, sl, qs, wl.causal, qo, S, wl.scale, po, pl, stream, hint=h)
             pa.paged_attn_combine(po, pl, out, lse, stream)
 
     def timed(fn, K):
@@ -612,6 +623,7 @@ def run_varlen(args, ws, rank, local):
         pa.paged_attn_fwd(q_dec, k, v, bt[n_pre:], sl[n_pre:], wl.causal, qo[n_pre:], 1, wl.scale, o_dec, l_dec, stream)
 
     ms_two = timed(two_launch, max(10, K // 4)) if S == 1 else None
+    ms_plain = timed(lambda: step(None), max(10, K // 4)) if hint is not None else None
 
     ab = varlen_bytes(wl)
     fl = varlen_flops(wl)
@@ -638,7 +650,7 @@ def run_varlen(args, ws, rank, local):
             q.copy_(q_h, non_blocking=True)
             for dst, src in zip((bt, sl, qs, qo), small):
                 dst.copy_(src, non_blocking=True)
-            step()
+            step(None if args.no_overlap else make_hint())  # the hint from this step's host arrays
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
 
@@ -647,8 +659,9 @@ def run_varlen(args, ws, rank, local):
         db = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
         e2e = {"value": round(job_throughput(ab["total"], ws, e2e_ms), 1), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(hb), "d2h_bytes_per_step": int(db),
-               "api": "paged_attn_fwd_varlen (host q / block table / seq_lens / q_start / q_offset in, "
-                      "host out / lse back)"}
+               "api": ("paged_attn_fwd_varlen" if args.no_overlap else
+                       "paged_attn_varlen_hint + paged_attn_fwd_varlen_overlap") +
+                      " (host q / block table / seq_lens / q_start / q_offset in, host out / lse back)"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -694,13 +707,17 @@ def run_varlen(args, ws, rank, local):
         "bytes_per_step": ab,
         "flops_per_step": fl,
         "roofline": roofline,
+        "api": "paged_attn_fwd_varlen" if hint is None else "paged_attn_fwd_varlen_overlap",
+        "plain_call": None if ms_plain is None else {
+            "ms_per_step": round(ms_plain, 5),
+            "how": "paged_attn_fwd_varlen: the same call with its two kernels one after the other on one stream"},
         "two_launch": None if ms_two is None else {
             "ms_per_step": round(ms_two, 5),
             "how": "the same batch as paged_attn_fwd on the prefill chunks (tcgen05 kernel) then on the "
                    "decode sequences (decode kernel), same stream"},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * (2 if S > 1 else 1),
+        "gpu_launches": K * (2 + (1 if S > 1 else 0)),  # tcgen05 + one-grid kernel (+ the combine)
         "clocks": clk.summary() if not args.no_clocks else None,
     }
     if rank == 0:

@@ -227,6 +227,45 @@ int paged_attn_fwd_varlen(const void *q, const void *k_cache, const void *v_cach
                           int split_kv, float scale, void *out, float *lse, const pa_dims *dims, void *stream);
 
 /*
+ * Work of a variable-length batch split the way paged_attn_fwd_varlen splits it, as the caller's
+ * host-side scheduler knows it (the library itself never reads q_start on the host).
+ *   long_pairs       over the sequences of at least 64 query rows (query tokens x Hq/Hkv >= 64):
+ *                    the sum over their query tokens of the keys each token attends to
+ *   short_kv_tokens  over the other sequences with at least one query token: the sum of seq_lens
+ * The values only steer how many SMs each kernel gets; any values give the same results.
+ */
+typedef struct {
+    int64_t long_pairs;
+    int64_t short_kv_tokens;
+} pa_varlen_hint;
+
+/*
+ * paged_attn_varlen_hint — fills *hint from HOST copies of a batch's q_start [B + 1], seq_lens [B]
+ * and q_offset [B] (NULL as in paged_attn_fwd_varlen), with the reach rules of paged_attn_fwd (a
+ * token sees keys [0, min(seq_len, q_offset + i + 1)) when causal, all seq_len keys otherwise).
+ * dims as for paged_attn_fwd_varlen (q_len = T).  Malformed q_start entries count as no tokens.
+ * Returns PA_OK, or PA_EINVAL for a NULL pointer or bad dims.
+ */
+int paged_attn_varlen_hint(const int32_t *q_start, const int32_t *seq_lens, const int32_t *q_offset, int causal,
+                           const pa_dims *dims, pa_varlen_hint *hint);
+
+/*
+ * paged_attn_fwd_varlen_overlap — paged_attn_fwd_varlen with its two kernels run at the same time
+ * on disjoint SMs: the tcgen05 kernel (sequences of at least 64 query rows; compute-bound) on as
+ * many SMs as balances its estimated time from hint->long_pairs against the short sequences'
+ * K/V read time from hint->short_kv_tokens, and the other kernel (bandwidth-bound) on the rest.
+ * The tcgen05 kernel runs on a high-priority stream that the library creates once per device; it
+ * waits for `stream`'s earlier work and `stream` waits for it, so the call keeps stream order
+ * and works under CUDA graph capture.  Arguments and results are those of paged_attn_fwd_varlen,
+ * bit for bit.  A NULL hint, a batch without sequences of both kinds, or a shape that does not
+ * take the tcgen05 kernel falls back to paged_attn_fwd_varlen's two launches on `stream`.
+ */
+int paged_attn_fwd_varlen_overlap(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_start,
+                                  int causal, const int32_t *q_offset, int split_kv, float scale, void *out,
+                                  float *lse, const pa_dims *dims, const pa_varlen_hint *hint, void *stream);
+
+/*
  * paged_attn_fwd_kvq — paged_attn_fwd over quantized K/V pools.  The pages' sweeps include i8
  * attention (rocMLIR PR #2371, Motivation; rocMLIR PR #2222, reviewed files); this library reads a
  * quantized pool as 8-bit elements with one float32 scale per (page, kv head):

@@ -12,6 +12,8 @@ import ctypes
 import os
 from typing import Optional
 
+import numpy as np
+
 from . import build as _build
 
 __all__ = [
@@ -19,7 +21,8 @@ __all__ = [
     "paged_attn_combine", "paged_attn_plan", "paged_attn_debug_gather", "paged_attn_last_error_word",
     "paged_attn_strerror", "paged_attn_version", "attention", "paged_attn_auto_split",
     "paged_attn_workspace_bytes", "paged_attn_fwd_splitkv", "paged_attn_fwd_splitkv_noalloc", "paged_attn_fwd_kvq",
-    "paged_attn_fwd_kvq_splitkv", "attention_kvq", "paged_attn_fwd_varlen", "attention_varlen", "PA_F32", "PA_F16", "PA_BF16", "PA_FP8_E4M3",
+    "paged_attn_fwd_kvq_splitkv", "attention_kvq", "paged_attn_fwd_varlen", "attention_varlen",
+    "paged_attn_fwd_varlen_overlap", "paged_attn_varlen_hint", "PaVarlenHint", "PA_F32", "PA_F16", "PA_BF16", "PA_FP8_E4M3",
     "PA_INT8",
     "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL", "VARIANT_TC05_PREFILL",
     "VARIANT_MMA_T", "VARIANT_MMA_SPLIT_GROUP",
@@ -35,6 +38,11 @@ class PaDims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("q_len", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("num_pages", ctypes.c_int64), ("bt_stride", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class PaVarlenHint(ctypes.Structure):
+    """pa_varlen_hint: a variable-length batch's work split (``paged_attn_varlen_hint``)."""
+    _fields_ = [("long_pairs", ctypes.c_int64), ("short_kv_tokens", ctypes.c_int64)]
 
 
 class PagedAttnError(RuntimeError):
@@ -85,6 +93,11 @@ def load_library(build_if_missing: bool = False):
     lib.paged_attn_fwd_kvq_splitkv.restype = ctypes.c_int
     lib.paged_attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I32, P, I32, F, P, P, D, P]
     lib.paged_attn_fwd_varlen.restype = ctypes.c_int
+    lib.paged_attn_fwd_varlen_overlap.argtypes = [P, P, P, P, P, P, I32, P, I32, F, P, P, D,
+                                                  ctypes.POINTER(PaVarlenHint), P]
+    lib.paged_attn_fwd_varlen_overlap.restype = ctypes.c_int
+    lib.paged_attn_varlen_hint.argtypes = [P, P, P, I32, D, ctypes.POINTER(PaVarlenHint)]
+    lib.paged_attn_varlen_hint.restype = ctypes.c_int
     lib.paged_attn_debug_gather.argtypes = [P, P, P, D, I32, P, P]
     lib.paged_attn_debug_wait_timeout.argtypes = [ctypes.c_uint32, P]
     lib.paged_attn_debug_wait_timeout.restype = ctypes.c_int
@@ -344,11 +357,34 @@ def paged_attn_fwd_kvq_splitkv(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     _raise(rc, "paged_attn_fwd_kvq_splitkv")
 
 
+def paged_attn_varlen_hint(q_start, seq_lens, q_offset, causal, num_q_heads, num_kv_heads,
+                           head_dim=128, dtype=PA_BF16) -> "PaVarlenHint":
+    """The work split of a variable-length batch from HOST arrays (numpy or CPU tensors): q_start
+    [B + 1], seq_lens [B], q_offset [B] or None; see ``paged_attn_varlen_hint`` in
+    include/paged_attn.h."""
+    qs = np.ascontiguousarray(np.asarray(q_start), dtype=np.int32)
+    sl = np.ascontiguousarray(np.asarray(seq_lens), dtype=np.int32)
+    qo = None if q_offset is None else np.ascontiguousarray(np.asarray(q_offset), dtype=np.int32)
+    B = sl.shape[0]
+    if qs.shape[0] != B + 1 or (qo is not None and qo.shape[0] != B):
+        raise ValueError("q_start must hold B + 1 entries and q_offset B")
+    T = int(qs[-1]) if B else 0
+    dims = PaDims(B, max(T, 0), int(num_q_heads), int(num_kv_heads), int(head_dim), 16, 1, 1, int(dtype))
+    hint = PaVarlenHint()
+    rc = load_library().paged_attn_varlen_hint(qs.ctypes.data, sl.ctypes.data,
+                                               None if qo is None else qo.ctypes.data, int(bool(causal)),
+                                               ctypes.byref(dims), ctypes.byref(hint))
+    _raise(rc, "paged_attn_varlen_hint")
+    return hint
+
+
 def paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, split_kv, scale,
-                          out, lse, stream=None) -> None:
+                          out, lse, stream=None, hint=None) -> None:
     """Forward over a batch with a different query count per sequence; see ``paged_attn_fwd_varlen``
     in include/paged_attn.h.  q [T, Hq, D] packed, q_start int32 [B + 1]; out [T, Hq, D] (S = 1) or
-    float32 [S, T, Hq, D]; lse [T, Hq] or [S, T, Hq]."""
+    float32 [S, T, Hq, D]; lse [T, Hq] or [S, T, Hq].  With ``hint`` (a ``PaVarlenHint``, see
+    ``paged_attn_varlen_hint``) the call is ``paged_attn_fwd_varlen_overlap``: the same results, its
+    two kernels side by side."""
     torch = _torch()
     _check(q, "q", ndim=3)
     _check(k_cache, "k_cache", q.dtype, 4)
@@ -367,10 +403,22 @@ def paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, c
     if D2 != D or q_start.shape[0] != B + 1 or seq_lens.shape[0] != B:
         raise ValueError("q / k_cache / block_table / q_start / seq_lens shapes disagree")
     dims = PaDims(B, T, Hq, Hkv, D, ps, P, block_table.shape[1], _dtype_code(q))
-    rc = load_library().paged_attn_fwd_varlen(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(q_start), int(bool(causal)),
-        _ptr(q_offset), int(split_kv), float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _stream(stream))
-    _raise(rc, "paged_attn_fwd_varlen")
+    args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(q_start),
+            int(bool(causal)), _ptr(q_offset), int(split_kv), float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims))
+    if hint is None:
+        rc = load_library().paged_attn_fwd_varlen(*args, _stream(stream))
+        _raise(rc, "paged_attn_fwd_varlen")
+    else:
+        rc = load_library().paged_attn_fwd_varlen_overlap(*args, ctypes.byref(hint), _stream(stream))
+        _raise(rc, "paged_attn_fwd_varlen_overlap")
+
+
+def paged_attn_fwd_varlen_overlap(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, split_kv,
+                                  scale, out, lse, hint, stream=None) -> None:
+    """``paged_attn_fwd_varlen`` with its two kernels side by side on disjoint SMs (``hint`` a
+    ``PaVarlenHint``)."""
+    paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, split_kv, scale,
+                          out, lse, stream, hint if hint is not None else PaVarlenHint())
 
 
 def paged_attn_combine(part_out, part_lse, out, lse=None, stream=None) -> None:

@@ -469,9 +469,47 @@ int paged_attn_fwd_kvq_splitkv(const void *q, const void *k_cache, const void *v
                         });
 }
 
-int paged_attn_fwd_varlen(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
-                          const int32_t *seq_lens, const int32_t *q_start, int causal, const int32_t *q_offset,
-                          int split_kv, float scale, void *out, float *lse, const pa_dims *dims, void *stream) {
+namespace {
+
+// The tcgen05 kernel's stream for paged_attn_fwd_varlen_overlap: one per device, created on first
+// use at the highest priority, so that when both kernels are ready its CTAs are placed first.
+int overlap_stream(cudaStream_t *out) {
+    static std::mutex mu;
+    static cudaStream_t streams[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ECUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!streams[dev]) {
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return PA_ECUDA;
+        if (cudaStreamCreateWithPriority(&streams[dev], cudaStreamNonBlocking, greatest) != cudaSuccess)
+            return PA_ECUDA;
+    }
+    *out = streams[dev];
+    return PA_OK;
+}
+
+// SMs for the tcgen05 kernel when it runs beside the short-sequence kernel: as many as make its
+// estimated time equal the short sequences' K/V read time.  The rates are the kernels' measured
+// ones on GB300 (useful flops per SM of causal prefill tiles; the decode kernel's read rate); 0 when
+// the batch has no work of one kind (nothing to overlap).
+int overlap_sms(const pa_dims *d, const pa_varlen_hint *h, int sms) {
+    if (!h || h->long_pairs <= 0 || h->short_kv_tokens <= 0 || sms < 16) return 0;
+    const double flops = 4.0 * d->head_dim * d->num_q_heads * (double)h->long_pairs;
+    const double flops_per_sm = d->dtype == PA_BF16 ? 4.4e12 : 5.8e12;
+    const double esz = d->dtype == PA_F32 ? 4.0 : 2.0;
+    const double bytes = 2.0 * (double)h->short_kv_tokens * d->num_kv_heads * d->head_dim * esz;
+    const double t_short = bytes / 6.9e12;
+    double n = ceil(flops / (flops_per_sm * t_short));
+    if (n < 8) n = 8;
+    if (n > sms * 3 / 4) n = sms * 3 / 4;  // keep enough SMs streaming the short sequences' pages
+    return (int)n;
+}
+
+int varlen_call(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                const int32_t *seq_lens, const int32_t *q_start, int causal, const int32_t *q_offset, int split_kv,
+                float scale, void *out, float *lse, const pa_dims *dims, const pa_varlen_hint *hint,
+                void *stream) {
     int rc = check_dims(dims);
     if (rc != PA_OK) return rc;
     if (dims->dtype == PA_F32) return PA_EDTYPE;
@@ -493,22 +531,96 @@ int paged_attn_fwd_varlen(const void *q, const void *k_cache, const void *v_cach
     p.rows = 0;
     p.rows_total = (long long)dims->q_len * dims->num_q_heads;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // Sequences of at least 64 query rows go to the tcgen05 kernel when it takes the shape (it
-    // finds them on the device, from q_start); the one-grid kernel takes the rest, or everything.
-    if (tc05_supports(dims) && scale > 0.f && dims->batch <= pa::kTc05VarlenMaxBatch) {
-        CUtensorMap tmq, tmk5, tmv5, tmo;
-        if ((rc = make_q_map(&tmq, q, dims, true)) != PA_OK) return rc;
-        if ((rc = make_pool_map(&tmk5, k_cache, dims, 1)) != PA_OK) return rc;
-        if ((rc = make_pool_map(&tmv5, v_cache, dims, 1)) != PA_OK) return rc;
-        if ((rc = make_tc05_out_map(&tmo, out, dims, split_kv, true)) != PA_OK) return rc;
-        rc = cuda_status(pa::launch_tc05_varlen(p, dims->q_len, dims->dtype, tmq, tmk5, tmv5, tmo, st));
-        if (rc != PA_OK) return rc;
-        p.varlen_rows_cap = 64;
-    }
     CUtensorMap tmk, tmv;
     if ((rc = make_pool_map(&tmk, k_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
     if ((rc = make_pool_map(&tmv, v_cache, dims, dims->head_dim / 64)) != PA_OK) return rc;
-    return cuda_status(pa::launch_mma_varlen(p, dims->q_len, dims->dtype, tmk, tmv, st));
+    // Sequences of at least 64 query rows go to the tcgen05 kernel when it takes the shape (it
+    // finds them on the device, from q_start); the one-grid kernel takes the rest, or everything.
+    if (!(tc05_supports(dims) && scale > 0.f && dims->batch <= pa::kTc05VarlenMaxBatch))
+        return cuda_status(pa::launch_mma_varlen(p, dims->q_len, dims->dtype, tmk, tmv, st));
+    CUtensorMap tmq, tmk5, tmv5, tmo;
+    if ((rc = make_q_map(&tmq, q, dims, true)) != PA_OK) return rc;
+    if ((rc = make_pool_map(&tmk5, k_cache, dims, 1)) != PA_OK) return rc;
+    if ((rc = make_pool_map(&tmv5, v_cache, dims, 1)) != PA_OK) return rc;
+    if ((rc = make_tc05_out_map(&tmo, out, dims, split_kv, true)) != PA_OK) return rc;
+    pa::FwdParams ps = p;
+    ps.varlen_rows_cap = 64;  // the one-grid kernel leaves those sequences to the tcgen05 kernel
+    const int n_long = overlap_sms(dims, hint, device_sm_count());
+    if (n_long == 0) {  // one after the other on the caller's stream
+        rc = cuda_status(pa::launch_tc05_varlen(p, dims->q_len, dims->dtype, tmq, tmk5, tmv5, tmo, 0, st));
+        if (rc != PA_OK) return rc;
+        return cuda_status(pa::launch_mma_varlen(ps, dims->q_len, dims->dtype, tmk, tmv, st));
+    }
+    // Side by side: fork the tcgen05 kernel onto the high-priority stream after the caller's earlier
+    // work, launch the short-sequence kernel on the caller's stream, and join.
+    cudaStream_t hi = nullptr;
+    if ((rc = overlap_stream(&hi)) != PA_OK) return rc;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return PA_ECUDA;
+    if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventDestroy(fork);
+        return PA_ECUDA;
+    }
+    cudaError_t e = cudaEventRecord(fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hi, fork, 0);
+    cudaError_t e_long = cudaSuccess, e_short = cudaSuccess;
+    if (e == cudaSuccess) {
+        e_long = pa::launch_tc05_varlen(p, dims->q_len, dims->dtype, tmq, tmk5, tmv5, tmo, n_long, hi);
+        e = cudaEventRecord(join, hi);  // recorded even if the launch failed, so the join below holds
+        e_short = pa::launch_mma_varlen(ps, dims->q_len, dims->dtype, tmk, tmv, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, join, 0);
+    }
+    cudaEventDestroy(fork);
+    cudaEventDestroy(join);
+    if (e == cudaSuccess) e = e_long != cudaSuccess ? e_long : e_short;
+    return cuda_status(e);
+}
+
+}  // namespace
+
+int paged_attn_fwd_varlen(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                          const int32_t *seq_lens, const int32_t *q_start, int causal, const int32_t *q_offset,
+                          int split_kv, float scale, void *out, float *lse, const pa_dims *dims, void *stream) {
+    return varlen_call(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, split_kv, scale, out,
+                       lse, dims, nullptr, stream);
+}
+
+int paged_attn_fwd_varlen_overlap(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_start,
+                                  int causal, const int32_t *q_offset, int split_kv, float scale, void *out,
+                                  float *lse, const pa_dims *dims, const pa_varlen_hint *hint, void *stream) {
+    return varlen_call(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, split_kv, scale, out,
+                       lse, dims, hint, stream);
+}
+
+int paged_attn_varlen_hint(const int32_t *q_start, const int32_t *seq_lens, const int32_t *q_offset, int causal,
+                           const pa_dims *dims, pa_varlen_hint *hint) {
+    if (!q_start || !seq_lens || !hint) return PA_EINVAL;
+    int rc = check_dims(dims);
+    if (rc != PA_OK) return rc;
+    const int64_t T = dims->q_len, G = dims->num_q_heads / dims->num_kv_heads;
+    int64_t long_pairs = 0, short_kv = 0;
+    for (int64_t b = 0; b < dims->batch; ++b) {
+        const int64_t a = q_start[b], e = q_start[b + 1];
+        if (a < 0 || e > T || e <= a) continue;  // no tokens (or a malformed entry)
+        const int64_t n = e - a, L = seq_lens[b] > 0 ? seq_lens[b] : 0;
+        if (n * G < 64) {
+            short_kv += L;
+            continue;
+        }
+        if (!causal) {
+            long_pairs += n * L;
+            continue;
+        }
+        const int64_t qoff = q_offset ? (int64_t)q_offset[b] : L - n;
+        for (int64_t i = 0; i < n; ++i) {  // token i sees keys [0, min(L, qoff + i + 1))
+            const int64_t reach = qoff + i + 1;
+            long_pairs += reach <= 0 ? 0 : (reach < L ? reach : L);
+        }
+    }
+    hint->long_pairs = long_pairs;
+    hint->short_kv_tokens = short_kv;
+    return PA_OK;
 }
 
 int paged_attn_combine(const float *part_out, const float *part_lse, int split_kv, int64_t rows, int head_dim,

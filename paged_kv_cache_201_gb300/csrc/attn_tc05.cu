@@ -817,10 +817,13 @@ static int num_sms_of_current_device() {
     return cached[dev];
 }
 
+// One persistent CTA per SM, or per SM of the first max_ctas (> 0) when the kernel shares the GPU
+// with another one running at the same time; any grid up to the unit count computes the same
+// results, since a unit's work does not depend on the CTA that takes it.
 template <typename T, bool PART, bool VARLEN>
 static cudaError_t launch_tc05_t(const FwdParams &p, long long total_q, const CUtensorMap &tmq,
                                  const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmo,
-                                 cudaStream_t stream) {
+                                 int max_ctas, cudaStream_t stream) {
     auto kern = paged_attn_tc05_kernel<T, PART, VARLEN>;
     const size_t smem = tc05_smem_bytes();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -853,8 +856,9 @@ static cudaError_t launch_tc05_t(const FwdParams &p, long long total_q, const CU
     const long long units = nb * p.split_kv * p.Hkv * q.row_tiles;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const int sms = num_sms_of_current_device();
+    int sms = num_sms_of_current_device();
     if (sms <= 0) return cudaErrorInvalidDevice;
+    if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
     const int grid = (int)(units < sms ? units : sms);
     const bool bf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t iqk = tc05::idesc_f16(bf, false, 128, 128);
@@ -866,24 +870,24 @@ static cudaError_t launch_tc05_t(const FwdParams &p, long long total_q, const CU
 template <bool VARLEN>
 static cudaError_t launch_tc05_any(const FwdParams &p, long long total_q, int dtype, const CUtensorMap &tmq,
                                    const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmo,
-                                   cudaStream_t stream) {
+                                   int max_ctas, cudaStream_t stream) {
     const bool part = p.split_kv > 1;
     if (dtype == PA_BF16)
-        return part ? launch_tc05_t<__nv_bfloat16, true, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, stream)
-                    : launch_tc05_t<__nv_bfloat16, false, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, stream);
-    return part ? launch_tc05_t<__half, true, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, stream)
-                : launch_tc05_t<__half, false, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, stream);
+        return part ? launch_tc05_t<__nv_bfloat16, true, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, max_ctas, stream)
+                    : launch_tc05_t<__nv_bfloat16, false, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, max_ctas, stream);
+    return part ? launch_tc05_t<__half, true, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, max_ctas, stream)
+                : launch_tc05_t<__half, false, VARLEN>(p, total_q, tmq, tmk, tmv, tmo, max_ctas, stream);
 }
 
 cudaError_t launch_tc05(const FwdParams &p, int dtype, const CUtensorMap &tmq, const CUtensorMap &tmk,
                         const CUtensorMap &tmv, const CUtensorMap &tmo, cudaStream_t stream) {
-    return launch_tc05_any<false>(p, 0, dtype, tmq, tmk, tmv, tmo, stream);
+    return launch_tc05_any<false>(p, 0, dtype, tmq, tmk, tmv, tmo, 0, stream);
 }
 
 cudaError_t launch_tc05_varlen(const FwdParams &p, long long total_q, int dtype, const CUtensorMap &tmq,
                                const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmo,
-                               cudaStream_t stream) {
-    return launch_tc05_any<true>(p, total_q, dtype, tmq, tmk, tmv, tmo, stream);
+                               int max_ctas, cudaStream_t stream) {
+    return launch_tc05_any<true>(p, total_q, dtype, tmq, tmk, tmv, tmo, max_ctas, stream);
 }
 
 }  // namespace pa

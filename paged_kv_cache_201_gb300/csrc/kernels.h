@@ -42,11 +42,11 @@ size_t tc05_smem_bytes();
 cudaError_t launch_tc05(const FwdParams &p, int dtype, const CUtensorMap &tmq, const CUtensorMap &tmk,
                         const CUtensorMap &tmv, const CUtensorMap &tmo, cudaStream_t stream);
 // Variable-length batch (p.q_start, total_q packed tokens, at most kTc05VarlenMaxBatch sequences):
-// the sequences of at least 64 query rows.
+// the sequences of at least 64 query rows, on at most max_ctas SMs (0: every SM).
 constexpr int kTc05VarlenMaxBatch = 1024;
 cudaError_t launch_tc05_varlen(const FwdParams &p, long long total_q, int dtype, const CUtensorMap &tmq,
                                const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmo,
-                               cudaStream_t stream);
+                               int max_ctas, cudaStream_t stream);
 cudaError_t launch_simt(const FwdParams &p, int dtype, cudaStream_t stream);
 // One query row per (sequence, kv head), bf16/f16, head_dim 64/128: CUDA cores over the TMA ring.
 cudaError_t launch_simt_decode(const FwdParams &p, int dtype, const CUtensorMap &tmk, const CUtensorMap &tmv,

@@ -6,6 +6,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 import paged_kv_cache_201_gb300 as pa
@@ -197,3 +198,35 @@ def test_fwd_varlen_validation(lib):
 def test_debug_wait_timeout_validation(lib):
     assert lib.paged_attn_debug_wait_timeout(0, None) == EINVAL
     assert lib.paged_attn_debug_wait_timeout(2_000_001, None) == EINVAL
+
+
+def test_varlen_hint_counts(lib):
+    """paged_attn_varlen_hint against a direct count on the host: pairs of the sequences with at least
+    64 query rows (causal reach with and without offsets), K/V tokens of the others; malformed
+    q_start entries count as no tokens."""
+    rng = np.random.default_rng(3)
+    for causal in (True, False):
+        for with_offset in (True, False):
+            for G in (1, 4, 8):
+                q_lens = rng.choice([0, 1, 1, 2, 7, 16, 40, 100, 300], size=23)
+                B = q_lens.size
+                q_start = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+                seq_lens = (q_lens + rng.integers(0, 500, size=B)).astype(np.int32)
+                q_offset = (rng.integers(-20, 400, size=B).astype(np.int32) if with_offset else None)
+                h = pa.paged_attn_varlen_hint(q_start, seq_lens, q_offset, causal, 8 * G, 8)
+                want_long = want_short = 0
+                for b in range(B):
+                    n, L = int(q_lens[b]), int(seq_lens[b])
+                    if n == 0:
+                        continue
+                    if n * G < 64:
+                        want_short += L
+                        continue
+                    qoff = int(q_offset[b]) if q_offset is not None else L - n
+                    for i in range(n):
+                        want_long += min(L, max(0, qoff + i + 1)) if causal else L
+                assert (h.long_pairs, h.short_kv_tokens) == (want_long, want_short)
+    # T = q_start[B] = 300: a decreasing pair and entries past T count as no tokens
+    qs = np.array([0, 100, 50, 20_000, 300], dtype=np.int32)
+    h = pa.paged_attn_varlen_hint(qs, np.array([300, 300, 300, 300], dtype=np.int32), None, True, 32, 8)
+    assert h.long_pairs == sum(range(201, 301)) and h.short_kv_tokens == 0

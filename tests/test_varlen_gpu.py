@@ -35,8 +35,9 @@ def _device(wl, k=None, v=None):
     return d
 
 
-def _run(pa, wl, d, S):
-    """Returns float64 numpy out [T, Hq, D], lse [T, Hq] (+ part_out / part_lse for S > 1)."""
+def _run(pa, wl, d, S, hint=None):
+    """Returns float64 numpy out [T, Hq, D], lse [T, Hq] (+ part_out / part_lse for S > 1).  With
+    ``hint`` the call is the overlapped one."""
     import torch
     T, Hq, D = wl.Sq, wl.Hq, wl.D
     res = {}
@@ -44,12 +45,12 @@ def _run(pa, wl, d, S):
         out = torch.empty_like(d["q"])
         lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
         pa.paged_attn_fwd_varlen(d["q"], d["k"], d["v"], d["bt"], d["sl"], d["qs"], wl.causal, d["qo"], 1, wl.scale,
-                                 out, lse)
+                                 out, lse, hint=hint)
     else:
         po = torch.empty((S, T, Hq, D), dtype=torch.float32, device="cuda")
         pl = torch.empty((S, T, Hq), dtype=torch.float32, device="cuda")
         pa.paged_attn_fwd_varlen(d["q"], d["k"], d["v"], d["bt"], d["sl"], d["qs"], wl.causal, d["qo"], S, wl.scale,
-                                 po, pl)
+                                 po, pl, hint=hint)
         out = torch.empty_like(d["q"])
         lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
         pa.paged_attn_combine(po, pl, out, lse)
@@ -173,6 +174,55 @@ def test_long_sequences_on_tcgen05(pa, Hq, Hkv, S):
     assert pa.paged_attn_last_error_word() == 0
 
 
+# ----------------------------------------------------------------------------- overlapped call
+def _hint(pa, wl, kind):
+    h = pa.paged_attn_varlen_hint(wl.q_start, wl.seq_lens, wl.q_offset, wl.causal, wl.Hq, wl.Hkv, wl.D,
+                                  pa.PA_BF16 if wl.dtype == "bf16" else pa.PA_F16)
+    if kind == "long_heavy":    # the tcgen05 kernel gets its largest share of the SMs
+        h.long_pairs *= 1000
+    elif kind == "short_heavy":  # and its smallest
+        h.short_kv_tokens *= 1000
+    return h
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("S", [1, 3])
+@pytest.mark.parametrize("kind", ["computed", "long_heavy", "short_heavy"])
+def test_overlap_bit_identical(pa, dtype, S, kind):
+    """paged_attn_fwd_varlen_overlap runs the tcgen05 kernel (long sequences) beside the one-grid
+    kernel on a share of the SMs that the hint sets; a unit's work does not depend on the CTA or SM
+    that takes it, so every output is bit-identical to paged_attn_fwd_varlen's, whatever the share."""
+    rng = np.random.default_rng(7 + S)
+    q_lens = [300, 1, 1, 200, 17, 0, 64, 3] + [1] * 40 + [130, 2]
+    qo = [int(x) for x in rng.integers(0, 600, size=len(q_lens))]
+    seq_lens = [o + q for o, q in zip(qo, q_lens)]
+    wl = W.make_varlen(dtype=dtype, Hq=32, Hkv=8, D=128, page_size=16, q_offset=qo, seed=123 + S,
+                       q_lens=q_lens, seq_lens=seq_lens)
+    d = _device(wl)
+    h = _hint(pa, wl, kind)
+    assert h.long_pairs > 0 and h.short_kv_tokens > 0
+    plain = _run(pa, wl, d, S)
+    over = _run(pa, wl, d, S, hint=h)
+    for key in plain:
+        assert np.array_equal(plain[key], over[key], equal_nan=True), key
+    if kind == "computed":
+        _compare(over, _oracle(wl, S), wl, S, f"overlap {dtype} S={S}")
+    assert pa.paged_attn_last_error_word() == 0
+
+
+def test_overlap_falls_back_without_both_kinds(pa):
+    """A hint with no short work (or a batch the tcgen05 kernel does not take) gives the plain call."""
+    q_lens = [100, 90, 1]
+    wl = W.make_varlen(dtype="bf16", Hq=32, Hkv=8, D=128, page_size=16, q_offset=[10, 0, 200], seed=5,
+                       q_lens=q_lens, seq_lens=[110, 90, 201])
+    d = _device(wl)
+    plain = _run(pa, wl, d, 1)
+    for h in (pa.PaVarlenHint(0, 0), pa.PaVarlenHint(10 ** 9, 0), pa.PaVarlenHint(0, 10 ** 9)):
+        over = _run(pa, wl, d, 1, hint=h)
+        for key in plain:
+            assert np.array_equal(plain[key], over[key], equal_nan=True), key
+
+
 # ----------------------------------------------------------------------------- full size
 @pytest.fixture(scope="module")
 def mixed_full():
@@ -210,4 +260,24 @@ def test_mixed_decode_prefill_full(pa, mixed_full):
         ref_lse.append(r["lse"])
     _gpu.assert_close(res["out"][sel], np.stack(ref_out), "bf16", "mixed full out")
     _gpu.assert_close(res["lse"][sel], np.stack(ref_lse), "bf16", "mixed full lse")
+    assert pa.paged_attn_last_error_word() == 0
+
+
+def test_mixed_decode_prefill_full_overlap(pa, mixed_full):
+    """The benchmarked mixed batch through the overlapped call: every output element equals the
+    plain call's."""
+    import torch
+    wl, kd, vd, k, v = mixed_full
+    d = _device(wl, kd, vd)
+    h = _hint(pa, wl, "computed")
+    outs = []
+    for hint in (None, h):
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((wl.Sq, wl.Hq), dtype=torch.float32, device="cuda")
+        pa.paged_attn_fwd_varlen(d["q"], d["k"], d["v"], d["bt"], d["sl"], d["qs"], wl.causal, d["qo"], 1, wl.scale,
+                                 out, lse, hint=hint)
+        outs.append((out, lse))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1].view(torch.int32), outs[1][1].view(torch.int32))
     assert pa.paged_attn_last_error_word() == 0
