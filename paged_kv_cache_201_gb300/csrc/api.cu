@@ -489,10 +489,13 @@ int overlap_stream(cudaStream_t *out) {
     return PA_OK;
 }
 
-// SMs for the tcgen05 kernel when it runs beside the short-sequence kernel: as many as make its
-// estimated time equal the short sequences' K/V read time.  The rates are the kernels' measured
-// ones on GB300 (useful flops per SM of causal prefill tiles; the decode kernel's read rate); 0 when
-// the batch has no work of one kind (nothing to overlap).
+// SMs for the tcgen05 kernel when it runs beside the short-sequence kernel: about as many as make
+// its estimated time equal the short sequences' K/V read time.  The rates are the kernels' measured
+// ones on GB300 (useful flops per SM of causal prefill tiles; the decode kernel's read rate).  The
+// estimate is raised by 1.3 because the two errors cost differently: on the mixed benchmark batch,
+// half the balancing share made the call 1.9 times slower, twice the share only 1.02 times, and
+// 1.2-1.5 times the share was fastest.  0 when the batch has no work of one kind (nothing to
+// overlap).
 int overlap_sms(const pa_dims *d, const pa_varlen_hint *h, int sms) {
     if (!h || h->long_pairs <= 0 || h->short_kv_tokens <= 0 || sms < 16) return 0;
     const double flops = 4.0 * d->head_dim * d->num_q_heads * (double)h->long_pairs;
@@ -500,7 +503,7 @@ int overlap_sms(const pa_dims *d, const pa_varlen_hint *h, int sms) {
     const double esz = d->dtype == PA_F32 ? 4.0 : 2.0;
     const double bytes = 2.0 * (double)h->short_kv_tokens * d->num_kv_heads * d->head_dim * esz;
     const double t_short = bytes / 6.9e12;
-    double n = ceil(flops / (flops_per_sm * t_short));
+    double n = ceil(1.3 * flops / (flops_per_sm * t_short));
     if (n < 8) n = 8;
     if (n > sms * 3 / 4) n = sms * 3 / 4;  // keep enough SMs streaming the short sequences' pages
     return (int)n;
