@@ -817,9 +817,9 @@ static int num_sms_of_current_device() {
     return cached[dev];
 }
 
-// One persistent CTA per SM, or per SM of the first max_ctas (> 0) when the kernel shares the GPU
-// with another one running at the same time; any grid up to the unit count computes the same
-// results, since a unit's work does not depend on the CTA that takes it.
+// One persistent CTA per SM; max_ctas > 0 caps the grid when the kernel shares the GPU with another
+// kernel running at the same time.  Any grid up to the unit count computes the same results, since
+// a unit's work does not depend on the CTA that takes it.
 template <typename T, bool PART, bool VARLEN>
 static cudaError_t launch_tc05_t(const FwdParams &p, long long total_q, const CUtensorMap &tmq,
                                  const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmo,
