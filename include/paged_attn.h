@@ -251,9 +251,11 @@ int paged_attn_varlen_hint(const int32_t *q_start, const int32_t *seq_lens, cons
 
 /*
  * paged_attn_fwd_varlen_overlap — paged_attn_fwd_varlen with its two kernels run at the same time
- * on disjoint SMs: the tcgen05 kernel (sequences of at least 64 query rows; compute-bound) on as
- * many SMs as balances its estimated time from hint->long_pairs against the short sequences'
- * K/V read time from hint->short_kv_tokens, and the other kernel (bandwidth-bound) on the rest.
+ * on disjoint SMs.  The tcgen05 kernel takes the sequences of at least 64 query rows and is
+ * compute-bound; the other kernel is bandwidth-bound and runs on the remaining SMs.  The tcgen05
+ * kernel's SM count balances its estimated time (from hint->long_pairs) against the short
+ * sequences' K/V read time (from hint->short_kv_tokens), raised by 1.3 and kept within
+ * [8, 3/4 of the SMs].
  * The tcgen05 kernel runs on a high-priority stream that the library creates once per device; it
  * waits for `stream`'s earlier work and `stream` waits for it, so the call keeps stream order
  * and works under CUDA graph capture.  Arguments and results are those of paged_attn_fwd_varlen,

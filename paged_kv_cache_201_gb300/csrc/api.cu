@@ -4,6 +4,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -170,15 +171,15 @@ bool split_group_fits(const pa_dims *d, int split_kv) {
 
 // Multiprocessor count of the current device (cached per device; 152 if it cannot be read).
 int device_sm_count() {
-    static int cached[64];
+    static std::atomic<int> cached[kMaxDevices];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-    if (!cached[dev]) {
-        int v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (!v) {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 152;
-        cached[dev] = v;
+        cached[dev].store(v, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return v;
 }
 
 bool tc05_supports(const pa_dims *d) {

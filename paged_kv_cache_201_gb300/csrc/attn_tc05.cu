@@ -29,6 +29,7 @@
 // Instantiations: PART (split_kv > 1's fp32 partials, or the final rows) x VARLEN (a batch of
 // sequences with their own query counts, whose units are blocks of the packed rows).  The row
 // maximum is taken over unscaled scores, so the host launches this kernel only for scale > 0.
+#include <atomic>
 #include <type_traits>
 
 #include "kernels.h"
@@ -806,15 +807,15 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 size_t tc05_smem_bytes() { return (size_t)(kT5Tile * 6 + 4 * kT5Stage + 1024); }
 
 static int num_sms_of_current_device() {
-    static int cached[128];
+    static std::atomic<int> cached[128];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
-    if (!cached[dev]) {
-        int v = 0;
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (!v) {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cached[dev] = v;
+        cached[dev].store(v, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return v;
 }
 
 // One persistent CTA per SM; max_ctas > 0 caps the grid when the kernel shares the GPU with another
@@ -830,14 +831,16 @@ static cudaError_t launch_tc05_t(const FwdParams &p, long long total_q, const CU
     if (e != cudaSuccess) return e;
     // The softmax warpgroups' setmaxnreg increase is served from what the launch holds: a build
     // that gave the kernel fewer registers per thread would leave them waiting, so refuse it.
-    static int launch_regs = 0;
-    if (!launch_regs) {
+    static std::atomic<int> launch_regs{0};
+    int regs = launch_regs.load(std::memory_order_relaxed);
+    if (!regs) {
         cudaFuncAttributes fa;
         e = cudaFuncGetAttributes(&fa, kern);
         if (e != cudaSuccess) return e;
-        launch_regs = fa.numRegs;
+        regs = fa.numRegs;
+        launch_regs.store(regs, std::memory_order_relaxed);
     }
-    if (launch_regs < kT5LaunchRegs) return cudaErrorInvalidConfiguration;
+    if (regs < kT5LaunchRegs) return cudaErrorInvalidConfiguration;
     int ps_shift = 0, g_shift = 0;
     while ((1 << ps_shift) < p.ps) ++ps_shift;
     while ((1 << g_shift) < p.G) ++g_shift;
