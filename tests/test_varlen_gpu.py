@@ -281,3 +281,40 @@ def test_mixed_decode_prefill_full_overlap(pa, mixed_full):
     assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
     assert torch.equal(outs[0][1].view(torch.int32), outs[1][1].view(torch.int32))
     assert pa.paged_attn_last_error_word() == 0
+
+
+def test_overlap_under_graph_capture(pa):
+    """The overlapped call forks onto the library's stream and joins back, so it can be captured in a
+    CUDA graph; replays give the plain call's outputs bit for bit."""
+    import torch
+    q_lens = [300, 1, 1, 200, 3] + [1] * 20
+    qo = [50 * i for i in range(len(q_lens))]
+    seq_lens = [o + q for o, q in zip(qo, q_lens)]
+    wl = W.make_varlen(dtype="bf16", Hq=32, Hkv=8, D=128, page_size=16, q_offset=qo, seed=77, q_lens=q_lens,
+                       seq_lens=seq_lens)
+    d = _device(wl)
+    h = _hint(pa, wl, "computed")
+    T, Hq = wl.Sq, wl.Hq
+    ref_out, ref_lse = torch.empty_like(d["q"]), torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+    pa.paged_attn_fwd_varlen(d["q"], d["k"], d["v"], d["bt"], d["sl"], d["qs"], wl.causal, d["qo"], 1, wl.scale,
+                             ref_out, ref_lse)
+    out, lse = torch.zeros_like(ref_out), torch.zeros_like(ref_lse)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside the capture (creates the library's stream)
+        pa.paged_attn_fwd_varlen(d["q"], d["k"], d["v"], d["bt"], d["sl"], d["qs"], wl.causal, d["qo"], 1,
+                                 wl.scale, out, lse, stream=s, hint=h)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    out.zero_()
+    lse.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pa.paged_attn_fwd_varlen(d["q"], d["k"], d["v"], d["bt"], d["sl"], d["qs"], wl.causal, d["qo"], 1,
+                                 wl.scale, out, lse, stream=torch.cuda.current_stream(), hint=h)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
+    assert pa.paged_attn_last_error_word() == 0
