@@ -542,8 +542,10 @@ def attention_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, 
 
 
 def attention_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, *, causal: bool = False, q_offset=None,
-                     split_kv: int = 1, scale: Optional[float] = None, want_lse: bool = False, stream=None):
-    """``attention`` for a packed variable-length batch: q [T, Hq, D], q_start [B + 1]."""
+                     split_kv: int = 1, scale: Optional[float] = None, want_lse: bool = False, stream=None,
+                     hint=None):
+    """``attention`` for a packed variable-length batch: q [T, Hq, D], q_start [B + 1].  With
+    ``hint`` (``paged_attn_varlen_hint``) the forward runs its two kernels side by side."""
     torch = _torch()
     T, Hq, D = q.shape
     if scale is None:
@@ -552,11 +554,11 @@ def attention_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, *, cau
     lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if (want_lse or split_kv > 1) else None
     if split_kv == 1:
         paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, 1, scale, out,
-                              lse, stream)
+                              lse, stream, hint)
     else:
         po = torch.empty((split_kv, T, Hq, D), dtype=torch.float32, device=q.device)
         pl = torch.empty((split_kv, T, Hq), dtype=torch.float32, device=q.device)
         paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, split_kv,
-                              scale, po, pl, stream)
+                              scale, po, pl, stream, hint)
         paged_attn_combine(po, pl, out, lse, stream)
     return (out, lse) if want_lse else out
