@@ -59,6 +59,71 @@ __global__ void __launch_bounds__(256) paged_attn_combine_kernel(const float *__
     if (lse && lane == 0) lse[row] = wsum > 0.f ? M + logf(wsum) : kNegInf;
 }
 
+// The same combine for launches with few rows, where a warp's chain of dependent loads (lse, then
+// the partial row, split after split) sets the time rather than DRAM: lane s reads lse_s (S <= 32),
+// the weights reach every lane by shuffle, and the partial rows of SB splits are loaded at once.
+// Sums run over the splits in the same order and with the same operations as above, so the two
+// kernels give the same bits.
+template <typename TO, int D, int SB>
+__global__ void __launch_bounds__(256) paged_attn_combine_wide_kernel(const float *__restrict__ part_out,
+                                                                      const float *__restrict__ part_lse, int S,
+                                                                      long long rows, TO *__restrict__ out,
+                                                                      float *__restrict__ lse) {
+    constexpr int DPL = D / 32;
+    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float l = lane < S ? __ldg(part_lse + (long long)lane * rows + row) : kNegInf;
+    float M = l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float acc[DPL];
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) acc[c] = 0.f;
+    float wsum = 0.f;
+    if (M != kNegInf) {
+        const float wl = expf(l - M);  // exp(-inf) = 0 for lanes past S and empty splits
+        for (int s0 = 0; s0 < S; s0 += SB) {
+            float w[SB], v[SB][DPL];
+#pragma unroll
+            for (int j = 0; j < SB; ++j) {
+                w[j] = __shfl_sync(0xffffffffu, wl, (s0 + j) & 31);
+                if (s0 + j >= S) w[j] = 0.f;
+                const int sj = min(s0 + j, S - 1);  // an address inside the partials even when unread
+                const float *src = part_out + ((long long)sj * rows + row) * D + lane * DPL;
+                if constexpr (DPL % 4 == 0) {
+#pragma unroll
+                    for (int c4 = 0; c4 < DPL; c4 += 4) {
+                        const float4 x = w[j] != 0.f ? __ldg(reinterpret_cast<const float4 *>(src + c4))
+                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[j][c4] = x.x;
+                        v[j][c4 + 1] = x.y;
+                        v[j][c4 + 2] = x.z;
+                        v[j][c4 + 3] = x.w;
+                    }
+                } else {
+                    const float2 x = w[j] != 0.f ? __ldg(reinterpret_cast<const float2 *>(src)) : make_float2(0.f, 0.f);
+                    v[j][0] = x.x;
+                    v[j][1] = x.y;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < SB; ++j) {
+                wsum += w[j];
+                if (w[j] != 0.f) {
+#pragma unroll
+                    for (int c = 0; c < DPL; ++c) acc[c] = fmaf(w[j], v[j][c], acc[c]);
+                }
+            }
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    TO *dst = out + row * D + lane * DPL;
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) dst[c] = from_float<TO>(acc[c] * inv);
+    if (lse && lane == 0) lse[row] = wsum > 0.f ? M + logf(wsum) : kNegInf;
+}
+
 template <typename TO>
 static cudaError_t launch_combine_t(const float *po, const float *pl, int S, long long rows, int D, void *out,
                                     float *lse, cudaStream_t stream) {
@@ -66,6 +131,19 @@ static cudaError_t launch_combine_t(const float *po, const float *pl, int S, lon
     const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // Up to 16384 rows (a warp each: about one wave of resident warps) the launch is latency-bound.
+    if (S <= 32 && rows <= 16384) {
+        if (D == 256)
+            paged_attn_combine_wide_kernel<TO, 256, 8>
+                <<<(unsigned)blocks, kRowsPerBlock * 32, 0, stream>>>(po, pl, S, rows, static_cast<TO *>(out), lse);
+        else if (D == 128)
+            paged_attn_combine_wide_kernel<TO, 128, 8>
+                <<<(unsigned)blocks, kRowsPerBlock * 32, 0, stream>>>(po, pl, S, rows, static_cast<TO *>(out), lse);
+        else
+            paged_attn_combine_wide_kernel<TO, 64, 8>
+                <<<(unsigned)blocks, kRowsPerBlock * 32, 0, stream>>>(po, pl, S, rows, static_cast<TO *>(out), lse);
+        return cudaGetLastError();
+    }
     if (D == 256)
         paged_attn_combine_kernel<TO, 256>
             <<<(unsigned)blocks, kRowsPerBlock * 32, 0, stream>>>(po, pl, S, rows, static_cast<TO *>(out), lse);
