@@ -8,16 +8,19 @@ namespace pa {
 // rocMLIR PR #2371 (Technical Details, f32 combine for narrow floats): per row,
 // M = max_s lse_s, w_s = exp(lse_s - M), out = sum w_s O_s / sum w_s, lse =
 // M + log(sum w_s), all in fp32; M = -inf (every split empty) gives out 0 and
-// lse -inf.  One warp per row; each lane owns D/32 consecutive columns.
+// lse -inf.  One warp per row; each lane owns D/32 consecutive columns.  Rows are taken from the
+// last one back: the forward kernels write the partials in row order, so the rows at the end were
+// written last and are the ones still in L2 when this kernel starts.
 template <typename TO, int D>
 __global__ void __launch_bounds__(256) paged_attn_combine_kernel(const float *__restrict__ part_out,
                                                                  const float *__restrict__ part_lse, int S,
                                                                  long long rows, TO *__restrict__ out,
                                                                  float *__restrict__ lse) {
     constexpr int DPL = D / 32;
-    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const long long idx = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
+    if (idx >= rows) return;
+    const long long row = rows - 1 - idx;
     float M = kNegInf;
     for (int s0 = 0; s0 < S; s0 += 32) {
         const float v = (s0 + lane < S) ? __ldg(part_lse + (long long)(s0 + lane) * rows + row) : kNegInf;
