@@ -229,8 +229,9 @@ def test_bounded_wait_gives_up_and_context_survives(pa):
 @pytest.mark.parametrize("ps,D,dtype", [(16, 128, "bf16"), (32, 64, "f16"), (64, 128, "f16")])
 def test_split_group_decode(pa, S, ps, D, dtype):
     """Decode with short splits (every split at most 8 pages), forced: one CTA per four consecutive
-    splits, one warp per split (the planner takes it for config 3's 1024 splits).  Partial last groups, empty splits inside a group, sentinel tails, 1-3
-    query tokens with causal offsets, every row against the oracle."""
+    splits, one warp per split (the planner takes it for the ragged decode's 1024 splits: B=32,
+    Hkv=4, split 8).  Partial last groups, empty splits inside a group, sentinel tails, 1-3 query
+    tokens with causal offsets, every row against the oracle."""
     lens = [0, 1, 15, ps, ps + 1, 3 * ps - 1, 5 * ps + 3, 8 * ps * S // 2 + 7]
     width = max(-(-max(lens) // ps), 1)
     assert -(-width // S) <= 8
