@@ -708,6 +708,9 @@ def run_varlen(args, ws, rank, local):
         "flops_per_step": fl,
         "roofline": roofline,
         "api": "paged_attn_fwd_varlen" if hint is None else "paged_attn_fwd_varlen_overlap",
+        "overlap_sms": None if hint is None else pa.paged_attn_varlen_overlap_share(
+            hint, torch.cuda.get_device_properties(dev).multi_processor_count, Hq, wl.Hkv, D,
+            pa.PA_BF16 if wl.dtype == "bf16" else pa.PA_F16),
         "plain_call": None if ms_plain is None else {
             "ms_per_step": round(ms_plain, 5),
             "how": "paged_attn_fwd_varlen: the same call with its two kernels one after the other on one stream"},

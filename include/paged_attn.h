@@ -262,6 +262,15 @@ int paged_attn_varlen_hint(const int32_t *q_start, const int32_t *seq_lens, cons
  * bit for bit.  A NULL hint, a batch without sequences of both kinds, or a shape that does not
  * take the tcgen05 kernel falls back to paged_attn_fwd_varlen's two launches on `stream`.
  */
+/*
+ * paged_attn_varlen_overlap_share — the number of SMs paged_attn_fwd_varlen_overlap gives the
+ * tcgen05 kernel for this hint on a GPU of num_sms SMs: 0 when the two kernels would run one
+ * after the other (NULL hint, no work of one kind, fewer than 16 SMs), else within
+ * [8, 3/4 of num_sms].  Host-only; it does not check whether the shape takes the tcgen05 kernel.
+ * Bad dims or num_sms < 1: PA_EINVAL (or the dims error).
+ */
+int paged_attn_varlen_overlap_share(const pa_dims *dims, const pa_varlen_hint *hint, int num_sms);
+
 int paged_attn_fwd_varlen_overlap(const void *q, const void *k_cache, const void *v_cache,
                                   const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_start,
                                   int causal, const int32_t *q_offset, int split_kv, float scale, void *out,

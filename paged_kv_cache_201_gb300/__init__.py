@@ -22,7 +22,7 @@ __all__ = [
     "paged_attn_strerror", "paged_attn_version", "attention", "paged_attn_auto_split",
     "paged_attn_workspace_bytes", "paged_attn_fwd_splitkv", "paged_attn_fwd_splitkv_noalloc", "paged_attn_fwd_kvq",
     "paged_attn_fwd_kvq_splitkv", "attention_kvq", "paged_attn_fwd_varlen", "attention_varlen",
-    "paged_attn_fwd_varlen_overlap", "paged_attn_varlen_hint", "PaVarlenHint", "PA_F32", "PA_F16", "PA_BF16", "PA_FP8_E4M3",
+    "paged_attn_fwd_varlen_overlap", "paged_attn_varlen_hint", "paged_attn_varlen_overlap_share", "PaVarlenHint", "PA_F32", "PA_F16", "PA_BF16", "PA_FP8_E4M3",
     "PA_INT8",
     "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA_DECODE", "VARIANT_MMA_PREFILL", "VARIANT_TC05_PREFILL",
     "VARIANT_MMA_T", "VARIANT_MMA_SPLIT_GROUP",
@@ -98,6 +98,8 @@ def load_library(build_if_missing: bool = False):
     lib.paged_attn_fwd_varlen_overlap.restype = ctypes.c_int
     lib.paged_attn_varlen_hint.argtypes = [P, P, P, I32, D, ctypes.POINTER(PaVarlenHint)]
     lib.paged_attn_varlen_hint.restype = ctypes.c_int
+    lib.paged_attn_varlen_overlap_share.argtypes = [D, ctypes.POINTER(PaVarlenHint), I32]
+    lib.paged_attn_varlen_overlap_share.restype = ctypes.c_int
     lib.paged_attn_debug_gather.argtypes = [P, P, P, D, I32, P, P]
     lib.paged_attn_debug_wait_timeout.argtypes = [ctypes.c_uint32, P]
     lib.paged_attn_debug_wait_timeout.restype = ctypes.c_int
@@ -376,6 +378,17 @@ def paged_attn_varlen_hint(q_start, seq_lens, q_offset, causal, num_q_heads, num
                                                ctypes.byref(dims), ctypes.byref(hint))
     _raise(rc, "paged_attn_varlen_hint")
     return hint
+
+
+def paged_attn_varlen_overlap_share(hint, num_sms, num_q_heads, num_kv_heads, head_dim=128, dtype=PA_BF16) -> int:
+    """SMs the overlapped call gives the tcgen05 kernel for ``hint`` (0: the kernels run one after
+    the other); see ``paged_attn_varlen_overlap_share`` in include/paged_attn.h."""
+    dims = PaDims(1, 1, int(num_q_heads), int(num_kv_heads), int(head_dim), 16, 1, 1, int(dtype))
+    rc = load_library().paged_attn_varlen_overlap_share(ctypes.byref(dims),
+                                                        None if hint is None else ctypes.byref(hint), int(num_sms))
+    if rc < 0:
+        _raise(rc, "paged_attn_varlen_overlap_share")
+    return rc
 
 
 def paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, split_kv, scale,

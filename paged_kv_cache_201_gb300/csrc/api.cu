@@ -597,6 +597,13 @@ int paged_attn_fwd_varlen_overlap(const void *q, const void *k_cache, const void
                        lse, dims, hint, stream);
 }
 
+int paged_attn_varlen_overlap_share(const pa_dims *dims, const pa_varlen_hint *hint, int num_sms) {
+    int rc = check_dims(dims);
+    if (rc != PA_OK) return rc;
+    if (num_sms < 1) return PA_EINVAL;
+    return overlap_sms(dims, hint, num_sms);
+}
+
 int paged_attn_varlen_hint(const int32_t *q_start, const int32_t *seq_lens, const int32_t *q_offset, int causal,
                            const pa_dims *dims, pa_varlen_hint *hint) {
     if (!q_start || !seq_lens || !hint) return PA_EINVAL;

@@ -230,3 +230,29 @@ def test_varlen_hint_counts(lib):
     qs = np.array([0, 100, 50, 20_000, 300], dtype=np.int32)
     h = pa.paged_attn_varlen_hint(qs, np.array([300, 300, 300, 300], dtype=np.int32), None, True, 32, 8)
     assert h.long_pairs == sum(range(201, 301)) and h.short_kv_tokens == 0
+
+
+def test_varlen_overlap_share(lib):
+    """The SM share of the overlapped call: 0 without work of both kinds or with fewer than 16 SMs,
+    the balancing estimate x 1.3 otherwise (57 of 152 SMs for the benchmark's mixed batch, where a
+    sweep measured 1.2-1.5 x the balancing share as fastest), clamped to [8, 3/4 of the SMs],
+    non-decreasing in the long sequences' work, smaller for f16 (its higher tensor rate)."""
+    share = pa.paged_attn_varlen_overlap_share
+    H = pa.PaVarlenHint
+    assert share(None, 152, 32, 8) == 0
+    assert share(H(0, 0), 152, 32, 8) == 0
+    assert share(H(10 ** 9, 0), 152, 32, 8) == 0 and share(H(0, 10 ** 9), 152, 32, 8) == 0
+    assert share(H(7318528, 1048576), 15, 32, 8) == 0
+    assert share(H(7318528, 1048576), 152, 32, 8) == 57
+    flops, t_short = 4.0 * 128 * 32 * 7318528, 2.0 * 1048576 * 8 * 128 * 2 / 6.9e12
+    assert share(H(7318528, 1048576), 152, 32, 8) == math.ceil(1.3 * flops / (4.4e12 * t_short))
+    assert share(H(1, 10 ** 9), 152, 32, 8) == 8
+    assert share(H(10 ** 12, 1), 152, 32, 8) == 114
+    last = 0
+    for lp in (10 ** 5, 10 ** 6, 3 * 10 ** 6, 10 ** 7, 3 * 10 ** 7, 10 ** 8):
+        n = share(H(lp, 1048576), 152, 32, 8)
+        assert 8 <= n <= 114 and n >= last
+        last = n
+    assert share(H(7318528, 1048576), 152, 32, 8, 128, pa.PA_F16) < 57
+    with pytest.raises(pa.PagedAttnError):
+        share(H(1, 1), 0, 32, 8)
