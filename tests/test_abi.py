@@ -256,3 +256,16 @@ def test_varlen_overlap_share(lib):
     assert share(H(7318528, 1048576), 152, 32, 8, 128, pa.PA_F16) < 57
     with pytest.raises(pa.PagedAttnError):
         share(H(1, 1), 0, 32, 8)
+
+
+def test_varlen_hint_binding_checks(lib):
+    """The binding refuses arrays of the wrong lengths; an empty batch gives a zero hint."""
+    with pytest.raises(ValueError):
+        pa.paged_attn_varlen_hint(np.array([0, 3], dtype=np.int32), np.array([5, 6], dtype=np.int32), None, True,
+                                  8, 2)
+    with pytest.raises(ValueError):
+        pa.paged_attn_varlen_hint(np.array([0, 3], dtype=np.int32), np.array([5], dtype=np.int32),
+                                  np.array([1, 2], dtype=np.int32), True, 8, 2)
+    h = pa.paged_attn_varlen_hint(np.array([0], dtype=np.int32), np.zeros(0, dtype=np.int32), None, True, 8, 2)
+    assert (h.long_pairs, h.short_kv_tokens) == (0, 0)
+    assert lib.paged_attn_varlen_hint(None, None, None, 1, None, None) == EINVAL
