@@ -228,7 +228,8 @@ int paged_attn_fwd_varlen(const void *q, const void *k_cache, const void *v_cach
 
 /*
  * Work of a variable-length batch split the way paged_attn_fwd_varlen splits it, as the caller's
- * host-side scheduler knows it (the library itself never reads q_start on the host).
+ * host-side scheduler knows it (the library itself never reads q_start on the host).  This hint and
+ * the calls that take it are this library's own; the pages have no counterpart.
  *   long_pairs       over the sequences of at least 64 query rows (query tokens x Hq/Hkv >= 64):
  *                    the sum over their query tokens of the keys each token attends to
  *   short_kv_tokens  over the other sequences with at least one query token: the sum of seq_lens
@@ -251,7 +252,8 @@ int paged_attn_varlen_hint(const int32_t *q_start, const int32_t *seq_lens, cons
 
 /*
  * paged_attn_fwd_varlen_overlap — paged_attn_fwd_varlen with its two kernels run at the same time
- * on disjoint SMs.  The tcgen05 kernel takes the sequences of at least 64 query rows and is
+ * on disjoint SMs.  The pages' unified entry point (rocm-libraries PR #14349, Performance) serves a
+ * mixed batch in one call; this one keeps the single call and runs its two kernels at once.  The tcgen05 kernel takes the sequences of at least 64 query rows and is
  * compute-bound; the other kernel is bandwidth-bound and runs on the remaining SMs.  The tcgen05
  * kernel's SM count balances its estimated time (from hint->long_pairs) against the short
  * sequences' K/V read time (from hint->short_kv_tokens), raised by 1.3 and kept within
