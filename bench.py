@@ -36,13 +36,13 @@ METRIC = "paged decode KV-read HBM GB/s and % of GB300 peak; µs per decode step
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=250)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode",
                     choices=["llama8b_decode", "over2gib_decode", "ragged_decode", "causal_prefill", "tiny_decode_f32",
                              "llama8b_decode_fp8", "llama8b_decode_int8", "mixed_decode_prefill", "d256_decode",
-                             "mha_decode", "causal_prefill_f16"])
+                             "mha_decode", "causal_prefill_f16", "llama8b_decode_over2gib"])
     ap.add_argument("--split-kv", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences (llama8b/over2gib workloads only; smaller pools for profiling)")
@@ -52,6 +52,8 @@ def parse():
                     help="variable-length batches: the plain call (its two kernels one after the other)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="the Llama-3-8B decode line without its over-2-GiB and prefill keys")
     return ap.parse_args()
 
 
@@ -225,9 +227,21 @@ def recorded_traffic(kernel: str, workload: str, split_kv: int):
     return ent.get("dram_bytes_per_launch")
 
 
+def traffic_fields(kernel: str, workload: str, split_kv: int) -> dict:
+    """``traffic`` and where it comes from: the bench does not run ncu, so the figure is one recorded
+    by an ncu capture of the same kernel, workload and split (profiles/traffic.json), valid only for
+    the kernel sources it was taken on (their digest); null when those sources have changed since."""
+    t = recorded_traffic(kernel, workload, split_kv)
+    return {"traffic": t,
+            "traffic_source": None if t is None else (
+                f"recorded: ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
+                f"profiles/traffic.json entry {kernel}/{workload}/split{split_kv}, "
+                f"kernel source digest {kernel_source_digest(kernel)}")}
+
+
 def build_workload(name, batch=None):
     from paged_kv_cache_201_gb300 import workloads as W
-    if batch is not None and name in ("llama8b_decode", "over2gib_decode", "llama8b_decode_fp8",
+    if batch is not None and name in ("llama8b_decode", "over2gib_decode", "llama8b_decode_fp8", "llama8b_decode_over2gib",
                                       "llama8b_decode_int8", "d256_decode", "mha_decode"):
         return W.make(name, B=batch)
     return W.make(name)
@@ -293,6 +307,208 @@ def l2_text(wl) -> str:
             "each timed step, outside its events")
 
 
+# ----------------------------------------------------------------------------- timing protocol
+N_BATCHES = 5
+
+
+def batch_sizes(K: int, n: int = N_BATCHES):
+    """K timed steps cut into n batches as equal as possible (fewer batches when K < n)."""
+    n = max(1, min(n, K))
+    return [K // n + (1 if j < K % n else 0) for j in range(n)]
+
+
+def timed_batches(fns, K: int, stream, flush=None):
+    """The timing protocol of rocm-libraries PR #14349 (Performance): after the caller's warm-up, the
+    K timed steps run as N_BATCHES batches, each bracketed by CUDA events on the launching stream; a
+    step's time is the median over batches of (batch time / steps in the batch).
+
+    ``fns`` is a list of callables that together make one step; the events around the first one
+    also give its own median time (the forward kernel when the second is the combine).  With
+    ``flush`` (a device buffer larger than L2) the buffer is written before every step and the
+    step's time is the sum of its own events, so the flush is not counted.
+    Returns (ms per step, ms of fns[0] per step)."""
+    import torch
+    sizes = batch_sizes(K)
+    step_ms, first_ms = [], []
+    for j, n in enumerate(sizes):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for i in range(n):
+            if flush is not None:
+                flush.fill_((j * 131 + i) & 0xFF)
+            ev[i][0].record(stream)
+            fns[0]()
+            ev[i][1].record(stream)
+            for f in fns[1:]:
+                f()
+            ev[i][2].record(stream)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        first_ms.append(sum(e[0].elapsed_time(e[1]) for e in ev) / n)
+        if flush is not None:
+            step_ms.append(sum(e[0].elapsed_time(e[2]) for e in ev) / n)
+        else:
+            step_ms.append(b0.elapsed_time(b1) / n)
+    return float(np.median(step_ms)), float(np.median(first_ms))
+
+
+E2E_TIMING = ("value / ms_per_step: host wall clock (time.perf_counter) from a synchronised device to the "
+              "synchronize after the batch's last step, median of batches, so host launch and copy-issue "
+              "costs count; event_value / event_ms_per_step: CUDA events on the stream around the same batches")
+
+
+def e2e_batches(step, K: int, stream):
+    """End-to-end timing of K calls of ``step`` in N_BATCHES batches: each batch starts from a
+    synchronised device and ends with a synchronize.  Returns (median event ms per step, median host
+    wall-clock ms per step)."""
+    import torch
+    ev_ms, wall_ms = [], []
+    for n in batch_sizes(K):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        a.record(stream)
+        for _ in range(n):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        wall_ms.append((time.perf_counter() - t0) * 1e3 / n)
+        ev_ms.append(a.elapsed_time(b) / n)
+    return float(np.median(ev_ms)), float(np.median(wall_ms))
+
+
+# ----------------------------------------------------------------------------- further workloads in the headline line
+def prepare_16bit(wl, S: int, dev, stream, variant: int = 0):
+    """Device tensors of a 16-bit-pool workload and the callables of one step: the forward and, for
+    S > 1, the combine."""
+    import torch
+    import paged_kv_cache_201_gb300 as pa
+    from paged_kv_cache_201_gb300 import workloads as W
+    t = {"q": W.host_to_torch(wl.q, wl.dtype).to(dev)}
+    if wl.k_cache is not None:
+        t["k"], t["v"] = W.host_to_torch(wl.k_cache, wl.dtype).to(dev), W.host_to_torch(wl.v_cache, wl.dtype).to(dev)
+    else:
+        t["k"], t["v"] = W.fill_device_cache(wl, dev)
+    t["bt"] = torch.from_numpy(wl.block_table).to(dev)
+    t["sl"] = torch.from_numpy(wl.seq_lens).to(dev)
+    t["qo"] = None if wl.q_offset is None else torch.from_numpy(wl.q_offset).to(dev)
+    B, Sq, Hq, D = wl.B, wl.Sq, wl.Hq, wl.D
+    t["out"] = torch.empty_like(t["q"])
+    t["lse"] = torch.empty((B, Sq, Hq), dtype=torch.float32, device=dev)
+    if S > 1:
+        t["po"] = torch.empty((S, B, Sq, Hq, D), dtype=torch.float32, device=dev)
+        t["pl"] = torch.empty((S, B, Sq, Hq), dtype=torch.float32, device=dev)
+    o, l = (t["out"], t["lse"]) if S == 1 else (t["po"], t["pl"])
+
+    def fwd():
+        pa.paged_attn_fwd_variant(t["q"], t["k"], t["v"], t["bt"], t["sl"], wl.causal, t["qo"], S, wl.scale, o, l,
+                                  variant, stream)
+
+    fns = [fwd]
+    if S > 1:
+        fns.append(lambda: pa.paged_attn_combine(t["po"], t["pl"], t["out"], t["lse"], stream))
+    return t, fns
+
+
+def warm(fns, n):
+    import torch
+    for _ in range(max(n, 3)):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+
+
+def interleaved_batches(fns_a, fns_b, K: int, stream):
+    """Two workloads timed in alternating batches (a, b, a, b, ...; N_BATCHES each of the K-step
+    protocol), so that both see the same clocks and the same state of the GPU.  Returns the two
+    median ms per step."""
+    import torch
+    ms_a, ms_b = [], []
+    for n in batch_sizes(K):
+        for fns, acc in ((fns_a, ms_a), (fns_b, ms_b)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                for f in fns:
+                    f()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            acc.append(e0.elapsed_time(e1) / n)
+    return float(np.median(ms_a)), float(np.median(ms_b))
+
+
+def extra_workloads(args, dev, stream, headline_fns, headline_bytes, hbm_peak, tensor_peak):
+    """The other targets of the headline in the same run and on the same GPU:
+    - ``over2gib``: the over-2^31-byte decode (B=256, Hq=64, Hkv=4, L=8192, 135168 pages per pool,
+      split 4), every sequence reading pages on both sides of byte 2^31;
+    - ``over2gib_same_shape``: the headline's own shape over pools of 65536 + 2048 pages, every
+      sequence holding pages on both sides of byte 2^31, timed in batches alternating with the
+      headline workload; ``ratio`` is its GB/s over the headline's (1.0 = no slowdown past 2^31);
+    - ``prefill``: the causal prefill (B=4, Sq=1024, GQA 32/8, q_offset up to 3072) at split 8 and 1,
+      useful (causal) flops per second against the measured bf16 burst peak.
+    Each runs the K-step protocol of the headline (warm-up, N_BATCHES batches, median)."""
+    import torch
+    from paged_kv_cache_201_gb300 import workloads as W
+    K = args.steps
+    res = {}
+
+    wl = W.llama8b_decode_over2gib()
+    t, fns = prepare_16bit(wl, 1, dev, stream)
+    warm(fns, args.warmup)
+    warm(headline_fns, 2)
+    ms_ref, ms_hi = interleaved_batches(headline_fns, fns, K, stream)
+    ab = algorithmic_bytes(wl, 1)
+    assert ab["total"] == headline_bytes
+    res["over2gib_same_shape"] = {
+        "workload": "llama8b_decode_over2gib", "num_pages": wl.num_pages, "split_kv": 1,
+        "pool_bytes": pool_bytes(wl), "pages_past_2gib_per_sequence": int(
+            (wl.block_table >= W.LLAMA_OVER2G_FIRST_HIGH).sum(axis=1).min()),
+        "us_per_step": round(ms_hi * 1e3, 2), "value": round(ab["total"] / (ms_hi * 1e-3) / 1e9, 1),
+        "headline_us_per_step": round(ms_ref * 1e3, 2),
+        "headline_value": round(headline_bytes / (ms_ref * 1e-3) / 1e9, 1),
+        "ratio": round(ms_ref / ms_hi, 4), "unit": "GB/s",
+        "how": "alternating batches with the headline workload (65536-page pools, below 2^31 bytes)"}
+    del t, fns
+    torch.cuda.empty_cache()
+
+    wl = W.over2gib_decode()
+    t, fns = prepare_16bit(wl, 4, dev, stream)
+    warm(fns, args.warmup)
+    ms, fwd_ms = timed_batches(fns, K, stream)
+    ab = algorithmic_bytes(wl, 4)
+    res["over2gib"] = {
+        "workload": "over2gib_decode", "num_pages": wl.num_pages, "pool_bytes": pool_bytes(wl), "split_kv": 4,
+        "us_per_step": round(ms * 1e3, 2), "value": round(ab["total"] / (ms * 1e-3) / 1e9, 1),
+        "frac": round(ab["total"] / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+        "kernel": "paged_attn_mma_kernel", "kernel_us": round(fwd_ms * 1e3, 2),
+        "kernel_frac": round(ab["total"] / (fwd_ms * 1e-3) / 1e9 / hbm_peak, 4), "unit": "GB/s",
+        "bytes_per_step": ab["total"], **traffic_fields("paged_attn_mma_kernel", "over2gib_decode", 4)}
+    del t, fns
+    torch.cuda.empty_cache()
+
+    wl = W.causal_prefill()
+    fl = causal_flops(wl)
+    pre = {"workload": "causal_prefill", "flops_per_step": fl, "unit": "TFLOP/s", "peak": tensor_peak,
+           "kernel": "paged_attn_tc05_kernel"}
+    for S in (8, 1):
+        t, fns = prepare_16bit(wl, S, dev, stream)
+        warm(fns, args.warmup)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # inputs (2 x 32 MiB pools) fit in L2
+        ms, fwd_ms = timed_batches(fns, K, stream, flush)
+        pre[f"split{S}"] = {
+            "us_per_step": round(ms * 1e3, 2), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+            "frac": round(fl / (ms * 1e-3) / 1e12 / tensor_peak, 4), "kernel_us": round(fwd_ms * 1e3, 2),
+            "kernel_tflops": round(fl / (fwd_ms * 1e-3) / 1e12, 1),
+            "kernel_frac": round(fl / (fwd_ms * 1e-3) / 1e12 / tensor_peak, 4),
+            **traffic_fields("paged_attn_tc05_kernel", "causal_prefill", S)}
+        del t, fns, flush
+    pre["l2"] = "pools smaller than L2: a 256 MiB buffer is written before each step, outside its events"
+    res["prefill"] = pre
+    torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args, ws, rank, local):
     import torch
@@ -350,32 +566,12 @@ def run_ours(args, ws, rank, local):
     # before every step, outside the step's events, and the step time is the sum of those events.
     flush = pool_bytes(wl) * 2 <= L2_BYTES
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
-    ev_f0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_f1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_s1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    fns = [fwd] + ([lambda: pa.paged_attn_combine(po, pl, out, lse, stream)] if S > 1 else [])
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local, enabled=not args.no_clocks) as clk:
-        t_start.record(stream)
-        for i in range(K):
-            if flush:
-                flush_buf.fill_(i & 0xFF)
-            ev_f0[i].record(stream)
-            fwd()
-            ev_f1[i].record(stream)
-            if S > 1:
-                pa.paged_attn_combine(po, pl, out, lse, stream)
-            ev_s1[i].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
+        ms_local, fwd_ms = timed_batches(fns, K, stream, flush_buf)
     barrier(ws)
-    fwd_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)]))
-    if flush:
-        ms_local = float(np.sum([a.elapsed_time(b) for a, b in zip(ev_f0, ev_s1)])) / K
-    else:
-        ms_local = t_start.elapsed_time(t_end) / K
     ms_step = max_over_ranks(ms_local, ws, dev)
     flags = pa.paged_attn_last_error_word()
     if flags:
@@ -413,11 +609,16 @@ def run_ours(args, ws, rank, local):
             tpeak, tpeak_src = FALLBACK_BF16_TFLOPS, "fallback"
         roofline = {"bound": "tensor", "kernel": kname, "achieved": round(tf_achieved, 1), "peak": tpeak,
                     "peak_source": tpeak_src, "unit": "TFLOP/s", "frac": round(tf_achieved / tpeak, 4),
-                    "kernel_ms": round(fwd_ms, 5), "traffic": recorded_traffic(kname, args.workload, S)}
+                    "kernel_ms": round(fwd_ms, 5), **traffic_fields(kname, args.workload, S)}
     else:
         roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                    "kernel_ms": round(fwd_ms, 5), "traffic": recorded_traffic(kname, args.workload, S)}
+                    "kernel_ms": round(fwd_ms, 5), **traffic_fields(kname, args.workload, S)}
+
+    extras = {}
+    if args.workload == "llama8b_decode" and ws == 1 and S == 1 and args.variant == 0 and not args.no_extras:
+        tpeak_x = float(peaks["bf16_tflops"]) if peaks and peaks.get("bf16_tflops") else FALLBACK_BF16_TFLOPS
+        extras = extra_workloads(args, dev, stream, fns, ab["total"], peak, tpeak_x)
 
     # ---- end to end through the public API: host inputs in, host result out, every step
     e2e = None
@@ -448,20 +649,17 @@ def run_ours(args, ws, rank, local):
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()
-        Ke = max(10, K // 4)
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(ws)
-        torch.cuda.synchronize()
-        a.record(stream)
-        for _ in range(Ke):
-            e2e_step()
-        b_.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(a.elapsed_time(b_) / Ke, ws, dev)
+        e2e_ev_ms, e2e_wall_ms = e2e_batches(e2e_step, max(10, K // 4), stream)
+        e2e_ms = max_over_ranks(e2e_wall_ms, ws, dev)
+        e2e_ev_ms = max_over_ranks(e2e_ev_ms, ws, dev)
         hb = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
         db = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
         e2e = {"value": round(job_throughput(ab["total"], ws, e2e_ms), 1), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(hb), "d2h_bytes_per_step": int(db),
+               "timing": E2E_TIMING,
+               "event_value": round(job_throughput(ab["total"], ws, e2e_ev_ms), 1),
+               "event_ms_per_step": round(e2e_ev_ms, 4),
                "api": ("paged_attn_fwd_kvq_splitkv" if kvq else "paged_attn_fwd_splitkv") +
                       " (host q / block table / seq_lens in, host out / lse back)"}
 
@@ -510,8 +708,16 @@ def run_ours(args, ws, rank, local):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": K * (2 if S > 1 else 1),
+        "timing": {"protocol": f"{max(args.warmup, 3)} warm-up steps, then the {K} timed steps in "
+                               f"{len(batch_sizes(K))} batches of {batch_sizes(K)} steps, CUDA events per batch; "
+                               "ms_per_step = median over batches (rocm-libraries PR #14349, Performance)"},
         "clocks": clocks,
     }
+    if extras:
+        line.update(extras)
+        line["extras_note"] = ("over2gib, over2gib_same_shape and prefill: further workloads timed in the same run "
+                               "with the same protocol; value, roofline and gpu_launches cover the headline "
+                               "workload only")
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -585,15 +791,9 @@ def run_varlen(args, ws, rank, local):
         for _ in range(max(args.warmup, 3)):
             fn()
         torch.cuda.synchronize()
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(ws)
         torch.cuda.synchronize()
-        a.record(stream)
-        for _ in range(K):
-            fn()
-        b_.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b_) / K
+        return timed_batches([fn], K, stream)[0]
 
     K = args.steps
     with ClockSampler(local, enabled=not args.no_clocks) as clk:
@@ -635,8 +835,7 @@ def run_varlen(args, ws, rank, local):
     achieved = ab["total"] / (ms_local * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": "paged_attn_mma_varlen_kernel", "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "kernel_ms": round(ms_local, 5), "traffic": recorded_traffic("paged_attn_mma_varlen_kernel",
-                                                                             args.workload, S),
+                "kernel_ms": round(ms_local, 5), **traffic_fields("paged_attn_mma_varlen_kernel", args.workload, S),
                 "tensor_side": {"achieved_tflops": round(fl / (ms_local * 1e-3) / 1e12, 1)}}
 
     e2e = None
@@ -654,11 +853,19 @@ def run_varlen(args, ws, rank, local):
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
 
-        e2e_ms = max_over_ranks(timed(e2e_step, max(10, K // 4)), ws, dev)
+        for _ in range(3):
+            e2e_step()
+        barrier(ws)
+        e2e_ev_ms, e2e_wall_ms = e2e_batches(e2e_step, max(10, K // 4), stream)
+        e2e_ms = max_over_ranks(e2e_wall_ms, ws, dev)
+        e2e_ev_ms = max_over_ranks(e2e_ev_ms, ws, dev)
         hb = q_h.numel() * q_h.element_size() + sum(t.numel() * 4 for t in small)
         db = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
         e2e = {"value": round(job_throughput(ab["total"], ws, e2e_ms), 1), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(hb), "d2h_bytes_per_step": int(db),
+               "timing": E2E_TIMING,
+               "event_value": round(job_throughput(ab["total"], ws, e2e_ev_ms), 1),
+               "event_ms_per_step": round(e2e_ev_ms, 4),
                "api": ("paged_attn_fwd_varlen" if args.no_overlap else
                        "paged_attn_varlen_hint + paged_attn_fwd_varlen_overlap") +
                       " (host q / block table / seq_lens / q_start / q_offset in, host out / lse back)"}

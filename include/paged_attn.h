@@ -52,7 +52,8 @@ enum {
     PA_EDTYPE = -2,        /* unsupported element type */
     PA_EUNSUPPORTED = -3,  /* shape outside the supported envelope (or forced variant cannot run it) */
     PA_ECUDA = -4,         /* a CUDA runtime/driver call failed */
-    PA_EBOUNDS = -5        /* device error word reported an out-of-range page id */
+    PA_EBOUNDS = -5,       /* paged_attn_last_error_word: a page id outside [0, num_pages) was read */
+    PA_ETIMEOUT = -6       /* paged_attn_last_error_word: a pipeline wait gave up; outputs are invalid */
 };
 
 /* bits of the device error word */
@@ -183,12 +184,20 @@ int paged_attn_fwd_splitkv(const void *q, const void *k_cache, const void *v_cac
  * this is a deployment convenience of this library, not part of the method.
  *
  * Same arguments and results as paged_attn_fwd_splitkv minus the workspace: the split partials go
- * to a fixed array of PA_NOALLOC_SCRATCH_BYTES inside the library's device image, which every GPU
- * that loads the library holds until the process exits.  Shapes whose partials need more than that
- * (paged_attn_workspace_bytes > PA_NOALLOC_SCRATCH_BYTES) return PA_EINVAL and launch nothing;
- * pass a smaller split_kv.  No call allocates device memory.
+ * to a fixed array of PA_NOALLOC_SCRATCH_BYTES inside the library's device image.  A device holds
+ * that array from the moment the CUDA runtime loads its module there until the process exits: under
+ * lazy module loading (CUDA's default) that is this entry point's first call on the device, under
+ * CUDA_MODULE_LOADING=EAGER it is when the library is first used on the device.  An explicit
+ * split_kv whose partials need more than the array (paged_attn_workspace_bytes >
+ * PA_NOALLOC_SCRATCH_BYTES) returns PA_EINVAL and launches nothing; pass a smaller split_kv.
+ * split_kv = 0 takes paged_attn_auto_split's choice, lowered to the largest split whose partials
+ * fit the array.  No call allocates device memory.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress);
  *     make that first call before any stream capture on that device.
+ *   - The address is kept per device ordinal for the life of the process.  It belongs to the
+ *     device's primary context (the one the CUDA runtime uses): calls made from another driver
+ *     context on the device, or after cudaDeviceReset, would use an address that context does not
+ *     map.  Use this entry point only from the primary context and never after a device reset.
  *   - All calls share the one array.  Calls that may overlap on the GPU (different streams, or
  *     different host threads) race on it: serialise them.  Nothing in it needs clearing between
  *     calls, because each call writes every partial it later reads.
@@ -259,8 +268,13 @@ int paged_attn_varlen_hint(const int32_t *q_start, const int32_t *seq_lens, cons
  * sequences' K/V read time (from hint->short_kv_tokens), raised by 1.3 and kept within
  * [8, 3/4 of the SMs].
  * The tcgen05 kernel runs on a high-priority stream that the library creates once per device; it
- * waits for `stream`'s earlier work and `stream` waits for it, so the call keeps stream order
- * and works under CUDA graph capture.  Arguments and results are those of paged_attn_fwd_varlen,
+ * waits for `stream`'s earlier work and `stream` waits for it, so the call keeps stream order.
+ *   - The first overlapped call on a device creates that stream, which cannot happen inside a
+ *     stream capture: make the first call outside any capture.  Later calls may be captured.
+ *   - Every overlapped call on a device shares the one stream.  Calls from different host threads,
+ *     or captures into different graphs at the same time, would interleave their work on it:
+ *     serialise them.
+ * Arguments and results are those of paged_attn_fwd_varlen,
  * bit for bit.  A NULL hint, a batch without sequences of both kinds, or a shape that does not
  * take the tcgen05 kernel falls back to paged_attn_fwd_varlen's two launches on `stream`.
  */
@@ -338,7 +352,20 @@ int paged_attn_debug_wait_timeout(uint32_t limit_us, void *stream);
 /*
  * paged_attn_last_error_word — synchronise the current device, then read and
  * clear its error word (PA_ERRBIT_* bits accumulated by every call since the
- * last read).  Returns PA_OK, or PA_ECUDA if the read failed.
+ * last read) into *flags.  The status says what the bits mean for the results:
+ *   PA_ETIMEOUT  PA_ERRBIT_TIMEOUT is set: a pipeline wait gave up after its
+ *                2 s limit and its warp left the pipeline, so outputs written
+ *                since the last read are invalid (not merely inaccurate);
+ *   PA_EBOUNDS   otherwise, PA_ERRBIT_PAGE_RANGE is set: a sequence's page id
+ *                lay outside [0, num_pages); its tokens read as zero (the
+ *                rocm-libraries PR #14349 kernel leaves this unchecked, "Not in
+ *                this PR"), every other sequence's results are exact;
+ *   PA_EINVAL    otherwise, PA_ERRBIT_QSTART is set (paged_attn_fwd_varlen);
+ *   PA_OK        no bit other than PA_ERRBIT_SEQ_CLIPPED is set.
+ * *flags holds the bits in every case but PA_ECUDA (the read failed) and
+ * PA_EINVAL for a NULL flags.  The forward calls are asynchronous and cannot
+ * return these themselves: a caller that must not consume invalid outputs
+ * checks this status before reading them.
  */
 int paged_attn_last_error_word(uint32_t *flags);
 

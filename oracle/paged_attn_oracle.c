@@ -234,9 +234,6 @@ int64_t oracle_key_limit(const int32_t *seq_lens, const int32_t *q_offset, int32
 
 /* ---------------------------------------------------------------- softmax */
 
-/* softmax(scale * q.k_j) . v_j over the keys j in [lo, hi), from the definition.
- * No keys: out = 0, lse = -inf.  scratch has room for hi - lo doubles. */
-/* Value of element (token j, kv head kvh, dim e) of sequence b in pool k (which = 0) or v (1). */
 /* Value of the element at flat index idx (token j, kv head kvh of sequence b) in pool k
  * (which = 0) or v (1): the stored element, times its (page, kv head) scale for quantized pools. */
 static double kv_value(const oracle_dims *d, const oracle_kv *kv, int which, const int32_t *block_table, int32_t b,
@@ -250,6 +247,8 @@ static double kv_value(const oracle_dims *d, const oracle_kv *kv, int which, con
     return x;
 }
 
+/* softmax(scale * q.k_j) . v_j over the keys j in [lo, hi), from the definition.
+ * No keys: out = 0, lse = -inf.  scratch has room for hi - lo doubles. */
 static int attend_keys(const oracle_dims *d, const double *qrow, const oracle_kv *kv,
                        const int32_t *block_table, int32_t b, int32_t kvh, int64_t lo, int64_t hi,
                        double scale, double *scratch, double *out, double *lse)
@@ -383,8 +382,7 @@ static int rows_impl(const void *q, const oracle_kv *kv, const int32_t *block_ta
         double *scratch = (double *)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1));
         double *pout = (double *)malloc(sizeof(double) * (size_t)S * D);
         double *plse = (double *)malloc(sizeof(double) * (size_t)S);
-        double *tmp = (double *)malloc(sizeof(double) * D);
-        if (!qrow || !scratch || !pout || !plse || !tmp) {
+        if (!qrow || !scratch || !pout || !plse) {
 #pragma omp critical
             status = ORACLE_ENOMEM;
         } else {
@@ -432,7 +430,6 @@ static int rows_impl(const void *q, const oracle_kv *kv, const int32_t *block_ta
         free(scratch);
         free(pout);
         free(plse);
-        free(tmp);
     }
     free(plan);
     return status;

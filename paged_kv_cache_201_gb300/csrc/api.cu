@@ -688,6 +688,11 @@ int paged_attn_last_error_word(uint32_t *flags) {
     if (cudaMemcpyFromSymbol(&v, g_pa_error_word, sizeof v) != cudaSuccess) return PA_ECUDA;
     if (cudaMemcpyToSymbol(g_pa_error_word, &zero, sizeof zero) != cudaSuccess) return PA_ECUDA;
     *flags = v;
+    // The most serious condition first: a wait that gave up leaves outputs unwritten, an
+    // out-of-range page id only zeroes that page's tokens.
+    if (v & PA_ERRBIT_TIMEOUT) return PA_ETIMEOUT;
+    if (v & PA_ERRBIT_PAGE_RANGE) return PA_EBOUNDS;
+    if (v & PA_ERRBIT_QSTART) return PA_EINVAL;
     return PA_OK;
 }
 
@@ -699,6 +704,7 @@ const char *paged_attn_strerror(int code) {
         case PA_EUNSUPPORTED: return "unsupported shape or variant";
         case PA_ECUDA: return "CUDA call failed";
         case PA_EBOUNDS: return "out-of-range page id";
+        case PA_ETIMEOUT: return "a pipeline wait timed out (results invalid)";
         default: return "unknown status";
     }
 }

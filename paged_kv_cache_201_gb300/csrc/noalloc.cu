@@ -4,8 +4,10 @@
 // host framework that owns and budgets every device byte, or a latency-critical serving
 // loop that must never hit cudaMalloc (which can synchronise the whole device).  For them,
 // paged_attn_fwd_splitkv_noalloc keeps the split partials in a fixed array that is part of
-// this library's device image.  Every GPU that loads the library holds that array until the
-// process exits.
+// this file's device module.  A device holds the array from the moment the CUDA runtime loads
+// that module on it until the process exits: with lazy module loading (CUDA's default) that is
+// the first call of this entry point on the device, with CUDA_MODULE_LOADING=EAGER it is when
+// the library's modules are loaded into the device's context.
 #include <mutex>
 
 #include "kernels.h"
@@ -20,7 +22,9 @@ constexpr int kMaxScratchDevices = 128;
 void *g_scratch_ptr[kMaxScratchDevices];
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device, looked up once per device.
+// Device address of the scratch array on the current device, looked up once per device and kept
+// for the life of the process: it belongs to the device's primary context, and is stale after
+// cudaDeviceReset or in any other context on the device.
 int scratch_ptr(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return PA_ECUDA;
@@ -41,6 +45,14 @@ extern "C" int paged_attn_fwd_splitkv_noalloc(const void *q, const void *k_cache
                                               const int32_t *q_offset, int split_kv, float scale, void *out,
                                               float *lse, const pa_dims *dims, int num_sms, int64_t device_bytes,
                                               void *stream) {
+    if (split_kv == 0) {
+        // The automatic split, lowered until its partials fit the fixed array (S = 1 needs none).
+        split_kv = paged_attn_auto_split(dims, num_sms, device_bytes);
+        if (split_kv < 0) return split_kv;
+        while (split_kv > 1 &&
+               paged_attn_workspace_bytes(dims, split_kv, num_sms, device_bytes) > (int64_t)PA_NOALLOC_SCRATCH_BYTES)
+            --split_kv;
+    }
     const int64_t need = paged_attn_workspace_bytes(dims, split_kv, num_sms, device_bytes);
     if (need < 0) return (int)need;
     if (need > (int64_t)PA_NOALLOC_SCRATCH_BYTES) return PA_EINVAL;  // partials would not fit the fixed array

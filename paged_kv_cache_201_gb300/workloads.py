@@ -259,12 +259,39 @@ def over2gib_decode(seed: int = 1004, B: int = 256) -> Workload:
                     seq_lens=seq_lens, block_table=bt, q=q, device_cache_seed=seed)
 
 
+LLAMA_OVER2G_PAGES = 65536 + 2048   # 2 GiB + 64 MiB per pool at 32 KiB pages (Hkv=8, D=128)
+LLAMA_OVER2G_FIRST_HIGH = 65536     # page whose first byte sits at byte 2^31
+
+
+def llama8b_decode_over2gib(seed: int = 1012, B: int = 256) -> Workload:
+    """The Llama-3-8B decode shape (Hq=32, Hkv=8, D=128, L=4096, bf16) over pools just past 2^31
+    bytes: 65536 + 2048 pages per pool.  Every sequence gets 8 of the 2048 pages that start at or
+    past byte 2^31 and 248 from below, shuffled within its table row, so every row reads on both
+    sides of byte 2^31.  The same work as ``llama8b_decode``; only where the pages lie differs."""
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D, ps, L = 32, 8, 128, 16, 4096
+    per_seq = L // ps                     # 256
+    n_high = (LLAMA_OVER2G_PAGES - LLAMA_OVER2G_FIRST_HIGH) // 256   # 8
+    n_low = per_seq - n_high
+    assert B * n_high <= LLAMA_OVER2G_PAGES - LLAMA_OVER2G_FIRST_HIGH
+    q = _normal_elems(rng, B * Hq * D, "bf16").reshape(B, 1, Hq, D)
+    high = LLAMA_OVER2G_FIRST_HIGH + rng.permutation(LLAMA_OVER2G_PAGES - LLAMA_OVER2G_FIRST_HIGH).astype(np.int64)
+    low = rng.permutation(LLAMA_OVER2G_FIRST_HIGH).astype(np.int64)
+    rows = np.concatenate([high[:B * n_high].reshape(B, n_high), low[:B * n_low].reshape(B, n_low)], axis=1)
+    bt = rng.permuted(rows, axis=1).astype(np.int32)
+    seq_lens = np.full(B, L, dtype=np.int32)
+    return Workload(name="llama8b_decode_over2gib", dtype="bf16", B=B, Sq=1, Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
+                    num_pages=LLAMA_OVER2G_PAGES, causal=False, scale=1.0 / math.sqrt(D), split_kv=(1, 4),
+                    seq_lens=seq_lens, block_table=bt, q=q, device_cache_seed=seed)
+
+
 CONFIGS = {
     "tiny_decode_f32": tiny_decode_f32,
     "llama8b_decode": llama8b_decode,
     "ragged_decode": ragged_decode,
     "over2gib_decode": over2gib_decode,
     "causal_prefill": causal_prefill,
+    "llama8b_decode_over2gib": llama8b_decode_over2gib,
 }
 
 

@@ -133,3 +133,53 @@ def compare_rows(res, ref, rows_bih, wl, split_kv, what):
         assert_close(po, ref["part_out"], dt, f"{what} partial out")
         assert_close(pl, ref["part_lse"], dt, f"{what} partial lse")
     return e
+
+
+def compare_all(res, ref, wl, split_kv, what, chunk=1 << 14):
+    """Compare every output row of a GPU result with an oracle result computed on
+    ``oracle.all_rows`` (b slowest, then i, then h), in chunks of rows so that the
+    full-size workloads' partials (up to 1 GiB of float64) need no indexed copies.
+
+    ``ref`` may come from an oracle call with a larger split count than ``split_kv``
+    only when split_kv == 1: then its unsplit ``out`` / ``lse`` are the reference."""
+    D, dt = wl.D, wl.dtype
+    n = wl.B * wl.Sq * wl.Hq
+    out = res["out"].reshape(n, D)
+    lse = res["lse"].reshape(n)
+    if split_kv > 1:
+        po = res["part_out"].reshape(split_kv, n, D)
+        pl = res["part_lse"].reshape(split_kv, n)
+    worst = 0.0
+    for a in range(0, n, chunk):
+        e = min(n, a + chunk)
+        tag = f"{what} rows {a}..{e - 1}"
+        if split_kv == 1:
+            worst = max(worst, assert_close(out[a:e], ref["out"][a:e], dt, f"{tag} out"))
+            assert_close(lse[a:e], ref["lse"][a:e], dt, f"{tag} lse")
+        else:
+            worst = max(worst, assert_close(out[a:e], ref["comb_out"][a:e], dt, f"{tag} combined out"))
+            assert_close(lse[a:e], ref["comb_lse"][a:e], dt, f"{tag} combined lse")
+            assert_close(np.moveaxis(po[:, a:e], 0, 1), ref["part_out"][a:e], dt, f"{tag} partial out")
+            assert_close(np.moveaxis(pl[:, a:e], 0, 1), ref["part_lse"][a:e], dt, f"{tag} partial lse")
+    return worst
+
+
+_ORACLE_CACHE = {}
+
+
+def oracle_all_rows(wl, split_kv, k_cache=None, v_cache=None, k_scale=None, v_scale=None):
+    """The oracle on every row of a named workload (unsplit result plus the split_kv partials and
+    their combination), computed once per (workload, split_kv) in this process: several test files
+    check the same full-size workloads, and one fp64 pass over them takes seconds to tens of seconds.
+    Quantized pools (8-bit elements) take their scales."""
+    import oracle
+    key = (wl.name, wl.B, wl.Sq, split_kv)
+    if key not in _ORACLE_CACHE:
+        rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)
+        if getattr(wl, "kv_dtype", None) in W.QUANT_KV:
+            _ORACLE_CACHE[key] = oracle.workload_rows_kvq(wl, split_kv=split_kv, row_bih=rows, k_cache=k_cache,
+                                                          v_cache=v_cache, k_scale=k_scale, v_scale=v_scale)
+        else:
+            _ORACLE_CACHE[key] = oracle.workload_rows(wl, split_kv=split_kv, row_bih=rows, k_cache=k_cache,
+                                                      v_cache=v_cache)
+    return _ORACLE_CACHE[key]

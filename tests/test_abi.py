@@ -46,6 +46,8 @@ def test_strerror_and_version(lib):
     assert pa.paged_attn_strerror(0) == "ok"
     assert pa.paged_attn_strerror(-3).startswith("unsupported")
     assert pa.paged_attn_strerror(12345) == "unknown status"
+    assert "page id" in pa.paged_attn_strerror(pa.PA_EBOUNDS)
+    assert "timed out" in pa.paged_attn_strerror(pa.PA_ETIMEOUT)
     assert pa.paged_attn_version() >= 100
 
 

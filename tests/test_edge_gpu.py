@@ -182,7 +182,9 @@ def test_out_of_range_page_is_flagged_not_read(pa):
     for variant in (0, 1):
         assert pa.paged_attn_last_error_word() == 0
         res = _gpu.run(_gpu.DeviceWorkload(bad), 1, variant)
-        assert pa.paged_attn_last_error_word() & pa.ERRBIT_PAGE_RANGE
+        status, bits = pa.paged_attn_last_error_status()
+        assert bits & pa.ERRBIT_PAGE_RANGE and status == pa.PA_EBOUNDS
+        assert pa.paged_attn_last_error_status() == (pa.PA_OK, 0)   # read and cleared
         rows = oracle.all_rows(1, 1, wl.Hq)
         rows[:, 0] = 1
         ref = oracle.workload_rows(wl, split_kv=1, row_bih=rows)
@@ -216,8 +218,8 @@ def test_bounded_wait_gives_up_and_context_survives(pa):
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     assert 0.04 < dt < 5.0
-    assert pa.paged_attn_last_error_word() == pa.ERRBIT_TIMEOUT
-    assert pa.paged_attn_last_error_word() == 0  # read and cleared
+    assert pa.paged_attn_last_error_status() == (pa.PA_ETIMEOUT, pa.ERRBIT_TIMEOUT)
+    assert pa.paged_attn_last_error_status() == (pa.PA_OK, 0)  # read and cleared
     wl = W.make_custom(dtype="bf16", B=2, Sq=1, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=[33, 90], seed=77)
     res = _gpu.run(_gpu.DeviceWorkload(wl), 2)
     rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)

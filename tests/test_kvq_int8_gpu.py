@@ -191,17 +191,14 @@ def test_int8_singlecall(pa):
 # ----------------------------------------------------------------------------- full size (1-GiB pools)
 @pytest.mark.parametrize("split_kv", [1, 4])
 def test_llama8b_decode_int8(pa, split_kv):
-    """The benchmarked launch (B=256, L=4096, GQA 4, 65536 pages of int8) on sampled sequences."""
+    """The benchmarked launch (B=256, L=4096, GQA 4, 65536 pages of int8): every row, and at split 4
+    every partial."""
     wl = W.llama8b_decode_int8()
     dw = _gpu.DeviceWorkload(wl)
     k, v = dw.host_pools()
     ks, vs = dw.host_scales()
     res = _gpu.run(dw, split_kv)
     assert not np.isnan(res["out"]).any() and np.isfinite(res["lse"]).all()
-    seqs = [0, 3, 100, 170, 254]
-    b, h = np.meshgrid(np.asarray(seqs), np.arange(wl.Hq), indexing="ij")
-    rows = np.stack([b.ravel(), np.zeros(b.size, dtype=np.int64), h.ravel()], axis=1).astype(np.int32)
-    ref = oracle.workload_rows_kvq(wl, split_kv=split_kv, row_bih=rows, k_cache=k, v_cache=v, k_scale=ks,
-                                   v_scale=vs)
-    _gpu.compare_rows(res, ref, rows, wl, split_kv, f"llama8b int8 S={split_kv}")
+    ref = _gpu.oracle_all_rows(wl, 4, k, v, ks, vs)   # its unsplit result is the split-1 reference
+    _gpu.compare_all(res, ref, wl, split_kv, f"llama8b int8 S={split_kv}")
     _check_clean(pa)

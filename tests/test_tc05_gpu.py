@@ -67,17 +67,15 @@ def test_tc05_noncausal_and_decode_shapes(pa):
 
 
 def test_tc05_causal_prefill_full(pa):
-    """The full causal prefill workload (B=4, Sq=1024, q_offset up to 3072, split 8) on sampled rows."""
+    """The full causal prefill workload (B=4, Sq=1024, q_offset up to 3072) on the forced tcgen05
+    variant: every row at split 8 (partials of every split included) and at split 1."""
     wl = W.causal_prefill()
     dw = _gpu.DeviceWorkload(wl)
-    toks = [0, 1, 2, 15, 16, 31, 32, 63, 64, 127, 128, 500, 777, 1000, 1023]
-    b, i, h = np.meshgrid(np.arange(wl.B), np.array(toks), np.arange(wl.Hq), indexing="ij")
-    rows = np.stack([b.ravel(), i.ravel(), h.ravel()], axis=1).astype(np.int32)
+    ref = _gpu.oracle_all_rows(wl, 8)   # its unsplit result is the split-1 reference
     for S in (8, 1):
         res = _gpu.run(dw, S, TC05)
-        ref = oracle.workload_rows(wl, split_kv=S, row_bih=rows)
-        _gpu.compare_rows(res, ref, rows, wl, S, f"tc05 full prefill S={S}")
         assert not np.isnan(res["out"]).any()
+        _gpu.compare_all(res, ref, wl, S, f"tc05 full prefill S={S}")
     assert pa.paged_attn_last_error_word() == 0
 
 

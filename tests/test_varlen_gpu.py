@@ -234,32 +234,15 @@ def mixed_full():
 
 def test_mixed_decode_prefill_full(pa, mixed_full):
     """The benchmarked mixed batch (4 causal prefill chunks of 1024 tokens + 256 decode sequences of
-    4096 keys, 2 x 2 GiB pools) on sampled rows: 8 tokens of each prefill chunk and 8 decode
-    sequences, every head."""
+    4096 keys, 2 x 2 GiB pools): every token and head against the oracle."""
     wl, kd, vd, k, v = mixed_full
     res = _run(pa, wl, _device(wl, kd, vd), 1)
     assert not np.isnan(res["out"]).any() and np.isfinite(res["lse"]).all()
-    toks = []
-    for b in range(4):
-        a = int(wl.q_start[b])
-        toks += [a + i for i in (0, 1, 63, 64, 511, 777, 1022, 1023)]
-    toks += [int(wl.q_start[b]) for b in (4, 5, 77, 128, 200, 255, 258, 259)]
-    sel = np.array(toks)
-    # oracle only on the sampled tokens: a batch of the sampled sequences with those tokens
-    ref_out, ref_lse = [], []
-    for tok in toks:
-        b = int(np.searchsorted(wl.q_start, tok, side="right")) - 1
-        i = tok - int(wl.q_start[b])
-        one = W.Workload(**{**wl.__dict__, "B": 1, "Sq": int(wl.q_start[b + 1] - wl.q_start[b]),
-                            "q": wl.q[int(wl.q_start[b]):int(wl.q_start[b + 1])][None],
-                            "seq_lens": wl.seq_lens[b:b + 1], "block_table": wl.block_table[b:b + 1],
-                            "q_offset": wl.q_offset[b:b + 1], "q_start": None})
-        rows = np.stack([np.zeros(wl.Hq), np.full(wl.Hq, i), np.arange(wl.Hq)], axis=1).astype(np.int32)
-        r = oracle.workload_rows(one, split_kv=1, row_bih=rows, k_cache=k, v_cache=v, want_split=False)
-        ref_out.append(r["out"])
-        ref_lse.append(r["lse"])
-    _gpu.assert_close(res["out"][sel], np.stack(ref_out), "bf16", "mixed full out")
-    _gpu.assert_close(res["lse"][sel], np.stack(ref_lse), "bf16", "mixed full lse")
+    ref = oracle.rows_varlen(q=wl.q, k_cache=k, v_cache=v, block_table=wl.block_table, seq_lens=wl.seq_lens,
+                             q_start=wl.q_start, q_offset=wl.q_offset, causal=wl.causal, dims=oracle.dims_of(wl),
+                             scale=wl.scale, split_kv=1, want_split=False)
+    _gpu.assert_close(res["out"], ref["out"], "bf16", "mixed full out")
+    _gpu.assert_close(res["lse"], ref["lse"], "bf16", "mixed full lse")
     assert pa.paged_attn_last_error_word() == 0
 
 
