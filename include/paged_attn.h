@@ -22,8 +22,10 @@
  *     offset; an f32 combine for narrow float types.
  *
  * Conventions shared by every call
- *   - All tensor pointers are DEVICE pointers, dense and row-major, 16-byte
- *     aligned.  The caller owns every buffer; the library allocates nothing.
+ *   - All tensor pointers are DEVICE pointers, row-major and 16-byte aligned;
+ *     every tensor is dense except q, whose tokens may be further apart
+ *     (pa_dims.q_stride).  The caller owns every buffer; the library
+ *     allocates nothing.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream).  The returned status reports argument validation and launch
  *     errors only; faults inside a kernel surface on the stream as CUDA errors.
@@ -93,6 +95,10 @@ enum {
  *                q_len newest tokens
  *   q_offset     [batch] int32 or NULL: position of query row 0 of sequence b
  *                inside its K/V sequence (NULL means seq_lens[b] - q_len)
+ * Layouts: the heads of one query token are dense (head h at h * head_dim); consecutive tokens are
+ * q_stride elements apart (q_stride = 0: dense, num_q_heads * head_dim), and sequence b's token i is
+ * token b * q_len + i (a variable-length batch's packed token t is token t).  Every other tensor
+ * (out, lse, partials, pools, block table rows within bt_stride) is dense.
  * Supported: dtype in {PA_F32, PA_F16, PA_BF16}; head_dim in {64, 128, 256} (256: not for the FP8 and
  * variable-length entry points);
  * page_size in {16, 32, 64}; num_q_heads a multiple of num_kv_heads;
@@ -108,6 +114,10 @@ typedef struct pa_dims {
     int64_t num_pages;     /* pages in each of the K and V pools */
     int32_t bt_stride;     /* elements between consecutive block-table rows */
     int32_t dtype;         /* PA_F32 / PA_F16 / PA_BF16 */
+    int64_t q_stride;      /* elements between consecutive query tokens of q; 0 = dense
+                              (num_q_heads * head_dim).  A larger stride reads q as a view, for
+                              example of a fused QKV projection's output; a multiple of
+                              16 bytes / element size (8 for 16-bit q, 4 for f32) */
 } pa_dims;
 
 /*

@@ -39,7 +39,8 @@ PA_OK, PA_EINVAL, PA_EDTYPE, PA_EUNSUPPORTED, PA_ECUDA, PA_EBOUNDS, PA_ETIMEOUT 
 class PaDims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("q_len", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("num_pages", ctypes.c_int64), ("bt_stride", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("num_pages", ctypes.c_int64), ("bt_stride", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("q_stride", ctypes.c_int64)]
 
 
 class PaVarlenHint(ctypes.Structure):
@@ -149,6 +150,34 @@ def _check(t, name, dtype=None, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
 
 
+def _check_q(q, ndim):
+    """q may be a view whose query tokens are further apart than its heads (for example sliced out of
+    a fused QKV projection): its heads dense, tokens evenly spaced.  Other tensors must be
+    contiguous."""
+    if not q.is_cuda:
+        raise ValueError("q must be a CUDA tensor")
+    if q.dim() != ndim:
+        raise ValueError(f"q must have {ndim} dims, got {q.dim()}")
+    _q_token_stride(q)
+
+
+def _q_token_stride(q) -> int:
+    """Elements between consecutive query tokens of q ([B, Sq, Hq, D] or packed [T, Hq, D]); 0 when q
+    is contiguous (the dense layout).  Raises if the tokens are not evenly spaced or the heads not dense."""
+    if q.is_contiguous():
+        return 0
+    Hq, D = q.shape[-2], q.shape[-1]
+    if (q.stride(-1) != 1 and D > 1) or (q.stride(-2) != D and Hq > 1):
+        raise ValueError("q's heads must be dense ([..., Hq, D] contiguous)")
+    if q.dim() == 3:
+        return int(q.stride(0))
+    B, Sq = q.shape[0], q.shape[1]
+    tok = int(q.stride(1)) if Sq > 1 else int(q.stride(0))
+    if B > 1 and Sq > 1 and q.stride(0) != Sq * q.stride(1):
+        raise ValueError("q's tokens must be evenly spaced across sequences (stride(0) == Sq * stride(1))")
+    return tok
+
+
 def _stream(stream) -> int:
     torch = _torch()
     s = torch.cuda.current_stream() if stream is None else stream
@@ -162,7 +191,7 @@ def dims_of(q, k_cache, block_table) -> PaDims:
         raise ValueError("q and k_cache head dims differ")
     if block_table.dim() != 2 or block_table.shape[0] != B:
         raise ValueError("block_table must be [B, W]")
-    return PaDims(B, Sq, Hq, Hkv, D, ps, P, block_table.shape[1], _dtype_code(q))
+    return PaDims(B, Sq, Hq, Hkv, D, ps, P, block_table.shape[1], _dtype_code(q), _q_token_stride(q))
 
 
 def _raise(rc: int, where: str):
@@ -175,7 +204,7 @@ def paged_attn_fwd_variant(q, k_cache, v_cache, block_table, seq_lens, causal, q
                            lse, variant: int = VARIANT_AUTO, stream=None) -> None:
     """Forward over the paged cache; see ``paged_attn_fwd`` in include/paged_attn.h."""
     torch = _torch()
-    _check(q, "q", ndim=4)
+    _check_q(q, 4)
     _check(k_cache, "k_cache", q.dtype, 4)
     _check(v_cache, "v_cache", q.dtype, 4)
     _check(block_table, "block_table", torch.int32, 2)
@@ -234,7 +263,7 @@ def paged_attn_fwd_splitkv(q, k_cache, v_cache, block_table, seq_lens, causal, q
                            workspace, num_sms=None, device_bytes=None, stream=None) -> None:
     """Split forward + combine in one call; ``workspace`` is a uint8 CUDA tensor (may be None when S == 1)."""
     torch = _torch()
-    _check(q, "q", ndim=4)
+    _check_q(q, 4)
     _check(k_cache, "k_cache", q.dtype, 4)
     _check(v_cache, "v_cache", q.dtype, 4)
     _check(block_table, "block_table", torch.int32, 2)
@@ -266,7 +295,7 @@ def paged_attn_fwd_splitkv_noalloc(q, k_cache, v_cache, block_table, seq_lens, c
     the library.  Calls that may overlap on the GPU share that array and must be serialised; the first
     call on a device should come before any stream capture there."""
     torch = _torch()
-    _check(q, "q", ndim=4)
+    _check_q(q, 4)
     _check(k_cache, "k_cache", q.dtype, 4)
     _check(v_cache, "v_cache", q.dtype, 4)
     _check(block_table, "block_table", torch.int32, 2)
@@ -307,7 +336,7 @@ def _kv_dtype_of(k_cache, kv_dtype):
 
 def _kvq_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, q_offset, out, lse, kv_dtype):
     torch = _torch()
-    _check(q, "q", ndim=4)
+    _check_q(q, 4)
     if q.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError(f"q must be bf16 or f16 with 8-bit pools, got {q.dtype}")
     _check_q8_pool(k_cache, "k_cache", kv_dtype)
@@ -401,7 +430,7 @@ def paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, c
     ``paged_attn_varlen_hint``) the call is ``paged_attn_fwd_varlen_overlap``: the same results, its
     two kernels side by side."""
     torch = _torch()
-    _check(q, "q", ndim=3)
+    _check_q(q, 3)
     _check(k_cache, "k_cache", q.dtype, 4)
     _check(v_cache, "v_cache", q.dtype, 4)
     _check(block_table, "block_table", torch.int32, 2)
@@ -417,7 +446,7 @@ def paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, c
     B = block_table.shape[0]
     if D2 != D or q_start.shape[0] != B + 1 or seq_lens.shape[0] != B:
         raise ValueError("q / k_cache / block_table / q_start / seq_lens shapes disagree")
-    dims = PaDims(B, T, Hq, Hkv, D, ps, P, block_table.shape[1], _dtype_code(q))
+    dims = PaDims(B, T, Hq, Hkv, D, ps, P, block_table.shape[1], _dtype_code(q), _q_token_stride(q))
     args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(q_start),
             int(bool(causal)), _ptr(q_offset), int(split_kv), float(scale), _ptr(out), _ptr(lse), ctypes.byref(dims))
     if hint is None:
@@ -528,7 +557,7 @@ def attention(q, k_cache, v_cache, block_table, seq_lens, *, causal: bool = Fals
     B, Sq, Hq, D = q.shape
     if scale is None:
         scale = D ** -0.5
-    out = torch.empty_like(q)
+    out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device) if (want_lse or split_kv > 1) else None
     if split_kv == 1:
         paged_attn_fwd_variant(q, k_cache, v_cache, block_table, seq_lens, causal, q_offset, 1, scale, out, lse,
@@ -554,7 +583,7 @@ def attention_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, 
     B, Sq, Hq, D = q.shape
     if scale is None:
         scale = D ** -0.5
-    out = torch.empty_like(q)
+    out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=q.device) if (want_lse or split_kv > 1) else None
     if split_kv == 1:
         paged_attn_fwd_kvq(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, causal, q_offset, 1, scale,
@@ -577,7 +606,7 @@ def attention_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, *, cau
     T, Hq, D = q.shape
     if scale is None:
         scale = D ** -0.5
-    out = torch.empty_like(q)
+    out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if (want_lse or split_kv > 1) else None
     if split_kv == 1:
         paged_attn_fwd_varlen(q, k_cache, v_cache, block_table, seq_lens, q_start, causal, q_offset, 1, scale, out,

@@ -75,7 +75,17 @@ int check_dims(const pa_dims *d) {
     if (d->num_pages * (int64_t)d->page_size >= (int64_t)1 << 31) return PA_EUNSUPPORTED;
     if ((int64_t)d->bt_stride * d->page_size >= (int64_t)1 << 31) return PA_EUNSUPPORTED;
     if ((int64_t)d->q_len * (d->num_q_heads / d->num_kv_heads) >= (int64_t)1 << 31) return PA_EUNSUPPORTED;
+    // q's token stride: dense, or at least a token's heads and keeping every row 16-byte aligned
+    if (d->q_stride != 0 &&
+        (d->q_stride < (int64_t)d->num_q_heads * d->head_dim || (d->q_stride * esize_of(d->dtype)) % 16 != 0 ||
+         d->q_stride >= (int64_t)1 << 40))
+        return PA_EINVAL;
     return PA_OK;
+}
+
+// Elements between consecutive query tokens of q.
+int64_t q_token_stride(const pa_dims *d) {
+    return d->q_stride ? d->q_stride : (int64_t)d->num_q_heads * d->head_dim;
 }
 
 CUtensorMapDataType tma_dtype(int dtype) {
@@ -129,7 +139,7 @@ int make_q_map(CUtensorMap *m, const void *q, const pa_dims *d, bool varlen = fa
     const int G = d->num_q_heads / d->num_kv_heads;
     const cuuint64_t tokens = varlen ? (cuuint64_t)d->q_len : (cuuint64_t)d->batch * (cuuint64_t)d->q_len;
     const cuuint64_t dims[4] = {64, D / 64, Hq, tokens};
-    const cuuint64_t strides[3] = {64 * esz, D * esz, Hq * D * esz};
+    const cuuint64_t strides[3] = {64 * esz, D * esz, (cuuint64_t)q_token_stride(d) * esz};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)G, (cuuint32_t)(128 / G)};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(m, tma_dtype(d->dtype), 4, const_cast<void *>(q), dims, strides, box, estr,
@@ -240,6 +250,7 @@ pa::FwdParams fill_params(const void *q, const void *k_cache, const void *v_cach
     p.scale_log2 = scale * pa::kLog2e;
     p.row_tiles = 1;
     p.rows_total = (long long)dims->batch * dims->q_len * dims->num_q_heads;
+    p.q_stride = q_token_stride(dims);
     return p;
 }
 

@@ -166,8 +166,8 @@ __device__ __forceinline__ void mma_unit(const CUtensorMap *tmK, const CUtensorM
     {
         const T *q = reinterpret_cast<const T *>(p.q);
         const bool va = ra < rows, vb = rb < rows;
-        const T *qa = q + (va ? out_row_index(p, sq, kvh, ra) * D : 0);
-        const T *qb = q + (vb ? out_row_index(p, sq, kvh, rb) * D : 0);
+        const T *qa = q + (va ? q_row_offset(p, out_row_index(p, sq, kvh, ra)) : 0);
+        const T *qb = q + (vb ? q_row_offset(p, out_row_index(p, sq, kvh, rb)) : 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int c0 = kk * 16 + 2 * tq;

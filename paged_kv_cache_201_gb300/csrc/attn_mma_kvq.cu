@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
     for (int nr = 0; nr < NR; ++nr) {
         const int r = nr * 8 + g;
         const bool valid = r < rows;
-        const T *qrow = reinterpret_cast<const T *>(p.q) + (valid ? out_row_index(p, sq, kvh, r) * D : 0);
+        const T *qrow = reinterpret_cast<const T *>(p.q) + (valid ? q_row_offset(p, out_row_index(p, sq, kvh, r)) : 0);
         uint32_t w[D / 8];
         float inv;
         load_q_row<T, D>(qrow, valid, tq, w, inv);
@@ -725,8 +725,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
         uint32_t wa[D / 8], wb[D / 8];
         const T *q = reinterpret_cast<const T *>(p.q);
         const bool va = ra < p.rows, vb = rb < p.rows;
-        load_q_row<T, D>(q + (va ? out_row_index(p, sq, kvh, ra) * D : 0), va, tq, wa, q_inv_a);
-        load_q_row<T, D>(q + (vb ? out_row_index(p, sq, kvh, rb) * D : 0), vb, tq, wb, q_inv_b);
+        load_q_row<T, D>(q + (va ? q_row_offset(p, out_row_index(p, sq, kvh, ra)) : 0), va, tq, wa, q_inv_a);
+        load_q_row<T, D>(q + (vb ? q_row_offset(p, out_row_index(p, sq, kvh, rb)) : 0), vb, tq, wb, q_inv_b);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             qf[kk][0] = wa[2 * kk];

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     {
         const int r = row0 + g;
         const bool valid = r < row_end;
-        const T *q = reinterpret_cast<const T *>(p.q) + (valid ? out_row_index(p, sq, kvh, r) * D : 0);
+        const T *q = reinterpret_cast<const T *>(p.q) + (valid ? q_row_offset(p, out_row_index(p, sq, kvh, r)) : 0);
 #pragma unroll
         for (int kk = 0; kk < MT; ++kk) {
             qb[kk][0] = valid ? __ldg(reinterpret_cast<const uint32_t *>(q + 16 * kk + 2 * tq)) : 0u;

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) paged_attn_simt_kernel(const 
         float v = 0.f;
         if (r < row_end) {
             const int i = r / p.G, h = kvh * p.G + (r - i * p.G);
-            v = to_float(q[(((long long)b * p.Sq + i) * p.Hq + h) * D + c]);
+            v = to_float(q[q_row_offset(p, ((long long)b * p.Sq + i) * p.Hq + h) + c]);
         }
         s_q[idx] = v;
     }

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     // q, half hh, as fp32 in the lane's visiting order: qh[8 i ..] is chunk (i + rot) % HC of the half
     float qh[D / 2];
     {
-        const T *q = reinterpret_cast<const T *>(p.q) + out_row_index(p, sq, kvh, 0) * D + hh * (D / 2);
+        const T *q = reinterpret_cast<const T *>(p.q) + q_row_offset(p, out_row_index(p, sq, kvh, 0)) + hh * (D / 2);
 #pragma unroll
         for (int i = 0; i < HC; ++i) {
             const uint4 x = __ldg(reinterpret_cast<const uint4 *>(q) + (i + rot) % HC);

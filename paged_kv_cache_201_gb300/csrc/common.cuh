@@ -32,6 +32,7 @@ struct FwdParams {
     const float *v_scale;
     const int32_t *q_start;    // variable-length batches: [B + 1] first packed query token per sequence; else null
     long long rows_total;      // query rows (tokens x heads) of the whole batch: the stride of one split's partials
+    long long q_stride;        // elements between consecutive query tokens of q (Hq * D when dense)
     unsigned int *err;         // device error word
     long long num_pages;
     int B, Sq, Hq, Hkv, D, ps, W;
@@ -45,6 +46,12 @@ struct FwdParams {
 };
 
 // ------------------------------------------------------------------ small helpers
+// Element offset in q of query row ridx = token * Hq + head (tokens q_stride elements apart).
+__device__ __forceinline__ long long q_row_offset(const FwdParams &p, long long ridx) {
+    const long long tok = ridx / p.Hq;
+    return tok * p.q_stride + (ridx - tok * p.Hq) * (long long)p.D;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

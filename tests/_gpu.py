@@ -80,14 +80,14 @@ def run(dw: DeviceWorkload, split_kv: int, variant: int = 0):
             pa.paged_attn_fwd_variant(dw.q, dw.k, dw.v, dw.bt, dw.sl, wl.causal, dw.qo, S, wl.scale, o, l, variant)
 
     if split_kv == 1:
-        out = torch.empty_like(dw.q)
+        out = torch.empty(dw.q.shape, dtype=dw.q.dtype, device=dw.q.device)
         lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=dw.q.device)
         fwd(1, out, lse)
     else:
         po = torch.empty((split_kv, B, Sq, Hq, D), dtype=torch.float32, device=dw.q.device)
         pl = torch.empty((split_kv, B, Sq, Hq), dtype=torch.float32, device=dw.q.device)
         fwd(split_kv, po, pl)
-        out = torch.empty_like(dw.q)
+        out = torch.empty(dw.q.shape, dtype=dw.q.dtype, device=dw.q.device)
         lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=dw.q.device)
         pa.paged_attn_combine(po, pl, out, lse)
         res["part_out"] = to_f64(po, "f32")

@@ -89,6 +89,11 @@ def _fwd(lib, dims, split=1, scale=0.1, lse=FAKE, q=FAKE, out=FAKE, variant=0):
     (dict(head_dim=256), 4, 0.1, dict(variant=6), EUNSUP),
     (dict(dtype=pa.PA_F32), 4, 0.1, dict(variant=6), EUNSUP),
     (dict(q_len=128), 1, -0.1, dict(variant=4), EUNSUP),
+    (dict(q_stride=8 * 128 - 8), 1, 0.1, {}, EINVAL),          # q tokens overlapping their heads
+    (dict(q_stride=12 * 128 + 4), 1, 0.1, {}, EINVAL),         # bf16 rows not 16-byte aligned
+    (dict(q_stride=12 * 128 + 2, dtype=pa.PA_F32), 1, 0.1, {}, EINVAL),
+    (dict(q_stride=1 << 40), 1, 0.1, {}, EINVAL),
+    (dict(batch=0, q_stride=12 * 128), 1, 0.1, {}, OK),       # a fused QKV view's stride is accepted
     (dict(batch=0), 1, 0.1, {}, OK),
     (dict(q_len=0), 4, 0.1, dict(lse=None), OK),
     (dict(q_len=0), 4, 0.1, {}, OK),
@@ -271,3 +276,19 @@ def test_varlen_hint_binding_checks(lib):
     h = pa.paged_attn_varlen_hint(np.array([0], dtype=np.int32), np.zeros(0, dtype=np.int32), None, True, 8, 2)
     assert (h.long_pairs, h.short_kv_tokens) == (0, 0)
     assert lib.paged_attn_varlen_hint(None, None, None, 1, None, None) == EINVAL
+
+
+def test_q_token_stride_of_views():
+    """The binding reads q's token stride from a view's strides (no GPU needed: strides only)."""
+    import torch
+    B, Sq, Hq, Hkv, D = 3, 5, 8, 2, 64
+    fused = torch.empty(B, Sq, Hq + 2 * Hkv, D, dtype=torch.bfloat16)
+    assert pa._q_token_stride(fused[:, :, :Hq]) == (Hq + 2 * Hkv) * D
+    assert pa._q_token_stride(torch.empty(B, Sq, Hq, D)) == 0              # dense
+    assert pa._q_token_stride(fused[:, :1, :Hq]) == Sq * (Hq + 2 * Hkv) * D  # one token per sequence
+    packed = torch.empty(7, Hq + 2 * Hkv, D, dtype=torch.float16)
+    assert pa._q_token_stride(packed[:, :Hq]) == (Hq + 2 * Hkv) * D
+    with pytest.raises(ValueError):                                          # heads not dense
+        pa._q_token_stride(fused[:, :, ::2])
+    with pytest.raises(ValueError):                                          # tokens unevenly spaced
+        pa._q_token_stride(fused[:, ::2, :Hq])
