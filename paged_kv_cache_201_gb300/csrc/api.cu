@@ -113,13 +113,13 @@ int make_pool_map(CUtensorMap *m, const void *base, const pa_dims *d, int halves
 // 3-D view of one 8-bit pool (E4M3 or int8 elements) for TMA: (byte within a row, token, kv head); one box = the page_size
 // rows of one page and one kv head.  128-byte rows (head_dim 128) land with the 128-byte swizzle,
 // which the kernel's conflict-free operand loads rely on; 64-byte rows land as they are.
-int make_pool_map_q8(CUtensorMap *m, const void *base, const pa_dims *d, int heads_per_box = 1) {
+int make_pool_map_q8(CUtensorMap *m, const void *base, const pa_dims *d) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PA_ECUDA;
     const cuuint64_t D = (cuuint64_t)d->head_dim, Hkv = (cuuint64_t)d->num_kv_heads;
     const cuuint64_t dims[3] = {D, (cuuint64_t)d->num_pages * (cuuint64_t)d->page_size, Hkv};
     const cuuint64_t strides[2] = {Hkv * D, D};
-    const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)d->page_size, (cuuint32_t)heads_per_box};
+    const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)d->page_size, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapSwizzle swz = d->head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
@@ -458,12 +458,10 @@ int paged_attn_fwd_kvq(const void *q, const void *k_cache, const void *v_cache, 
                                   out, lse, dims, err);
     p.k_scale = k_scale;
     p.v_scale = v_scale;
-    const int mode = p.rows <= pa::kDecodeRows ? pa::MODE_DECODE : pa::MODE_PREFILL;
-    // boxes of the heads one CTA takes (two adjacent kv heads for decode where the kernel can)
-    const int hp = pa::kvq_heads_per_cta(mode, dims->num_kv_heads, dims->page_size);
     CUtensorMap tmk, tmv;
-    if ((rc = make_pool_map_q8(&tmk, k_cache, dims, hp)) != PA_OK) return rc;
-    if ((rc = make_pool_map_q8(&tmv, v_cache, dims, hp)) != PA_OK) return rc;
+    if ((rc = make_pool_map_q8(&tmk, k_cache, dims)) != PA_OK) return rc;
+    if ((rc = make_pool_map_q8(&tmv, v_cache, dims)) != PA_OK) return rc;
+    const int mode = p.rows <= pa::kDecodeRows ? pa::MODE_DECODE : pa::MODE_PREFILL;
     if (mode == pa::MODE_PREFILL) p.row_tiles = (p.rows + pa::kPrefillRows - 1) / pa::kPrefillRows;
     return cuda_status(pa::launch_mma_kvq(p, mode, dims->dtype, kv_dtype, tmk, tmv, static_cast<cudaStream_t>(stream)));
 }

@@ -214,37 +214,32 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 // and its rows read as zeros).  Per SK-key stage t it writes the stage's page scales into slot
 // t % (2 NSTAGE), arms the stage's barriers and issues one 3-D TMA box per page and pool into
 // ring stage t % NSTAGE.
-template <int D, int NSTAGE, int SK, int HP>
+template <int D, int NSTAGE, int SK>
 __device__ __forceinline__ void kvq_produce(const CUtensorMap *tmK, const CUtensorMap *tmV, const FwdParams &p,
                                             int b, int kvh, int pg0, int k_hi, int n_tiles, int ps_shift,
                                             uint32_t sbase, uint32_t bar_fk, uint32_t bar_fv, uint32_t bar_em,
-                                            float *s_ks, float *s_vs, int lane) {
-    constexpr int kStage8 = SK * HP * D;  // bytes of one K (or V) stage: SK keys of HP kv heads
+                                            float (*s_ks)[SK / 16], float (*s_vs)[SK / 16], int lane) {
+    constexpr int kStage8 = SK * D;  // bytes of one K (or V) stage of SK keys
     constexpr int kSlots = 2 * NSTAGE;
     if (lane == 0) {
         tma_prefetch_desc(tmK);
         tma_prefetch_desc(tmV);
     }
     const int ps = 1 << ps_shift;
-    const int pps = SK >> ps_shift;                      // pages per stage (page_size >= 16: at most SK / 16)
-    const uint32_t box_bytes = (uint32_t)(HP * ps * D);  // one page of HP kv heads, 8-bit elements
+    const int pps = SK >> ps_shift;                 // pages per stage (page_size >= 16: at most SK / 16)
+    const uint32_t box_bytes = (uint32_t)(ps * D);  // one page of one kv head, 8-bit elements
     const int pg_end = (k_hi + ps - 1) >> ps_shift;
     const int32_t *bt_row = p.block_table + (long long)b * p.W;
-    // a lane's page scales of the HP kv heads from kvh (0 for an id outside the pool)
-    auto scales_of = [&](const float *sc, int id, float (&out)[HP]) {
-        const bool in = id >= 0 && (long long)id < p.num_pages;
-#pragma unroll
-        for (int hh = 0; hh < HP; ++hh) out[hh] = in ? __ldg(sc + (long long)id * p.Hkv + kvh + hh) : 0.f;
+    auto scale_of = [&](const float *sc, int id) -> float {
+        return (id >= 0 && (long long)id < p.num_pages) ? __ldg(sc + (long long)id * p.Hkv + kvh) : 0.f;
     };
     int batch = pg0;
     int id_cur = (batch + lane < pg_end) ? __ldg(bt_row + batch + lane) : 0;
     int id_next = (batch + 32 + lane < pg_end) ? __ldg(bt_row + batch + 32 + lane) : 0;
-    float ks_cur[HP], vs_cur[HP], ks_next[HP], vs_next[HP];
-#pragma unroll
-    for (int hh = 0; hh < HP; ++hh) ks_cur[hh] = vs_cur[hh] = ks_next[hh] = vs_next[hh] = 0.f;
+    float ks_cur = 0.f, vs_cur = 0.f, ks_next = 0.f, vs_next = 0.f;
     if (batch + lane < pg_end) {
-        scales_of(p.k_scale, id_cur, ks_cur);
-        scales_of(p.v_scale, id_cur, vs_cur);
+        ks_cur = scale_of(p.k_scale, id_cur);
+        vs_cur = scale_of(p.v_scale, id_cur);
     }
     bool pend = true;  // scales of id_next not loaded yet
     bool bad = false;
@@ -259,40 +254,29 @@ __device__ __forceinline__ void kvq_produce(const CUtensorMap *tmK, const CUtens
         const int pg_first = pg0 + t * pps;
         if (pg_first >= batch + 32) {
             if (pend && batch + 32 + lane < pg_end) {
-                scales_of(p.k_scale, id_next, ks_next);
-                scales_of(p.v_scale, id_next, vs_next);
+                ks_next = scale_of(p.k_scale, id_next);
+                vs_next = scale_of(p.v_scale, id_next);
             }
             batch += 32;
             id_cur = id_next;
-#pragma unroll
-            for (int hh = 0; hh < HP; ++hh) {
-                ks_cur[hh] = ks_next[hh];
-                vs_cur[hh] = vs_next[hh];
-                ks_next[hh] = vs_next[hh] = 0.f;
-            }
+            ks_cur = ks_next;
+            vs_cur = vs_next;
             const int nx = batch + 32 + lane;
             id_next = (nx < pg_end) ? __ldg(bt_row + nx) : 0;
+            ks_next = vs_next = 0.f;
             pend = true;
         }
         const int src = (pg_first + lane - batch) & 31;
         const int id = __shfl_sync(0xffffffffu, id_cur, src);
-        float ks[HP], vs[HP];
-#pragma unroll
-        for (int hh = 0; hh < HP; ++hh) {
-            ks[hh] = __shfl_sync(0xffffffffu, ks_cur[hh], src);
-            vs[hh] = __shfl_sync(0xffffffffu, vs_cur[hh], src);
-        }
+        const float ks = __shfl_sync(0xffffffffu, ks_cur, src);
+        const float vs = __shfl_sync(0xffffffffu, vs_cur, src);
         if (bad) break;
         const int nvalid = min(pps, pg_end - pg_first);
         // Slot t % (2 NSTAGE) was last read for stage t - 2 NSTAGE; every consumer warp has
         // finished that stage once it released stage t - NSTAGE, which the wait above saw.
-        // Scale layout: [slot][head][page of the stage].
         if (lane < pps) {
-#pragma unroll
-            for (int hh = 0; hh < HP; ++hh) {
-                s_ks[(slot * HP + hh) * (SK / 16) + lane] = ks[hh];
-                s_vs[(slot * HP + hh) * (SK / 16) + lane] = vs[hh];
-            }
+            s_ks[slot][lane] = ks;
+            s_vs[slot][lane] = vs;
         }
         __syncwarp();
         if (lane == 0) {
@@ -315,8 +299,8 @@ __device__ __forceinline__ void kvq_produce(const CUtensorMap *tmK, const CUtens
         issued = t + 1;
         if (pend) {  // after this stage's copies are on their way
             if (batch + 32 + lane < pg_end) {
-                scales_of(p.k_scale, id_next, ks_next);
-                scales_of(p.v_scale, id_next, vs_next);
+                ks_next = scale_of(p.k_scale, id_next);
+                vs_next = scale_of(p.v_scale, id_next);
             }
             pend = false;
         }
@@ -356,46 +340,38 @@ __device__ __forceinline__ KvqUnit kvq_unit(const FwdParams &p, int b, int s, in
 // ============================================================================ decode
 // At most 16 query rows per (sequence, kv head): the kernel computes S^T = K Q^T and O^T = V^T P^T,
 // so that keys and head dimension fill the MMA's 16-row side and the few query rows (GQA group x
-// query tokens, padded to NR x 8) its 8-column side.  A CTA takes HP adjacent kv heads of one
-// (sequence, split): each TMA box is a page of all HP heads, so a token's rows of those heads are
-// one contiguous read of HP x D bytes.  The 4 / HP warps of head hh read keys [16 w, 16 w + 16) of
-// every stage (one page: page_size >= 16), and each head's warps merge their softmax states at the
-// end.
-template <typename T, int FMT, int D, int NR, int NSTAGE, int KPW, int MINB, int HP>
+// query tokens, padded to NR x 8) its 8-column side.  Warp w reads keys [16 w, 16 w + 16) of every
+// stage (one page: page_size >= 16); the four warps' softmax states are merged at the end.
+template <typename T, int FMT, int D, int NR, int NSTAGE, int KPW, int MINB>
 __global__ void __launch_bounds__(kMmaThreads, MINB)
     paged_attn_kvq_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                                  const FwdParams p, int ps_shift) {
     using Op = MmaOp<__half>;
-    constexpr int WPH = kMmaConsumerWarps / HP;  // consumer warps per kv head
-    constexpr int SK = WPH * KPW;                // keys per stage (of each head)
+    constexpr int SK = kMmaConsumerWarps * KPW;  // keys per stage
     constexpr int NB = KPW / 16;                 // 16-key blocks per warp and stage (one page each)
-    constexpr int kStage8 = SK * HP * D;         // bytes of one K (or V) stage
+    constexpr int kStage8 = SK * D;              // bytes of one K (or V) stage
     constexpr int kSlots = 2 * NSTAGE;
     constexpr int MT = D / 16;                   // 16-wide head-dim tiles of O^T
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[3 * NSTAGE];
-    __shared__ float s_ks[kSlots][HP][SK / 16];
-    __shared__ float s_vs[kSlots][HP][SK / 16];
+    __shared__ float s_ks[kSlots][SK / 16];
+    __shared__ float s_vs[kSlots][SK / 16];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     int unit = blockIdx.x;
-    const int kvh0 = (unit % (p.Hkv / HP)) * HP;  // first kv head of the CTA
-    unit /= p.Hkv / HP;
+    const int kvh = unit % p.Hkv;
+    unit /= p.Hkv;
     const int s = unit % p.split_kv;
     const int b = unit / p.split_kv;
-    const int hh = warp < kMmaConsumerWarps ? warp / WPH : 0;  // this warp's head within the CTA
-    const int kvh = kvh0 + hh;
     const KvqUnit u = kvq_unit(p, b, s, ps_shift);
     const SeqRows sq = uniform_seq(p, b);
     const int rows = p.rows;  // <= 8 NR
     const int k_hi = min(u.k_hi_split, row_key_limit(p, b, u.L, (rows - 1) / p.G));
     const int n_tiles = k_hi > u.k_lo ? (k_hi - u.k_lo + SK - 1) / SK : 0;
     if (n_tiles == 0) {
-        if (warp < kMmaConsumerWarps)
-#pragma unroll
-            for (int h = 0; h < HP; ++h) store_empty_unit<T, D>(p, sq, kvh0 + h, s, 0, rows);
+        if (warp < kMmaConsumerWarps) store_empty_unit<T, D>(p, sq, kvh, s, 0, rows);
         return;
     }
 
@@ -415,18 +391,15 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
     __syncthreads();
 
     if (warp == kMmaConsumerWarps) {
-        kvq_produce<D, NSTAGE, SK, HP>(&tmK, &tmV, p, b, kvh0, u.pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk,
-                                       bar_fv, bar_em, &s_ks[0][0][0], &s_vs[0][0][0], lane);
+        kvq_produce<D, NSTAGE, SK>(&tmK, &tmV, p, b, kvh, u.pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk, bar_fv,
+                                   bar_em, s_ks, s_vs, lane);
         return;
     }
 
     // ==================================================================== consumers
     const int g = lane >> 2;
     const int tq = lane & 3;
-    const int kw0 = (warp % WPH) * KPW;  // this warp's keys in every stage: NB blocks of 16
-    // ring row of stage key k of this warp's head: a stage holds its pages one after the other, each
-    // page as HP heads x page_size rows of D bytes
-    auto krow = [&](int k) { return (((k >> ps_shift) * HP + hh) << ps_shift) | (k & ((1 << ps_shift) - 1)); };
+    const int kw0 = warp * KPW;  // this warp's keys in every stage: NB blocks of 16
     // Q^T operands: row-tile nr, this lane's row 8 nr + g.  The score and output fragments hold
     // rows 8 nr + 2 tq + e (e = 0, 1): their inverse query scalings come from lanes 4 (2 tq + e).
     uint32_t qb[NR][D / 16][2];
@@ -496,8 +469,8 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {
                     uint32_t wg[4], w8[4];
-                    lds_v4(ring_chunk_addr<D>(kring, krow(kw0 + 16 * hb + g), (D / 64) * tq + h), wg);
-                    lds_v4(ring_chunk_addr<D>(kring, krow(kw0 + 16 * hb + g + 8), (D / 64) * tq + h), w8);
+                    lds_v4(ring_chunk_addr<D>(kring, kw0 + 16 * hb + g, (D / 64) * tq + h), wg);
+                    lds_v4(ring_chunk_addr<D>(kring, kw0 + 16 * hb + g + 8, (D / 64) * tq + h), w8);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int kk = 4 * h + i;
@@ -513,7 +486,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
             // per row over the warp's KPW keys
             float ksc[NB];
 #pragma unroll
-            for (int hb = 0; hb < NB; ++hb) ksc[hb] = s_ks[slot][hh][(kw0 + 16 * hb) >> ps_shift];
+            for (int hb = 0; hb < NB; ++hb) ksc[hb] = s_ks[slot][(kw0 + 16 * hb) >> ps_shift];
             float al[NR][2], pv[NB][NR][2][2];
             bool moved = false;
 #pragma unroll
@@ -593,7 +566,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h) {
                         uint32_t w[4];
-                        lds_v4(ring_chunk_addr<D>(vring, krow(kw0 + 16 * hb + g + 8 * kh), (D / 64) * tq + h), w);
+                        lds_v4(ring_chunk_addr<D>(vring, kw0 + 16 * hb + g + 8 * kh, (D / 64) * tq + h), w);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) vw[hb][kh][4 * h + i] = w[i];
                     }
@@ -613,7 +586,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
                 // this lane's bytes 4 mt + {0..3} of keys g and g + 8: four 8 x 8 blocks (keys x 2-byte
                 // d slots) which movmatrix turns into the A operand (d x keys), so output row m of the
                 // tile is head-dim index out_d(mt, m) (see the merge below).
-                const float vsc = s_vs[slot][hh][(kw0 + 16 * hb) >> ps_shift];
+                const float vsc = s_vs[slot][(kw0 + 16 * hb) >> ps_shift];
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     uint32_t x00, x01, x10, x11;  // [key half][d slot half]
@@ -674,9 +647,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
         }
     }
     named_bar_sync(1, kMmaConsumerWarps * 32);
-    if (!bad)
-#pragma unroll
-        for (int h = 0; h < HP; ++h) decode_merge_store<T, D, WPH>(p, sm, sq, kvh0 + h, s, 0, rows, h * WPH);
+    if (!bad) decode_merge_store<T, D>(p, sm, sq, kvh, s, 0, rows);
 }
 
 // ============================================================================ prefill
@@ -736,8 +707,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     __syncthreads();
 
     if (warp == kMmaConsumerWarps) {
-        kvq_produce<D, NSTAGE, kMmaTileKeys, 1>(&tmK, &tmV, p, b, kvh, u.pg0, k_hi, n_tiles, ps_shift, sbase,
-                                                bar_fk, bar_fv, bar_em, &s_ks[0][0], &s_vs[0][0], lane);
+        kvq_produce<D, NSTAGE, kMmaTileKeys>(&tmK, &tmV, p, b, kvh, u.pg0, k_hi, n_tiles, ps_shift, sbase, bar_fk,
+                                             bar_fv, bar_em, s_ks, s_vs, lane);
         return;
     }
 
@@ -915,17 +886,15 @@ static int ps_shift_of(int ps) {
 
 // Decode shape: KPW keys per consumer warp and stage (stages of 4 KPW keys), NSTAGE-deep ring,
 // MINB CTAs per SM.
-template <typename T, int FMT, int D, int NR, int KPW, int NSTAGE, int MINB, int HP>
+template <typename T, int FMT, int D, int NR, int KPW, int NSTAGE, int MINB>
 static cudaError_t launch_kvq_decode(const FwdParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                      cudaStream_t stream) {
-    // a stage is (4 / HP) KPW keys of HP heads: the same bytes for every HP
     constexpr size_t smem = (size_t)NSTAGE * 2 * kMmaConsumerWarps * KPW * D + 1024;
     static_assert(merge_scratch_bytes(D) + 1024 <= smem, "decode merge scratch must fit in the ring");
-    auto kern = paged_attn_kvq_decode_kernel<T, FMT, D, NR, NSTAGE, KPW, MINB, HP>;
+    auto kern = paged_attn_kvq_decode_kernel<T, FMT, D, NR, NSTAGE, KPW, MINB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (p.Hkv % HP != 0) return cudaErrorInvalidValue;
-    const long long units = (long long)p.B * p.split_kv * (p.Hkv / HP);
+    const long long units = (long long)p.B * p.split_kv * p.Hkv;
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)units, kMmaThreads, smem, stream>>>(tmk, tmv, p, ps_shift_of(p.ps));
@@ -954,13 +923,8 @@ static cudaError_t launch_kvq_d(const FwdParams &p, int mode, const CUtensorMap 
     // 16 keys per warp and stage, 4 (D = 128) or 8 (D = 64) 64-key stages: 65 KiB, so 3 CTAs per SM
     // for <= 8 rows.  Measured on the FP8 Llama-3-8B decode: 32 keys per warp (two blocks sharing one
     // softmax step) with 2 or 3 stages, and 6 stages at 2 CTAs per SM, were no faster.
-    // The tensor maps' boxes hold kvq_heads_per_cta() heads (the host made them for this choice).
-    if (kvq_heads_per_cta(mode, p.Hkv, p.ps) == 2) {
-        if (p.rows <= 8) return launch_kvq_decode<T, FMT, D, 1, 16, (D == 128 ? 4 : 8), 3, 2>(p, tmk, tmv, stream);
-        return launch_kvq_decode<T, FMT, D, 2, 16, (D == 128 ? 4 : 8), 2, 2>(p, tmk, tmv, stream);
-    }
-    if (p.rows <= 8) return launch_kvq_decode<T, FMT, D, 1, 16, (D == 128 ? 4 : 8), 3, 1>(p, tmk, tmv, stream);
-    return launch_kvq_decode<T, FMT, D, 2, 16, (D == 128 ? 4 : 8), 2, 1>(p, tmk, tmv, stream);
+    if (p.rows <= 8) return launch_kvq_decode<T, FMT, D, 1, 16, (D == 128 ? 4 : 8), 3>(p, tmk, tmv, stream);
+    return launch_kvq_decode<T, FMT, D, 2, 16, (D == 128 ? 4 : 8), 2>(p, tmk, tmv, stream);
 }
 
 template <int FMT>

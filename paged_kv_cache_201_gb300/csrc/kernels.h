@@ -33,12 +33,6 @@ cudaError_t launch_mma(const FwdParams &p, int mode, int dtype, const CUtensorMa
 // Variable-length batch (p.q_start set, p.B sequences, total_q packed query tokens).
 cudaError_t launch_mma_varlen(const FwdParams &p, long long total_q, int dtype, const CUtensorMap &tmk,
                               const CUtensorMap &tmv, cudaStream_t stream);
-// kv heads per CTA, and per TMA box, of the 8-bit-pool kernels: two adjacent heads for decode when
-// the pool has an even head count and pages of at most 32 tokens (a stage then holds whole pages of
-// both heads), else one.  The host builds the tensor maps with boxes of this many heads.
-inline int kvq_heads_per_cta(int mode, int Hkv, int ps) {
-    return (mode == MODE_DECODE && Hkv % 2 == 0 && ps <= 32) ? 2 : 1;
-}
 // 8-bit pools (kv_dtype PA_FP8_E4M3 or PA_INT8) with per-(page, kv head) scales in p.k_scale /
 // p.v_scale; bf16/f16 queries.
 cudaError_t launch_mma_kvq(const FwdParams &p, int mode, int dtype, int kv_dtype, const CUtensorMap &tmk,

@@ -260,15 +260,15 @@ __host__ __device__ constexpr size_t merge_scratch_bytes(int D) {
 
 // Second half of the decode merge: shared memory `sm` holds, for each consumer warp w, rows
 // [w][16][D + 4] of unnormalised outputs, then maxima [w][16] and sums [w][16] (log2 domain), for
-// unit rows row0 .. row0 + 15.  Each row below row_end is combined over the NW warps from w0 (0/0
-// guard: l == 0 stores 0, lse -inf) and stored as kv head kvh's rows.
-template <typename T, int D, int NW = kMmaConsumerWarps>
+// unit rows row0 .. row0 + 15.  Each row below row_end is combined over the warps (0/0 guard:
+// l == 0 stores 0, lse -inf) and stored.
+template <typename T, int D>
 __device__ __forceinline__ void decode_merge_store(const FwdParams &p, const float *sm, const SeqRows &sq, int kvh,
-                                                   int s, int row0, int row_end, int w0 = 0) {
+                                                   int s, int row0, int row_end) {
     constexpr int ACC_STRIDE = D + 4;
-    const float *s_acc = sm + w0 * 16 * ACC_STRIDE;
-    const float *s_m = sm + kMmaConsumerWarps * 16 * ACC_STRIDE + w0 * 16;
-    const float *s_l = sm + kMmaConsumerWarps * 16 * ACC_STRIDE + kMmaConsumerWarps * 16 + w0 * 16;
+    const float *s_acc = sm;
+    const float *s_m = sm + kMmaConsumerWarps * 16 * ACC_STRIDE;
+    const float *s_l = s_m + kMmaConsumerWarps * 16;
     const int tid = threadIdx.x;  // 0..127
     const int r = tid >> 3;       // 16 rows x 8 column groups
     const int cg = tid & 7;
@@ -276,11 +276,11 @@ __device__ __forceinline__ void decode_merge_store(const FwdParams &p, const flo
     if (row0 + r < row_end) {
         float M = kNegInf;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w * 16 + r]);
-        float wsc[NW];
+        for (int w = 0; w < kMmaConsumerWarps; ++w) M = fmaxf(M, s_m[w * 16 + r]);
+        float wsc[kMmaConsumerWarps];
         float Lsum = 0.f;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
+        for (int w = 0; w < kMmaConsumerWarps; ++w) {
             wsc[w] = (M == kNegInf) ? 0.f : exp2f(s_m[w * 16 + r] - M);
             Lsum += wsc[w] * s_l[w * 16 + r];
         }
@@ -291,7 +291,7 @@ __device__ __forceinline__ void decode_merge_store(const FwdParams &p, const flo
             const int col = cg * COLS + c;
             float o0 = 0.f, o1 = 0.f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
+            for (int w = 0; w < kMmaConsumerWarps; ++w) {
                 const float2 v = *reinterpret_cast<const float2 *>(s_acc + (w * 16 + r) * ACC_STRIDE + col);
                 o0 += wsc[w] * v.x;
                 o1 += wsc[w] * v.y;
