@@ -354,24 +354,79 @@ def timed_batches(fns, K: int, stream, flush=None):
 
 
 E2E_TIMING = ("value / ms_per_step: host wall clock (time.perf_counter) from a synchronised device to the "
-              "synchronize after the batch's last step, median of batches, so host launch and copy-issue "
-              "costs count; event_value / event_ms_per_step: CUDA events on the stream around the same batches")
+              "synchronize after the batch's last read-back, median of 5 batches, so host launch and copy-issue "
+              "costs count; event_value / event_ms_per_step: CUDA events from the batch's first upload to its "
+              "last read-back")
+E2E_PIPELINING = ("every step uploads its inputs from pinned host memory, makes the public call and reads its "
+                  "outputs back to pinned host memory; two buffer sets let step i+1's upload and step i-1's "
+                  "read-back run on copy streams while step i computes, as a serving loop does")
 
 
-def e2e_batches(step, K: int, stream):
-    """End-to-end timing of K calls of ``step`` in N_BATCHES batches: each batch starts from a
-    synchronised device and ends with a synchronize.  Returns (median event ms per step, median host
-    wall-clock ms per step)."""
+class PipelinedE2E:
+    """End-to-end steps the way a serving loop runs them: every step uploads its inputs from pinned
+    host memory, makes the public call and reads its results back to pinned host memory, with two
+    buffer sets so that step i + 1's upload and step i - 1's read-back run on copy streams while step
+    i computes.  Each step's own copies are in the timed region; events order every reuse of a buffer
+    (an upload waits until the call two steps earlier has read that set, a call until the read-back
+    two steps earlier has left its outputs).
+
+    host_in: pinned host tensors; dev_in(j): device tensors of set j in the same order; dev_out(j) /
+    host_out(j): the call's outputs and their pinned host copies; call(ins, outs, stream) runs one
+    step on `stream`."""
+
+    def __init__(self, host_in, dev_in, dev_out, host_out, call, stream):
+        import torch
+        self.torch, self.host_in, self.call, self.stream = torch, host_in, call, stream
+        self.dev_in = [dev_in(j) for j in range(2)]
+        self.dev_out = [dev_out(j) for j in range(2)]
+        self.host_out = [host_out(j) for j in range(2)]
+        self.h2d, self.d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.in_ready, self.in_free, self.out_ready, self.out_free = ev(), ev(), ev(), ev()
+        self.i = 0
+
+    def step(self):
+        torch = self.torch
+        j, first = self.i & 1, self.i < 2
+        with torch.cuda.stream(self.h2d):
+            if not first:
+                self.h2d.wait_event(self.in_free[j])
+            for dst, src in zip(self.dev_in[j], self.host_in):
+                dst.copy_(src, non_blocking=True)
+            self.in_ready[j].record(self.h2d)
+        self.stream.wait_event(self.in_ready[j])
+        if not first:
+            self.stream.wait_event(self.out_free[j])
+        self.call(self.dev_in[j], self.dev_out[j], self.stream)
+        self.in_free[j].record(self.stream)
+        self.out_ready[j].record(self.stream)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.out_ready[j])
+            for dst, src in zip(self.host_out[j], self.dev_out[j]):
+                dst.copy_(src, non_blocking=True)
+            self.out_free[j].record(self.d2h)
+        self.i += 1
+
+    def bytes(self):
+        h = sum(t.numel() * t.element_size() for t in self.host_in)
+        d = sum(t.numel() * t.element_size() for t in self.host_out[0])
+        return int(h), int(d)
+
+
+def e2e_pipelined_batches(pipe, K: int):
+    """K pipelined steps in N_BATCHES batches, each from a synchronised device to a synchronize after
+    its last read-back.  Returns (median event ms per step, first upload to last read-back; median
+    host wall-clock ms per step)."""
     import torch
     ev_ms, wall_ms = [], []
     for n in batch_sizes(K):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        a.record(stream)
+        a.record(pipe.h2d)
         for _ in range(n):
-            step()
-        b.record(stream)
+            pipe.step()
+        b.record(pipe.d2h)
         torch.cuda.synchronize()
         wall_ms.append((time.perf_counter() - t0) * 1e3 / n)
         ev_ms.append(a.elapsed_time(b) / n)
@@ -623,41 +678,35 @@ def run_ours(args, ws, rank, local):
     # ---- end to end through the public API: host inputs in, host result out, every step
     e2e = None
     if not args.no_e2e:
-        q_h = q.cpu().pin_memory()
-        bt_h = bt.cpu().pin_memory()
-        sl_h = sl.cpu().pin_memory()
-        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-
+        host_in = [q.cpu().pin_memory(), bt.cpu().pin_memory(), sl.cpu().pin_memory()]
         wsp_bytes = pa.paged_attn_workspace_bytes(q, k, bt, S)
         wsp = torch.empty(max(wsp_bytes, 256), dtype=torch.uint8, device=dev)
 
-        def e2e_step():
+        def call(ins, outs, st):
             # the single public call: split forward into the workspace, then the combine
-            q.copy_(q_h, non_blocking=True)
-            bt.copy_(bt_h, non_blocking=True)
-            sl.copy_(sl_h, non_blocking=True)
+            qd, btd, sld = ins
+            od, ld = outs
             if kvq:
-                pa.paged_attn_fwd_kvq_splitkv(q, k, v, ks, vs, bt, sl, wl.causal, qo, S, wl.scale, out, lse, wsp,
-                                              stream=stream, kv_dtype=kv_code)
+                pa.paged_attn_fwd_kvq_splitkv(qd, k, v, ks, vs, btd, sld, wl.causal, qo, S, wl.scale, od, ld, wsp,
+                                              stream=st, kv_dtype=kv_code)
             else:
-                pa.paged_attn_fwd_splitkv(q, k, v, bt, sl, wl.causal, qo, S, wl.scale, out, lse, wsp,
-                                          stream=stream)
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+                pa.paged_attn_fwd_splitkv(qd, k, v, btd, sld, wl.causal, qo, S, wl.scale, od, ld, wsp, stream=st)
 
+        pipe = PipelinedE2E(host_in, lambda j: [torch.empty_like(t, device=dev) for t in host_in],
+                            lambda j: [torch.empty_like(out), torch.empty_like(lse)],
+                            lambda j: [torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                                       torch.empty(lse.shape, dtype=lse.dtype).pin_memory()], call, stream)
         for _ in range(3):
-            e2e_step()
+            pipe.step()
         torch.cuda.synchronize()
         barrier(ws)
-        e2e_ev_ms, e2e_wall_ms = e2e_batches(e2e_step, max(10, K // 4), stream)
+        e2e_ev_ms, e2e_wall_ms = e2e_pipelined_batches(pipe, max(10, K // 4))
         e2e_ms = max_over_ranks(e2e_wall_ms, ws, dev)
         e2e_ev_ms = max_over_ranks(e2e_ev_ms, ws, dev)
-        hb = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
-        db = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+        hb, db = pipe.bytes()
         e2e = {"value": round(job_throughput(ab["total"], ws, e2e_ms), 1), "unit": "GB/s",
-               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(hb), "d2h_bytes_per_step": int(db),
-               "timing": E2E_TIMING,
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db,
+               "timing": E2E_TIMING, "pipelining": E2E_PIPELINING,
                "event_value": round(job_throughput(ab["total"], ws, e2e_ev_ms), 1),
                "event_ms_per_step": round(e2e_ev_ms, 4),
                "api": ("paged_attn_fwd_kvq_splitkv" if kvq else "paged_attn_fwd_splitkv") +
@@ -840,30 +889,35 @@ def run_varlen(args, ws, rank, local):
 
     e2e = None
     if not args.no_e2e:
-        q_h = q.cpu().pin_memory()
-        small = [t.cpu().pin_memory() for t in (bt, sl, qs, qo)]
-        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        host_in = [t.cpu().pin_memory() for t in (q, bt, sl, qs, qo)]
+        po_e = torch.empty_like(po) if S > 1 else None
+        pl_e = torch.empty_like(pl) if S > 1 else None
 
-        def e2e_step():
-            q.copy_(q_h, non_blocking=True)
-            for dst, src in zip((bt, sl, qs, qo), small):
-                dst.copy_(src, non_blocking=True)
-            step(None if args.no_overlap else make_hint())  # the hint from this step's host arrays
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+        def call(ins, outs, st):
+            qd, btd, sld, qsd, qod = ins
+            od, ld = outs
+            h = None if args.no_overlap else make_hint()  # the hint from this step's host arrays
+            if S == 1:
+                pa.paged_attn_fwd_varlen(qd, k, v, btd, sld, qsd, wl.causal, qod, 1, wl.scale, od, ld, st, hint=h)
+            else:
+                pa.paged_attn_fwd_varlen(qd, k, v, btd, sld, qsd, wl.causal, qod, S, wl.scale, po_e, pl_e, st, hint=h)
+                pa.paged_attn_combine(po_e, pl_e, od, ld, st)
 
+        pipe = PipelinedE2E(host_in, lambda j: [torch.empty_like(t, device=dev) for t in host_in],
+                            lambda j: [torch.empty_like(out), torch.empty_like(lse)],
+                            lambda j: [torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                                       torch.empty(lse.shape, dtype=lse.dtype).pin_memory()], call, stream)
         for _ in range(3):
-            e2e_step()
+            pipe.step()
+        torch.cuda.synchronize()
         barrier(ws)
-        e2e_ev_ms, e2e_wall_ms = e2e_batches(e2e_step, max(10, K // 4), stream)
+        e2e_ev_ms, e2e_wall_ms = e2e_pipelined_batches(pipe, max(10, K // 4))
         e2e_ms = max_over_ranks(e2e_wall_ms, ws, dev)
         e2e_ev_ms = max_over_ranks(e2e_ev_ms, ws, dev)
-        hb = q_h.numel() * q_h.element_size() + sum(t.numel() * 4 for t in small)
-        db = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+        hb, db = pipe.bytes()
         e2e = {"value": round(job_throughput(ab["total"], ws, e2e_ms), 1), "unit": "GB/s",
-               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(hb), "d2h_bytes_per_step": int(db),
-               "timing": E2E_TIMING,
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db,
+               "timing": E2E_TIMING, "pipelining": E2E_PIPELINING,
                "event_value": round(job_throughput(ab["total"], ws, e2e_ev_ms), 1),
                "event_ms_per_step": round(e2e_ev_ms, 4),
                "api": ("paged_attn_fwd_varlen" if args.no_overlap else

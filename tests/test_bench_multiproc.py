@@ -52,3 +52,16 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.0, 1, None) == 3.0
     assert bench.job_throughput(4_000_000_000, 1, 2.0) == pytest.approx(2000.0)
+
+
+def test_timing_protocol_batches():
+    """K timed steps are cut into 5 batches (fewer when K < 5) that add up to exactly K."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.batch_sizes(250) == [50] * 5
+    assert bench.batch_sizes(20) == [4] * 5
+    assert bench.batch_sizes(3) == [1, 1, 1]
+    for K in range(1, 300):
+        b = bench.batch_sizes(K)
+        assert sum(b) == K and len(b) == min(5, K) and max(b) - min(b) <= 1
