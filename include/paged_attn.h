@@ -55,8 +55,7 @@ enum {
     PA_EUNSUPPORTED = -3,  /* shape outside the supported envelope (or forced variant cannot run it) */
     PA_ECUDA = -4,         /* a CUDA runtime/driver call failed */
     PA_EBOUNDS = -5,       /* paged_attn_last_error_word: a page id outside [0, num_pages) was read */
-    PA_ETIMEOUT = -6,      /* paged_attn_last_error_word: a pipeline wait gave up; outputs are invalid */
-    PA_ERANGE = -7         /* paged_attn_last_error_word: PA_ERRBIT_RANGE; the affected rows are not finite */
+    PA_ETIMEOUT = -6       /* paged_attn_last_error_word: a pipeline wait gave up; outputs are invalid */
 };
 
 /* bits of the device error word */
@@ -64,10 +63,7 @@ enum {
     PA_ERRBIT_PAGE_RANGE = 1u,   /* a block-table page id used by a sequence was outside [0, num_pages) */
     PA_ERRBIT_TIMEOUT = 2u,      /* a pipeline wait gave up after its time limit (results invalid) */
     PA_ERRBIT_SEQ_CLIPPED = 4u,  /* seq_lens[b] needed more pages than bt_stride holds; clipped to bt_stride pages */
-    PA_ERRBIT_QSTART = 8u,       /* paged_attn_fwd_varlen: a q_start entry out of [0, total tokens] or decreasing */
-    PA_ERRBIT_RANGE = 16u        /* tcgen05 kernel, bf16: a V tile held values more than 2^15 times larger than an
-                                    earlier tile of the same unit could scale to (see PA_VARIANT_TC05_PREFILL);
-                                    rows that weight them are not finite */
+    PA_ERRBIT_QSTART = 8u        /* paged_attn_fwd_varlen: a q_start entry out of [0, total tokens] or decreasing */
 };
 
 /* kernel variants (paged_attn_fwd_variant) */
@@ -370,8 +366,6 @@ int paged_attn_debug_wait_timeout(uint32_t limit_us, void *stream);
  *   PA_ETIMEOUT  PA_ERRBIT_TIMEOUT is set: a pipeline wait gave up after its
  *                2 s limit and its warp left the pipeline, so outputs written
  *                since the last read are invalid (not merely inaccurate);
- *   PA_ERANGE    otherwise, PA_ERRBIT_RANGE is set (tcgen05 kernel, bf16 V
- *                values beyond its per-unit scaling; see PA_VARIANT_TC05_PREFILL);
  *   PA_EBOUNDS   otherwise, PA_ERRBIT_PAGE_RANGE is set: a sequence's page id
  *                lay outside [0, num_pages); its tokens read as zero (the
  *                rocm-libraries PR #14349 kernel leaves this unchecked, "Not in

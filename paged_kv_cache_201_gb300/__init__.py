@@ -32,8 +32,8 @@ __all__ = [
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_INT8 = 0, 1, 2, 3, 4
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA_DECODE, VARIANT_MMA_PREFILL, VARIANT_TC05_PREFILL, VARIANT_MMA_T = 0, 1, 2, 3, 4, 5
 VARIANT_MMA_SPLIT_GROUP = 6
-ERRBIT_PAGE_RANGE, ERRBIT_TIMEOUT, ERRBIT_SEQ_CLIPPED, ERRBIT_QSTART, ERRBIT_RANGE = 1, 2, 4, 8, 16
-PA_OK, PA_EINVAL, PA_EDTYPE, PA_EUNSUPPORTED, PA_ECUDA, PA_EBOUNDS, PA_ETIMEOUT, PA_ERANGE = 0, -1, -2, -3, -4, -5, -6, -7
+ERRBIT_PAGE_RANGE, ERRBIT_TIMEOUT, ERRBIT_SEQ_CLIPPED, ERRBIT_QSTART = 1, 2, 4, 8
+PA_OK, PA_EINVAL, PA_EDTYPE, PA_EUNSUPPORTED, PA_ECUDA, PA_EBOUNDS, PA_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 
 
 class PaDims(ctypes.Structure):
@@ -520,17 +520,17 @@ def paged_attn_debug_wait_timeout(limit_us: int, stream=None) -> None:
 
 def paged_attn_last_error_word() -> int:
     """Read and clear the device error word; returns its PA_ERRBIT_* bits.  The C call's statuses
-    that describe the bits (PA_ETIMEOUT, PA_ERANGE, PA_EBOUNDS, PA_EINVAL with bits set) are not raised here:
+    that describe the bits (PA_ETIMEOUT, PA_EBOUNDS, PA_EINVAL with bits set) are not raised here:
     the bits carry the same facts (see ``paged_attn_last_error_status``)."""
     return paged_attn_last_error_status()[1]
 
 
 def paged_attn_last_error_status():
-    """(status, bits) of paged_attn_last_error_word: status PA_OK, PA_ETIMEOUT, PA_ERANGE, PA_EBOUNDS or
+    """(status, bits) of paged_attn_last_error_word: status PA_OK, PA_ETIMEOUT, PA_EBOUNDS or
     PA_EINVAL (a bad q_start entry), as the header defines them.  A failed read raises."""
     v = ctypes.c_uint32(0)
     rc = load_library().paged_attn_last_error_word(ctypes.byref(v))
-    if rc in (PA_ETIMEOUT, PA_ERANGE, PA_EBOUNDS) or (rc == PA_EINVAL and v.value):
+    if rc in (PA_ETIMEOUT, PA_EBOUNDS) or (rc == PA_EINVAL and v.value):
         return rc, int(v.value)
     _raise(rc, "paged_attn_last_error_word")
     return rc, int(v.value)

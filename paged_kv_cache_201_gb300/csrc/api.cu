@@ -702,7 +702,6 @@ int paged_attn_last_error_word(uint32_t *flags) {
     // The most serious condition first: a wait that gave up leaves outputs unwritten, an
     // out-of-range page id only zeroes that page's tokens.
     if (v & PA_ERRBIT_TIMEOUT) return PA_ETIMEOUT;
-    if (v & PA_ERRBIT_RANGE) return PA_ERANGE;
     if (v & PA_ERRBIT_PAGE_RANGE) return PA_EBOUNDS;
     if (v & PA_ERRBIT_QSTART) return PA_EINVAL;
     return PA_OK;
@@ -717,7 +716,6 @@ const char *paged_attn_strerror(int code) {
         case PA_ECUDA: return "CUDA call failed";
         case PA_EBOUNDS: return "out-of-range page id";
         case PA_ETIMEOUT: return "a pipeline wait timed out (results invalid)";
-        case PA_ERANGE: return "values outside the kernel's scaling range (affected rows not finite)";
         default: return "unknown status";
     }
 }

@@ -64,11 +64,9 @@ constexpr int kT5StageLens = 1024;            // batches up to this size keep se
 //   OFREE  O buffer read out by the epilogue threads (128 arrive)
 //   LF/LE  a unit's row maxima and sums handed to the epilogue (256 softmax threads arrive) / read
 //          by it (128 epilogue threads arrive); indexed like the O buffers
-//   XF     bf16: a unit's V exponent handed to the epilogue (32 V-gate threads arrive); its slot is
-//          rewritten only after LE of the unit two before
 enum {
     B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_PF = 14, B_OF = 16, B_OFREE = 18,
-    B_OD = 20, B_VZ = 21, B_LF = 23, B_LE = 25, B_XF = 27, B_COUNT = 29
+    B_OD = 20, B_VZ = 21, B_LF = 23, B_LE = 25, B_COUNT = 27
 };
 
 // Output row of query token tok (of the sequence whose first packed token is q0) and head kvh G + g.
@@ -88,17 +86,17 @@ __device__ __forceinline__ void t5_store_lse(const FwdParams &p, int s, long lon
 
 }  // namespace
 
-// P V runs in f16 for both input types: P in [0, 1] rounded to f16 is 2^-11 relative, and a bf16 V
-// tile is turned into f16 in shared memory before the product reads it (t5_convert_v), so one
-// product per 16 keys carries the weights.
+// P V with P split into a 16-bit high part and its rounding remainder (two products) for bf16; f16
+// rounds P to 2^-11 relative (p in [0, 1]), well inside the tolerance, so one product is enough.
 template <typename T>
-__host__ __device__ constexpr bool t5_convert_v() { return std::is_same<T, __nv_bfloat16>::value; }
+__host__ __device__ constexpr bool t5_split_p() { return !std::is_same<T, __half>::value; }
 
 // P for 32 keys of one row: p = exp2(s * c2 + nmu), where the caller has set the scores of masked
 // keys to -inf (c2 > 0, so their p is exactly 0: one code path for every tile keeps the loop small
-// in the instruction cache); l accumulates the p; the first 16 of the 32 columns at `taddr` receive
-// the weights as f16 pairs.  Packed pairs of fp32 (the f32x2 arithmetic of sm_100-family cores: one
-// instruction per pair, each lane rounded as its scalar counterpart).
+// in the instruction cache); l accumulates the p; the 32 columns at `taddr` receive [16 columns of
+// high parts | 16 columns of remainders] (bf16/f16 pairs; the remainders only when t5_split_p<T>()).
+// Packed pairs of fp32 (the f32x2 arithmetic of sm_100-family cores: one instruction per pair,
+// each lane rounded as its scalar counterpart).
 __device__ __forceinline__ uint64_t f2_pack(float x, float y) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
@@ -119,14 +117,15 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
     uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 
+template <typename T>
 __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], float c2, float nmu, float &l, uint32_t taddr) {
-    uint32_t hi[16];
+    uint32_t hi[16], lo[16];
     const uint64_t c2x2 = f2_pack(c2, c2), nmux2 = f2_pack(nmu, nmu);
     uint64_t l2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};  // two pair sums: short dependency chains
 #pragma unroll
@@ -136,77 +135,17 @@ __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], float c2, 
         const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
         const uint64_t pp = f2_pack(p0, p1);
         l2[i & 1] = f2_add(l2[i & 1], pp);
-        hi[i] = MmaOp<__half>::pack(p0, p1);
+        hi[i] = MmaOp<T>::pack(p0, p1);
+        if (t5_split_p<T>()) {
+            const float2 h2 = MmaOp<T>::unpack(hi[i]);
+            const float2 d = f2_unpack(f2_sub(pp, f2_pack(h2.x, h2.y)));
+            lo[i] = MmaOp<T>::pack(d.x, d.y);
+        }
     }
     const float2 ls = f2_unpack(f2_add(l2[0], l2[1]));
     l += ls.x + ls.y;
     tc05::st_16cols(taddr, hi);
-}
-
-// 16-byte chunk i of a 128 x 128 V tile (two 64-column halves of 128 rows x 128 bytes, 128-byte
-// swizzled): row i / 16, half (i / 8) % 2, chunk i % 8 of that half-row.  The swizzle only permutes
-// chunks within a row, so row-wise work needs no knowledge of it.
-__device__ __forceinline__ uint32_t t5_vchunk(uint32_t tile, int i) {
-    return tile + (uint32_t)((i >> 3) & 1) * (uint32_t)kT5Half + (uint32_t)(i >> 4) * 128u + 16u * (uint32_t)(i & 7);
-}
-
-// One warp turns a bf16 V tile into f16 in place: rows [0, z0) become v 2^-E, rows [z0, 128) (past
-// the unit's last key: any bits) become 0.  E is the unit's V exponent: the first tile sets it to
-// what the tile needs, a later tile raises it by up to 15 when it holds larger values, and the
-// return value is that raise, which the tile's first P V instruction applies to the accumulator
-// (scale-input-d: D 2^-raise + P V).  A tile needs E >= e when its largest |v| >= 2^(e + 14), so
-// |v 2^-E| < 2^15 and every element of magnitude >= 2^(E - 14) is exact in f16 (smaller ones round
-// to f16's subnormal spacing 2^(E - 24)).  A raise past 15 would be needed only for a jump by more
-// than 2^15 within one unit: the tile is then converted with the capped E (its largest values
-// become infinite) and PA_ERRBIT_RANGE is set.
-__device__ __forceinline__ int t5_convert_v(uint32_t tile, int z0, bool first, int &E, unsigned int *err) {
-    const int lane = threadIdx.x & 31;
-    const int nvalid = (z0 < 128 ? (z0 > 0 ? z0 : 0) : 128) * 16;   // chunks of the valid rows
-    uint32_t mx = 0;                                                // |v| bits of pairs (ordered as integers)
-    for (int i = lane; i < nvalid; i += 32) {
-        uint32_t w0, w1, w2, w3;
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                     : "r"(t5_vchunk(tile, i)));
-        asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(w0 & 0x7fff7fffu));
-        asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(w1 & 0x7fff7fffu));
-        asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(w2 & 0x7fff7fffu));
-        asm("max.u16x2 %0, %0, %1;" : "+r"(mx) : "r"(w3 & 0x7fff7fffu));
-    }
-    mx = max(mx & 0xffffu, mx >> 16);
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    // bf16 bits >= 0x4700 is |v| >= 2^15; exponent field f gives |v| < 2^(f - 126)
-    const int need = mx >= 0x4700u ? (int)(mx >> 7) - 141 : 0;
-    int raise = 0;
-    if (first) {
-        E = need;
-    } else if (need > E) {
-        raise = min(need - E, 15);
-        E += raise;
-    }
-    if (need > E && lane == 0) atomicOr(err, (unsigned int)PA_ERRBIT_RANGE);
-    const uint64_t sc = f2_pack(__int_as_float((127 - E) << 23), __int_as_float((127 - E) << 23));  // 2^-E
-    auto conv = [&](uint32_t w) {  // a bf16 pair -> the f16 pair of its values times 2^-E
-        const float2 v = f2_unpack(f2_mul(f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)), sc));
-        return MmaOp<__half>::pack(v.x, v.y);
-    };
-    for (int i = lane; i < 2048; i += 32) {
-        const uint32_t a = t5_vchunk(tile, i);
-        uint32_t o0 = 0, o1 = 0, o2 = 0, o3 = 0;
-        if (i < nvalid) {
-            uint32_t w0, w1, w2, w3;
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                         : "r"(a));
-            o0 = conv(w0);
-            o1 = conv(w1);
-            o2 = conv(w2);
-            o3 = conv(w3);
-        }
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(o0), "r"(o1), "r"(o2), "r"(o3)
-                     : "memory");
-    }
-    return raise;
+    if (t5_split_p<T>()) tc05::st_16cols(taddr + 16u, lo);
 }
 
 // Everything a role needs to know about one work unit; every role derives it the same way.
@@ -347,8 +286,6 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     __shared__ float s_xmax[2][2][128];   // [tile parity][column half][row]: partial row maxima
     __shared__ float s_lsum[2][2][128];   // [O buffer][column half][row]: a unit's partial row sums
     __shared__ float s_lmax[2][128];      // [O buffer][row]: a unit's running row maximum (log2 domain)
-    __shared__ int s_vraise[2];           // [V ring slot]: the tile's accumulator scale (bf16 V, t5_convert_v)
-    __shared__ int s_vexp[2];             // [O buffer]: the unit's V exponent E (bf16 V: O holds sum p v 2^-E)
     __shared__ int32_t s_seqlen[kT5StageLens], s_qoff[kT5StageLens];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -390,7 +327,6 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_init(bar(B_VZ + i), 32);
             mbar_init(bar(B_LF + i), 256);
             mbar_init(bar(B_LE + i), 128);
-            mbar_init(bar(B_XF + i), 32);
         }
         mbar_init(bar(B_OD), 1);
         fence_barrier_init();
@@ -532,18 +468,14 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     tc05::fence_after_sync();
                     const uint32_t pcol = tmem + (slot ? 128u : 0u);
                     const uint32_t ocol = tmem + kColO + 128u * (uint32_t)ob;
-                    // a bf16 V tile that raised the unit's V exponent scales the accumulator first
-                    const int raise = (t5_convert_v<T>() && !first) ? s_vraise[slot] : 0;
     #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t vd =
                             tc05::smem_desc_sw128(sV(slot) + (uint32_t)kk * 2048u, (uint32_t)kT5Half, 1024);
-                        // keys 16kk..16kk+15: the f16 weights of chunk kk/2 of 32 keys, columns +0 / +8
+                        // keys 16kk..16kk+15: chunk kk/2 of 32 keys; highs at +0, remainders at +16
                         const uint32_t pa = pcol + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
-                        if (kk == 0 && raise > 0)
-                            tc05::mma_ts_scaled(ocol, pa, vd, idesc_pv, raise);
-                        else
-                            tc05::mma_ts(ocol, pa, vd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                        tc05::mma_ts(ocol, pa, vd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                        if (t5_split_p<T>()) tc05::mma_ts(ocol, pa + 16u, vd, idesc_pv, 1u);
                     }
                     tc05::commit(bar(B_VE + slot));
                     tc05::commit(bar(B_OD));
@@ -587,17 +519,13 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             // ================================================================ V gate
             // Keys at or past the unit's k_hi (past the sequence, past the split, past every row's causal
             // reach, or never loaded) sit in the V rows of the unit's last tile with any bits: their
-            // weight is 0, but 0 * NaN is NaN, so those rows are cleared before P V reads the slot.  A
-            // bf16 tile is turned into f16 here as well (t5_convert_v), with its accumulator scale for
-            // the MMA thread, and at a unit's end its V exponent goes to the epilogue.  Every tile passes
-            // through here (the P V product waits on VZ, not VF), so the phases stay in step with the
-            // ring.
+            // weight is 0, but 0 * NaN is NaN, so those rows are cleared before P V reads the slot.
+            // Every tile passes through here (the P V product waits on VZ, not VF), so the phases
+            // stay in step with the ring.
             bool bad = false;
-            int g0 = 0, n = 0;
+            int g0 = 0;
             for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < nb; t5_advance(p, pos, step)) {
                 const T5Unit U = t5_unit<VARLEN>(p, ln, pos, tpt, ps_shift, g_shift);
-                if (U.n_tiles == 0) continue;
-                int E = 0;
                 for (int t = 0; t < U.n_tiles; ++t) {
                     const int g = g0 + t, st = g & 1;
                     if (!bad) {
@@ -605,35 +533,18 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                         bad = __any_sync(0xffffffffu, !ok);
                     }
                     const int z0 = U.k_hi - (U.k_lo + t * 128);  // first row to clear (< 128 on the last tile only)
-                    if (!bad) {
-                        if constexpr (t5_convert_v<T>()) {
-                            const int raise = t5_convert_v(sV(st), z0, t == 0, E, p.err);
-                            if (lane == 0) s_vraise[st] = raise;
-                            fence_proxy_async_smem();
-                        } else if (z0 < 128) {
-                            // (128 - z0) rows x 2 halves x 8 16-byte chunks; a quarter warp covers one 128-byte row half
-                            for (int i = lane + z0 * 16; i < 2048; i += 32)
-                                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(t5_vchunk(sV(st), i)),
-                                             "r"(0u)
-                                             : "memory");
-                            fence_proxy_async_smem();
+                    if (!bad && z0 < 128) {
+                        // (128 - z0) rows x 2 halves x 8 16-byte chunks; a quarter warp covers one 128-byte row half
+                        for (int i = lane; i < (128 - z0) * 16; i += 32) {
+                            const uint32_t a = sV(st) + (uint32_t)((i >> 3) & 1) * kT5Half +
+                                               (uint32_t)(z0 + (i >> 4)) * 128u + 16u * (uint32_t)(i & 7);
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
                         }
+                        fence_proxy_async_smem();
                     }
-                    __syncwarp();
                     mbar_arrive(bar(B_VZ + st));
                 }
-                if constexpr (t5_convert_v<T>()) {
-                    const int ob = n & 1;
-                    if (!bad && n >= 2) {  // the epilogue has read unit n-2's exponent out of this slot
-                        const bool ok = mbar_wait(bar(B_LE + ob), ((n >> 1) - 1) & 1, p.err);
-                        bad = __any_sync(0xffffffffu, !ok);
-                    }
-                    if (lane == 0) s_vexp[ob] = E;
-                    __syncwarp();
-                    mbar_arrive(bar(B_XF + ob));
-                }
                 g0 += U.n_tiles;
-                ++n;
             }
         }
     } else if (wg == 1 || wg == 2) {
@@ -725,14 +636,14 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     }
                 }
                 if (!bad) {
-                    // pass 2: P = exp2(scale_log2 * s - m) for 32 keys at a time, stored as f16 pairs over
-                    // the first 16 of the same 32 columns
+                    // pass 2: P = exp2(scale_log2 * s - m) for 32 keys at a time, stored over the same 32
+                    // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs)
                     const float nmu = (m_used == kNegInf) ? 0.f : -m_used;  // -inf - (-inf) guard
                     const float c2 = p.scale_log2;
                     // one copy of the chunk's code, run twice (the second 32 scores moved into ua)
 #pragma unroll 1
                     for (int c = 0; c < 2; ++c) {
-                        t5_exp_chunk(ua, c2, nmu, l, sbuf + 64u * hh + 32u * (uint32_t)c);
+                        t5_exp_chunk<T>(ua, c2, nmu, l, sbuf + 64u * hh + 32u * (uint32_t)c);
                         if (c == 0) {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) ua[j] = ub[j];
@@ -835,16 +746,14 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             if (!bad) {
                 bool ok = mbar_wait(bar(B_LF + ob), (n >> 1) & 1, p.err);
                 ok = ok && mbar_wait(bar(B_OF + ob), (n >> 1) & 1, p.err);
-                if constexpr (t5_convert_v<T>()) ok = ok && mbar_wait(bar(B_XF + ob), (n >> 1) & 1, p.err);
                 bad = __any_sync(0xffffffffu, !ok);
             }
             const float l_tot = s_lsum[ob][0][r] + s_lsum[ob][1][r];
             const float m = s_lmax[ob][r];
-            const int vexp = t5_convert_v<T>() ? s_vexp[ob] : 0;  // O holds sum p v 2^-vexp
             mbar_arrive(bar(B_LE + ob));
             if (!bad) {
                 tc05::fence_after_sync();
-                const float inv = l_tot > 0.f ? __int_as_float((127 + vexp) << 23) / l_tot : 0.f;
+                const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
                 const uint32_t ocol = tmem + lane_addr + kColO + 128u * (uint32_t)ob;
 #pragma unroll 1
                 for (int ch = 0; ch < nch; ++ch) {
@@ -956,7 +865,7 @@ static cudaError_t launch_tc05_t(const FwdParams &p, long long total_q, const CU
     const int grid = (int)(units < sms ? units : sms);
     const bool bf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t iqk = tc05::idesc_f16(bf, false, 128, 128);
-    const uint32_t ipv = tc05::idesc_f16(false, true, 128, 128);  // P and V in f16 (a bf16 V tile is converted)
+    const uint32_t ipv = tc05::idesc_f16(bf, true, 128, 128);
     kern<<<grid, kT5Threads, smem, stream>>>(tmq, tmk, tmv, tmo, q, tpt, ps_shift, g_shift, iqk, ipv, (int)nb);
     return cudaGetLastError();
 }

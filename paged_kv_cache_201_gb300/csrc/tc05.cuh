@@ -66,36 +66,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
-// D[tmem] = A[tmem] * B[smem desc] + D * 2^-sd for sd in 1..15 (the instruction's scale-input-d, an
-// immediate): the accumulator is scaled down by a power of two before the product is added.
-template <int SD>
-__device__ __forceinline__ void mma_ts_sd(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
-    static_assert(SD >= 1 && SD <= 15, "scale-input-d is 0..15");
-    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1, %4;" ::"r"(d_tmem), "r"(a_tmem),
-                 "l"(b_desc), "r"(idesc), "n"(SD)
-                 : "memory");
-}
-__device__ __forceinline__ void mma_ts_scaled(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                              int sd) {
-    switch (sd) {
-        case 1: mma_ts_sd<1>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 2: mma_ts_sd<2>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 3: mma_ts_sd<3>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 4: mma_ts_sd<4>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 5: mma_ts_sd<5>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 6: mma_ts_sd<6>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 7: mma_ts_sd<7>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 8: mma_ts_sd<8>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 9: mma_ts_sd<9>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 10: mma_ts_sd<10>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 11: mma_ts_sd<11>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 12: mma_ts_sd<12>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 13: mma_ts_sd<13>(d_tmem, a_tmem, b_desc, idesc); break;
-        case 14: mma_ts_sd<14>(d_tmem, a_tmem, b_desc, idesc); break;
-        default: mma_ts_sd<15>(d_tmem, a_tmem, b_desc, idesc); break;
-    }
-}
-
 // ---------------------------------------------------------------- TMEM <-> registers
 // Each thread of a warp reads 32 consecutive 32-bit columns of its own lane.
 __device__ __forceinline__ void ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {

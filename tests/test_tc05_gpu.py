@@ -108,70 +108,16 @@ def test_tc05_many_units_per_cta(pa):
     assert pa.paged_attn_last_error_word() == 0
 
 
-@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("scale_mult", [1.0, 8.0])
-def test_tc05_f16_single_product(pa, scale_mult, dtype):
-    """P V is one product with P rounded to f16 (bf16 V tiles turned into f16 first): causal prefill
-    rows including peaky softmaxes (scores scaled up 8x, so a few keys carry the weight), every row
-    against the oracle."""
+def test_tc05_f16_single_product(pa, scale_mult):
+    """f16 runs P V as one product with P rounded to f16: causal prefill rows including peaky
+    softmaxes (scores scaled up 8x, so a few keys carry the weight), every row against the oracle."""
     lens = [70, 333, 1000]
-    wl = W.make_custom(dtype=dtype, B=3, Sq=64, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=lens, causal=True,
+    wl = W.make_custom(dtype="f16", B=3, Sq=64, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=lens, causal=True,
                        seed=880, scale=scale_mult / np.sqrt(128))
     for S in (1, 3):
         res = _gpu.run(_gpu.DeviceWorkload(wl), S, variant=4)
         rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)
         ref = oracle.workload_rows(wl, split_kv=S, row_bih=rows)
-        _gpu.compare_rows(res, ref, rows, wl, S, f"{dtype} tc05 x{scale_mult} S={S}")
+        _gpu.compare_rows(res, ref, rows, wl, S, f"f16 tc05 x{scale_mult} S={S}")
     assert pa.paged_attn_last_error_word() == 0
-
-
-def _scale_v_tokens(wl, b, lo, hi, k):
-    """Multiply sequence b's V rows of logical tokens [lo, hi) by 2^k in the bf16 pool (exact: a power
-    of two), every kv head."""
-    v = W.Workload(**wl.__dict__).v_cache.copy()
-    f = (v.astype(np.uint32) << 16).view(np.float32)
-    for j in range(lo, hi):
-        page = wl.block_table[b, j // wl.page_size]
-        f[page, j % wl.page_size] *= np.float32(2.0 ** k)
-    bits = W.bf16_bits_rne(f)
-    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32), f)
-    return bits
-
-
-def test_tc05_bf16_large_v_scaled(pa):
-    """bf16 V tiles beyond f16's range take a power-of-two exponent per unit: sequence 0's first key
-    tile holds values near 2^20 (the unit's exponent starts there, later tiles are scaled down with
-    it); sequence 1's third tile holds values near 2^28 (a raise of the running exponent by 14,
-    applied to the accumulator by the tile's first P V instruction).  Every row against the oracle,
-    at split 1 and 2, and no range bit."""
-    lens = [600, 700]
-    wl = W.make_custom(dtype="bf16", B=2, Sq=64, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=lens, causal=True,
-                       seed=881)
-    v = _scale_v_tokens(wl, 0, 0, 128, 20)
-    wl = W.Workload(**{**wl.__dict__, "v_cache": v})
-    v = _scale_v_tokens(wl, 1, 256, 384, 26)
-    wl = W.Workload(**{**wl.__dict__, "v_cache": v})
-    for S in (1, 2):
-        res = _gpu.run(_gpu.DeviceWorkload(wl), S, TC05)
-        rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)
-        ref = oracle.workload_rows(wl, split_kv=S, row_bih=rows)
-        _gpu.compare_rows(res, ref, rows, wl, S, f"bf16 large V S={S}")
-    assert pa.paged_attn_last_error_status() == (pa.PA_OK, 0)
-
-
-def test_tc05_bf16_v_jump_past_the_range(pa):
-    """A V tile 2^30 times larger than the unit's earlier tiles needs a raise past 15: the kernel sets
-    PA_ERRBIT_RANGE (status PA_ERANGE) instead of returning finite but wrong rows; the other
-    sequence's rows stay exact."""
-    lens = [600, 500]
-    wl = W.make_custom(dtype="bf16", B=2, Sq=64, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=lens, causal=True,
-                       seed=882)
-    v = _scale_v_tokens(wl, 0, 256, 384, 30)
-    bad = W.Workload(**{**wl.__dict__, "v_cache": v})
-    res = _gpu.run(_gpu.DeviceWorkload(bad), 1, TC05)
-    status, bits = pa.paged_attn_last_error_status()
-    assert status == pa.PA_ERANGE and bits & pa.ERRBIT_RANGE
-    rows = oracle.all_rows(1, wl.Sq, wl.Hq)
-    rows[:, 0] = 1
-    ref = oracle.workload_rows(bad, split_kv=1, row_bih=rows)
-    _gpu.assert_close(res["out"][1].reshape(-1, wl.D), ref["out"], "bf16", "other sequence")
