@@ -243,3 +243,45 @@ def test_split_group_decode(pa, S, ps, D, dtype):
                            W=width, causal=Sq > 1, q_offset=qo, seed=140 + S + ps + Sq)
         _full_check(wl, S, pa.VARIANT_MMA_SPLIT_GROUP, f"split group S={S} ps={ps} D={D} Sq={Sq}")
     assert pa.paged_attn_last_error_word() == 0
+
+
+CLIP_CASES = [
+    # (name, variant, workload kwargs)
+    ("gqa decode", 2, dict(dtype="bf16", Sq=1, Hq=8, Hkv=2, D=128, page_size=16)),
+    ("single-head decode", 1, dict(dtype="bf16", Sq=1, Hq=4, Hkv=4, D=128, page_size=32)),
+    ("f32 cuda cores", 1, dict(dtype="f32", Sq=2, Hq=4, Hkv=2, D=64, page_size=16, causal=True)),
+    ("mma prefill", 3, dict(dtype="f16", Sq=20, Hq=8, Hkv=2, D=64, page_size=16, causal=True)),
+    ("tcgen05 prefill", 4, dict(dtype="bf16", Sq=64, Hq=8, Hkv=2, D=128, page_size=16, causal=True)),
+    ("head dim 256", 5, dict(dtype="bf16", Sq=3, Hq=8, Hkv=2, D=256, page_size=16, causal=True)),
+]
+
+
+@pytest.mark.parametrize("name,variant,kw", CLIP_CASES, ids=[c[0] for c in CLIP_CASES])
+@pytest.mark.parametrize("S", [1, 3])
+def test_overlong_sequence_is_clipped(pa, name, variant, kw, S):
+    """seq_lens[b] beyond the block-table row (bt_stride x page_size tokens) is clipped to the row: the
+    result is that of the clipped length (the default query offset follows it), the other sequences
+    are exact, and PA_ERRBIT_SEQ_CLIPPED is set (a status of PA_OK: nothing outside the row is read)."""
+    W_ = 6
+    row = W_ * kw["page_size"]
+    clipped = [row, 70, row]
+    wl = W.make_custom(B=3, seq_lens=clipped, W=W_, seed=6161, **kw)
+    over = W.Workload(**{**wl.__dict__, "seq_lens": np.array([row + 7, 70, row + 300], dtype=np.int32)})
+    assert pa.paged_attn_last_error_word() == 0
+    res = _gpu.run(_gpu.DeviceWorkload(over), S, variant)
+    status, bits = pa.paged_attn_last_error_status()
+    assert bits == pa.ERRBIT_SEQ_CLIPPED and status == pa.PA_OK
+    rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)
+    _gpu.compare_rows(res, oracle.workload_rows(wl, split_kv=S, row_bih=rows), rows, wl, S, f"{name} clipped S={S}")
+
+
+def test_overlong_sequence_is_clipped_fp8(pa):
+    """The same clipping on the 8-bit-pool decode kernel."""
+    W_ = 5
+    wl = W.make_custom_fp8(dtype="bf16", B=3, Sq=1, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=[80, 33, 80], W=W_,
+                           seed=6162)
+    over = W.Workload(**{**wl.__dict__, "seq_lens": np.array([81, 33, 500], dtype=np.int32)})
+    res = _gpu.run(_gpu.DeviceWorkload(over), 2)
+    assert pa.paged_attn_last_error_word() == pa.ERRBIT_SEQ_CLIPPED
+    rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)
+    _gpu.compare_rows(res, oracle.workload_rows_kvq(wl, split_kv=2, row_bih=rows), rows, wl, 2, "fp8 clipped")

@@ -301,3 +301,26 @@ def test_overlap_under_graph_capture(pa):
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
     assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
     assert pa.paged_attn_last_error_word() == 0
+
+
+def test_batch_past_the_tcgen05_sequence_limit(pa):
+    """More sequences than the tcgen05 variable-length kernel stages (1030 > 1024): every sequence,
+    the long ones included, runs on the one-grid kernel, plain and with a hint (which then falls
+    back), and matches the oracle on every row."""
+    import torch
+    rng = np.random.default_rng(7171)
+    B = 1030
+    q_lens = np.where(rng.random(B) < 0.01, 70, rng.integers(0, 3, size=B))
+    seq_lens = q_lens + rng.integers(0, 120, size=B)
+    wl = W.make_varlen(dtype="bf16", Hq=8, Hkv=2, D=128, page_size=16, seed=7172, q_lens=q_lens.tolist(),
+                       seq_lens=seq_lens.tolist())
+    assert (np.diff(wl.q_start) * wl.G >= 64).any()   # sequences the tcgen05 kernel would take below the limit
+    d = _device(wl)
+    ref = oracle.rows_varlen(q=wl.q, k_cache=wl.k_cache, v_cache=wl.v_cache, block_table=wl.block_table,
+                             seq_lens=wl.seq_lens, q_start=wl.q_start, q_offset=wl.q_offset, causal=wl.causal,
+                             dims=oracle.dims_of(wl), scale=wl.scale, split_kv=1, want_split=False)
+    for kind in ("plain", "computed"):
+        res = _run(pa, wl, d, 1, hint=None if kind == "plain" else _hint(pa, wl, "computed"))
+        _gpu.assert_close(res["out"], ref["out"], "bf16", f"B=1030 {kind} out")
+        _gpu.assert_close(res["lse"], ref["lse"], "bf16", f"B=1030 {kind} lse")
+    assert pa.paged_attn_last_error_word() == 0
