@@ -3,10 +3,20 @@
 // For query runs long enough to fill a 128-row tile (prefill, head_dim 128, bf16/f16).
 // A work unit = (sequence b, kv head, split s, tile of 128/G query tokens x the G query heads of
 // the kv head's group), so all 128 rows share every K/V tile.  The kernel is persistent: one CTA
-// per SM walks its units, with four warpgroups:
+// per SM takes units until none is left.  With split_kv = 1 the grid has one CTA per unit, of which
+// one fits an SM; a running CTA takes the next unit by cancelling the launch of a CTA that has not
+// started (cluster launch control), so units go, in CTA order, to whichever SM frees up first, and
+// that order puts the most key tiles first: the sequences by key count, longest first, each from
+// its last row tile down.  Lane 0 of warp 0 takes the units and posts each to an 8-entry
+// shared-memory ring that every other role reads.  Otherwise (split_kv > 1, whose units include
+// long runs of empty ones, and variable-length batches) CTA c takes units c, c + gridDim.x, ...,
+// each role walking them by itself.  Four warpgroups:
 //   warps 0,2   TMA producers (0: Q and K, 2: V): each unit's Q tile (double-buffered), then per 128-key
 //               tile the block-table ids (32 pages per batch, never past the sequence's page count)
-//               and one box per page, half-row and pool into 2-slot K and V rings.
+//               and one box per page, half-row and pool into 2-slot K and V rings.  From the ring they
+//               take the next unit only once every load of the current one is out (a post waits for
+//               the readers of an older entry, which may need those loads); the static walk takes it
+//               one unit ahead.
 //   warp 1      allocates all 512 TMEM columns and issues tcgen05.mma from one thread:
 //               S_g = Q K_g^T into one of two S buffers (128 fp32 columns each), then
 //               O += Ph_{g-1} V_{g-1} + Pl_{g-1} V_{g-1} with P read from TMEM into one of two O
@@ -51,6 +61,10 @@ constexpr uint32_t kT5TmemCols = 512;
 constexpr uint32_t kColO = 256;               // O buffers at columns 256 and 384
 constexpr float kRescaleLog2 = 8.f;           // rescale O only when the max grows by > 2^8
 constexpr int kT5StageLens = 1024;            // batches up to this size keep seq_lens / q_offset in smem
+constexpr int kT5SortMax = 256;               // batches up to this size are ordered by key count
+constexpr int kT5Ring = 8;                    // entries of the unit ring (a power of two)
+// ring readers' arrivals per entry: lane 0 of warps 2 and 3, the MMA thread, 8 softmax and 4 epilogue warps
+constexpr uint32_t kT5RingReaders = 15;
 
 // barrier slots (pairs are indexed by buffer / ring slot)
 //   QF/QE  Q buffer full (TMA) / empty (after the unit's last Q K^T)
@@ -64,10 +78,49 @@ constexpr int kT5StageLens = 1024;            // batches up to this size keep se
 //   OFREE  O buffer read out by the epilogue threads (128 arrive)
 //   LF/LE  a unit's row maxima and sums handed to the epilogue (256 softmax threads arrive) / read
 //          by it (128 epilogue threads arrive); indexed like the O buffers
+//   RF/RE  unit ring entry written (warp 0) / read by every reader (kT5RingReaders arrive)
+//   CLC    the response to a launch-cancel request has landed (16 bytes)
 enum {
     B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_PF = 14, B_OF = 16, B_OFREE = 18,
-    B_OD = 20, B_VZ = 21, B_LF = 23, B_LE = 25, B_COUNT = 27
+    B_OD = 20, B_VZ = 21, B_LF = 23, B_LE = 25, B_RF = 27, B_RE = B_RF + kT5Ring, B_CLC = B_RE + kT5Ring,
+    B_COUNT = B_CLC + 1
 };
+
+// Cluster launch control (sm_100 family): ask to cancel the launch of a CTA that has not started;
+// the 16-byte response lands at `resp` and completes 16 bytes of transactions on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                     resp),
+                 "r"(bar)
+                 : "memory");
+}
+// Whether the request whose response is at `resp` cancelled a CTA, and if so its blockIdx.x.
+__device__ __forceinline__ bool clc_query(uint32_t resp, int &cta) {
+    uint32_t ok, x = 0;
+    asm volatile(
+        "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 h, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+        : "=r"(ok), "+r"(x)
+        : "r"(resp)
+        : "memory");
+    cta = (int)x;
+    return ok != 0;
+}
+
+// Named barrier over `count` threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
 
 // Output row of query token tok (of the sequence whose first packed token is q0) and head kvh G + g.
 __device__ __forceinline__ long long t5_row_index(const FwdParams &p, int q0, int kvh, int tok, int g) {
@@ -170,10 +223,12 @@ __device__ __forceinline__ int t5_key_limit(const FwdParams &p, const T5Lens &ln
     return (int)(reach < L ? reach : L);
 }
 
-// A unit's place in the order unit = ((b * split_kv + s) * Hkv + kvh) * row_tiles + rt.  Every role
-// walks its CTA's units c, c + gridDim.x, ... by adding gridDim.x's own digits with one carry per
-// digit (no division per unit: the per-unit code stays small, so it does not push the softmax's
-// loop out of the instruction cache).
+// A unit's digits: sequence b (in a variable-length batch, block b of the packed rows), split s,
+// kv head kvh, row tile rt.  The static walk's unit order is
+// unit = ((b * split_kv + s) * Hkv + kvh) * row_tiles + rt, and every role walks its CTA's units c,
+// c + gridDim.x, ... by adding gridDim.x's own digits with one carry per digit (no division per
+// unit: the per-unit code stays small, so it does not push the softmax's loop out of the
+// instruction cache).
 struct T5Pos {
     int rt, kvh, s, b;
 };
@@ -203,10 +258,28 @@ __device__ __forceinline__ void t5_advance(const FwdParams &p, T5Pos &u, const T
     u.b += d.b + c;
 }
 
+// The cancelled-CTA schedule (split_kv = 1): the unit of CTA r.  Sequences by key count, longest
+// first (perm; null: the last sequence first), each from its last row tile down, so the units with
+// the most key tiles start first and the short ones fill in at the end.
+__device__ __forceinline__ T5Pos t5_dyn_pos(const FwdParams &p, int r, const int16_t *perm) {
+    T5Pos u;
+    const int ri = r % p.row_tiles;
+    r /= p.row_tiles;
+    u.kvh = r % p.Hkv;
+    const int bi = r / p.Hkv;
+    u.rt = p.row_tiles - 1 - ri;
+    u.s = 0;
+    u.b = perm ? (int)perm[bi] : p.B - 1 - bi;
+    return u;
+}
+
 // Variable-length batches (at most kT5StageLens sequences): q_start staged in shared memory by
 // the CTA (a fixed address, so reading it costs the softmax warps no pointer register).
 __shared__ int32_t t5_qstart[kT5StageLens + 1];
 static_assert(kTc05VarlenMaxBatch <= kT5StageLens, "the host's variable-length batch limit must fit the stage");
+// The sequences by key count, longest first (batches of at most kT5SortMax sequences).
+__shared__ int16_t t5_perm[kT5SortMax];
+static_assert(kT5SortMax <= kT5StageLens, "the order is taken over staged sequence lengths");
 
 // The packed rows are cut into blocks, sequence b's first being floor(q_start[b] G / 128) + b
 // (strictly increasing, and at least as many blocks as the sequence has 128-row tiles before the
@@ -267,21 +340,26 @@ __device__ __forceinline__ T5Unit t5_unit(const FwdParams &p, const T5Lens &ln, 
     return U;
 }
 
-// Persistent: CTA c processes units c, c + gridDim.x, ...  Barrier phases and the K / V rings run
+// Persistent: a CTA takes units until none is left (the schedule at the top of the file; DYN: by
+// cancelling CTAs, the grid then holding one CTA per unit).  Barrier phases and the K / V rings run
 // on the CTA's global tile counter g; Q and O are double-buffered by the CTA's count of non-empty
 // units n, so a unit's read-out and the next unit's loads overlap its neighbours' work.  PART: the
 // output is split_kv > 1's fp32 partials (else the final rows in T); one store path per kernel keeps
 // the code the SM must hold small.  G = 2^g_shift (it divides 128).  VARLEN: a variable-length
 // batch (q_start), whose sequences of at least 64 query rows this kernel takes; the unit order's
-// b digit is then the block of the packed rows (nb of them), and row_tiles is 1.
+// b digit is then the block of the packed rows (nb of them), and row_tiles is 1.  units: the unit
+// count, nb * split_kv * Hkv * row_tiles.
 template <typename T, bool PART, bool VARLEN>
 __global__ void __launch_bounds__(kT5Threads, 1)
     paged_attn_tc05_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                            const FwdParams p, int tpt, int ps_shift, int g_shift, uint32_t idesc_qk,
-                           uint32_t idesc_pv, int nb) {
+                           uint32_t idesc_pv, int nb, int units) {
+    constexpr bool DYN = !PART && !VARLEN;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[B_COUNT];
+    __shared__ int4 s_ring[kT5Ring];      // the unit ring: {rt, kvh, s, b}, b = -1 after the last unit
+    __shared__ __align__(16) uint4 s_clc;  // the launch-cancel response
     __shared__ uint32_t s_tmem;
     __shared__ float s_xmax[2][2][128];   // [tile parity][column half][row]: partial row maxima
     __shared__ float s_lsum[2][2][128];   // [O buffer][column half][row]: a unit's partial row sums
@@ -328,7 +406,12 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_init(bar(B_LF + i), 256);
             mbar_init(bar(B_LE + i), 128);
         }
+        for (int i = 0; i < kT5Ring; ++i) {
+            mbar_init(bar(B_RF + i), 1);
+            mbar_init(bar(B_RE + i), kT5RingReaders);
+        }
         mbar_init(bar(B_OD), 1);
+        mbar_init(bar(B_CLC), 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -340,7 +423,56 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     tc05::fence_after_sync();
     const uint32_t tmem = s_tmem;
     const int wg = warp >> 2;
-    const T5Pos step = t5_pos(p, gridDim.x);  // gridDim.x <= the unit count, so b < nb here
+
+    // DYN: the sequences by key count (the clipped length), longest first, ties by index.
+    const int16_t *perm = nullptr;
+    if constexpr (DYN) {
+        if (p.B <= kT5SortMax) {  // seq_lens staged
+            const int cap = p.W * ps;
+            for (int b = threadIdx.x; b < p.B; b += kT5Threads) {
+                const int lb = min(max(ln.seq_lens[b], 0), cap);
+                int rank = 0;
+                for (int c = 0; c < p.B; ++c) {
+                    const int lc = min(max(ln.seq_lens[c], 0), cap);
+                    rank += (lc > lb) || (lc == lb && c < b);
+                }
+                t5_perm[rank] = (int16_t)b;
+            }
+            __syncthreads();
+            perm = t5_perm;
+        }
+    }
+
+    // Ring entry k (the CTA's k-th unit): 1 a unit (in q), 0 the end, -1 a time-out.  whole_warp:
+    // every lane of the calling warp reads it (and agrees on a time-out); else one thread.
+    auto ring_read = [&](int k, T5Pos &q, bool whole_warp) -> int {
+        const int slot = k & (kT5Ring - 1);
+        bool ok = mbar_wait(bar(B_RF + slot), (uint32_t)(k / kT5Ring) & 1u, p.err);
+        if (whole_warp) ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return -1;
+        const int4 e = s_ring[slot];
+        if (whole_warp) __syncwarp();
+        if (!whole_warp || lane == 0) mbar_arrive(bar(B_RE + slot));
+        q = T5Pos{e.x, e.y, e.z, e.w};
+        return e.w >= 0 ? 1 : 0;
+    };
+    // Static walk: gridDim.x's digits (gridDim.x <= the unit count, so b < nb here); each role's
+    // cursor starts at the CTA's first unit.
+    T5Pos step{};
+    if constexpr (!DYN) step = t5_pos(p, gridDim.x);
+    auto start = [&]() { return DYN ? T5Pos{} : t5_pos(p, blockIdx.x); };
+    // A role's next unit: 1 a unit (in q), 0 none left, -1 a time-out.  DYN: ring entry k (whole_warp
+    // as for ring_read); else the static walk from cursor c.
+    auto walk = [&](int &k, T5Pos &c, T5Pos &q, bool whole_warp) -> int {
+        if constexpr (DYN) {
+            return ring_read(k++, q, whole_warp);
+        } else {
+            if (c.b >= nb) return 0;
+            q = c;
+            t5_advance(p, c, step);
+            return 1;
+        }
+    };
 
     if (wg == 0) {
         tc05::setmaxnreg_dec<kRegLoad>();
@@ -361,8 +493,45 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             const uint32_t box = (uint32_t)ps * 128u;            // bytes of one page half-row box
             bool bad = false;
             int n = 0, g0 = 0;                                   // non-empty units so far, global tile base
-            // The first id batch of the next non-empty unit is loaded one unit ahead, so its latency
-            // hides behind the current unit's copies.
+            // the first block-table batch of a unit
+            auto first_ids = [&](const T5Unit &V) {
+                const int pe = (V.k_hi + ps - 1) >> ps_shift;
+                return (V.pg0 + lane < pe) ? __ldg(p.block_table + (long long)V.b * p.W + V.pg0 + lane) : 0;
+            };
+            // ---- DYN: warp 0 takes units (its own CTA's, then cancelled CTAs') and posts each, or the
+            // end, to the ring; warp 2 reads them from it.  Both take the next unit only once every load
+            // of the current one is out: a post waits for the ring's readers, and a reader of an older
+            // entry may need those loads.
+            int kr = 0;                                          // ring entries written (warp 0) / read (warp 2)
+            bool own = true, clc_pending = false;                // warp 0, lane 0
+            uint32_t clc_parity = 0;
+            auto clc_request = [&]() {
+                fence_proxy_async_smem();  // the previous response has been read (generic) before the async write
+                mbar_arrive_expect_tx(bar(B_CLC), 16u);
+                clc_try_cancel(smem_u32(&s_clc), bar(B_CLC));
+                clc_pending = true;
+            };
+            // lane 0 of warp 0: the next CTA whose unit this CTA takes; -1: none left; -2: a time-out
+            auto next_cta = [&]() -> int {
+                if (own) {  // the CTA's own unit; ask for the next one at once
+                    own = false;
+                    clc_request();
+                    return (int)blockIdx.x;
+                }
+                if (!clc_pending) return -1;
+                if (!mbar_wait(bar(B_CLC), clc_parity, p.err)) return -2;
+                clc_parity ^= 1u;
+                clc_pending = false;
+                int r;
+                if (!clc_query(smem_u32(&s_clc), r)) return -1;  // no CTA left to cancel: no request after this
+                clc_request();
+                return r;
+            };
+            // ---- static: the walk of units c, c + gridDim.x, ..., the next unit with key tiles and its
+            // first block-table batch taken one unit ahead
+            T5Pos spos{};
+            T5Unit sU{};
+            int s_ids = 0;
             // the first unit with key tiles at or after position q (q.b >= nb: none), into V
             auto next_unit = [&](T5Pos q, T5Unit &V) {
                 for (; q.b < nb; t5_advance(p, q, step)) {
@@ -371,21 +540,63 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 }
                 return q;
             };
-            auto first_ids = [&](const T5Pos &q, const T5Unit &V) {
-                if (q.b >= nb) return 0;
-                const int pe = (V.k_hi + ps - 1) >> ps_shift;
-                return (V.pg0 + lane < pe) ? __ldg(p.block_table + (long long)V.b * p.W + V.pg0 + lane) : 0;
+            if constexpr (!DYN) {
+                spos = next_unit(t5_pos(p, blockIdx.x), sU);
+                s_ids = spos.b < nb ? first_ids(sU) : 0;
+            }
+            // the CTA's next unit with key tiles and its first ids (false: none left, or a wait gave up)
+            auto next_work = [&](T5Unit &V, int &ids) -> bool {
+                if (bad) return false;
+                if constexpr (DYN) {
+                    for (;;) {
+                        T5Pos q{0, 0, 0, -1};
+                        if (kq) {
+                            int r = 0;
+                            if (lane == 0) r = next_cta();
+                            r = __shfl_sync(0xffffffffu, r, 0);
+                            if (r == -2) {
+                                bad = true;
+                                return false;
+                            }
+                            if (r >= 0) q = t5_dyn_pos(p, r, perm);
+                            const int slot = kr & (kT5Ring - 1);
+                            if (kr >= kT5Ring) {  // every reader is done with entry kr - kT5Ring
+                                const bool ok =
+                                    mbar_wait(bar(B_RE + slot), (uint32_t)(kr / kT5Ring - 1) & 1u, p.err);
+                                bad = __any_sync(0xffffffffu, !ok);
+                                if (bad) return false;
+                            }
+                            if (lane == 0) {
+                                s_ring[slot] = make_int4(q.rt, q.kvh, q.s, q.b);
+                                mbar_arrive(bar(B_RF + slot));  // release: the entry is visible to its readers
+                            }
+                            ++kr;
+                        } else {
+                            const int got = ring_read(kr++, q, true);
+                            if (got < 0) bad = true;
+                            if (got != 1) return false;
+                        }
+                        if (q.b < 0) return false;
+                        V = t5_unit<VARLEN>(p, ln, q, tpt, ps_shift, g_shift);
+                        if (V.n_tiles > 0) {
+                            ids = first_ids(V);
+                            return true;
+                        }
+                    }
+                } else {
+                    if (spos.b >= nb) return false;
+                    V = sU;
+                    ids = s_ids;
+                    t5_advance(p, spos, step);
+                    spos = next_unit(spos, sU);
+                    s_ids = spos.b < nb ? first_ids(sU) : 0;
+                    return true;
+                }
             };
-            T5Unit Un{};
-            T5Pos pos = next_unit(t5_pos(p, blockIdx.x), Un);
-            int ids_pref = first_ids(pos, Un);
-            while (pos.b < nb && !bad) {
-                const T5Unit U = Un;
-                T5Pos nxt = pos;
-                t5_advance(p, nxt, step);
-                nxt = next_unit(nxt, Un);
-                const int ids_now = ids_pref;
-                ids_pref = first_ids(nxt, Un);
+            T5Unit U{};
+            int ids_now = 0;
+            bool have = next_work(U, ids_now);
+            while (have && !bad) {
                 const int qb = n & 1;
                 if (kq && n >= 2) {  // Q buffer free once every Q K^T of unit n-2 is done
                     const bool ok = mbar_wait(bar(B_QE + qb), ((n >> 1) - 1) & 1, p.err);
@@ -442,7 +653,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 }
                 g0 += U.n_tiles;
                 ++n;
-                pos = nxt;
+                have = next_work(U, ids_now);  // every load of this unit is out
             }
             // No copy may outlive the CTA: wait (bounded) for the last phase armed on every slot.  After a
             // time-out some of these were never armed; their waits then give up too.
@@ -452,6 +663,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 if (kq)
                     for (int k = max(0, n - 2); k < n; ++k) mbar_wait(bar(B_QF + (k & 1)), (k >> 1) & 1, p.err);
             }
+            // nor a launch-cancel response (one is outstanding only after a time-out)
+            if (DYN && kq && lane == 0 && clc_pending) mbar_wait(bar(B_CLC), clc_parity, p.err);
         } else if (warp == 1) {
             // ================================================================ MMA issuer
             if (lane == 0) {
@@ -482,8 +695,15 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     if (last) tc05::commit(bar(B_OF + ob));
                     return true;
                 };
-                int n = 0, g0 = 0;
-                for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < nb && !bad; t5_advance(p, pos, step)) {
+                int n = 0, g0 = 0, kr = 0;
+                T5Pos cur = start();
+                while (!bad) {
+                    T5Pos pos;
+                    const int got = walk(kr, cur, pos, false);
+                    if (got != 1) {
+                        bad = got < 0;
+                        break;
+                    }
                     const T5Unit U = t5_unit<VARLEN>(p, ln, pos, tpt, ps_shift, g_shift);
                     if (U.n_tiles == 0) continue;
                     const int qb = n & 1;
@@ -523,8 +743,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             // Every tile passes through here (the P V product waits on VZ, not VF), so the phases
             // stay in step with the ring.
             bool bad = false;
-            int g0 = 0;
-            for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < nb; t5_advance(p, pos, step)) {
+            int g0 = 0, kr = 0;
+            T5Pos cur = start(), pos;
+            while (walk(kr, cur, pos, true) == 1) {
                 const T5Unit U = t5_unit<VARLEN>(p, ln, pos, tpt, ps_shift, g_shift);
                 for (int t = 0; t < U.n_tiles; ++t) {
                     const int g = g0 + t, st = g & 1;
@@ -553,15 +774,19 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         // Two warpgroups share every row: group hh (warps 4-7: hh = 0, warps 8-11: hh = 1) owns
         // score columns / keys [64 hh, 64 hh + 64).  They exchange the row maximum once per tile;
         // both keep the same running maximum, so the rescale decisions agree.  Every named barrier
-        // is reached on every path (a warp that gave up on a wait still walks the loops), so none
-        // can hang.
+        // is reached on every path (a warp that gave up on a wait still walks the loops, and the eight
+        // warps agree on each unit before they walk it), so none can hang.
         const int hh = wg - 1;
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;                       // TMEM lane = query row of the tile
         const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
         bool bad = false;
-        int n = 0, g0 = 0;
-        for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < nb; t5_advance(p, pos, step)) {
+        int n = 0, g0 = 0, kr = 0;
+        T5Pos cur = start();
+        for (;;) {
+            T5Pos pos;
+            const int got = walk(kr, cur, pos, true);
+            if (DYN ? !named_bar_and(3, 256, got == 1) : got != 1) break;
             const T5Unit U = t5_unit<VARLEN>(p, ln, pos, tpt, ps_shift, g_shift);
             if (U.n_tiles == 0) continue;  // the epilogue warps write its rows
             const int tk = U.tok0 + (r >> g_shift);
@@ -716,8 +941,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             }
         };
         bool bad = false;
-        int n = 0;
-        for (T5Pos pos = t5_pos(p, blockIdx.x); pos.b < nb; t5_advance(p, pos, step)) {
+        int n = 0, kr = 0;
+        T5Pos cur = start(), pos;
+        while (walk(kr, cur, pos, true) == 1) {
             const T5Unit U = t5_unit<VARLEN>(p, ln, pos, tpt, ps_shift, g_shift);
             if (U.skip) continue;  // another kernel's unit (variable-length batches)
             if (threadIdx.x == 384 && U.s == 0 && U.tok0 == 0 && p.seq_lens[U.b] > p.W * ps)
@@ -818,9 +1044,10 @@ static int num_sms_of_current_device() {
     return v;
 }
 
-// One persistent CTA per SM; max_ctas > 0 caps the grid when the kernel shares the GPU with another
-// kernel running at the same time.  Any grid up to the unit count computes the same results, since
-// a unit's work does not depend on the CTA that takes it.
+// split_kv = 1: one CTA per unit, of which one runs per SM and takes the rest by cancelling their
+// launches.  Otherwise one persistent CTA per SM; max_ctas > 0 caps the grid when the kernel shares
+// the GPU with another kernel running at the same time.  Any grid up to the unit count computes the
+// same results, since a unit's work does not depend on the CTA that takes it.
 template <typename T, bool PART, bool VARLEN>
 static cudaError_t launch_tc05_t(const FwdParams &p, long long total_q, const CUtensorMap &tmq,
                                  const CUtensorMap &tmk, const CUtensorMap &tmv, const CUtensorMap &tmo,
@@ -862,11 +1089,13 @@ static cudaError_t launch_tc05_t(const FwdParams &p, long long total_q, const CU
     int sms = num_sms_of_current_device();
     if (sms <= 0) return cudaErrorInvalidDevice;
     if (max_ctas > 0 && max_ctas < sms) sms = max_ctas;
-    const int grid = (int)(units < sms ? units : sms);
+    constexpr bool dyn = !PART && !VARLEN;  // the kernel's DYN
+    const int grid = dyn ? (int)units : (int)(units < sms ? units : sms);
     const bool bf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t iqk = tc05::idesc_f16(bf, false, 128, 128);
     const uint32_t ipv = tc05::idesc_f16(bf, true, 128, 128);
-    kern<<<grid, kT5Threads, smem, stream>>>(tmq, tmk, tmv, tmo, q, tpt, ps_shift, g_shift, iqk, ipv, (int)nb);
+    kern<<<grid, kT5Threads, smem, stream>>>(tmq, tmk, tmv, tmo, q, tpt, ps_shift, g_shift, iqk, ipv, (int)nb,
+                                             (int)units);
     return cudaGetLastError();
 }
 

@@ -121,3 +121,38 @@ def test_tc05_f16_single_product(pa, scale_mult):
         ref = oracle.workload_rows(wl, split_kv=S, row_bih=rows)
         _gpu.compare_rows(res, ref, rows, wl, S, f"f16 tc05 x{scale_mult} S={S}")
     assert pa.paged_attn_last_error_word() == 0
+
+
+def test_tc05_split1_schedule_orders(pa):
+    """split_kv = 1 hands units out longest sequence first (sequences ordered by key count in the
+    CTA, ties by index) to CTAs that take the next one by cancelling a pending CTA's launch.  Equal
+    lengths (ties), a zero-length and a fully masked sequence (units with no key tile), against the
+    oracle; and the result does not depend on which CTA took which unit: a second run is bit-identical."""
+    Sq = 128
+    qo = [200, 200, 0, 37, -Sq, 200]
+    lens = [328, 328, 0, 165, 40, 328]
+    wl = W.make_custom(dtype="bf16", B=6, Sq=Sq, Hq=16, Hkv=2, D=128, page_size=16, seq_lens=lens, causal=True,
+                       q_offset=qo, seed=213)
+    dw = _gpu.DeviceWorkload(wl)
+    first = _gpu.run(dw, 1, TC05)
+    rows = oracle.all_rows(wl.B, wl.Sq, wl.Hq)
+    _gpu.compare_rows(first, oracle.workload_rows(wl, split_kv=1, row_bih=rows), rows, wl, 1, "tc05 split-1 order")
+    assert np.all(first["lse"][2] == -np.inf) and np.all(first["lse"][4] == -np.inf)
+    again = _gpu.run(dw, 1, TC05)
+    for key in first:
+        assert np.array_equal(first[key], again[key], equal_nan=True), key
+    assert pa.paged_attn_last_error_word() == 0
+
+
+def test_tc05_split1_batch_past_the_sort(pa):
+    """More sequences than the in-CTA ordering takes (256): the schedule falls back to the last
+    sequence first.  300 sequences of 16 query tokens (G = 4: one 64-row tile each), ragged
+    lengths, far more units than SMs, every row against the oracle."""
+    rng = np.random.default_rng(214)
+    B, Sq = 300, 16
+    qo = rng.integers(0, 200, size=B).tolist()
+    lens = [o + Sq for o in qo]
+    wl = W.make_custom(dtype="bf16", B=B, Sq=Sq, Hq=8, Hkv=2, D=128, page_size=16, seq_lens=lens, causal=True,
+                       q_offset=qo, seed=215)
+    _check(wl, 1, "tc05 split-1 B=300")
+    assert pa.paged_attn_last_error_word() == 0
