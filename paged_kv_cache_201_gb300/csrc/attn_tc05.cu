@@ -66,14 +66,16 @@ constexpr int kT5Ring = 8;                    // entries of the unit ring (a pow
 // ring readers' arrivals per entry: lane 0 of warps 2 and 3, the MMA thread, 8 softmax and 4 epilogue warps
 constexpr uint32_t kT5RingReaders = 15;
 
-// barrier slots (pairs are indexed by buffer / ring slot)
+// barrier slots (pairs are indexed by buffer / ring slot); each commit costs the MMA thread issue
+// time, so one completion serves every waiter that needs it:
 //   QF/QE  Q buffer full (TMA) / empty (after the unit's last Q K^T)
-//   KF/KE, VF/VE  K and V ring slots full (TMA) / empty (after the product that reads them)
+//   KF/KE  K ring slot full (TMA) / Q K^T of its tile done: the slot is free, and the S buffer of
+//          the same index holds the scores (the softmax waits on it too)
+//   VF/VE  V ring slot full (TMA) / P V of its tile done: the slot is free, and O holds that
+//          tile's product (the softmax waits on it before rescaling O).  Every such wait is at
+//          most one phase behind: the barrier's next phase needs the waiter's own later work.
 //   VZ     V ring slot cleared past the unit's last key, where needed (32 V-gate threads arrive)
-//   SF/PF  S buffer holds Q K^T / P written back over it (256 softmax threads arrive)
-//   OD     once per P V product; a parity wait on it is exact only while it is at most one
-//          phase behind, which holds inside a unit's tile loop (Q K^T of tile g done implies
-//          P V of tile g-2 done) but not after it, hence
+//   PF     P written back over the S buffer (256 softmax threads arrive)
 //   OF     once per use of an O buffer, after the unit's last P V
 //   OFREE  O buffer read out by the epilogue threads (128 arrive)
 //   LF/LE  a unit's row maxima and sums handed to the epilogue (256 softmax threads arrive) / read
@@ -81,9 +83,8 @@ constexpr uint32_t kT5RingReaders = 15;
 //   RF/RE  unit ring entry written (warp 0) / read by every reader (kT5RingReaders arrive)
 //   CLC    the response to a launch-cancel request has landed (16 bytes)
 enum {
-    B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_PF = 14, B_OF = 16, B_OFREE = 18,
-    B_OD = 20, B_VZ = 21, B_LF = 23, B_LE = 25, B_RF = 27, B_RE = B_RF + kT5Ring, B_CLC = B_RE + kT5Ring,
-    B_COUNT = B_CLC + 1
+    B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_PF = 12, B_OF = 14, B_OFREE = 16,
+    B_VZ = 18, B_LF = 20, B_LE = 22, B_RF = 24, B_RE = B_RF + kT5Ring, B_CLC = B_RE + kT5Ring, B_COUNT = B_CLC + 1
 };
 
 // Cluster launch control (sm_100 family): ask to cancel the launch of a CTA that has not started;
@@ -259,14 +260,15 @@ __device__ __forceinline__ void t5_advance(const FwdParams &p, T5Pos &u, const T
 }
 
 // The cancelled-CTA schedule (split_kv = 1): the unit of CTA r.  Sequences by key count, longest
-// first (perm; null: the last sequence first), each from its last row tile down, so the units with
-// the most key tiles start first and the short ones fill in at the end.
+// first (perm; null: the last sequence first), each from its last row tile down with the kv heads
+// of a row tile side by side, so a sequence's units come in falling order of key tiles: the
+// longest start first and the short ones fill in at the end.
 __device__ __forceinline__ T5Pos t5_dyn_pos(const FwdParams &p, int r, const int16_t *perm) {
     T5Pos u;
-    const int ri = r % p.row_tiles;
-    r /= p.row_tiles;
     u.kvh = r % p.Hkv;
-    const int bi = r / p.Hkv;
+    r /= p.Hkv;
+    const int ri = r % p.row_tiles;
+    const int bi = r / p.row_tiles;
     u.rt = p.row_tiles - 1 - ri;
     u.s = 0;
     u.b = perm ? (int)perm[bi] : p.B - 1 - bi;
@@ -398,7 +400,6 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_init(bar(B_KE + i), 1);
             mbar_init(bar(B_VF + i), 1);
             mbar_init(bar(B_VE + i), 1);
-            mbar_init(bar(B_SF + i), 1);
             mbar_init(bar(B_PF + i), 256);
             mbar_init(bar(B_OF + i), 1);
             mbar_init(bar(B_OFREE + i), 128);
@@ -410,7 +411,6 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_init(bar(B_RF + i), 1);
             mbar_init(bar(B_RE + i), kT5RingReaders);
         }
-        mbar_init(bar(B_OD), 1);
         mbar_init(bar(B_CLC), 1);
         fence_barrier_init();
     }
@@ -669,6 +669,13 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             // ================================================================ MMA issuer
             if (lane == 0) {
                 bool bad = false;
+                // Operand descriptors: the low halves of the buffers' first 16-column slices (the
+                // slices of one operand sit at constant offsets from it), one high half for all.
+                const uint32_t dhi = tc05::smem_desc_sw128_hi(1024);
+                const uint32_t dq0 = tc05::smem_desc_sw128_lo(sQ(0), 16), dq1 = tc05::smem_desc_sw128_lo(sQ(1), 16);
+                const uint32_t dk0 = tc05::smem_desc_sw128_lo(sK(0), 16), dk1 = tc05::smem_desc_sw128_lo(sK(1), 16);
+                const uint32_t dv0 = tc05::smem_desc_sw128_lo(sV(0), (uint32_t)kT5Half);
+                const uint32_t dv1 = tc05::smem_desc_sw128_lo(sV(1), (uint32_t)kT5Half);
                 // P V of tile g is issued after Q K^T of tile g+1 (which may belong to the next unit)
                 bool pend = false;
                 int pg = 0, pn = 0;
@@ -681,17 +688,16 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     tc05::fence_after_sync();
                     const uint32_t pcol = tmem + (slot ? 128u : 0u);
                     const uint32_t ocol = tmem + kColO + 128u * (uint32_t)ob;
+                    const uint32_t dv = slot ? dv1 : dv0;
     #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t vd =
-                            tc05::smem_desc_sw128(sV(slot) + (uint32_t)kk * 2048u, (uint32_t)kT5Half, 1024);
+                        const uint32_t vlo = dv + (uint32_t)kk * (2048u >> 4);  // V rows 16kk..16kk+15
                         // keys 16kk..16kk+15: chunk kk/2 of 32 keys; highs at +0, remainders at +16
                         const uint32_t pa = pcol + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
-                        tc05::mma_ts(ocol, pa, vd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                        if (t5_split_p<T>()) tc05::mma_ts(ocol, pa + 16u, vd, idesc_pv, 1u);
+                        tc05::mma_ts_lh(ocol, pa, vlo, dhi, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                        if (t5_split_p<T>()) tc05::mma_ts_lh(ocol, pa + 16u, vlo, dhi, idesc_pv, 1u);
                     }
-                    tc05::commit(bar(B_VE + slot));
-                    tc05::commit(bar(B_OD));
+                    tc05::commit(bar(B_VE + slot));  // V slot free, O holds this product
                     if (last) tc05::commit(bar(B_OF + ob));
                     return true;
                 };
@@ -713,14 +719,14 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                         if (!mbar_wait(bar(B_KF + slot), (g >> 1) & 1, p.err)) { bad = true; break; }
                         tc05::fence_after_sync();
                         const uint32_t d = tmem + (slot ? 128u : 0u);
+                        const uint32_t dq = qb ? dq1 : dq0, dk = slot ? dk1 : dk0;
     #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t off = (uint32_t)(kk >> 2) * kT5Half + (uint32_t)(kk & 3) * 32u;
-                            tc05::mma_ss(d, tc05::smem_desc_sw128(sQ(qb) + off, 16, 1024),
-                                         tc05::smem_desc_sw128(sK(slot) + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                            // columns 16kk..16kk+15: 64-column half kk/4, 32-byte slice kk%4 of its rows
+                            const uint32_t off = ((uint32_t)(kk >> 2) * kT5Half + (uint32_t)(kk & 3) * 32u) >> 4;
+                            tc05::mma_ss_lh(d, dq + off, dhi, dk + off, dhi, idesc_qk, kk > 0 ? 1u : 0u);
                         }
-                        tc05::commit(bar(B_KE + slot));   // K slot reusable once this product is done
-                        tc05::commit(bar(B_SF + slot));
+                        tc05::commit(bar(B_KE + slot));  // K slot free, S holds the scores
                         if (t == U.n_tiles - 1) tc05::commit(bar(B_QE + qb));
                         if (pend && !issue_pv(pg, pn, pfirst, plast)) { bad = true; break; }
                         pend = true;
@@ -798,7 +804,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             for (int t = 0; t < U.n_tiles; ++t) {
                 const int g = g0 + t, st = g & 1;
                 if (!bad) {
-                    const bool ok = mbar_wait(bar(B_SF + st), (g >> 1) & 1, p.err);
+                    const bool ok = mbar_wait(bar(B_KE + st), (g >> 1) & 1, p.err);  // S = Q K^T of tile g
                     bad = __any_sync(0xffffffffu, !ok);
                 }
                 tc05::fence_after_sync();
@@ -841,10 +847,10 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                         m_used = m_new;
                     }
                     if (t > 0) {
-                        // O holds P V of this unit's earlier tiles: wait for the last one (tile g-1; Q K^T
-                        // of tile g having completed, P V of g-2 has, so the parity wait is exact), then
+                        // O holds P V of this unit's earlier tiles: wait for the last one (tile g-1; its
+                        // slot's next phase needs P of tile g+1, so the parity wait is exact), then
                         // rescale my half of the row
-                        const bool ok = mbar_wait(bar(B_OD), (g - 1) & 1, p.err);
+                        const bool ok = mbar_wait(bar(B_VE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, p.err);
                         bad = __any_sync(0xffffffffu, !ok);
                         if (!bad) {
                             tc05::fence_after_sync();
