@@ -23,7 +23,7 @@
 //               buffers (one per unit, alternating).
 //   warp 3      V gate: clears the V rows of a unit's last tile that lie past its last valid key
 //               (they may hold any bits, and a zero weight times NaN is NaN), then releases the slot
-//               to the P V product.
+//               to the P V product (one barrier with the softmax's P).
 //   warps 4-11  softmax, two threads per TMEM lane (query row), 64 columns each: mask (sequence
 //               length, split end, causal reach with q_offset), running max in the log2 domain,
 //               P = exp2(s - m) written back over S as a 16-bit high part and its rounding
@@ -74,8 +74,8 @@ constexpr uint32_t kT5RingReaders = 15;
 //   VF/VE  V ring slot full (TMA) / P V of its tile done: the slot is free, and O holds that
 //          tile's product (the softmax waits on it before rescaling O).  Every such wait is at
 //          most one phase behind: the barrier's next phase needs the waiter's own later work.
-//   VZ     V ring slot cleared past the unit's last key, where needed (32 V-gate threads arrive)
-//   PF     P written back over the S buffer (256 softmax threads arrive)
+//   PF     P written back over the S buffer (256 softmax threads arrive) and the V slot of the same
+//          index cleared past the unit's last key, where needed (32 V-gate threads arrive)
 //   OF     once per use of an O buffer, after the unit's last P V
 //   OFREE  O buffer read out by the epilogue threads (128 arrive)
 //   LF/LE  a unit's row maxima and sums handed to the epilogue (256 softmax threads arrive) / read
@@ -83,8 +83,8 @@ constexpr uint32_t kT5RingReaders = 15;
 //   RF/RE  unit ring entry written (warp 0) / read by every reader (kT5RingReaders arrive)
 //   CLC    the response to a launch-cancel request has landed (16 bytes)
 enum {
-    B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_PF = 12, B_OF = 14, B_OFREE = 16,
-    B_VZ = 18, B_LF = 20, B_LE = 22, B_RF = 24, B_RE = B_RF + kT5Ring, B_CLC = B_RE + kT5Ring, B_COUNT = B_CLC + 1
+    B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_PF = 12, B_OF = 14, B_OFREE = 16, B_LF = 18,
+    B_LE = 20, B_RF = 22, B_RE = B_RF + kT5Ring, B_CLC = B_RE + kT5Ring, B_COUNT = B_CLC + 1
 };
 
 // Cluster launch control (sm_100 family): ask to cancel the launch of a CTA that has not started;
@@ -400,10 +400,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_init(bar(B_KE + i), 1);
             mbar_init(bar(B_VF + i), 1);
             mbar_init(bar(B_VE + i), 1);
-            mbar_init(bar(B_PF + i), 256);
+            mbar_init(bar(B_PF + i), 256 + 32);
             mbar_init(bar(B_OF + i), 1);
             mbar_init(bar(B_OFREE + i), 128);
-            mbar_init(bar(B_VZ + i), 32);
             mbar_init(bar(B_LF + i), 256);
             mbar_init(bar(B_LE + i), 128);
         }
@@ -682,8 +681,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 bool pfirst = false, plast = false;
                 auto issue_pv = [&](int g, int un, bool first, bool last) -> bool {
                     const int slot = g & 1, ob = un & 1;
-                    if (!mbar_wait(bar(B_PF + slot), (g >> 1) & 1, p.err)) return false;
-                    if (!mbar_wait(bar(B_VZ + slot), (g >> 1) & 1, p.err)) return false;
+                    if (!mbar_wait(bar(B_PF + slot), (g >> 1) & 1, p.err)) return false;  // P, V cleared
                     if (first && un >= 2 && !mbar_wait(bar(B_OFREE + ob), ((un >> 1) - 1) & 1, p.err)) return false;
                     tc05::fence_after_sync();
                     const uint32_t pcol = tmem + (slot ? 128u : 0u);
@@ -746,8 +744,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             // Keys at or past the unit's k_hi (past the sequence, past the split, past every row's causal
             // reach, or never loaded) sit in the V rows of the unit's last tile with any bits: their
             // weight is 0, but 0 * NaN is NaN, so those rows are cleared before P V reads the slot.
-            // Every tile passes through here (the P V product waits on VZ, not VF), so the phases
-            // stay in step with the ring.
+            // Every tile passes through here (the P V product waits for the V gate's arrival on PF,
+            // not for VF), so the phases stay in step with the ring.  The gate cannot arrive for tile
+            // g + 2 before PF's phase for tile g completes: V of g + 2 lands only after P V of g.
             bool bad = false;
             int g0 = 0, kr = 0;
             T5Pos cur = start(), pos;
@@ -769,7 +768,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                         }
                         fence_proxy_async_smem();
                     }
-                    mbar_arrive(bar(B_VZ + st));
+                    mbar_arrive(bar(B_PF + st));
                 }
                 g0 += U.n_tiles;
             }
