@@ -62,3 +62,16 @@ def test_workspace_too_small_is_rejected(pa):
     with pytest.raises(pa.PagedAttnError) as e:
         pa.paged_attn_fwd_splitkv(dw.q, dw.k, dw.v, dw.bt, dw.sl, False, None, 4, wl.scale, out, None, ws)
     assert e.value.code == -1
+
+
+@pytest.mark.parametrize("S", [3, 8])
+def test_single_call_equals_two_calls_prefill(pa, S):
+    """The single call on the causal prefill (tcgen05 kernel, split partials in the workspace) gives
+    the bits of paged_attn_fwd into caller partials followed by paged_attn_combine."""
+    wl = W.causal_prefill()
+    dw = _gpu.DeviceWorkload(wl)
+    out, lse, _ = _single_call(pa, dw, S)
+    ref = _gpu.run(dw, S)
+    assert np.array_equal(_gpu.to_f64(out, wl.dtype), ref["out"])
+    assert np.array_equal(_gpu.to_f64(lse, "f32"), ref["lse"])
+    assert pa.paged_attn_last_error_word() == 0
