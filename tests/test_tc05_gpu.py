@@ -156,3 +156,30 @@ def test_tc05_split1_batch_past_the_sort(pa):
                        q_offset=qo, seed=215)
     _check(wl, 1, "tc05 split-1 B=300")
     assert pa.paged_attn_last_error_word() == 0
+
+
+def test_tc05_split1_in_cuda_graph(pa):
+    """The split-1 schedule takes its units by cancelling its own grid's pending CTAs, so every launch
+    carries its own schedule: replays of a captured call give the eager call's bits."""
+    import torch
+    wl = W.causal_prefill()
+    dw = _gpu.DeviceWorkload(wl)
+    eager = _gpu.run(dw, 1, TC05)
+    out = torch.empty_like(dw.q)
+    lse = torch.empty((wl.B, wl.Sq, wl.Hq), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):   # warm-up outside the capture
+        pa.paged_attn_fwd_variant(dw.q, dw.k, dw.v, dw.bt, dw.sl, wl.causal, dw.qo, 1, wl.scale, out, lse, TC05)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pa.paged_attn_fwd_variant(dw.q, dw.k, dw.v, dw.bt, dw.sl, wl.causal, dw.qo, 1, wl.scale, out, lse, TC05)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(_gpu.to_f64(out, wl.dtype), eager["out"])
+        assert np.array_equal(_gpu.to_f64(lse, "f32"), eager["lse"])
+    assert pa.paged_attn_last_error_word() == 0
