@@ -133,8 +133,11 @@ typedef struct pa_dims {
  *           lse [B, Sq, Hq] float32 natural-log sum-exp, or NULL.
  *   S >  1: out [S, B, Sq, Hq, D] float32 per-split outputs, each normalised by
  *           its own softmax sum; lse [S, B, Sq, Hq] float32 (required).
- * A row with no valid key in a partition gets output 0 and lse -inf, never
- * NaN (rocMLIR PR #2371, the -inf - (-inf) and 0/0 guards).
+ * A row with no valid key in a partition gets lse -inf, never NaN, and output 0
+ * (rocMLIR PR #2371, the -inf - (-inf) and 0/0 guards).  With S > 1 such a row's
+ * partial output is not always written (the prefill kernel skips the rows of a tile
+ * that its split's keys do not reach): read a partial row only where its lse is
+ * finite, as paged_attn_combine does (it gives weight 0 to a row with lse -inf).
  * Returns PA_OK or a negative status; nothing is launched on error.
  */
 int paged_attn_fwd(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,

@@ -57,7 +57,11 @@ def _run_both(dw, split_kv, variant, extra_heads):
 
 def _assert_identical(dense, strided, what):
     for key in dense:
-        assert np.array_equal(dense[key], strided[key]), f"{what}: {key} differs between dense and strided q"
+        a, b = dense[key], strided[key]
+        if key == "part_out":  # rows with lse -inf need not be written (the combine never reads them)
+            keep = ~np.isneginf(dense["part_lse"])
+            a, b = a[keep], b[keep]
+        assert np.array_equal(a, b), f"{what}: {key} differs between dense and strided q"
 
 
 CASES = [
