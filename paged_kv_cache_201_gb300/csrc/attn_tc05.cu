@@ -27,9 +27,10 @@
 //   warps 4-11  softmax, two threads per TMEM lane (query row), 64 columns each: mask (sequence
 //               length, split end, causal reach with q_offset), running max in the log2 domain,
 //               P = exp2(s - m) written back over S as a 16-bit high part and its rounding
-//               remainder.  O is rescaled in TMEM only when the running max grows by more than
-//               2^8 (otherwise the stale max is kept), and the -inf - (-inf) guard of rocMLIR
-//               PR #2371 applies.  At a unit's end they hand its row maximum and sum over.
+//               remainder (at split 1 every high part first, on its own barrier).  O is rescaled
+//               in TMEM only when the running max grows by more than 2^8 (otherwise the stale max
+//               is kept), and the -inf - (-inf) guard of rocMLIR PR #2371 applies.  At a unit's
+//               end they hand its row maximum and sum over.
 //   warps 12-15 epilogue: one thread per query row reads the unit's O out of TMEM, divides by the
 //               row sum (0/0 guard), stages the rows in shared memory and stores them with TMA (the
 //               log-sum-exp with plain stores), while the softmax warps already work on the next
@@ -74,8 +75,10 @@ constexpr uint32_t kT5RingReaders = 15;
 //   VF/VE  V ring slot full (TMA) / P V of its tile done: the slot is free, and O holds that
 //          tile's product (the softmax waits on it before rescaling O).  Every such wait is at
 //          most one phase behind: the barrier's next phase needs the waiter's own later work.
-//   PF     P written back over the S buffer (256 softmax threads arrive) and the V slot of the same
-//          index cleared past the unit's last key, where needed (32 V-gate threads arrive)
+//   PF     P written back over the S buffer (256 softmax threads arrive; at split 1 its high parts
+//          only) and the V slot of the same index cleared past the unit's last key, where needed
+//          (32 V-gate threads arrive)
+//   PL     at split 1 (bf16), P's remainders written (256 softmax threads arrive)
 //   OF     once per use of an O buffer, after the unit's last P V
 //   OFREE  O buffer read out by the epilogue threads (128 arrive)
 //   LF/LE  a unit's row maxima and sums handed to the epilogue (256 softmax threads arrive) / read
@@ -84,7 +87,7 @@ constexpr uint32_t kT5RingReaders = 15;
 //   CLC    the response to a launch-cancel request has landed (16 bytes)
 enum {
     B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_PF = 12, B_OF = 14, B_OFREE = 16, B_LF = 18,
-    B_LE = 20, B_RF = 22, B_RE = B_RF + kT5Ring, B_CLC = B_RE + kT5Ring, B_COUNT = B_CLC + 1
+    B_LE = 20, B_PL = 22, B_RF = 24, B_RE = B_RF + kT5Ring, B_CLC = B_RE + kT5Ring, B_COUNT = B_CLC + 1
 };
 
 // Cluster launch control (sm_100 family): ask to cancel the launch of a CTA that has not started;
@@ -200,6 +203,46 @@ __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], float c2, 
     l += ls.x + ls.y;
     tc05::st_16cols(taddr, hi);
     if (t5_split_p<T>()) tc05::st_16cols(taddr + 16u, lo);
+}
+
+// The same in two passes (the split-1 schedule releases P's high parts before the remainders).
+// Pass 1 over 32 keys of one row: p = exp2(s * c2 + nmu), where the caller has set the scores of
+// masked keys to -inf (c2 > 0, so their p is exactly 0); l accumulates the p, u is overwritten with
+// the p (fp32 bits), and their 16-bit high parts go to the first 16 of the 32 columns at `taddr`.
+template <typename T>
+__device__ __forceinline__ void t5_exp_hi(uint32_t (&u)[32], float c2, float nmu, float &l, uint32_t taddr) {
+    uint32_t hi[16];
+    const uint64_t c2x2 = f2_pack(c2, c2), nmux2 = f2_pack(nmu, nmu);
+    uint64_t l2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};  // two pair sums: short dependency chains
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint64_t sc = f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+        const float2 x = f2_unpack(f2_fma(sc, c2x2, nmux2));
+        const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+        l2[i & 1] = f2_add(l2[i & 1], f2_pack(p0, p1));
+        hi[i] = MmaOp<T>::pack(p0, p1);
+        u[2 * i] = __float_as_uint(p0);
+        u[2 * i + 1] = __float_as_uint(p1);
+    }
+    const float2 ls = f2_unpack(f2_add(l2[0], l2[1]));
+    l += ls.x + ls.y;
+    tc05::st_16cols(taddr, hi);
+}
+
+// Pass 2 (bf16): the rounding remainders p - hi of the same 32 keys into the last 16 columns (hi
+// rounded again: the same bits as pass 1's, without holding them in registers).
+template <typename T>
+__device__ __forceinline__ void t5_exp_lo(const uint32_t (&u)[32], uint32_t taddr) {
+    uint32_t lo[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float2 h2 =
+            MmaOp<T>::unpack(MmaOp<T>::pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])));
+        const float2 d = f2_unpack(f2_sub(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])),
+                                          f2_pack(h2.x, h2.y)));
+        lo[i] = MmaOp<T>::pack(d.x, d.y);
+    }
+    tc05::st_16cols(taddr + 16u, lo);
 }
 
 // Everything a role needs to know about one work unit; every role derives it the same way.
@@ -358,6 +401,11 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                            const FwdParams p, int tpt, int ps_shift, int g_shift, uint32_t idesc_qk,
                            uint32_t idesc_pv, int nb, int units) {
     constexpr bool DYN = !PART && !VARLEN;
+    // In the split-1 schedule the softmax writes P in two passes (every high part, released on PF,
+    // then every remainder, released on PL) and P V takes the high parts' products first: 3 %
+    // faster there.  Next to the partial-output epilogue that larger code measured 5 % slower, so
+    // the other schedules keep one pass per 32-key chunk (one copy run twice) and one release.
+    constexpr bool kEarlyHi = DYN;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[B_COUNT];
     __shared__ int4 s_ring[kT5Ring];      // the unit ring: {rt, kvh, s, b}, b = -1 after the last unit
@@ -401,6 +449,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_init(bar(B_VF + i), 1);
             mbar_init(bar(B_VE + i), 1);
             mbar_init(bar(B_PF + i), 256 + 32);
+            mbar_init(bar(B_PL + i), 256);
             mbar_init(bar(B_OF + i), 1);
             mbar_init(bar(B_OFREE + i), 128);
             mbar_init(bar(B_LF + i), 256);
@@ -687,13 +736,27 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     const uint32_t pcol = tmem + (slot ? 128u : 0u);
                     const uint32_t ocol = tmem + kColO + 128u * (uint32_t)ob;
                     const uint32_t dv = slot ? dv1 : dv0;
-    #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
+                    // keys 16kk..16kk+15 are chunk kk/2 of 32 keys: highs at +0, remainders at +16
+                    auto pv_one = [&](int kk, uint32_t part, uint32_t acc) {
                         const uint32_t vlo = dv + (uint32_t)kk * (2048u >> 4);  // V rows 16kk..16kk+15
-                        // keys 16kk..16kk+15: chunk kk/2 of 32 keys; highs at +0, remainders at +16
-                        const uint32_t pa = pcol + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
-                        tc05::mma_ts_lh(ocol, pa, vlo, dhi, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                        if (t5_split_p<T>()) tc05::mma_ts_lh(ocol, pa + 16u, vlo, dhi, idesc_pv, 1u);
+                        const uint32_t pa = pcol + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1) + part;
+                        tc05::mma_ts_lh(ocol, pa, vlo, dhi, idesc_pv, acc);
+                    };
+                    if constexpr (kEarlyHi && t5_split_p<T>()) {
+                        // the high parts' products, then (once written) the remainders'
+    #pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) pv_one(kk, 0u, (!first || kk > 0) ? 1u : 0u);
+                        if (!mbar_wait(bar(B_PL + slot), (g >> 1) & 1, p.err)) return false;  // P's remainders
+                        tc05::fence_after_sync();
+    #pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) pv_one(kk, 16u, 1u);
+                    } else {
+                        // both products of each V slice back to back
+    #pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            pv_one(kk, 0u, (!first || kk > 0) ? 1u : 0u);
+                            if (t5_split_p<T>()) pv_one(kk, 16u, 1u);
+                        }
                     }
                     tc05::commit(bar(B_VE + slot));  // V slot free, O holds this product
                     if (last) tc05::commit(bar(B_OF + ob));
@@ -865,24 +928,40 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                         }
                     }
                 }
+                // pass 2: P = exp2(scale_log2 * s - m) for 32 keys at a time, stored over the same 32
+                // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs); at
+                // split 1 every high part first (PF), then every remainder (PL).
                 if (!bad) {
-                    // pass 2: P = exp2(scale_log2 * s - m) for 32 keys at a time, stored over the same 32
-                    // columns as [16 columns of high parts | 16 columns of remainders] (bf16/f16 pairs)
                     const float nmu = (m_used == kNegInf) ? 0.f : -m_used;  // -inf - (-inf) guard
                     const float c2 = p.scale_log2;
-                    // one copy of the chunk's code, run twice (the second 32 scores moved into ua)
+                    if constexpr (kEarlyHi && t5_split_p<T>()) {
+                        t5_exp_hi<T>(ua, c2, nmu, l, sbuf + 64u * hh);  // ua, ub <- p
+                        t5_exp_hi<T>(ub, c2, nmu, l, sbuf + 64u * hh + 32u);
+                    } else {
+                        // one copy of the chunk's code, run twice (small in the instruction cache next to
+                        // the partial-output epilogue)
 #pragma unroll 1
-                    for (int c = 0; c < 2; ++c) {
-                        t5_exp_chunk<T>(ua, c2, nmu, l, sbuf + 64u * hh + 32u * (uint32_t)c);
-                        if (c == 0) {
+                        for (int c = 0; c < 2; ++c) {  // the second 32 scores moved into ua
+                            t5_exp_chunk<T>(ua, c2, nmu, l, sbuf + 64u * hh + 32u * (uint32_t)c);
+                            if (c == 0) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) ua[j] = ub[j];
+                                for (int j = 0; j < 32; ++j) ua[j] = ub[j];
+                            }
                         }
                     }
                     tc05::wait_st();
                 }
                 tc05::fence_before_sync();
                 mbar_arrive(bar(B_PF + st));
+                if constexpr (kEarlyHi && t5_split_p<T>()) {
+                    if (!bad) {
+                        t5_exp_lo<T>(ua, sbuf + 64u * hh);
+                        t5_exp_lo<T>(ub, sbuf + 64u * hh + 32u);
+                        tc05::wait_st();
+                    }
+                    tc05::fence_before_sync();
+                    mbar_arrive(bar(B_PL + st));
+                }
             }
             // hand the row's maximum and partial sum to the epilogue (the slot of unit n-2 read first)
             if (!bad && n >= 2) {
