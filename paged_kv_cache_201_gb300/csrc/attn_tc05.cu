@@ -192,11 +192,16 @@ __device__ __forceinline__ void t5_exp_chunk(const uint32_t (&u)[32], float c2, 
         const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
         const uint64_t pp = f2_pack(p0, p1);
         l2[i & 1] = f2_add(l2[i & 1], pp);
-        hi[i] = MmaOp<T>::pack(p0, p1);
         if (t5_split_p<T>()) {
-            const float2 h2 = MmaOp<T>::unpack(hi[i]);
-            const float2 d = f2_unpack(f2_sub(pp, f2_pack(h2.x, h2.y)));
+            // bf16: the high parts truncated (the top 16 bits of each p); p - hi is then exact in
+            // fp32 and below 2^-7 p, and its bf16 rounding leaves P within 2^-16 of p
+            hi[i] = __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x7632);
+            const uint64_t h2 = f2_pack(__uint_as_float(__float_as_uint(p0) & 0xffff0000u),
+                                        __uint_as_float(__float_as_uint(p1) & 0xffff0000u));
+            const float2 d = f2_unpack(f2_sub(pp, h2));
             lo[i] = MmaOp<T>::pack(d.x, d.y);
+        } else {
+            hi[i] = MmaOp<T>::pack(p0, p1);
         }
     }
     const float2 ls = f2_unpack(f2_add(l2[0], l2[1]));
@@ -220,7 +225,9 @@ __device__ __forceinline__ void t5_exp_hi(uint32_t (&u)[32], float c2, float nmu
         const float2 x = f2_unpack(f2_fma(sc, c2x2, nmux2));
         const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
         l2[i & 1] = f2_add(l2[i & 1], f2_pack(p0, p1));
-        hi[i] = MmaOp<T>::pack(p0, p1);
+        // bf16: the high parts truncated (the top 16 bits of each p), so that pass 2 finds them with a
+        // mask; the remainder p - hi is then exact in fp32 and below 2^-7 p
+        hi[i] = t5_split_p<T>() ? __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x7632) : MmaOp<T>::pack(p0, p1);
         u[2 * i] = __float_as_uint(p0);
         u[2 * i + 1] = __float_as_uint(p1);
     }
@@ -229,17 +236,16 @@ __device__ __forceinline__ void t5_exp_hi(uint32_t (&u)[32], float c2, float nmu
     tc05::st_16cols(taddr, hi);
 }
 
-// Pass 2 (bf16): the rounding remainders p - hi of the same 32 keys into the last 16 columns (hi
-// rounded again: the same bits as pass 1's, without holding them in registers).
+// Pass 2 (bf16): the remainders p - hi of the same 32 keys (hi = p with its low 16 bits cleared,
+// as pass 1 stored it), rounded to bf16, into the last 16 columns.
 template <typename T>
 __device__ __forceinline__ void t5_exp_lo(const uint32_t (&u)[32], uint32_t taddr) {
     uint32_t lo[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const float2 h2 =
-            MmaOp<T>::unpack(MmaOp<T>::pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])));
-        const float2 d = f2_unpack(f2_sub(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])),
-                                          f2_pack(h2.x, h2.y)));
+        const uint64_t h2 =
+            f2_pack(__uint_as_float(u[2 * i] & 0xffff0000u), __uint_as_float(u[2 * i + 1] & 0xffff0000u));
+        const float2 d = f2_unpack(f2_sub(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), h2));
         lo[i] = MmaOp<T>::pack(d.x, d.y);
     }
     tc05::st_16cols(taddr + 16u, lo);
