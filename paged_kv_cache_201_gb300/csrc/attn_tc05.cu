@@ -26,8 +26,9 @@
 //               to the P V product (one barrier with the softmax's P).
 //   warps 4-11  softmax, two threads per TMEM lane (query row), 64 columns each: mask (sequence
 //               length, split end, causal reach with q_offset), running max in the log2 domain,
-//               P = exp2(s - m) written back over S as a 16-bit high part and its rounding
-//               remainder (at split 1 every high part first, on its own barrier).  O is rescaled
+//               P = exp2(s - m) written back over S as a 16-bit high part (bf16: p truncated to
+//               its top 16 bits) and its remainder (at split 1 every high part first, on its
+//               own barrier).  O is rescaled
 //               in TMEM only when the running max grows by more than 2^8 (otherwise the stale max
 //               is kept), and the -inf - (-inf) guard of rocMLIR PR #2371 applies.  At a unit's
 //               end they hand its row maximum and sum over.
@@ -778,7 +779,17 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                         break;
                     }
                     const T5Unit U = t5_unit<VARLEN>(p, ln, pos, tpt, ps_shift, g_shift);
-                    if (U.n_tiles == 0) continue;
+                    if (U.n_tiles == 0) {
+                        // From the ring, issue the held-back P V now: the producer posts units with
+                        // no key tile without loads, so a run of them (a sequence of length 0 or
+                        // masked whole) may take it a ring's length ahead of the epilogue, which
+                        // waits for that product before it reads further entries.
+                        if (DYN && pend) {
+                            if (!issue_pv(pg, pn, pfirst, plast)) { bad = true; break; }
+                            pend = false;
+                        }
+                        continue;
+                    }
                     const int qb = n & 1;
                     if (!mbar_wait(bar(B_QF + qb), (n >> 1) & 1, p.err)) { bad = true; break; }
                     for (int t = 0; t < U.n_tiles; ++t) {
