@@ -144,21 +144,23 @@ def test_tc05_split1_schedule_orders(pa):
     assert pa.paged_attn_last_error_word() == 0
 
 
-@pytest.mark.parametrize("empty", ["length0", "masked"])
+@pytest.mark.parametrize("empty", ["length0", "masked", "all0"])
 def test_tc05_split1_runs_of_empty_units(pa, empty):
     """Units with no key tile in long runs.  length0: 60 sequences of length 0 come after the four
     real ones in the split-1 order, 3840 empty units for ~150 CTAs, so a CTA takes far more of them
     in a row than the unit ring holds while the last product of its last real unit is still held
     back.  masked: the 60 are fully masked instead (q_offset -Sq) and long, so they come first.
-    Every row against the oracle (rows with no key: output 0, lse -inf), and no wait gives up."""
+    all0: every sequence has length 0.  Every row against the oracle (rows with no key: output 0,
+    lse -inf), and no wait gives up."""
     B, Sq = 64, 256
-    lens, qo = ([0] * B, [0] * B) if empty == "length0" else ([600] * B, [-Sq] * B)
-    for b, (L, o) in zip((0, 17, 33, 50), ((300, 44), (256, 0), (400, 144), (280, 24))):
+    lens, qo = ([0] * B, [0] * B) if empty != "masked" else ([600] * B, [-Sq] * B)
+    real = (0, 17, 33, 50) if empty != "all0" else ()
+    for b, (L, o) in zip(real, ((300, 44), (256, 0), (400, 144), (280, 24))):
         lens[b], qo[b] = L, o
     wl = W.make_custom(dtype="bf16", B=B, Sq=Sq, Hq=32, Hkv=8, D=128, page_size=16, seq_lens=lens, causal=True,
                        q_offset=qo, seed=216)
     res = _check(wl, 1, f"tc05 split-1 empty runs ({empty})")
-    assert np.all(res["lse"][[b for b in range(B) if b not in (0, 17, 33, 50)]] == -np.inf)
+    assert np.all(res["lse"][[b for b in range(B) if b not in real]] == -np.inf)
     assert pa.paged_attn_last_error_word() == 0
 
 
